@@ -1,0 +1,157 @@
+"""FP64 CPU oracle for single-token GQA decode attention.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference legs of ``bench.py`` may import this package.  The
+product path (``gqa_decode_attention_sm_gb300``) never imports it, and this
+package imports nothing from the product.
+
+The arithmetic lives in ``gqa_oracle.c`` (plain C, FP64, POSIX threads); this
+module only compiles it and marshals numpy arrays through ctypes.  What it
+computes, and the pages it restates:
+
+* "FlashInfer sm110_gqa_decode" article, sections "Input contract" and
+  "Convenience API": q [batch,32,128], kv [batch,2,8,capacity,128] (K plane 0,
+  V plane 1), int32 lengths in [1, capacity]; softmax scale q_scale/sqrt(128);
+  query heads 4g..4g+3 read KV head g (the grouped view q.view(batch,8,4,128)).
+* "FP8 KV cache port on Jetson AGX Thor" blog, section 1 (patches 1 and 2):
+  e4m3 cache bytes are reinterpreted, not converted; scores are multiplied by
+  k_scale and the normalised output by v_scale.
+* "FreeToken-Kai on Turing" notes, change 7: score the whole key range, then a
+  plain softmax with no running maximum.
+
+Every function here is pinned by ``tests/test_oracle_*.py`` against closed
+forms, invariants, exhaustive format tables and torch's float64
+``scaled_dot_product_attention``; none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+F16, BF16, E4M3 = 0, 1, 2
+HQ, HKV, D = 32, 8, 128
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gqa_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle_gqa.so")
+_lib = None
+_lock = threading.Lock()
+
+_ERRORS = {1: "invalid argument", 2: "a length is outside [1, capacity]", 3: "out of memory"}
+
+
+def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH) -> str:
+    """Compile the oracle with gcc (no fast-math, no FMA contraction)."""
+    if force or not os.path.exists(out) or os.path.getmtime(out) < os.path.getmtime(src):
+        tmp = out + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-ffp-contract=off", "-fPIC", "-shared", "-pthread",
+               "-std=c11", "-Wall", "-o", tmp, src, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, out)
+    return out
+
+
+def load(path: str | None = None):
+    """Load (building if needed) and return the ctypes handle."""
+    global _lib
+    with _lock:
+        if path is not None:
+            return _bind(ctypes.CDLL(path))
+        if _lib is None:
+            _lib = _bind(ctypes.CDLL(build()))
+        return _lib
+
+
+def _bind(lib):
+    lib.orc_decode_f16.restype = ctypes.c_double
+    lib.orc_decode_f16.argtypes = [ctypes.c_uint16]
+    lib.orc_decode_bf16.restype = ctypes.c_double
+    lib.orc_decode_bf16.argtypes = [ctypes.c_uint16]
+    lib.orc_decode_e4m3.restype = ctypes.c_double
+    lib.orc_decode_e4m3.argtypes = [ctypes.c_uint8]
+    lib.orc_round_f16.restype = ctypes.c_uint16
+    lib.orc_round_f16.argtypes = [ctypes.c_double]
+    lib.orc_round_bf16.restype = ctypes.c_uint16
+    lib.orc_round_bf16.argtypes = [ctypes.c_double]
+    p = ctypes.c_void_p
+    lib.orc_decode_array.restype = None
+    lib.orc_decode_array.argtypes = [p, ctypes.c_int, ctypes.c_size_t, p]
+    lib.orc_round_array.restype = None
+    lib.orc_round_array.argtypes = [p, ctypes.c_size_t, ctypes.c_int, p]
+    lib.orc_gqa_decode.restype = ctypes.c_int
+    lib.orc_gqa_decode.argtypes = [p, ctypes.c_int, p, ctypes.c_int, p, ctypes.c_int,
+                                   ctypes.c_int, ctypes.c_double, ctypes.c_double,
+                                   ctypes.c_double, p, ctypes.c_int, p, p, ctypes.c_int,
+                                   ctypes.c_int]
+    return lib
+
+
+def decode(bits: np.ndarray, fmt: int, lib=None) -> np.ndarray:
+    """Decode raw bit patterns (uint16 for f16/bf16, uint8 for e4m3) to float64."""
+    lib = lib or load()
+    flat = np.ascontiguousarray(np.asarray(bits).ravel(),
+                                dtype=np.uint8 if fmt == E4M3 else np.uint16)
+    out = np.empty(flat.size, dtype=np.float64)
+    lib.orc_decode_array(flat.ctypes.data, fmt, flat.size, out.ctypes.data)
+    return out.reshape(np.shape(bits))
+
+
+def round_to(x: np.ndarray, fmt: int, lib=None) -> np.ndarray:
+    """Round float64 values to f16/bf16 bits, nearest-even, in one step."""
+    lib = lib or load()
+    assert fmt in (F16, BF16)
+    flat = np.ascontiguousarray(np.asarray(x, dtype=np.float64).ravel())
+    out = np.empty(flat.size, dtype=np.uint16)
+    lib.orc_round_array(flat.ctypes.data, flat.size, fmt, out.ctypes.data)
+    return out.reshape(np.shape(x))
+
+
+def default_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def gqa_decode(q_bits: np.ndarray, q_fmt: int, kv_bits: np.ndarray, kv_fmt: int,
+               lens: np.ndarray, q_scale: float = 1.0, k_scale: float = 1.0,
+               v_scale: float = 1.0, rows=None, out_fmt: int | None = None,
+               threads: int | None = None, lib=None):
+    """Oracle attention output.
+
+    q_bits  uint16 [B,32,128] (f16 or bf16 bit patterns)
+    kv_bits uint16 [B,2,8,C,128] (f16/bf16) or uint8 (e4m3 bytes)
+    lens    int32 [B]
+    rows    optional iterable of b*32+h; default all rows in order
+    Returns (out_f64 [n_rows,128], out_bits uint16 [n_rows,128]).
+    """
+    lib = lib or load()
+    q_bits = np.ascontiguousarray(q_bits)
+    kv_bits = np.ascontiguousarray(kv_bits)
+    lens = np.ascontiguousarray(lens, dtype=np.int32)
+    B = q_bits.shape[0]
+    assert q_bits.shape == (B, HQ, D) and q_bits.dtype == np.uint16
+    assert kv_bits.ndim == 5 and kv_bits.shape[:3] == (B, 2, HKV) and kv_bits.shape[4] == D
+    assert kv_bits.dtype == (np.uint8 if kv_fmt == E4M3 else np.uint16)
+    assert lens.shape == (B,)
+    C = kv_bits.shape[3]
+    if out_fmt is None:
+        out_fmt = q_fmt
+    if rows is None:
+        rows_arr = np.arange(B * HQ, dtype=np.int32)
+    else:
+        rows_arr = np.ascontiguousarray(np.asarray(list(rows), dtype=np.int32))
+    n = int(rows_arr.size)
+    out = np.zeros((n, D), dtype=np.float64)
+    bits = np.zeros((n, D), dtype=np.uint16)
+    st = lib.orc_gqa_decode(q_bits.ctypes.data, q_fmt, kv_bits.ctypes.data, kv_fmt,
+                            lens.ctypes.data, B, C, float(q_scale), float(k_scale),
+                            float(v_scale), rows_arr.ctypes.data, n, out.ctypes.data,
+                            bits.ctypes.data, out_fmt, threads or default_threads())
+    if st != 0:
+        raise ValueError(f"oracle: {_ERRORS.get(st, st)}")
+    return out, bits

@@ -1,0 +1,82 @@
+"""Shared test helpers: building small inputs from explicit values, bit views,
+and the library special case (torch float64 scaled_dot_product_attention).
+
+Nothing here computes attention except ``sdpa_f64``, which is torch's own
+routine called on the dequantised inputs (a library special case, used as a pin
+for the oracle), and ``tolerance_ok``, the parity bar.
+"""
+import math
+
+import numpy as np
+import torch
+
+HQ, HKV, D = 32, 8, 128
+
+# GPU vs oracle bar: |gpu - ref| <= 3e-3, or relative 1e-2 where |ref| > 0.3
+ABS_TOL = 3e-3
+REL_TOL = 1e-2
+REL_FLOOR = 0.3
+
+
+def f16_bits(x) -> np.ndarray:
+    return np.asarray(x, dtype=np.float64).astype(np.float16).view(np.uint16)
+
+
+def bf16_bits(x) -> np.ndarray:
+    t = torch.as_tensor(np.asarray(x, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def bits_of(t: torch.Tensor) -> np.ndarray:
+    t = t.detach().contiguous().cpu()
+    if t.dtype in (torch.float16, torch.bfloat16):
+        return t.view(torch.int16).numpy().view(np.uint16)
+    if t.dtype == torch.uint8:
+        return t.numpy()
+    if t.dtype == torch.float8_e4m3fn:
+        return t.view(torch.uint8).numpy()
+    raise TypeError(t.dtype)
+
+
+def values_of_bits(b: np.ndarray, fmt: str) -> np.ndarray:
+    """Library decode (torch) of raw bits to float64."""
+    if fmt == "f16":
+        return b.view(np.float16).astype(np.float64)
+    if fmt == "bf16":
+        return torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    if fmt == "e4m3":
+        return torch.from_numpy(b).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    raise ValueError(fmt)
+
+
+def sdpa_f64(q_vals, k_vals, v_vals, lens, q_scale=1.0, k_scale=1.0, v_scale=1.0, rows=None):
+    """torch float64 SDPA with K/V repeated per query head (repeat_interleave(4)).
+
+    q_vals [B,32,128], k_vals/v_vals [B,8,C,128] float64 arrays.  Returns [n_rows,128].
+    """
+    B = q_vals.shape[0]
+    rows = list(range(B * HQ)) if rows is None else list(rows)
+    out = np.zeros((len(rows), D))
+    by_b = {}
+    for i, r in enumerate(rows):
+        by_b.setdefault(r // HQ, []).append((i, r % HQ))
+    for b, items in by_b.items():
+        L = int(lens[b])
+        q = torch.from_numpy(np.ascontiguousarray(q_vals[b])).reshape(1, HQ, 1, D)
+        k = torch.from_numpy(np.ascontiguousarray(k_vals[b, :, :L])) * k_scale
+        v = torch.from_numpy(np.ascontiguousarray(v_vals[b, :, :L])) * v_scale
+        k = k.repeat_interleave(HQ // HKV, dim=0).unsqueeze(0)
+        v = v.repeat_interleave(HQ // HKV, dim=0).unsqueeze(0)
+        o = torch.nn.functional.scaled_dot_product_attention(
+            q, k, v, scale=q_scale / math.sqrt(D))[0, :, 0, :].numpy()
+        for i, h in items:
+            out[i] = o[h]
+    return out
+
+
+def tolerance_ok(got: np.ndarray, ref: np.ndarray):
+    """Element-wise parity bar; returns (ok, worst abs error, worst excess)."""
+    err = np.abs(got - ref)
+    allowed = np.where(np.abs(ref) > REL_FLOOR, np.maximum(ABS_TOL, REL_TOL * np.abs(ref)), ABS_TOL)
+    excess = err - allowed
+    return bool(np.all(excess <= 0) and np.all(np.isfinite(got))), float(err.max()), float(excess.max())

@@ -1,0 +1,256 @@
+"""Pins for the oracle's attention arithmetic.
+
+Each test checks the FP64 oracle against something other than itself: exact
+rational answers of hand-built cases (tests/golden/worked_examples.json),
+closed forms (length 1 gives V[0]; q_scale = 0 or equal keys give the mean of
+V; a very large q_scale gives the value row of the largest score), invariants
+of softmax attention (slot permutation, a common shift of every key, the
+convex hull of the value rows, power-of-two scaling of V, k_scale and q_scale
+acting only through their product), the grouped head map, and torch's float64
+scaled_dot_product_attention on the dequantised inputs.
+"""
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gqa_decode_attention_sm_gb300 import inputs
+from helpers import D, HKV, HQ, bits_of, f16_bits, bf16_bits, sdpa_f64, values_of_bits
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "worked_examples.json")
+FMT = {"f16": oracle.F16, "bf16": oracle.BF16, "e4m3": oracle.E4M3}
+
+
+def _to_bits(vals, fmt):
+    return f16_bits(vals) if fmt == "f16" else bf16_bits(vals)
+
+
+def _explicit(lib, q_vals, k_vals, v_vals, lens, fmt="f16", **kw):
+    """Run the oracle on explicit values (exactly representable in ``fmt``)."""
+    qb = _to_bits(q_vals, fmt)
+    kv = np.stack([k_vals, v_vals], axis=1)  # [B,2,8,C,128]
+    kvb = _to_bits(kv, fmt)
+    assert np.array_equal(values_of_bits(kvb, fmt), kv), "test values must be exact"
+    return oracle.gqa_decode(qb, FMT[fmt], kvb, FMT[fmt], np.asarray(lens, np.int32), lib=lib,
+                             **kw)
+
+
+def _random(w, seed=None):
+    t = inputs.make(w, "cpu", seed=seed)
+    return t, bits_of(t["q"]), bits_of(t["kv"]), t["lens"].numpy()
+
+
+def _run(lib, t, qb, kvb, lens, **kw):
+    w = t["workload"]
+    args = dict(q_scale=t["q_scale"], k_scale=t["k_scale"], v_scale=t["v_scale"])
+    args.update(kw)
+    return oracle.gqa_decode(qb, FMT[w.q_dtype], kvb, FMT[w.kv_dtype], lens, lib=lib, **args)
+
+
+# ------------------------------------------------------------------ golden
+
+
+def test_golden_worked_examples(orc):
+    spec = json.load(open(GOLDEN))
+    q_scale = math.log(2.0) * math.sqrt(128.0) / 8.0
+    for case in spec["cases"]:
+        L = len(case["k_dim0"])
+        C = L + 3
+        q = np.zeros((1, HQ, D)); q[0, :, 0] = 1.0
+        k = np.zeros((1, HKV, C, D)); v = np.zeros((1, HKV, C, D))
+        k[0, :, :L, 0] = case["k_dim0"]
+        vv = np.asarray(case["v"], dtype=np.float64)
+        v[0, :, :L, :vv.shape[1]] = vv
+        k[0, :, L:, :] = np.nan  # slots past the length hold NaN; they must not be read
+        v[0, :, L:, :] = np.nan
+        qb = f16_bits(q)
+        kvb = f16_bits(np.stack([k, v], axis=1))
+        out, _ = oracle.gqa_decode(qb, oracle.F16, kvb, oracle.F16, np.array([L], np.int32),
+                                   q_scale=q_scale, lib=orc)
+        want = [float(Fraction(x)) for x in case["expected"]]
+        for h in range(HQ):
+            np.testing.assert_allclose(out[h, :len(want)], want, rtol=1e-13, atol=1e-15,
+                                       err_msg=case["name"])
+            assert np.all(out[h, len(want):] == 0.0)
+
+
+# ------------------------------------------------------------- closed forms
+
+
+@pytest.mark.parametrize("kv_dtype", ["f16", "bf16", "e4m3"])
+def test_length_one_returns_first_value_row(orc, kv_dtype):
+    w = inputs.custom(3, 16, 1, kv_dtype=kv_dtype, nan_tail=True)
+    t, qb, kvb, lens = _random(w)
+    out, bits = _run(orc, t, qb, kvb, lens)
+    vals = values_of_bits(kvb, kv_dtype)
+    for r in range(3 * HQ):
+        b, h = divmod(r, HQ)
+        v0 = vals[b, 1, h // 4, 0] * t["v_scale"]
+        assert np.array_equal(out[r], v0)
+        if kv_dtype != "e4m3":  # V[0] is representable in the output type
+            assert np.array_equal(bits[r], kvb[b, 1, h // 4, 0])
+
+
+@pytest.mark.parametrize("kv_dtype", ["f16", "bf16", "e4m3"])
+def test_zero_q_scale_gives_mean_of_values(orc, kv_dtype):
+    w = inputs.custom(2, 96, 40, 96, kv_dtype=kv_dtype)
+    t, qb, kvb, lens = _random(w)
+    out, _ = _run(orc, t, qb, kvb, lens, q_scale=0.0)
+    vals = values_of_bits(kvb, kv_dtype)
+    for r in range(2 * HQ):
+        b, h = divmod(r, HQ)
+        L = lens[b]
+        mean = [math.fsum(vals[b, 1, h // 4, :L, d]) / L * t["v_scale"] for d in range(D)]
+        np.testing.assert_allclose(out[r], mean, rtol=1e-12, atol=1e-14)
+
+
+def test_equal_keys_give_mean_of_values(orc):
+    rng = np.random.default_rng(11)
+    B, C, L = 2, 48, 37
+    q = rng.integers(-3, 4, (B, HQ, D)).astype(np.float64)
+    k = np.repeat(rng.integers(-3, 4, (B, HKV, 1, D)), C, axis=2).astype(np.float64)
+    v = rng.integers(-8, 9, (B, HKV, C, D)).astype(np.float64)
+    out, _ = _explicit(orc, q, k, v, [L, L])
+    for r in range(B * HQ):
+        b, h = divmod(r, HQ)
+        want = [math.fsum(v[b, h // 4, :L, d]) / L for d in range(D)]
+        np.testing.assert_allclose(out[r], want, rtol=1e-13, atol=1e-14)
+
+
+def test_large_q_scale_selects_largest_score(orc):
+    # k_t = t * e0 and q = e0: the score grows with t, so the limit is V[L-1]
+    B, C, L = 1, 32, 20
+    q = np.zeros((B, HQ, D)); q[..., 0] = 1.0
+    k = np.zeros((B, HKV, C, D)); k[0, :, :, 0] = np.arange(C)
+    v = np.random.default_rng(2).integers(-50, 50, (B, HKV, C, D)).astype(np.float64)
+    out, _ = _explicit(orc, q, k, v, [L], q_scale=2000.0)  # adjacent weights differ by e^-177
+    for h in range(HQ):
+        np.testing.assert_allclose(out[h], v[0, h // 4, L - 1], rtol=1e-14, atol=1e-14)
+
+
+def test_grouped_head_map(orc):
+    # every V row of KV head g equals g+1, so query head h must return h//4 + 1
+    rng = np.random.default_rng(5)
+    B, C = 2, 24
+    q = rng.integers(-4, 5, (B, HQ, D)).astype(np.float64)
+    k = rng.integers(-4, 5, (B, HKV, C, D)).astype(np.float64)
+    v = np.broadcast_to((np.arange(HKV) + 1.0)[None, :, None, None], (B, HKV, C, D)).copy()
+    out, _ = _explicit(orc, q, k, v, [C, 9])
+    for r in range(B * HQ):
+        np.testing.assert_allclose(out[r], (r % HQ) // 4 + 1.0, rtol=1e-14)
+
+
+# --------------------------------------------------------------- invariants
+
+
+def test_permuting_slots_leaves_output_unchanged(orc):
+    w = inputs.custom(2, 80, 60, 80)
+    t, qb, kvb, lens = _random(w)
+    ref, _ = _run(orc, t, qb, kvb, lens)
+    rng = np.random.default_rng(9)
+    kvp = kvb.copy()
+    for b in range(2):
+        L = lens[b]
+        perm = rng.permutation(L)
+        kvp[b, :, :, :L] = np.take(kvb[b], perm, axis=2)
+    got, _ = _run(orc, t, qb, kvp, lens)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-14)
+
+
+def test_common_key_shift_leaves_output_unchanged(orc):
+    rng = np.random.default_rng(12)
+    B, C = 1, 40
+    q = (rng.integers(-8, 9, (B, HQ, D)) / 8.0)
+    k = rng.integers(-6, 7, (B, HKV, C, D)).astype(np.float64)
+    v = rng.integers(-6, 7, (B, HKV, C, D)).astype(np.float64)
+    shift = rng.integers(-5, 6, (B, HKV, 1, D)).astype(np.float64)
+    a, _ = _explicit(orc, q, k, v, [C])
+    b, _ = _explicit(orc, q, k + shift, v, [C])
+    np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-14)
+
+
+def test_output_inside_convex_hull_of_values(orc):
+    w = inputs.custom(4, 64, 1, 64)
+    t, qb, kvb, lens = _random(w, seed=77)
+    out, _ = _run(orc, t, qb, kvb, lens, q_scale=3.0)
+    vals = values_of_bits(kvb, "f16")
+    for r in range(4 * HQ):
+        b, h = divmod(r, HQ)
+        vv = vals[b, 1, h // 4, :lens[b]]
+        assert np.all(out[r] >= vv.min(axis=0) - 1e-12) and np.all(out[r] <= vv.max(axis=0) + 1e-12)
+
+
+def test_slots_past_length_are_never_read(orc):
+    w = inputs.custom(4, 128, 1, 127)
+    t, qb, kvb, lens = _random(w, seed=3)
+    kv_nan = t["kv"].clone(); inputs.fill_tail(kv_nan, lens, "f16", float("nan"))
+    kv_big = t["kv"].clone(); inputs.fill_tail(kv_big, lens, "f16", 60000.0)
+    a, abits = _run(orc, t, qb, bits_of(kv_nan), lens)
+    b, bbits = _run(orc, t, qb, bits_of(kv_big), lens)
+    assert np.array_equal(a, b) and np.array_equal(abits, bbits) and np.isfinite(a).all()
+
+
+def test_v_scale_is_linear_and_k_scale_folds_into_q_scale(orc):
+    w = inputs.custom(2, 64, 30, 64, kv_dtype="e4m3", kv_std=2.0)
+    t, qb, kvb, lens = _random(w)
+    base, _ = _run(orc, t, qb, kvb, lens, q_scale=0.75, k_scale=0.5, v_scale=1.0)
+    scaled, _ = _run(orc, t, qb, kvb, lens, q_scale=0.75, k_scale=0.5, v_scale=4.0)
+    assert np.array_equal(scaled, 4.0 * base)  # power-of-two scaling is exact
+    folded, _ = _run(orc, t, qb, kvb, lens, q_scale=0.375, k_scale=1.0, v_scale=1.0)
+    np.testing.assert_allclose(base, folded, rtol=1e-12, atol=1e-14)
+    other, _ = _run(orc, t, qb, kvb, lens, q_scale=0.75, k_scale=1.0, v_scale=1.0)
+    assert not np.allclose(base, other, rtol=1e-6)  # k_scale really changes the scores
+
+
+def test_rejects_lengths_outside_capacity(orc):
+    w = inputs.custom(2, 16, 4)
+    t, qb, kvb, _ = _random(w)
+    for bad in ([0, 4], [4, 17], [-1, 4]):
+        with pytest.raises(ValueError):
+            _run(orc, t, qb, kvb, np.array(bad, np.int32))
+
+
+# -------------------------------------------------- library special case
+
+
+def _check_sdpa(orc, t, qb, kvb, lens, rows=None, **kw):
+    w = t["workload"]
+    out, bits = _run(orc, t, qb, kvb, lens, rows=rows, **kw)
+    qv = values_of_bits(qb, w.q_dtype)
+    kvv = values_of_bits(kvb, w.kv_dtype)
+    args = dict(q_scale=t["q_scale"], k_scale=t["k_scale"], v_scale=t["v_scale"])
+    args.update(kw)
+    ref = sdpa_f64(qv, kvv[:, 0], kvv[:, 1], lens, rows=rows, **args)
+    np.testing.assert_allclose(out, ref, rtol=1e-10, atol=1e-12)
+    # the single rounding step agrees with the reference value rounded by numpy/torch
+    ref_t = torch.from_numpy(ref)
+    if w.q_dtype == "f16":
+        assert np.mean(bits == ref.astype(np.float16).view(np.uint16)) > 0.999
+    else:
+        rb = ref_t.to(torch.float32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        assert np.mean(bits == rb) > 0.999
+
+
+@pytest.mark.parametrize("index", [1, 2])
+def test_matches_torch_sdpa_on_small_workloads(orc, index):
+    t, qb, kvb, lens = _random(inputs.WORKLOADS[index])
+    _check_sdpa(orc, t, qb, kvb, lens)
+
+
+def test_matches_torch_sdpa_on_ragged_nan_tail_sample(orc):
+    # the ragged workload's recipe (NaN tails, U[1,C] lengths) at a smaller capacity
+    w = inputs.with_(inputs.WORKLOADS[3], capacity=1024, len_hi=1024, batch=8)
+    t, qb, kvb, lens = _random(w)
+    _check_sdpa(orc, t, qb, kvb, lens, rows=list(range(0, 8 * HQ, 5)))
+
+
+def test_matches_torch_sdpa_fp8_with_distinct_scales(orc):
+    w = inputs.custom(3, 200, 50, 200, kv_dtype="e4m3", kv_std=2.0)
+    t, qb, kvb, lens = _random(w)
+    _check_sdpa(orc, t, qb, kvb, lens, q_scale=1.0, k_scale=t["k_scale"] * 0.5,
+                v_scale=t["v_scale"] * 3.0)
