@@ -1,0 +1,451 @@
+"""Benchmark: GQA decode KV-read GB/s (% of GB300 HBM peak) and us/call.
+
+One step = one full pass of the decode hot path (stage 1 split-KV kernel and
+stage 2 log-sum-exp combine) over one batch of synthetic inputs already
+resident in HBM.  The headline workload is the long-context bf16 case
+(batch 8, 32 q / 8 KV heads, head_dim 128, capacity = length = 131072: 4.3 GB
+of KV per step, far larger than the 129 MB L2, so no flush is needed between
+steps).  Every workload's us/call and GB/s are reported in ``per_config``
+(cold L2: a 512 MB buffer is written before each timed call).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 4]
+  python bench.py --impl reference ...   # the FP64 CPU oracle, same metric
+
+GB/s counts algorithmic bytes: sum_b len_b x (4096 B fp16/bf16 | 2048 B e4m3)
+of K+V, plus q, out and the lengths; workspace traffic is not counted.
+With N > 1 (torchrun) every rank runs its own replica of the workload on its
+own GPU (the work items are independent; there is no data-path collective),
+the step time is the max over ranks and ``value`` sums all ranks' bytes.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GQA decode KV-read GB/s (% of GB300 HBM peak) and µs/call per config"
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "split_kv_traffic.json")
+KERNEL_SOURCES = ["gqa_decode_attention_sm_gb300/csrc/kernels/common.cuh",
+                  "gqa_decode_attention_sm_gb300/csrc/kernels/split_kv.cuh"]
+
+
+# ------------------------------------------------------------------ helpers
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def traffic_per_launch(workload_index: int):
+    """DRAM bytes per split-kernel launch from the committed ncu summary, if it
+    was taken on the current kernel source and this workload; else None."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("source_hash") != kernel_source_hash() or d.get("workload") != workload_index:
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def algorithmic_bytes(w, lens_list) -> int:
+    per_token = 2048 if w.kv_dtype == "e4m3" else 4096
+    return sum(lens_list) * per_token + 2 * w.batch * 32 * 128 * 2 + 4 * w.batch
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons (read-only)."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.thread:
+                self.thread.join(timeout=2)
+
+    def summary(self, t0: float, t1: float):
+        rows = [s for t, s in self.samples if t0 <= t <= t1]
+        window = "timed region"
+        if len(rows) < 3:  # a short timed region: widen to the samples around it
+            rows = [s for t, s in self.samples if t0 - 1.0 <= t <= t1 + 1.0]
+            window = "timed region +/- 1 s"
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+        sm = sorted(float(r[1]) for r in rows if r[1].replace(".", "").isdigit())
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if len(r) > 5 + i and r[5 + i] == "Active"})
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "window": window,
+                "power_w_max": max((float(r[3]) for r in rows if r[3].replace(".", "").isdigit()),
+                                   default=None)}
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------- CPU baseline
+
+
+def host_batch_row(t, b):
+    """Bit patterns of batch row b (q, kv, length) copied to the host."""
+    from gqa_decode_attention_sm_gb300.inputs import bits
+    return bits(t["q"][b:b + 1]), bits(t["kv"][b:b + 1]), t["lens"][b:b + 1].cpu().numpy()
+
+
+def oracle_rows(t, host, rows, threads):
+    """Time the oracle on query-head `rows` of one host batch row.
+
+    Returns (seconds, KV bytes those rows stand for: len x bytes_per_token / 32
+    per row, the same accounting as the GPU metric)."""
+    import oracle
+    w = t["workload"]
+    fmt = {"f16": oracle.F16, "bf16": oracle.BF16, "e4m3": oracle.E4M3}
+    qb, kvb, lens = host
+    t0 = time.perf_counter()
+    oracle.gqa_decode(qb, fmt[w.q_dtype], kvb, fmt[w.kv_dtype], lens, q_scale=t["q_scale"],
+                      k_scale=t["k_scale"], v_scale=t["v_scale"], rows=rows, threads=threads)
+    secs = time.perf_counter() - t0
+    per_token = 2048 if w.kv_dtype == "e4m3" else 4096
+    return secs, int(lens[0]) * per_token * len(rows) // 32
+
+
+# ------------------------------------------------------------------- arms
+
+
+def run_reference(args):
+    """The oracle as it stands, timed on the host cores (the reference arm)."""
+    import oracle
+    from gqa_decode_attention_sm_gb300 import inputs
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    oracle.build()
+    w = inputs.WORKLOADS[args.workload]
+    # one batch row of the workload, generated on the CPU with the same recipe
+    t = inputs.make(inputs.with_(w, batch=1), "cpu")
+    host = host_batch_row(t, 0)
+    threads = oracle.default_threads()
+    rows = list(range(min(32, threads)))  # one query-head row per core per step
+    times, nb = [], 0
+    for i in range(args.warmup + args.steps):
+        secs, nb = oracle_rows(t, host, rows, threads)
+        if i >= args.warmup:
+            times.append(secs)
+    mean = sum(times) / len(times)
+    gbs = nb / mean / 1e9
+    sample = (f"{len(rows)} query-head rows (length {int(host[2][0])}) of one batch row of "
+              f"'{w.name}' per step, FP64, {threads} threads")
+    line = {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * mean, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "batch": w.batch, "capacity": w.capacity,
+                       "kv_dtype": w.kv_dtype, "parallelism": "host cores"},
+            "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def time_calls(fn, n, flush=None, stream=None):
+    """Median us of `fn` over n calls, each bracketed by CUDA events (flush outside)."""
+    import torch
+    res = []
+    for _ in range(n):
+        if flush is not None:
+            flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        b.synchronize()
+        res.append(a.elapsed_time(b) * 1e3)
+    res.sort()
+    return res[len(res) // 2]
+
+
+def per_config_table(dev, peak, gq, inputs, quick=False):
+    import torch
+    flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    def flush():
+        flush_buf.fill_(1)
+
+    table = {}
+    for idx, w in inputs.WORKLOADS.items():
+        t = inputs.make(w, dev)
+        out = torch.empty_like(t["q"])
+        fp8 = w.kv_dtype == "e4m3"
+        p = gq.prepare({"Q": t["q"], "KV": t["kv"], "O": out, "sequence_lengths": t["lens"]},
+                       q_scale=t["q_scale"], k_scale=t["k_scale"] if fp8 else None,
+                       v_scale=t["v_scale"] if fp8 else None)
+        nbytes = algorithmic_bytes(w, t["lens"].cpu().tolist())
+        for _ in range(3):
+            gq.launch(p)
+        torch.cuda.synchronize()
+        n = 5 if quick else (20 if w.capacity * w.batch > 1 << 20 else 50)
+        us = time_calls(lambda: gq.launch(p), n, flush=flush)
+        row = {"us_per_call": round(us, 2), "GBps": round(nbytes / us / 1e3, 1),
+               "frac_of_peak": round(nbytes / us / 1e3 / peak, 4), "alg_bytes": nbytes,
+               "splits": p.num_splits, "l2": "cold"}
+        if w.capacity * w.batch <= 1 << 16 or idx == 2:
+            wus = time_calls(lambda: gq.launch(p), n)
+            row["us_per_call_warm_l2"] = round(wus, 2)
+        table[str(idx)] = row
+        del t, out, p
+        torch.cuda.empty_cache()
+    return table
+
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+
+    from gqa_decode_attention_sm_gb300 import build as gbuild
+    import gqa_decode_attention_sm_gb300 as gq
+    from gqa_decode_attention_sm_gb300 import inputs
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if rank == 0:
+        gbuild.build()
+    barrier(world)
+
+    peak, peak_kind = measured_peak()
+    w = inputs.WORKLOADS[args.workload]
+    t = inputs.make(w, dev, seed=w.seed + 7919 * rank)
+    lens_list = t["lens"].cpu().tolist()
+    fp8 = w.kv_dtype == "e4m3"
+    out = torch.empty_like(t["q"])
+    p = gq.prepare({"Q": t["q"], "KV": t["kv"], "O": out, "sequence_lengths": t["lens"]},
+                   q_scale=t["q_scale"], k_scale=t["k_scale"] if fp8 else None,
+                   v_scale=t["v_scale"] if fp8 else None)
+    splits_eff = p.splits_effective
+    launches_per_step = 2 if splits_eff > 1 else 1
+    nbytes = algorithmic_bytes(w, lens_list)
+    stream = torch.cuda.current_stream(dev)
+
+    for _ in range(max(3, args.warmup)):
+        gq.split_stage(p)
+        gq.combine_stage(p)
+    torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(local).start()
+    time.sleep(0.3)
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    wall0 = time.time()
+    start.record(stream)
+    for i in range(K):
+        ev[i][0].record(stream)
+        gq.split_stage(p)
+        ev[i][1].record(stream)
+        gq.combine_stage(p)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    wall1 = time.time()
+    time.sleep(0.3)
+    clocks.stop()
+
+    total_ms = start.elapsed_time(end)
+    split_ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    total_ms = max_over_ranks(total_ms, world, dev)
+    all_bytes = sum_over_ranks(float(nbytes), world, dev)
+    ms_per_step = total_ms / K
+    value = all_bytes / (ms_per_step * 1e-3) / 1e9
+
+    # end to end through the public API with host buffers (pinned), copies timed
+    e2e = None
+    if not args.no_e2e:
+        hq = torch.empty(t["q"].shape, dtype=t["q"].dtype, pin_memory=True).copy_(t["q"])
+        hkv = torch.empty(t["kv"].shape, dtype=t["kv"].dtype, pin_memory=True).copy_(t["kv"])
+        hlens = torch.empty(t["lens"].shape, dtype=t["lens"].dtype, pin_memory=True).copy_(t["lens"])
+        hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        ke = max(2, min(K, args.e2e_steps))
+
+        def e2e_step():
+            t["q"].copy_(hq, non_blocking=True)
+            t["kv"].copy_(hkv, non_blocking=True)
+            t["lens"].copy_(hlens, non_blocking=True)
+            gq.launch(p)
+            hout.copy_(out, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        a.record(stream)
+        for _ in range(ke):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = max_over_ranks(a.elapsed_time(b) / ke, world, dev)
+        h2d = hq.numel() * hq.element_size() + hkv.numel() * hkv.element_size() + hlens.numel() * 4
+        e2e = {"value": round(all_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "ms_per_step": round(e2e_ms, 3), "steps": ke, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": hout.numel() * hout.element_size(),
+               "path": "pinned host q/kv/lens -> H2D -> gqa_decode_prepared/fp8kv -> D2H out"}
+        del hq, hkv, hlens, hout
+
+    achieved = nbytes / (split_ms * 1e-3) / 1e9
+    traffic = traffic_per_launch(args.workload)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": max(3, args.warmup), "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "capacity": w.capacity, "kv_dtype": w.kv_dtype,
+                   "q_dtype": w.q_dtype, "lengths": f"U[{w.len_lo},{w.len_hi}]" if w.len_lo != w.len_hi
+                   else w.len_lo, "num_splits": p.num_splits, "splits_effective": splits_eff,
+                   "alg_bytes_per_step_per_gpu": nbytes,
+                   "l2": "inputs (4.3 GB) larger than L2 (129 MB); no flush between steps",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "us_per_call": round(ms_per_step * 1e3, 2),
+                   "frac_of_peak": round(value / world / peak, 4)},
+        "roofline": {"bound": "hbm", "kernel": "split_kv_kernel", "achieved": round(achieved, 1),
+                     "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs (copy, burst)", "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "frac_of_nominal_7900": round(achieved / NOMINAL_HBM_GBS, 4),
+                     "traffic": traffic, "kernel_ms": round(split_ms, 4),
+                     "alg_bytes_per_launch": nbytes},
+        "gpu_launches": K * launches_per_step,
+        "clocks": clocks.summary(wall0, wall1),
+        "e2e": e2e,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        threads = oracle.default_threads()
+        secs, sb, nrows = 0.0, 0, 0
+        for b in range(min(w.batch, args.cpu_batch_rows)):
+            host = host_batch_row(t, b)
+            s_, b_ = oracle_rows(t, host, list(range(32)), threads)
+            secs, sb, nrows = secs + s_, sb + b_, nrows + 32
+        line["cpu_baseline"] = {"value": round(sb / secs / 1e9, 4), "unit": "GB/s", "cores": threads,
+                                "kind": "oracle", "seconds": round(secs, 2),
+                                "sample": f"{nrows} query-head rows ({nrows // 32} batch rows) of "
+                                          f"'{w.name}', FP64, {threads} threads; {sb} KV bytes"}
+    if rank == 0 and not args.no_per_config:
+        line["per_config"] = per_config_table(dev, peak, gq, inputs, quick=args.quick)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=4, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-batch-rows", type=int, default=2,
+                    help="batch rows (all 32 query heads each) in the oracle CPU-baseline sample")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true")
+    ap.add_argument("--quick", action="store_true")
+    args = ap.parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,244 @@
+"""Thin PyTorch-facing binding over the C ABI (argument marshalling only).
+
+Mirrors the three calls of the "FlashInfer sm110_gqa_decode" article
+(sections "Convenience API" and "Prepared continuous decoding"):
+``gqa_decode`` (convenience), ``prepare`` + ``launch`` (prepared: validation
+and workspace allocation happen once, the launch allocates nothing and can be
+captured in a CUDA graph), plus ``gqa_decode_fp8kv`` for an e4m3 KV cache
+(the "FP8 KV cache port on Jetson AGX Thor" blog: uint8 cache bytes are
+reinterpreted as float8_e4m3fn; k_scale on the scores, v_scale on the output).
+Every step of the computation runs in the library's CUDA kernels; PyTorch only
+provides device memory and the current stream.
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+
+import torch
+
+from . import _lib
+from ._lib import GqaError
+
+HQ, HKV, D = 32, 8, 128
+F16, BF16 = 0, 1
+KV_F16, KV_BF16, KV_E4M3 = 0, 1, 2
+MAX_SPLITS = 256
+FLAG_LENGTH_CLAMPED = 0x1
+FLAG_WAIT_TIMEOUT = 0x2
+
+_QDT = {torch.float16: F16, torch.bfloat16: BF16}
+_KVF = {torch.float16: KV_F16, torch.bfloat16: KV_BF16, torch.uint8: KV_E4M3,
+        torch.float8_e4m3fn: KV_E4M3}
+
+__all__ = ["GqaError", "gqa_decode", "gqa_decode_fp8kv", "prepare", "launch", "Prepared",
+           "workspace_size", "plan", "get_status", "split_stage", "combine_stage", "split_geometry"]
+
+
+def _ptr(t: torch.Tensor) -> int:
+    return t.data_ptr()
+
+
+def _stream(device: torch.device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _require(t, name, shape, dtypes, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def _geometry(q, kv, lens):
+    _require(q, "q", None, (torch.float16, torch.bfloat16))
+    if q.dim() != 3 or q.shape[1:] != (HQ, D):
+        raise ValueError(f"q must be [batch, {HQ}, {D}], got {tuple(q.shape)}")
+    B = q.shape[0]
+    if kv.dim() != 5 or kv.shape[0] != B or kv.shape[1:3] != (2, HKV) or kv.shape[4] != D:
+        raise ValueError(f"kv must be [{B}, 2, {HKV}, capacity, {D}], got {tuple(kv.shape)}")
+    C = kv.shape[3]
+    _require(kv, "kv", None, tuple(_KVF), q.device)
+    _require(lens, "sequence_lengths", (B,), (torch.int32,), q.device)
+    return B, C
+
+
+def workspace_size(batch: int, capacity: int, num_splits: int) -> int:
+    n = _lib.load().gqa_decode_workspace_size(batch, capacity, num_splits)
+    if n == 0:
+        raise ValueError("invalid batch/capacity/num_splits")
+    return int(n)
+
+
+def plan(batch: int, capacity: int, kv_format: int, device=None) -> int:
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    out = ctypes.c_int(0)
+    _lib.check(_lib.load().gqa_decode_plan(batch, capacity, kv_format, dev.index or 0,
+                                           ctypes.byref(out)))
+    return out.value
+
+
+def split_geometry(capacity: int, num_splits: int, kv_format: int):
+    """(tokens per split, number of splits holding slots) for this geometry."""
+    chunk, eff = ctypes.c_int(0), ctypes.c_int(0)
+    _lib.check(_lib.load().gqa_decode_split_geometry(capacity, num_splits, kv_format,
+                                                     ctypes.byref(chunk), ctypes.byref(eff)))
+    return chunk.value, eff.value
+
+
+def gqa_decode(q, kv, sequence_lengths, q_scale: float = 1.0, out=None):
+    """Convenience call: plans, takes a stream-ordered workspace, launches."""
+    B, C = _geometry(q, kv, sequence_lengths)
+    if kv.dtype != q.dtype:
+        raise ValueError("kv must have the dtype of q (use gqa_decode_fp8kv for e4m3)")
+    if out is None:
+        out = torch.empty_like(q)
+    _require(out, "out", q.shape, (q.dtype,), q.device)
+    with torch.cuda.device(q.device):
+        _lib.check(_lib.load().gqa_decode(_ptr(q), _ptr(kv), _ptr(sequence_lengths), _ptr(out), B, C,
+                                          _QDT[q.dtype], float(q_scale), _stream(q.device)))
+    return out
+
+
+@dataclass
+class Prepared:
+    """Everything a launch needs, validated once.  Keep it (and its tensors)
+    alive until every launch or graph replay that uses it has finished.  One
+    Prepared per concurrently running stream/graph: its workspace is mutable."""
+    q: torch.Tensor
+    kv: torch.Tensor
+    out: torch.Tensor
+    lens: torch.Tensor
+    workspace: torch.Tensor
+    batch: int
+    capacity: int
+    q_dtype: int
+    kv_format: int
+    q_scale: float
+    k_scale: float
+    v_scale: float
+    num_splits: int
+
+    @property
+    def workspace_bytes(self) -> int:
+        return self.workspace.numel()
+
+    @property
+    def splits_effective(self) -> int:
+        return split_geometry(self.capacity, self.num_splits, self.kv_format)[1]
+
+
+def _storage_overlaps(a: torch.Tensor, b: torch.Tensor) -> bool:
+    sa, sb = a.untyped_storage(), b.untyped_storage()
+    x0, y0 = sa.data_ptr(), sb.data_ptr()
+    return x0 < y0 + sb.nbytes() and y0 < x0 + sa.nbytes()
+
+
+def prepare(tensors: dict, q_scale: float = 1.0, num_splits=None, k_scale=None, v_scale=None,
+            workspace: torch.Tensor | None = None) -> Prepared:
+    """Validate once and allocate the split workspace once (outside any capture).
+
+    ``tensors`` holds "Q", "KV", "O", "sequence_lengths".  An e4m3 cache
+    (uint8 or float8_e4m3fn storage) needs k_scale and v_scale.
+    """
+    q, kv, out, lens = tensors["Q"], tensors["KV"], tensors["O"], tensors["sequence_lengths"]
+    B, C = _geometry(q, kv, lens)
+    _require(out, "O", q.shape, (q.dtype,), q.device)
+    for name, t in (("Q", q), ("KV", kv), ("sequence_lengths", lens)):
+        if _storage_overlaps(out, t):
+            raise ValueError(f"O must not share storage with {name}")
+    kvf = _KVF[kv.dtype]
+    if kvf != KV_E4M3 and kv.dtype != q.dtype:
+        raise ValueError("fp16/bf16 KV must have the dtype of Q")
+    if kvf == KV_E4M3:
+        if k_scale is None or v_scale is None:
+            raise ValueError("an e4m3 KV cache needs k_scale and v_scale")
+    else:
+        k_scale = 1.0 if k_scale is None else k_scale
+        v_scale = 1.0 if v_scale is None else v_scale
+    if not (float(q_scale) > 0.0 and float(q_scale) < float("inf")):
+        raise ValueError("q_scale must be finite and > 0")
+    S = plan(B, C, kvf, q.device) if not num_splits else int(num_splits)
+    nbytes = workspace_size(B, C, S)
+    if workspace is None:
+        workspace = torch.zeros(nbytes, dtype=torch.uint8, device=q.device)
+    else:
+        _require(workspace, "workspace", None, (torch.uint8,), q.device)
+        if workspace.numel() < nbytes:
+            raise ValueError(f"workspace has {workspace.numel()} bytes, needs {nbytes}")
+    return Prepared(q, kv, out, lens, workspace, B, C, _QDT[q.dtype], kvf, float(q_scale),
+                    float(k_scale), float(v_scale), S)
+
+
+def launch(p: Prepared) -> torch.Tensor:
+    """Run both stages on the current stream: no allocation, no host read."""
+    lib = _lib.load()
+    with torch.cuda.device(p.q.device):
+        st = _stream(p.q.device)
+        if p.kv_format == KV_E4M3 and p.q_dtype == BF16:
+            _lib.check(lib.gqa_decode_fp8kv(_ptr(p.q), _ptr(p.kv), _ptr(p.lens), _ptr(p.out), p.batch,
+                                            p.capacity, p.q_scale, p.k_scale, p.v_scale, p.num_splits,
+                                            _ptr(p.workspace), p.workspace_bytes, st))
+        elif p.kv_format == KV_E4M3:
+            split_stage(p)
+            combine_stage(p)
+        else:
+            _lib.check(lib.gqa_decode_prepared(_ptr(p.q), _ptr(p.kv), _ptr(p.lens), _ptr(p.out), p.batch,
+                                               p.capacity, p.q_dtype, p.q_scale, p.num_splits,
+                                               _ptr(p.workspace), p.workspace_bytes, st))
+    return p.out
+
+
+def split_stage(p: Prepared) -> None:
+    """Stage 1 alone (streams K/V, writes partials or, with one split, out)."""
+    with torch.cuda.device(p.q.device):
+        _lib.check(_lib.load().gqa_decode_split_stage(
+            _ptr(p.q), p.q_dtype, _ptr(p.kv), p.kv_format, _ptr(p.lens), _ptr(p.out), p.batch,
+            p.capacity, p.q_scale, p.k_scale, p.v_scale, p.num_splits, _ptr(p.workspace),
+            p.workspace_bytes, _stream(p.q.device)))
+
+
+def combine_stage(p: Prepared) -> None:
+    """Stage 2 alone (log-sum-exp merge of the partials; nothing with one split)."""
+    with torch.cuda.device(p.q.device):
+        _lib.check(_lib.load().gqa_decode_combine_stage(
+            _ptr(p.lens), _ptr(p.out), p.q_dtype, p.kv_format, p.batch, p.capacity, p.v_scale,
+            p.num_splits, _ptr(p.workspace), p.workspace_bytes, _stream(p.q.device)))
+
+
+def gqa_decode_fp8kv(q, kv, sequence_lengths, k_scale: float, v_scale: float, q_scale: float = 1.0,
+                     out=None, num_splits=None, workspace=None):
+    """e4m3 KV cache (uint8 or float8_e4m3fn storage), bf16 q and out."""
+    B, C = _geometry(q, kv, sequence_lengths)
+    if q.dtype != torch.bfloat16 or _KVF[kv.dtype] != KV_E4M3:
+        raise ValueError("gqa_decode_fp8kv takes bf16 q and an e4m3 (uint8) KV cache")
+    if out is None:
+        out = torch.empty_like(q)
+    _require(out, "out", q.shape, (torch.bfloat16,), q.device)
+    S = plan(B, C, KV_E4M3, q.device) if not num_splits else int(num_splits)
+    nbytes = workspace_size(B, C, S)
+    if workspace is None:
+        workspace = torch.zeros(nbytes, dtype=torch.uint8, device=q.device)
+    with torch.cuda.device(q.device):
+        _lib.check(_lib.load().gqa_decode_fp8kv(
+            _ptr(q), _ptr(kv), _ptr(sequence_lengths), _ptr(out), B, C, float(q_scale), float(k_scale),
+            float(v_scale), S, _ptr(workspace), workspace.numel(), _stream(q.device)))
+    return out
+
+
+def get_status(p_or_workspace) -> int:
+    """Debug only (synchronises): read and clear the workspace status flags."""
+    ws = p_or_workspace.workspace if isinstance(p_or_workspace, Prepared) else p_or_workspace
+    flags = ctypes.c_uint32(0)
+    with torch.cuda.device(ws.device):
+        _lib.check(_lib.load().gqa_decode_get_status(_ptr(ws), ws.numel(), _stream(ws.device),
+                                                     ctypes.byref(flags)))
+    return flags.value

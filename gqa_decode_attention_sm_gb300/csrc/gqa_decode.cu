@@ -1,0 +1,514 @@
+// Host side of libgqa_decode.so: argument validation, the one-time device
+// check, the split planner, workspace layout and kernel launches behind the C
+// ABI declared in include/gqa_decode.h.
+//
+// The API shape follows the "FlashInfer sm110_gqa_decode" article: a
+// convenience call, a prepared call that allocates nothing and reads nothing
+// back (capturable in a CUDA graph), fail-fast validation before any launch
+// (its "prepare" step: contiguous/aligned tensors, output not aliasing an
+// input, finite positive q_scale, a compatible device), and a split-KV
+// workspace owned by the caller.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "gqa_decode.h"
+#include "kernels/combine.cuh"
+#include "kernels/common.cuh"
+#include "kernels/split_kv.cuh"
+
+namespace {
+
+using namespace gqa;
+
+thread_local std::string g_last_error;
+
+gqa_status_t fail(gqa_status_t st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+gqa_status_t cuda_fail(cudaError_t e, const char* what) {
+  return fail(GQA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// ---------------------------------------------------------------- devices
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  std::once_flag once;
+  gqa_status_t status = GQA_ERR_UNSUPPORTED_DEVICE;
+  int sm_count = 0;
+  std::string message;
+};
+DeviceState g_devices[kMaxDevices];
+
+template <int KVF, int QF>
+cudaError_t set_split_attributes() {
+  return cudaFuncSetAttribute(split_kv_kernel<KVF, QF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kSplitSmemBytes);
+}
+
+// One-time per-device check (compute capability 10.3) and opt-in to the
+// split kernel's dynamic shared memory.  Runs with `dev` current.
+void init_device(int dev, DeviceState& st) {
+  int major = 0, minor = 0, sms = 0;
+  cudaError_t e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) {
+    st.status = GQA_ERR_CUDA;
+    st.message = std::string("device query failed: ") + cudaGetErrorString(e);
+    return;
+  }
+  if (major != 10 || minor != 3) {
+    st.status = GQA_ERR_UNSUPPORTED_DEVICE;
+    char buf[160];
+    snprintf(buf, sizeof buf, "GQA decode requires compute capability 10.3 (sm_103); device %d is %d.%d",
+             dev, major, minor);
+    st.message = buf;
+    return;
+  }
+  int prev = -1;
+  cudaGetDevice(&prev);
+  if (prev != dev) cudaSetDevice(dev);
+  cudaError_t a = set_split_attributes<kKvF16, kQF16>();
+  if (a == cudaSuccess) a = set_split_attributes<kKvBF16, kQBF16>();
+  if (a == cudaSuccess) a = set_split_attributes<kKvE4M3, kQBF16>();
+  if (a == cudaSuccess) a = set_split_attributes<kKvE4M3, kQF16>();
+  if (prev >= 0 && prev != dev) cudaSetDevice(prev);
+  if (a != cudaSuccess) {
+    st.status = GQA_ERR_CUDA;
+    st.message = std::string("cudaFuncSetAttribute failed: ") + cudaGetErrorString(a);
+    return;
+  }
+  st.sm_count = sms;
+  st.status = GQA_OK;
+}
+
+gqa_status_t device_ready(int dev, int* sm_count) {
+  if (dev < 0 || dev >= kMaxDevices) return fail(GQA_ERR_UNSUPPORTED_DEVICE, "device %d out of range", dev);
+  DeviceState& st = g_devices[dev];
+  std::call_once(st.once, [&] { init_device(dev, st); });
+  if (st.status != GQA_OK) return fail(st.status, "%s", st.message.c_str());
+  if (sm_count) *sm_count = st.sm_count;
+  return GQA_OK;
+}
+
+gqa_status_t current_device_ready(int* sm_count) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  return device_ready(dev, sm_count);
+}
+
+// ------------------------------------------------------------- validation
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+size_t kv_elem_bytes(int fmt) { return fmt == kKvE4M3 ? 1 : 2; }
+
+size_t partial_o_bytes(int batch, int splits) {
+  return align_up((size_t)batch * kHq * splits * kD * sizeof(float), 256);
+}
+size_t partial_ml_bytes(int batch, int splits) {
+  return align_up((size_t)batch * kHq * splits * sizeof(float), 256);
+}
+
+size_t workspace_bytes_for(int batch, int splits) {
+  if (splits <= 1) return GQA_WORKSPACE_HEADER_BYTES;
+  return GQA_WORKSPACE_HEADER_BYTES + partial_o_bytes(batch, splits) + 2 * partial_ml_bytes(batch, splits);
+}
+
+struct Call {
+  const void* q;
+  int q_dtype;
+  const void* kv;
+  int kv_format;
+  const int32_t* lens;
+  void* out;
+  int batch, capacity;
+  float q_scale, k_scale, v_scale;
+  int num_splits;
+  void* workspace;
+  size_t workspace_bytes;
+  cudaStream_t stream;
+};
+
+gqa_status_t validate_shape(int batch, int capacity) {
+  if (batch < 1 || batch > 65535) return fail(GQA_ERR_INVALID_ARGUMENT, "batch %d outside [1, 65535]", batch);
+  if (capacity < 1 || capacity > (1 << 30))
+    return fail(GQA_ERR_INVALID_ARGUMENT, "capacity %d outside [1, 2^30]", capacity);
+  return GQA_OK;
+}
+
+// Checks that need no CUDA call.  `q_scale_min_exclusive`: the prepared entry
+// requires q_scale > 0, the others q_scale >= 0.
+gqa_status_t validate(const Call& c, bool q_scale_positive, bool need_q) {
+  if ((need_q && !c.q) || !c.kv || !c.lens || !c.out || !c.workspace)
+    return fail(GQA_ERR_INVALID_ARGUMENT, "null pointer argument");
+  gqa_status_t st = validate_shape(c.batch, c.capacity);
+  if (st != GQA_OK) return st;
+  if (c.q_dtype != GQA_F16 && c.q_dtype != GQA_BF16)
+    return fail(GQA_ERR_INVALID_ARGUMENT, "unknown q/out dtype %d", c.q_dtype);
+  if (c.kv_format != kKvF16 && c.kv_format != kKvBF16 && c.kv_format != kKvE4M3)
+    return fail(GQA_ERR_INVALID_ARGUMENT, "unknown KV format %d", c.kv_format);
+  if (c.kv_format != kKvE4M3 && c.kv_format != c.q_dtype)
+    return fail(GQA_ERR_INVALID_ARGUMENT, "fp16/bf16 KV must have the dtype of q");
+  if (!std::isfinite(c.q_scale) || c.q_scale < 0.f || (q_scale_positive && c.q_scale == 0.f))
+    return fail(GQA_ERR_INVALID_ARGUMENT, "q_scale must be finite and %s 0", q_scale_positive ? ">" : ">=");
+  if (!std::isfinite(c.k_scale) || c.k_scale <= 0.f || !std::isfinite(c.v_scale) || c.v_scale <= 0.f)
+    return fail(GQA_ERR_INVALID_ARGUMENT, "k_scale and v_scale must be finite and > 0");
+  if (c.num_splits < 1 || c.num_splits > GQA_MAX_SPLITS)
+    return fail(GQA_ERR_INVALID_ARGUMENT, "num_splits %d outside [1, %d]", c.num_splits, GQA_MAX_SPLITS);
+  if ((need_q && !aligned(c.q, 16)) || !aligned(c.kv, 16) || !aligned(c.out, 16) ||
+      !aligned(c.workspace, 16) || !aligned(c.lens, 4))
+    return fail(GQA_ERR_INVALID_ARGUMENT, "q, kv, out, workspace must be 16-byte aligned, lens 4-byte");
+  const size_t need = workspace_bytes_for(c.batch, c.num_splits);
+  if (c.workspace_bytes < need)
+    return fail(GQA_ERR_WORKSPACE_TOO_SMALL, "workspace has %zu bytes, needs %zu", c.workspace_bytes, need);
+  const size_t qo_bytes = (size_t)c.batch * kHq * kD * 2;
+  const size_t kv_bytes = (size_t)c.batch * 2 * kHkv * (size_t)c.capacity * kD * kv_elem_bytes(c.kv_format);
+  const size_t lens_bytes = (size_t)c.batch * 4;
+  if ((need_q && overlap(c.out, qo_bytes, c.q, qo_bytes)) || overlap(c.out, qo_bytes, c.kv, kv_bytes) ||
+      overlap(c.out, qo_bytes, c.lens, lens_bytes) || overlap(c.out, qo_bytes, c.workspace, need))
+    return fail(GQA_ERR_ALIASING, "out overlaps q, kv, lens or the workspace");
+  if ((need_q && overlap(c.workspace, need, c.q, qo_bytes)) || overlap(c.workspace, need, c.kv, kv_bytes) ||
+      overlap(c.workspace, need, c.lens, lens_bytes))
+    return fail(GQA_ERR_ALIASING, "workspace overlaps q, kv or lens");
+  return GQA_OK;
+}
+
+// --------------------------------------------------------------- planning
+
+int plan_splits(int batch, int capacity, int kv_format, int sm_count) {
+  // Aim for about 8 waves of one-CTA-per-SM work items over the worst case
+  // (every length = capacity), with whole tiles per split.
+  const long long tile = tile_tokens(kv_format);
+  const long long units = (long long)batch * kHkv;
+  const long long target_ctas = 8LL * (sm_count > 0 ? sm_count : 148);
+  long long per = (units * capacity + target_ctas - 1) / target_ctas;
+  per = (per + tile - 1) / tile * tile;
+  if (per < tile) per = tile;
+  long long s = (capacity + per - 1) / per;
+  if (s < 1) s = 1;
+  if (s > GQA_MAX_SPLITS) s = GQA_MAX_SPLITS;
+  return (int)s;
+}
+
+// ---------------------------------------------------------------- launches
+
+template <int KVF, int QF>
+cudaError_t launch_split_t(const SplitParams& sp, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(sp.splits_eff, kHkv, sp.batch);
+  cfg.blockDim = dim3(kSplitThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSplitSmemBytes;
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, split_kv_kernel<KVF, QF>, sp);
+}
+
+template <int QF>
+cudaError_t launch_combine_t(const CombineParams& cp, int batch, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kHkv, batch, 1);
+  cfg.blockDim = dim3(kCombineThreads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, combine_kernel<QF>, cp);
+}
+
+struct Layout {
+  float* part_o;
+  float* part_m;
+  float* part_l;
+  uint32_t* flags;
+};
+
+Layout layout_of(void* ws, int batch, int splits) {
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  Layout l;
+  l.flags = reinterpret_cast<uint32_t*>(base);
+  uint8_t* p = base + GQA_WORKSPACE_HEADER_BYTES;
+  l.part_o = reinterpret_cast<float*>(p);
+  p += partial_o_bytes(batch, splits);
+  l.part_m = reinterpret_cast<float*>(p);
+  p += partial_ml_bytes(batch, splits);
+  l.part_l = reinterpret_cast<float*>(p);
+  return l;
+}
+
+gqa_status_t run_split(const Call& c) {
+  const Layout lay = layout_of(c.workspace, c.batch, c.num_splits);
+  SplitParams sp;
+  sp.q = c.q;
+  sp.kv = c.kv;
+  sp.lens = c.lens;
+  sp.out = c.out;
+  sp.part_o = lay.part_o;
+  sp.part_m = lay.part_m;
+  sp.part_l = lay.part_l;
+  sp.flags = lay.flags;
+  sp.batch = c.batch;
+  sp.capacity = c.capacity;
+  sp.num_splits = c.num_splits;
+  sp.chunk = split_chunk(c.capacity, c.num_splits, c.kv_format);
+  sp.splits_eff = split_count(c.capacity, c.num_splits, c.kv_format);
+  // log2(e) / sqrt(128): the softmax runs in the exp2 domain
+  sp.scale_log2 = (float)((double)c.q_scale * (double)c.k_scale * 1.4426950408889634 / std::sqrt(128.0));
+  sp.v_scale = c.v_scale;
+  cudaError_t e;
+  if (c.kv_format == kKvF16) e = launch_split_t<kKvF16, kQF16>(sp, c.stream);
+  else if (c.kv_format == kKvBF16) e = launch_split_t<kKvBF16, kQBF16>(sp, c.stream);
+  else if (c.q_dtype == GQA_BF16) e = launch_split_t<kKvE4M3, kQBF16>(sp, c.stream);
+  else e = launch_split_t<kKvE4M3, kQF16>(sp, c.stream);
+  if (e != cudaSuccess) return cuda_fail(e, "split kernel launch");
+  return GQA_OK;
+}
+
+gqa_status_t run_combine(const Call& c) {
+  const int splits_eff = split_count(c.capacity, c.num_splits, c.kv_format);
+  if (splits_eff == 1) return GQA_OK;
+  const Layout lay = layout_of(c.workspace, c.batch, c.num_splits);
+  CombineParams cp;
+  cp.lens = c.lens;
+  cp.out = c.out;
+  cp.part_o = lay.part_o;
+  cp.part_m = lay.part_m;
+  cp.part_l = lay.part_l;
+  cp.capacity = c.capacity;
+  cp.num_splits = c.num_splits;
+  cp.chunk = split_chunk(c.capacity, c.num_splits, c.kv_format);
+  cp.v_scale = c.v_scale;
+  cudaError_t e = c.q_dtype == GQA_F16 ? launch_combine_t<kQF16>(cp, c.batch, c.stream)
+                                       : launch_combine_t<kQBF16>(cp, c.batch, c.stream);
+  if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
+  return GQA_OK;
+}
+
+// Resolve num_splits = 0 (auto) and validate; then the device check.
+gqa_status_t prepare_call(Call& c, bool q_scale_positive, bool need_q) {
+  int sms = 0;
+  if (c.num_splits == 0) {
+    // validate everything that does not depend on the split count first
+    Call probe = c;
+    probe.num_splits = 1;
+    probe.workspace_bytes = (size_t)-1;
+    gqa_status_t st = validate(probe, q_scale_positive, need_q);
+    if (st != GQA_OK) return st;
+    st = current_device_ready(&sms);
+    if (st != GQA_OK) return st;
+    c.num_splits = plan_splits(c.batch, c.capacity, c.kv_format, sms);
+  }
+  gqa_status_t st = validate(c, q_scale_positive, need_q);
+  if (st != GQA_OK) return st;
+  return current_device_ready(&sms);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* gqa_status_string(gqa_status_t status) {
+  switch (status) {
+    case GQA_OK: return "GQA_OK";
+    case GQA_ERR_INVALID_ARGUMENT: return "GQA_ERR_INVALID_ARGUMENT";
+    case GQA_ERR_UNSUPPORTED_DEVICE: return "GQA_ERR_UNSUPPORTED_DEVICE";
+    case GQA_ERR_WORKSPACE_TOO_SMALL: return "GQA_ERR_WORKSPACE_TOO_SMALL";
+    case GQA_ERR_ALIASING: return "GQA_ERR_ALIASING";
+    case GQA_ERR_CUDA: return "GQA_ERR_CUDA";
+  }
+  return "GQA_ERR_UNKNOWN";
+}
+
+const char* gqa_last_error(void) { return g_last_error.c_str(); }
+
+size_t gqa_decode_workspace_size(int batch, int capacity, int num_splits) {
+  if (batch < 1 || capacity < 1 || num_splits < 1 || num_splits > GQA_MAX_SPLITS) return 0;
+  return workspace_bytes_for(batch, num_splits);
+}
+
+gqa_status_t gqa_decode_plan(int batch, int capacity, gqa_kv_format_t kv_format, int device,
+                             int* num_splits_out) {
+  if (!num_splits_out) return fail(GQA_ERR_INVALID_ARGUMENT, "num_splits_out is null");
+  gqa_status_t st = validate_shape(batch, capacity);
+  if (st != GQA_OK) return st;
+  if (kv_format != GQA_KV_F16 && kv_format != GQA_KV_BF16 && kv_format != GQA_KV_E4M3)
+    return fail(GQA_ERR_INVALID_ARGUMENT, "unknown KV format %d", (int)kv_format);
+  int sms = 0;
+  st = device_ready(device, &sms);
+  if (st != GQA_OK) return st;
+  *num_splits_out = plan_splits(batch, capacity, kv_format, sms);
+  return GQA_OK;
+}
+
+gqa_status_t gqa_decode_plan_for(int batch, int capacity, gqa_kv_format_t kv_format, int sm_count,
+                                 int* num_splits_out) {
+  if (!num_splits_out) return fail(GQA_ERR_INVALID_ARGUMENT, "num_splits_out is null");
+  gqa_status_t st = validate_shape(batch, capacity);
+  if (st != GQA_OK) return st;
+  if (kv_format != GQA_KV_F16 && kv_format != GQA_KV_BF16 && kv_format != GQA_KV_E4M3)
+    return fail(GQA_ERR_INVALID_ARGUMENT, "unknown KV format %d", (int)kv_format);
+  if (sm_count < 1) return fail(GQA_ERR_INVALID_ARGUMENT, "sm_count %d < 1", sm_count);
+  *num_splits_out = plan_splits(batch, capacity, kv_format, sm_count);
+  return GQA_OK;
+}
+
+gqa_status_t gqa_decode_split_geometry(int capacity, int num_splits, gqa_kv_format_t kv_format,
+                                       int* chunk_tokens_out, int* splits_effective_out) {
+  if (!chunk_tokens_out || !splits_effective_out) return fail(GQA_ERR_INVALID_ARGUMENT, "null output pointer");
+  gqa_status_t st = validate_shape(1, capacity);
+  if (st != GQA_OK) return st;
+  if (kv_format != GQA_KV_F16 && kv_format != GQA_KV_BF16 && kv_format != GQA_KV_E4M3)
+    return fail(GQA_ERR_INVALID_ARGUMENT, "unknown KV format %d", (int)kv_format);
+  if (num_splits < 1 || num_splits > GQA_MAX_SPLITS)
+    return fail(GQA_ERR_INVALID_ARGUMENT, "num_splits %d outside [1, %d]", num_splits, GQA_MAX_SPLITS);
+  *chunk_tokens_out = split_chunk(capacity, num_splits, (int)kv_format);
+  *splits_effective_out = split_count(capacity, num_splits, (int)kv_format);
+  return GQA_OK;
+}
+
+gqa_status_t gqa_decode_prepared(const void* q, const void* kv, const int32_t* lens, void* out, int batch,
+                                 int capacity, gqa_dtype_t dtype, float q_scale, int num_splits,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+  Call c{q, (int)dtype, kv, (int)dtype, lens, out, batch, capacity, q_scale, 1.f, 1.f, num_splits,
+         workspace, workspace_bytes, static_cast<cudaStream_t>(stream)};
+  gqa_status_t st = prepare_call(c, /*q_scale_positive=*/true, true);
+  if (st != GQA_OK) return st;
+  st = run_split(c);
+  if (st != GQA_OK) return st;
+  return run_combine(c);
+}
+
+gqa_status_t gqa_decode_fp8kv(const void* q_bf16, const uint8_t* kv_e4m3, const int32_t* lens, void* out_bf16,
+                              int batch, int capacity, float q_scale, float k_scale, float v_scale,
+                              int num_splits, void* workspace, size_t workspace_bytes, void* stream) {
+  Call c{q_bf16, GQA_BF16, kv_e4m3, kKvE4M3, lens, out_bf16, batch, capacity, q_scale, k_scale, v_scale,
+         num_splits, workspace, workspace_bytes, static_cast<cudaStream_t>(stream)};
+  gqa_status_t st = prepare_call(c, false, true);
+  if (st != GQA_OK) return st;
+  st = run_split(c);
+  if (st != GQA_OK) return st;
+  return run_combine(c);
+}
+
+gqa_status_t gqa_decode_split_stage(const void* q, gqa_dtype_t q_dtype, const void* kv,
+                                    gqa_kv_format_t kv_format, const int32_t* lens, void* out, int batch,
+                                    int capacity, float q_scale, float k_scale, float v_scale, int num_splits,
+                                    void* workspace, size_t workspace_bytes, void* stream) {
+  Call c{q, (int)q_dtype, kv, (int)kv_format, lens, out, batch, capacity, q_scale, k_scale, v_scale,
+         num_splits, workspace, workspace_bytes, static_cast<cudaStream_t>(stream)};
+  gqa_status_t st = prepare_call(c, false, true);
+  if (st != GQA_OK) return st;
+  return run_split(c);
+}
+
+gqa_status_t gqa_decode_combine_stage(const int32_t* lens, void* out, gqa_dtype_t out_dtype,
+                                      gqa_kv_format_t kv_format, int batch, int capacity, float v_scale,
+                                      int num_splits, const void* workspace, size_t workspace_bytes,
+                                      void* stream) {
+  // kv and q are not read by stage 2; stand in a dummy aligned address for
+  // the checks (a null kv would be rejected) and skip the q checks.
+  static const uint4 dummy = {0, 0, 0, 0};
+  const int fmt = (int)kv_format;
+  Call c{nullptr, (int)out_dtype, &dummy, fmt == kKvE4M3 ? fmt : (int)out_dtype, lens, out, batch,
+         capacity, 1.f, 1.f, v_scale, num_splits, const_cast<void*>(workspace), workspace_bytes,
+         static_cast<cudaStream_t>(stream)};
+  if (fmt != kKvE4M3 && fmt != (int)out_dtype && fmt != kKvF16 && fmt != kKvBF16)
+    return fail(GQA_ERR_INVALID_ARGUMENT, "unknown KV format %d", fmt);
+  c.kv_format = fmt;
+  if (fmt != kKvE4M3 && fmt != (int)out_dtype)
+    return fail(GQA_ERR_INVALID_ARGUMENT, "fp16/bf16 KV must have the dtype of out");
+  // the dummy kv range (batch*capacity*...) would spuriously overlap out; check
+  // only what stage 2 touches
+  if (!lens || !out || !workspace) return fail(GQA_ERR_INVALID_ARGUMENT, "null pointer argument");
+  gqa_status_t st = validate_shape(batch, capacity);
+  if (st != GQA_OK) return st;
+  if (out_dtype != GQA_F16 && out_dtype != GQA_BF16)
+    return fail(GQA_ERR_INVALID_ARGUMENT, "unknown out dtype %d", (int)out_dtype);
+  if (!std::isfinite(v_scale) || v_scale <= 0.f)
+    return fail(GQA_ERR_INVALID_ARGUMENT, "v_scale must be finite and > 0");
+  if (num_splits < 1 || num_splits > GQA_MAX_SPLITS)
+    return fail(GQA_ERR_INVALID_ARGUMENT, "num_splits %d outside [1, %d]", num_splits, GQA_MAX_SPLITS);
+  if (!aligned(out, 16) || !aligned(workspace, 16) || !aligned(lens, 4))
+    return fail(GQA_ERR_INVALID_ARGUMENT, "out, workspace must be 16-byte aligned, lens 4-byte");
+  const size_t need = workspace_bytes_for(batch, num_splits);
+  if (workspace_bytes < need)
+    return fail(GQA_ERR_WORKSPACE_TOO_SMALL, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
+  if (overlap(out, (size_t)batch * kHq * kD * 2, workspace, need))
+    return fail(GQA_ERR_ALIASING, "out overlaps the workspace");
+  st = current_device_ready(nullptr);
+  if (st != GQA_OK) return st;
+  return run_combine(c);
+}
+
+gqa_status_t gqa_decode(const void* q, const void* kv, const int32_t* lens, void* out, int batch, int capacity,
+                        gqa_dtype_t dtype, float q_scale, void* stream) {
+  static const uint4 dummy_ws = {0, 0, 0, 0};
+  Call c{q, (int)dtype, kv, (int)dtype, lens, out, batch, capacity, q_scale, 1.f, 1.f, 0,
+         const_cast<uint4*>(&dummy_ws), (size_t)-1, static_cast<cudaStream_t>(stream)};
+  // validate with a stand-in workspace, then allocate the real one
+  Call probe = c;
+  probe.num_splits = 1;
+  gqa_status_t st = validate(probe, false, true);
+  if (st != GQA_OK) return st;
+  int sms = 0;
+  st = current_device_ready(&sms);
+  if (st != GQA_OK) return st;
+  c.num_splits = plan_splits(batch, capacity, (int)dtype, sms);
+  const size_t bytes = workspace_bytes_for(batch, c.num_splits);
+  void* ws = nullptr;
+  cudaError_t e = cudaMallocAsync(&ws, bytes, c.stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync(workspace)");
+  c.workspace = ws;
+  c.workspace_bytes = bytes;
+  e = cudaMemsetAsync(ws, 0, GQA_WORKSPACE_HEADER_BYTES, c.stream);
+  if (e != cudaSuccess) st = cuda_fail(e, "cudaMemsetAsync(workspace header)");
+  if (st == GQA_OK) st = validate(c, false, true);
+  if (st == GQA_OK) st = run_split(c);
+  if (st == GQA_OK) st = run_combine(c);
+  e = cudaFreeAsync(ws, c.stream);
+  if (st == GQA_OK && e != cudaSuccess) st = cuda_fail(e, "cudaFreeAsync(workspace)");
+  return st;
+}
+
+gqa_status_t gqa_decode_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
+  if (!workspace || workspace_bytes < GQA_WORKSPACE_HEADER_BYTES)
+    return fail(GQA_ERR_INVALID_ARGUMENT, "workspace must be non-null and hold the %d-byte header",
+                GQA_WORKSPACE_HEADER_BYTES);
+  cudaError_t e = cudaMemsetAsync(workspace, 0, GQA_WORKSPACE_HEADER_BYTES, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(workspace header)");
+  return GQA_OK;
+}
+
+gqa_status_t gqa_decode_get_status(void* workspace, size_t workspace_bytes, void* stream, uint32_t* flags) {
+  if (!workspace || !flags || workspace_bytes < GQA_WORKSPACE_HEADER_BYTES)
+    return fail(GQA_ERR_INVALID_ARGUMENT, "workspace and flags must be non-null; workspace >= header");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t host = 0;
+  cudaError_t e = cudaMemcpyAsync(&host, workspace, sizeof host, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, sizeof(uint32_t), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the workspace status word");
+  *flags = host;
+  return GQA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,73 @@
+// Stage 2 of GQA decode: log-sum-exp merge of the split-KV partials.
+//
+// For each (b, query head h) the splits that hold tokens (n = ceil(len/chunk)
+// of them; later splits are skipped, never read) carry an unnormalised
+// accumulator O_s, a running max m_s (log2 domain) and a denominator l_s.
+// With M = max_s m_s and w_s = 2^(m_s - M):
+//   out = v_scale * (sum_s w_s O_s) / (sum_s w_s l_s)
+// rounded once to fp16/bf16 (nearest even).  This is the merge of the
+// "FlashInfer sm110_gqa_decode" article's "num_splits" section, written as a
+// separate kernel so stage 1 needs no inter-CTA ticket.  One warp per
+// (b, h), each lane owning 4 dims; the splits are merged in a fixed order, so
+// the result is bitwise deterministic.
+#pragma once
+
+#include "common.cuh"
+
+namespace gqa {
+
+constexpr int kCombineThreads = kGroup * 32;  // one warp per query head of a KV head
+
+struct CombineParams {
+  const int32_t* lens;
+  void* out;
+  const float* part_o;
+  const float* part_m;
+  const float* part_l;
+  int capacity, num_splits, chunk;
+  float v_scale;
+};
+
+template <int QF>
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_constant__ CombineParams p) {
+  const int g = blockIdx.x, b = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = g * kGroup + warp;
+  const int L = min(max(__ldg(p.lens + b), 0), p.capacity);
+  const int n = (L + p.chunk - 1) / p.chunk;
+  const size_t base = (size_t)(b * kHq + h) * p.num_splits;
+
+  float M = -INFINITY;
+  for (int s = lane; s < n; s += 32) M = fmaxf(M, __ldg(p.part_m + base + s));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+
+  float Ls = 0.f;
+  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+  const float4* po = reinterpret_cast<const float4*>(p.part_o) + base * (kD / 4) + lane;
+#pragma unroll 4
+  for (int s = 0; s < n; ++s) {
+    const float w = ex2(__ldg(p.part_m + base + s) - M);
+    Ls = fmaf(w, __ldg(p.part_l + base + s), Ls);
+    const float4 v = __ldg(po + (size_t)s * (kD / 4));
+    o.x = fmaf(w, v.x, o.x);
+    o.y = fmaf(w, v.y, o.y);
+    o.z = fmaf(w, v.z, o.z);
+    o.w = fmaf(w, v.w, o.w);
+  }
+  const float inv = n > 0 ? p.v_scale / Ls : 0.f;
+  uint2 packed;
+  if constexpr (QF == kQF16) {
+    const __half2 a = __floats2half2_rn(o.x * inv, o.y * inv);
+    const __half2 c = __floats2half2_rn(o.z * inv, o.w * inv);
+    packed = make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&c));
+  } else {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(o.x * inv, o.y * inv);
+    const __nv_bfloat162 c = __floats2bfloat162_rn(o.z * inv, o.w * inv);
+    packed = make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&c));
+  }
+  *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) + ((size_t)(b * kHq + h) * kD + 4 * lane) * 2) =
+      packed;
+}
+
+}  // namespace gqa

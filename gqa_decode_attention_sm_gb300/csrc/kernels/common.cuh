@@ -1,0 +1,152 @@
+// Device-side building blocks shared by the decode kernels: the fixed head
+// geometry, the KV formats, and thin inline-PTX wrappers for the sm_90+ async
+// machinery used on sm_103a (mbarrier, 1-D bulk copies through the TMA unit,
+// L2 eviction policies, the global nanosecond timer) and the ex2 instruction.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+namespace gqa {
+
+// 32 query heads share 8 KV heads (4 per KV head), head_dim 128, one query
+// token per request ("FlashInfer sm110_gqa_decode" article, "Input contract").
+constexpr int kHq = 32;
+constexpr int kHkv = 8;
+constexpr int kGroup = kHq / kHkv;
+constexpr int kD = 128;
+
+enum KvFormat : int { kKvF16 = 0, kKvBF16 = 1, kKvE4M3 = 2 };
+enum QFormat : int { kQF16 = 0, kQBF16 = 1 };
+
+// Tokens per pipeline tile: one tile of one plane is 16 KB for every format.
+__host__ __device__ constexpr int tile_tokens(int kv_format) {
+  return kv_format == kKvE4M3 ? 128 : 64;
+}
+
+template <int KVF>
+struct KvTraits {
+  static constexpr int kElemBytes = KVF == kKvE4M3 ? 1 : 2;
+  static constexpr int kRowBytes = kD * kElemBytes;  // one token of one KV head
+  static constexpr int kTile = tile_tokens(KVF);
+  static constexpr int kTileBytes = kTile * kRowBytes;
+};
+
+// Split geometry shared by the split and combine kernels: chunk = tokens per
+// split, rounded up to whole tiles; effective split count = ceil(C / chunk).
+__host__ __device__ inline int split_chunk(int capacity, int num_splits, int kv_format) {
+  const int tile = tile_tokens(kv_format);
+  const int per = (capacity + num_splits - 1) / num_splits;
+  return (per + tile - 1) / tile * tile;
+}
+__host__ __device__ inline int split_count(int capacity, int num_splits, int kv_format) {
+  const int chunk = split_chunk(capacity, num_splits, kv_format);
+  return (capacity + chunk - 1) / chunk;
+}
+
+// A pipeline wait gives up after this long (a healthy wait lasts microseconds).
+constexpr uint64_t kWaitBudgetNs = 4000000000ull;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+// Make barrier initialisation visible to the async (TMA) proxy.
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Wait until the phase with the given parity has completed, or until the
+// global timer passes `deadline_ns`; returns false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t deadline_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  for (uint32_t spin = 1;; ++spin) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((spin & 63u) == 0 && global_timer_ns() > deadline_ns) return false;
+  }
+}
+
+// L2 policy for data streamed exactly once (the KV cache).
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// 1-D bulk copy global -> shared through the TMA unit; completion is counted
+// in bytes on `bar`.  dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// 2^x with the hardware approximation (subnormal results flushed to zero).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ---- element conversions (exact) -------------------------------------------
+
+__device__ __forceinline__ float2 f16x2_to_f32x2(uint32_t w) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&w));
+}
+
+// bf16 is the upper half of an fp32 bit pattern.
+__device__ __forceinline__ float2 bf16x2_to_f32x2(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+// Two e4m3 bytes (low byte = first element) -> f16x2 with the hardware
+// conversion; every e4m3 value is exact in fp16.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t two) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(two));
+  return h2;
+}
+
+}  // namespace gqa

@@ -1,0 +1,183 @@
+/*
+ * gqa_decode.h -- C ABI of libgqa_decode.so: single-token grouped-query decode
+ * attention over a KV cache on NVIDIA GB300 (sm_103a).
+ *
+ * What is computed (restated from the "FlashInfer sm110_gqa_decode" article,
+ * sections "Input contract", "Convenience API" and "Prepared continuous
+ * decoding", and for FP8 from the "FP8 KV cache port on Jetson AGX Thor" blog,
+ * section 1, patch 2):
+ *
+ *   Fixed geometry: 32 query heads, 8 KV heads, head_dim 128, one query token
+ *   per request.  Query head h reads KV head g = h / 4 (the grouped view
+ *   q.view(batch, 8, 4, 128)).  For every batch row b and query head h:
+ *     s_t   = q_scale * k_scale / sqrt(128) * dot(q[b,h,:], K[b,g,t,:]),  0 <= t < len[b]
+ *     out[b,h,:] = v_scale * sum_t softmax(s)_t * V[b,g,t,:]
+ *   k_scale = v_scale = 1 except on the e4m3 entry point.  Slots t >= len[b]
+ *   are never read.  Arithmetic is FP32 (exp2-domain online softmax); the
+ *   output is rounded once to fp16/bf16, round-to-nearest-even.
+ *
+ * Layouts (all dense, row-major, contiguous; element offsets):
+ *   q    [batch, 32, 128]              fp16 or bf16 (gqa_dtype_t)
+ *   kv   [batch, 2, 8, capacity, 128]  plane 0 = K, plane 1 = V;
+ *                                      same dtype as q, or e4m3 bytes (fp8 entry)
+ *   lens int32 [batch], device memory, read only by the kernels; the contract
+ *        is 1 <= lens[b] <= capacity (see "Lengths" below)
+ *   out  [batch, 32, 128]              same dtype as q (bf16 on the fp8 entry)
+ *   q, kv, out and the workspace must be 16-byte aligned; lens 4-byte aligned.
+ *
+ * Pointers are device pointers unless stated.  `stream` is a cudaStream_t
+ * (NULL = the legacy default stream).  Every launching call is asynchronous,
+ * enqueues on `stream`, reads nothing back to the host and performs no host
+ * synchronisation, except gqa_decode_get_status (documented there).
+ *
+ * Ownership: the caller owns every buffer (q, kv, lens, out, workspace).  The
+ * library never frees caller memory and keeps no pointer past the call.  The
+ * only library-owned state is a per-device cache of the device check and of
+ * kernel attributes.
+ *
+ * Errors: every function validates its arguments before any CUDA call and
+ * returns a gqa_status_t; no exception or abort crosses this ABI.  A
+ * thread-local message with details of the last failure on the calling thread
+ * is available from gqa_last_error().
+ *
+ * Lengths: read on the device only.  A length outside [1, capacity] is
+ * clamped to [0, capacity] (0 produces a zero output row), never read out of
+ * bounds, and flagged with GQA_FLAG_LENGTH_CLAMPED in the workspace header
+ * (gqa_decode_get_status).
+ *
+ * Workspace (split-KV, the flash-decoding scheme of the article's
+ * "num_splits" section): a caller-owned device buffer of
+ * gqa_decode_workspace_size(batch, capacity, num_splits) bytes.  It holds a
+ * 256-byte header (status flags) and FP32 partial results (unnormalised
+ * output, running max in the log2 domain, softmax denominator) per
+ * (b, query head, split).  Zero the header once before first use
+ * (gqa_decode_workspace_init).  Launches that may run concurrently (different
+ * streams or graphs) need distinct workspaces; launches ordered on one stream
+ * may share one.
+ */
+#ifndef GQA_DECODE_H_
+#define GQA_DECODE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GQA_NUM_Q_HEADS 32
+#define GQA_NUM_KV_HEADS 8
+#define GQA_HEAD_DIM 128
+#define GQA_MAX_SPLITS 256
+#define GQA_WORKSPACE_HEADER_BYTES 256
+
+typedef enum {
+  GQA_OK = 0,
+  GQA_ERR_INVALID_ARGUMENT = 1,   /* null pointer, size, dtype, scale, misalignment */
+  GQA_ERR_UNSUPPORTED_DEVICE = 2, /* not a compute capability 10.3 (sm_103) device */
+  GQA_ERR_WORKSPACE_TOO_SMALL = 3,
+  GQA_ERR_ALIASING = 4,           /* out overlaps q, kv or lens */
+  GQA_ERR_CUDA = 5                /* a CUDA runtime call failed (see gqa_last_error) */
+} gqa_status_t;
+
+typedef enum { GQA_F16 = 0, GQA_BF16 = 1 } gqa_dtype_t;
+
+typedef enum { GQA_KV_F16 = 0, GQA_KV_BF16 = 1, GQA_KV_E4M3 = 2 } gqa_kv_format_t;
+
+/* Bits of the status word in the workspace header. */
+#define GQA_FLAG_LENGTH_CLAMPED 0x1u  /* some lens[b] was outside [1, capacity] */
+#define GQA_FLAG_WAIT_TIMEOUT 0x2u    /* a pipeline wait gave up; outputs are invalid */
+
+/* Name of a status code (static string). */
+const char* gqa_status_string(gqa_status_t status);
+
+/* Details of the last failure on the calling thread ("" if none). */
+const char* gqa_last_error(void);
+
+/* Bytes of workspace needed for (batch, capacity, num_splits); 0 if the
+ * arguments are invalid (batch, capacity < 1; num_splits outside
+ * [1, GQA_MAX_SPLITS]).  num_splits = 1 needs only the 256-byte header. */
+size_t gqa_decode_workspace_size(int batch, int capacity, int num_splits);
+
+/* Host-only split planner (no CUDA call besides a cached SM-count query; safe
+ * during stream capture once the device has been seen).  Picks the number of
+ * KV splits from batch x capacity, the KV format and the SM count of `device`,
+ * so that the (batch, KV head, split) work items fill the GPU several times
+ * over.  Writes the chosen count (1..GQA_MAX_SPLITS) to *num_splits_out. */
+gqa_status_t gqa_decode_plan(int batch, int capacity, gqa_kv_format_t kv_format, int device,
+                             int* num_splits_out);
+
+/* The same planner with the SM count given: pure host arithmetic, no CUDA
+ * call.  sm_count < 1 is invalid. */
+gqa_status_t gqa_decode_plan_for(int batch, int capacity, gqa_kv_format_t kv_format, int sm_count,
+                                 int* num_splits_out);
+
+/* Split geometry (pure host arithmetic): tokens per split, rounded up to
+ * whole 64-token (fp16/bf16) or 128-token (e4m3) tiles, and the number of
+ * splits that hold slots, ceil(capacity / chunk) <= num_splits.  Split s covers
+ * slots [s * chunk, min((s + 1) * chunk, len)); stage 2 runs only when the
+ * effective count is above 1. */
+gqa_status_t gqa_decode_split_geometry(int capacity, int num_splits, gqa_kv_format_t kv_format,
+                                       int* chunk_tokens_out, int* splits_effective_out);
+
+/* Convenience call (the article's sm110_gqa_decode): plans the split count,
+ * takes a stream-ordered workspace with cudaMallocAsync/cudaFreeAsync on
+ * `stream`, and launches.  q_scale must be finite and >= 0 (0 gives the mean
+ * of V).  Length-clamp flags are not observable through this call. */
+gqa_status_t gqa_decode(const void* q, const void* kv, const int32_t* lens, void* out,
+                        int batch, int capacity, gqa_dtype_t dtype, float q_scale,
+                        void* stream);
+
+/* Prepared call (the article's launch_sm110_gqa_decode_prepared): no
+ * allocation and no host synchronisation, so it can be captured in a CUDA
+ * graph.  q_scale must be finite and > 0 (as the article's prepare step
+ * requires).  num_splits = 0 picks gqa_decode_plan's choice; otherwise
+ * 1..GQA_MAX_SPLITS.  `workspace` must hold gqa_decode_workspace_size(batch,
+ * capacity, num_splits) bytes (after resolving 0).  `out` must not overlap q,
+ * kv or lens. */
+gqa_status_t gqa_decode_prepared(const void* q, const void* kv, const int32_t* lens, void* out,
+                                 int batch, int capacity, gqa_dtype_t dtype, float q_scale,
+                                 int num_splits, void* workspace, size_t workspace_bytes,
+                                 void* stream);
+
+/* FP8 KV cache (the blog's e4m3 port): kv holds float8 e4m3fn bytes (OCP FP8:
+ * bias 7, no infinities, 0x7F/0xFF NaN), q and out are bf16.  k_scale
+ * multiplies the scores, v_scale the normalised output; both finite and > 0.
+ * q_scale finite and >= 0.  Other rules as gqa_decode_prepared. */
+gqa_status_t gqa_decode_fp8kv(const void* q_bf16, const uint8_t* kv_e4m3, const int32_t* lens,
+                              void* out_bf16, int batch, int capacity, float q_scale,
+                              float k_scale, float v_scale, int num_splits, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/* The two stages of a prepared launch, for callers that schedule (or time)
+ * them separately.  Stage 1 streams K/V once per (b, KV head, split) and
+ * writes FP32 partials to the workspace, or the final output when
+ * num_splits == 1.  Stage 2 merges the partials of each (b, query head) with
+ * a log-sum-exp combine and writes `out`; with num_splits == 1 it launches
+ * nothing.  Both must be given the same geometry, scales and workspace, in
+ * this order, on one stream.  Validation as gqa_decode_prepared, except that
+ * q_scale may be 0. */
+gqa_status_t gqa_decode_split_stage(const void* q, gqa_dtype_t q_dtype, const void* kv,
+                                    gqa_kv_format_t kv_format, const int32_t* lens, void* out,
+                                    int batch, int capacity, float q_scale, float k_scale,
+                                    float v_scale, int num_splits, void* workspace,
+                                    size_t workspace_bytes, void* stream);
+gqa_status_t gqa_decode_combine_stage(const int32_t* lens, void* out, gqa_dtype_t out_dtype,
+                                      gqa_kv_format_t kv_format, int batch, int capacity,
+                                      float v_scale, int num_splits, const void* workspace,
+                                      size_t workspace_bytes, void* stream);
+
+/* Zero the workspace header (status flags) on `stream`.  Asynchronous. */
+gqa_status_t gqa_decode_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/* Debug only, never inside a capture: synchronises `stream`, copies the
+ * status word of the workspace header to *flags (GQA_FLAG_* bits) and clears
+ * it. */
+gqa_status_t gqa_decode_get_status(void* workspace, size_t workspace_bytes, void* stream,
+                                   uint32_t* flags);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_DECODE_H_ */

@@ -1,0 +1,201 @@
+"""Host-side tests of the C ABI that need no GPU.
+
+The library is built with nvcc (cross-compiling for sm_103a works without a
+GPU) and loaded with ctypes.  Checked here: every function declared in
+include/gqa_decode.h is exported; workspace sizes; the split planner's table;
+and that argument validation returns the documented status before any CUDA
+call (the fake device addresses below are never dereferenced).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from gqa_decode_attention_sm_gb300 import _lib
+from gqa_decode_attention_sm_gb300 import build as gbuild
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "gqa_decode.h")
+
+OK, EINVAL, EDEV, EWS, EALIAS, ECUDA = 0, 1, 2, 3, 4, 5
+F16, BF16 = 0, 1
+KV_F16, KV_BF16, KV_E4M3 = 0, 1, 2
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gbuild.build()
+    return _lib.load()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gqa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_and_binding_agree():
+    assert _declared_functions() == sorted(_lib.EXPORTS)
+
+
+def test_library_exports_every_declared_function(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError, match="missing"):
+        _lib.load(str(tmp_path / "libnothing.so"))
+
+
+def test_status_strings(lib):
+    names = [lib.gqa_status_string(i).decode() for i in range(6)]
+    assert names == ["GQA_OK", "GQA_ERR_INVALID_ARGUMENT", "GQA_ERR_UNSUPPORTED_DEVICE",
+                     "GQA_ERR_WORKSPACE_TOO_SMALL", "GQA_ERR_ALIASING", "GQA_ERR_CUDA"]
+
+
+def _ws_expected(B, S):
+    if S == 1:
+        return 256
+    up = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    return 256 + up(B * 32 * S * 128 * 4) + 2 * up(B * 32 * S * 4)
+
+
+@pytest.mark.parametrize("B,C,S", [(1, 64, 1), (1, 1024, 16), (8, 131072, 19), (64, 32768, 3),
+                                   (32, 8192, 256), (3, 5, 7)])
+def test_workspace_size(lib, B, C, S):
+    assert lib.gqa_decode_workspace_size(B, C, S) == _ws_expected(B, S)
+
+
+@pytest.mark.parametrize("args", [(0, 64, 1), (1, 0, 1), (1, 64, 0), (1, 64, 257), (-1, 64, 2)])
+def test_workspace_size_invalid(lib, args):
+    assert lib.gqa_decode_workspace_size(*args) == 0
+
+
+def _plan(lib, B, C, fmt, sms):
+    n = ctypes.c_int(-1)
+    st = lib.gqa_decode_plan_for(B, C, fmt, sms, ctypes.byref(n))
+    return st, n.value
+
+
+def _chunk(C, S, fmt):
+    tile = 128 if fmt == KV_E4M3 else 64
+    per = -(-C // S)
+    return -(-per // tile) * tile
+
+
+# (batch, capacity, format, SM count) -> splits: about 8 waves of one-CTA-per-SM
+# work over the worst case, whole tiles per split, 1..256 splits.
+PLAN_TABLE = [
+    ((1, 64, KV_F16, 152), 1),
+    ((1, 1024, KV_F16, 152), 16),
+    ((32, 8192, KV_F16, 152), 5),
+    ((8, 131072, KV_BF16, 152), 19),
+    ((64, 32768, KV_E4M3, 152), 3),
+    ((1, 1 << 20, KV_BF16, 152), 152),
+    ((1, 1 << 22, KV_BF16, 400), 256),
+    ((1, 1, KV_F16, 152), 1),
+    ((65535, 64, KV_F16, 152), 1),
+]
+
+
+@pytest.mark.parametrize("args,want", PLAN_TABLE)
+def test_plan_table(lib, args, want):
+    st, S = _plan(lib, *args)
+    assert st == OK and S == want
+
+
+@pytest.mark.parametrize("B,C,fmt", [(b, c, f) for b in (1, 3, 8, 64) for c in (1, 63, 64, 65, 1000, 131072)
+                                     for f in (KV_F16, KV_E4M3)])
+def test_plan_invariants(lib, B, C, fmt):
+    st, S = _plan(lib, B, C, fmt, 152)
+    assert st == OK and 1 <= S <= 256
+    chunk = _chunk(C, S, fmt)
+    tile = 128 if fmt == KV_E4M3 else 64
+    assert chunk % tile == 0 and chunk * S >= C
+    splits_eff = -(-C // chunk)
+    assert 1 <= splits_eff <= S
+
+
+@pytest.mark.parametrize("C,S,fmt,chunk,eff", [(64, 1, KV_F16, 64, 1), (1024, 16, KV_F16, 64, 16),
+                                                (1000, 7, KV_F16, 192, 6), (1000, 256, KV_E4M3, 128, 8),
+                                                (131072, 19, KV_BF16, 6912, 19), (1, 3, KV_F16, 64, 1)])
+def test_split_geometry(lib, C, S, fmt, chunk, eff):
+    a, b = ctypes.c_int(0), ctypes.c_int(0)
+    assert lib.gqa_decode_split_geometry(C, S, fmt, ctypes.byref(a), ctypes.byref(b)) == OK
+    assert (a.value, b.value) == (chunk, eff) == (_chunk(C, S, fmt), -(-C // _chunk(C, S, fmt)))
+
+
+def test_plan_rejects_bad_arguments(lib):
+    assert _plan(lib, 0, 64, KV_F16, 152)[0] == EINVAL
+    assert _plan(lib, 1, 64, 7, 152)[0] == EINVAL
+    assert _plan(lib, 1, 64, KV_F16, 0)[0] == EINVAL
+    assert lib.gqa_decode_plan_for(1, 64, KV_F16, 152, None) == EINVAL
+
+
+# Fake, well-aligned device addresses: validation must fail before any use.
+Q, KV, LENS, OUT, WS = 0x10000000, 0x20000000, 0x30000000, 0x40000000, 0x50000000
+
+
+def _prepared(lib, **kw):
+    a = dict(q=Q, kv=KV, lens=LENS, out=OUT, B=2, C=64, dtype=F16, q_scale=1.0, S=1, ws=WS,
+             ws_bytes=256, stream=None)
+    a.update(kw)
+    return lib.gqa_decode_prepared(a["q"], a["kv"], a["lens"], a["out"], a["B"], a["C"], a["dtype"],
+                                   a["q_scale"], a["S"], a["ws"], a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(q=None), EINVAL), (dict(kv=None), EINVAL), (dict(lens=None), EINVAL),
+    (dict(out=None), EINVAL), (dict(ws=None), EINVAL),
+    (dict(B=0), EINVAL), (dict(B=70000), EINVAL), (dict(C=0), EINVAL),
+    (dict(dtype=2), EINVAL),
+    (dict(q_scale=0.0), EINVAL), (dict(q_scale=-1.0), EINVAL), (dict(q_scale=float("inf")), EINVAL),
+    (dict(q_scale=float("nan")), EINVAL),
+    (dict(S=-1), EINVAL), (dict(S=257), EINVAL),
+    (dict(q=Q + 8), EINVAL), (dict(kv=KV + 4), EINVAL), (dict(out=OUT + 2), EINVAL),
+    (dict(lens=LENS + 2), EINVAL), (dict(ws=WS + 8), EINVAL),
+    (dict(S=4, ws_bytes=256), EWS), (dict(ws_bytes=100), EWS),
+    (dict(out=Q), EALIAS), (dict(out=KV + 4096), EALIAS), (dict(out=LENS - 16), EALIAS),
+    (dict(ws=OUT + 1024), EALIAS), (dict(ws=KV + 256), EALIAS),
+])
+def test_prepared_validation(lib, kw, want):
+    assert _prepared(lib, **kw) == want
+    assert lib.gqa_last_error().decode() != ""
+
+
+def test_fp8_validation(lib):
+    f = lib.gqa_decode_fp8kv
+    assert f(Q, KV, LENS, OUT, 2, 64, 1.0, 0.0, 1.0, 1, WS, 256, None) == EINVAL   # k_scale 0
+    assert f(Q, KV, LENS, OUT, 2, 64, 1.0, 1.0, -2.0, 1, WS, 256, None) == EINVAL  # v_scale < 0
+    assert f(Q, KV, LENS, OUT, 2, 64, 1.0, 1.0, float("inf"), 1, WS, 256, None) == EINVAL
+    assert f(Q, KV, LENS, OUT, 2, 64, -1.0, 1.0, 1.0, 1, WS, 256, None) == EINVAL  # q_scale < 0
+    assert f(Q, KV, LENS, OUT, 2, 64, 1.0, 1.0, 1.0, 3, WS, 256, None) == EWS
+
+
+def test_stage_validation(lib):
+    s = lib.gqa_decode_split_stage
+    # fp16 KV with bf16 q is rejected; e4m3 KV accepts either q dtype
+    assert s(Q, BF16, KV, KV_F16, LENS, OUT, 2, 64, 1.0, 1.0, 1.0, 1, WS, 256, None) == EINVAL
+    assert s(Q, F16, KV, 9, LENS, OUT, 2, 64, 1.0, 1.0, 1.0, 1, WS, 256, None) == EINVAL
+    c = lib.gqa_decode_combine_stage
+    assert c(None, OUT, F16, KV_F16, 2, 64, 1.0, 1, WS, 256, None) == EINVAL
+    assert c(LENS, OUT, F16, KV_F16, 2, 64, 0.0, 1, WS, 256, None) == EINVAL
+    assert c(LENS, OUT, F16, KV_F16, 2, 64, 1.0, 4, WS, 256, None) == EWS
+    assert c(LENS, WS + 64, F16, KV_F16, 2, 64, 1.0, 1, WS, 256, None) == EALIAS
+
+
+def test_convenience_validation(lib):
+    g = lib.gqa_decode
+    assert g(None, KV, LENS, OUT, 1, 64, F16, 1.0, None) == EINVAL
+    assert g(Q, KV, LENS, OUT, 1, 64, F16, -0.5, None) == EINVAL
+    assert g(Q, KV, LENS, Q, 1, 64, F16, 1.0, None) == EALIAS
+
+
+def test_status_calls_validate(lib):
+    flags = ctypes.c_uint32(0)
+    assert lib.gqa_decode_get_status(None, 256, None, ctypes.byref(flags)) == EINVAL
+    assert lib.gqa_decode_get_status(WS, 16, None, ctypes.byref(flags)) == EINVAL
+    assert lib.gqa_decode_workspace_init(None, 256, None) == EINVAL
+    assert lib.gqa_decode_workspace_init(WS, 8, None) == EINVAL

@@ -1,0 +1,344 @@
+"""GPU parity: the CUDA path (through the C ABI) against the FP64 oracle.
+
+Bar (element-wise): |gpu - oracle| <= 3e-3, or <= 1e-2 * |oracle| where
+|oracle| > 0.3, every output finite.  Small workloads are compared on every
+element; the two full-size workloads (bf16 8 x 131072, e4m3 64 x U[16k,32k])
+are run in the launch configuration the benchmark times and compared on
+sampled (b, KV head) units (all 4 query heads each).  Also covered: ragged
+lengths and tile edges, capacity 1, every split count, q_scale 0, distinct
+fp8 scales, NaN tails (bit-exact output whatever the unused slots hold; the
+cache is never written), guard bands around the output and the workspace,
+run-to-run determinism, CUDA-graph capture and replay, length clamping flags,
+the convenience and staged entry points, and errors reported before launch.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import gqa_decode_attention_sm_gb300 as gq
+from gqa_decode_attention_sm_gb300 import api, inputs
+from helpers import HQ, bits_of, tolerance_ok
+
+pytestmark = pytest.mark.gpu
+
+FMT = {"f16": oracle.F16, "bf16": oracle.BF16, "e4m3": oracle.E4M3}
+DEV = torch.device("cuda", 0)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from gqa_decode_attention_sm_gb300 import build as gbuild
+    gbuild.build()
+    oracle.build()
+    torch.cuda.init()
+
+
+def _make(w, **kw):
+    return inputs.make(w, DEV, **kw)
+
+
+def _prepare(t, out=None, num_splits=None, workspace=None):
+    w = t["workload"]
+    out = torch.empty_like(t["q"]) if out is None else out
+    fp8 = w.kv_dtype == "e4m3"
+    return gq.prepare({"Q": t["q"], "KV": t["kv"], "O": out, "sequence_lengths": t["lens"]},
+                      q_scale=t["q_scale"], num_splits=num_splits,
+                      k_scale=t["k_scale"] if fp8 else None, v_scale=t["v_scale"] if fp8 else None,
+                      workspace=workspace)
+
+
+def _run(t, num_splits=None):
+    p = _prepare(t, num_splits=num_splits)
+    gq.launch(p)
+    torch.cuda.synchronize()
+    return p
+
+
+def _oracle_full(t, **kw):
+    w = t["workload"]
+    args = dict(q_scale=t["q_scale"], k_scale=t["k_scale"], v_scale=t["v_scale"])
+    args.update(kw)
+    out, _ = oracle.gqa_decode(bits_of(t["q"]), FMT[w.q_dtype], bits_of(t["kv"]), FMT[w.kv_dtype],
+                               t["lens"].cpu().numpy(), **args)
+    return out
+
+
+def _oracle_units(t, units):
+    """Oracle rows for sampled (b, g) units: copies only those K/V planes to the host."""
+    w = t["workload"]
+    C = w.capacity
+    lens = t["lens"].cpu().numpy()
+    res = {}
+    for b, g in units:
+        qb = bits_of(t["q"][b:b + 1])
+        kvb = np.zeros((1, 2, 8, C, 128), dtype=np.uint8 if w.kv_dtype == "e4m3" else np.uint16)
+        kvb[0, :, g] = bits_of(t["kv"][b, :, g])
+        rows = [4 * g + j for j in range(4)]
+        out, _ = oracle.gqa_decode(qb, FMT[w.q_dtype], kvb, FMT[w.kv_dtype], lens[b:b + 1],
+                                   q_scale=t["q_scale"], k_scale=t["k_scale"],
+                                   v_scale=t["v_scale"], rows=rows)
+        for j, r in enumerate(rows):
+            res[b * HQ + r] = out[j]
+    return res
+
+
+def _gpu_rows(out):
+    return out.float().cpu().numpy().reshape(-1, 128)
+
+
+def _assert_parity(got, ref, what=""):
+    ok, err, excess = tolerance_ok(got, ref)
+    rms = float(np.sqrt(np.mean(ref ** 2))) or 1.0
+    print(f"{what}: max|err| {err:.3e}, max err / rms(ref) {err / rms:.3e}")
+    assert ok, f"{what}: max |gpu - oracle| {err:.3e} exceeds the bar by {excess:.3e}"
+
+
+# ---------------------------------------------------------------- workloads
+
+
+@pytest.mark.parametrize("index", [1, 2, 3])
+def test_workload_every_element(index):
+    t = _make(inputs.WORKLOADS[index])
+    p = _run(t)
+    _assert_parity(_gpu_rows(p.out), _oracle_full(t), f"workload {index} (splits {p.num_splits})")
+
+
+@pytest.mark.parametrize("index", [4, 5])
+def test_full_size_workload_sampled(index):
+    w = inputs.WORKLOADS[index]
+    t = _make(w)
+    p = _run(t)  # the auto plan: the launch configuration the benchmark times
+    rng = np.random.default_rng(index)
+    units = sorted({(int(b), int(g)) for b, g in zip(rng.integers(0, w.batch, 6), rng.integers(0, 8, 6))}
+                   | {(0, 0), (w.batch - 1, 7)})
+    ref = _oracle_units(t, units)
+    got = _gpu_rows(p.out)
+    rows = sorted(ref)
+    _assert_parity(got[rows], np.stack([ref[r] for r in rows]), f"workload {index} sampled")
+    assert np.isfinite(got).all()
+
+
+# ---------------------------------------------------------------- edge cases
+
+
+@pytest.mark.parametrize("kv_dtype", ["f16", "bf16", "e4m3"])
+def test_tile_edges_and_ragged_lengths(kv_dtype):
+    lens = [1, 2, 63, 64, 65, 127, 128, 129, 255, 256, 200, 17]
+    w = inputs.custom(len(lens), 256, 1, kv_dtype=kv_dtype, kv_std=2.0 if kv_dtype == "e4m3" else 1.0,
+                      nan_tail=True)
+    t = _make(w, lens=lens)
+    for S in (None, 1, 3):
+        p = _run(t, num_splits=S)
+        _assert_parity(_gpu_rows(p.out), _oracle_full(t), f"{kv_dtype} edges splits={p.num_splits}")
+
+
+def test_capacity_one():
+    t = _make(inputs.custom(5, 1, 1))
+    p = _run(t)
+    got = _gpu_rows(p.out)
+    _assert_parity(got, _oracle_full(t), "capacity 1")
+    # one slot: the output is V[0] itself, exactly
+    v0 = t["kv"][:, 1, :, 0, :].float().cpu().numpy()  # [B,8,128]
+    assert np.array_equal(got.reshape(5, 32, 128), np.repeat(v0, 4, axis=1))
+
+
+@pytest.mark.parametrize("kv_dtype", ["f16", "e4m3"])
+@pytest.mark.parametrize("S", [1, 2, 3, 7, 16, 64, 256])
+def test_every_split_count(kv_dtype, S):
+    w = inputs.custom(3, 1000, 1, kv_dtype=kv_dtype, kv_std=2.0 if kv_dtype == "e4m3" else 1.0,
+                      nan_tail=True)
+    t = _make(w, lens=[1000, 333, 1])
+    p = _run(t, num_splits=S)
+    _assert_parity(_gpu_rows(p.out), _oracle_full(t), f"{kv_dtype} splits={S}")
+
+
+def test_bf16_every_element_multi_split():
+    t = _make(inputs.custom(2, 4096, 4096, kv_dtype="bf16"))
+    p = _run(t)
+    assert p.num_splits > 1
+    _assert_parity(_gpu_rows(p.out), _oracle_full(t), "bf16 2x4096")
+
+
+def test_q_scale_zero_gives_mean_through_convenience_call():
+    w = inputs.custom(2, 500, 100, 500)
+    t = _make(w)
+    out = gq.gqa_decode(t["q"], t["kv"], t["lens"], q_scale=0.0)
+    torch.cuda.synchronize()
+    _assert_parity(_gpu_rows(out), _oracle_full(t, q_scale=0.0), "q_scale=0")
+
+
+def test_large_q_scale_peaky_softmax():
+    w = inputs.custom(2, 700, 300, 700, q_scale=8.0)
+    t = _make(w)
+    p = _run(t)
+    _assert_parity(_gpu_rows(p.out), _oracle_full(t), "q_scale=8")
+
+
+def test_fp8_distinct_scales():
+    w = inputs.custom(4, 2048, 500, 2048, kv_dtype="e4m3", kv_std=2.0)
+    t = _make(w)
+    t["k_scale"] *= 0.5
+    t["v_scale"] *= 3.0
+    p = _run(t)
+    _assert_parity(_gpu_rows(p.out), _oracle_full(t), "fp8 k_scale != v_scale")
+
+
+def test_fp8_with_f16_query_through_stages():
+    w = inputs.custom(3, 900, 50, 900, kv_dtype="e4m3", q_dtype="f16", kv_std=2.0, nan_tail=True)
+    t = _make(w)
+    p = _prepare(t, num_splits=4)
+    gq.split_stage(p)
+    gq.combine_stage(p)
+    torch.cuda.synchronize()
+    _assert_parity(_gpu_rows(p.out), _oracle_full(t), "e4m3 KV, f16 q")
+
+
+def test_large_batch_small_capacity():
+    t = _make(inputs.custom(4096, 64, 1, 64))
+    p = _run(t)
+    _assert_parity(_gpu_rows(p.out), _oracle_full(t), "B=4096 C=64")
+
+
+def test_max_capacity_sampled():
+    w = inputs.custom(1, 1 << 20, 1 << 20, kv_dtype="bf16")
+    t = _make(w)
+    for S in (None, 256):
+        p = _run(t, num_splits=S)
+        ref = _oracle_units(t, [(0, 0), (0, 5)])
+        rows = sorted(ref)
+        _assert_parity(_gpu_rows(p.out)[rows], np.stack([ref[r] for r in rows]),
+                       f"C=2^20 splits={p.num_splits}")
+
+
+# ------------------------------------------------------ unused slots, safety
+
+
+@pytest.mark.parametrize("kv_dtype", ["f16", "e4m3"])
+def test_output_bit_exact_whatever_the_unused_slots_hold(kv_dtype):
+    w = inputs.custom(6, 640, 1, 600, kv_dtype=kv_dtype, kv_std=2.0 if kv_dtype == "e4m3" else 1.0)
+    t = _make(w)
+    outs = []
+    for fill in (float("nan"), 0.0, 300.0):
+        kv = t["kv"].clone()
+        inputs.fill_tail(kv, t["lens"], kv_dtype, fill)
+        before = kv.clone()
+        t2 = dict(t, kv=kv)
+        for S in (1, 5):
+            p = _run(t2, num_splits=S)
+            outs.append((S, p.out.clone()))
+        assert torch.equal(kv.view(torch.uint8), before.view(torch.uint8)), "the cache was written"
+    for S in (1, 5):
+        same = [o for s, o in outs if s == S]
+        for o in same[1:]:
+            assert torch.equal(o.view(torch.int16), same[0].view(torch.int16))
+
+
+def test_guard_bands_untouched():
+    w = inputs.custom(3, 512, 100, 512)
+    t = _make(w)
+    G = 4096
+    out_buf = torch.full((G + 3 * 32 * 128 + G,), 0x5A5A, dtype=torch.int16, device=DEV)
+    out = out_buf[G:G + 3 * 32 * 128].view(torch.float16).view(3, 32, 128)
+    S = 6
+    nws = gq.workspace_size(3, 512, S)
+    ws_buf = torch.full((G + nws + G,), 0xA5, dtype=torch.uint8, device=DEV)
+    ws = ws_buf[G:G + nws]
+    ws[:256].zero_()
+    p = _prepare(t, out=out, num_splits=S, workspace=ws)
+    gq.launch(p)
+    torch.cuda.synchronize()
+    assert bool((out_buf[:G] == 0x5A5A).all() and (out_buf[-G:] == 0x5A5A).all())
+    assert bool((ws_buf[:G] == 0xA5).all() and (ws_buf[-G:] == 0xA5).all())
+    _assert_parity(_gpu_rows(out), _oracle_full(t), "guarded")
+
+
+def test_deterministic_across_runs():
+    t = _make(inputs.WORKLOADS[3])
+    p = _prepare(t)
+    first = gq.launch(p).clone()
+    for _ in range(3):
+        assert torch.equal(gq.launch(p).view(torch.int16), first.view(torch.int16))
+
+
+def test_graph_capture_replay_matches_eager():
+    w = inputs.custom(4, 4096, 1000, 4096)
+    t = _make(w)
+    p = _prepare(t)
+    eager = gq.launch(p).clone()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        gq.launch(p)  # warm-up on a side stream before capture
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        gq.launch(p)
+    p.out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(p.out.view(torch.int16), eager.view(torch.int16))
+    # update the lengths in place (same address) and replay
+    t["lens"].fill_(777)
+    g.replay()
+    torch.cuda.synchronize()
+    replayed = p.out.clone()
+    assert torch.equal(replayed.view(torch.int16), gq.launch(p).view(torch.int16))
+    _assert_parity(_gpu_rows(replayed), _oracle_full(t), "graph replay, lengths 777")
+
+
+def test_convenience_and_stages_match_prepared_bitwise():
+    t = _make(inputs.WORKLOADS[2])
+    p = _run(t)
+    conv = gq.gqa_decode(t["q"], t["kv"], t["lens"])
+    out2 = torch.empty_like(t["q"])
+    p2 = _prepare(t, out=out2)
+    gq.split_stage(p2)
+    gq.combine_stage(p2)
+    torch.cuda.synchronize()
+    assert torch.equal(conv.view(torch.int16), p.out.view(torch.int16))
+    assert torch.equal(out2.view(torch.int16), p.out.view(torch.int16))
+
+
+@pytest.mark.parametrize("S", [1, 4])
+def test_out_of_range_lengths_are_clamped_and_flagged(S):
+    C = 256
+    w = inputs.custom(3, C, 5)
+    t = _make(w, lens=[0, C + 7, 5])
+    p = _prepare(t, num_splits=S)
+    assert gq.get_status(p) == 0
+    gq.launch(p)
+    flags = gq.get_status(p)
+    assert flags & api.FLAG_LENGTH_CLAMPED and not flags & api.FLAG_WAIT_TIMEOUT
+    assert gq.get_status(p) == 0  # read-and-clear
+    got = p.out.clone()
+    assert torch.all(got[0] == 0)
+    t["lens"].copy_(torch.tensor([1, C, 5], dtype=torch.int32))
+    gq.launch(p)
+    torch.cuda.synchronize()
+    assert torch.equal(got[1:].view(torch.int16), p.out[1:].view(torch.int16))
+    assert gq.get_status(p) == 0
+
+
+def test_in_contract_lengths_raise_no_flags():
+    t = _make(inputs.WORKLOADS[3])
+    p = _run(t)
+    assert gq.get_status(p) == 0
+
+
+def test_errors_are_reported_before_launch():
+    t = _make(inputs.custom(2, 128, 128))
+    p = _prepare(t, num_splits=4)
+    small = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    with pytest.raises(gq.GqaError) as e:
+        api._lib.check(api._lib.load().gqa_decode_prepared(
+            t["q"].data_ptr(), t["kv"].data_ptr(), t["lens"].data_ptr(), p.out.data_ptr(), 2, 128, 0,
+            1.0, 4, small.data_ptr(), 256, None))
+    assert e.value.name == "GQA_ERR_WORKSPACE_TOO_SMALL"
+    with pytest.raises(ValueError):
+        gq.prepare({"Q": t["q"], "KV": t["kv"], "O": t["q"], "sequence_lengths": t["lens"]})
+    with pytest.raises(gq.GqaError) as e:
+        api._lib.check(api._lib.load().gqa_decode_prepared(
+            t["q"].data_ptr(), t["kv"].data_ptr(), t["lens"].data_ptr(), t["q"].data_ptr(), 2, 128, 0,
+            1.0, 1, p.workspace.data_ptr(), p.workspace_bytes, None))
+    assert e.value.name == "GQA_ERR_ALIASING"
