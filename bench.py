@@ -273,10 +273,17 @@ def per_config_table(dev, peak, gq, inputs, quick=False):
         us = time_calls(lambda: gq.launch(p), n, flush=flush)
         row = {"us_per_call": round(us, 2), "GBps": round(nbytes / us / 1e3, 1),
                "frac_of_peak": round(nbytes / us / 1e3 / peak, 4), "alg_bytes": nbytes,
-               "splits": p.num_splits, "l2": "cold"}
-        if w.capacity * w.batch <= 1 << 16 or idx == 2:
-            wus = time_calls(lambda: gq.launch(p), n)
-            row["us_per_call_warm_l2"] = round(wus, 2)
+               "splits": p.num_splits, "l2": "cold (512 MB written before each call)"}
+        if w.batch * w.capacity <= 1 << 12:
+            # warm L2, device time: 20 calls back to back inside one CUDA graph
+            reps = 20
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for _ in range(reps):
+                    gq.launch(p)
+            g.replay()
+            torch.cuda.synchronize()
+            row["us_per_call_warm_l2_graph"] = round(time_calls(g.replay, 10) / reps, 2)
         table[str(idx)] = row
         del t, out, p
         torch.cuda.empty_cache()
@@ -303,6 +310,8 @@ def run_gpu(args):
 
     peak, peak_kind = measured_peak()
     w = inputs.WORKLOADS[args.workload]
+    if args.batch:
+        w = inputs.with_(w, batch=args.batch)
     t = inputs.make(w, dev, seed=w.seed + 7919 * rank)
     lens_list = t["lens"].cpu().tolist()
     fp8 = w.kv_dtype == "e4m3"
@@ -391,7 +400,8 @@ def run_gpu(args):
                    "q_dtype": w.q_dtype, "lengths": f"U[{w.len_lo},{w.len_hi}]" if w.len_lo != w.len_hi
                    else w.len_lo, "num_splits": p.num_splits, "splits_effective": splits_eff,
                    "alg_bytes_per_step_per_gpu": nbytes,
-                   "l2": "inputs (4.3 GB) larger than L2 (129 MB); no flush between steps",
+                   "l2": f"inputs ({nbytes / 1e9:.2f} GB) larger than L2 (129 MB); no flush between steps"
+                   if nbytes > 2 * 129e6 else "inputs smaller than 2x L2: steps run warm",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "us_per_call": round(ms_per_step * 1e3, 2),
                    "frac_of_peak": round(value / world / peak, 4)},
@@ -434,8 +444,10 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=4, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch (smaller cases for profiling)")
     ap.add_argument("--e2e-steps", type=int, default=5)
-    ap.add_argument("--cpu-batch-rows", type=int, default=2,
+    ap.add_argument("--cpu-batch-rows", type=int, default=4,
                     help="batch rows (all 32 query heads each) in the oracle CPU-baseline sample")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
