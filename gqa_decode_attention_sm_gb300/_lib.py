@@ -19,6 +19,7 @@ EXPORTS = (
     "gqa_decode_plan_for", "gqa_decode_split_geometry",
     "gqa_decode", "gqa_decode_prepared", "gqa_decode_fp8kv", "gqa_decode_split_stage",
     "gqa_decode_combine_stage", "gqa_decode_workspace_init", "gqa_decode_get_status",
+    "gqa_decode_noalloc",
 )
 
 
@@ -46,6 +47,7 @@ def _declare(lib):
         "gqa_decode_combine_stage": (i, [p, p, i, i, i, i, f, i, p, sz, p]),
         "gqa_decode_workspace_init": (i, [p, sz, p]),
         "gqa_decode_get_status": (i, [p, sz, p, ctypes.POINTER(ctypes.c_uint32)]),
+        "gqa_decode_noalloc": (i, [p, p, p, p, i, i, i, f, i, p]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

@@ -196,6 +196,31 @@ gqa_status_t validate(const Call& c, bool q_scale_positive, bool need_q) {
   return GQA_OK;
 }
 
+// ------------------------------------------------ static (no-alloc) scratch
+
+// Scratch for gqa_decode_noalloc.  In host code this name is only a stand-in
+// for the device symbol: its device address comes from cudaGetSymbolAddress,
+// once per device, with that device current.
+constexpr size_t kStaticWorkspaceBytes = GQA_STATIC_WORKSPACE_BYTES;
+static __device__ __align__(256) unsigned char g_static_workspace[kStaticWorkspaceBytes];
+
+struct StaticWorkspace {
+  std::once_flag once;
+  cudaError_t err = cudaSuccess;
+  void* ptr = nullptr;
+};
+StaticWorkspace g_static_ws[kMaxDevices];
+
+// Device address of the static scratch on the current device `dev`.
+gqa_status_t static_workspace(int dev, void** ptr) {
+  if (dev < 0 || dev >= kMaxDevices) return fail(GQA_ERR_UNSUPPORTED_DEVICE, "device %d out of range", dev);
+  StaticWorkspace& s = g_static_ws[dev];
+  std::call_once(s.once, [&] { s.err = cudaGetSymbolAddress(&s.ptr, g_static_workspace); });
+  if (s.err != cudaSuccess) return cuda_fail(s.err, "cudaGetSymbolAddress(static workspace)");
+  *ptr = s.ptr;
+  return GQA_OK;
+}
+
 // --------------------------------------------------------------- planning
 
 int plan_splits(int batch, int capacity, int kv_format, int sm_count) {
@@ -487,6 +512,45 @@ gqa_status_t gqa_decode(const void* q, const void* kv, const int32_t* lens, void
   e = cudaFreeAsync(ws, c.stream);
   if (st == GQA_OK && e != cudaSuccess) st = cuda_fail(e, "cudaFreeAsync(workspace)");
   return st;
+}
+
+gqa_status_t gqa_decode_noalloc(const void* q, const void* kv, const int32_t* lens, void* out, int batch,
+                                int capacity, gqa_dtype_t dtype, float q_scale, int num_splits, void* stream) {
+  static const uint4 dummy_ws = {0, 0, 0, 0};
+  Call c{q, (int)dtype, kv, (int)dtype, lens, out, batch, capacity, q_scale, 1.f, 1.f, 1,
+         const_cast<uint4*>(&dummy_ws), (size_t)-1, static_cast<cudaStream_t>(stream)};
+  gqa_status_t st = validate(c, false, true);  // everything but the split count and scratch
+  if (st != GQA_OK) return st;
+  if (num_splits < 0 || num_splits > GQA_MAX_SPLITS)
+    return fail(GQA_ERR_INVALID_ARGUMENT, "num_splits %d outside [0, %d]", num_splits, GQA_MAX_SPLITS);
+  if (num_splits > 0 && workspace_bytes_for(batch, num_splits) > kStaticWorkspaceBytes)
+    return fail(GQA_ERR_WORKSPACE_TOO_SMALL,
+                "batch %d with %d splits needs %zu bytes of scratch; the static scratch holds %zu",
+                batch, num_splits, workspace_bytes_for(batch, num_splits), kStaticWorkspaceBytes);
+  int dev = -1, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  st = device_ready(dev, &sms);
+  if (st != GQA_OK) return st;
+  void* ws = nullptr;
+  st = static_workspace(dev, &ws);
+  if (st != GQA_OK) return st;
+  int S = num_splits;
+  if (S == 0) {
+    S = plan_splits(batch, capacity, (int)dtype, sms);
+    while (S > 1 && workspace_bytes_for(batch, S) > kStaticWorkspaceBytes) --S;
+  }
+  c.num_splits = S;
+  c.workspace = ws;
+  c.workspace_bytes = kStaticWorkspaceBytes;
+  st = validate(c, false, true);
+  if (st != GQA_OK) return st;
+  // the status word accumulates with atomicOr: start every call from zero
+  e = cudaMemsetAsync(ws, 0, GQA_WORKSPACE_HEADER_BYTES, c.stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(static workspace header)");
+  st = run_split(c);
+  if (st != GQA_OK) return st;
+  return run_combine(c);
 }
 
 gqa_status_t gqa_decode_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {

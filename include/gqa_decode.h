@@ -167,6 +167,38 @@ gqa_status_t gqa_decode_combine_stage(const int32_t* lens, void* out, gqa_dtype_
                                       float v_scale, int num_splits, const void* workspace,
                                       size_t workspace_bytes, void* stream);
 
+/* No-allocation variant of gqa_decode, for callers that cannot allocate
+ * device memory at call time: code running inside a memory-budgeted runtime
+ * or a custom allocator that forbids cudaMalloc on the decode path, plugins
+ * handed only pre-existing buffers, or hosts that must not touch the
+ * allocator between steps.  The pages have no counterpart to this call (their
+ * convenience call allocates its workspace and their prepared call takes one
+ * from the caller).
+ *
+ * The split-KV scratch lives in a file-scope static __device__ array of
+ * GQA_STATIC_WORKSPACE_BYTES (16 MiB) that every GPU which loads this library
+ * holds until the process exits.  The caller still passes q, kv, lens and out.
+ * This call performs no cudaMalloc, cudaFree or other allocation; it clears
+ * the scratch header with cudaMemsetAsync and launches the two stages on
+ * `stream`.
+ *
+ * Set-up: the first call on a device (with that device current) looks up the
+ * array's device address with cudaGetSymbolAddress and caches it; make that
+ * first call before any stream capture.  Every call on a device shares the
+ * one array, which keeps the last call's contents: calls that may overlap on
+ * the GPU (different streams or graphs without ordering) race and corrupt
+ * each other's results; order them on one stream.
+ *
+ * num_splits = 0 takes gqa_decode_plan's choice, lowered if needed to the
+ * largest split count whose scratch fits the array.  An explicit num_splits
+ * whose scratch (gqa_decode_workspace_size) exceeds GQA_STATIC_WORKSPACE_BYTES
+ * is rejected with GQA_ERR_WORKSPACE_TOO_SMALL.  q_scale finite and >= 0;
+ * other rules as gqa_decode_prepared. */
+#define GQA_STATIC_WORKSPACE_BYTES (16u << 20)
+gqa_status_t gqa_decode_noalloc(const void* q, const void* kv, const int32_t* lens, void* out,
+                                int batch, int capacity, gqa_dtype_t dtype, float q_scale,
+                                int num_splits, void* stream);
+
 /* Zero the workspace header (status flags) on `stream`.  Asynchronous. */
 gqa_status_t gqa_decode_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
 
