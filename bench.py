@@ -37,7 +37,7 @@ FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "split_kv_traffic.json")
 KERNEL_SOURCES = ["gqa_decode_attention_sm_gb300/csrc/kernels/common.cuh",
-                  "gqa_decode_attention_sm_gb300/csrc/kernels/split_kv.cuh"]
+                  "gqa_decode_attention_sm_gb300/csrc/kernels/split_kv_mma.cuh"]
 
 
 # ------------------------------------------------------------------ helpers
@@ -405,7 +405,7 @@ def run_gpu(args):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "us_per_call": round(ms_per_step * 1e3, 2),
                    "frac_of_peak": round(value / world / peak, 4)},
-        "roofline": {"bound": "hbm", "kernel": "split_kv_kernel", "achieved": round(achieved, 1),
+        "roofline": {"bound": "hbm", "kernel": "split_kv_mma_kernel", "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs (copy, burst)", "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "frac_of_nominal_7900": round(achieved / NOMINAL_HBM_GBS, 4),
                      "traffic": traffic, "kernel_ms": round(split_ms, 4),

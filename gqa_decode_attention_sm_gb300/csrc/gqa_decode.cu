@@ -19,7 +19,7 @@
 #include "gqa_decode.h"
 #include "kernels/combine.cuh"
 #include "kernels/common.cuh"
-#include "kernels/split_kv.cuh"
+#include "kernels/split_kv_mma.cuh"
 
 namespace {
 
@@ -55,8 +55,8 @@ DeviceState g_devices[kMaxDevices];
 
 template <int KVF, int QF>
 cudaError_t set_split_attributes() {
-  return cudaFuncSetAttribute(split_kv_kernel<KVF, QF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kSplitSmemBytes);
+  return cudaFuncSetAttribute(split_kv_mma_kernel<KVF, QF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kMmaSmemBytes);
 }
 
 // One-time per-device check (compute capability 10.3) and opt-in to the
@@ -223,12 +223,14 @@ gqa_status_t static_workspace(int dev, void** ptr) {
 
 // --------------------------------------------------------------- planning
 
+constexpr int kSplitCtasPerSm = 2;  // the split kernel's occupancy (shared memory bound)
+
 int plan_splits(int batch, int capacity, int kv_format, int sm_count) {
-  // Aim for about 8 waves of one-CTA-per-SM work items over the worst case
-  // (every length = capacity), with whole tiles per split.
+  // Aim for about 8 waves of work items (kSplitCtasPerSm resident per SM) over
+  // the worst case (every length = capacity), with whole tiles per split.
   const long long tile = tile_tokens(kv_format);
   const long long units = (long long)batch * kHkv;
-  const long long target_ctas = 8LL * (sm_count > 0 ? sm_count : 148);
+  const long long target_ctas = 8LL * kSplitCtasPerSm * (sm_count > 0 ? sm_count : 148);
   long long per = (units * capacity + target_ctas - 1) / target_ctas;
   per = (per + tile - 1) / tile * tile;
   if (per < tile) per = tile;
@@ -244,10 +246,10 @@ template <int KVF, int QF>
 cudaError_t launch_split_t(const SplitParams& sp, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(sp.splits_eff, kHkv, sp.batch);
-  cfg.blockDim = dim3(kSplitThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSplitSmemBytes;
+  cfg.blockDim = dim3(kMmaThreads, 1, 1);
+  cfg.dynamicSmemBytes = kMmaSmemBytes;
   cfg.stream = stream;
-  return cudaLaunchKernelEx(&cfg, split_kv_kernel<KVF, QF>, sp);
+  return cudaLaunchKernelEx(&cfg, split_kv_mma_kernel<KVF, QF>, sp);
 }
 
 template <int QF>

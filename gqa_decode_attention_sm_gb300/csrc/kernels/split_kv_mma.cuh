@@ -1,0 +1,470 @@
+// Stage 1 of GQA decode with the QK^T and P.V contractions on the tensor cores.
+//
+// One CTA
+// per (split s, KV head g, batch row b) serving the 4 query heads of its KV
+// head, so every K/V byte of the chunk [s*chunk, min((s+1)*chunk, len[b])) is
+// read from HBM exactly once; a producer warp streams 16 KB K and V tiles with
+// 1-D bulk copies (TMA unit) into an mbarrier ring, copying only rows below
+// the length.  The contractions run on the tensor cores because ncu showed an
+// FP32 CUDA-core version of the same kernel to be instruction-bound (about 75
+// warp instructions per token and KV head; on e4m3 KV, short-scoreboard stalls
+// held DRAM throughput near a quarter of peak); this version executes about
+// 21, and the kernel streams at the HBM roofline.
+//
+// Consumers: 4 warps, each owning 16-token slabs of the tile.  Per slab:
+//   scores  S^T[16 tokens x 8] = K[16 x 128] . Q^T[128 x 8] as 8 mma.sync
+//           m16n8k16 (FP32 accumulate).  Tokens are the M dimension and the 4
+//           query heads fill half of N = 8 (columns 4..7 are zero padding).
+//           The dims are permuted consistently in K and Q so each lane reads
+//           whole 16-byte chunks of its K rows straight from the row-major
+//           tile (no swizzle, no transpose).
+//   softmax online, in the log2 domain (ex2), per head; the running max is
+//           shared by the 8 lanes that hold a head (xor shuffles); the
+//           accumulator is rescaled only when a max grows (warp vote).
+//   output  O^T[128 dims x 8] += V^T[128 x 16 tokens] . P^T[16 x 8] as 8 mma
+//           (one per 16-dim m-tile).  Each lane reads 16 contiguous dims of 4
+//           token rows and pairs tokens with byte permutes; P^T reaches the
+//           B-fragment layout through 4 shuffles.  bf16 P is split into a
+//           high and a low bf16 part (two mma) so the weights keep ~16 bits.
+// e4m3 K/V are widened with the hardware cvt (e4m3x2 -> f16x2, exact); the
+// tensor-core type is then f16 and a bf16 q is converted to f16 once per CTA
+// (exact for 2^-17 <= |q| <= 65504; smaller magnitudes round to the f16
+// subnormal grid, larger ones saturate).  fp16 and bf16 KV use their own type.
+//
+// Sources: "FlashInfer sm110_gqa_decode" article ("Convenience API": log2-domain
+// softmax with the host-folded scale q_scale/sqrt(128)/ln 2 and ex2;
+// "num_splits": FP32 split partials merged by a separate step); "FP8 KV cache
+// port on Jetson AGX Thor" blog, section 1 patch 2 (fp8 tile promoted before
+// the dot product, k_scale on scores, v_scale on the output).
+#pragma once
+
+#include "common.cuh"
+
+namespace gqa {
+
+constexpr int kStageBytes = 2 * 16384;  // one K tile + one V tile (16 KB each)
+
+struct SplitParams {
+  const void* q;          // [B,32,128] fp16/bf16
+  const void* kv;         // [B,2,8,C,128] fp16/bf16/e4m3
+  const int32_t* lens;    // [B]
+  void* out;              // [B,32,128], written when the effective split count is 1
+  float* part_o;          // [B,32,S,128] unnormalised accumulator
+  float* part_m;          // [B,32,S]  running max, log2 domain
+  float* part_l;          // [B,32,S]  softmax denominator
+  uint32_t* flags;        // workspace status word
+  int batch, capacity, num_splits, chunk, splits_eff;
+  float scale_log2;       // q_scale * k_scale * log2(e) / sqrt(128)
+  float v_scale;
+};
+
+template <int QF>
+__device__ __forceinline__ uint32_t pack_out(float a, float b) {
+  if constexpr (QF == kQF16) {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  } else {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  }
+}
+
+constexpr int kMmaConsumerWarps = 4;
+constexpr int kMmaThreads = (kMmaConsumerWarps + 1) * 32;
+constexpr int kMmaStages = 3;
+constexpr int kMmaMergeBytes = kMmaConsumerWarps * kGroup * kD * 4 + 2 * kMmaConsumerWarps * kGroup * 4;
+constexpr int kMmaSmemBytes = kMmaStages * kStageBytes + kMmaMergeBytes + 2 * kMmaStages * 8;
+
+// ---------------------------------------------------------------- mma.sync
+
+template <bool BF16>
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  if constexpr (BF16) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// (lo, hi) -> packed pair, round to nearest even.
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t pack_f16_satfinite(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+__device__ __forceinline__ float bf16_lo_to_f32(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi_to_f32(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Tensor-core element type: bf16 for bf16 KV, f16 otherwise (e4m3 widens to f16).
+template <int KVF>
+constexpr bool kMmaBF16 = KVF == kKvBF16;
+
+// ------------------------------------------------------------ dim mapping
+//
+// Lane (gq = lane/4, cq = lane%4).  QK A-fragment registers for k-step ks:
+//   a0 = K[row gq][kp = 2cq, 2cq+1], a2 = K[row gq][kp = 2cq+8, 2cq+9]
+//   (a1, a3: row gq+8).  Logical (ks, kp) maps to physical dims:
+//   2-byte KV: lane cq reads 16-byte chunks cq + 4i (i = 0..3, 8 dims each);
+//              ks = 2i + h covers chunk dims 4h..4h+3 (a0 <- 4h,4h+1; a2 <- 4h+2,4h+3)
+//   e4m3 KV:   lane cq reads 16-byte chunks cq + 4i (i = 0..1, 16 dims each);
+//              ks = 4i + s covers chunk dims 4s..4s+3 (a0 <- 4s,4s+1; a2 <- 4s+2,4s+3)
+// The Q^T B-fragment (b0 = Q[head gq][kp 2cq,2cq+1], b1 = [2cq+8, 2cq+9]) uses
+// the same map, so the dot products are unchanged.
+template <int KVF>
+__device__ __forceinline__ int qk_dim(int cq, int ks, int pair /*0: a0/b0, 1: a2/b1*/) {
+  if constexpr (KVF == kKvE4M3) return 16 * (cq + 4 * (ks >> 2)) + 4 * (ks & 3) + 2 * pair;
+  else return 8 * (cq + 4 * (ks >> 1)) + 4 * (ks & 1) + 2 * pair;
+}
+
+template <int KVF, int QF>
+__global__ void __launch_bounds__(kMmaThreads, 2) split_kv_mma_kernel(const __grid_constant__ SplitParams p) {
+  using T = KvTraits<KVF>;
+  constexpr bool kBF16 = kMmaBF16<KVF>;
+  constexpr int kSlabs = T::kTile / (16 * kMmaConsumerWarps);  // 16-token slabs per warp per tile
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* ring = smem;
+  float* mrg_acc = reinterpret_cast<float*>(smem + kMmaStages * kStageBytes);  // [4 warps][4 heads][128]
+  float* mrg_m = mrg_acc + kMmaConsumerWarps * kGroup * kD;                      // [4][4]
+  float* mrg_l = mrg_m + kMmaConsumerWarps * kGroup;                             // [4][4]
+  uint64_t* full = reinterpret_cast<uint64_t*>(mrg_l + kMmaConsumerWarps * kGroup);
+  uint64_t* empty = full + kMmaStages;
+
+  const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int C = p.capacity;
+  const int len_raw = __ldg(p.lens + b);
+  const int L = min(max(len_raw, 0), C);
+  if (s == 0 && g == 0 && threadIdx.x == 0 && (len_raw < 1 || len_raw > C))
+    atomicOr(p.flags, GQA_FLAG_LENGTH_CLAMPED);
+  const int t_begin = s * p.chunk;
+  const int t_end = min(L, t_begin + p.chunk);
+
+  if (t_begin >= t_end) {
+    if (p.splits_eff == 1 && threadIdx.x < kMmaConsumerWarps * 32) {
+      // one-split launch with length 0: the output rows are zero
+      const int j = threadIdx.x / 32, d0 = 4 * (threadIdx.x % 32);
+      *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) +
+                                ((size_t)(b * kHq + g * kGroup + j) * kD + d0) * 2) = make_uint2(0u, 0u);
+    }
+    return;
+  }
+  const int n_tiles = (t_end - t_begin + T::kTile - 1) / T::kTile;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kMmaStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kMmaConsumerWarps);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const uint64_t deadline = global_timer_ns() + kWaitBudgetNs;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (warp == kMmaConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const size_t plane = (size_t)kHkv * C * T::kRowBytes;
+      const uint8_t* gK = static_cast<const uint8_t*>(p.kv) +
+                          ((size_t)b * 2 * kHkv + g) * (size_t)C * T::kRowBytes;
+      const uint8_t* gV = gK + plane;
+      const uint64_t pol = policy_evict_first();
+      bool ok = true;
+      int issued = 0;
+      for (int i = 0; i < n_tiles; ++i) {
+        const int st = i % kMmaStages;
+        if (i >= kMmaStages && !mbar_wait(&empty[st], ((i / kMmaStages) & 1) ^ 1, deadline)) {
+          ok = false;
+          break;
+        }
+        const int t0 = t_begin + i * T::kTile;
+        const uint32_t bytes = (uint32_t)min(T::kTile, t_end - t0) * T::kRowBytes;
+        mbar_arrive_expect_tx(&full[st], 2 * bytes);
+        bulk_load(ring + st * kStageBytes, gK + (size_t)t0 * T::kRowBytes, bytes, &full[st], pol);
+        bulk_load(ring + st * kStageBytes + T::kTileBytes, gV + (size_t)t0 * T::kRowBytes, bytes, &full[st],
+                  pol);
+        ++issued;
+      }
+      if (!ok) atomicOr(p.flags, GQA_FLAG_WAIT_TIMEOUT);
+      for (int i = max(0, issued - kMmaStages); i < issued; ++i)
+        mbar_wait(&full[i % kMmaStages], (i / kMmaStages) & 1, deadline + kWaitBudgetNs);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int gq = lane >> 2, cq = lane & 3;
+  const bool real_heads = cq < 2;  // score/output columns 2cq, 2cq+1 are query heads 0..3
+
+  // Q^T B-fragments (head gq; zero for the padding heads gq >= 4), unscaled.
+  uint32_t qb[8][2];
+  {
+    const uint16_t* qrow = static_cast<const uint16_t*>(p.q) + ((size_t)b * kHq + g * kGroup + (gq & 3)) * kD;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks)
+#pragma unroll
+      for (int pr = 0; pr < 2; ++pr) {
+        const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(qrow + qk_dim<KVF>(cq, ks, pr)));
+        uint32_t v = w;
+        if constexpr (KVF == kKvE4M3 && QF == kQBF16) v = pack_f16_satfinite(bf16_lo_to_f32(w), bf16_hi_to_f32(w));
+        qb[ks][pr] = gq < kGroup ? v : 0u;
+      }
+  }
+
+  float o[8][4];
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[mt][e] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY;  // running max of heads 2cq, 2cq+1 (log2 domain)
+  float l0 = 0.f, l1 = 0.f;              // this lane's share of the denominators
+  const float sl2 = p.scale_log2;
+  // P^T shuffle sources: tokens 2cq and 2cq+1 of the slab, head pair gq/2
+  const int src0 = 4 * (2 * cq) + (gq >> 1), src1 = 4 * (2 * cq + 1) + (gq >> 1);
+  const uint32_t half_sel = (gq & 1) ? 0x7632u : 0x5410u;
+
+  for (int i = 0; i < n_tiles; ++i) {
+    const int st = i % kMmaStages;
+    if (!mbar_wait(&full[st], (i / kMmaStages) & 1, deadline)) {
+      if (lane == 0) atomicOr(p.flags, GQA_FLAG_WAIT_TIMEOUT);
+      break;
+    }
+    const uint8_t* sK = ring + st * kStageBytes;
+    const uint8_t* sV = sK + T::kTileBytes;
+    const int rows = min(T::kTile, t_end - (t_begin + i * T::kTile));
+
+#pragma unroll
+    for (int sl = 0; sl < kSlabs; ++sl) {
+      const int R = (warp * kSlabs + sl) * 16;  // first tile row of this slab
+      if (R >= rows) break;                     // warp-uniform
+      const bool partial = R + 16 > rows;
+
+      // ---- scores: S^T[16 tokens x 8] = K . Q^T
+      float sc[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        const uint8_t* k0 = sK + (R + gq) * T::kRowBytes;
+        const uint8_t* k1 = k0 + 8 * T::kRowBytes;
+        if constexpr (KVF == kKvE4M3) {
+#pragma unroll
+          for (int ci = 0; ci < 2; ++ci) {
+            const uint4 x = *reinterpret_cast<const uint4*>(k0 + 16 * (cq + 4 * ci));
+            const uint4 y = *reinterpret_cast<const uint4*>(k1 + 16 * (cq + 4 * ci));
+            const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+            for (int s4 = 0; s4 < 4; ++s4) {
+              const int ks = 4 * ci + s4;
+              mma16816<false>(sc, e4m3x2_to_f16x2((uint16_t)(xs[s4] & 0xffffu)),
+                              e4m3x2_to_f16x2((uint16_t)(ys[s4] & 0xffffu)),
+                              e4m3x2_to_f16x2((uint16_t)(xs[s4] >> 16)), e4m3x2_to_f16x2((uint16_t)(ys[s4] >> 16)),
+                              qb[ks][0], qb[ks][1]);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int ci = 0; ci < 4; ++ci) {
+            const uint4 x = *reinterpret_cast<const uint4*>(k0 + 16 * (cq + 4 * ci));
+            const uint4 y = *reinterpret_cast<const uint4*>(k1 + 16 * (cq + 4 * ci));
+            mma16816<kBF16>(sc, x.x, y.x, x.y, y.y, qb[2 * ci][0], qb[2 * ci][1]);
+            mma16816<kBF16>(sc, x.z, y.z, x.w, y.w, qb[2 * ci + 1][0], qb[2 * ci + 1][1]);
+          }
+        }
+      }
+      // sc: [0] token R+gq head 2cq, [1] token R+gq head 2cq+1, [2]/[3] token R+gq+8
+      float x0 = sc[0] * sl2, x1 = sc[1] * sl2, x2 = sc[2] * sl2, x3 = sc[3] * sl2;
+      if (!real_heads || R + gq >= rows) x0 = x1 = -INFINITY;      // select, never multiply
+      if (!real_heads || R + gq + 8 >= rows) x2 = x3 = -INFINITY;
+
+      // ---- online softmax per head (max over the slab's 16 tokens)
+      float h0 = fmaxf(x0, x2), h1 = fmaxf(x1, x3);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        h0 = fmaxf(h0, __shfl_xor_sync(0xffffffffu, h0, off));
+        h1 = fmaxf(h1, __shfl_xor_sync(0xffffffffu, h1, off));
+      }
+      const float n0 = fmaxf(m0, h0), n1 = fmaxf(m1, h1);
+      if (__any_sync(0xffffffffu, n0 > m0 || n1 > m1)) {
+        // 0 when the old max was -inf; 1 when unchanged (also covers -inf == -inf)
+        const float a0 = n0 == m0 ? 1.f : ex2(m0 - n0), a1 = n1 == m1 ? 1.f : ex2(m1 - n1);
+        l0 *= a0;
+        l1 *= a1;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          o[mt][0] *= a0;
+          o[mt][2] *= a0;
+          o[mt][1] *= a1;
+          o[mt][3] *= a1;
+        }
+        m0 = n0;
+        m1 = n1;
+      }
+      const float p0 = x0 == -INFINITY ? 0.f : ex2(x0 - m0);
+      const float p1 = x1 == -INFINITY ? 0.f : ex2(x1 - m1);
+      const float p2 = x2 == -INFINITY ? 0.f : ex2(x2 - m0);
+      const float p3 = x3 == -INFINITY ? 0.f : ex2(x3 - m1);
+
+      // ---- P^T B-fragments: lane (gq, cq) needs head gq of tokens 2cq, 2cq+1 (b0)
+      // and 2cq+8, 2cq+9 (b1); they sit in lanes src0/src1 as (head pair) packs.
+      uint32_t bh0, bh1, bl0 = 0u, bl1 = 0u;
+      if constexpr (kBF16) {
+        const uint32_t ph_a = pack_bf16(p0, p1), ph_b = pack_bf16(p2, p3);
+        const uint32_t pl_a = pack_bf16(p0 - bf16_lo_to_f32(ph_a), p1 - bf16_hi_to_f32(ph_a));
+        const uint32_t pl_b = pack_bf16(p2 - bf16_lo_to_f32(ph_b), p3 - bf16_hi_to_f32(ph_b));
+        l0 += bf16_lo_to_f32(ph_a) + bf16_lo_to_f32(pl_a) + bf16_lo_to_f32(ph_b) + bf16_lo_to_f32(pl_b);
+        l1 += bf16_hi_to_f32(ph_a) + bf16_hi_to_f32(pl_a) + bf16_hi_to_f32(ph_b) + bf16_hi_to_f32(pl_b);
+        bh0 = prmt(__shfl_sync(0xffffffffu, ph_a, src0), __shfl_sync(0xffffffffu, ph_a, src1), half_sel);
+        bh1 = prmt(__shfl_sync(0xffffffffu, ph_b, src0), __shfl_sync(0xffffffffu, ph_b, src1), half_sel);
+        bl0 = prmt(__shfl_sync(0xffffffffu, pl_a, src0), __shfl_sync(0xffffffffu, pl_a, src1), half_sel);
+        bl1 = prmt(__shfl_sync(0xffffffffu, pl_b, src0), __shfl_sync(0xffffffffu, pl_b, src1), half_sel);
+      } else {
+        const uint32_t pa = pack_f16(p0, p1), pb = pack_f16(p2, p3);
+        // the denominator sums the same rounded weights the tensor core multiplies
+        const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&pa));
+        const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&pb));
+        l0 += fa.x + fb.x;
+        l1 += fa.y + fb.y;
+        bh0 = prmt(__shfl_sync(0xffffffffu, pa, src0), __shfl_sync(0xffffffffu, pa, src1), half_sel);
+        bh1 = prmt(__shfl_sync(0xffffffffu, pb, src0), __shfl_sync(0xffffffffu, pb, src1), half_sel);
+      }
+
+      // ---- O^T[128 dims x 8] += V^T . P^T: lane (gq, cq) reads dims
+      // 16gq..16gq+15 of tokens R+2cq, R+2cq+1, R+2cq+8, R+2cq+9.
+      const int r0 = R + 2 * cq;
+      const uint8_t* v0 = sV + r0 * T::kRowBytes;
+      const bool ok0 = !partial || r0 < rows, ok1 = !partial || r0 + 1 < rows;
+      const bool ok2 = !partial || r0 + 8 < rows, ok3 = !partial || r0 + 9 < rows;
+      if constexpr (KVF == kKvE4M3) {
+        uint4 w0 = *reinterpret_cast<const uint4*>(v0 + 16 * gq);
+        uint4 w1 = *reinterpret_cast<const uint4*>(v0 + T::kRowBytes + 16 * gq);
+        uint4 w2 = *reinterpret_cast<const uint4*>(v0 + 8 * T::kRowBytes + 16 * gq);
+        uint4 w3 = *reinterpret_cast<const uint4*>(v0 + 9 * T::kRowBytes + 16 * gq);
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+        if (!ok0) w0 = z;
+        if (!ok1) w1 = z;
+        if (!ok2) w2 = z;
+        if (!ok3) w3 = z;
+        const uint32_t a[4] = {w0.x, w0.y, w0.z, w0.w}, bq[4] = {w1.x, w1.y, w1.z, w1.w};
+        const uint32_t c[4] = {w2.x, w2.y, w2.z, w2.w}, d[4] = {w3.x, w3.y, w3.z, w3.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {  // word j: dims 16gq+4j .. +3 -> m-tiles 2j, 2j+1
+          const uint32_t lo01 = prmt(a[j], bq[j], 0x5140u), lo23 = prmt(a[j], bq[j], 0x7362u);
+          const uint32_t hi01 = prmt(c[j], d[j], 0x5140u), hi23 = prmt(c[j], d[j], 0x7362u);
+          mma16816<false>(o[2 * j], e4m3x2_to_f16x2((uint16_t)(lo01 & 0xffffu)),
+                          e4m3x2_to_f16x2((uint16_t)(lo01 >> 16)), e4m3x2_to_f16x2((uint16_t)(hi01 & 0xffffu)),
+                          e4m3x2_to_f16x2((uint16_t)(hi01 >> 16)), bh0, bh1);
+          mma16816<false>(o[2 * j + 1], e4m3x2_to_f16x2((uint16_t)(lo23 & 0xffffu)),
+                          e4m3x2_to_f16x2((uint16_t)(lo23 >> 16)), e4m3x2_to_f16x2((uint16_t)(hi23 & 0xffffu)),
+                          e4m3x2_to_f16x2((uint16_t)(hi23 >> 16)), bh0, bh1);
+        }
+      } else {
+        const uint8_t* v1 = v0 + T::kRowBytes;
+        const uint8_t* v2 = v0 + 8 * T::kRowBytes;
+        const uint8_t* v3 = v0 + 9 * T::kRowBytes;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {  // dims 16gq + 8half .. +7 -> m-tiles 4half..4half+3
+          uint4 w0 = *reinterpret_cast<const uint4*>(v0 + 32 * gq + 16 * half);
+          uint4 w1 = *reinterpret_cast<const uint4*>(v1 + 32 * gq + 16 * half);
+          uint4 w2 = *reinterpret_cast<const uint4*>(v2 + 32 * gq + 16 * half);
+          uint4 w3 = *reinterpret_cast<const uint4*>(v3 + 32 * gq + 16 * half);
+          const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+          if (!ok0) w0 = z;
+          if (!ok1) w1 = z;
+          if (!ok2) w2 = z;
+          if (!ok3) w3 = z;
+          const uint32_t a[4] = {w0.x, w0.y, w0.z, w0.w}, bq[4] = {w1.x, w1.y, w1.z, w1.w};
+          const uint32_t c[4] = {w2.x, w2.y, w2.z, w2.w}, d[4] = {w3.x, w3.y, w3.z, w3.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {  // word j: dims 16gq + 8half + 2j, +1 -> m-tile 4half + j
+            const uint32_t A0 = prmt(a[j], bq[j], 0x5410u), A1 = prmt(a[j], bq[j], 0x7632u);
+            const uint32_t A2 = prmt(c[j], d[j], 0x5410u), A3 = prmt(c[j], d[j], 0x7632u);
+            mma16816<kBF16>(o[4 * half + j], A0, A1, A2, A3, bh0, bh1);
+            if constexpr (kBF16) mma16816<kBF16>(o[4 * half + j], A0, A1, A2, A3, bl0, bl1);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[st]);
+  }
+
+  // ---- per-warp denominators: sum over the 8 lanes holding each head
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+  }
+  // O^T fragment: o[mt][0] = O[dim 16gq+2mt][head 2cq], [1] = [..][2cq+1],
+  //               o[mt][2] = O[dim 16gq+2mt+1][2cq],  [3] = [..+1][2cq+1]
+  if (real_heads) {
+    float* ha = mrg_acc + (warp * kGroup + 2 * cq) * kD + 16 * gq;
+    float* hb = ha + kD;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      *reinterpret_cast<float2*>(ha + 2 * mt) = make_float2(o[mt][0], o[mt][2]);
+      *reinterpret_cast<float2*>(hb + 2 * mt) = make_float2(o[mt][1], o[mt][3]);
+    }
+    if (gq == 0) {
+      mrg_m[warp * kGroup + 2 * cq] = m0;
+      mrg_m[warp * kGroup + 2 * cq + 1] = m1;
+      mrg_l[warp * kGroup + 2 * cq] = l0;
+      mrg_l[warp * kGroup + 2 * cq + 1] = l1;
+    }
+  }
+  named_barrier_sync(1, kMmaConsumerWarps * 32);
+
+  // ---- merge the 4 warps: thread -> (head j, dims d0..d0+3)
+  const int ctid = threadIdx.x;
+  const int j = ctid >> 5, d0 = 4 * (ctid & 31);
+  float M = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < kMmaConsumerWarps; ++w) M = fmaxf(M, mrg_m[w * kGroup + j]);
+  float Ls = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int w = 0; w < kMmaConsumerWarps; ++w) {
+    const float mw = mrg_m[w * kGroup + j];
+    const float a = mw == -INFINITY ? 0.f : ex2(mw - M);
+    Ls = fmaf(mrg_l[w * kGroup + j], a, Ls);
+    const float4 v = *reinterpret_cast<const float4*>(&mrg_acc[(w * kGroup + j) * kD + d0]);
+    acc.x = fmaf(v.x, a, acc.x);
+    acc.y = fmaf(v.y, a, acc.y);
+    acc.z = fmaf(v.z, a, acc.z);
+    acc.w = fmaf(v.w, a, acc.w);
+  }
+  const int h = g * kGroup + j;
+  if (p.splits_eff == 1) {
+    const float inv = p.v_scale / Ls;
+    *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) + ((size_t)(b * kHq + h) * kD + d0) * 2) =
+        make_uint2(pack_out<QF>(acc.x * inv, acc.y * inv), pack_out<QF>(acc.z * inv, acc.w * inv));
+  } else {
+    const size_t idx = (size_t)(b * kHq + h) * p.num_splits + s;
+    *reinterpret_cast<float4*>(p.part_o + idx * kD + d0) = acc;
+    if (d0 == 0) {
+      p.part_m[idx] = M;
+      p.part_l[idx] = Ls;
+    }
+  }
+}
+
+}  // namespace gqa
