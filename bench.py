@@ -74,9 +74,17 @@ def traffic_per_launch(workload_index: int):
     return d.get("dram_bytes_per_launch")
 
 
+def bytes_per_token(kv_dtype: str) -> int:
+    """KV bytes per (token, batch row), all 8 KV heads, K and V."""
+    if kv_dtype == "e4m3":
+        return 2048
+    if kv_dtype == "i8":  # int8 codes plus one bf16 scale per (plane, KV head) row
+        return 2048 + 2 * 8 * 2
+    return 4096
+
+
 def algorithmic_bytes(w, lens_list) -> int:
-    per_token = 2048 if w.kv_dtype == "e4m3" else 4096
-    return sum(lens_list) * per_token + 2 * w.batch * 32 * 128 * 2 + 4 * w.batch
+    return sum(lens_list) * bytes_per_token(w.kv_dtype) + 2 * w.batch * 32 * 128 * 2 + 4 * w.batch
 
 
 class ClockSampler:
@@ -258,12 +266,17 @@ def per_config_table(dev, peak, gq, inputs, quick=False):
         flush_buf.fill_(1)
 
     table = {}
-    for idx, w in inputs.WORKLOADS.items():
+    cases = dict(inputs.WORKLOADS)
+    # beyond the five workloads: an int8 cache (one bf16 scale per row) with workload 5's shape
+    cases["5-int8"] = inputs.custom(64, 32768, 16384, 32768, kv_dtype="i8", index=5)
+    for idx, w in cases.items():
         t = inputs.make(w, dev)
         out = torch.empty_like(t["q"])
         fp8 = w.kv_dtype == "e4m3"
-        p = gq.prepare({"Q": t["q"], "KV": t["kv"], "O": out, "sequence_lengths": t["lens"]},
-                       q_scale=t["q_scale"], k_scale=t["k_scale"] if fp8 else None,
+        tensors = {"Q": t["q"], "KV": t["kv"], "O": out, "sequence_lengths": t["lens"]}
+        if t["kv_scales"] is not None:
+            tensors["KV_SCALES"] = t["kv_scales"]
+        p = gq.prepare(tensors, q_scale=t["q_scale"], k_scale=t["k_scale"] if fp8 else None,
                        v_scale=t["v_scale"] if fp8 else None)
         nbytes = algorithmic_bytes(w, t["lens"].cpu().tolist())
         for _ in range(3):
@@ -274,6 +287,8 @@ def per_config_table(dev, peak, gq, inputs, quick=False):
         row = {"us_per_call": round(us, 2), "GBps": round(nbytes / us / 1e3, 1),
                "frac_of_peak": round(nbytes / us / 1e3 / peak, 4), "alg_bytes": nbytes,
                "splits": p.num_splits, "l2": "cold (512 MB written before each call)"}
+        if w.kv_dtype == "i8":
+            row["note"] = "int8 codes + bf16 row scales, workload 5 shape (not one of the five workloads)"
         if w.batch * w.capacity <= 1 << 12:
             # warm L2, device time: 20 calls back to back inside one CUDA graph
             reps = 20
@@ -287,6 +302,28 @@ def per_config_table(dev, peak, gq, inputs, quick=False):
         table[str(idx)] = row
         del t, out, p
         torch.cuda.empty_cache()
+    # a paged cache: workload 4 scattered over a shuffled pool of 256-token pages
+    w = inputs.WORKLOADS[4]
+    t = inputs.make(w, dev)
+    pt = inputs.paginate(t, 256, extra_pages=8)
+    del t["kv"]
+    out = torch.empty_like(pt["q"])
+    S = gq.plan(w.batch, w.capacity, 1, dev)
+    ws = torch.zeros(gq.workspace_size(w.batch, w.capacity, S), dtype=torch.uint8, device=dev)
+
+    def paged():
+        gq.gqa_decode_paged(pt["q"], pt["kv_pages"], pt["block_table"], pt["lens"], out=out, num_splits=S,
+                            workspace=ws)
+
+    for _ in range(3):
+        paged()
+    torch.cuda.synchronize()
+    nbytes = algorithmic_bytes(w, pt["lens"].cpu().tolist())
+    us = time_calls(paged, 5 if quick else 20, flush=flush)
+    table["4-paged"] = {"us_per_call": round(us, 2), "GBps": round(nbytes / us / 1e3, 1),
+                        "frac_of_peak": round(nbytes / us / 1e3 / peak, 4), "alg_bytes": nbytes, "splits": S,
+                        "l2": "cold (512 MB written before each call)",
+                        "note": "workload 4 in a shuffled pool of 256-token pages (block table)"}
     return table
 
 

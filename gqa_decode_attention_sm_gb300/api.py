@@ -22,16 +22,19 @@ from ._lib import GqaError
 
 HQ, HKV, D = 32, 8, 128
 F16, BF16 = 0, 1
-KV_F16, KV_BF16, KV_E4M3 = 0, 1, 2
+KV_F16, KV_BF16, KV_E4M3, KV_I8 = 0, 1, 2, 3
 MAX_SPLITS = 256
 FLAG_LENGTH_CLAMPED = 0x1
 FLAG_WAIT_TIMEOUT = 0x2
+FLAG_PAGE_CLAMPED = 0x4
 
 _QDT = {torch.float16: F16, torch.bfloat16: BF16}
 _KVF = {torch.float16: KV_F16, torch.bfloat16: KV_BF16, torch.uint8: KV_E4M3,
-        torch.float8_e4m3fn: KV_E4M3}
+        torch.float8_e4m3fn: KV_E4M3, torch.int8: KV_I8}
 
-__all__ = ["GqaError", "gqa_decode", "gqa_decode_fp8kv", "prepare", "launch", "Prepared",
+__all__ = ["GqaError", "gqa_decode", "gqa_decode_fp8kv", "gqa_decode_int8kv", "gqa_decode_paged",
+           "prepare", "launch",
+           "Prepared",
            "workspace_size", "plan", "get_status", "split_stage", "combine_stage", "split_geometry"]
 
 
@@ -126,6 +129,7 @@ class Prepared:
     k_scale: float
     v_scale: float
     num_splits: int
+    kv_scales: torch.Tensor | None = None  # int8 cache: bf16 [B,2,8,C]
 
     @property
     def workspace_bytes(self) -> int:
@@ -146,17 +150,21 @@ def prepare(tensors: dict, q_scale: float = 1.0, num_splits=None, k_scale=None, 
             workspace: torch.Tensor | None = None) -> Prepared:
     """Validate once and allocate the split workspace once (outside any capture).
 
-    ``tensors`` holds "Q", "KV", "O", "sequence_lengths".  An e4m3 cache
-    (uint8 or float8_e4m3fn storage) needs k_scale and v_scale.
+    ``tensors`` holds "Q", "KV", "O", "sequence_lengths", and "KV_SCALES" for an
+    int8 cache.  An e4m3 cache (uint8 or float8_e4m3fn storage) needs k_scale
+    and v_scale.
     """
     q, kv, out, lens = tensors["Q"], tensors["KV"], tensors["O"], tensors["sequence_lengths"]
     B, C = _geometry(q, kv, lens)
+    kv_scales = tensors.get("KV_SCALES")
+    if kv.dtype == torch.int8:
+        _require(kv_scales, "KV_SCALES", (B, 2, HKV, C), (torch.bfloat16,), q.device)
     _require(out, "O", q.shape, (q.dtype,), q.device)
-    for name, t in (("Q", q), ("KV", kv), ("sequence_lengths", lens)):
-        if _storage_overlaps(out, t):
+    for name, t in (("Q", q), ("KV", kv), ("sequence_lengths", lens), ("KV_SCALES", kv_scales)):
+        if t is not None and _storage_overlaps(out, t):
             raise ValueError(f"O must not share storage with {name}")
     kvf = _KVF[kv.dtype]
-    if kvf != KV_E4M3 and kv.dtype != q.dtype:
+    if kvf not in (KV_E4M3, KV_I8) and kv.dtype != q.dtype:
         raise ValueError("fp16/bf16 KV must have the dtype of Q")
     if kvf == KV_E4M3:
         if k_scale is None or v_scale is None:
@@ -175,7 +183,7 @@ def prepare(tensors: dict, q_scale: float = 1.0, num_splits=None, k_scale=None, 
         if workspace.numel() < nbytes:
             raise ValueError(f"workspace has {workspace.numel()} bytes, needs {nbytes}")
     return Prepared(q, kv, out, lens, workspace, B, C, _QDT[q.dtype], kvf, float(q_scale),
-                    float(k_scale), float(v_scale), S)
+                    float(k_scale), float(v_scale), S, kv_scales if kvf == KV_I8 else None)
 
 
 def launch(p: Prepared) -> torch.Tensor:
@@ -183,7 +191,11 @@ def launch(p: Prepared) -> torch.Tensor:
     lib = _lib.load()
     with torch.cuda.device(p.q.device):
         st = _stream(p.q.device)
-        if p.kv_format == KV_E4M3 and p.q_dtype == BF16:
+        if p.kv_format == KV_I8:
+            _lib.check(lib.gqa_decode_int8kv(_ptr(p.q), _ptr(p.kv), _ptr(p.kv_scales), _ptr(p.lens),
+                                             _ptr(p.out), p.batch, p.capacity, p.q_dtype, p.q_scale,
+                                             p.num_splits, _ptr(p.workspace), p.workspace_bytes, st))
+        elif p.kv_format == KV_E4M3 and p.q_dtype == BF16:
             _lib.check(lib.gqa_decode_fp8kv(_ptr(p.q), _ptr(p.kv), _ptr(p.lens), _ptr(p.out), p.batch,
                                             p.capacity, p.q_scale, p.k_scale, p.v_scale, p.num_splits,
                                             _ptr(p.workspace), p.workspace_bytes, st))
@@ -198,7 +210,8 @@ def launch(p: Prepared) -> torch.Tensor:
 
 
 def split_stage(p: Prepared) -> None:
-    """Stage 1 alone (streams K/V, writes partials or, with one split, out)."""
+    """Stage 1 alone (streams K/V, writes partials or, with one split, out).
+    Not for an int8 cache (its scales go through gqa_decode_int8kv)."""
     with torch.cuda.device(p.q.device):
         _lib.check(_lib.load().gqa_decode_split_stage(
             _ptr(p.q), p.q_dtype, _ptr(p.kv), p.kv_format, _ptr(p.lens), _ptr(p.out), p.batch,
@@ -230,6 +243,61 @@ def gqa_decode_fp8kv(q, kv, sequence_lengths, k_scale: float, v_scale: float, q_
     with torch.cuda.device(q.device):
         _lib.check(_lib.load().gqa_decode_fp8kv(
             _ptr(q), _ptr(kv), _ptr(sequence_lengths), _ptr(out), B, C, float(q_scale), float(k_scale),
+            float(v_scale), S, _ptr(workspace), workspace.numel(), _stream(q.device)))
+    return out
+
+
+def gqa_decode_int8kv(q, kv, kv_scales, sequence_lengths, q_scale: float = 1.0, out=None,
+                      num_splits=None, workspace=None):
+    """int8 cache with one bf16 scale per (plane, KV head, slot) row; fp16/bf16 q and out."""
+    B, C = _geometry(q, kv, sequence_lengths)
+    if kv.dtype != torch.int8:
+        raise ValueError("gqa_decode_int8kv takes an int8 KV cache")
+    _require(kv_scales, "kv_scales", (B, 2, HKV, C), (torch.bfloat16,), q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    _require(out, "out", q.shape, (q.dtype,), q.device)
+    S = plan(B, C, KV_I8, q.device) if not num_splits else int(num_splits)
+    nbytes = workspace_size(B, C, S)
+    if workspace is None:
+        workspace = torch.zeros(nbytes, dtype=torch.uint8, device=q.device)
+    with torch.cuda.device(q.device):
+        _lib.check(_lib.load().gqa_decode_int8kv(
+            _ptr(q), _ptr(kv), _ptr(kv_scales), _ptr(sequence_lengths), _ptr(out), B, C, _QDT[q.dtype],
+            float(q_scale), S, _ptr(workspace), workspace.numel(), _stream(q.device)))
+    return out
+
+
+def gqa_decode_paged(q, kv_pages, block_table, sequence_lengths, q_scale: float = 1.0,
+                     k_scale: float = 1.0, v_scale: float = 1.0, out=None, num_splits=None,
+                     workspace=None):
+    """Paged cache: kv_pages [num_pages, 2, 8, page_size, 128] (fp16/bf16, or e4m3 as
+    uint8/float8_e4m3fn), block_table int32 [batch, max_pages]; returns out."""
+    _require(q, "q", None, (torch.float16, torch.bfloat16))
+    B = q.shape[0]
+    if q.dim() != 3 or q.shape[1:] != (HQ, D):
+        raise ValueError(f"q must be [batch, {HQ}, {D}]")
+    if kv_pages.dim() != 5 or kv_pages.shape[1:3] != (2, HKV) or kv_pages.shape[4] != D:
+        raise ValueError("kv_pages must be [num_pages, 2, 8, page_size, 128]")
+    _require(kv_pages, "kv_pages", None, tuple(_KVF), q.device)
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("block_table must be [batch, max_pages]")
+    _require(block_table, "block_table", None, (torch.int32,), q.device)
+    _require(sequence_lengths, "sequence_lengths", (B,), (torch.int32,), q.device)
+    kvf = _KVF[kv_pages.dtype]
+    num_pages, page_size, max_pages = kv_pages.shape[0], kv_pages.shape[3], block_table.shape[1]
+    C = max_pages * page_size
+    if out is None:
+        out = torch.empty_like(q)
+    _require(out, "out", q.shape, (q.dtype,), q.device)
+    S = plan(B, C, kvf, q.device) if not num_splits else int(num_splits)
+    nbytes = workspace_size(B, C, S)
+    if workspace is None:
+        workspace = torch.zeros(nbytes, dtype=torch.uint8, device=q.device)
+    with torch.cuda.device(q.device):
+        _lib.check(_lib.load().gqa_decode_paged(
+            _ptr(q), _QDT[q.dtype], _ptr(kv_pages), kvf, _ptr(block_table), max_pages, num_pages,
+            page_size, _ptr(sequence_lengths), _ptr(out), B, float(q_scale), float(k_scale),
             float(v_scale), S, _ptr(workspace), workspace.numel(), _stream(q.device)))
     return out
 

@@ -86,6 +86,8 @@ void init_device(int dev, DeviceState& st) {
   if (a == cudaSuccess) a = set_split_attributes<kKvBF16, kQBF16>();
   if (a == cudaSuccess) a = set_split_attributes<kKvE4M3, kQBF16>();
   if (a == cudaSuccess) a = set_split_attributes<kKvE4M3, kQF16>();
+  if (a == cudaSuccess) a = set_split_attributes<kKvI8, kQBF16>();
+  if (a == cudaSuccess) a = set_split_attributes<kKvI8, kQF16>();
   if (prev >= 0 && prev != dev) cudaSetDevice(prev);
   if (a != cudaSuccess) {
     st.status = GQA_ERR_CUDA;
@@ -123,7 +125,7 @@ bool overlap(const void* a, size_t na, const void* b, size_t nb) {
   return x < y + nb && y < x + na;
 }
 
-size_t kv_elem_bytes(int fmt) { return fmt == kKvE4M3 ? 1 : 2; }
+size_t kv_elem_bytes(int fmt) { return is_8bit(fmt) ? 1 : 2; }
 
 size_t partial_o_bytes(int batch, int splits) {
   return align_up((size_t)batch * kHq * splits * kD * sizeof(float), 256);
@@ -150,6 +152,11 @@ struct Call {
   void* workspace;
   size_t workspace_bytes;
   cudaStream_t stream;
+  uint64_t wait_budget_ns = kWaitBudgetNs;
+  int skip_tile = -1;
+  const uint16_t* kv_scales = nullptr;  // int8 cache only
+  const int32_t* block_table = nullptr;  // paged cache only
+  int page_log2 = 0, max_pages = 0, num_pages = 0;
 };
 
 gqa_status_t validate_shape(int batch, int capacity) {
@@ -168,10 +175,13 @@ gqa_status_t validate(const Call& c, bool q_scale_positive, bool need_q) {
   if (st != GQA_OK) return st;
   if (c.q_dtype != GQA_F16 && c.q_dtype != GQA_BF16)
     return fail(GQA_ERR_INVALID_ARGUMENT, "unknown q/out dtype %d", c.q_dtype);
-  if (c.kv_format != kKvF16 && c.kv_format != kKvBF16 && c.kv_format != kKvE4M3)
+  if (c.kv_format != kKvF16 && c.kv_format != kKvBF16 && c.kv_format != kKvE4M3 && c.kv_format != kKvI8)
     return fail(GQA_ERR_INVALID_ARGUMENT, "unknown KV format %d", c.kv_format);
-  if (c.kv_format != kKvE4M3 && c.kv_format != c.q_dtype)
+  if (!is_8bit(c.kv_format) && c.kv_format != c.q_dtype)
     return fail(GQA_ERR_INVALID_ARGUMENT, "fp16/bf16 KV must have the dtype of q");
+  if (c.kv_format == kKvI8 && (!c.kv_scales || !aligned(c.kv_scales, 16) || c.capacity % 8 != 0))
+    return fail(GQA_ERR_INVALID_ARGUMENT,
+                "an int8 cache needs a 16-byte aligned bf16 scale array and a capacity that is a multiple of 8");
   if (!std::isfinite(c.q_scale) || c.q_scale < 0.f || (q_scale_positive && c.q_scale == 0.f))
     return fail(GQA_ERR_INVALID_ARGUMENT, "q_scale must be finite and %s 0", q_scale_positive ? ">" : ">=");
   if (!std::isfinite(c.k_scale) || c.k_scale <= 0.f || !std::isfinite(c.v_scale) || c.v_scale <= 0.f)
@@ -185,7 +195,9 @@ gqa_status_t validate(const Call& c, bool q_scale_positive, bool need_q) {
   if (c.workspace_bytes < need)
     return fail(GQA_ERR_WORKSPACE_TOO_SMALL, "workspace has %zu bytes, needs %zu", c.workspace_bytes, need);
   const size_t qo_bytes = (size_t)c.batch * kHq * kD * 2;
-  const size_t kv_bytes = (size_t)c.batch * 2 * kHkv * (size_t)c.capacity * kD * kv_elem_bytes(c.kv_format);
+  const size_t kv_bytes =
+      c.block_table ? (size_t)c.num_pages * 2 * kHkv * ((size_t)1 << c.page_log2) * kD * kv_elem_bytes(c.kv_format)
+                    : (size_t)c.batch * 2 * kHkv * (size_t)c.capacity * kD * kv_elem_bytes(c.kv_format);
   const size_t lens_bytes = (size_t)c.batch * 4;
   if ((need_q && overlap(c.out, qo_bytes, c.q, qo_bytes)) || overlap(c.out, qo_bytes, c.kv, kv_bytes) ||
       overlap(c.out, qo_bytes, c.lens, lens_bytes) || overlap(c.out, qo_bytes, c.workspace, need))
@@ -193,6 +205,16 @@ gqa_status_t validate(const Call& c, bool q_scale_positive, bool need_q) {
   if ((need_q && overlap(c.workspace, need, c.q, qo_bytes)) || overlap(c.workspace, need, c.kv, kv_bytes) ||
       overlap(c.workspace, need, c.lens, lens_bytes))
     return fail(GQA_ERR_ALIASING, "workspace overlaps q, kv or lens");
+  if (c.block_table) {
+    const size_t bt_bytes = (size_t)c.batch * c.max_pages * 4;
+    if (overlap(c.out, qo_bytes, c.block_table, bt_bytes) || overlap(c.workspace, need, c.block_table, bt_bytes))
+      return fail(GQA_ERR_ALIASING, "out or the workspace overlaps the block table");
+  }
+  if (c.kv_format == kKvI8) {
+    const size_t sc_bytes = (size_t)c.batch * 2 * kHkv * (size_t)c.capacity * 2;
+    if (overlap(c.out, qo_bytes, c.kv_scales, sc_bytes) || overlap(c.workspace, need, c.kv_scales, sc_bytes))
+      return fail(GQA_ERR_ALIASING, "out or the workspace overlaps the int8 scales");
+  }
   return GQA_OK;
 }
 
@@ -259,6 +281,13 @@ cudaError_t launch_combine_t(const CombineParams& cp, int batch, cudaStream_t st
   cfg.blockDim = dim3(kCombineThreads, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
+  // programmatic dependent launch: may be scheduled while stage 1 drains; the
+  // kernel waits (griddepcontrol.wait) before it reads the partials
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, combine_kernel<QF>, cp);
 }
 
@@ -301,11 +330,22 @@ gqa_status_t run_split(const Call& c) {
   // log2(e) / sqrt(128): the softmax runs in the exp2 domain
   sp.scale_log2 = (float)((double)c.q_scale * (double)c.k_scale * 1.4426950408889634 / std::sqrt(128.0));
   sp.v_scale = c.v_scale;
+  sp.wait_budget_ns = c.wait_budget_ns;
+  sp.skip_tile = c.skip_tile;
+  sp.kv_scales = c.kv_scales;
+  sp.block_table = c.block_table;
+  sp.page_log2 = c.page_log2;
+  sp.max_pages = c.max_pages;
+  sp.num_pages = c.num_pages;
   cudaError_t e;
   if (c.kv_format == kKvF16) e = launch_split_t<kKvF16, kQF16>(sp, c.stream);
   else if (c.kv_format == kKvBF16) e = launch_split_t<kKvBF16, kQBF16>(sp, c.stream);
-  else if (c.q_dtype == GQA_BF16) e = launch_split_t<kKvE4M3, kQBF16>(sp, c.stream);
-  else e = launch_split_t<kKvE4M3, kQF16>(sp, c.stream);
+  else if (c.kv_format == kKvE4M3)
+    e = c.q_dtype == GQA_BF16 ? launch_split_t<kKvE4M3, kQBF16>(sp, c.stream)
+                              : launch_split_t<kKvE4M3, kQF16>(sp, c.stream);
+  else
+    e = c.q_dtype == GQA_BF16 ? launch_split_t<kKvI8, kQBF16>(sp, c.stream)
+                              : launch_split_t<kKvI8, kQF16>(sp, c.stream);
   if (e != cudaSuccess) return cuda_fail(e, "split kernel launch");
   return GQA_OK;
 }
@@ -377,7 +417,8 @@ gqa_status_t gqa_decode_plan(int batch, int capacity, gqa_kv_format_t kv_format,
   if (!num_splits_out) return fail(GQA_ERR_INVALID_ARGUMENT, "num_splits_out is null");
   gqa_status_t st = validate_shape(batch, capacity);
   if (st != GQA_OK) return st;
-  if (kv_format != GQA_KV_F16 && kv_format != GQA_KV_BF16 && kv_format != GQA_KV_E4M3)
+  if (kv_format != GQA_KV_F16 && kv_format != GQA_KV_BF16 && kv_format != GQA_KV_E4M3 &&
+      kv_format != GQA_KV_I8)
     return fail(GQA_ERR_INVALID_ARGUMENT, "unknown KV format %d", (int)kv_format);
   int sms = 0;
   st = device_ready(device, &sms);
@@ -391,7 +432,8 @@ gqa_status_t gqa_decode_plan_for(int batch, int capacity, gqa_kv_format_t kv_for
   if (!num_splits_out) return fail(GQA_ERR_INVALID_ARGUMENT, "num_splits_out is null");
   gqa_status_t st = validate_shape(batch, capacity);
   if (st != GQA_OK) return st;
-  if (kv_format != GQA_KV_F16 && kv_format != GQA_KV_BF16 && kv_format != GQA_KV_E4M3)
+  if (kv_format != GQA_KV_F16 && kv_format != GQA_KV_BF16 && kv_format != GQA_KV_E4M3 &&
+      kv_format != GQA_KV_I8)
     return fail(GQA_ERR_INVALID_ARGUMENT, "unknown KV format %d", (int)kv_format);
   if (sm_count < 1) return fail(GQA_ERR_INVALID_ARGUMENT, "sm_count %d < 1", sm_count);
   *num_splits_out = plan_splits(batch, capacity, kv_format, sm_count);
@@ -403,7 +445,8 @@ gqa_status_t gqa_decode_split_geometry(int capacity, int num_splits, gqa_kv_form
   if (!chunk_tokens_out || !splits_effective_out) return fail(GQA_ERR_INVALID_ARGUMENT, "null output pointer");
   gqa_status_t st = validate_shape(1, capacity);
   if (st != GQA_OK) return st;
-  if (kv_format != GQA_KV_F16 && kv_format != GQA_KV_BF16 && kv_format != GQA_KV_E4M3)
+  if (kv_format != GQA_KV_F16 && kv_format != GQA_KV_BF16 && kv_format != GQA_KV_E4M3 &&
+      kv_format != GQA_KV_I8)
     return fail(GQA_ERR_INVALID_ARGUMENT, "unknown KV format %d", (int)kv_format);
   if (num_splits < 1 || num_splits > GQA_MAX_SPLITS)
     return fail(GQA_ERR_INVALID_ARGUMENT, "num_splits %d outside [1, %d]", num_splits, GQA_MAX_SPLITS);
@@ -436,12 +479,74 @@ gqa_status_t gqa_decode_fp8kv(const void* q_bf16, const uint8_t* kv_e4m3, const 
   return run_combine(c);
 }
 
+gqa_status_t gqa_decode_int8kv(const void* q, const int8_t* kv_i8, const uint16_t* kv_scales_bf16,
+                               const int32_t* lens, void* out, int batch, int capacity, gqa_dtype_t dtype,
+                               float q_scale, int num_splits, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+  Call c{q, (int)dtype, kv_i8, kKvI8, lens, out, batch, capacity, q_scale, 1.f, 1.f, num_splits, workspace,
+         workspace_bytes, static_cast<cudaStream_t>(stream)};
+  c.kv_scales = kv_scales_bf16;
+  gqa_status_t st = prepare_call(c, false, true);
+  if (st != GQA_OK) return st;
+  st = run_split(c);
+  if (st != GQA_OK) return st;
+  return run_combine(c);
+}
+
+gqa_status_t gqa_decode_paged(const void* q, gqa_dtype_t q_dtype, const void* kv_pages, gqa_kv_format_t kv_format,
+                              const int32_t* block_table, int max_pages_per_seq, int num_pages, int page_size,
+                              const int32_t* lens, void* out, int batch, float q_scale, float k_scale,
+                              float v_scale, int num_splits, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  if (!block_table) return fail(GQA_ERR_INVALID_ARGUMENT, "block_table is null");
+  if (kv_format == GQA_KV_I8) return fail(GQA_ERR_INVALID_ARGUMENT, "a paged int8 cache is not supported");
+  if (page_size < 16 || page_size > 65536 || (page_size & (page_size - 1)) != 0)
+    return fail(GQA_ERR_INVALID_ARGUMENT, "page_size %d is not a power of two in [16, 65536]", page_size);
+  if (num_pages < 1 || max_pages_per_seq < 1)
+    return fail(GQA_ERR_INVALID_ARGUMENT, "num_pages and max_pages_per_seq must be >= 1");
+  const long long cap = (long long)max_pages_per_seq * page_size;
+  if (cap > (1LL << 30)) return fail(GQA_ERR_INVALID_ARGUMENT, "max_pages_per_seq * page_size exceeds 2^30");
+  if (!aligned(block_table, 4)) return fail(GQA_ERR_INVALID_ARGUMENT, "block_table must be 4-byte aligned");
+  Call c{q, (int)q_dtype, kv_pages, (int)kv_format, lens, out, batch, (int)cap, q_scale, k_scale, v_scale,
+         num_splits, workspace, workspace_bytes, static_cast<cudaStream_t>(stream)};
+  c.block_table = block_table;
+  c.max_pages = max_pages_per_seq;
+  c.num_pages = num_pages;
+  int lg = 0;
+  while ((1 << lg) < page_size) ++lg;
+  c.page_log2 = lg;
+  gqa_status_t st = prepare_call(c, false, true);
+  if (st != GQA_OK) return st;
+  st = run_split(c);
+  if (st != GQA_OK) return st;
+  return run_combine(c);
+}
+
 gqa_status_t gqa_decode_split_stage(const void* q, gqa_dtype_t q_dtype, const void* kv,
                                     gqa_kv_format_t kv_format, const int32_t* lens, void* out, int batch,
                                     int capacity, float q_scale, float k_scale, float v_scale, int num_splits,
                                     void* workspace, size_t workspace_bytes, void* stream) {
+  if (kv_format == GQA_KV_I8)
+    return fail(GQA_ERR_INVALID_ARGUMENT, "an int8 cache needs its scales: use gqa_decode_int8kv");
   Call c{q, (int)q_dtype, kv, (int)kv_format, lens, out, batch, capacity, q_scale, k_scale, v_scale,
          num_splits, workspace, workspace_bytes, static_cast<cudaStream_t>(stream)};
+  gqa_status_t st = prepare_call(c, false, true);
+  if (st != GQA_OK) return st;
+  return run_split(c);
+}
+
+gqa_status_t gqa_decode_debug_skip_tile(const void* q, gqa_dtype_t q_dtype, const void* kv,
+                                        gqa_kv_format_t kv_format, const int32_t* lens, void* out, int batch,
+                                        int capacity, float q_scale, float k_scale, float v_scale,
+                                        int num_splits, void* workspace, size_t workspace_bytes,
+                                        int skip_tile, uint64_t wait_budget_ns, void* stream) {
+  Call c{q, (int)q_dtype, kv, (int)kv_format, lens, out, batch, capacity, q_scale, k_scale, v_scale,
+         num_splits, workspace, workspace_bytes, static_cast<cudaStream_t>(stream)};
+  if (skip_tile < 0) return fail(GQA_ERR_INVALID_ARGUMENT, "skip_tile must be >= 0");
+  if (wait_budget_ns < 1000000ull || wait_budget_ns > kWaitBudgetNs)
+    return fail(GQA_ERR_INVALID_ARGUMENT, "wait_budget_ns must be in [1 ms, 4 s]");
+  c.skip_tile = skip_tile;
+  c.wait_budget_ns = wait_budget_ns;
   gqa_status_t st = prepare_call(c, false, true);
   if (st != GQA_OK) return st;
   return run_split(c);
@@ -455,13 +560,13 @@ gqa_status_t gqa_decode_combine_stage(const int32_t* lens, void* out, gqa_dtype_
   // the checks (a null kv would be rejected) and skip the q checks.
   static const uint4 dummy = {0, 0, 0, 0};
   const int fmt = (int)kv_format;
-  Call c{nullptr, (int)out_dtype, &dummy, fmt == kKvE4M3 ? fmt : (int)out_dtype, lens, out, batch,
+  Call c{nullptr, (int)out_dtype, &dummy, is_8bit(fmt) ? fmt : (int)out_dtype, lens, out, batch,
          capacity, 1.f, 1.f, v_scale, num_splits, const_cast<void*>(workspace), workspace_bytes,
          static_cast<cudaStream_t>(stream)};
-  if (fmt != kKvE4M3 && fmt != (int)out_dtype && fmt != kKvF16 && fmt != kKvBF16)
+  if (fmt != kKvE4M3 && fmt != kKvI8 && fmt != kKvF16 && fmt != kKvBF16)
     return fail(GQA_ERR_INVALID_ARGUMENT, "unknown KV format %d", fmt);
   c.kv_format = fmt;
-  if (fmt != kKvE4M3 && fmt != (int)out_dtype)
+  if (!is_8bit(fmt) && fmt != (int)out_dtype)
     return fail(GQA_ERR_INVALID_ARGUMENT, "fp16/bf16 KV must have the dtype of out");
   // the dummy kv range (batch*capacity*...) would spuriously overlap out; check
   // only what stage 2 touches

@@ -7,7 +7,8 @@
 //   out = v_scale * (sum_s w_s O_s) / (sum_s w_s l_s)
 // rounded once to fp16/bf16 (nearest even).  This is the merge of the
 // "FlashInfer sm110_gqa_decode" article's "num_splits" section, written as a
-// separate kernel so stage 1 needs no inter-CTA ticket.  One warp per
+// separate kernel so stage 1 needs no inter-CTA ticket; it is launched as a
+// programmatic dependent of stage 1, so its launch overlaps stage 1's tail.  One warp per
 // (b, h), each lane owning 4 dims; the splits are merged in a fixed order, so
 // the result is bitwise deterministic.
 #pragma once
@@ -36,24 +37,39 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
   const int L = min(max(__ldg(p.lens + b), 0), p.capacity);
   const int n = (L + p.chunk - 1) / p.chunk;
   const size_t base = (size_t)(b * kHq + h) * p.num_splits;
+  // launched as a programmatic dependent of stage 1: wait for its partials
+  pdl_wait_prior_grid();
 
+  // Splits are handled 32 at a time: lane k loads the max / denominator of
+  // split s0 + k, the weights 2^(m_s - M) are formed once per split and
+  // broadcast with shuffles, and the partial-output loads are independent.
   float M = -INFINITY;
-  for (int s = lane; s < n; s += 32) M = fmaxf(M, __ldg(p.part_m + base + s));
+  for (int s = lane; s < n; s += 32) M = fmaxf(M, p.part_m[base + s]);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
 
   float Ls = 0.f;
   float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
   const float4* po = reinterpret_cast<const float4*>(p.part_o) + base * (kD / 4) + lane;
-#pragma unroll 4
-  for (int s = 0; s < n; ++s) {
-    const float w = ex2(__ldg(p.part_m + base + s) - M);
-    Ls = fmaf(w, __ldg(p.part_l + base + s), Ls);
-    const float4 v = __ldg(po + (size_t)s * (kD / 4));
-    o.x = fmaf(w, v.x, o.x);
-    o.y = fmaf(w, v.y, o.y);
-    o.z = fmaf(w, v.z, o.z);
-    o.w = fmaf(w, v.w, o.w);
+  for (int s0 = 0; s0 < n; s0 += 32) {
+    const int cnt = min(32, n - s0);
+    float w = 0.f, lw = 0.f;
+    if (lane < cnt) {
+      w = ex2(p.part_m[base + s0 + lane] - M);
+      lw = w * p.part_l[base + s0 + lane];
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, off);
+    Ls += lw;
+#pragma unroll 8
+    for (int k = 0; k < cnt; ++k) {
+      const float wk = __shfl_sync(0xffffffffu, w, k);
+      const float4 v = po[(size_t)(s0 + k) * (kD / 4)];
+      o.x = fmaf(wk, v.x, o.x);
+      o.y = fmaf(wk, v.y, o.y);
+      o.z = fmaf(wk, v.z, o.z);
+      o.w = fmaf(wk, v.w, o.w);
+    }
   }
   const float inv = n > 0 ? p.v_scale / Ls : 0.f;
   uint2 packed;

@@ -17,17 +17,21 @@ constexpr int kHkv = 8;
 constexpr int kGroup = kHq / kHkv;
 constexpr int kD = 128;
 
-enum KvFormat : int { kKvF16 = 0, kKvBF16 = 1, kKvE4M3 = 2 };
+enum KvFormat : int { kKvF16 = 0, kKvBF16 = 1, kKvE4M3 = 2, kKvI8 = 3 };
 enum QFormat : int { kQF16 = 0, kQBF16 = 1 };
+
+__host__ __device__ constexpr bool is_8bit(int kv_format) {
+  return kv_format == kKvE4M3 || kv_format == kKvI8;
+}
 
 // Tokens per pipeline tile: one tile of one plane is 16 KB for every format.
 __host__ __device__ constexpr int tile_tokens(int kv_format) {
-  return kv_format == kKvE4M3 ? 128 : 64;
+  return is_8bit(kv_format) ? 128 : 64;
 }
 
 template <int KVF>
 struct KvTraits {
-  static constexpr int kElemBytes = KVF == kKvE4M3 ? 1 : 2;
+  static constexpr int kElemBytes = is_8bit(KVF) ? 1 : 2;
   static constexpr int kRowBytes = kD * kElemBytes;  // one token of one KV head
   static constexpr int kTile = tile_tokens(KVF);
   static constexpr int kTileBytes = kTile * kRowBytes;
@@ -45,7 +49,7 @@ __host__ __device__ inline int split_count(int capacity, int num_splits, int kv_
   return (capacity + chunk - 1) / chunk;
 }
 
-// A pipeline wait gives up after this long (a healthy wait lasts microseconds).
+// Default bound of a pipeline wait (a healthy wait lasts microseconds).
 constexpr uint64_t kWaitBudgetNs = 4000000000ull;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -119,6 +123,17 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
+// Programmatic dependent launch: allow the next kernel in the stream (launched
+// with programmatic stream serialization) to be scheduled now; and, in that
+// kernel, wait until the preceding grid has completed and its writes are
+// visible.  Both are no-ops when the launch did not opt in.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_prior_grid() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
@@ -147,6 +162,19 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t two) {
   uint32_t h2;
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(two));
   return h2;
+}
+
+// Two int8 codes (low byte = first element) -> exact f16x2.  With b = code +
+// 128 (flip the sign bit), the f16 pattern 0x6400 | b is 1024 + b; subtracting
+// 1152 leaves the code.  Four codes of a word give two pairs.
+__device__ __forceinline__ void i8x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t x = w ^ 0x80808080u;
+  uint32_t a, b;
+  asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(a) : "r"(x), "r"(0x64646464u));
+  asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(b) : "r"(x), "r"(0x64646464u));
+  const uint32_t bias = 0x64806480u;  // (1152, 1152)
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(bias));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(bias));
 }
 
 }  // namespace gqa

@@ -26,10 +26,15 @@
 //           token rows and pairs tokens with byte permutes; P^T reaches the
 //           B-fragment layout through 4 shuffles.  bf16 P is split into a
 //           high and a low bf16 part (two mma) so the weights keep ~16 bits.
-// e4m3 K/V are widened with the hardware cvt (e4m3x2 -> f16x2, exact); the
-// tensor-core type is then f16 and a bf16 q is converted to f16 once per CTA
-// (exact for 2^-17 <= |q| <= 65504; smaller magnitudes round to the f16
-// subnormal grid, larger ones saturate).  fp16 and bf16 KV use their own type.
+// e4m3 K/V are widened with the hardware cvt (e4m3x2 -> f16x2, exact), int8
+// codes with a byte permute and one f16 subtraction (exact); the tensor-core
+// type is then f16 and a bf16 q is converted to f16 once per CTA (exact for
+// 2^-17 <= |q| <= 65504; smaller magnitudes round to the f16 subnormal grid,
+// larger ones saturate).  fp16 and bf16 KV use their own type.  For the int8
+// cache ("Qwen3-VL official BF16 on Jetson Orin (SM87)" docs, "INT8 KV cache
+// (kv_mode)": one bf16 scale per (position, KV head) row) the K row scale
+// multiplies that token's scores and the V row scale joins that token's
+// weight in P; the scales of slots past the length are never read.
 //
 // Sources: "FlashInfer sm110_gqa_decode" article ("Convenience API": log2-domain
 // softmax with the host-folded scale q_scale/sqrt(128)/ln 2 and ex2;
@@ -46,7 +51,8 @@ constexpr int kStageBytes = 2 * 16384;  // one K tile + one V tile (16 KB each)
 
 struct SplitParams {
   const void* q;          // [B,32,128] fp16/bf16
-  const void* kv;         // [B,2,8,C,128] fp16/bf16/e4m3
+  const void* kv;         // [B,2,8,C,128] fp16/bf16/e4m3/int8
+  const uint16_t* kv_scales;  // int8 cache: bf16 [B,2,8,C], one scale per (plane, KV head, slot)
   const int32_t* lens;    // [B]
   void* out;              // [B,32,128], written when the effective split count is 1
   float* part_o;          // [B,32,S,128] unnormalised accumulator
@@ -56,6 +62,12 @@ struct SplitParams {
   int batch, capacity, num_splits, chunk, splits_eff;
   float scale_log2;       // q_scale * k_scale * log2(e) / sqrt(128)
   float v_scale;
+  uint64_t wait_budget_ns;  // every pipeline wait gives up after this long
+  int skip_tile;            // test hook: tile index whose copies are never issued (-1: none)
+  // paged cache (block_table != nullptr): kv is a pool [num_pages, 2, 8, 2^page_log2, 128];
+  // slot t of batch row b lives in page block_table[b * max_pages + (t >> page_log2)]
+  const int32_t* block_table;
+  int page_log2, max_pages, num_pages;
 };
 
 template <int QF>
@@ -73,7 +85,9 @@ constexpr int kMmaConsumerWarps = 4;
 constexpr int kMmaThreads = (kMmaConsumerWarps + 1) * 32;
 constexpr int kMmaStages = 3;
 constexpr int kMmaMergeBytes = kMmaConsumerWarps * kGroup * kD * 4 + 2 * kMmaConsumerWarps * kGroup * 4;
-constexpr int kMmaSmemBytes = kMmaStages * kStageBytes + kMmaMergeBytes + 2 * kMmaStages * 8;
+constexpr int kScaleStageBytes = 2 * 128 * 2;  // int8 cache: K and V row scales of one 128-token tile
+constexpr int kMmaSmemBytes =
+    kMmaStages * kStageBytes + kMmaMergeBytes + kMmaStages * kScaleStageBytes + 2 * kMmaStages * 8;
 
 // ---------------------------------------------------------------- mma.sync
 
@@ -118,7 +132,19 @@ __device__ __forceinline__ uint32_t pack_f16_satfinite(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo_to_f32(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi_to_f32(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// Tensor-core element type: bf16 for bf16 KV, f16 otherwise (e4m3 widens to f16).
+// Four 8-bit KV elements (bytes b0..b3 of w) -> f16x2 pairs (b0,b1), (b2,b3),
+// exactly: hardware cvt for e4m3, byte-permute + subtract for int8 codes.
+template <int KVF>
+__device__ __forceinline__ void widen4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  if constexpr (KVF == kKvI8) {
+    i8x4_to_f16x2x2(w, lo, hi);
+  } else {
+    lo = e4m3x2_to_f16x2((uint16_t)(w & 0xffffu));
+    hi = e4m3x2_to_f16x2((uint16_t)(w >> 16));
+  }
+}
+
+// Tensor-core element type: bf16 for bf16 KV, f16 otherwise (8-bit KV widens to f16).
 template <int KVF>
 constexpr bool kMmaBF16 = KVF == kKvBF16;
 
@@ -135,7 +161,7 @@ constexpr bool kMmaBF16 = KVF == kKvBF16;
 // the same map, so the dot products are unchanged.
 template <int KVF>
 __device__ __forceinline__ int qk_dim(int cq, int ks, int pair /*0: a0/b0, 1: a2/b1*/) {
-  if constexpr (KVF == kKvE4M3) return 16 * (cq + 4 * (ks >> 2)) + 4 * (ks & 3) + 2 * pair;
+  if constexpr (is_8bit(KVF)) return 16 * (cq + 4 * (ks >> 2)) + 4 * (ks & 3) + 2 * pair;
   else return 8 * (cq + 4 * (ks >> 1)) + 4 * (ks & 1) + 2 * pair;
 }
 
@@ -149,9 +175,13 @@ __global__ void __launch_bounds__(kMmaThreads, 2) split_kv_mma_kernel(const __gr
   float* mrg_acc = reinterpret_cast<float*>(smem + kMmaStages * kStageBytes);  // [4 warps][4 heads][128]
   float* mrg_m = mrg_acc + kMmaConsumerWarps * kGroup * kD;                      // [4][4]
   float* mrg_l = mrg_m + kMmaConsumerWarps * kGroup;                             // [4][4]
-  uint64_t* full = reinterpret_cast<uint64_t*>(mrg_l + kMmaConsumerWarps * kGroup);
+  uint16_t* scl = reinterpret_cast<uint16_t*>(mrg_l + kMmaConsumerWarps * kGroup);  // [stage][K|V][128]
+  uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(scl) + kMmaStages * kScaleStageBytes);
   uint64_t* empty = full + kMmaStages;
 
+  // Every CTA of this grid is resident or done: let stage 2 be scheduled
+  // (it waits for this grid's completion before reading the partials).
+  pdl_launch_dependents();
   const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int C = p.capacity;
   const int len_raw = __ldg(p.lens + b);
@@ -180,36 +210,99 @@ __global__ void __launch_bounds__(kMmaThreads, 2) split_kv_mma_kernel(const __gr
     fence_barrier_init();
   }
   __syncthreads();
-  const uint64_t deadline = global_timer_ns() + kWaitBudgetNs;
+  const uint64_t deadline = global_timer_ns() + p.wait_budget_ns;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (warp == kMmaConsumerWarps) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      const size_t plane = (size_t)kHkv * C * T::kRowBytes;
-      const uint8_t* gK = static_cast<const uint8_t*>(p.kv) +
-                          ((size_t)b * 2 * kHkv + g) * (size_t)C * T::kRowBytes;
-      const uint8_t* gV = gK + plane;
-      const uint64_t pol = policy_evict_first();
-      bool ok = true;
-      int issued = 0;
-      for (int i = 0; i < n_tiles; ++i) {
-        const int st = i % kMmaStages;
-        if (i >= kMmaStages && !mbar_wait(&empty[st], ((i / kMmaStages) & 1) ^ 1, deadline)) {
+    // The whole warp runs the loop (its lanes fetch block-table entries 32 at
+    // a time); lane 0 waits on the barriers and issues the copies.
+    const bool paged = p.block_table != nullptr;
+    const size_t page_rows = paged ? ((size_t)1 << p.page_log2) : (size_t)C;
+    const size_t head_bytes = page_rows * T::kRowBytes;  // one (page, plane, KV head) block
+    const uint8_t* base = static_cast<const uint8_t*>(p.kv);
+    const uint64_t pol = policy_evict_first();
+    int last[kMmaStages];  // last tile issued into each stage (-1: none)
+#pragma unroll
+    for (int k = 0; k < kMmaStages; ++k) last[k] = -1;
+    int bt_first = -1, bt_val = 0;  // paged: entry bt_first + lane of this row's block table
+    bool ok = true;
+    for (int i = 0; i < n_tiles; ++i) {
+      const int st = i % kMmaStages;
+      if (i >= kMmaStages) {
+        int got = 1;
+        if (lane == 0) got = mbar_wait(&empty[st], ((i / kMmaStages) & 1) ^ 1, deadline);
+        if (!__shfl_sync(0xffffffffu, got, 0)) {
           ok = false;
           break;
         }
-        const int t0 = t_begin + i * T::kTile;
-        const uint32_t bytes = (uint32_t)min(T::kTile, t_end - t0) * T::kRowBytes;
-        mbar_arrive_expect_tx(&full[st], 2 * bytes);
-        bulk_load(ring + st * kStageBytes, gK + (size_t)t0 * T::kRowBytes, bytes, &full[st], pol);
-        bulk_load(ring + st * kStageBytes + T::kTileBytes, gV + (size_t)t0 * T::kRowBytes, bytes, &full[st],
-                  pol);
-        ++issued;
       }
+      if (i == p.skip_tile) continue;  // test hook: the consumers' wait on this tile runs out
+      const int t0 = t_begin + i * T::kTile;
+      const int rows = min(T::kTile, t_end - t0);
+      uint8_t* dK = ring + st * kStageBytes;
+      uint8_t* dV = dK + T::kTileBytes;
+      uint32_t scale_bytes = 0;
+      const uint16_t* gsk = nullptr;
+      uint16_t* dsk = scl + st * (kScaleStageBytes / 2);
+      if constexpr (KVF == kKvI8) {
+        // row scales of the tile (contiguous cache): whole 16-byte groups by
+        // bulk copy, the ragged tail (< 8 rows) with plain loads before the arrive
+        gsk = p.kv_scales + ((size_t)b * 2 * kHkv + g) * (size_t)C + t0;
+        const int n8 = rows & ~7;
+        if (lane == 0)
+          for (int r = n8; r < rows; ++r) {
+            dsk[r] = gsk[r];
+            dsk[T::kTile + r] = gsk[(size_t)kHkv * C + r];
+          }
+        scale_bytes = 2u * (uint32_t)n8 * 2u;
+      }
+      if (lane == 0) mbar_arrive_expect_tx(&full[st], 2u * (uint32_t)rows * T::kRowBytes + scale_bytes);
+      // rows [t0, t0 + rows) in page segments; a contiguous cache is one page per batch row
+      for (int t = t0; t < t0 + rows;) {
+        size_t page = (size_t)b;
+        int in_page = t, seg_end = t0 + rows;
+        if (paged) {
+          const int pg = t >> p.page_log2;
+          if (bt_first < 0 || pg >= bt_first + 32) {
+            bt_first = pg;
+            const int e = pg + lane;
+            bt_val = e < p.max_pages ? __ldg(p.block_table + (size_t)b * p.max_pages + e) : 0;
+          }
+          int id = __shfl_sync(0xffffffffu, bt_val, pg - bt_first);
+          if (id < 0 || id >= p.num_pages) {  // out-of-contract page id: clamp, flag, never fault
+            if (lane == 0) atomicOr(p.flags, GQA_FLAG_PAGE_CLAMPED);
+            id = min(max(id, 0), p.num_pages - 1);
+          }
+          page = (size_t)id;
+          in_page = t - (pg << p.page_log2);
+          seg_end = min(t0 + rows, (pg + 1) << p.page_log2);
+        }
+        if (lane == 0) {
+          const uint32_t seg_bytes = (uint32_t)(seg_end - t) * T::kRowBytes;
+          const uint8_t* src = base + (page * 2 * kHkv + g) * head_bytes + (size_t)in_page * T::kRowBytes;
+          bulk_load(dK + (t - t0) * T::kRowBytes, src, seg_bytes, &full[st], pol);
+          bulk_load(dV + (t - t0) * T::kRowBytes, src + kHkv * head_bytes, seg_bytes, &full[st], pol);
+        }
+        t = seg_end;
+      }
+      if constexpr (KVF == kKvI8) {
+        if (lane == 0 && scale_bytes > 0) {
+          bulk_load(dsk, gsk, scale_bytes / 2, &full[st], pol);
+          bulk_load(dsk + T::kTile, gsk + (size_t)kHkv * C, scale_bytes / 2, &full[st], pol);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kMmaStages; ++k)
+        if (k == st) last[k] = i;
+    }
+    if (lane == 0) {
       if (!ok) atomicOr(p.flags, GQA_FLAG_WAIT_TIMEOUT);
-      for (int i = max(0, issued - kMmaStages); i < issued; ++i)
-        mbar_wait(&full[i % kMmaStages], (i / kMmaStages) & 1, deadline + kWaitBudgetNs);
+      // Never leave the CTA with copies in flight: wait (bounded) for the last
+      // copy issued into every stage to land.
+#pragma unroll
+      for (int k = 0; k < kMmaStages; ++k)
+        if (last[k] >= 0) mbar_wait(&full[k], (last[k] / kMmaStages) & 1, deadline + p.wait_budget_ns);
     }
     return;
   }
@@ -228,7 +321,7 @@ __global__ void __launch_bounds__(kMmaThreads, 2) split_kv_mma_kernel(const __gr
       for (int pr = 0; pr < 2; ++pr) {
         const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(qrow + qk_dim<KVF>(cq, ks, pr)));
         uint32_t v = w;
-        if constexpr (KVF == kKvE4M3 && QF == kQBF16) v = pack_f16_satfinite(bf16_lo_to_f32(w), bf16_hi_to_f32(w));
+        if constexpr (is_8bit(KVF) && QF == kQBF16) v = pack_f16_satfinite(bf16_lo_to_f32(w), bf16_hi_to_f32(w));
         qb[ks][pr] = gq < kGroup ? v : 0u;
       }
   }
@@ -254,6 +347,19 @@ __global__ void __launch_bounds__(kMmaThreads, 2) split_kv_mma_kernel(const __gr
     const uint8_t* sK = ring + st * kStageBytes;
     const uint8_t* sV = sK + T::kTileBytes;
     const int rows = min(T::kTile, t_end - (t_begin + i * T::kTile));
+    // int8: K and V row scales of this lane's tokens (R+gq, R+gq+8 of each slab)
+    float sk[kSlabs][2], sv[kSlabs][2];
+    if constexpr (KVF == kKvI8) {
+      const uint16_t* tsk = scl + st * (kScaleStageBytes / 2);
+#pragma unroll
+      for (int sl = 0; sl < kSlabs; ++sl)
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int r = (warp * kSlabs + sl) * 16 + gq + 8 * u;
+          sk[sl][u] = r < rows ? __uint_as_float((uint32_t)tsk[r] << 16) : 0.f;
+          sv[sl][u] = r < rows ? __uint_as_float((uint32_t)tsk[T::kTile + r] << 16) : 0.f;
+        }
+    }
 
 #pragma unroll
     for (int sl = 0; sl < kSlabs; ++sl) {
@@ -266,7 +372,7 @@ __global__ void __launch_bounds__(kMmaThreads, 2) split_kv_mma_kernel(const __gr
       {
         const uint8_t* k0 = sK + (R + gq) * T::kRowBytes;
         const uint8_t* k1 = k0 + 8 * T::kRowBytes;
-        if constexpr (KVF == kKvE4M3) {
+        if constexpr (is_8bit(KVF)) {
 #pragma unroll
           for (int ci = 0; ci < 2; ++ci) {
             const uint4 x = *reinterpret_cast<const uint4*>(k0 + 16 * (cq + 4 * ci));
@@ -275,10 +381,10 @@ __global__ void __launch_bounds__(kMmaThreads, 2) split_kv_mma_kernel(const __gr
 #pragma unroll
             for (int s4 = 0; s4 < 4; ++s4) {
               const int ks = 4 * ci + s4;
-              mma16816<false>(sc, e4m3x2_to_f16x2((uint16_t)(xs[s4] & 0xffffu)),
-                              e4m3x2_to_f16x2((uint16_t)(ys[s4] & 0xffffu)),
-                              e4m3x2_to_f16x2((uint16_t)(xs[s4] >> 16)), e4m3x2_to_f16x2((uint16_t)(ys[s4] >> 16)),
-                              qb[ks][0], qb[ks][1]);
+              uint32_t a0, a1, a2, a3;
+              widen4<KVF>(xs[s4], a0, a2);  // row gq: dims (4s,4s+1), (4s+2,4s+3)
+              widen4<KVF>(ys[s4], a1, a3);  // row gq+8
+              mma16816<false>(sc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
             }
           }
         } else {
@@ -293,6 +399,12 @@ __global__ void __launch_bounds__(kMmaThreads, 2) split_kv_mma_kernel(const __gr
       }
       // sc: [0] token R+gq head 2cq, [1] token R+gq head 2cq+1, [2]/[3] token R+gq+8
       float x0 = sc[0] * sl2, x1 = sc[1] * sl2, x2 = sc[2] * sl2, x3 = sc[3] * sl2;
+      if constexpr (KVF == kKvI8) {  // per-row K scale multiplies that token's scores
+        x0 *= sk[sl][0];
+        x1 *= sk[sl][0];
+        x2 *= sk[sl][1];
+        x3 *= sk[sl][1];
+      }
       if (!real_heads || R + gq >= rows) x0 = x1 = -INFINITY;      // select, never multiply
       if (!real_heads || R + gq + 8 >= rows) x2 = x3 = -INFINITY;
 
@@ -337,6 +449,15 @@ __global__ void __launch_bounds__(kMmaThreads, 2) split_kv_mma_kernel(const __gr
         bh1 = prmt(__shfl_sync(0xffffffffu, ph_b, src0), __shfl_sync(0xffffffffu, ph_b, src1), half_sel);
         bl0 = prmt(__shfl_sync(0xffffffffu, pl_a, src0), __shfl_sync(0xffffffffu, pl_a, src1), half_sel);
         bl1 = prmt(__shfl_sync(0xffffffffu, pl_b, src0), __shfl_sync(0xffffffffu, pl_b, src1), half_sel);
+      } else if constexpr (KVF == kKvI8) {
+        // the per-row V scale joins the weight of its token; the denominator
+        // keeps the unscaled weights
+        const uint32_t pa = pack_f16(p0 * sv[sl][0], p1 * sv[sl][0]);
+        const uint32_t pb = pack_f16(p2 * sv[sl][1], p3 * sv[sl][1]);
+        l0 += p0 + p2;
+        l1 += p1 + p3;
+        bh0 = prmt(__shfl_sync(0xffffffffu, pa, src0), __shfl_sync(0xffffffffu, pa, src1), half_sel);
+        bh1 = prmt(__shfl_sync(0xffffffffu, pb, src0), __shfl_sync(0xffffffffu, pb, src1), half_sel);
       } else {
         const uint32_t pa = pack_f16(p0, p1), pb = pack_f16(p2, p3);
         // the denominator sums the same rounded weights the tensor core multiplies
@@ -354,7 +475,7 @@ __global__ void __launch_bounds__(kMmaThreads, 2) split_kv_mma_kernel(const __gr
       const uint8_t* v0 = sV + r0 * T::kRowBytes;
       const bool ok0 = !partial || r0 < rows, ok1 = !partial || r0 + 1 < rows;
       const bool ok2 = !partial || r0 + 8 < rows, ok3 = !partial || r0 + 9 < rows;
-      if constexpr (KVF == kKvE4M3) {
+      if constexpr (is_8bit(KVF)) {
         uint4 w0 = *reinterpret_cast<const uint4*>(v0 + 16 * gq);
         uint4 w1 = *reinterpret_cast<const uint4*>(v0 + T::kRowBytes + 16 * gq);
         uint4 w2 = *reinterpret_cast<const uint4*>(v0 + 8 * T::kRowBytes + 16 * gq);
@@ -368,14 +489,14 @@ __global__ void __launch_bounds__(kMmaThreads, 2) split_kv_mma_kernel(const __gr
         const uint32_t c[4] = {w2.x, w2.y, w2.z, w2.w}, d[4] = {w3.x, w3.y, w3.z, w3.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {  // word j: dims 16gq+4j .. +3 -> m-tiles 2j, 2j+1
-          const uint32_t lo01 = prmt(a[j], bq[j], 0x5140u), lo23 = prmt(a[j], bq[j], 0x7362u);
-          const uint32_t hi01 = prmt(c[j], d[j], 0x5140u), hi23 = prmt(c[j], d[j], 0x7362u);
-          mma16816<false>(o[2 * j], e4m3x2_to_f16x2((uint16_t)(lo01 & 0xffffu)),
-                          e4m3x2_to_f16x2((uint16_t)(lo01 >> 16)), e4m3x2_to_f16x2((uint16_t)(hi01 & 0xffffu)),
-                          e4m3x2_to_f16x2((uint16_t)(hi01 >> 16)), bh0, bh1);
-          mma16816<false>(o[2 * j + 1], e4m3x2_to_f16x2((uint16_t)(lo23 & 0xffffu)),
-                          e4m3x2_to_f16x2((uint16_t)(lo23 >> 16)), e4m3x2_to_f16x2((uint16_t)(hi23 & 0xffffu)),
-                          e4m3x2_to_f16x2((uint16_t)(hi23 >> 16)), bh0, bh1);
+          // pair the two tokens of each k-step: bytes [r0.d, r1.d, r0.d', r1.d']
+          uint32_t A0, A1, A2, A3;
+          widen4<KVF>(prmt(a[j], bq[j], 0x5140u), A0, A1);  // dims 4j, 4j+1 of tokens r0, r0+1
+          widen4<KVF>(prmt(c[j], d[j], 0x5140u), A2, A3);   // tokens r0+8, r0+9
+          mma16816<false>(o[2 * j], A0, A1, A2, A3, bh0, bh1);
+          widen4<KVF>(prmt(a[j], bq[j], 0x7362u), A0, A1);  // dims 4j+2, 4j+3
+          widen4<KVF>(prmt(c[j], d[j], 0x7362u), A2, A3);
+          mma16816<false>(o[2 * j + 1], A0, A1, A2, A3, bh0, bh1);
         }
       } else {
         const uint8_t* v1 = v0 + T::kRowBytes;

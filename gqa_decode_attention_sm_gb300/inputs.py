@@ -13,6 +13,10 @@ Workloads (shapes, distributions and structure of the five decode cases):
      K,V ~ N(0,1)*2 quantised with one per-tensor scale amax/448
 q ~ N(0,1) everywhere; K,V ~ N(0,1) for workloads 1-4; q_scale = 1.
 
+An INT8 cache (kv_dtype "i8") stores int8 codes with one bf16 scale per
+(plane, KV head, position) row: scale = amax(|row|)/127 rounded to bf16,
+code = round(x / scale) clipped to [-127, 127].
+
 Recipe: a torch.Generator on the target device; lengths drawn first from
 ``seed``; q from ``seed + 1``; the KV slice of batch row b from
 ``seed * 7919 + 1000 + b`` so rows can be generated (and regenerated) one at a
@@ -32,7 +36,7 @@ E4M3_MAX = 448.0
 class Workload:
     index: int
     name: str
-    kv_dtype: str          # "f16" | "bf16" | "e4m3"
+    kv_dtype: str          # "f16" | "bf16" | "e4m3" | "i8"
     q_dtype: str           # "f16" | "bf16"
     batch: int
     capacity: int
@@ -63,7 +67,7 @@ def custom(batch: int, capacity: int, len_lo: int, len_hi: int | None = None,
            kv_std: float = 1.0, q_scale: float = 1.0, index: int = 0) -> Workload:
     """A workload of any size with the same recipe (edge cases, small tests)."""
     if q_dtype is None:
-        q_dtype = "bf16" if kv_dtype == "e4m3" else kv_dtype
+        q_dtype = "bf16" if kv_dtype in ("e4m3", "i8") else kv_dtype
     return Workload(index, f"custom B{batch} C{capacity}", kv_dtype, q_dtype, batch, capacity,
                     len_lo, len_lo if len_hi is None else len_hi, nan_tail, kv_std, q_scale)
 
@@ -78,7 +82,11 @@ def _gen(device, seed: int) -> torch.Generator:
 
 
 def kv_storage_dtype(w: Workload) -> torch.dtype:
-    return torch.uint8 if w.kv_dtype == "e4m3" else _TORCH[w.kv_dtype]
+    if w.kv_dtype == "e4m3":
+        return torch.uint8
+    if w.kv_dtype == "i8":
+        return torch.int8
+    return _TORCH[w.kv_dtype]
 
 
 def _kv_row_fp32(w: Workload, b: int, device, seed: int) -> torch.Tensor:
@@ -92,9 +100,10 @@ def _kv_row_fp32(w: Workload, b: int, device, seed: int) -> torch.Tensor:
 def make(w: Workload, device="cpu", seed: int | None = None, lens=None) -> dict:
     """Build one batch of inputs on ``device``.
 
-    Returns a dict with q [B,32,128], kv [B,2,8,C,128] (uint8 bytes for e4m3),
-    lens int32 [B], q_scale, k_scale, v_scale (python floats; the e4m3 scale is
-    the fp32 value actually stored), and the workload.
+    Returns a dict with q [B,32,128], kv [B,2,8,C,128] (uint8 bytes for e4m3,
+    int8 codes for i8), kv_scales (bf16 [B,2,8,C] for i8, else None), lens
+    int32 [B], q_scale, k_scale, v_scale (python floats; the e4m3 scale is the
+    fp32 value actually stored), and the workload.
     ``lens`` overrides the drawn lengths (a list or tensor of B ints).
     """
     seed = w.seed if seed is None else int(seed)
@@ -113,7 +122,17 @@ def make(w: Workload, device="cpu", seed: int | None = None, lens=None) -> dict:
 
     kv = torch.empty((B, 2, HKV, C, D), device=device, dtype=kv_storage_dtype(w))
     k_scale = v_scale = 1.0
-    if w.kv_dtype == "e4m3":
+    kv_scales = None
+    if w.kv_dtype == "i8":
+        kv_scales = torch.empty((B, 2, HKV, C), device=device, dtype=torch.bfloat16)
+        for b in range(B):
+            x = _kv_row_fp32(w, b, device, seed)
+            sc = (x.abs().amax(dim=-1) / 127.0).to(torch.bfloat16)   # one scale per row
+            sc = torch.where(sc == 0, torch.ones_like(sc), sc)
+            codes = torch.round(x / sc.float().unsqueeze(-1)).clamp_(-127, 127)
+            kv[b].copy_(codes.to(torch.int8))
+            kv_scales[b].copy_(sc)
+    elif w.kv_dtype == "e4m3":
         # one amax over every K and V value of the allocated cache
         amax = torch.zeros((), device=device, dtype=torch.float32)
         for b in range(B):
@@ -128,8 +147,11 @@ def make(w: Workload, device="cpu", seed: int | None = None, lens=None) -> dict:
             kv[b].copy_(_kv_row_fp32(w, b, device, seed).to(_TORCH[w.kv_dtype]))
     if w.nan_tail:
         fill_tail(kv, lens_t, w.kv_dtype)
+        if kv_scales is not None:  # codes have no NaN: poison the unused rows' scales instead
+            for b, L in enumerate(lens_t.tolist()):
+                kv_scales[b, :, :, L:] = float("nan")
     return dict(q=q, kv=kv, lens=lens_t.to(device), q_scale=w.q_scale, k_scale=k_scale,
-                v_scale=v_scale, workload=w)
+                v_scale=v_scale, kv_scales=kv_scales, workload=w)
 
 
 def fill_tail(kv: torch.Tensor, lens, kv_dtype: str, value: float = float("nan")) -> None:
@@ -141,7 +163,9 @@ def fill_tail(kv: torch.Tensor, lens, kv_dtype: str, value: float = float("nan")
     for b, L in enumerate(lens_l):
         if L >= kv.shape[3]:
             continue
-        if kv_dtype == "e4m3":
+        if kv_dtype == "i8":  # codes cannot hold NaN: use the extreme code
+            kv[b, :, :, L:, :].fill_(-128 if value != value else int(max(-127, min(127, value))))
+        elif kv_dtype == "e4m3":
             if value != value:  # NaN
                 kv[b, :, :, L:, :].fill_(0x7F)
             else:
@@ -158,6 +182,8 @@ def bits(t: torch.Tensor):
         return t.view(torch.int16).cpu().numpy().view("uint16")
     if t.dtype == torch.uint8:
         return t.cpu().numpy()
+    if t.dtype == torch.int8:
+        return t.cpu().numpy().view("uint8")
     if t.dtype == torch.float8_e4m3fn:
         return t.view(torch.uint8).cpu().numpy()
     raise TypeError(f"no bit view for {t.dtype}")
@@ -165,3 +191,40 @@ def bits(t: torch.Tensor):
 
 def with_(w: Workload, **kw) -> Workload:
     return replace(w, **kw)
+
+
+def paginate(t: dict, page_size: int, extra_pages: int = 3, seed: int = 0) -> dict:
+    """Scatter a contiguous cache into a shuffled page pool (a paged cache).
+
+    Returns a copy of ``t`` with kv_pages [num_pages, 2, 8, page_size, 128]
+    (same dtype), block_table int32 [B, C/page_size] and num_pages.  Page ids
+    are a seeded permutation; ``extra_pages`` spare pages, and the block-table
+    entries of pages past each length, point at pages filled with NaN (0x7F
+    for e4m3 bytes), which a correct kernel never reads.
+    """
+    kv = t["kv"]
+    B, _, H, C, Dd = kv.shape
+    assert C % page_size == 0, "capacity must be a whole number of pages"
+    per = C // page_size
+    lens = [int(x) for x in t["lens"].cpu().tolist()]
+    used = [(b, j) for b in range(B) for j in range(per) if j * page_size < lens[b]]
+    num_pages = len(used) + extra_pages
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed) + 77)
+    ids = torch.randperm(num_pages, generator=g)
+    pages = torch.empty((num_pages, 2, H, page_size, Dd), dtype=kv.dtype, device=kv.device)
+    if kv.dtype == torch.uint8:
+        pages.fill_(0x7F)
+    elif kv.dtype == torch.int8:
+        pages.fill_(-128)
+    else:
+        pages.fill_(float("nan"))
+    spare = [int(x) for x in ids[len(used):]] or [int(ids[0])]
+    table = torch.full((B, per), spare[0], dtype=torch.int32)
+    for n, (b, j) in enumerate(used):
+        pid = int(ids[n])
+        table[b, j] = pid
+        pages[pid].copy_(kv[b, :, :, j * page_size:(j + 1) * page_size, :])
+    out = dict(t)
+    out.update(kv_pages=pages, block_table=table.to(kv.device), num_pages=num_pages, page_size=page_size)
+    return out

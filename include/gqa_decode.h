@@ -82,11 +82,12 @@ typedef enum {
 
 typedef enum { GQA_F16 = 0, GQA_BF16 = 1 } gqa_dtype_t;
 
-typedef enum { GQA_KV_F16 = 0, GQA_KV_BF16 = 1, GQA_KV_E4M3 = 2 } gqa_kv_format_t;
+typedef enum { GQA_KV_F16 = 0, GQA_KV_BF16 = 1, GQA_KV_E4M3 = 2, GQA_KV_I8 = 3 } gqa_kv_format_t;
 
 /* Bits of the status word in the workspace header. */
 #define GQA_FLAG_LENGTH_CLAMPED 0x1u  /* some lens[b] was outside [1, capacity] */
 #define GQA_FLAG_WAIT_TIMEOUT 0x2u    /* a pipeline wait gave up; outputs are invalid */
+#define GQA_FLAG_PAGE_CLAMPED 0x4u    /* a block-table entry was outside [0, num_pages) */
 
 /* Name of a status code (static string). */
 const char* gqa_status_string(gqa_status_t status);
@@ -149,6 +150,45 @@ gqa_status_t gqa_decode_fp8kv(const void* q_bf16, const uint8_t* kv_e4m3, const 
                               float k_scale, float v_scale, int num_splits, void* workspace,
                               size_t workspace_bytes, void* stream);
 
+/* INT8 KV cache (the "Qwen3-VL official BF16 on Jetson Orin (SM87)" docs,
+ * section "INT8 KV cache (kv_mode)": INT8 mirrors of the cache with one BF16
+ * scale per (position, KV head) row).  kv_i8 holds int8 codes [batch, 2, 8,
+ * capacity, 128]; kv_scales_bf16 holds bf16 scales [batch, 2, 8, capacity]
+ * (plane 0 K rows, plane 1 V rows), 16-byte aligned, and capacity must be a
+ * multiple of 8 (the scales are staged by 16-byte bulk copies); element (b, p, g, t, d)
+ * of the cache is code * scale[b, p, g, t].  q and out are fp16 or bf16
+ * (`dtype`).  The K row scale multiplies that slot's scores, the V row scale
+ * its weight; scales of slots >= len[b] are never read.  q_scale finite and
+ * >= 0.  Other rules as gqa_decode_prepared (no allocation, no host sync). */
+gqa_status_t gqa_decode_int8kv(const void* q, const int8_t* kv_i8, const uint16_t* kv_scales_bf16,
+                               const int32_t* lens, void* out, int batch, int capacity,
+                               gqa_dtype_t dtype, float q_scale, int num_splits, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
+/* Paged KV cache.  The pages only say that a paged cache is gathered into
+ * one contiguous prefix matrix before attention; this entry reads the pages
+ * in place instead, with the same result.  Layout (this library's reading):
+ *   kv_pages    [num_pages, 2, 8, page_size, 128] in `kv_format` (fp16, bf16
+ *               or e4m3; not int8), each (page, plane, KV head) block contiguous
+ *   block_table int32 [batch, max_pages_per_seq], device memory, read only by
+ *               the kernels: slot t of batch row b is row t % page_size of page
+ *               block_table[b][t / page_size]
+ * page_size is a power of two in [16, 65536]; the capacity is
+ * max_pages_per_seq * page_size (<= 2^30), and lengths follow the usual
+ * contract against it.  Only the entries of pages holding slots < len[b] are
+ * used; an entry outside [0, num_pages) is clamped and flagged with
+ * GQA_FLAG_PAGE_CLAMPED, never dereferenced out of bounds.  q/out dtype
+ * `q_dtype` (must equal fp16/bf16 KV; either for e4m3).  k_scale, v_scale as
+ * gqa_decode_fp8kv (1 for fp16/bf16).  Both stages, no allocation, no host
+ * sync; the workspace as gqa_decode_prepared for capacity
+ * max_pages_per_seq * page_size. */
+gqa_status_t gqa_decode_paged(const void* q, gqa_dtype_t q_dtype, const void* kv_pages,
+                              gqa_kv_format_t kv_format, const int32_t* block_table,
+                              int max_pages_per_seq, int num_pages, int page_size,
+                              const int32_t* lens, void* out, int batch, float q_scale,
+                              float k_scale, float v_scale, int num_splits, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
 /* The two stages of a prepared launch, for callers that schedule (or time)
  * them separately.  Stage 1 streams K/V once per (b, KV head, split) and
  * writes FP32 partials to the workspace, or the final output when
@@ -156,7 +196,8 @@ gqa_status_t gqa_decode_fp8kv(const void* q_bf16, const uint8_t* kv_e4m3, const 
  * a log-sum-exp combine and writes `out`; with num_splits == 1 it launches
  * nothing.  Both must be given the same geometry, scales and workspace, in
  * this order, on one stream.  Validation as gqa_decode_prepared, except that
- * q_scale may be 0. */
+ * q_scale may be 0.  Stage 1 does not take an int8 cache (it has no scale
+ * argument: use gqa_decode_int8kv); stage 2 accepts every format. */
 gqa_status_t gqa_decode_split_stage(const void* q, gqa_dtype_t q_dtype, const void* kv,
                                     gqa_kv_format_t kv_format, const int32_t* lens, void* out,
                                     int batch, int capacity, float q_scale, float k_scale,
@@ -198,6 +239,22 @@ gqa_status_t gqa_decode_combine_stage(const int32_t* lens, void* out, gqa_dtype_
 gqa_status_t gqa_decode_noalloc(const void* q, const void* kv, const int32_t* lens, void* out,
                                 int batch, int capacity, gqa_dtype_t dtype, float q_scale,
                                 int num_splits, void* stream);
+
+/* Test hook for the failure path (not for production use).  Launches stage 1
+ * exactly as gqa_decode_split_stage does, except that the producer never
+ * issues the copies of tile `skip_tile` (0-based, 64 tokens for fp16/bf16,
+ * 128 for e4m3) of each split, so the consumers' wait on that tile runs out
+ * after `wait_budget_ns` (1 ms .. 4 s).  Each affected CTA then sets
+ * GQA_FLAG_WAIT_TIMEOUT in the workspace header, waits (bounded) for its own
+ * copies in flight and returns; outputs and partials are invalid.  Lets a test
+ * check that a stalled pipeline is reported to the host while the CUDA
+ * context stays usable, without faulting or hanging the GPU. */
+gqa_status_t gqa_decode_debug_skip_tile(const void* q, gqa_dtype_t q_dtype, const void* kv,
+                                        gqa_kv_format_t kv_format, const int32_t* lens, void* out,
+                                        int batch, int capacity, float q_scale, float k_scale,
+                                        float v_scale, int num_splits, void* workspace,
+                                        size_t workspace_bytes, int skip_tile,
+                                        uint64_t wait_budget_ns, void* stream);
 
 /* Zero the workspace header (status flags) on `stream`.  Asynchronous. */
 gqa_status_t gqa_decode_workspace_init(void* workspace, size_t workspace_bytes, void* stream);

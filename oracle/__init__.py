@@ -16,6 +16,8 @@ computes, and the pages it restates:
 * "FP8 KV cache port on Jetson AGX Thor" blog, section 1 (patches 1 and 2):
   e4m3 cache bytes are reinterpreted, not converted; scores are multiplied by
   k_scale and the normalised output by v_scale.
+* "Qwen3-VL official BF16 on Jetson Orin (SM87)" docs, "INT8 KV cache
+  (kv_mode)": int8 codes with one bf16 scale per (position, KV head) row.
 * "FreeToken-Kai on Turing" notes, change 7: score the whole key range, then a
   plain softmax with no running maximum.
 
@@ -32,7 +34,7 @@ import threading
 
 import numpy as np
 
-F16, BF16, E4M3 = 0, 1, 2
+F16, BF16, E4M3, I8 = 0, 1, 2, 3
 HQ, HKV, D = 32, 8, 128
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -83,7 +85,7 @@ def _bind(lib):
     lib.orc_round_array.restype = None
     lib.orc_round_array.argtypes = [p, ctypes.c_size_t, ctypes.c_int, p]
     lib.orc_gqa_decode.restype = ctypes.c_int
-    lib.orc_gqa_decode.argtypes = [p, ctypes.c_int, p, ctypes.c_int, p, ctypes.c_int,
+    lib.orc_gqa_decode.argtypes = [p, ctypes.c_int, p, ctypes.c_int, p, p, ctypes.c_int,
                                    ctypes.c_int, ctypes.c_double, ctypes.c_double,
                                    ctypes.c_double, p, ctypes.c_int, p, p, ctypes.c_int,
                                    ctypes.c_int]
@@ -93,8 +95,9 @@ def _bind(lib):
 def decode(bits: np.ndarray, fmt: int, lib=None) -> np.ndarray:
     """Decode raw bit patterns (uint16 for f16/bf16, uint8 for e4m3) to float64."""
     lib = lib or load()
-    flat = np.ascontiguousarray(np.asarray(bits).ravel(),
-                                dtype=np.uint8 if fmt == E4M3 else np.uint16)
+    flat = np.asarray(bits).ravel()
+    flat = np.ascontiguousarray(flat.view(np.uint8) if fmt == I8 and flat.dtype == np.int8 else flat,
+                                dtype=np.uint8 if fmt in (E4M3, I8) else np.uint16)
     out = np.empty(flat.size, dtype=np.float64)
     lib.orc_decode_array(flat.ctypes.data, fmt, flat.size, out.ctypes.data)
     return out.reshape(np.shape(bits))
@@ -120,12 +123,13 @@ def default_threads() -> int:
 def gqa_decode(q_bits: np.ndarray, q_fmt: int, kv_bits: np.ndarray, kv_fmt: int,
                lens: np.ndarray, q_scale: float = 1.0, k_scale: float = 1.0,
                v_scale: float = 1.0, rows=None, out_fmt: int | None = None,
-               threads: int | None = None, lib=None):
+               threads: int | None = None, lib=None, kv_scales: np.ndarray | None = None):
     """Oracle attention output.
 
-    q_bits  uint16 [B,32,128] (f16 or bf16 bit patterns)
-    kv_bits uint16 [B,2,8,C,128] (f16/bf16) or uint8 (e4m3 bytes)
-    lens    int32 [B]
+    q_bits    uint16 [B,32,128] (f16 or bf16 bit patterns)
+    kv_bits   uint16 [B,2,8,C,128] (f16/bf16), uint8 (e4m3 bytes) or int8 codes (I8)
+    kv_scales bf16 bit patterns (uint16) [B,2,8,C], required for I8
+    lens      int32 [B]
     rows    optional iterable of b*32+h; default all rows in order
     Returns (out_f64 [n_rows,128], out_bits uint16 [n_rows,128]).
     """
@@ -136,7 +140,13 @@ def gqa_decode(q_bits: np.ndarray, q_fmt: int, kv_bits: np.ndarray, kv_fmt: int,
     B = q_bits.shape[0]
     assert q_bits.shape == (B, HQ, D) and q_bits.dtype == np.uint16
     assert kv_bits.ndim == 5 and kv_bits.shape[:3] == (B, 2, HKV) and kv_bits.shape[4] == D
-    assert kv_bits.dtype == (np.uint8 if kv_fmt == E4M3 else np.uint16)
+    if kv_fmt == I8:
+        kv_bits = kv_bits.view(np.int8)
+        assert kv_scales is not None
+        kv_scales = np.ascontiguousarray(kv_scales).view(np.uint16)
+        assert kv_scales.shape == kv_bits.shape[:4]
+    else:
+        assert kv_bits.dtype == (np.uint8 if kv_fmt == E4M3 else np.uint16)
     assert lens.shape == (B,)
     C = kv_bits.shape[3]
     if out_fmt is None:
@@ -149,9 +159,29 @@ def gqa_decode(q_bits: np.ndarray, q_fmt: int, kv_bits: np.ndarray, kv_fmt: int,
     out = np.zeros((n, D), dtype=np.float64)
     bits = np.zeros((n, D), dtype=np.uint16)
     st = lib.orc_gqa_decode(q_bits.ctypes.data, q_fmt, kv_bits.ctypes.data, kv_fmt,
+                            kv_scales.ctypes.data if kv_fmt == I8 else None,
                             lens.ctypes.data, B, C, float(q_scale), float(k_scale),
                             float(v_scale), rows_arr.ctypes.data, n, out.ctypes.data,
                             bits.ctypes.data, out_fmt, threads or default_threads())
     if st != 0:
         raise ValueError(f"oracle: {_ERRORS.get(st, st)}")
     return out, bits
+
+
+def gather_pages(pages: np.ndarray, block_table: np.ndarray, lens: np.ndarray) -> np.ndarray:
+    """A paged cache gathered into one contiguous prefix matrix per batch row.
+
+    pages [num_pages, 2, 8, page_size, 128] (bits), block_table int [B, max_pages]:
+    slot t of row b is row t % page_size of page block_table[b, t // page_size].
+    Only the pages that hold slots below each length are gathered; the rest of
+    the returned [B, 2, 8, max_pages * page_size, 128] array is zero.
+    (The "FreeToken-Kai on Turing" notes, change 7: gather the prefix out of the
+    paged cache so the keys are one contiguous matrix.)
+    """
+    B, max_pages = block_table.shape
+    ps = pages.shape[3]
+    out = np.zeros((B, 2, HKV, max_pages * ps, D), dtype=pages.dtype)
+    for b in range(B):
+        for j in range(-(-int(lens[b]) // ps)):
+            out[b, :, :, j * ps:(j + 1) * ps] = pages[int(block_table[b, j])]
+    return out

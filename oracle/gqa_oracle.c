@@ -19,6 +19,10 @@
  *         product, scores are multiplied by k_scale, the normalised output
  *         by v_scale; patch 1 item 5: the cache bytes are reinterpreted as
  *         float8_e4m3fn, not converted.
+ *   [ORIN] "Qwen3-VL official BF16 on Jetson Orin (SM87)" docs, section
+ *         "INT8 KV cache (kv_mode)": INT8 mirrors of the cache with one BF16
+ *         scale per (position, KV head) row; section "Decode weight
+ *         quantization": INT8 symmetric, scale = amax/127.
  *   [TU]  "FreeToken-Kai on Turing" notes, change 7: the whole key range is
  *         scored at once and the softmax is the plain one (no running
  *         maximum, nothing to rescale).  This oracle takes that form.
@@ -30,6 +34,8 @@
  *   s_t = (q_scale / sqrt(128)) * sum_d dec(q[b,h,d]) * K_t[d]
  *   w_t = exp(s_t - max_u s_u)
  *   out = sum_t w_t V_t / sum_t w_t,  rounded once, FP64 -> fp16/bf16, RNE.
+ * For the INT8 cache ([ORIN]) dec(kv[b,p,g,t,d]) = code * scale[b,p,g,t], the
+ * int8 code times the bf16 scale of that (plane, KV head, position) row.
  * For fp16/bf16 KV, k_scale = v_scale = 1.  Multiplying V by v_scale before
  * the weighted sum equals multiplying the normalised output by v_scale in
  * exact arithmetic ([FP8]).
@@ -48,7 +54,7 @@
 #include <stdlib.h>
 #include <string.h>
 
-enum { ORC_F16 = 0, ORC_BF16 = 1, ORC_E4M3 = 2 };
+enum { ORC_F16 = 0, ORC_BF16 = 1, ORC_E4M3 = 2, ORC_I8 = 3 };
 
 enum {
   ORC_OK = 0,
@@ -133,7 +139,8 @@ uint16_t orc_round_bf16(double x) {
 /* Array forms of the two functions above (one call instead of one per value). */
 void orc_decode_array(const void* in, int fmt, size_t n, double* out) {
   for (size_t i = 0; i < n; ++i) {
-    if (fmt == ORC_E4M3) out[i] = orc_decode_e4m3(((const uint8_t*)in)[i]);
+    if (fmt == ORC_I8) out[i] = (double)((const int8_t*)in)[i];
+    else if (fmt == ORC_E4M3) out[i] = orc_decode_e4m3(((const uint8_t*)in)[i]);
     else if (fmt == ORC_F16) out[i] = orc_decode_f16(((const uint16_t*)in)[i]);
     else out[i] = orc_decode_bf16(((const uint16_t*)in)[i]);
   }
@@ -151,6 +158,7 @@ typedef struct {
   int q_type;
   const void* kv;
   int kv_type;
+  const uint16_t* kv_scales;  /* ORC_I8: bf16 bits [B,2,8,C]; else NULL */
   const int32_t* lens;
   int batch, capacity;
   double q_scale, k_scale, v_scale;
@@ -165,6 +173,7 @@ typedef struct {
 } orc_job;
 
 static double orc_elem(const void* base, int type, size_t i) {
+  if (type == ORC_I8) return (double)((const int8_t*)base)[i];
   if (type == ORC_E4M3) return orc_decode_e4m3(((const uint8_t*)base)[i]);
   uint16_t h = ((const uint16_t*)base)[i];
   return type == ORC_F16 ? orc_decode_f16(h) : orc_decode_bf16(h);
@@ -187,11 +196,15 @@ static int orc_row(const orc_job* j, int r, double* s) {
   for (int d = 0; d < ORC_D; ++d) qd[d] = orc_elem(j->q, j->q_type, q_off + d);
 
   /* pass 1: every score, and their maximum */
+  /* one scale per (plane, KV head, position) row for the INT8 cache */
+  const size_t ks_off = (((size_t)b * 2 + 0) * ORC_HKV + g) * C;
+  const size_t vs_off = (((size_t)b * 2 + 1) * ORC_HKV + g) * C;
   double m = -INFINITY;
   for (int t = 0; t < L; ++t) {
+    const double row_k = j->kv_type == ORC_I8 ? orc_decode_bf16(j->kv_scales[ks_off + t]) : 1.0;
     double dot = 0.0;
     for (int d = 0; d < ORC_D; ++d) {
-      double k = orc_elem(j->kv, j->kv_type, k_off + (size_t)t * ORC_D + d) * j->k_scale;
+      double k = orc_elem(j->kv, j->kv_type, k_off + (size_t)t * ORC_D + d) * row_k * j->k_scale;
       dot += qd[d] * k;
     }
     s[t] = scale * dot;
@@ -204,8 +217,9 @@ static int orc_row(const orc_job* j, int r, double* s) {
   for (int t = 0; t < L; ++t) {
     double w = exp(s[t] - m);
     denom += w;
+    const double row_v = j->kv_type == ORC_I8 ? orc_decode_bf16(j->kv_scales[vs_off + t]) : 1.0;
     for (int d = 0; d < ORC_D; ++d) {
-      double v = orc_elem(j->kv, j->kv_type, v_off + (size_t)t * ORC_D + d) * j->v_scale;
+      double v = orc_elem(j->kv, j->kv_type, v_off + (size_t)t * ORC_D + d) * row_v * j->v_scale;
       acc[d] += w * v;
     }
   }
@@ -232,16 +246,18 @@ static void* orc_worker(void* arg) {
 }
 
 /* Compute the rows listed in `rows` (each b*32 + h; NULL = all batch*32 rows
- * in order) with `n_threads` POSIX threads.  Returns ORC_OK or an error code;
+ * in order) with `n_threads` POSIX threads.  kv_scales: bf16 bit patterns
+ * [batch,2,8,capacity] for kv_type ORC_I8 (int8 codes), ignored otherwise.  Returns ORC_OK or an error code;
  * on ORC_ELENGTH nothing about the other rows is promised. */
 int orc_gqa_decode(const void* q, int q_type, const void* kv, int kv_type,
-                   const int32_t* lens, int batch, int capacity,
+                   const uint16_t* kv_scales, const int32_t* lens, int batch, int capacity,
                    double q_scale, double k_scale, double v_scale,
                    const int32_t* rows, int n_rows,
                    double* out_f64, uint16_t* out_bits, int out_type, int n_threads) {
   if (!q || !kv || !lens || !out_f64 || batch < 1 || capacity < 1) return ORC_EINVAL;
   if ((q_type != ORC_F16 && q_type != ORC_BF16) ||
-      (kv_type != ORC_F16 && kv_type != ORC_BF16 && kv_type != ORC_E4M3) ||
+      (kv_type != ORC_F16 && kv_type != ORC_BF16 && kv_type != ORC_E4M3 && kv_type != ORC_I8) ||
+      (kv_type == ORC_I8 && !kv_scales) ||
       (out_type != ORC_F16 && out_type != ORC_BF16))
     return ORC_EINVAL;
   int32_t* all = NULL;
@@ -261,7 +277,7 @@ int orc_gqa_decode(const void* q, int q_type, const void* kv, int kv_type,
   pthread_t* tids = (pthread_t*)calloc((size_t)n_threads, sizeof(pthread_t));
   if (!jobs || !tids) { free(jobs); free(tids); free(all); return ORC_ENOMEM; }
   for (int t = 0; t < n_threads; ++t) {
-    orc_job j = {q, q_type, kv, kv_type, lens, batch, capacity, q_scale, k_scale, v_scale,
+    orc_job j = {q, q_type, kv, kv_type, kv_scales, lens, batch, capacity, q_scale, k_scale, v_scale,
                  rows, n_rows, out_f64, out_bits, out_type, n_threads, t, ORC_OK};
     jobs[t] = j;
   }

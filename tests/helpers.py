@@ -33,6 +33,8 @@ def bits_of(t: torch.Tensor) -> np.ndarray:
         return t.view(torch.int16).numpy().view(np.uint16)
     if t.dtype == torch.uint8:
         return t.numpy()
+    if t.dtype == torch.int8:
+        return t.numpy().view(np.uint8)
     if t.dtype == torch.float8_e4m3fn:
         return t.view(torch.uint8).numpy()
     raise TypeError(t.dtype)
@@ -46,6 +48,8 @@ def values_of_bits(b: np.ndarray, fmt: str) -> np.ndarray:
         return torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
     if fmt == "e4m3":
         return torch.from_numpy(b).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    if fmt == "i8":  # the codes only (the row scales are separate)
+        return b.view(np.int8).astype(np.float64)
     raise ValueError(fmt)
 
 

@@ -20,7 +20,7 @@ HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))
 
 OK, EINVAL, EDEV, EWS, EALIAS, ECUDA = 0, 1, 2, 3, 4, 5
 F16, BF16 = 0, 1
-KV_F16, KV_BF16, KV_E4M3 = 0, 1, 2
+KV_F16, KV_BF16, KV_E4M3, KV_I8 = 0, 1, 2, 3
 
 
 @pytest.fixture(scope="module")
@@ -185,6 +185,45 @@ def test_stage_validation(lib):
     assert c(LENS, OUT, F16, KV_F16, 2, 64, 0.0, 1, WS, 256, None) == EINVAL
     assert c(LENS, OUT, F16, KV_F16, 2, 64, 1.0, 4, WS, 256, None) == EWS
     assert c(LENS, WS + 64, F16, KV_F16, 2, 64, 1.0, 1, WS, 256, None) == EALIAS
+
+
+def test_int8_validation(lib):
+    f = lib.gqa_decode_int8kv
+    SC = 0x60000000
+    assert f(Q, KV, None, LENS, OUT, 2, 64, F16, 1.0, 1, WS, 256, None) == EINVAL      # no scales
+    assert f(Q, KV, SC + 2, LENS, OUT, 2, 64, F16, 1.0, 1, WS, 256, None) == EINVAL    # misaligned
+    assert f(Q, KV, SC, LENS, OUT, 2, 60, F16, 1.0, 1, WS, 256, None) == EINVAL        # capacity % 8
+    assert f(Q, KV, SC, LENS, OUT, 2, 64, 7, 1.0, 1, WS, 256, None) == EINVAL          # dtype
+    assert f(Q, KV, SC, LENS, SC + 64, 2, 64, F16, 1.0, 1, WS, 256, None) == EALIAS    # out on scales
+    assert f(Q, KV, SC, LENS, OUT, 2, 64, F16, 1.0, 4, WS, 256, None) == EWS
+    # stage 1 alone has no scale argument, so it refuses an int8 cache
+    assert lib.gqa_decode_split_stage(Q, F16, KV, KV_I8, LENS, OUT, 2, 64, 1.0, 1.0, 1.0, 1, WS, 256,
+                                      None) == EINVAL
+    # 8-bit formats share the 128-token tile
+    a, b = ctypes.c_int(0), ctypes.c_int(0)
+    assert lib.gqa_decode_split_geometry(1000, 256, KV_I8, ctypes.byref(a), ctypes.byref(b)) == OK
+    assert (a.value, b.value) == (128, 8)
+
+
+def test_paged_validation(lib):
+    f = lib.gqa_decode_paged
+    BT = 0x70000000
+
+    def call(**kw):
+        a = dict(q=Q, qd=F16, kv=KV, kvf=KV_F16, bt=BT, maxp=4, nump=16, ps=64, lens=LENS, out=OUT, B=2,
+                 S=1, ws=WS, wsb=256)
+        a.update(kw)
+        return f(a["q"], a["qd"], a["kv"], a["kvf"], a["bt"], a["maxp"], a["nump"], a["ps"], a["lens"],
+                 a["out"], a["B"], 1.0, 1.0, 1.0, a["S"], a["ws"], a["wsb"], None)
+
+    assert call(bt=None) == EINVAL
+    assert call(kvf=KV_I8) == EINVAL                 # no paged int8
+    assert call(ps=48) == EINVAL and call(ps=8) == EINVAL and call(ps=1 << 17) == EINVAL
+    assert call(nump=0) == EINVAL and call(maxp=0) == EINVAL
+    assert call(maxp=1 << 20, ps=2048) == EINVAL     # capacity above 2^30
+    assert call(bt=BT + 2) == EINVAL
+    assert call(out=BT) == EALIAS                    # out on the block table
+    assert call(S=4) == EWS
 
 
 def test_convenience_validation(lib):

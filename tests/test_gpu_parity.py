@@ -22,7 +22,7 @@ from helpers import HQ, bits_of, tolerance_ok
 
 pytestmark = pytest.mark.gpu
 
-FMT = {"f16": oracle.F16, "bf16": oracle.BF16, "e4m3": oracle.E4M3}
+FMT = {"f16": oracle.F16, "bf16": oracle.BF16, "e4m3": oracle.E4M3, "i8": oracle.I8}
 DEV = torch.device("cuda", 0)
 
 
@@ -42,7 +42,10 @@ def _prepare(t, out=None, num_splits=None, workspace=None):
     w = t["workload"]
     out = torch.empty_like(t["q"]) if out is None else out
     fp8 = w.kv_dtype == "e4m3"
-    return gq.prepare({"Q": t["q"], "KV": t["kv"], "O": out, "sequence_lengths": t["lens"]},
+    tensors = {"Q": t["q"], "KV": t["kv"], "O": out, "sequence_lengths": t["lens"]}
+    if t.get("kv_scales") is not None:
+        tensors["KV_SCALES"] = t["kv_scales"]
+    return gq.prepare(tensors,
                       q_scale=t["q_scale"], num_splits=num_splits,
                       k_scale=t["k_scale"] if fp8 else None, v_scale=t["v_scale"] if fp8 else None,
                       workspace=workspace)
@@ -58,6 +61,8 @@ def _run(t, num_splits=None):
 def _oracle_full(t, **kw):
     w = t["workload"]
     args = dict(q_scale=t["q_scale"], k_scale=t["k_scale"], v_scale=t["v_scale"])
+    if t.get("kv_scales") is not None:
+        args["kv_scales"] = bits_of(t["kv_scales"])
     args.update(kw)
     out, _ = oracle.gqa_decode(bits_of(t["q"]), FMT[w.q_dtype], bits_of(t["kv"]), FMT[w.kv_dtype],
                                t["lens"].cpu().numpy(), **args)
@@ -72,12 +77,17 @@ def _oracle_units(t, units):
     res = {}
     for b, g in units:
         qb = bits_of(t["q"][b:b + 1])
-        kvb = np.zeros((1, 2, 8, C, 128), dtype=np.uint8 if w.kv_dtype == "e4m3" else np.uint16)
+        kvb = np.zeros((1, 2, 8, C, 128), dtype=np.uint8 if w.kv_dtype in ("e4m3", "i8") else np.uint16)
         kvb[0, :, g] = bits_of(t["kv"][b, :, g])
+        extra = {}
+        if t.get("kv_scales") is not None:
+            scb = np.zeros((1, 2, 8, C), dtype=np.uint16)
+            scb[0, :, g] = bits_of(t["kv_scales"][b, :, g])
+            extra["kv_scales"] = scb
         rows = [4 * g + j for j in range(4)]
         out, _ = oracle.gqa_decode(qb, FMT[w.q_dtype], kvb, FMT[w.kv_dtype], lens[b:b + 1],
                                    q_scale=t["q_scale"], k_scale=t["k_scale"],
-                                   v_scale=t["v_scale"], rows=rows)
+                                   v_scale=t["v_scale"], rows=rows, **extra)
         for j, r in enumerate(rows):
             res[b * HQ + r] = out[j]
     return res
@@ -122,7 +132,7 @@ def test_full_size_workload_sampled(index):
 # ---------------------------------------------------------------- edge cases
 
 
-@pytest.mark.parametrize("kv_dtype", ["f16", "bf16", "e4m3"])
+@pytest.mark.parametrize("kv_dtype", ["f16", "bf16", "e4m3", "i8"])
 def test_tile_edges_and_ragged_lengths(kv_dtype):
     lens = [1, 2, 63, 64, 65, 127, 128, 129, 255, 256, 200, 17]
     w = inputs.custom(len(lens), 256, 1, kv_dtype=kv_dtype, kv_std=2.0 if kv_dtype == "e4m3" else 1.0,
@@ -143,7 +153,7 @@ def test_capacity_one():
     assert np.array_equal(got.reshape(5, 32, 128), np.repeat(v0, 4, axis=1))
 
 
-@pytest.mark.parametrize("kv_dtype", ["f16", "e4m3"])
+@pytest.mark.parametrize("kv_dtype", ["f16", "e4m3", "i8"])
 @pytest.mark.parametrize("S", [1, 2, 3, 7, 16, 64, 256])
 def test_every_split_count(kv_dtype, S):
     w = inputs.custom(3, 1000, 1, kv_dtype=kv_dtype, kv_std=2.0 if kv_dtype == "e4m3" else 1.0,
@@ -151,6 +161,25 @@ def test_every_split_count(kv_dtype, S):
     t = _make(w, lens=[1000, 333, 1])
     p = _run(t, num_splits=S)
     _assert_parity(_gpu_rows(p.out), _oracle_full(t), f"{kv_dtype} splits={S}")
+
+
+@pytest.mark.parametrize("q_dtype", ["bf16", "f16"])
+def test_int8_every_element(q_dtype):
+    t = _make(inputs.custom(6, 1024, 1, 1024, kv_dtype="i8", q_dtype=q_dtype, nan_tail=True))
+    for S in (None, 1, 5):
+        p = _run(t, num_splits=S)
+        _assert_parity(_gpu_rows(p.out), _oracle_full(t), f"int8 KV, {q_dtype} q, splits={p.num_splits}")
+
+
+def test_int8_full_size_sampled():
+    # the e4m3 workload's shape and length mix with an int8 cache (4.3 GB of codes)
+    w = inputs.custom(64, 32768, 16384, 32768, kv_dtype="i8", index=5)
+    t = _make(w)
+    p = _run(t)
+    units = [(0, 0), (17, 3), (40, 6), (63, 7)]
+    ref = _oracle_units(t, units)
+    rows = sorted(ref)
+    _assert_parity(_gpu_rows(p.out)[rows], np.stack([ref[r] for r in rows]), "int8 64 x U[16k,32k] sampled")
 
 
 def test_bf16_every_element_multi_split():
@@ -214,7 +243,7 @@ def test_max_capacity_sampled():
 # ------------------------------------------------------ unused slots, safety
 
 
-@pytest.mark.parametrize("kv_dtype", ["f16", "e4m3"])
+@pytest.mark.parametrize("kv_dtype", ["f16", "e4m3", "i8"])
 def test_output_bit_exact_whatever_the_unused_slots_hold(kv_dtype):
     w = inputs.custom(6, 640, 1, 600, kv_dtype=kv_dtype, kv_std=2.0 if kv_dtype == "e4m3" else 1.0)
     t = _make(w)
@@ -224,6 +253,11 @@ def test_output_bit_exact_whatever_the_unused_slots_hold(kv_dtype):
         inputs.fill_tail(kv, t["lens"], kv_dtype, fill)
         before = kv.clone()
         t2 = dict(t, kv=kv)
+        if kv_dtype == "i8":  # the unused rows' scales too
+            sc = t["kv_scales"].clone()
+            for b, L in enumerate(t["lens"].tolist()):
+                sc[b, :, :, L:] = fill
+            t2["kv_scales"] = sc
         for S in (1, 5):
             p = _run(t2, num_splits=S)
             outs.append((S, p.out.clone()))
@@ -342,3 +376,82 @@ def test_errors_are_reported_before_launch():
             t["q"].data_ptr(), t["kv"].data_ptr(), t["lens"].data_ptr(), t["q"].data_ptr(), 2, 128, 0,
             1.0, 1, p.workspace.data_ptr(), p.workspace_bytes, None))
     assert e.value.name == "GQA_ERR_ALIASING"
+
+
+def test_stalled_pipeline_times_out_is_flagged_and_context_survives():
+    # The test hook never issues tile 3 of each split: the consumers' bounded
+    # wait runs out after 100 ms, the CTAs flag GQA_FLAG_WAIT_TIMEOUT, drain
+    # their own copies and return.  No fault, no hang; the next launch is fine.
+    import time
+    t = _make(inputs.custom(1, 1024, 1024))
+    p = _prepare(t, num_splits=2)  # 16 CTAs of 8 tiles
+    lib = api._lib.load()
+    stream = torch.cuda.current_stream(DEV).cuda_stream
+    t0 = time.time()
+    st = lib.gqa_decode_debug_skip_tile(
+        t["q"].data_ptr(), 0, t["kv"].data_ptr(), 0, t["lens"].data_ptr(), p.out.data_ptr(), 1, 1024,
+        1.0, 1.0, 1.0, 2, p.workspace.data_ptr(), p.workspace_bytes, 3, 100_000_000, stream)
+    assert st == 0, lib.gqa_last_error().decode()
+    flags = gq.get_status(p)  # synchronises
+    assert flags & api.FLAG_WAIT_TIMEOUT
+    assert time.time() - t0 < 10.0
+    gq.launch(p)
+    torch.cuda.synchronize()
+    assert gq.get_status(p) == 0
+    _assert_parity(_gpu_rows(p.out), _oracle_full(t), "after a timed-out launch")
+
+
+
+# ------------------------------------------------------------- paged cache
+
+
+def _paged(pt, out=None, num_splits=None):
+    w = pt["workload"]
+    fp8 = w.kv_dtype == "e4m3"
+    return gq.gqa_decode_paged(pt["q"], pt["kv_pages"], pt["block_table"], pt["lens"],
+                               q_scale=pt["q_scale"], k_scale=pt["k_scale"] if fp8 else 1.0,
+                               v_scale=pt["v_scale"] if fp8 else 1.0, out=out, num_splits=num_splits)
+
+
+@pytest.mark.parametrize("kv_dtype", ["f16", "bf16", "e4m3"])
+@pytest.mark.parametrize("page_size", [16, 64, 256])
+def test_paged_matches_oracle_and_contiguous_path(kv_dtype, page_size):
+    w = inputs.custom(5, 1024, 1, 1024, kv_dtype=kv_dtype, kv_std=2.0 if kv_dtype == "e4m3" else 1.0,
+                      nan_tail=True)
+    t = _make(w, lens=[1, 17, 300, 1000, 1024])
+    pt = inputs.paginate(t, page_size, extra_pages=5, seed=page_size)
+    for S in (None, 3):
+        out = _paged(pt, num_splits=S)
+        torch.cuda.synchronize()
+        contiguous = _run(t, num_splits=S).out
+        assert torch.equal(out.view(torch.int16), contiguous.view(torch.int16))
+        g = oracle.gather_pages(bits_of(pt["kv_pages"]), pt["block_table"].cpu().numpy(),
+                                t["lens"].cpu().numpy())
+        ref, _ = oracle.gqa_decode(bits_of(t["q"]), FMT[w.q_dtype], g, FMT[kv_dtype], t["lens"].cpu().numpy(),
+                                   q_scale=t["q_scale"], k_scale=t["k_scale"], v_scale=t["v_scale"])
+        _assert_parity(_gpu_rows(out), ref, f"paged {kv_dtype} page {page_size} splits {S}")
+
+
+def test_paged_out_of_range_page_ids_are_clamped_and_flagged():
+    t = _make(inputs.custom(2, 512, 512))
+    pt = inputs.paginate(t, 64, extra_pages=2)
+    pt["block_table"][1, 3] = pt["num_pages"] + 10  # a used entry points outside the pool
+    B, C, S = 2, 512, 2
+    ws = torch.zeros(gq.workspace_size(B, C, S), dtype=torch.uint8, device=DEV)
+    _paged_out = gq.gqa_decode_paged(pt["q"], pt["kv_pages"], pt["block_table"], pt["lens"],
+                                     num_splits=S, workspace=ws)
+    flags = gq.get_status(ws)
+    assert flags & api.FLAG_PAGE_CLAMPED and not flags & api.FLAG_WAIT_TIMEOUT
+    pt["block_table"][1, 3] = -4
+    gq.gqa_decode_paged(pt["q"], pt["kv_pages"], pt["block_table"], pt["lens"], num_splits=S, workspace=ws)
+    assert gq.get_status(ws) & api.FLAG_PAGE_CLAMPED
+
+
+def test_paged_full_size_bitwise_equals_contiguous():
+    t = _make(inputs.WORKLOADS[4])
+    contiguous = _run(t).out.clone()
+    pt = inputs.paginate(t, 256, extra_pages=7)
+    del t["kv"]
+    out = _paged(pt)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), contiguous.view(torch.int16))

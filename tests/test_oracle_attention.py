@@ -23,7 +23,7 @@ from gqa_decode_attention_sm_gb300 import inputs
 from helpers import D, HKV, HQ, bits_of, f16_bits, bf16_bits, sdpa_f64, values_of_bits
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "worked_examples.json")
-FMT = {"f16": oracle.F16, "bf16": oracle.BF16, "e4m3": oracle.E4M3}
+FMT = {"f16": oracle.F16, "bf16": oracle.BF16, "e4m3": oracle.E4M3, "i8": oracle.I8}
 
 
 def _to_bits(vals, fmt):
@@ -48,6 +48,8 @@ def _random(w, seed=None):
 def _run(lib, t, qb, kvb, lens, **kw):
     w = t["workload"]
     args = dict(q_scale=t["q_scale"], k_scale=t["k_scale"], v_scale=t["v_scale"])
+    if t.get("kv_scales") is not None:
+        args["kv_scales"] = bits_of(t["kv_scales"])
     args.update(kw)
     return oracle.gqa_decode(qb, FMT[w.q_dtype], kvb, FMT[w.kv_dtype], lens, lib=lib, **args)
 
@@ -223,6 +225,8 @@ def _check_sdpa(orc, t, qb, kvb, lens, rows=None, **kw):
     out, bits = _run(orc, t, qb, kvb, lens, rows=rows, **kw)
     qv = values_of_bits(qb, w.q_dtype)
     kvv = values_of_bits(kvb, w.kv_dtype)
+    if w.kv_dtype == "i8":  # dequantise: code x the bf16 scale of its row
+        kvv = kvv * t["kv_scales"].to(torch.float64).numpy()[..., None]
     args = dict(q_scale=t["q_scale"], k_scale=t["k_scale"], v_scale=t["v_scale"])
     args.update(kw)
     ref = sdpa_f64(qv, kvv[:, 0], kvv[:, 1], lens, rows=rows, **args)
@@ -254,3 +258,62 @@ def test_matches_torch_sdpa_fp8_with_distinct_scales(orc):
     t, qb, kvb, lens = _random(w)
     _check_sdpa(orc, t, qb, kvb, lens, q_scale=1.0, k_scale=t["k_scale"] * 0.5,
                 v_scale=t["v_scale"] * 3.0)
+
+
+# ------------------------------------------------------------ INT8 cache
+
+
+def test_int8_length_one_returns_scaled_first_row(orc):
+    w = inputs.custom(3, 16, 1, kv_dtype="i8", nan_tail=True)
+    t, qb, kvb, lens = _random(w)
+    out, _ = _run(orc, t, qb, kvb, lens)
+    codes = kvb.view(np.int8).astype(np.float64)
+    scales = t["kv_scales"].to(torch.float64).numpy()
+    for r in range(3 * HQ):
+        b, h = divmod(r, HQ)
+        assert np.array_equal(out[r], codes[b, 1, h // 4, 0] * scales[b, 1, h // 4, 0])
+
+
+def test_int8_matches_torch_sdpa_on_dequantised_rows(orc):
+    w = inputs.custom(3, 200, 50, 200, kv_dtype="i8", nan_tail=True)
+    t, qb, kvb, lens = _random(w)
+    _check_sdpa(orc, t, qb, kvb, lens)
+
+
+def test_int8_scales_act_per_row(orc):
+    # codes c with row scale s, or codes 2c with row scale s/2: the same values,
+    # so the same output (exactly); a different scale on one V row changes it
+    rng = np.random.default_rng(21)
+    B, C, L = 1, 24, 20
+    t = inputs.make(inputs.custom(B, C, L, kv_dtype="i8"), "cpu")
+    codes = rng.integers(-63, 64, (B, 2, 8, C, 128)).astype(np.int8)
+    scales = np.exp2(rng.integers(-8, -2, (B, 2, 8, C))).astype(np.float32)
+    qb = bits_of(t["q"])
+    lens = np.array([L], np.int32)
+
+    def run(c, s):
+        return oracle.gqa_decode(qb, oracle.BF16, c.view(np.uint8), oracle.I8, lens, lib=orc,
+                                 kv_scales=bf16_bits(s))[0]
+
+    a = run(codes, scales)
+    b = run((codes.astype(np.int16) * 2).astype(np.int8), scales / 2)
+    assert np.array_equal(a, b)
+    s2 = scales.copy()
+    s2[0, 1, :, 3] *= 2
+    assert not np.allclose(run(codes, s2), a, rtol=1e-9)
+
+
+# ------------------------------------------------------------- paged cache
+
+
+@pytest.mark.parametrize("page_size", [16, 64])
+def test_paged_gather_reproduces_the_contiguous_cache(orc, page_size):
+    w = inputs.custom(3, 256, 1, 256, nan_tail=True)
+    t, qb, kvb, lens = _random(w, seed=5)
+    pt = inputs.paginate(t, page_size, extra_pages=4, seed=9)
+    g = oracle.gather_pages(bits_of(pt["kv_pages"]), pt["block_table"].numpy(), lens)
+    for b in range(3):  # every slot below the length comes back in place
+        assert np.array_equal(g[b, :, :, :lens[b]], kvb[b, :, :, :lens[b]])
+    a, _ = _run(orc, t, qb, kvb, lens)
+    c, _ = _run(orc, t, qb, g, lens)
+    assert np.array_equal(a, c)

@@ -25,11 +25,19 @@ MUTANTS = {
     "scale times sqrt(d)": ("j->q_scale / sqrt((double)ORC_D)", "j->q_scale * sqrt((double)ORC_D)"),
     "softmax sign flipped": ("double w = exp(s[t] - m);", "double w = exp(m - s[t]);"),
     "no max subtraction": ("double w = exp(s[t] - m);", "double w = exp(s[t]);"),
-    "score pass reads one slot too many": ("for (int t = 0; t < L; ++t) {\n    double dot",
-                                           "for (int t = 0; t <= L; ++t) {\n    double dot"),
+    "score pass reads slot L when it exists": (
+        "for (int t = 0; t < L; ++t) {\n    const double row_k",
+        "for (int t = 0; t < L + (L < j->capacity); ++t) {\n    const double row_k"),
     "value pass drops the last slot": ("for (int t = 0; t < L; ++t) {\n    double w",
                                        "for (int t = 0; t < L - 1; ++t) {\n    double w"),
-    "K and V planes swapped": ("(((size_t)b * 2 + 0) * ORC_HKV + g)", "(((size_t)b * 2 + 1) * ORC_HKV + g)"),
+    "K and V planes swapped": ("(((size_t)b * 2 + 0) * ORC_HKV + g) * C * ORC_D",
+                               "(((size_t)b * 2 + 1) * ORC_HKV + g) * C * ORC_D"),
+    "int8 K rows scaled by the V-plane scale": ("const size_t ks_off = (((size_t)b * 2 + 0)",
+                                                "const size_t ks_off = (((size_t)b * 2 + 1)"),
+    "int8 scale of the next row": ("orc_decode_bf16(j->kv_scales[vs_off + t])",
+                                   "orc_decode_bf16(j->kv_scales[vs_off + (t + 1) % L])"),
+    "int8 codes read as unsigned": ("if (type == ORC_I8) return (double)((const int8_t*)base)[i];",
+                                    "if (type == ORC_I8) return (double)((const uint8_t*)base)[i];"),
     "k_scale applied to V": ("* j->v_scale;\n      acc", "* j->k_scale;\n      acc"),
     "v_scale dropped": ("* j->v_scale;\n      acc", ";\n      acc"),
     "f16 exponent bias off by one": ("ldexp((double)(1024 + m), e - 25)", "ldexp((double)(1024 + m), e - 24)"),
@@ -58,6 +66,9 @@ PINS = [
     F.test_decode_e4m3_all_patterns,
     F.test_round_f16_matches_numpy_single_step,
     F.test_round_exact_ties_to_even,
+    A.test_int8_length_one_returns_scaled_first_row,
+    A.test_int8_matches_torch_sdpa_on_dequantised_rows,
+    A.test_int8_scales_act_per_row,
 ]
 
 
