@@ -6,8 +6,8 @@ Importing the package does not load the library; the first call does, and
 raises if the library has not been built (there is no fallback path).
 """
 from .api import (GqaError, Prepared, combine_stage, get_status, gqa_decode, gqa_decode_fp8kv,
-                  gqa_decode_int8kv, gqa_decode_paged, launch, plan, prepare, split_stage,
+                  gqa_decode_int8kv, gqa_decode_paged, gqa_decode_verify, launch, plan, prepare, split_stage,
                   workspace_size)
 
 __all__ = ["GqaError", "Prepared", "combine_stage", "get_status", "gqa_decode", "gqa_decode_fp8kv",
-           "gqa_decode_int8kv", "gqa_decode_paged", "launch", "plan", "prepare", "split_stage", "workspace_size"]
+           "gqa_decode_int8kv", "gqa_decode_paged", "gqa_decode_verify", "launch", "plan", "prepare", "split_stage", "workspace_size"]

@@ -33,6 +33,7 @@ _KVF = {torch.float16: KV_F16, torch.bfloat16: KV_BF16, torch.uint8: KV_E4M3,
         torch.float8_e4m3fn: KV_E4M3, torch.int8: KV_I8}
 
 __all__ = ["GqaError", "gqa_decode", "gqa_decode_fp8kv", "gqa_decode_int8kv", "gqa_decode_paged",
+           "gqa_decode_verify",
            "prepare", "launch",
            "Prepared",
            "workspace_size", "plan", "get_status", "split_stage", "combine_stage", "split_geometry"]
@@ -299,6 +300,38 @@ def gqa_decode_paged(q, kv_pages, block_table, sequence_lengths, q_scale: float 
             _ptr(q), _QDT[q.dtype], _ptr(kv_pages), kvf, _ptr(block_table), max_pages, num_pages,
             page_size, _ptr(sequence_lengths), _ptr(out), B, float(q_scale), float(k_scale),
             float(v_scale), S, _ptr(workspace), workspace.numel(), _stream(q.device)))
+    return out
+
+
+def gqa_decode_verify(q, kv, sequence_lengths, q_scale: float = 1.0, k_scale: float = 1.0,
+                      v_scale: float = 1.0, kv_scales=None, out=None, num_splits=None, workspace=None):
+    """Verify window: q [batch, T, 32, 128] (T = 1..4 draft tokens, the last T slots
+    of each cache row); query j attends slots [0, len - T + j].  Any KV format
+    (int8 needs kv_scales).  Returns out [batch, T, 32, 128]."""
+    _require(q, "q", None, (torch.float16, torch.bfloat16))
+    if q.dim() != 4 or q.shape[2:] != (HQ, D):
+        raise ValueError(f"q must be [batch, T, {HQ}, {D}], got {tuple(q.shape)}")
+    B, T = q.shape[0], q.shape[1]
+    if kv.dim() != 5 or kv.shape[0] != B or kv.shape[1:3] != (2, HKV) or kv.shape[4] != D:
+        raise ValueError(f"kv must be [{B}, 2, {HKV}, capacity, {D}]")
+    C = kv.shape[3]
+    _require(kv, "kv", None, tuple(_KVF), q.device)
+    _require(sequence_lengths, "sequence_lengths", (B,), (torch.int32,), q.device)
+    kvf = _KVF[kv.dtype]
+    if kvf == KV_I8:
+        _require(kv_scales, "kv_scales", (B, 2, HKV, C), (torch.bfloat16,), q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    _require(out, "out", q.shape, (q.dtype,), q.device)
+    S = plan(B, C, kvf, q.device) if not num_splits else int(num_splits)
+    nbytes = workspace_size(B * T, C, S)
+    if workspace is None:
+        workspace = torch.zeros(nbytes, dtype=torch.uint8, device=q.device)
+    with torch.cuda.device(q.device):
+        _lib.check(_lib.load().gqa_decode_verify(
+            _ptr(q), _QDT[q.dtype], _ptr(kv), kvf, _ptr(kv_scales) if kvf == KV_I8 else None,
+            _ptr(sequence_lengths), _ptr(out), B, C, T, float(q_scale), float(k_scale), float(v_scale), S,
+            _ptr(workspace), workspace.numel(), _stream(q.device)))
     return out
 
 

@@ -55,8 +55,15 @@ DeviceState g_devices[kMaxDevices];
 
 template <int KVF, int QF>
 cudaError_t set_split_attributes() {
-  return cudaFuncSetAttribute(split_kv_mma_kernel<KVF, QF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kMmaSmemBytes);
+  cudaError_t e = cudaSuccess;
+  const auto set = [&](auto kernel) {
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmaSmemBytes);
+  };
+  set(split_kv_mma_kernel<KVF, QF, 1>);
+  set(split_kv_mma_kernel<KVF, QF, 2>);
+  set(split_kv_mma_kernel<KVF, QF, 3>);
+  set(split_kv_mma_kernel<KVF, QF, 4>);
+  return e;
 }
 
 // One-time per-device check (compute capability 10.3) and opt-in to the
@@ -157,6 +164,7 @@ struct Call {
   const uint16_t* kv_scales = nullptr;  // int8 cache only
   const int32_t* block_table = nullptr;  // paged cache only
   int page_log2 = 0, max_pages = 0, num_pages = 0;
+  int q_len = 1;  // query tokens per request (verify window)
 };
 
 gqa_status_t validate_shape(int batch, int capacity) {
@@ -191,10 +199,10 @@ gqa_status_t validate(const Call& c, bool q_scale_positive, bool need_q) {
   if ((need_q && !aligned(c.q, 16)) || !aligned(c.kv, 16) || !aligned(c.out, 16) ||
       !aligned(c.workspace, 16) || !aligned(c.lens, 4))
     return fail(GQA_ERR_INVALID_ARGUMENT, "q, kv, out, workspace must be 16-byte aligned, lens 4-byte");
-  const size_t need = workspace_bytes_for(c.batch, c.num_splits);
+  const size_t need = workspace_bytes_for(c.batch * c.q_len, c.num_splits);
   if (c.workspace_bytes < need)
     return fail(GQA_ERR_WORKSPACE_TOO_SMALL, "workspace has %zu bytes, needs %zu", c.workspace_bytes, need);
-  const size_t qo_bytes = (size_t)c.batch * kHq * kD * 2;
+  const size_t qo_bytes = (size_t)c.batch * c.q_len * kHq * kD * 2;
   const size_t kv_bytes =
       c.block_table ? (size_t)c.num_pages * 2 * kHkv * ((size_t)1 << c.page_log2) * kD * kv_elem_bytes(c.kv_format)
                     : (size_t)c.batch * 2 * kHkv * (size_t)c.capacity * kD * kv_elem_bytes(c.kv_format);
@@ -265,19 +273,24 @@ int plan_splits(int batch, int capacity, int kv_format, int sm_count) {
 // ---------------------------------------------------------------- launches
 
 template <int KVF, int QF>
-cudaError_t launch_split_t(const SplitParams& sp, cudaStream_t stream) {
+cudaError_t launch_split_t(const SplitParams& sp, int q_len, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(sp.splits_eff, kHkv, sp.batch);
   cfg.blockDim = dim3(kMmaThreads, 1, 1);
   cfg.dynamicSmemBytes = kMmaSmemBytes;
   cfg.stream = stream;
-  return cudaLaunchKernelEx(&cfg, split_kv_mma_kernel<KVF, QF>, sp);
+  switch (q_len) {
+    case 1: return cudaLaunchKernelEx(&cfg, split_kv_mma_kernel<KVF, QF, 1>, sp);
+    case 2: return cudaLaunchKernelEx(&cfg, split_kv_mma_kernel<KVF, QF, 2>, sp);
+    case 3: return cudaLaunchKernelEx(&cfg, split_kv_mma_kernel<KVF, QF, 3>, sp);
+    default: return cudaLaunchKernelEx(&cfg, split_kv_mma_kernel<KVF, QF, 4>, sp);
+  }
 }
 
 template <int QF>
-cudaError_t launch_combine_t(const CombineParams& cp, int batch, cudaStream_t stream) {
+cudaError_t launch_combine_t(const CombineParams& cp, int batch_rows, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(kHkv, batch, 1);
+  cfg.gridDim = dim3(kHkv, batch_rows, 1);
   cfg.blockDim = dim3(kCombineThreads, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
@@ -312,7 +325,7 @@ Layout layout_of(void* ws, int batch, int splits) {
 }
 
 gqa_status_t run_split(const Call& c) {
-  const Layout lay = layout_of(c.workspace, c.batch, c.num_splits);
+  const Layout lay = layout_of(c.workspace, c.batch * c.q_len, c.num_splits);
   SplitParams sp;
   sp.q = c.q;
   sp.kv = c.kv;
@@ -338,14 +351,15 @@ gqa_status_t run_split(const Call& c) {
   sp.max_pages = c.max_pages;
   sp.num_pages = c.num_pages;
   cudaError_t e;
-  if (c.kv_format == kKvF16) e = launch_split_t<kKvF16, kQF16>(sp, c.stream);
-  else if (c.kv_format == kKvBF16) e = launch_split_t<kKvBF16, kQBF16>(sp, c.stream);
+  const int ql = c.q_len;
+  if (c.kv_format == kKvF16) e = launch_split_t<kKvF16, kQF16>(sp, ql, c.stream);
+  else if (c.kv_format == kKvBF16) e = launch_split_t<kKvBF16, kQBF16>(sp, ql, c.stream);
   else if (c.kv_format == kKvE4M3)
-    e = c.q_dtype == GQA_BF16 ? launch_split_t<kKvE4M3, kQBF16>(sp, c.stream)
-                              : launch_split_t<kKvE4M3, kQF16>(sp, c.stream);
+    e = c.q_dtype == GQA_BF16 ? launch_split_t<kKvE4M3, kQBF16>(sp, ql, c.stream)
+                              : launch_split_t<kKvE4M3, kQF16>(sp, ql, c.stream);
   else
-    e = c.q_dtype == GQA_BF16 ? launch_split_t<kKvI8, kQBF16>(sp, c.stream)
-                              : launch_split_t<kKvI8, kQF16>(sp, c.stream);
+    e = c.q_dtype == GQA_BF16 ? launch_split_t<kKvI8, kQBF16>(sp, ql, c.stream)
+                              : launch_split_t<kKvI8, kQF16>(sp, ql, c.stream);
   if (e != cudaSuccess) return cuda_fail(e, "split kernel launch");
   return GQA_OK;
 }
@@ -353,7 +367,7 @@ gqa_status_t run_split(const Call& c) {
 gqa_status_t run_combine(const Call& c) {
   const int splits_eff = split_count(c.capacity, c.num_splits, c.kv_format);
   if (splits_eff == 1) return GQA_OK;
-  const Layout lay = layout_of(c.workspace, c.batch, c.num_splits);
+  const Layout lay = layout_of(c.workspace, c.batch * c.q_len, c.num_splits);
   CombineParams cp;
   cp.lens = c.lens;
   cp.out = c.out;
@@ -363,9 +377,10 @@ gqa_status_t run_combine(const Call& c) {
   cp.capacity = c.capacity;
   cp.num_splits = c.num_splits;
   cp.chunk = split_chunk(c.capacity, c.num_splits, c.kv_format);
+  cp.q_len = c.q_len;
   cp.v_scale = c.v_scale;
-  cudaError_t e = c.q_dtype == GQA_F16 ? launch_combine_t<kQF16>(cp, c.batch, c.stream)
-                                       : launch_combine_t<kQBF16>(cp, c.batch, c.stream);
+  cudaError_t e = c.q_dtype == GQA_F16 ? launch_combine_t<kQF16>(cp, c.batch * c.q_len, c.stream)
+                                       : launch_combine_t<kQBF16>(cp, c.batch * c.q_len, c.stream);
   if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
   return GQA_OK;
 }
@@ -515,6 +530,23 @@ gqa_status_t gqa_decode_paged(const void* q, gqa_dtype_t q_dtype, const void* kv
   int lg = 0;
   while ((1 << lg) < page_size) ++lg;
   c.page_log2 = lg;
+  gqa_status_t st = prepare_call(c, false, true);
+  if (st != GQA_OK) return st;
+  st = run_split(c);
+  if (st != GQA_OK) return st;
+  return run_combine(c);
+}
+
+gqa_status_t gqa_decode_verify(const void* q, gqa_dtype_t q_dtype, const void* kv, gqa_kv_format_t kv_format,
+                               const uint16_t* kv_scales_bf16, const int32_t* lens, void* out, int batch,
+                               int capacity, int q_len, float q_scale, float k_scale, float v_scale,
+                               int num_splits, void* workspace, size_t workspace_bytes, void* stream) {
+  if (q_len < 1 || q_len > kMaxQLen)
+    return fail(GQA_ERR_INVALID_ARGUMENT, "q_len %d outside [1, %d]", q_len, kMaxQLen);
+  Call c{q, (int)q_dtype, kv, (int)kv_format, lens, out, batch, capacity, q_scale, k_scale, v_scale,
+         num_splits, workspace, workspace_bytes, static_cast<cudaStream_t>(stream)};
+  c.q_len = q_len;
+  c.kv_scales = kv_scales_bf16;
   gqa_status_t st = prepare_call(c, false, true);
   if (st != GQA_OK) return st;
   st = run_split(c);

@@ -26,17 +26,19 @@ struct CombineParams {
   const float* part_m;
   const float* part_l;
   int capacity, num_splits, chunk;
+  int q_len;  // rows are (b * q_len + j, head); query j attends len - q_len + 1 + j slots
   float v_scale;
 };
 
 template <int QF>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_constant__ CombineParams p) {
-  const int g = blockIdx.x, b = blockIdx.y;
+  const int g = blockIdx.x, bq = blockIdx.y;  // bq = b * q_len + query token
+  const int b = bq / p.q_len, jq = bq % p.q_len;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = g * kGroup + warp;
-  const int L = min(max(__ldg(p.lens + b), 0), p.capacity);
-  const int n = (L + p.chunk - 1) / p.chunk;
-  const size_t base = (size_t)(b * kHq + h) * p.num_splits;
+  const int L = min(max(__ldg(p.lens + b), 0), p.capacity) - p.q_len + 1 + jq;
+  const int n = L > 0 ? (L + p.chunk - 1) / p.chunk : 0;
+  const size_t base = (size_t)(bq * kHq + h) * p.num_splits;
   // launched as a programmatic dependent of stage 1: wait for its partials
   pdl_wait_prior_grid();
 
@@ -82,7 +84,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
     const __nv_bfloat162 c = __floats2bfloat162_rn(o.z * inv, o.w * inv);
     packed = make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&c));
   }
-  *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) + ((size_t)(b * kHq + h) * kD + 4 * lane) * 2) =
+  *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) + ((size_t)(bq * kHq + h) * kD + 4 * lane) * 2) =
       packed;
 }
 

@@ -60,6 +60,8 @@ struct SplitParams {
   float* part_l;          // [B,32,S]  softmax denominator
   uint32_t* flags;        // workspace status word
   int batch, capacity, num_splits, chunk, splits_eff;
+  // q and out are [B, q_len, 32, 128]; query j attends slots [0, len - q_len + j]
+  // (q_len = 1: plain decode); partials are indexed by (b * q_len + j, head)
   float scale_log2;       // q_scale * k_scale * log2(e) / sqrt(128)
   float v_scale;
   uint64_t wait_budget_ns;  // every pipeline wait gives up after this long
@@ -84,10 +86,13 @@ __device__ __forceinline__ uint32_t pack_out(float a, float b) {
 constexpr int kMmaConsumerWarps = 4;
 constexpr int kMmaThreads = (kMmaConsumerWarps + 1) * 32;
 constexpr int kMmaStages = 3;
-constexpr int kMmaMergeBytes = kMmaConsumerWarps * kGroup * kD * 4 + 2 * kMmaConsumerWarps * kGroup * 4;
+constexpr int kMaxQLen = 4;  // query tokens per request (a verify window when > 1)
 constexpr int kScaleStageBytes = 2 * 128 * 2;  // int8 cache: K and V row scales of one 128-token tile
-constexpr int kMmaSmemBytes =
-    kMmaStages * kStageBytes + kMmaMergeBytes + kMmaStages * kScaleStageBytes + 2 * kMmaStages * 8;
+constexpr int kMmaSmemBytes = kMmaStages * kStageBytes + kMmaStages * kScaleStageBytes + 2 * kMmaStages * 8;
+// The epilogue merges the 4 warps' states in the ring (idle by then):
+// [warp][column][128] accumulators + [warp][column] max and denominator.
+static_assert(kMmaConsumerWarps * kGroup * kMaxQLen * (kD + 2) * 4 <= kMmaStages * kStageBytes,
+              "merge area must fit in the ring");
 
 // ---------------------------------------------------------------- mma.sync
 
@@ -165,19 +170,21 @@ __device__ __forceinline__ int qk_dim(int cq, int ks, int pair /*0: a0/b0, 1: a2
   else return 8 * (cq + 4 * (ks >> 1)) + 4 * (ks & 1) + 2 * pair;
 }
 
-template <int KVF, int QF>
+template <int KVF, int QF, int NQ>
 __global__ void __launch_bounds__(kMmaThreads, 2) split_kv_mma_kernel(const __grid_constant__ SplitParams p) {
   using T = KvTraits<KVF>;
   constexpr bool kBF16 = kMmaBF16<KVF>;
   constexpr int kSlabs = T::kTile / (16 * kMmaConsumerWarps);  // 16-token slabs per warp per tile
+  constexpr int kCols = kGroup * NQ;                            // (query token, head) columns
+  constexpr int kNT = (kCols + 7) / 8;                          // 8-column mma n-tiles
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem;
-  float* mrg_acc = reinterpret_cast<float*>(smem + kMmaStages * kStageBytes);  // [4 warps][4 heads][128]
-  float* mrg_m = mrg_acc + kMmaConsumerWarps * kGroup * kD;                      // [4][4]
-  float* mrg_l = mrg_m + kMmaConsumerWarps * kGroup;                             // [4][4]
-  uint16_t* scl = reinterpret_cast<uint16_t*>(mrg_l + kMmaConsumerWarps * kGroup);  // [stage][K|V][128]
+  uint16_t* scl = reinterpret_cast<uint16_t*>(smem + kMmaStages * kStageBytes);  // [stage][K|V][128]
   uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(scl) + kMmaStages * kScaleStageBytes);
   uint64_t* empty = full + kMmaStages;
+  float* mrg_acc = reinterpret_cast<float*>(ring);                    // [4 warps][kCols][128] (epilogue)
+  float* mrg_m = mrg_acc + kMmaConsumerWarps * kCols * kD;           // [4][kCols]
+  float* mrg_l = mrg_m + kMmaConsumerWarps * kCols;                  // [4][kCols]
 
   // Every CTA of this grid is resident or done: let stage 2 be scheduled
   // (it waits for this grid's completion before reading the partials).
@@ -186,7 +193,7 @@ __global__ void __launch_bounds__(kMmaThreads, 2) split_kv_mma_kernel(const __gr
   const int C = p.capacity;
   const int len_raw = __ldg(p.lens + b);
   const int L = min(max(len_raw, 0), C);
-  if (s == 0 && g == 0 && threadIdx.x == 0 && (len_raw < 1 || len_raw > C))
+  if (s == 0 && g == 0 && threadIdx.x == 0 && (len_raw < NQ || len_raw > C))
     atomicOr(p.flags, GQA_FLAG_LENGTH_CLAMPED);
   const int t_begin = s * p.chunk;
   const int t_end = min(L, t_begin + p.chunk);
@@ -194,9 +201,12 @@ __global__ void __launch_bounds__(kMmaThreads, 2) split_kv_mma_kernel(const __gr
   if (t_begin >= t_end) {
     if (p.splits_eff == 1 && threadIdx.x < kMmaConsumerWarps * 32) {
       // one-split launch with length 0: the output rows are zero
-      const int j = threadIdx.x / 32, d0 = 4 * (threadIdx.x % 32);
-      *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) +
-                                ((size_t)(b * kHq + g * kGroup + j) * kD + d0) * 2) = make_uint2(0u, 0u);
+      const int hh = threadIdx.x / 32, d0 = 4 * (threadIdx.x % 32);
+#pragma unroll
+      for (int jq = 0; jq < NQ; ++jq)
+        *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) +
+                                  ((size_t)((b * NQ + jq) * kHq + g * kGroup + hh) * kD + d0) * 2) =
+            make_uint2(0u, 0u);
     }
     return;
   }
@@ -309,12 +319,24 @@ __global__ void __launch_bounds__(kMmaThreads, 2) split_kv_mma_kernel(const __gr
 
   // -------------------------------------------------------------- consumers
   const int gq = lane >> 2, cq = lane & 3;
-  const bool real_heads = cq < 2;  // score/output columns 2cq, 2cq+1 are query heads 0..3
+  // Column n of n-tile nt is (query token 2nt + n/4, head n%4).  This lane's
+  // score/output columns are n = 2cq, 2cq+1: query token 2nt + cq/2, heads
+  // 2(cq%2) and 2(cq%2)+1.  A column past the window is zero padding.
+  int lim[kNT];  // slots below lim[nt] are attended by this lane's columns
+#pragma unroll
+  for (int nt = 0; nt < kNT; ++nt) {
+    const int jq = 2 * nt + (cq >> 1);
+    lim[nt] = jq < NQ ? min(t_end, L - NQ + 1 + jq) : 0;
+  }
 
-  // Q^T B-fragments (head gq; zero for the padding heads gq >= 4), unscaled.
-  uint32_t qb[8][2];
-  {
-    const uint16_t* qrow = static_cast<const uint16_t*>(p.q) + ((size_t)b * kHq + g * kGroup + (gq & 3)) * kD;
+  // Q^T B-fragments: column gq of each n-tile, unscaled (zero for padding).
+  uint32_t qb[kNT][8][2];
+#pragma unroll
+  for (int nt = 0; nt < kNT; ++nt) {
+    const int jq = 2 * nt + (gq >> 2);
+    const bool real = jq < NQ;
+    const uint16_t* qrow = static_cast<const uint16_t*>(p.q) +
+                           ((size_t)((b * NQ + (real ? jq : 0)) * kHq) + g * kGroup + (gq & 3)) * kD;
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks)
 #pragma unroll
@@ -322,19 +344,23 @@ __global__ void __launch_bounds__(kMmaThreads, 2) split_kv_mma_kernel(const __gr
         const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(qrow + qk_dim<KVF>(cq, ks, pr)));
         uint32_t v = w;
         if constexpr (is_8bit(KVF) && QF == kQBF16) v = pack_f16_satfinite(bf16_lo_to_f32(w), bf16_hi_to_f32(w));
-        qb[ks][pr] = gq < kGroup ? v : 0u;
+        qb[nt][ks][pr] = real ? v : 0u;
       }
   }
 
-  float o[8][4];
+  float o[kNT][8][4];
+  float m[kNT][2], l[kNT][2];  // per column: running max (log2 domain), this lane's denominator share
 #pragma unroll
-  for (int mt = 0; mt < 8; ++mt)
+  for (int nt = 0; nt < kNT; ++nt) {
+    m[nt][0] = m[nt][1] = -INFINITY;
+    l[nt][0] = l[nt][1] = 0.f;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) o[mt][e] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY;  // running max of heads 2cq, 2cq+1 (log2 domain)
-  float l0 = 0.f, l1 = 0.f;              // this lane's share of the denominators
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[nt][mt][e] = 0.f;
+  }
   const float sl2 = p.scale_log2;
-  // P^T shuffle sources: tokens 2cq and 2cq+1 of the slab, head pair gq/2
+  // P^T shuffle sources: tokens 2cq and 2cq+1 of the slab, column pair gq/2
   const int src0 = 4 * (2 * cq) + (gq >> 1), src1 = 4 * (2 * cq + 1) + (gq >> 1);
   const uint32_t half_sel = (gq & 1) ? 0x7632u : 0x5410u;
 
@@ -346,7 +372,8 @@ __global__ void __launch_bounds__(kMmaThreads, 2) split_kv_mma_kernel(const __gr
     }
     const uint8_t* sK = ring + st * kStageBytes;
     const uint8_t* sV = sK + T::kTileBytes;
-    const int rows = min(T::kTile, t_end - (t_begin + i * T::kTile));
+    const int tile_t0 = t_begin + i * T::kTile;
+    const int rows = min(T::kTile, t_end - tile_t0);
     // int8: K and V row scales of this lane's tokens (R+gq, R+gq+8 of each slab)
     float sk[kSlabs][2], sv[kSlabs][2];
     if constexpr (KVF == kKvI8) {
@@ -367,8 +394,10 @@ __global__ void __launch_bounds__(kMmaThreads, 2) split_kv_mma_kernel(const __gr
       if (R >= rows) break;                     // warp-uniform
       const bool partial = R + 16 > rows;
 
-      // ---- scores: S^T[16 tokens x 8] = K . Q^T
-      float sc[4] = {0.f, 0.f, 0.f, 0.f};
+      // ---- scores: S^T[16 tokens x 8] = K . Q^T for each n-tile
+      float sc[kNT][4];
+#pragma unroll
+      for (int nt = 0; nt < kNT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
       {
         const uint8_t* k0 = sK + (R + gq) * T::kRowBytes;
         const uint8_t* k1 = k0 + 8 * T::kRowBytes;
@@ -384,7 +413,8 @@ __global__ void __launch_bounds__(kMmaThreads, 2) split_kv_mma_kernel(const __gr
               uint32_t a0, a1, a2, a3;
               widen4<KVF>(xs[s4], a0, a2);  // row gq: dims (4s,4s+1), (4s+2,4s+3)
               widen4<KVF>(ys[s4], a1, a3);  // row gq+8
-              mma16816<false>(sc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+#pragma unroll
+              for (int nt = 0; nt < kNT; ++nt) mma16816<false>(sc[nt], a0, a1, a2, a3, qb[nt][ks][0], qb[nt][ks][1]);
             }
           }
         } else {
@@ -392,84 +422,109 @@ __global__ void __launch_bounds__(kMmaThreads, 2) split_kv_mma_kernel(const __gr
           for (int ci = 0; ci < 4; ++ci) {
             const uint4 x = *reinterpret_cast<const uint4*>(k0 + 16 * (cq + 4 * ci));
             const uint4 y = *reinterpret_cast<const uint4*>(k1 + 16 * (cq + 4 * ci));
-            mma16816<kBF16>(sc, x.x, y.x, x.y, y.y, qb[2 * ci][0], qb[2 * ci][1]);
-            mma16816<kBF16>(sc, x.z, y.z, x.w, y.w, qb[2 * ci + 1][0], qb[2 * ci + 1][1]);
+#pragma unroll
+            for (int nt = 0; nt < kNT; ++nt) {
+              mma16816<kBF16>(sc[nt], x.x, y.x, x.y, y.y, qb[nt][2 * ci][0], qb[nt][2 * ci][1]);
+              mma16816<kBF16>(sc[nt], x.z, y.z, x.w, y.w, qb[nt][2 * ci + 1][0], qb[nt][2 * ci + 1][1]);
+            }
           }
         }
       }
-      // sc: [0] token R+gq head 2cq, [1] token R+gq head 2cq+1, [2]/[3] token R+gq+8
-      float x0 = sc[0] * sl2, x1 = sc[1] * sl2, x2 = sc[2] * sl2, x3 = sc[3] * sl2;
-      if constexpr (KVF == kKvI8) {  // per-row K scale multiplies that token's scores
-        x0 *= sk[sl][0];
-        x1 *= sk[sl][0];
-        x2 *= sk[sl][1];
-        x3 *= sk[sl][1];
-      }
-      if (!real_heads || R + gq >= rows) x0 = x1 = -INFINITY;      // select, never multiply
-      if (!real_heads || R + gq + 8 >= rows) x2 = x3 = -INFINITY;
-
-      // ---- online softmax per head (max over the slab's 16 tokens)
-      float h0 = fmaxf(x0, x2), h1 = fmaxf(x1, x3);
+      // sc[nt]: [0] token R+gq column 2cq, [1] token R+gq column 2cq+1, [2]/[3] token R+gq+8
+      const int ta = tile_t0 + R + gq, tb = ta + 8;
+      float x[kNT][4];
 #pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        h0 = fmaxf(h0, __shfl_xor_sync(0xffffffffu, h0, off));
-        h1 = fmaxf(h1, __shfl_xor_sync(0xffffffffu, h1, off));
-      }
-      const float n0 = fmaxf(m0, h0), n1 = fmaxf(m1, h1);
-      if (__any_sync(0xffffffffu, n0 > m0 || n1 > m1)) {
-        // 0 when the old max was -inf; 1 when unchanged (also covers -inf == -inf)
-        const float a0 = n0 == m0 ? 1.f : ex2(m0 - n0), a1 = n1 == m1 ? 1.f : ex2(m1 - n1);
-        l0 *= a0;
-        l1 *= a1;
+      for (int nt = 0; nt < kNT; ++nt) {
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          o[mt][0] *= a0;
-          o[mt][2] *= a0;
-          o[mt][1] *= a1;
-          o[mt][3] *= a1;
+        for (int e = 0; e < 4; ++e) x[nt][e] = sc[nt][e] * sl2;
+        if constexpr (KVF == kKvI8) {  // per-row K scale multiplies that token's scores
+          x[nt][0] *= sk[sl][0];
+          x[nt][1] *= sk[sl][0];
+          x[nt][2] *= sk[sl][1];
+          x[nt][3] *= sk[sl][1];
         }
-        m0 = n0;
-        m1 = n1;
-      }
-      const float p0 = x0 == -INFINITY ? 0.f : ex2(x0 - m0);
-      const float p1 = x1 == -INFINITY ? 0.f : ex2(x1 - m1);
-      const float p2 = x2 == -INFINITY ? 0.f : ex2(x2 - m0);
-      const float p3 = x3 == -INFINITY ? 0.f : ex2(x3 - m1);
-
-      // ---- P^T B-fragments: lane (gq, cq) needs head gq of tokens 2cq, 2cq+1 (b0)
-      // and 2cq+8, 2cq+9 (b1); they sit in lanes src0/src1 as (head pair) packs.
-      uint32_t bh0, bh1, bl0 = 0u, bl1 = 0u;
-      if constexpr (kBF16) {
-        const uint32_t ph_a = pack_bf16(p0, p1), ph_b = pack_bf16(p2, p3);
-        const uint32_t pl_a = pack_bf16(p0 - bf16_lo_to_f32(ph_a), p1 - bf16_hi_to_f32(ph_a));
-        const uint32_t pl_b = pack_bf16(p2 - bf16_lo_to_f32(ph_b), p3 - bf16_hi_to_f32(ph_b));
-        l0 += bf16_lo_to_f32(ph_a) + bf16_lo_to_f32(pl_a) + bf16_lo_to_f32(ph_b) + bf16_lo_to_f32(pl_b);
-        l1 += bf16_hi_to_f32(ph_a) + bf16_hi_to_f32(pl_a) + bf16_hi_to_f32(ph_b) + bf16_hi_to_f32(pl_b);
-        bh0 = prmt(__shfl_sync(0xffffffffu, ph_a, src0), __shfl_sync(0xffffffffu, ph_a, src1), half_sel);
-        bh1 = prmt(__shfl_sync(0xffffffffu, ph_b, src0), __shfl_sync(0xffffffffu, ph_b, src1), half_sel);
-        bl0 = prmt(__shfl_sync(0xffffffffu, pl_a, src0), __shfl_sync(0xffffffffu, pl_a, src1), half_sel);
-        bl1 = prmt(__shfl_sync(0xffffffffu, pl_b, src0), __shfl_sync(0xffffffffu, pl_b, src1), half_sel);
-      } else if constexpr (KVF == kKvI8) {
-        // the per-row V scale joins the weight of its token; the denominator
-        // keeps the unscaled weights
-        const uint32_t pa = pack_f16(p0 * sv[sl][0], p1 * sv[sl][0]);
-        const uint32_t pb = pack_f16(p2 * sv[sl][1], p3 * sv[sl][1]);
-        l0 += p0 + p2;
-        l1 += p1 + p3;
-        bh0 = prmt(__shfl_sync(0xffffffffu, pa, src0), __shfl_sync(0xffffffffu, pa, src1), half_sel);
-        bh1 = prmt(__shfl_sync(0xffffffffu, pb, src0), __shfl_sync(0xffffffffu, pb, src1), half_sel);
-      } else {
-        const uint32_t pa = pack_f16(p0, p1), pb = pack_f16(p2, p3);
-        // the denominator sums the same rounded weights the tensor core multiplies
-        const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&pa));
-        const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&pb));
-        l0 += fa.x + fb.x;
-        l1 += fa.y + fb.y;
-        bh0 = prmt(__shfl_sync(0xffffffffu, pa, src0), __shfl_sync(0xffffffffu, pa, src1), half_sel);
-        bh1 = prmt(__shfl_sync(0xffffffffu, pb, src0), __shfl_sync(0xffffffffu, pb, src1), half_sel);
+        if (ta >= lim[nt]) x[nt][0] = x[nt][1] = -INFINITY;  // select, never multiply
+        if (tb >= lim[nt]) x[nt][2] = x[nt][3] = -INFINITY;
       }
 
-      // ---- O^T[128 dims x 8] += V^T . P^T: lane (gq, cq) reads dims
+      // ---- online softmax per column (max over the slab's 16 tokens)
+      float nm[kNT][2];
+      bool grow = false;
+#pragma unroll
+      for (int nt = 0; nt < kNT; ++nt) {
+        float h0 = fmaxf(x[nt][0], x[nt][2]), h1 = fmaxf(x[nt][1], x[nt][3]);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          h0 = fmaxf(h0, __shfl_xor_sync(0xffffffffu, h0, off));
+          h1 = fmaxf(h1, __shfl_xor_sync(0xffffffffu, h1, off));
+        }
+        nm[nt][0] = fmaxf(m[nt][0], h0);
+        nm[nt][1] = fmaxf(m[nt][1], h1);
+        grow |= nm[nt][0] > m[nt][0] || nm[nt][1] > m[nt][1];
+      }
+      if (__any_sync(0xffffffffu, grow)) {
+#pragma unroll
+        for (int nt = 0; nt < kNT; ++nt) {
+          // 0 when the old max was -inf; 1 when unchanged (also covers -inf == -inf)
+          const float a0 = nm[nt][0] == m[nt][0] ? 1.f : ex2(m[nt][0] - nm[nt][0]);
+          const float a1 = nm[nt][1] == m[nt][1] ? 1.f : ex2(m[nt][1] - nm[nt][1]);
+          l[nt][0] *= a0;
+          l[nt][1] *= a1;
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            o[nt][mt][0] *= a0;
+            o[nt][mt][2] *= a0;
+            o[nt][mt][1] *= a1;
+            o[nt][mt][3] *= a1;
+          }
+          m[nt][0] = nm[nt][0];
+          m[nt][1] = nm[nt][1];
+        }
+      }
+
+      // ---- P^T B-fragments per n-tile: lane (gq, cq) needs column gq of tokens
+      // 2cq, 2cq+1 (b0) and 2cq+8, 2cq+9 (b1), held by lanes src0/src1 as
+      // (column pair) packs.
+      uint32_t bh[kNT][2], bl[kNT][2];
+#pragma unroll
+      for (int nt = 0; nt < kNT; ++nt) {
+        const float p0 = x[nt][0] == -INFINITY ? 0.f : ex2(x[nt][0] - m[nt][0]);
+        const float p1 = x[nt][1] == -INFINITY ? 0.f : ex2(x[nt][1] - m[nt][1]);
+        const float p2 = x[nt][2] == -INFINITY ? 0.f : ex2(x[nt][2] - m[nt][0]);
+        const float p3 = x[nt][3] == -INFINITY ? 0.f : ex2(x[nt][3] - m[nt][1]);
+        bl[nt][0] = bl[nt][1] = 0u;
+        if constexpr (kBF16) {
+          const uint32_t ph_a = pack_bf16(p0, p1), ph_b = pack_bf16(p2, p3);
+          const uint32_t pl_a = pack_bf16(p0 - bf16_lo_to_f32(ph_a), p1 - bf16_hi_to_f32(ph_a));
+          const uint32_t pl_b = pack_bf16(p2 - bf16_lo_to_f32(ph_b), p3 - bf16_hi_to_f32(ph_b));
+          l[nt][0] += bf16_lo_to_f32(ph_a) + bf16_lo_to_f32(pl_a) + bf16_lo_to_f32(ph_b) + bf16_lo_to_f32(pl_b);
+          l[nt][1] += bf16_hi_to_f32(ph_a) + bf16_hi_to_f32(pl_a) + bf16_hi_to_f32(ph_b) + bf16_hi_to_f32(pl_b);
+          bh[nt][0] = prmt(__shfl_sync(0xffffffffu, ph_a, src0), __shfl_sync(0xffffffffu, ph_a, src1), half_sel);
+          bh[nt][1] = prmt(__shfl_sync(0xffffffffu, ph_b, src0), __shfl_sync(0xffffffffu, ph_b, src1), half_sel);
+          bl[nt][0] = prmt(__shfl_sync(0xffffffffu, pl_a, src0), __shfl_sync(0xffffffffu, pl_a, src1), half_sel);
+          bl[nt][1] = prmt(__shfl_sync(0xffffffffu, pl_b, src0), __shfl_sync(0xffffffffu, pl_b, src1), half_sel);
+        } else if constexpr (KVF == kKvI8) {
+          // the per-row V scale joins the weight of its token; the denominator
+          // keeps the unscaled weights
+          const uint32_t pa = pack_f16(p0 * sv[sl][0], p1 * sv[sl][0]);
+          const uint32_t pb = pack_f16(p2 * sv[sl][1], p3 * sv[sl][1]);
+          l[nt][0] += p0 + p2;
+          l[nt][1] += p1 + p3;
+          bh[nt][0] = prmt(__shfl_sync(0xffffffffu, pa, src0), __shfl_sync(0xffffffffu, pa, src1), half_sel);
+          bh[nt][1] = prmt(__shfl_sync(0xffffffffu, pb, src0), __shfl_sync(0xffffffffu, pb, src1), half_sel);
+        } else {
+          const uint32_t pa = pack_f16(p0, p1), pb = pack_f16(p2, p3);
+          // the denominator sums the same rounded weights the tensor core multiplies
+          const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&pa));
+          const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&pb));
+          l[nt][0] += fa.x + fb.x;
+          l[nt][1] += fa.y + fb.y;
+          bh[nt][0] = prmt(__shfl_sync(0xffffffffu, pa, src0), __shfl_sync(0xffffffffu, pa, src1), half_sel);
+          bh[nt][1] = prmt(__shfl_sync(0xffffffffu, pb, src0), __shfl_sync(0xffffffffu, pb, src1), half_sel);
+        }
+      }
+
+      // ---- O^T[128 dims x 8] += V^T . P^T per n-tile: lane (gq, cq) reads dims
       // 16gq..16gq+15 of tokens R+2cq, R+2cq+1, R+2cq+8, R+2cq+9.
       const int r0 = R + 2 * cq;
       const uint8_t* v0 = sV + r0 * T::kRowBytes;
@@ -493,10 +548,13 @@ __global__ void __launch_bounds__(kMmaThreads, 2) split_kv_mma_kernel(const __gr
           uint32_t A0, A1, A2, A3;
           widen4<KVF>(prmt(a[j], bq[j], 0x5140u), A0, A1);  // dims 4j, 4j+1 of tokens r0, r0+1
           widen4<KVF>(prmt(c[j], d[j], 0x5140u), A2, A3);   // tokens r0+8, r0+9
-          mma16816<false>(o[2 * j], A0, A1, A2, A3, bh0, bh1);
+#pragma unroll
+          for (int nt = 0; nt < kNT; ++nt) mma16816<false>(o[nt][2 * j], A0, A1, A2, A3, bh[nt][0], bh[nt][1]);
           widen4<KVF>(prmt(a[j], bq[j], 0x7362u), A0, A1);  // dims 4j+2, 4j+3
           widen4<KVF>(prmt(c[j], d[j], 0x7362u), A2, A3);
-          mma16816<false>(o[2 * j + 1], A0, A1, A2, A3, bh0, bh1);
+#pragma unroll
+          for (int nt = 0; nt < kNT; ++nt)
+            mma16816<false>(o[nt][2 * j + 1], A0, A1, A2, A3, bh[nt][0], bh[nt][1]);
         }
       } else {
         const uint8_t* v1 = v0 + T::kRowBytes;
@@ -519,8 +577,11 @@ __global__ void __launch_bounds__(kMmaThreads, 2) split_kv_mma_kernel(const __gr
           for (int j = 0; j < 4; ++j) {  // word j: dims 16gq + 8half + 2j, +1 -> m-tile 4half + j
             const uint32_t A0 = prmt(a[j], bq[j], 0x5410u), A1 = prmt(a[j], bq[j], 0x7632u);
             const uint32_t A2 = prmt(c[j], d[j], 0x5410u), A3 = prmt(c[j], d[j], 0x7632u);
-            mma16816<kBF16>(o[4 * half + j], A0, A1, A2, A3, bh0, bh1);
-            if constexpr (kBF16) mma16816<kBF16>(o[4 * half + j], A0, A1, A2, A3, bl0, bl1);
+#pragma unroll
+            for (int nt = 0; nt < kNT; ++nt) {
+              mma16816<kBF16>(o[nt][4 * half + j], A0, A1, A2, A3, bh[nt][0], bh[nt][1]);
+              if constexpr (kBF16) mma16816<kBF16>(o[nt][4 * half + j], A0, A1, A2, A3, bl[nt][0], bl[nt][1]);
+            }
           }
         }
       }
@@ -529,61 +590,73 @@ __global__ void __launch_bounds__(kMmaThreads, 2) split_kv_mma_kernel(const __gr
     if (lane == 0) mbar_arrive(&empty[st]);
   }
 
-  // ---- per-warp denominators: sum over the 8 lanes holding each head
+  // ---- per-warp denominators: sum over the 8 lanes holding each column
 #pragma unroll
-  for (int off = 4; off < 32; off <<= 1) {
-    l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, off);
-  }
-  // O^T fragment: o[mt][0] = O[dim 16gq+2mt][head 2cq], [1] = [..][2cq+1],
-  //               o[mt][2] = O[dim 16gq+2mt+1][2cq],  [3] = [..+1][2cq+1]
-  if (real_heads) {
-    float* ha = mrg_acc + (warp * kGroup + 2 * cq) * kD + 16 * gq;
-    float* hb = ha + kD;
+  for (int nt = 0; nt < kNT; ++nt)
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      *reinterpret_cast<float2*>(ha + 2 * mt) = make_float2(o[mt][0], o[mt][2]);
-      *reinterpret_cast<float2*>(hb + 2 * mt) = make_float2(o[mt][1], o[mt][3]);
+    for (int off = 4; off < 32; off <<= 1) {
+      l[nt][0] += __shfl_xor_sync(0xffffffffu, l[nt][0], off);
+      l[nt][1] += __shfl_xor_sync(0xffffffffu, l[nt][1], off);
     }
-    if (gq == 0) {
-      mrg_m[warp * kGroup + 2 * cq] = m0;
-      mrg_m[warp * kGroup + 2 * cq + 1] = m1;
-      mrg_l[warp * kGroup + 2 * cq] = l0;
-      mrg_l[warp * kGroup + 2 * cq + 1] = l1;
+  // every consumer warp is done with the ring: reuse it for the merge
+  named_barrier_sync(1, kMmaConsumerWarps * 32);
+  // O^T fragment: o[nt][mt][0] = O[dim 16gq+2mt][column 2cq], [1] = [..][2cq+1],
+  //               o[nt][mt][2] = O[dim 16gq+2mt+1][2cq],  [3] = [..+1][2cq+1]
+#pragma unroll
+  for (int nt = 0; nt < kNT; ++nt) {
+    const int col = 8 * nt + 2 * cq;  // this lane's first column in the n-tile
+    if (col < kCols) {
+      float* ha = mrg_acc + (warp * kCols + col) * kD + 16 * gq;
+      float* hb = ha + kD;
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        *reinterpret_cast<float2*>(ha + 2 * mt) = make_float2(o[nt][mt][0], o[nt][mt][2]);
+        *reinterpret_cast<float2*>(hb + 2 * mt) = make_float2(o[nt][mt][1], o[nt][mt][3]);
+      }
+      if (gq == 0) {
+        mrg_m[warp * kCols + col] = m[nt][0];
+        mrg_m[warp * kCols + col + 1] = m[nt][1];
+        mrg_l[warp * kCols + col] = l[nt][0];
+        mrg_l[warp * kCols + col + 1] = l[nt][1];
+      }
     }
   }
   named_barrier_sync(1, kMmaConsumerWarps * 32);
 
-  // ---- merge the 4 warps: thread -> (head j, dims d0..d0+3)
+  // ---- merge the 4 warps: thread -> (column, dims d0..d0+3)
   const int ctid = threadIdx.x;
-  const int j = ctid >> 5, d0 = 4 * (ctid & 31);
-  float M = -INFINITY;
+  const int d0 = 4 * (ctid & 31);
 #pragma unroll
-  for (int w = 0; w < kMmaConsumerWarps; ++w) M = fmaxf(M, mrg_m[w * kGroup + j]);
-  float Ls = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int it = 0; it < NQ; ++it) {
+    const int col = (ctid >> 5) + kGroup * it;  // query token it, head ctid/32
+    float M = -INFINITY;
 #pragma unroll
-  for (int w = 0; w < kMmaConsumerWarps; ++w) {
-    const float mw = mrg_m[w * kGroup + j];
-    const float a = mw == -INFINITY ? 0.f : ex2(mw - M);
-    Ls = fmaf(mrg_l[w * kGroup + j], a, Ls);
-    const float4 v = *reinterpret_cast<const float4*>(&mrg_acc[(w * kGroup + j) * kD + d0]);
-    acc.x = fmaf(v.x, a, acc.x);
-    acc.y = fmaf(v.y, a, acc.y);
-    acc.z = fmaf(v.z, a, acc.z);
-    acc.w = fmaf(v.w, a, acc.w);
-  }
-  const int h = g * kGroup + j;
-  if (p.splits_eff == 1) {
-    const float inv = p.v_scale / Ls;
-    *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) + ((size_t)(b * kHq + h) * kD + d0) * 2) =
-        make_uint2(pack_out<QF>(acc.x * inv, acc.y * inv), pack_out<QF>(acc.z * inv, acc.w * inv));
-  } else {
-    const size_t idx = (size_t)(b * kHq + h) * p.num_splits + s;
-    *reinterpret_cast<float4*>(p.part_o + idx * kD + d0) = acc;
-    if (d0 == 0) {
-      p.part_m[idx] = M;
-      p.part_l[idx] = Ls;
+    for (int w = 0; w < kMmaConsumerWarps; ++w) M = fmaxf(M, mrg_m[w * kCols + col]);
+    float Ls = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < kMmaConsumerWarps; ++w) {
+      const float mw = mrg_m[w * kCols + col];
+      const float a = mw == -INFINITY ? 0.f : ex2(mw - M);
+      Ls = fmaf(mrg_l[w * kCols + col], a, Ls);
+      const float4 v = *reinterpret_cast<const float4*>(&mrg_acc[(w * kCols + col) * kD + d0]);
+      acc.x = fmaf(v.x, a, acc.x);
+      acc.y = fmaf(v.y, a, acc.y);
+      acc.z = fmaf(v.z, a, acc.z);
+      acc.w = fmaf(v.w, a, acc.w);
+    }
+    const int row = (b * NQ + it) * kHq + g * kGroup + (ctid >> 5);  // (b, query token, head)
+    if (p.splits_eff == 1) {
+      const float inv = Ls > 0.f ? p.v_scale / Ls : 0.f;  // a query with no slot gets zeros
+      *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) + ((size_t)row * kD + d0) * 2) =
+          make_uint2(pack_out<QF>(acc.x * inv, acc.y * inv), pack_out<QF>(acc.z * inv, acc.w * inv));
+    } else {
+      const size_t idx = (size_t)row * p.num_splits + s;
+      *reinterpret_cast<float4*>(p.part_o + idx * kD + d0) = acc;
+      if (d0 == 0) {
+        p.part_m[idx] = M;
+        p.part_l[idx] = Ls;
+      }
     }
   }
 }

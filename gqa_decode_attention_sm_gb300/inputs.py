@@ -45,6 +45,7 @@ class Workload:
     nan_tail: bool = False  # fill K/V slots >= length with NaN
     kv_std: float = 1.0
     q_scale: float = 1.0
+    q_len: int = 1          # query tokens per request (a verify window when > 1)
 
     @property
     def seed(self) -> int:
@@ -64,12 +65,12 @@ WORKLOADS = {
 
 def custom(batch: int, capacity: int, len_lo: int, len_hi: int | None = None,
            kv_dtype: str = "f16", q_dtype: str | None = None, nan_tail: bool = False,
-           kv_std: float = 1.0, q_scale: float = 1.0, index: int = 0) -> Workload:
+           kv_std: float = 1.0, q_scale: float = 1.0, index: int = 0, q_len: int = 1) -> Workload:
     """A workload of any size with the same recipe (edge cases, small tests)."""
     if q_dtype is None:
         q_dtype = "bf16" if kv_dtype in ("e4m3", "i8") else kv_dtype
     return Workload(index, f"custom B{batch} C{capacity}", kv_dtype, q_dtype, batch, capacity,
-                    len_lo, len_lo if len_hi is None else len_hi, nan_tail, kv_std, q_scale)
+                    len_lo, len_lo if len_hi is None else len_hi, nan_tail, kv_std, q_scale, q_len)
 
 
 _TORCH = {"f16": torch.float16, "bf16": torch.bfloat16}
@@ -100,7 +101,8 @@ def _kv_row_fp32(w: Workload, b: int, device, seed: int) -> torch.Tensor:
 def make(w: Workload, device="cpu", seed: int | None = None, lens=None) -> dict:
     """Build one batch of inputs on ``device``.
 
-    Returns a dict with q [B,32,128], kv [B,2,8,C,128] (uint8 bytes for e4m3,
+    Returns a dict with q [B,32,128] ([B,q_len,32,128] for a verify window),
+    kv [B,2,8,C,128] (uint8 bytes for e4m3,
     int8 codes for i8), kv_scales (bf16 [B,2,8,C] for i8, else None), lens
     int32 [B], q_scale, k_scale, v_scale (python floats; the e4m3 scale is the
     fp32 value actually stored), and the workload.
@@ -117,7 +119,8 @@ def make(w: Workload, device="cpu", seed: int | None = None, lens=None) -> dict:
                                    dtype=torch.int64).to(torch.int32)
     else:
         lens_t = torch.as_tensor(lens, dtype=torch.int32).reshape(B).clone()
-    q = torch.randn((B, HQ, D), generator=_gen(device, seed + 1), device=device,
+    q_shape = (B, HQ, D) if w.q_len == 1 else (B, w.q_len, HQ, D)
+    q = torch.randn(q_shape, generator=_gen(device, seed + 1), device=device,
                     dtype=torch.float32).to(_TORCH[w.q_dtype])
 
     kv = torch.empty((B, 2, HKV, C, D), device=device, dtype=kv_storage_dtype(w))

@@ -189,6 +189,24 @@ gqa_status_t gqa_decode_paged(const void* q, gqa_dtype_t q_dtype, const void* kv
                               float k_scale, float v_scale, int num_splits, void* workspace,
                               size_t workspace_bytes, void* stream);
 
+/* Verify window: q_len query tokens per request (1..4), the draft tokens of
+ * speculative / multi-token-prediction decoding (the "FP8 KV cache port on
+ * Jetson AGX Thor" blog, section 2, MTP).  The window's tokens are the last
+ * q_len slots already written to the cache: query token j of row b sits at
+ * slot len[b] - q_len + j and attends slots [0, len[b] - q_len + j] (causal
+ * within the window).  q and out are [batch, q_len, 32, 128]; the workspace
+ * holds gqa_decode_workspace_size(batch * q_len, capacity, num_splits) bytes.
+ * Lengths must lie in [q_len, capacity]; a query with no slot (len below
+ * q_len) gets a zero row and GQA_FLAG_LENGTH_CLAMPED.  kv_format: fp16 / bf16
+ * (= q_dtype), e4m3 or int8 (kv_scales_bf16 as gqa_decode_int8kv, else NULL).
+ * k_scale, v_scale as gqa_decode_fp8kv (1 unless e4m3).  q_scale finite and
+ * >= 0.  Both stages, no allocation, no host sync. */
+gqa_status_t gqa_decode_verify(const void* q, gqa_dtype_t q_dtype, const void* kv,
+                               gqa_kv_format_t kv_format, const uint16_t* kv_scales_bf16,
+                               const int32_t* lens, void* out, int batch, int capacity, int q_len,
+                               float q_scale, float k_scale, float v_scale, int num_splits,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
 /* The two stages of a prepared launch, for callers that schedule (or time)
  * them separately.  Stage 1 streams K/V once per (b, KV head, split) and
  * writes FP32 partials to the workspace, or the final output when

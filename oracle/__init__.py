@@ -86,7 +86,7 @@ def _bind(lib):
     lib.orc_round_array.argtypes = [p, ctypes.c_size_t, ctypes.c_int, p]
     lib.orc_gqa_decode.restype = ctypes.c_int
     lib.orc_gqa_decode.argtypes = [p, ctypes.c_int, p, ctypes.c_int, p, p, ctypes.c_int,
-                                   ctypes.c_int, ctypes.c_double, ctypes.c_double,
+                                   ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_double,
                                    ctypes.c_double, p, ctypes.c_int, p, p, ctypes.c_int,
                                    ctypes.c_int]
     return lib
@@ -126,11 +126,12 @@ def gqa_decode(q_bits: np.ndarray, q_fmt: int, kv_bits: np.ndarray, kv_fmt: int,
                threads: int | None = None, lib=None, kv_scales: np.ndarray | None = None):
     """Oracle attention output.
 
-    q_bits    uint16 [B,32,128] (f16 or bf16 bit patterns)
+    q_bits    uint16 [B,32,128] (f16 or bf16 bit patterns), or [B,T,32,128] for a
+              verify window of T query tokens (query j attends slots [0, L-T+j])
     kv_bits   uint16 [B,2,8,C,128] (f16/bf16), uint8 (e4m3 bytes) or int8 codes (I8)
     kv_scales bf16 bit patterns (uint16) [B,2,8,C], required for I8
     lens      int32 [B]
-    rows    optional iterable of b*32+h; default all rows in order
+    rows      optional iterable of (b*T + j)*32 + h; default all rows in order
     Returns (out_f64 [n_rows,128], out_bits uint16 [n_rows,128]).
     """
     lib = lib or load()
@@ -138,7 +139,8 @@ def gqa_decode(q_bits: np.ndarray, q_fmt: int, kv_bits: np.ndarray, kv_fmt: int,
     kv_bits = np.ascontiguousarray(kv_bits)
     lens = np.ascontiguousarray(lens, dtype=np.int32)
     B = q_bits.shape[0]
-    assert q_bits.shape == (B, HQ, D) and q_bits.dtype == np.uint16
+    T = 1 if q_bits.ndim == 3 else q_bits.shape[1]
+    assert q_bits.shape in ((B, HQ, D), (B, T, HQ, D)) and q_bits.dtype == np.uint16
     assert kv_bits.ndim == 5 and kv_bits.shape[:3] == (B, 2, HKV) and kv_bits.shape[4] == D
     if kv_fmt == I8:
         kv_bits = kv_bits.view(np.int8)
@@ -152,7 +154,7 @@ def gqa_decode(q_bits: np.ndarray, q_fmt: int, kv_bits: np.ndarray, kv_fmt: int,
     if out_fmt is None:
         out_fmt = q_fmt
     if rows is None:
-        rows_arr = np.arange(B * HQ, dtype=np.int32)
+        rows_arr = np.arange(B * T * HQ, dtype=np.int32)
     else:
         rows_arr = np.ascontiguousarray(np.asarray(list(rows), dtype=np.int32))
     n = int(rows_arr.size)
@@ -160,7 +162,7 @@ def gqa_decode(q_bits: np.ndarray, q_fmt: int, kv_bits: np.ndarray, kv_fmt: int,
     bits = np.zeros((n, D), dtype=np.uint16)
     st = lib.orc_gqa_decode(q_bits.ctypes.data, q_fmt, kv_bits.ctypes.data, kv_fmt,
                             kv_scales.ctypes.data if kv_fmt == I8 else None,
-                            lens.ctypes.data, B, C, float(q_scale), float(k_scale),
+                            lens.ctypes.data, B, C, T, float(q_scale), float(k_scale),
                             float(v_scale), rows_arr.ctypes.data, n, out.ctypes.data,
                             bits.ctypes.data, out_fmt, threads or default_threads())
     if st != 0:

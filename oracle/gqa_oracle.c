@@ -34,6 +34,9 @@
  *   s_t = (q_scale / sqrt(128)) * sum_d dec(q[b,h,d]) * K_t[d]
  *   w_t = exp(s_t - max_u s_u)
  *   out = sum_t w_t V_t / sum_t w_t,  rounded once, FP64 -> fp16/bf16, RNE.
+ * Verify window (q_len = T > 1, [FP8] section 2, MTP draft tokens): q is
+ * [batch, T, 32, 128]; query token j sits at position L - T + j and attends
+ * slots [0, L - T + j], i.e. the definition above with L_j = L - T + 1 + j.
  * For the INT8 cache ([ORIN]) dec(kv[b,p,g,t,d]) = code * scale[b,p,g,t], the
  * int8 code times the bf16 scale of that (plane, KV head, position) row.
  * For fp16/bf16 KV, k_scale = v_scale = 1.  Multiplying V by v_scale before
@@ -160,9 +163,9 @@ typedef struct {
   int kv_type;
   const uint16_t* kv_scales;  /* ORC_I8: bf16 bits [B,2,8,C]; else NULL */
   const int32_t* lens;
-  int batch, capacity;
+  int batch, capacity, q_len;
   double q_scale, k_scale, v_scale;
-  const int32_t* rows;  /* b*32 + h */
+  const int32_t* rows;  /* (b*q_len + j)*32 + h */
   int n_rows;
   double* out_f64;      /* [n_rows][128] */
   uint16_t* out_bits;   /* [n_rows][128] or NULL */
@@ -182,12 +185,14 @@ static double orc_elem(const void* base, int type, size_t i) {
 /* One output row: the plain two-pass softmax of [TU] over slots [0, L). */
 static int orc_row(const orc_job* j, int r, double* s) {
   const int bh = j->rows[r];
-  const int b = bh / ORC_HQ, h = bh % ORC_HQ;
+  const int bq = bh / ORC_HQ, h = bh % ORC_HQ;   /* bq = b * q_len + query token */
+  const int b = bq / j->q_len, qt = bq % j->q_len;
   const int g = h / (ORC_HQ / ORC_HKV);
-  const int L = j->lens[b];
-  if (L < 1 || L > j->capacity) return ORC_ELENGTH;
+  const int len = j->lens[b];
+  if (len < j->q_len || len > j->capacity) return ORC_ELENGTH;
+  const int L = len - j->q_len + 1 + qt;         /* causal within the window */
   const size_t C = (size_t)j->capacity;
-  const size_t q_off = ((size_t)b * ORC_HQ + h) * ORC_D;
+  const size_t q_off = ((size_t)bq * ORC_HQ + h) * ORC_D;
   const size_t k_off = (((size_t)b * 2 + 0) * ORC_HKV + g) * C * ORC_D;
   const size_t v_off = (((size_t)b * 2 + 1) * ORC_HKV + g) * C * ORC_D;
   const double scale = j->q_scale / sqrt((double)ORC_D);
@@ -245,16 +250,17 @@ static void* orc_worker(void* arg) {
   return NULL;
 }
 
-/* Compute the rows listed in `rows` (each b*32 + h; NULL = all batch*32 rows
- * in order) with `n_threads` POSIX threads.  kv_scales: bf16 bit patterns
+/* Compute the rows listed in `rows` (each (b*q_len + j)*32 + h; NULL = all
+ * batch*q_len*32 rows in order) with `n_threads` POSIX threads.  q is
+ * [batch, q_len, 32, 128]; lengths must lie in [q_len, capacity].  kv_scales: bf16 bit patterns
  * [batch,2,8,capacity] for kv_type ORC_I8 (int8 codes), ignored otherwise.  Returns ORC_OK or an error code;
  * on ORC_ELENGTH nothing about the other rows is promised. */
 int orc_gqa_decode(const void* q, int q_type, const void* kv, int kv_type,
                    const uint16_t* kv_scales, const int32_t* lens, int batch, int capacity,
-                   double q_scale, double k_scale, double v_scale,
+                   int q_len, double q_scale, double k_scale, double v_scale,
                    const int32_t* rows, int n_rows,
                    double* out_f64, uint16_t* out_bits, int out_type, int n_threads) {
-  if (!q || !kv || !lens || !out_f64 || batch < 1 || capacity < 1) return ORC_EINVAL;
+  if (!q || !kv || !lens || !out_f64 || batch < 1 || capacity < 1 || q_len < 1) return ORC_EINVAL;
   if ((q_type != ORC_F16 && q_type != ORC_BF16) ||
       (kv_type != ORC_F16 && kv_type != ORC_BF16 && kv_type != ORC_E4M3 && kv_type != ORC_I8) ||
       (kv_type == ORC_I8 && !kv_scales) ||
@@ -262,14 +268,14 @@ int orc_gqa_decode(const void* q, int q_type, const void* kv, int kv_type,
     return ORC_EINVAL;
   int32_t* all = NULL;
   if (!rows) {
-    n_rows = batch * ORC_HQ;
+    n_rows = batch * q_len * ORC_HQ;
     all = (int32_t*)malloc(sizeof(int32_t) * (size_t)n_rows);
     if (!all) return ORC_ENOMEM;
     for (int i = 0; i < n_rows; ++i) all[i] = i;
     rows = all;
   }
   for (int i = 0; i < n_rows; ++i)
-    if (rows[i] < 0 || rows[i] >= batch * ORC_HQ) { free(all); return ORC_EINVAL; }
+    if (rows[i] < 0 || rows[i] >= batch * q_len * ORC_HQ) { free(all); return ORC_EINVAL; }
   if (n_threads < 1) n_threads = 1;
   if (n_threads > n_rows) n_threads = n_rows > 0 ? n_rows : 1;
 
@@ -277,7 +283,7 @@ int orc_gqa_decode(const void* q, int q_type, const void* kv, int kv_type,
   pthread_t* tids = (pthread_t*)calloc((size_t)n_threads, sizeof(pthread_t));
   if (!jobs || !tids) { free(jobs); free(tids); free(all); return ORC_ENOMEM; }
   for (int t = 0; t < n_threads; ++t) {
-    orc_job j = {q, q_type, kv, kv_type, kv_scales, lens, batch, capacity, q_scale, k_scale, v_scale,
+    orc_job j = {q, q_type, kv, kv_type, kv_scales, lens, batch, capacity, q_len, q_scale, k_scale, v_scale,
                  rows, n_rows, out_f64, out_bits, out_type, n_threads, t, ORC_OK};
     jobs[t] = j;
   }

@@ -226,6 +226,21 @@ def test_paged_validation(lib):
     assert call(S=4) == EWS
 
 
+def test_verify_validation(lib):
+    f = lib.gqa_decode_verify
+    assert f(Q, F16, KV, KV_F16, None, LENS, OUT, 2, 64, 0, 1.0, 1.0, 1.0, 1, WS, 256, None) == EINVAL
+    assert f(Q, F16, KV, KV_F16, None, LENS, OUT, 2, 64, 5, 1.0, 1.0, 1.0, 1, WS, 256, None) == EINVAL
+    assert f(Q, F16, KV, KV_I8, None, LENS, OUT, 2, 64, 2, 1.0, 1.0, 1.0, 1, WS, 256, None) == EINVAL
+    # the workspace is sized for batch * q_len rows
+    need = lib.gqa_decode_workspace_size(2 * 3, 64, 4)
+    assert f(Q, F16, KV, KV_F16, None, LENS, OUT, 2, 64, 3, 1.0, 1.0, 1.0, 4, WS,
+             lib.gqa_decode_workspace_size(2, 64, 4), None) == EWS
+    assert need > lib.gqa_decode_workspace_size(2, 64, 4)
+    # out spans batch * q_len rows: placing it right after q's first row overlaps
+    assert f(Q, F16, KV, KV_F16, None, LENS, Q + 2 * 32 * 128 * 2, 2, 64, 3, 1.0, 1.0, 1.0, 1, WS, 256,
+             None) == EALIAS
+
+
 def test_convenience_validation(lib):
     g = lib.gqa_decode
     assert g(None, KV, LENS, OUT, 1, 64, F16, 1.0, None) == EINVAL

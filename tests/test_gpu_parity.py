@@ -455,3 +455,55 @@ def test_paged_full_size_bitwise_equals_contiguous():
     out = _paged(pt)
     torch.cuda.synchronize()
     assert torch.equal(out.view(torch.int16), contiguous.view(torch.int16))
+
+
+
+# ----------------------------------------------------------- verify window
+
+
+def _verify(t, num_splits=None):
+    w = t["workload"]
+    fp8 = w.kv_dtype == "e4m3"
+    q = t["q"] if t["q"].dim() == 4 else t["q"][:, None].contiguous()  # [B, T, 32, 128]
+    out = gq.gqa_decode_verify(q, t["kv"], t["lens"], q_scale=t["q_scale"],
+                               k_scale=t["k_scale"] if fp8 else 1.0, v_scale=t["v_scale"] if fp8 else 1.0,
+                               kv_scales=t["kv_scales"], num_splits=num_splits)
+    torch.cuda.synchronize()
+    return out
+
+
+@pytest.mark.parametrize("kv_dtype", ["f16", "bf16", "e4m3", "i8"])
+@pytest.mark.parametrize("T", [1, 2, 3, 4])
+def test_verify_window_every_element(kv_dtype, T):
+    w = inputs.custom(6, 1024, T, 1024, kv_dtype=kv_dtype, kv_std=2.0 if kv_dtype == "e4m3" else 1.0,
+                      nan_tail=True, q_len=T)
+    t = _make(w, lens=[T, T + 1, 63 + T, 64, 500, 1024])
+    for S in (None, 1, 3):
+        out = _verify(t, num_splits=S)
+        _assert_parity(_gpu_rows(out), _oracle_full(t), f"verify T={T} {kv_dtype} splits={S}")
+
+
+def test_verify_window_of_one_is_the_plain_decode():
+    t = _make(inputs.WORKLOADS[3])
+    plain = _run(t).out
+    t1 = dict(t, q=t["q"][:, None].contiguous())
+    out = _verify(t1)
+    assert torch.equal(out[:, 0].contiguous().view(torch.int16), plain.view(torch.int16))
+
+
+def test_verify_window_lengths_below_q_len_give_zero_rows_and_a_flag():
+    T, C = 3, 256
+    t = _make(inputs.custom(2, C, 2, 2, q_len=T), lens=[2, 200])  # row 0: only queries 1, 2 have slots
+    ws = torch.zeros(gq.workspace_size(2 * T, C, 4), dtype=torch.uint8, device=DEV)
+    out = gq.gqa_decode_verify(t["q"], t["kv"], t["lens"], num_splits=4, workspace=ws)
+    assert gq.get_status(ws) & api.FLAG_LENGTH_CLAMPED
+    assert torch.all(out[0, 0] == 0)
+    ref = oracle.gqa_decode(bits_of(t["q"][1:]), oracle.F16, bits_of(t["kv"][1:]), oracle.F16,
+                            np.array([200], np.int32))[0]
+    _assert_parity(_gpu_rows(out[1:]), ref, "verify row with a valid length")
+
+
+def test_verify_window_medium_size_bf16():
+    t = _make(inputs.custom(4, 16384, 8000, 16384, kv_dtype="bf16", q_len=2))
+    out = _verify(t)
+    _assert_parity(_gpu_rows(out), _oracle_full(t), "verify T=2 bf16 4 x U[8000,16384]")

@@ -317,3 +317,59 @@ def test_paged_gather_reproduces_the_contiguous_cache(orc, page_size):
     a, _ = _run(orc, t, qb, kvb, lens)
     c, _ = _run(orc, t, qb, g, lens)
     assert np.array_equal(a, c)
+
+
+# ----------------------------------------------------------- verify window
+
+
+def _window_sdpa(t):
+    """torch float64 SDPA with an explicit causal mask over the window."""
+    w = t["workload"]
+    T = w.q_len
+    qv = values_of_bits(bits_of(t["q"]), w.q_dtype)            # [B,T,32,128]
+    kvv = values_of_bits(bits_of(t["kv"]), w.kv_dtype)         # [B,2,8,C,128]
+    lens = t["lens"].numpy()
+    out = np.zeros((w.batch, T, HQ, D))
+    for b in range(w.batch):
+        L = int(lens[b])
+        q = torch.from_numpy(np.ascontiguousarray(qv[b].transpose(1, 0, 2)))[None]  # [1,32,T,128]
+        k = torch.from_numpy(np.ascontiguousarray(kvv[b, 0, :, :L])).repeat_interleave(4, 0)[None]
+        v = torch.from_numpy(np.ascontiguousarray(kvv[b, 1, :, :L])).repeat_interleave(4, 0)[None]
+        mask = torch.arange(L)[None, :] <= (L - T + torch.arange(T))[:, None]          # [T,L]
+        o = torch.nn.functional.scaled_dot_product_attention(q, k, v, attn_mask=mask,
+                                                             scale=t["q_scale"] / math.sqrt(D))
+        out[b] = o[0].numpy().transpose(1, 0, 2)
+    return out.reshape(-1, D)
+
+
+@pytest.mark.parametrize("T", [2, 3, 4])
+def test_window_matches_torch_sdpa_with_causal_mask(orc, T):
+    w = inputs.custom(2, 128, 4, 128, kv_dtype="bf16", q_len=T, nan_tail=True)
+    t, qb, kvb, lens = _random(w, seed=30 + T)
+    out, _ = _run(orc, t, qb, kvb, lens)
+    np.testing.assert_allclose(out, _window_sdpa(t), rtol=1e-10, atol=1e-12)
+
+
+def test_window_2(orc):
+    test_window_matches_torch_sdpa_with_causal_mask(orc, 2)
+
+
+def test_window_rows_are_single_token_problems(orc):
+    # query j of a T-token window equals a one-token decode over the first L-T+1+j slots
+    T = 3
+    w = inputs.custom(2, 64, 10, 64, q_len=T)
+    t, qb, kvb, lens = _random(w, seed=4)
+    out, _ = _run(orc, t, qb, kvb, lens)
+    for b in range(2):
+        for j in range(T):
+            one, _ = oracle.gqa_decode(qb[b:b + 1, j], oracle.F16, kvb[b:b + 1], oracle.F16,
+                                       np.array([lens[b] - T + 1 + j], np.int32), lib=orc)
+            r0 = (b * T + j) * HQ
+            assert np.array_equal(out[r0:r0 + HQ], one)
+
+
+def test_window_rejects_lengths_below_q_len(orc):
+    w = inputs.custom(2, 16, 4, q_len=4)
+    t, qb, kvb, _ = _random(w)
+    with pytest.raises(ValueError):
+        _run(orc, t, qb, kvb, np.array([3, 4], np.int32))

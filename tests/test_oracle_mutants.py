@@ -36,6 +36,8 @@ MUTANTS = {
                                                 "const size_t ks_off = (((size_t)b * 2 + 1)"),
     "int8 scale of the next row": ("orc_decode_bf16(j->kv_scales[vs_off + t])",
                                    "orc_decode_bf16(j->kv_scales[vs_off + (t + 1) % L])"),
+    "verify window shifted by one slot": ("const int L = len - j->q_len + 1 + qt;",
+                                          "const int L = len - j->q_len + qt + (qt == 0);"),
     "int8 codes read as unsigned": ("if (type == ORC_I8) return (double)((const int8_t*)base)[i];",
                                     "if (type == ORC_I8) return (double)((const uint8_t*)base)[i];"),
     "k_scale applied to V": ("* j->v_scale;\n      acc", "* j->k_scale;\n      acc"),
@@ -69,6 +71,7 @@ PINS = [
     A.test_int8_length_one_returns_scaled_first_row,
     A.test_int8_matches_torch_sdpa_on_dequantised_rows,
     A.test_int8_scales_act_per_row,
+    A.test_window_2,
 ]
 
 
