@@ -80,6 +80,8 @@ def _bind(lib):
     lib.orc_round_bf16.restype = ctypes.c_uint16
     lib.orc_round_bf16.argtypes = [ctypes.c_double]
     p = ctypes.c_void_p
+    lib.orc_norm_rope.restype = None
+    lib.orc_norm_rope.argtypes = [p, p, ctypes.c_int, ctypes.c_double, ctypes.c_double, p]
     lib.orc_decode_array.restype = None
     lib.orc_decode_array.argtypes = [p, ctypes.c_int, ctypes.c_size_t, p]
     lib.orc_round_array.restype = None
@@ -187,3 +189,28 @@ def gather_pages(pages: np.ndarray, block_table: np.ndarray, lens: np.ndarray) -
         for j in range(-(-int(lens[b]) // ps)):
             out[b, :, :, j * ps:(j + 1) * ps] = pages[int(block_table[b, j])]
     return out
+
+
+def norm_rope(x: np.ndarray, w: np.ndarray, pos: int, eps: float, theta: float, lib=None) -> np.ndarray:
+    """RMS norm (weight w) then rotate-half RoPE at position pos, FP64; x, w [128]."""
+    lib = lib or load()
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    w = np.ascontiguousarray(w, dtype=np.float64)
+    z = np.empty(D, dtype=np.float64)
+    lib.orc_norm_rope(x.ctypes.data, w.ctypes.data, int(pos), float(eps), float(theta), z.ctypes.data)
+    return z
+
+
+def append_kv(q_proj, k_proj, v_proj, q_norm_w, k_norm_w, positions, eps, theta, lib=None):
+    """The appended token in FP64: q_out [B,32,128], k_new [B,8,128], v_new [B,8,128].
+
+    Inputs are FP64 values (decode the bf16/fp16 bits first)."""
+    B = q_proj.shape[0]
+    qo = np.empty((B, HQ, D))
+    ko = np.empty((B, HKV, D))
+    for b in range(B):
+        for h in range(HQ):
+            qo[b, h] = norm_rope(q_proj[b, h], q_norm_w, positions[b], eps, theta, lib)
+        for g in range(HKV):
+            ko[b, g] = norm_rope(k_proj[b, g], k_norm_w, positions[b], eps, theta, lib)
+    return qo, ko, np.array(v_proj, dtype=np.float64)

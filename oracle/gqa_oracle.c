@@ -304,3 +304,30 @@ int orc_gqa_decode(const void* q, int q_type, const void* kv, int kv_type,
   free(all);
   return status;
 }
+
+/* ------------------------------------------------------------ K/V append */
+
+/* The step before decode ("Qwen3-VL official BF16 on Jetson Thor (SM110)"
+ * docs, "Runtime architecture": fused Q/K norm + RoPE + KV-write kernels;
+ * decode graphs keyed by (cache_pos, rope_pos)).  For one new token per batch
+ * row b, each query head and each KV head vector x of 128:
+ *   y_d  = x_d / sqrt(mean_e(x_e^2) + eps) * w_d            (RMS norm, weight w)
+ *   a_i  = pos[b] * theta^(-i/64), i = 0..63                 (rotary angles)
+ *   z_i      = y_i cos a_i - y_{i+64} sin a_i                (rotate-half RoPE)
+ *   z_{i+64} = y_{i+64} cos a_i + y_i sin a_i
+ * q heads use w = q_norm_w, k heads k_norm_w; v is copied unchanged.  Output
+ * is FP64 (the caller rounds or quantises).  x, w are given as FP64 values. */
+void orc_norm_rope(const double* x, const double* w, int pos, double eps, double theta, double* z) {
+  double ss = 0.0;
+  for (int d = 0; d < ORC_D; ++d) ss += x[d] * x[d];
+  const double r = 1.0 / sqrt(ss / ORC_D + eps);
+  double y[ORC_D];
+  for (int d = 0; d < ORC_D; ++d) y[d] = x[d] * r * w[d];
+  const int half = ORC_D / 2;
+  for (int i = 0; i < half; ++i) {
+    const double a = (double)pos * pow(theta, -(double)i / half);
+    const double c = cos(a), s = sin(a);
+    z[i] = y[i] * c - y[i + half] * s;
+    z[i + half] = y[i + half] * c + y[i] * s;
+  }
+}

@@ -14,6 +14,7 @@ import shutil
 import pytest
 
 import oracle
+import test_oracle_append as P
 import test_oracle_attention as A
 import test_oracle_formats as F
 
@@ -38,6 +39,13 @@ MUTANTS = {
                                    "orc_decode_bf16(j->kv_scales[vs_off + (t + 1) % L])"),
     "verify window shifted by one slot": ("const int L = len - j->q_len + 1 + qt;",
                                           "const int L = len - j->q_len + qt + (qt == 0);"),
+    "RoPE pairs interleaved": ("    z[i] = y[i] * c - y[i + half] * s;\n    z[i + half] = y[i + half] * c + y[i] * s;",
+                               "    z[2 * (i % 64)] = y[2 * (i % 64)] * c - y[2 * (i % 64) + 1] * s;\n"
+                               "    z[2 * (i % 64) + 1] = y[2 * (i % 64) + 1] * c + y[2 * (i % 64)] * s;"),
+    "RoPE rotation sign flipped": ("z[i + half] = y[i + half] * c + y[i] * s;", "z[i + half] = y[i + half] * c - y[i] * s;"),
+    "RoPE frequency doubled": ("pow(theta, -(double)i / half)", "pow(theta, -2.0 * (double)i / half)"),
+    "RMS over the sum, not the mean": ("sqrt(ss / ORC_D + eps)", "sqrt(ss + eps)"),
+    "RMS eps dropped": ("sqrt(ss / ORC_D + eps)", "sqrt(ss / ORC_D)"),
     "int8 codes read as unsigned": ("if (type == ORC_I8) return (double)((const int8_t*)base)[i];",
                                     "if (type == ORC_I8) return (double)((const uint8_t*)base)[i];"),
     "k_scale applied to V": ("* j->v_scale;\n      acc", "* j->k_scale;\n      acc"),
@@ -72,6 +80,11 @@ PINS = [
     A.test_int8_matches_torch_sdpa_on_dequantised_rows,
     A.test_int8_scales_act_per_row,
     A.test_window_2,
+    P.test_constant_vector_normalises_to_the_weight,
+    P.test_position_zero_is_the_plain_rms_norm,
+    lambda lib: [P.test_one_hot_rotates_into_its_rotate_half_partner(lib, i) for i in (0, 17, 63)],
+    P.test_exact_one_radian_example,
+    P.test_relative_position_property,
 ]
 
 
