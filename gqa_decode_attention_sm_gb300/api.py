@@ -27,13 +27,14 @@ MAX_SPLITS = 256
 FLAG_LENGTH_CLAMPED = 0x1
 FLAG_WAIT_TIMEOUT = 0x2
 FLAG_PAGE_CLAMPED = 0x4
+FLAG_SLOT_CLAMPED = 0x8
 
 _QDT = {torch.float16: F16, torch.bfloat16: BF16}
 _KVF = {torch.float16: KV_F16, torch.bfloat16: KV_BF16, torch.uint8: KV_E4M3,
         torch.float8_e4m3fn: KV_E4M3, torch.int8: KV_I8}
 
 __all__ = ["GqaError", "gqa_decode", "gqa_decode_fp8kv", "gqa_decode_int8kv", "gqa_decode_paged",
-           "gqa_decode_verify",
+           "gqa_decode_verify", "append_kv",
            "prepare", "launch",
            "Prepared",
            "workspace_size", "plan", "get_status", "split_stage", "combine_stage", "split_geometry"]
@@ -333,6 +334,38 @@ def gqa_decode_verify(q, kv, sequence_lengths, q_scale: float = 1.0, k_scale: fl
             _ptr(sequence_lengths), _ptr(out), B, C, T, float(q_scale), float(k_scale), float(v_scale), S,
             _ptr(workspace), workspace.numel(), _stream(q.device)))
     return out
+
+
+def append_kv(q_proj, k_proj, v_proj, q_norm_w, k_norm_w, positions, slots, kv, q_out=None,
+              eps: float = 1e-6, rope_theta: float = 1e6, k_scale: float = 1.0, v_scale: float = 1.0,
+              kv_scales=None, workspace=None):
+    """RMS norm + RoPE of the new token's q and k heads; k and v written into
+    ``kv`` at ``slots``; returns q_out [batch, 32, 128] ready for decode."""
+    _require(q_proj, "q_proj", None, (torch.float16, torch.bfloat16))
+    B = q_proj.shape[0]
+    dt = q_proj.dtype
+    _require(q_proj, "q_proj", (B, HQ, D), (dt,))
+    _require(k_proj, "k_proj", (B, HKV, D), (dt,), q_proj.device)
+    _require(v_proj, "v_proj", (B, HKV, D), (dt,), q_proj.device)
+    _require(q_norm_w, "q_norm_w", (D,), (dt,), q_proj.device)
+    _require(k_norm_w, "k_norm_w", (D,), (dt,), q_proj.device)
+    _require(positions, "positions", (B,), (torch.int32,), q_proj.device)
+    _require(slots, "slots", (B,), (torch.int32,), q_proj.device)
+    if kv.dim() != 5 or kv.shape[0] != B or kv.shape[1:3] != (2, HKV) or kv.shape[4] != D:
+        raise ValueError(f"kv must be [{B}, 2, {HKV}, capacity, {D}]")
+    _require(kv, "kv", None, tuple(_KVF), q_proj.device)
+    kvf = _KVF[kv.dtype]
+    if q_out is None:
+        q_out = torch.empty_like(q_proj)
+    _require(q_out, "q_out", q_proj.shape, (dt,), q_proj.device)
+    with torch.cuda.device(q_proj.device):
+        _lib.check(_lib.load().gqa_append_kv(
+            _ptr(q_proj), _ptr(k_proj), _ptr(v_proj), _ptr(q_norm_w), _ptr(k_norm_w), _QDT[dt],
+            _ptr(positions), _ptr(slots), B, _ptr(q_out), _ptr(kv), kvf,
+            _ptr(kv_scales) if kv_scales is not None else None, kv.shape[3], float(eps), float(rope_theta),
+            float(k_scale), float(v_scale), _ptr(workspace) if workspace is not None else None,
+            workspace.numel() if workspace is not None else 0, _stream(q_proj.device)))
+    return q_out
 
 
 def get_status(p_or_workspace) -> int:

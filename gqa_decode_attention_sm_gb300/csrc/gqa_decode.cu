@@ -17,6 +17,7 @@
 #include <string>
 
 #include "gqa_decode.h"
+#include "kernels/append_kv.cuh"
 #include "kernels/combine.cuh"
 #include "kernels/common.cuh"
 #include "kernels/split_kv_mma.cuh"
@@ -552,6 +553,82 @@ gqa_status_t gqa_decode_verify(const void* q, gqa_dtype_t q_dtype, const void* k
   st = run_split(c);
   if (st != GQA_OK) return st;
   return run_combine(c);
+}
+
+gqa_status_t gqa_append_kv(const void* q_proj, const void* k_proj, const void* v_proj, const void* q_norm_w,
+                           const void* k_norm_w, gqa_dtype_t dtype, const int32_t* positions, const int32_t* slots,
+                           int batch, void* q_out, void* kv, gqa_kv_format_t kv_format, uint16_t* kv_scales_bf16,
+                           int capacity, float eps, float rope_theta, float k_scale, float v_scale, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  if (!q_proj || !k_proj || !v_proj || !q_norm_w || !k_norm_w || !positions || !slots || !q_out || !kv)
+    return fail(GQA_ERR_INVALID_ARGUMENT, "null pointer argument");
+  gqa_status_t st = validate_shape(batch, capacity);
+  if (st != GQA_OK) return st;
+  if (dtype != GQA_F16 && dtype != GQA_BF16) return fail(GQA_ERR_INVALID_ARGUMENT, "unknown dtype %d", (int)dtype);
+  const int fmt = (int)kv_format;
+  if (fmt != kKvF16 && fmt != kKvBF16 && fmt != kKvE4M3 && fmt != kKvI8)
+    return fail(GQA_ERR_INVALID_ARGUMENT, "unknown KV format %d", fmt);
+  if (!is_8bit(fmt) && fmt != (int)dtype)
+    return fail(GQA_ERR_INVALID_ARGUMENT, "fp16/bf16 KV must have the dtype of the projections");
+  if (fmt == kKvI8 && !kv_scales_bf16) return fail(GQA_ERR_INVALID_ARGUMENT, "an int8 cache needs kv_scales_bf16");
+  if (!std::isfinite(eps) || eps < 0.f) return fail(GQA_ERR_INVALID_ARGUMENT, "eps must be finite and >= 0");
+  if (!std::isfinite(rope_theta) || rope_theta <= 0.f)
+    return fail(GQA_ERR_INVALID_ARGUMENT, "rope_theta must be finite and > 0");
+  if (!std::isfinite(k_scale) || k_scale <= 0.f || !std::isfinite(v_scale) || v_scale <= 0.f)
+    return fail(GQA_ERR_INVALID_ARGUMENT, "k_scale and v_scale must be finite and > 0");
+  if (workspace && workspace_bytes < GQA_WORKSPACE_HEADER_BYTES)
+    return fail(GQA_ERR_WORKSPACE_TOO_SMALL, "workspace smaller than its %d-byte header", GQA_WORKSPACE_HEADER_BYTES);
+  const void* h16[] = {q_proj, k_proj, v_proj, q_norm_w, k_norm_w, q_out};
+  for (const void* ptr : h16)
+    if (!aligned(ptr, 2)) return fail(GQA_ERR_INVALID_ARGUMENT, "16-bit arrays must be 2-byte aligned");
+  if (!aligned(positions, 4) || !aligned(slots, 4) || (workspace && !aligned(workspace, 4)) ||
+      (!is_8bit(fmt) && !aligned(kv, 2)) || (kv_scales_bf16 && !aligned(kv_scales_bf16, 2)))
+    return fail(GQA_ERR_INVALID_ARGUMENT, "misaligned argument");
+  const size_t qb = (size_t)batch * kHq * kD * 2, kvb_in = (size_t)batch * kHkv * kD * 2;
+  const size_t cache = (size_t)batch * 2 * kHkv * (size_t)capacity * kD * kv_elem_bytes(fmt);
+  const void* ins[] = {q_proj, k_proj, v_proj};
+  const size_t in_bytes[] = {qb, kvb_in, kvb_in};
+  for (int i = 0; i < 3; ++i)
+    if (overlap(q_out, qb, ins[i], in_bytes[i]) || overlap(kv, cache, ins[i], in_bytes[i]))
+      return fail(GQA_ERR_ALIASING, "q_out or kv overlaps an input projection");
+  if (overlap(q_out, qb, kv, cache)) return fail(GQA_ERR_ALIASING, "q_out overlaps kv");
+  int dev_sms = 0;
+  st = current_device_ready(&dev_sms);
+  if (st != GQA_OK) return st;
+  AppendParams ap;
+  ap.q_proj = q_proj;
+  ap.k_proj = k_proj;
+  ap.v_proj = v_proj;
+  ap.q_norm_w = q_norm_w;
+  ap.k_norm_w = k_norm_w;
+  ap.positions = positions;
+  ap.slots = slots;
+  ap.q_out = q_out;
+  ap.kv = kv;
+  ap.kv_scales = kv_scales_bf16;
+  ap.flags = static_cast<uint32_t*>(workspace);
+  ap.batch = batch;
+  ap.capacity = capacity;
+  ap.eps = eps;
+  ap.k_inv_scale = 1.f / k_scale;
+  ap.v_inv_scale = 1.f / v_scale;
+  ap.theta = (double)rope_theta;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(batch, 1, 1);
+  cfg.blockDim = dim3(kAppendThreads, 1, 1);
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  const bool bf = dtype == GQA_BF16;
+  if (fmt == kKvF16) e = cudaLaunchKernelEx(&cfg, append_kv_kernel<kKvF16, kQF16>, ap);
+  else if (fmt == kKvBF16) e = cudaLaunchKernelEx(&cfg, append_kv_kernel<kKvBF16, kQBF16>, ap);
+  else if (fmt == kKvE4M3)
+    e = bf ? cudaLaunchKernelEx(&cfg, append_kv_kernel<kKvE4M3, kQBF16>, ap)
+           : cudaLaunchKernelEx(&cfg, append_kv_kernel<kKvE4M3, kQF16>, ap);
+  else
+    e = bf ? cudaLaunchKernelEx(&cfg, append_kv_kernel<kKvI8, kQBF16>, ap)
+           : cudaLaunchKernelEx(&cfg, append_kv_kernel<kKvI8, kQF16>, ap);
+  if (e != cudaSuccess) return cuda_fail(e, "append kernel launch");
+  return GQA_OK;
 }
 
 gqa_status_t gqa_decode_split_stage(const void* q, gqa_dtype_t q_dtype, const void* kv,

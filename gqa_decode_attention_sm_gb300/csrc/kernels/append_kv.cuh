@@ -1,0 +1,147 @@
+// The step before decode: normalise and rotate the new token's query and key
+// heads and write its key and value into the cache.
+//
+// "Qwen3-VL official BF16 on Jetson Thor (SM110)" docs, "Runtime
+// architecture": fused Q/K norm + RoPE + KV-write kernels (q staged for
+// attention, k and v written at the cache position); decode graphs are keyed
+// by (cache_pos, rope_pos), so the rotary position and the cache slot are
+// separate inputs.  For each head vector x of 128 (32 query heads, 8 KV heads):
+//   y_d = x_d / sqrt(mean(x^2) + eps) * w_d      (w = q_norm_w or k_norm_w)
+//   z_i = y_i cos a_i - y_{i+64} sin a_i,  z_{i+64} = y_{i+64} cos a_i + y_i sin a_i,
+//   a_i = pos * theta^(-i/64)                    (rotate-half RoPE)
+// q -> q_out (q's dtype, RNE); k -> K plane at `slot`; v is written unchanged
+// to the V plane.  The cache format decides the write: fp16/bf16 (RNE),
+// e4m3 (value / scale, RNE, saturating), int8 (one bf16 scale amax/127 per
+// row, codes round-to-nearest-even, clipped to +-127).
+//
+// One CTA per batch row, 8 warps; each warp takes whole head vectors and lane
+// l holds dims l, l+32, l+64, l+96, so every RoPE pair (i, i+64) stays in one
+// lane.  The 64 angles are formed in FP64 (pos * theta^(-i/64) reaches 1e5
+// radians at long contexts, beyond FP32's reach) once per CTA.
+#pragma once
+
+#include "common.cuh"
+
+namespace gqa {
+
+constexpr int kAppendThreads = 256;
+
+struct AppendParams {
+  const void* q_proj;      // [B,32,128] q/out dtype
+  const void* k_proj;      // [B,8,128]
+  const void* v_proj;      // [B,8,128]
+  const void* q_norm_w;    // [128]
+  const void* k_norm_w;    // [128]
+  const int32_t* positions;  // [B] rotary positions
+  const int32_t* slots;      // [B] cache slots to write
+  void* q_out;             // [B,32,128]
+  void* kv;                // [B,2,8,C,128] in the cache format
+  uint16_t* kv_scales;     // int8 cache: [B,2,8,C] bf16
+  uint32_t* flags;         // optional status word
+  int batch, capacity;
+  float eps, k_inv_scale, v_inv_scale;  // e4m3: 1/k_scale, 1/v_scale
+  double theta;
+};
+
+template <int QF>
+__device__ __forceinline__ float load_elem(const void* base, size_t i) {
+  const uint16_t h = static_cast<const uint16_t*>(base)[i];
+  if constexpr (QF == kQF16) return __half2float(__ushort_as_half(h));
+  else return __uint_as_float((uint32_t)h << 16);
+}
+
+template <int QF>
+__device__ __forceinline__ uint16_t round_elem(float x) {
+  if constexpr (QF == kQF16) return __half_as_ushort(__float2half_rn(x));
+  else return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+__device__ __forceinline__ uint8_t to_e4m3(float x) {
+  uint16_t two;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(two) : "f"(0.f), "f"(x));
+  return (uint8_t)(two & 0xffu);
+}
+
+template <int KVF, int QF>
+__global__ void __launch_bounds__(kAppendThreads) append_kv_kernel(const __grid_constant__ AppendParams p) {
+  __shared__ float cs[kD / 2], sn[kD / 2];
+  const int b = blockIdx.x;
+  const int pos = __ldg(p.positions + b);
+  if (threadIdx.x < kD / 2) {
+    const double a = (double)pos * pow(p.theta, -(double)threadIdx.x / (kD / 2));
+    double sv, cv;
+    sincos(a, &sv, &cv);
+    cs[threadIdx.x] = (float)cv;
+    sn[threadIdx.x] = (float)sv;
+  }
+  __syncthreads();
+  const int C = p.capacity;
+  const int slot = __ldg(p.slots + b);
+  const bool slot_ok = slot >= 0 && slot < C;
+  if (!slot_ok && threadIdx.x == 0 && p.flags) atomicOr(p.flags, GQA_FLAG_SLOT_CLAMPED);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int dims[4] = {lane, lane + 32, lane + 64, lane + 96};
+
+  // vectors 0..31: query heads; 32..39: key heads; 40..47: value heads
+  for (int v = warp; v < kHq + 2 * kHkv; v += kAppendThreads / 32) {
+    const bool is_q = v < kHq, is_k = v >= kHq && v < kHq + kHkv;
+    const int g = is_q ? 0 : (v - kHq) % kHkv;
+    const void* src = is_q ? p.q_proj : (is_k ? p.k_proj : p.v_proj);
+    const size_t row = is_q ? ((size_t)b * kHq + v) * kD : ((size_t)b * kHkv + g) * kD;
+    float z[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) z[k] = load_elem<QF>(src, row + dims[k]);
+    if (!is_q && !is_k && !slot_ok) continue;
+    if (is_q || is_k) {
+      float ss = z[0] * z[0] + z[1] * z[1] + z[2] * z[2] + z[3] * z[3];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+      const float r = 1.f / sqrtf(ss / kD + p.eps);
+      const void* w = is_q ? p.q_norm_w : p.k_norm_w;
+      float y[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) y[k] = z[k] * r * load_elem<QF>(w, dims[k]);
+      // pairs (lane, lane+64) with angle lane, (lane+32, lane+96) with angle lane+32
+      const float c0 = cs[lane], s0 = sn[lane], c1 = cs[lane + 32], s1 = sn[lane + 32];
+      z[0] = y[0] * c0 - y[2] * s0;
+      z[2] = y[2] * c0 + y[0] * s0;
+      z[1] = y[1] * c1 - y[3] * s1;
+      z[3] = y[3] * c1 + y[1] * s1;
+    }
+    if (is_q) {
+      uint16_t* out = static_cast<uint16_t*>(p.q_out) + row;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) out[dims[k]] = round_elem<QF>(z[k]);
+      continue;
+    }
+    if (!slot_ok) continue;  // never write outside the cache
+    const int plane = is_k ? 0 : 1;
+    const size_t crow = ((((size_t)b * 2 + plane) * kHkv + g) * (size_t)C + slot) * kD;
+    if constexpr (KVF == kKvE4M3) {
+      const float inv = is_k ? p.k_inv_scale : p.v_inv_scale;
+      uint8_t* dst = static_cast<uint8_t*>(p.kv) + crow;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) dst[dims[k]] = to_e4m3(z[k] * inv);
+    } else if constexpr (KVF == kKvI8) {
+      float amax = fmaxf(fmaxf(fabsf(z[0]), fabsf(z[1])), fmaxf(fabsf(z[2]), fabsf(z[3])));
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+      uint16_t sb = __bfloat16_as_ushort(__float2bfloat16_rn(amax / 127.f));
+      if (sb == 0) sb = 0x3f80;  // an all-zero row keeps scale 1
+      const float scale = __uint_as_float((uint32_t)sb << 16);
+      int8_t* dst = reinterpret_cast<int8_t*>(p.kv) + crow;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int code = max(-127, min(127, __float2int_rn(z[k] / scale)));
+        dst[dims[k]] = (int8_t)code;
+      }
+      if (lane == 0) p.kv_scales[(((size_t)b * 2 + plane) * kHkv + g) * (size_t)C + slot] = sb;
+    } else {
+      uint16_t* dst = static_cast<uint16_t*>(p.kv) + crow;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) dst[dims[k]] = round_elem<QF>(z[k]);
+    }
+  }
+}
+
+}  // namespace gqa

@@ -88,6 +88,7 @@ typedef enum { GQA_KV_F16 = 0, GQA_KV_BF16 = 1, GQA_KV_E4M3 = 2, GQA_KV_I8 = 3 }
 #define GQA_FLAG_LENGTH_CLAMPED 0x1u  /* some lens[b] was outside [1, capacity] */
 #define GQA_FLAG_WAIT_TIMEOUT 0x2u    /* a pipeline wait gave up; outputs are invalid */
 #define GQA_FLAG_PAGE_CLAMPED 0x4u    /* a block-table entry was outside [0, num_pages) */
+#define GQA_FLAG_SLOT_CLAMPED 0x8u    /* gqa_append_kv: a slot outside [0, capacity), not written */
 
 /* Name of a status code (static string). */
 const char* gqa_status_string(gqa_status_t status);
@@ -273,6 +274,32 @@ gqa_status_t gqa_decode_debug_skip_tile(const void* q, gqa_dtype_t q_dtype, cons
                                         float v_scale, int num_splits, void* workspace,
                                         size_t workspace_bytes, int skip_tile,
                                         uint64_t wait_budget_ns, void* stream);
+
+/* The step before decode: one new token per batch row (the "Qwen3-VL
+ * official BF16 on Jetson Thor (SM110)" docs, "Runtime architecture": fused
+ * Q/K norm + RoPE + KV-write kernels; decode graphs keyed by (cache_pos,
+ * rope_pos)).  For each query head and each KV head vector x of 128:
+ *   y_d = x_d / sqrt(mean(x^2) + eps) * w_d     (w = q_norm_w or k_norm_w, [128])
+ *   z_i = y_i cos a_i - y_{i+64} sin a_i,  z_{i+64} = y_{i+64} cos a_i + y_i sin a_i,
+ *   a_i = positions[b] * rope_theta^(-i/64)     (rotate-half RoPE, i = 0..63)
+ * q_out[b] <- z of the 32 query heads (dtype, RNE); the K plane of `kv` at
+ * slot slots[b] <- z of the 8 key heads; the V plane at that slot <- v_proj
+ * unchanged.  q_proj [batch,32,128], k_proj and v_proj [batch,8,128] and the
+ * weights are `dtype`.  The cache format decides the write: fp16/bf16 (must
+ * equal dtype; RNE), e4m3 (value / k_scale or / v_scale, RNE, saturating) or
+ * int8 (codes round-to-nearest-even of value / scale with a fresh bf16 row
+ * scale amax/127 written to kv_scales_bf16, clipped to +-127).  positions and
+ * slots are int32 [batch] in device memory, read only by the kernel; a slot
+ * outside [0, capacity) is not written and, when a workspace is given, sets
+ * GQA_FLAG_SLOT_CLAMPED in its header (workspace may be NULL).  eps finite >= 0,
+ * rope_theta finite > 0.  One launch, no allocation, no host sync.  A decode
+ * that should see the new token uses len[b] = slots[b] + 1. */
+gqa_status_t gqa_append_kv(const void* q_proj, const void* k_proj, const void* v_proj,
+                           const void* q_norm_w, const void* k_norm_w, gqa_dtype_t dtype,
+                           const int32_t* positions, const int32_t* slots, int batch, void* q_out,
+                           void* kv, gqa_kv_format_t kv_format, uint16_t* kv_scales_bf16, int capacity,
+                           float eps, float rope_theta, float k_scale, float v_scale, void* workspace,
+                           size_t workspace_bytes, void* stream);
 
 /* Zero the workspace header (status flags) on `stream`.  Asynchronous. */
 gqa_status_t gqa_decode_workspace_init(void* workspace, size_t workspace_bytes, void* stream);

@@ -241,6 +241,28 @@ def test_verify_validation(lib):
              None) == EALIAS
 
 
+def test_append_validation(lib):
+    f = lib.gqa_append_kv
+    QP, KP, VP, WQ, WK, POS, SL, QO, KVC = (0x10000000 + i * 0x1000000 for i in range(9))
+
+    def call(**kw):
+        a = dict(qp=QP, kp=KP, vp=VP, wq=WQ, wk=WK, dt=BF16, pos=POS, sl=SL, B=2, qo=QO, kv=KVC,
+                 fmt=KV_BF16, sc=None, C=64, eps=1e-6, th=1e6, ks=1.0, vs=1.0, ws=None, wsb=0)
+        a.update(kw)
+        return f(a["qp"], a["kp"], a["vp"], a["wq"], a["wk"], a["dt"], a["pos"], a["sl"], a["B"], a["qo"],
+                 a["kv"], a["fmt"], a["sc"], a["C"], a["eps"], a["th"], a["ks"], a["vs"], a["ws"], a["wsb"],
+                 None)
+
+    assert call(qp=None) == EINVAL and call(sl=None) == EINVAL
+    assert call(fmt=KV_F16) == EINVAL                 # fp16 cache with bf16 projections
+    assert call(fmt=KV_I8) == EINVAL                  # int8 cache without scales
+    assert call(eps=-1.0) == EINVAL and call(th=0.0) == EINVAL and call(ks=0.0, fmt=KV_E4M3) == EINVAL
+    assert call(ws=WS, wsb=16) == EWS
+    assert call(qp=QP + 1) == EINVAL
+    assert call(qo=QP) == EALIAS                      # q_out on q_proj
+    assert call(kv=KP) == EALIAS                      # cache on k_proj
+
+
 def test_convenience_validation(lib):
     g = lib.gqa_decode
     assert g(None, KV, LENS, OUT, 1, 64, F16, 1.0, None) == EINVAL

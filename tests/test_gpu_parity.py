@@ -507,3 +507,120 @@ def test_verify_window_medium_size_bf16():
     t = _make(inputs.custom(4, 16384, 8000, 16384, kv_dtype="bf16", q_len=2))
     out = _verify(t)
     _assert_parity(_gpu_rows(out), _oracle_full(t), "verify T=2 bf16 4 x U[8000,16384]")
+
+
+
+# --------------------------------------------------- K/V append (before decode)
+
+
+def _append_inputs(B, C, dtype, seed=0):
+    g = torch.Generator(device=DEV)
+    g.manual_seed(seed)
+    dt = {"f16": torch.float16, "bf16": torch.bfloat16}[dtype]
+    rnd = lambda *shape: torch.randn(shape, generator=g, device=DEV, dtype=torch.float32)  # noqa: E731
+    qp, kp, vp = rnd(B, 32, 128).to(dt), rnd(B, 8, 128).to(dt), rnd(B, 8, 128).to(dt)
+    wq, wk = (1 + 0.1 * rnd(128)).to(dt), (1 + 0.1 * rnd(128)).to(dt)
+    pos = torch.randint(0, 200000, (B,), generator=g, device=DEV, dtype=torch.int32)
+    slots = torch.randint(0, C, (B,), generator=g, device=DEV, dtype=torch.int32)
+    return qp, kp, vp, wq, wk, pos, slots
+
+
+def _vals(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_append_matches_oracle_and_touches_only_its_slot(dtype):
+    B, C = 6, 300
+    qp, kp, vp, wq, wk, pos, slots = _append_inputs(B, C, dtype, seed=1)
+    kv = _make(inputs.custom(B, C, C, kv_dtype=dtype))["kv"]
+    before = kv.clone()
+    q_out = gq.append_kv(qp, kp, vp, wq, wk, pos, slots, kv, eps=1e-6, rope_theta=1e6)
+    torch.cuda.synchronize()
+    qo, ko, vo = oracle.append_kv(_vals(qp), _vals(kp), _vals(vp), _vals(wq), _vals(wk),
+                                  pos.cpu().numpy(), 1e-6, 1e6)
+    _assert_parity(_gpu_rows(q_out), qo.reshape(-1, 128), f"append q_out {dtype}")
+    sl = slots.cpu().tolist()
+    k_new = torch.stack([kv[b, 0, :, sl[b]] for b in range(B)])
+    _assert_parity(_gpu_rows(k_new), ko.reshape(-1, 128), f"append k {dtype}")
+    v_new = torch.stack([kv[b, 1, :, sl[b]] for b in range(B)])
+    assert torch.equal(v_new.view(torch.int16), vp.view(torch.int16))
+    for b in range(B):  # nothing else in the cache changed
+        before[b, :, :, sl[b]] = kv[b, :, :, sl[b]]
+    assert torch.equal(kv.view(torch.int16), before.view(torch.int16))
+
+
+def _nearest_codes(ref, table_vals):
+    """Indices of the two representable values bracketing ref (sorted table)."""
+    i = np.searchsorted(table_vals, ref)
+    return np.clip(i - 1, 0, len(table_vals) - 1), np.clip(i, 0, len(table_vals) - 1)
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "i8"])
+def test_append_quantising_writes(fmt):
+    B, C = 4, 256
+    qp, kp, vp, wq, wk, pos, slots = _append_inputs(B, C, "bf16", seed=2)
+    w = inputs.custom(B, C, C, kv_dtype=fmt, kv_std=2.0 if fmt == "e4m3" else 1.0)
+    t = _make(w)
+    kv, sc = t["kv"], t["kv_scales"]
+    ks, vs = (0.02, 0.03) if fmt == "e4m3" else (1.0, 1.0)
+    gq.append_kv(qp, kp, vp, wq, wk, pos, slots, kv, k_scale=ks, v_scale=vs, kv_scales=sc)
+    torch.cuda.synchronize()
+    _, ko, vo = oracle.append_kv(_vals(qp), _vals(kp), _vals(vp), _vals(wq), _vals(wk), pos.cpu().numpy(),
+                                 1e-6, 1e6)
+    sl = slots.cpu().tolist()
+    for b in range(B):
+        for plane, ref_rows, scale in ((0, ko[b], ks), (1, vo[b], vs)):
+            codes = kv[b, plane, :, sl[b]].cpu()
+            if fmt == "e4m3":
+                got = torch.from_numpy(codes.numpy()).view(torch.float8_e4m3fn).double().numpy()
+                ref = ref_rows / scale
+                # the kernel's choice must be one of the two e4m3 values bracketing ref
+                table = np.sort(np.unique(torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn)
+                                          .double().numpy()))
+                table = table[np.isfinite(table)]
+                lo, hi = _nearest_codes(ref, table)
+                ok = (got == table[lo]) | (got == table[hi])
+                assert ok.all(), f"e4m3 codes off the bracketing pair at b={b} plane={plane}"
+            else:
+                row_scale = sc[b, plane, :, sl[b]].double().cpu().numpy()  # [8]
+                amax = np.abs(ref_rows).max(axis=1)
+                np.testing.assert_allclose(row_scale, amax / 127, rtol=2 ** -7)  # bf16 of amax/127
+                got = codes.numpy().astype(np.float64) * row_scale[:, None]
+                assert np.all(np.abs(got - ref_rows) <= 0.5 * row_scale[:, None] * (1 + 1e-3) + 1e-6)
+
+
+def test_append_out_of_range_slot_is_skipped_and_flagged():
+    B, C = 3, 128
+    qp, kp, vp, wq, wk, pos, _ = _append_inputs(B, C, "bf16", seed=3)
+    slots = torch.tensor([5, C + 3, -1], dtype=torch.int32, device=DEV)
+    kv = _make(inputs.custom(B, C, C, kv_dtype="bf16"))["kv"]
+    before = kv.clone()
+    ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    gq.append_kv(qp, kp, vp, wq, wk, pos, slots, kv, workspace=ws)
+    assert gq.get_status(ws) & api.FLAG_SLOT_CLAMPED
+    before[0, :, :, 5] = kv[0, :, :, 5]
+    assert torch.equal(kv.view(torch.int16), before.view(torch.int16))
+
+
+def test_append_then_decode_matches_the_oracle_chain():
+    # GPU: append the new token, then decode over len = slot + 1.  Oracle: the
+    # same two steps computed from the same inputs, rounding the appended rows
+    # with its own RNE, never reading anything the GPU produced.
+    B, C = 4, 2048
+    qp, kp, vp, wq, wk, pos, _ = _append_inputs(B, C, "bf16", seed=4)
+    t = _make(inputs.custom(B, C, 1000, 2000, kv_dtype="bf16"))
+    slots = t["lens"].clone()                       # append at the current length
+    kv_bits0 = bits_of(t["kv"]).copy()
+    q_out = gq.append_kv(qp, kp, vp, wq, wk, pos, slots, t["kv"])
+    lens = slots + 1
+    out = gq.gqa_decode(q_out, t["kv"], lens)
+    torch.cuda.synchronize()
+    qo, ko, vo = oracle.append_kv(_vals(qp), _vals(kp), _vals(vp), _vals(wq), _vals(wk), pos.cpu().numpy(),
+                                  1e-6, 1e6)
+    q_bits = oracle.round_to(qo, oracle.BF16)
+    for b, s_ in enumerate(slots.cpu().tolist()):
+        kv_bits0[b, 0, :, s_] = oracle.round_to(ko[b], oracle.BF16)
+        kv_bits0[b, 1, :, s_] = bits_of(vp[b])
+    ref, _ = oracle.gqa_decode(q_bits, oracle.BF16, kv_bits0, oracle.BF16, lens.cpu().numpy())
+    _assert_parity(_gpu_rows(out), ref, "append -> decode chain")
