@@ -57,13 +57,14 @@ DeviceState g_devices[kMaxDevices];
 template <int KVF, int QF>
 cudaError_t set_split_attributes() {
   cudaError_t e = cudaSuccess;
-  const auto set = [&](auto kernel) {
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmaSmemBytes);
+  const auto set = [&](auto kernel, int nq) {
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, mma_smem_bytes(KVF, nq));
   };
-  set(split_kv_mma_kernel<KVF, QF, 1>);
-  set(split_kv_mma_kernel<KVF, QF, 2>);
-  set(split_kv_mma_kernel<KVF, QF, 3>);
-  set(split_kv_mma_kernel<KVF, QF, 4>);
+  set(split_kv_mma_kernel<KVF, QF, 1>, 1);
+  set(split_kv_mma_kernel<KVF, QF, 2>, 2);
+  set(split_kv_mma_kernel<KVF, QF, 3>, 3);
+  set(split_kv_mma_kernel<KVF, QF, 4>, 4);
   return e;
 }
 
@@ -254,14 +255,14 @@ gqa_status_t static_workspace(int dev, void** ptr) {
 
 // --------------------------------------------------------------- planning
 
-constexpr int kSplitCtasPerSm = 2;  // the split kernel's occupancy (shared memory bound)
-
 int plan_splits(int batch, int capacity, int kv_format, int sm_count) {
-  // Aim for about 8 waves of work items (kSplitCtasPerSm resident per SM) over
-  // the worst case (every length = capacity), with whole tiles per split.
+  // Aim for about 8 waves of work items (as many resident per SM as the
+  // single-token split kernel of this format allows) over the worst case
+  // (every length = capacity), with whole tiles per split.
   const long long tile = tile_tokens(kv_format);
   const long long units = (long long)batch * kHkv;
-  const long long target_ctas = 8LL * kSplitCtasPerSm * (sm_count > 0 ? sm_count : 148);
+  const long long ctas_per_sm = mma_ctas_per_sm(kv_format, 1);
+  const long long target_ctas = 8LL * ctas_per_sm * (sm_count > 0 ? sm_count : 148);
   long long per = (units * capacity + target_ctas - 1) / target_ctas;
   per = (per + tile - 1) / tile * tile;
   if (per < tile) per = tile;
@@ -278,7 +279,7 @@ cudaError_t launch_split_t(const SplitParams& sp, int q_len, cudaStream_t stream
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(sp.splits_eff, kHkv, sp.batch);
   cfg.blockDim = dim3(kMmaThreads, 1, 1);
-  cfg.dynamicSmemBytes = kMmaSmemBytes;
+  cfg.dynamicSmemBytes = mma_smem_bytes(KVF, q_len);
   cfg.stream = stream;
   switch (q_len) {
     case 1: return cudaLaunchKernelEx(&cfg, split_kv_mma_kernel<KVF, QF, 1>, sp);

@@ -85,13 +85,22 @@ __device__ __forceinline__ uint32_t pack_out(float a, float b) {
 
 constexpr int kMmaConsumerWarps = 4;
 constexpr int kMmaThreads = (kMmaConsumerWarps + 1) * 32;
-constexpr int kMmaStages = 3;
+// Ring depth and residency: 8-bit KV does twice the arithmetic per byte, and
+// with one query token it fits in <= 136 registers, so 3 CTAs of 2 stages
+// share an SM (more warps to hide latency); 16-bit KV and verify windows use
+// 3 stages at 2 CTAs per SM (measured: bf16 streams fastest so, e4m3 is 2-3 %
+// faster at 3 CTAs).
+__host__ __device__ constexpr int mma_stages(int kvf, int nq) { return is_8bit(kvf) && nq == 1 ? 2 : 3; }
+__host__ __device__ constexpr int mma_ctas_per_sm(int kvf, int nq) { return is_8bit(kvf) && nq == 1 ? 3 : 2; }
 constexpr int kMaxQLen = 4;  // query tokens per request (a verify window when > 1)
 constexpr int kScaleStageBytes = 2 * 128 * 2;  // int8 cache: K and V row scales of one 128-token tile
-constexpr int kMmaSmemBytes = kMmaStages * kStageBytes + kMmaStages * kScaleStageBytes + 2 * kMmaStages * 8;
+__host__ __device__ constexpr int mma_smem_bytes(int kvf, int nq) {
+  return mma_stages(kvf, nq) * (kStageBytes + kScaleStageBytes + 2 * 8);
+}
 // The epilogue merges the 4 warps' states in the ring (idle by then):
 // [warp][column][128] accumulators + [warp][column] max and denominator.
-static_assert(kMmaConsumerWarps * kGroup * kMaxQLen * (kD + 2) * 4 <= kMmaStages * kStageBytes,
+static_assert(kMmaConsumerWarps * kGroup * 1 * (kD + 2) * 4 <= mma_stages(kKvE4M3, 1) * kStageBytes &&
+                  kMmaConsumerWarps * kGroup * kMaxQLen * (kD + 2) * 4 <= mma_stages(kKvF16, kMaxQLen) * kStageBytes,
               "merge area must fit in the ring");
 
 // ---------------------------------------------------------------- mma.sync
@@ -171,7 +180,9 @@ __device__ __forceinline__ int qk_dim(int cq, int ks, int pair /*0: a0/b0, 1: a2
 }
 
 template <int KVF, int QF, int NQ>
-__global__ void __launch_bounds__(kMmaThreads, 2) split_kv_mma_kernel(const __grid_constant__ SplitParams p) {
+__global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
+    split_kv_mma_kernel(const __grid_constant__ SplitParams p) {
+  constexpr int kMmaStages = mma_stages(KVF, NQ);
   using T = KvTraits<KVF>;
   constexpr bool kBF16 = kMmaBF16<KVF>;
   constexpr int kSlabs = T::kTile / (16 * kMmaConsumerWarps);  // 16-token slabs per warp per tile
