@@ -87,10 +87,10 @@ def _chunk(C, S, fmt):
 
 # (batch, capacity, format, SM count) -> splits: about 8 waves of work items
 # (2 resident per SM for 16-bit KV, 3 for 8-bit KV) over the worst case, whole
-# tiles per split, 1..256 splits.
+# tiles per split (at least two), 1..256 splits.
 PLAN_TABLE = [
     ((1, 64, KV_F16, 152), 1),
-    ((1, 1024, KV_F16, 152), 16),
+    ((1, 1024, KV_F16, 152), 8),
     ((32, 8192, KV_F16, 152), 10),
     ((8, 131072, KV_BF16, 152), 38),
     ((64, 32768, KV_E4M3, 152), 8),
