@@ -7,7 +7,8 @@ raises if the library has not been built (there is no fallback path).
 """
 from .api import (GqaError, Prepared, append_kv, combine_stage, get_status, gqa_decode, gqa_decode_fp8kv,
                   gqa_decode_int8kv, gqa_decode_paged, gqa_decode_verify, launch, plan, prepare, split_stage,
-                  workspace_size)
+                  workspace_init, workspace_size)
 
 __all__ = ["GqaError", "Prepared", "append_kv", "combine_stage", "get_status", "gqa_decode", "gqa_decode_fp8kv",
-           "gqa_decode_int8kv", "gqa_decode_paged", "gqa_decode_verify", "launch", "plan", "prepare", "split_stage", "workspace_size"]
+           "gqa_decode_int8kv", "gqa_decode_paged", "gqa_decode_verify", "launch", "plan", "prepare", "split_stage",
+           "workspace_init", "workspace_size"]

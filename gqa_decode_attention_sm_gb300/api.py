@@ -154,7 +154,9 @@ def prepare(tensors: dict, q_scale: float = 1.0, num_splits=None, k_scale=None, 
 
     ``tensors`` holds "Q", "KV", "O", "sequence_lengths", and "KV_SCALES" for an
     int8 cache.  An e4m3 cache (uint8 or float8_e4m3fn storage) needs k_scale
-    and v_scale.
+    and v_scale.  A ``workspace`` given by the caller (uint8, at least
+    workspace_size bytes) should have its 256-byte header (status flags) zeroed
+    before first use (``workspace_init``).
     """
     q, kv, out, lens = tensors["Q"], tensors["KV"], tensors["O"], tensors["sequence_lengths"]
     B, C = _geometry(q, kv, lens)
@@ -366,6 +368,13 @@ def append_kv(q_proj, k_proj, v_proj, q_norm_w, k_norm_w, positions, slots, kv, 
             float(k_scale), float(v_scale), _ptr(workspace) if workspace is not None else None,
             workspace.numel() if workspace is not None else 0, _stream(q_proj.device)))
     return q_out
+
+
+def workspace_init(workspace: torch.Tensor) -> None:
+    """Zero a workspace's header (status flags) on the current stream."""
+    with torch.cuda.device(workspace.device):
+        _lib.check(_lib.load().gqa_decode_workspace_init(_ptr(workspace), workspace.numel(),
+                                                         _stream(workspace.device)))
 
 
 def get_status(p_or_workspace) -> int:

@@ -461,6 +461,19 @@ def test_paged_full_size_bitwise_equals_contiguous():
 # ----------------------------------------------------------- verify window
 
 
+def test_workspace_init_zeroes_a_dirty_workspace():
+    t = _make(inputs.custom(5, 2048, 1, 2048, kv_dtype="bf16"))
+    S = 8
+    ws = torch.full((gq.workspace_size(5, 2048, S),), 0xA5, dtype=torch.uint8, device=DEV)
+    gq.workspace_init(ws)
+    assert int(ws[:256].sum()) == 0
+    p = _prepare(t, num_splits=S, workspace=ws)
+    gq.launch(p)
+    torch.cuda.synchronize()
+    assert gq.get_status(p) == 0
+    _assert_parity(_gpu_rows(p.out), _oracle_full(t), "after workspace_init")
+
+
 def _verify(t, num_splits=None):
     w = t["workload"]
     fp8 = w.kv_dtype == "e4m3"
