@@ -57,14 +57,14 @@ DeviceState g_devices[kMaxDevices];
 template <int KVF, int QF>
 cudaError_t set_split_attributes() {
   cudaError_t e = cudaSuccess;
-  const auto set = [&](auto kernel, int nq) {
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, mma_smem_bytes(KVF, nq));
+  const auto set = [&](auto kernel, int bytes) {
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   };
-  set(split_kv_mma_kernel<KVF, QF, 1>, 1);
-  set(split_kv_mma_kernel<KVF, QF, 2>, 2);
-  set(split_kv_mma_kernel<KVF, QF, 3>, 3);
-  set(split_kv_mma_kernel<KVF, QF, 4>, 4);
+  set(split_kv_mma_kernel<KVF, QF, 1, false>, mma_smem_bytes(KVF, 1));
+  set(split_kv_mma_kernel<KVF, QF, 2, false>, mma_smem_bytes(KVF, 2));
+  set(split_kv_mma_kernel<KVF, QF, 3, false>, mma_smem_bytes(KVF, 3));
+  set(split_kv_mma_kernel<KVF, QF, 4, false>, mma_smem_bytes(KVF, 4));
+  set(split_kv_mma_kernel<KVF, QF, 1, true>, mma_smem_bytes(KVF, 1) + kBalMergeBytes);
   return e;
 }
 
@@ -167,6 +167,7 @@ struct Call {
   const int32_t* block_table = nullptr;  // paged cache only
   int page_log2 = 0, max_pages = 0, num_pages = 0;
   int q_len = 1;  // query tokens per request (verify window)
+  int sms = 0;    // SM count of the current device (set once validated)
 };
 
 gqa_status_t validate_shape(int batch, int capacity) {
@@ -276,18 +277,24 @@ int plan_splits(int batch, int capacity, int kv_format, int sm_count) {
 
 // ---------------------------------------------------------------- launches
 
+// `bal_ctas` > 0: the balanced schedule on that many CTAs (single token).
 template <int KVF, int QF>
-cudaError_t launch_split_t(const SplitParams& sp, int q_len, cudaStream_t stream) {
+cudaError_t launch_split_t(const SplitParams& sp, int q_len, int bal_ctas, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(sp.splits_eff, kHkv, sp.batch);
   cfg.blockDim = dim3(kMmaThreads, 1, 1);
-  cfg.dynamicSmemBytes = mma_smem_bytes(KVF, q_len);
   cfg.stream = stream;
+  if (bal_ctas > 0) {
+    cfg.gridDim = dim3(bal_ctas, 1, 1);
+    cfg.dynamicSmemBytes = mma_smem_bytes(KVF, 1) + kBalMergeBytes;
+    return cudaLaunchKernelEx(&cfg, split_kv_mma_kernel<KVF, QF, 1, true>, sp);
+  }
+  cfg.gridDim = dim3(kHkv, sp.batch, sp.splits_eff);
+  cfg.dynamicSmemBytes = mma_smem_bytes(KVF, q_len);
   switch (q_len) {
-    case 1: return cudaLaunchKernelEx(&cfg, split_kv_mma_kernel<KVF, QF, 1>, sp);
-    case 2: return cudaLaunchKernelEx(&cfg, split_kv_mma_kernel<KVF, QF, 2>, sp);
-    case 3: return cudaLaunchKernelEx(&cfg, split_kv_mma_kernel<KVF, QF, 3>, sp);
-    default: return cudaLaunchKernelEx(&cfg, split_kv_mma_kernel<KVF, QF, 4>, sp);
+    case 1: return cudaLaunchKernelEx(&cfg, split_kv_mma_kernel<KVF, QF, 1, false>, sp);
+    case 2: return cudaLaunchKernelEx(&cfg, split_kv_mma_kernel<KVF, QF, 2, false>, sp);
+    case 3: return cudaLaunchKernelEx(&cfg, split_kv_mma_kernel<KVF, QF, 3, false>, sp);
+    default: return cudaLaunchKernelEx(&cfg, split_kv_mma_kernel<KVF, QF, 4, false>, sp);
   }
 }
 
@@ -328,6 +335,40 @@ Layout layout_of(void* ws, int batch, int splits) {
   return l;
 }
 
+// The balanced schedule serves single-token decode of batches up to
+// kBalMaxBatch whose rows can be split (two or more tiles of capacity) and
+// whose one-piece-per-CTA grid would take more than one wave, as long as the
+// global tile count fits an int.  q_min keeps every row within the
+// workspace's split slots: a row of n <= nmax tiles meets at most
+// ceil(n / q) + 1 <= num_splits CTAs.  Measured on GB300 (us per call, back
+// to back): fp16 32 x U[1,8192] 96.4 -> 89.9, e4m3 64 x U[16k,32k] 459.4 ->
+// 443.7, bf16 8 x 131072 589.4 -> 584.3.
+struct BalPlan {
+  int ctas = 0;  // 0: the one-piece-per-CTA grid
+  int q_min = 0;
+};
+
+BalPlan bal_plan(const Call& c) {
+  BalPlan bp;
+  const int tile = tile_tokens(c.kv_format);
+  const long long nmax = ((long long)c.capacity + tile - 1) / tile;
+  if (c.q_len != 1 || c.batch > kBalMaxBatch || c.num_splits < 2 || c.sms < 1) return bp;
+  const int splits_eff = split_count(c.capacity, c.num_splits, c.kv_format);
+  if (splits_eff < 2) return bp;
+  if ((long long)kHkv * c.batch * nmax > 0x7fffffffLL) return bp;
+  const long long slots = (long long)mma_ctas_per_sm(c.kv_format, 1) * c.sms;
+  // one wave of pieces or less: nothing to balance, the plain grid starts sooner
+  if ((long long)kHkv * c.batch * splits_eff <= slots) return bp;
+  // One CTA per resident slot for a contiguous cache.  A paged cache runs 4
+  // waves of smaller runs: its per-CTA rates vary more (pages scattered over
+  // HBM), and the later waves let the hardware even them out (bf16 8 x 131072
+  // in shuffled 256-token pages, GB300: 608 us with one wave, 590 with four,
+  // 592 with the one-piece-per-CTA grid).
+  bp.ctas = (int)((c.block_table != nullptr ? 4 : 1) * slots);
+  bp.q_min = (int)((nmax + c.num_splits - 2) / (c.num_splits - 1));
+  return bp;
+}
+
 gqa_status_t run_split(const Call& c) {
   const Layout lay = layout_of(c.workspace, c.batch * c.q_len, c.num_splits);
   SplitParams sp;
@@ -354,16 +395,18 @@ gqa_status_t run_split(const Call& c) {
   sp.page_log2 = c.page_log2;
   sp.max_pages = c.max_pages;
   sp.num_pages = c.num_pages;
+  const BalPlan bp = bal_plan(c);
+  sp.bal_q_min = bp.q_min;
   cudaError_t e;
-  const int ql = c.q_len;
-  if (c.kv_format == kKvF16) e = launch_split_t<kKvF16, kQF16>(sp, ql, c.stream);
-  else if (c.kv_format == kKvBF16) e = launch_split_t<kKvBF16, kQBF16>(sp, ql, c.stream);
+  const int ql = c.q_len, nb = bp.ctas;
+  if (c.kv_format == kKvF16) e = launch_split_t<kKvF16, kQF16>(sp, ql, nb, c.stream);
+  else if (c.kv_format == kKvBF16) e = launch_split_t<kKvBF16, kQBF16>(sp, ql, nb, c.stream);
   else if (c.kv_format == kKvE4M3)
-    e = c.q_dtype == GQA_BF16 ? launch_split_t<kKvE4M3, kQBF16>(sp, ql, c.stream)
-                              : launch_split_t<kKvE4M3, kQF16>(sp, ql, c.stream);
+    e = c.q_dtype == GQA_BF16 ? launch_split_t<kKvE4M3, kQBF16>(sp, ql, nb, c.stream)
+                              : launch_split_t<kKvE4M3, kQF16>(sp, ql, nb, c.stream);
   else
-    e = c.q_dtype == GQA_BF16 ? launch_split_t<kKvI8, kQBF16>(sp, ql, c.stream)
-                              : launch_split_t<kKvI8, kQF16>(sp, ql, c.stream);
+    e = c.q_dtype == GQA_BF16 ? launch_split_t<kKvI8, kQBF16>(sp, ql, nb, c.stream)
+                              : launch_split_t<kKvI8, kQF16>(sp, ql, nb, c.stream);
   if (e != cudaSuccess) return cuda_fail(e, "split kernel launch");
   return GQA_OK;
 }
@@ -383,6 +426,11 @@ gqa_status_t run_combine(const Call& c) {
   cp.chunk = split_chunk(c.capacity, c.num_splits, c.kv_format);
   cp.q_len = c.q_len;
   cp.v_scale = c.v_scale;
+  const BalPlan bp = bal_plan(c);
+  cp.bal_ctas = bp.ctas;
+  cp.bal_q_min = bp.q_min;
+  cp.tile = tile_tokens(c.kv_format);
+  cp.batch = c.batch;
   cudaError_t e = c.q_dtype == GQA_F16 ? launch_combine_t<kQF16>(cp, c.batch * c.q_len, c.stream)
                                        : launch_combine_t<kQBF16>(cp, c.batch * c.q_len, c.stream);
   if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
@@ -405,7 +453,9 @@ gqa_status_t prepare_call(Call& c, bool q_scale_positive, bool need_q) {
   }
   gqa_status_t st = validate(c, q_scale_positive, need_q);
   if (st != GQA_OK) return st;
-  return current_device_ready(&sms);
+  st = current_device_ready(&sms);
+  c.sms = sms;
+  return st;
 }
 
 }  // namespace
@@ -698,8 +748,10 @@ gqa_status_t gqa_decode_combine_stage(const int32_t* lens, void* out, gqa_dtype_
     return fail(GQA_ERR_WORKSPACE_TOO_SMALL, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
   if (overlap(out, (size_t)batch * kHq * kD * 2, workspace, need))
     return fail(GQA_ERR_ALIASING, "out overlaps the workspace");
-  st = current_device_ready(nullptr);
+  int sms = 0;
+  st = current_device_ready(&sms);
   if (st != GQA_OK) return st;
+  c.sms = sms;
   return run_combine(c);
 }
 
@@ -717,6 +769,7 @@ gqa_status_t gqa_decode(const void* q, const void* kv, const int32_t* lens, void
   st = current_device_ready(&sms);
   if (st != GQA_OK) return st;
   c.num_splits = plan_splits(batch, capacity, (int)dtype, sms);
+  c.sms = sms;
   const size_t bytes = workspace_bytes_for(batch, c.num_splits);
   void* ws = nullptr;
   cudaError_t e = cudaMallocAsync(&ws, bytes, c.stream);
@@ -760,6 +813,7 @@ gqa_status_t gqa_decode_noalloc(const void* q, const void* kv, const int32_t* le
     while (S > 1 && workspace_bytes_for(batch, S) > kStaticWorkspaceBytes) --S;
   }
   c.num_splits = S;
+  c.sms = sms;
   c.workspace = ws;
   c.workspace_bytes = kStaticWorkspaceBytes;
   st = validate(c, false, true);

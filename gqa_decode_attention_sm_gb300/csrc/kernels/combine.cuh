@@ -10,7 +10,10 @@
 // separate kernel so stage 1 needs no inter-CTA ticket; it is launched as a
 // programmatic dependent of stage 1, so its launch overlaps stage 1's tail.  One warp per
 // (b, h), each lane owning 4 dims; the splits are merged in a fixed order, so
-// the result is bitwise deterministic.
+// the result is bitwise deterministic.  With stage 1's balanced schedule the
+// "splits" of a row are its pieces (their number follows from the lengths);
+// a row of one piece was written by stage 1, a row without tokens is zeroed
+// here.
 #pragma once
 
 #include "common.cuh"
@@ -28,23 +31,20 @@ struct CombineParams {
   int capacity, num_splits, chunk;
   int q_len;  // rows are (b * q_len + j, head); query j attends len - q_len + 1 + j slots
   float v_scale;
+  // balanced schedule of stage 1 (bal_ctas > 0, q_len = 1): pieces per row
+  // follow from the lengths, the CTA count, q_min and the tile size
+  int bal_ctas, bal_q_min, tile, batch;
 };
 
+// Merge of the first n split partials of one (b, query head) row by one warp
+// (lane l owns dims 4l..4l+3) into out row `row`; n = 0 writes zeros.
+// Splits are handled 32 at a time: lane k loads the max / denominator of
+// split s0 + k, the weights 2^(m_s - M) are formed once per split and
+// broadcast with shuffles, and the partial-output loads are independent.
 template <int QF>
-__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_constant__ CombineParams p) {
-  const int g = blockIdx.x, bq = blockIdx.y;  // bq = b * q_len + query token
-  const int b = bq / p.q_len, jq = bq % p.q_len;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = g * kGroup + warp;
-  const int L = min(max(__ldg(p.lens + b), 0), p.capacity) - p.q_len + 1 + jq;
-  const int n = L > 0 ? (L + p.chunk - 1) / p.chunk : 0;
-  const size_t base = (size_t)(bq * kHq + h) * p.num_splits;
-  // launched as a programmatic dependent of stage 1: wait for its partials
-  pdl_wait_prior_grid();
-
-  // Splits are handled 32 at a time: lane k loads the max / denominator of
-  // split s0 + k, the weights 2^(m_s - M) are formed once per split and
-  // broadcast with shuffles, and the partial-output loads are independent.
+__device__ __forceinline__ void merge_splits(const CombineParams& p, size_t row, int n) {
+  const int lane = threadIdx.x & 31;
+  const size_t base = row * p.num_splits;
   float M = -INFINITY;
   for (int s = lane; s < n; s += 32) M = fmaxf(M, p.part_m[base + s]);
 #pragma unroll
@@ -84,8 +84,58 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
     const __nv_bfloat162 c = __floats2bfloat162_rn(o.z * inv, o.w * inv);
     packed = make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&c));
   }
-  *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) + ((size_t)(bq * kHq + h) * kD + 4 * lane) * 2) =
-      packed;
+  *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) + (row * kD + 4 * lane) * 2) = packed;
+}
+
+template <int QF>
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_constant__ CombineParams p) {
+  const int g = blockIdx.x, bq = blockIdx.y;  // bq = b * q_len + query token
+  const int b = bq / p.q_len, jq = bq % p.q_len;
+  const size_t row = (size_t)bq * kHq + g * kGroup + (threadIdx.x >> 5);
+  int n;
+  if (p.bal_ctas > 0) {
+    // The tile counts stage 1 used (integers, so both kernels agree exactly),
+    // read while stage 1 still runs.
+    __shared__ int red[2][kCombineThreads / 32];
+    int before = 0, all = 0;
+    for (int bb = threadIdx.x; bb < p.batch; bb += kCombineThreads) {
+      const int nb = (min(max(__ldg(p.lens + bb), 0), p.capacity) + p.tile - 1) / p.tile;
+      all += nb;
+      if (bb < b) before += nb;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      before += __shfl_xor_sync(0xffffffffu, before, off);
+      all += __shfl_xor_sync(0xffffffffu, all, off);
+    }
+    if ((threadIdx.x & 31) == 0) {
+      red[0][threadIdx.x >> 5] = before;
+      red[1][threadIdx.x >> 5] = all;
+    }
+    __syncthreads();
+    before = all = 0;
+#pragma unroll
+    for (int w = 0; w < kCombineThreads / 32; ++w) {
+      before += red[0][w];
+      all += red[1][w];
+    }
+    const int nb = (min(max(__ldg(p.lens + b), 0), p.capacity) + p.tile - 1) / p.tile;
+    if (nb == 0) {  // no tokens: a zero row (stage 1 holds no piece of it)
+      merge_splits<QF>(p, row, 0);
+      return;
+    }
+    const int total = kHkv * all;
+    const int q = max((total + p.bal_ctas - 1) / p.bal_ctas, p.bal_q_min);
+    const int tf = kHkv * before + g * nb;
+    n = (tf + nb - 1) / q - tf / q + 1;
+    if (n == 1) return;  // one piece: stage 1 wrote the row itself
+  } else {
+    const int L = min(max(__ldg(p.lens + b), 0), p.capacity) - p.q_len + 1 + jq;
+    n = L > 0 ? (L + p.chunk - 1) / p.chunk : 0;
+  }
+  // launched as a programmatic dependent of stage 1: wait for its partials
+  pdl_wait_prior_grid();
+  merge_splits<QF>(p, row, n);
 }
 
 }  // namespace gqa

@@ -70,6 +70,9 @@ struct SplitParams {
   // slot t of batch row b lives in page block_table[b * max_pages + (t >> page_log2)]
   const int32_t* block_table;
   int page_log2, max_pages, num_pages;
+  // balanced schedule: the least number of tiles a CTA takes (so that no row
+  // is cut into more pieces than the workspace has split slots)
+  int bal_q_min;
 };
 
 template <int QF>
@@ -97,6 +100,12 @@ constexpr int kScaleStageBytes = 2 * 128 * 2;  // int8 cache: K and V row scales
 __host__ __device__ constexpr int mma_smem_bytes(int kvf, int nq) {
   return mma_stages(kvf, nq) * (kStageBytes + kScaleStageBytes + 2 * 8);
 }
+// Balanced schedule (one CTA per resident slot, each taking an equal run of
+// the tiles of all rows): batches up to this size (the prologue scans the
+// lengths), single-token decode only.  Its merge area sits outside the ring.
+constexpr int kBalMaxBatch = 1024;
+constexpr int kBalMergeBytes = kMmaConsumerWarps * kGroup * (kD + 2) * 4;
+static_assert((kMmaThreads + 3 + kBalMaxBatch) * 4 <= kBalMergeBytes, "the length scan uses the merge area");
 // The epilogue merges the 4 warps' states in the ring (idle by then):
 // [warp][column][128] accumulators + [warp][column] max and denominator.
 static_assert(kMmaConsumerWarps * kGroup * 1 * (kD + 2) * 4 <= mma_stages(kKvE4M3, 1) * kStageBytes &&
@@ -179,7 +188,90 @@ __device__ __forceinline__ int qk_dim(int cq, int ks, int pair /*0: a0/b0, 1: a2
   else return 8 * (cq + 4 * (ks >> 1)) + 4 * (ks & 1) + 2 * pair;
 }
 
-template <int KVF, int QF, int NQ>
+// ------------------------------------------------------------ work pieces
+
+// Tokens [t_begin, t_end) of row (b, KV head g) (L = the row's length).  Its
+// FP32 partials go to split slot `slot`; a piece that is its row's only one
+// (`direct`) writes the normalised output itself.
+struct Piece {
+  int b, g, L, t_begin, t_end, slot;
+  bool direct;
+};
+
+template <int kTile, bool BAL>
+struct PieceCursor;
+
+// One piece per CTA (grid = KV heads x batch x splits).
+template <int kTile>
+struct PieceCursor<kTile, false> {
+  Piece one;
+  bool pending = false;
+  __device__ void start_single(int b, int g, int L, int t_begin, int t_end, int slot, bool direct) {
+    one = Piece{b, g, L, t_begin, t_end, slot, direct};
+    pending = true;
+  }
+  __device__ bool next(Piece& pc, int) {
+    if (!pending) return false;
+    pc = one;
+    pending = false;
+    return true;
+  }
+};
+
+// Balanced schedule: the CTA's tiles [x, x1) of the global stream (rows
+// r = 8b + g in order, ceil(L_b / tile) tiles each), cut at row ends.  Row r
+// starts at global tile tf = 8 pb + g nb (pb: tiles per KV head of the rows
+// before b); CTA c holds its piece number c - floor(tf / q), and the row has
+// floor((tf + nb - 1) / q) - floor(tf / q) + 1 pieces.
+template <int kTile>
+struct PieceCursor<kTile, true> {
+  const int32_t* lens;
+  int batch, capacity, b, g, j, nb, L, L_next, pb, x, x1, q;
+  // L0, L1: clamped lengths of rows b0 and b0 + 1 (0 past the batch)
+  __device__ void start(const int32_t* lens_, int B, int C, int b0, int pb0, int L0, int L1, int x0, int x1_,
+                        int q_) {
+    lens = lens_;
+    batch = B;
+    capacity = C;
+    b = b0;
+    pb = pb0;
+    x = x0;
+    x1 = x1_;
+    q = q_;
+    L = L0;
+    L_next = L1;
+    nb = (L + kTile - 1) / kTile;
+    const int within = x0 - kHkv * pb;
+    g = within / nb;
+    j = within - g * nb;
+  }
+  __device__ bool next(Piece& pc, int cta) {
+    if (x >= x1) return false;
+    const int cnt = min(nb - j, x1 - x);
+    const int tf = kHkv * pb + g * nb;
+    const int fq = tf / q;
+    pc = Piece{b, g, L, j * kTile, min(L, (j + cnt) * kTile), cta - fq, (tf + nb - 1) / q == fq};
+    x += cnt;
+    j += cnt;
+    if (j == nb) {
+      j = 0;
+      if (++g == kHkv) {
+        g = 0;
+        pb += nb;
+        while (x < x1) {  // the next row that holds tokens; its successor's
+          ++b;              // length is loaded a whole piece ahead of its use
+          L = L_next;
+          L_next = b + 1 < batch ? min(max(__ldg(lens + b + 1), 0), capacity) : 0;
+          nb = (L + kTile - 1) / kTile;
+          if (nb > 0) break;
+        }
+      }
+    }
+    return true;
+  }
+};
+
+template <int KVF, int QF, int NQ, bool BAL>
 __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
     split_kv_mma_kernel(const __grid_constant__ SplitParams p) {
   constexpr int kMmaStages = mma_stages(KVF, NQ);
@@ -193,35 +285,115 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
   uint16_t* scl = reinterpret_cast<uint16_t*>(smem + kMmaStages * kStageBytes);  // [stage][K|V][128]
   uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(scl) + kMmaStages * kScaleStageBytes);
   uint64_t* empty = full + kMmaStages;
-  float* mrg_acc = reinterpret_cast<float*>(ring);                    // [4 warps][kCols][128] (epilogue)
+  static_assert(!BAL || NQ == 1, "the balanced schedule serves single-token decode");
+  // epilogue merge area [4 warps][kCols][128] + max + denominator: in the idle
+  // ring with one piece per CTA, after the barriers with several (the ring is
+  // then still streaming the next piece)
+  float* mrg_acc = BAL ? reinterpret_cast<float*>(empty + kMmaStages) : reinterpret_cast<float*>(ring);
   float* mrg_m = mrg_acc + kMmaConsumerWarps * kCols * kD;           // [4][kCols]
   float* mrg_l = mrg_m + kMmaConsumerWarps * kCols;                  // [4][kCols]
 
   // Every CTA of this grid is resident or done: let stage 2 be scheduled
   // (it waits for this grid's completion before reading the partials).
   pdl_launch_dependents();
-  const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int C = p.capacity;
-  const int len_raw = __ldg(p.lens + b);
-  const int L = min(max(len_raw, 0), C);
-  if (s == 0 && g == 0 && threadIdx.x == 0 && (len_raw < NQ || len_raw > C))
-    atomicOr(p.flags, GQA_FLAG_LENGTH_CLAMPED);
-  const int t_begin = s * p.chunk;
-  const int t_end = min(L, t_begin + p.chunk);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  if (t_begin >= t_end) {
-    if (p.splits_eff == 1 && threadIdx.x < kMmaConsumerWarps * 32) {
-      // one-split launch with length 0: the output rows are zero
-      const int hh = threadIdx.x / 32, d0 = 4 * (threadIdx.x % 32);
-#pragma unroll
-      for (int jq = 0; jq < NQ; ++jq)
-        *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) +
-                                  ((size_t)((b * NQ + jq) * kHq + g * kGroup + hh) * kD + d0) * 2) =
-            make_uint2(0u, 0u);
+  // ---- this CTA's pieces
+  PieceCursor<T::kTile, BAL> cur;
+  if constexpr (BAL) {
+    // Balanced schedule: the tiles of every (b, KV head) row, rows in order,
+    // form one stream of 8 * sum_b ceil(len_b / tile) tiles; CTA c takes
+    // tiles [c * Q, (c + 1) * Q) with Q = max(ceil(total / grid), q_min).
+    // Prefix sums of tiles per row over the batch (all threads; the merge
+    // area is the scratch, idle until the first epilogue: per-thread sums,
+    // the total, the first row and its prefix, then the clamped lengths).
+    int* scan = reinterpret_cast<int*>(mrg_acc);
+    int* lsh = scan + kMmaThreads + 3;
+    const int B = p.batch;
+    const int per_t = (B + kMmaThreads - 1) / kMmaThreads;
+    const int rb0 = min(B, (int)threadIdx.x * per_t), rb1 = min(B, rb0 + per_t);
+    int mine = 0;
+    bool clamped = false;
+    for (int bb = rb0; bb < rb1; ++bb) {
+      const int lr = __ldg(p.lens + bb);
+      clamped |= lr < 1 || lr > C;
+      lsh[bb] = min(max(lr, 0), C);
+      mine += (lsh[bb] + T::kTile - 1) / T::kTile;
     }
-    return;
+    if (clamped && blockIdx.x == 0) atomicOr(p.flags, GQA_FLAG_LENGTH_CLAMPED);
+    scan[threadIdx.x] = mine;
+    __syncthreads();
+    if (warp == 0) {  // exclusive scan of the 160 per-thread sums
+      constexpr int kPer = (kMmaThreads + 31) / 32;
+      int v[kPer], sum = 0;
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int idx = lane * kPer + k;
+        v[k] = idx < kMmaThreads ? scan[idx] : 0;
+        sum += v[k];
+      }
+      int incl = sum;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += t;
+      }
+      int run = incl - sum;
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int idx = lane * kPer + k;
+        if (idx < kMmaThreads) scan[idx] = run;
+        run += v[k];
+      }
+      if (lane == 31) scan[kMmaThreads] = incl;
+    }
+    __syncthreads();
+    const int total = kHkv * scan[kMmaThreads];
+    const int q = max((total + (int)gridDim.x - 1) / (int)gridDim.x, p.bal_q_min);
+    const int x0 = (int)blockIdx.x * q;
+    if (x0 < total) {  // the thread whose rows hold tile x0 records the first row
+      int pre = scan[threadIdx.x];
+      if (kHkv * pre <= x0 && x0 < kHkv * (pre + mine)) {
+        for (int bb = rb0; bb < rb1; ++bb) {
+          const int nb = (lsh[bb] + T::kTile - 1) / T::kTile;
+          if (x0 < kHkv * (pre + nb)) {
+            scan[kMmaThreads + 1] = bb;
+            scan[kMmaThreads + 2] = pre;
+            break;
+          }
+          pre += nb;
+        }
+      }
+    }
+    __syncthreads();
+    if (x0 >= total) return;  // more CTAs than work
+    const int b0 = scan[kMmaThreads + 1];
+    cur.start(p.lens, B, C, b0, scan[kMmaThreads + 2], lsh[b0], b0 + 1 < B ? lsh[b0 + 1] : 0, x0,
+              min(x0 + q, total), q);
+  } else {
+    // one piece per CTA: split s of row (b, g)
+    const int g = blockIdx.x, b = blockIdx.y, s = blockIdx.z;
+    const int len_raw = __ldg(p.lens + b);
+    const int L = min(max(len_raw, 0), C);
+    if (s == 0 && g == 0 && threadIdx.x == 0 && (len_raw < NQ || len_raw > C))
+      atomicOr(p.flags, GQA_FLAG_LENGTH_CLAMPED);
+    const int t_begin = s * p.chunk;
+    const int t_end = min(L, t_begin + p.chunk);
+    if (t_begin >= t_end) {
+      if (p.splits_eff == 1 && threadIdx.x < kMmaConsumerWarps * 32) {
+        // one-split launch with length 0: the output rows are zero
+        const int hh = threadIdx.x / 32, d0 = 4 * (threadIdx.x % 32);
+#pragma unroll
+        for (int jq = 0; jq < NQ; ++jq)
+          *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) +
+                                    ((size_t)((b * NQ + jq) * kHq + g * kGroup + hh) * kD + d0) * 2) =
+              make_uint2(0u, 0u);
+      }
+      return;
+    }
+    cur.start_single(b, g, L, t_begin, t_end, s, p.splits_eff == 1);
   }
-  const int n_tiles = (t_end - t_begin + T::kTile - 1) / T::kTile;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kMmaStages; ++i) {
@@ -232,12 +404,13 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
   }
   __syncthreads();
   const uint64_t deadline = global_timer_ns() + p.wait_budget_ns;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (warp == kMmaConsumerWarps) {
     // ------------------------------------------------------------ producer
     // The whole warp runs the loop (its lanes fetch block-table entries 32 at
-    // a time); lane 0 waits on the barriers and issues the copies.
+    // a time); lane 0 waits on the barriers and issues the copies.  `it`
+    // counts this CTA's tiles over all its pieces: it sets the ring stage and
+    // barrier phase, so the ring streams straight from one piece to the next.
     const bool paged = p.block_table != nullptr;
     const size_t page_rows = paged ? ((size_t)1 << p.page_log2) : (size_t)C;
     const size_t head_bytes = page_rows * T::kRowBytes;  // one (page, plane, KV head) block
@@ -246,76 +419,82 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
     int last[kMmaStages];  // last tile issued into each stage (-1: none)
 #pragma unroll
     for (int k = 0; k < kMmaStages; ++k) last[k] = -1;
-    int bt_first = -1, bt_val = 0;  // paged: entry bt_first + lane of this row's block table
     bool ok = true;
-    for (int i = 0; i < n_tiles; ++i) {
-      const int st = i % kMmaStages;
-      if (i >= kMmaStages) {
-        int got = 1;
-        if (lane == 0) got = mbar_wait(&empty[st], ((i / kMmaStages) & 1) ^ 1, deadline);
-        if (!__shfl_sync(0xffffffffu, got, 0)) {
-          ok = false;
-          break;
-        }
-      }
-      if (i == p.skip_tile) continue;  // test hook: the consumers' wait on this tile runs out
-      const int t0 = t_begin + i * T::kTile;
-      const int rows = min(T::kTile, t_end - t0);
-      uint8_t* dK = ring + st * kStageBytes;
-      uint8_t* dV = dK + T::kTileBytes;
-      uint32_t scale_bytes = 0;
-      const uint16_t* gsk = nullptr;
-      uint16_t* dsk = scl + st * (kScaleStageBytes / 2);
-      if constexpr (KVF == kKvI8) {
-        // row scales of the tile (contiguous cache): whole 16-byte groups by
-        // bulk copy, the ragged tail (< 8 rows) with plain loads before the arrive
-        gsk = p.kv_scales + ((size_t)b * 2 * kHkv + g) * (size_t)C + t0;
-        const int n8 = rows & ~7;
-        if (lane == 0)
-          for (int r = n8; r < rows; ++r) {
-            dsk[r] = gsk[r];
-            dsk[T::kTile + r] = gsk[(size_t)kHkv * C + r];
+    int it = 0;
+    Piece pc;
+    while (ok && cur.next(pc, blockIdx.x)) {
+      const int b = pc.b, g = pc.g, t_begin = pc.t_begin, t_end = pc.t_end;
+      const int n_tiles = (t_end - t_begin + T::kTile - 1) / T::kTile;
+      int bt_first = -1, bt_val = 0;  // paged: entry bt_first + lane of this row's block table
+      for (int i = 0; i < n_tiles; ++i, ++it) {
+        const int st = it % kMmaStages;
+        if (it >= kMmaStages) {
+          int got = 1;
+          if (lane == 0) got = mbar_wait(&empty[st], ((it / kMmaStages) & 1) ^ 1, deadline);
+          if (!__shfl_sync(0xffffffffu, got, 0)) {
+            ok = false;
+            break;
           }
-        scale_bytes = 2u * (uint32_t)n8 * 2u;
-      }
-      if (lane == 0) mbar_arrive_expect_tx(&full[st], 2u * (uint32_t)rows * T::kRowBytes + scale_bytes);
-      // rows [t0, t0 + rows) in page segments; a contiguous cache is one page per batch row
-      for (int t = t0; t < t0 + rows;) {
-        size_t page = (size_t)b;
-        int in_page = t, seg_end = t0 + rows;
-        if (paged) {
-          const int pg = t >> p.page_log2;
-          if (bt_first < 0 || pg >= bt_first + 32) {
-            bt_first = pg;
-            const int e = pg + lane;
-            bt_val = e < p.max_pages ? __ldg(p.block_table + (size_t)b * p.max_pages + e) : 0;
+        }
+        if (it == p.skip_tile) continue;  // test hook: the consumers' wait on this tile runs out
+        const int t0 = t_begin + i * T::kTile;
+        const int rows = min(T::kTile, t_end - t0);
+        uint8_t* dK = ring + st * kStageBytes;
+        uint8_t* dV = dK + T::kTileBytes;
+        uint32_t scale_bytes = 0;
+        const uint16_t* gsk = nullptr;
+        uint16_t* dsk = scl + st * (kScaleStageBytes / 2);
+        if constexpr (KVF == kKvI8) {
+          // row scales of the tile (contiguous cache): whole 16-byte groups by
+          // bulk copy, the ragged tail (< 8 rows) with plain loads before the arrive
+          gsk = p.kv_scales + ((size_t)b * 2 * kHkv + g) * (size_t)C + t0;
+          const int n8 = rows & ~7;
+          if (lane == 0)
+            for (int r = n8; r < rows; ++r) {
+              dsk[r] = gsk[r];
+              dsk[T::kTile + r] = gsk[(size_t)kHkv * C + r];
+            }
+          scale_bytes = 2u * (uint32_t)n8 * 2u;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(&full[st], 2u * (uint32_t)rows * T::kRowBytes + scale_bytes);
+        // rows [t0, t0 + rows) in page segments; a contiguous cache is one page per batch row
+        for (int t = t0; t < t0 + rows;) {
+          size_t page = (size_t)b;
+          int in_page = t, seg_end = t0 + rows;
+          if (paged) {
+            const int pg = t >> p.page_log2;
+            if (bt_first < 0 || pg >= bt_first + 32) {
+              bt_first = pg;
+              const int e = pg + lane;
+              bt_val = e < p.max_pages ? __ldg(p.block_table + (size_t)b * p.max_pages + e) : 0;
+            }
+            int id = __shfl_sync(0xffffffffu, bt_val, pg - bt_first);
+            if (id < 0 || id >= p.num_pages) {  // out-of-contract page id: clamp, flag, never fault
+              if (lane == 0) atomicOr(p.flags, GQA_FLAG_PAGE_CLAMPED);
+              id = min(max(id, 0), p.num_pages - 1);
+            }
+            page = (size_t)id;
+            in_page = t - (pg << p.page_log2);
+            seg_end = min(t0 + rows, (pg + 1) << p.page_log2);
           }
-          int id = __shfl_sync(0xffffffffu, bt_val, pg - bt_first);
-          if (id < 0 || id >= p.num_pages) {  // out-of-contract page id: clamp, flag, never fault
-            if (lane == 0) atomicOr(p.flags, GQA_FLAG_PAGE_CLAMPED);
-            id = min(max(id, 0), p.num_pages - 1);
+          if (lane == 0) {
+            const uint32_t seg_bytes = (uint32_t)(seg_end - t) * T::kRowBytes;
+            const uint8_t* src = base + (page * 2 * kHkv + g) * head_bytes + (size_t)in_page * T::kRowBytes;
+            bulk_load(dK + (t - t0) * T::kRowBytes, src, seg_bytes, &full[st], pol);
+            bulk_load(dV + (t - t0) * T::kRowBytes, src + kHkv * head_bytes, seg_bytes, &full[st], pol);
           }
-          page = (size_t)id;
-          in_page = t - (pg << p.page_log2);
-          seg_end = min(t0 + rows, (pg + 1) << p.page_log2);
+          t = seg_end;
         }
-        if (lane == 0) {
-          const uint32_t seg_bytes = (uint32_t)(seg_end - t) * T::kRowBytes;
-          const uint8_t* src = base + (page * 2 * kHkv + g) * head_bytes + (size_t)in_page * T::kRowBytes;
-          bulk_load(dK + (t - t0) * T::kRowBytes, src, seg_bytes, &full[st], pol);
-          bulk_load(dV + (t - t0) * T::kRowBytes, src + kHkv * head_bytes, seg_bytes, &full[st], pol);
+        if constexpr (KVF == kKvI8) {
+          if (lane == 0 && scale_bytes > 0) {
+            bulk_load(dsk, gsk, scale_bytes / 2, &full[st], pol);
+            bulk_load(dsk + T::kTile, gsk + (size_t)kHkv * C, scale_bytes / 2, &full[st], pol);
+          }
         }
-        t = seg_end;
+  #pragma unroll
+        for (int k = 0; k < kMmaStages; ++k)
+          if (k == st) last[k] = it;
       }
-      if constexpr (KVF == kKvI8) {
-        if (lane == 0 && scale_bytes > 0) {
-          bulk_load(dsk, gsk, scale_bytes / 2, &full[st], pol);
-          bulk_load(dsk + T::kTile, gsk + (size_t)kHkv * C, scale_bytes / 2, &full[st], pol);
-        }
-      }
-#pragma unroll
-      for (int k = 0; k < kMmaStages; ++k)
-        if (k == st) last[k] = i;
     }
     if (lane == 0) {
       if (!ok) atomicOr(p.flags, GQA_FLAG_WAIT_TIMEOUT);
@@ -330,253 +509,229 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
 
   // -------------------------------------------------------------- consumers
   const int gq = lane >> 2, cq = lane & 3;
-  // Column n of n-tile nt is (query token 2nt + n/4, head n%4).  This lane's
-  // score/output columns are n = 2cq, 2cq+1: query token 2nt + cq/2, heads
-  // 2(cq%2) and 2(cq%2)+1.  A column past the window is zero padding.
-  int lim[kNT];  // slots below lim[nt] are attended by this lane's columns
-#pragma unroll
-  for (int nt = 0; nt < kNT; ++nt) {
-    const int jq = 2 * nt + (cq >> 1);
-    lim[nt] = jq < NQ ? min(t_end, L - NQ + 1 + jq) : 0;
-  }
-
-  // Q^T B-fragments: column gq of each n-tile, unscaled (zero for padding).
-  uint32_t qb[kNT][8][2];
-#pragma unroll
-  for (int nt = 0; nt < kNT; ++nt) {
-    const int jq = 2 * nt + (gq >> 2);
-    const bool real = jq < NQ;
-    const uint16_t* qrow = static_cast<const uint16_t*>(p.q) +
-                           ((size_t)((b * NQ + (real ? jq : 0)) * kHq) + g * kGroup + (gq & 3)) * kD;
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks)
-#pragma unroll
-      for (int pr = 0; pr < 2; ++pr) {
-        const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(qrow + qk_dim<KVF>(cq, ks, pr)));
-        uint32_t v = w;
-        if constexpr (is_8bit(KVF) && QF == kQBF16) v = pack_f16_satfinite(bf16_lo_to_f32(w), bf16_hi_to_f32(w));
-        qb[nt][ks][pr] = real ? v : 0u;
-      }
-  }
-
-  float o[kNT][8][4];
-  float m[kNT][2], l[kNT][2];  // per column: running max (log2 domain), this lane's denominator share
-#pragma unroll
-  for (int nt = 0; nt < kNT; ++nt) {
-    m[nt][0] = m[nt][1] = -INFINITY;
-    l[nt][0] = l[nt][1] = 0.f;
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) o[nt][mt][e] = 0.f;
-  }
   const float sl2 = p.scale_log2;
   // P^T shuffle sources: tokens 2cq and 2cq+1 of the slab, column pair gq/2
   const int src0 = 4 * (2 * cq) + (gq >> 1), src1 = 4 * (2 * cq + 1) + (gq >> 1);
   const uint32_t half_sel = (gq & 1) ? 0x7632u : 0x5410u;
-
-  for (int i = 0; i < n_tiles; ++i) {
-    const int st = i % kMmaStages;
-    if (!mbar_wait(&full[st], (i / kMmaStages) & 1, deadline)) {
-      if (lane == 0) atomicOr(p.flags, GQA_FLAG_WAIT_TIMEOUT);
-      break;
-    }
-    const uint8_t* sK = ring + st * kStageBytes;
-    const uint8_t* sV = sK + T::kTileBytes;
-    const int tile_t0 = t_begin + i * T::kTile;
-    const int rows = min(T::kTile, t_end - tile_t0);
-    // int8: K and V row scales of this lane's tokens (R+gq, R+gq+8 of each slab)
-    float sk[kSlabs][2], sv[kSlabs][2];
-    if constexpr (KVF == kKvI8) {
-      const uint16_t* tsk = scl + st * (kScaleStageBytes / 2);
+  bool alive = true;  // false once a wait has run out: the remaining tiles are skipped
+  int it = 0;         // this CTA's tiles over all its pieces (ring stage and phase)
+  Piece pc;
+  while (cur.next(pc, blockIdx.x)) {
+    const int b = pc.b, g = pc.g, L = pc.L, t_begin = pc.t_begin, t_end = pc.t_end;
+    const int n_tiles = (t_end - t_begin + T::kTile - 1) / T::kTile;
+    // Column n of n-tile nt is (query token 2nt + n/4, head n%4).  This lane's
+    // score/output columns are n = 2cq, 2cq+1: query token 2nt + cq/2, heads
+    // 2(cq%2) and 2(cq%2)+1.  A column past the window is zero padding.
+    int lim[kNT];  // slots below lim[nt] are attended by this lane's columns
 #pragma unroll
-      for (int sl = 0; sl < kSlabs; ++sl)
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int r = (warp * kSlabs + sl) * 16 + gq + 8 * u;
-          sk[sl][u] = r < rows ? __uint_as_float((uint32_t)tsk[r] << 16) : 0.f;
-          sv[sl][u] = r < rows ? __uint_as_float((uint32_t)tsk[T::kTile + r] << 16) : 0.f;
-        }
+    for (int nt = 0; nt < kNT; ++nt) {
+      const int jq = 2 * nt + (cq >> 1);
+      lim[nt] = jq < NQ ? min(t_end, L - NQ + 1 + jq) : 0;
     }
 
-#pragma unroll
-    for (int sl = 0; sl < kSlabs; ++sl) {
-      const int R = (warp * kSlabs + sl) * 16;  // first tile row of this slab
-      if (R >= rows) break;                     // warp-uniform
-      const bool partial = R + 16 > rows;
+    // Q^T B-fragments: column gq of each n-tile, unscaled (zero for padding).
+    uint32_t qb[kNT][8][2];
+  #pragma unroll
+    for (int nt = 0; nt < kNT; ++nt) {
+      const int jq = 2 * nt + (gq >> 2);
+      const bool real = jq < NQ;
+      const uint16_t* qrow = static_cast<const uint16_t*>(p.q) +
+                             ((size_t)((b * NQ + (real ? jq : 0)) * kHq) + g * kGroup + (gq & 3)) * kD;
+  #pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+  #pragma unroll
+        for (int pr = 0; pr < 2; ++pr) {
+          const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(qrow + qk_dim<KVF>(cq, ks, pr)));
+          uint32_t v = w;
+          if constexpr (is_8bit(KVF) && QF == kQBF16) v = pack_f16_satfinite(bf16_lo_to_f32(w), bf16_hi_to_f32(w));
+          qb[nt][ks][pr] = real ? v : 0u;
+        }
+    }
 
-      // ---- scores: S^T[16 tokens x 8] = K . Q^T for each n-tile
-      float sc[kNT][4];
+    float o[kNT][8][4];
+    float m[kNT][2], l[kNT][2];  // per column: running max (log2 domain), this lane's denominator share
 #pragma unroll
-      for (int nt = 0; nt < kNT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-      {
-        const uint8_t* k0 = sK + (R + gq) * T::kRowBytes;
-        const uint8_t* k1 = k0 + 8 * T::kRowBytes;
-        if constexpr (is_8bit(KVF)) {
+    for (int nt = 0; nt < kNT; ++nt) {
+      m[nt][0] = m[nt][1] = -INFINITY;
+      l[nt][0] = l[nt][1] = 0.f;
 #pragma unroll
-          for (int ci = 0; ci < 2; ++ci) {
-            const uint4 x = *reinterpret_cast<const uint4*>(k0 + 16 * (cq + 4 * ci));
-            const uint4 y = *reinterpret_cast<const uint4*>(k1 + 16 * (cq + 4 * ci));
-            const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+      for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
-            for (int s4 = 0; s4 < 4; ++s4) {
-              const int ks = 4 * ci + s4;
-              uint32_t a0, a1, a2, a3;
-              widen4<KVF>(xs[s4], a0, a2);  // row gq: dims (4s,4s+1), (4s+2,4s+3)
-              widen4<KVF>(ys[s4], a1, a3);  // row gq+8
-#pragma unroll
-              for (int nt = 0; nt < kNT; ++nt) mma16816<false>(sc[nt], a0, a1, a2, a3, qb[nt][ks][0], qb[nt][ks][1]);
-            }
-          }
-        } else {
-#pragma unroll
-          for (int ci = 0; ci < 4; ++ci) {
-            const uint4 x = *reinterpret_cast<const uint4*>(k0 + 16 * (cq + 4 * ci));
-            const uint4 y = *reinterpret_cast<const uint4*>(k1 + 16 * (cq + 4 * ci));
-#pragma unroll
-            for (int nt = 0; nt < kNT; ++nt) {
-              mma16816<kBF16>(sc[nt], x.x, y.x, x.y, y.y, qb[nt][2 * ci][0], qb[nt][2 * ci][1]);
-              mma16816<kBF16>(sc[nt], x.z, y.z, x.w, y.w, qb[nt][2 * ci + 1][0], qb[nt][2 * ci + 1][1]);
-            }
-          }
-        }
+        for (int e = 0; e < 4; ++e) o[nt][mt][e] = 0.f;
+    }
+
+    for (int i = 0; i < n_tiles; ++i, ++it) {
+      const int st = it % kMmaStages;
+      if (alive && !mbar_wait(&full[st], (it / kMmaStages) & 1, deadline)) {
+        if (lane == 0) atomicOr(p.flags, GQA_FLAG_WAIT_TIMEOUT);
+        alive = false;
       }
-      // sc[nt]: [0] token R+gq column 2cq, [1] token R+gq column 2cq+1, [2]/[3] token R+gq+8
-      const int ta = tile_t0 + R + gq, tb = ta + 8;
-      float x[kNT][4];
-#pragma unroll
-      for (int nt = 0; nt < kNT; ++nt) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) x[nt][e] = sc[nt][e] * sl2;
-        if constexpr (KVF == kKvI8) {  // per-row K scale multiplies that token's scores
-          x[nt][0] *= sk[sl][0];
-          x[nt][1] *= sk[sl][0];
-          x[nt][2] *= sk[sl][1];
-          x[nt][3] *= sk[sl][1];
-        }
-        if (ta >= lim[nt]) x[nt][0] = x[nt][1] = -INFINITY;  // select, never multiply
-        if (tb >= lim[nt]) x[nt][2] = x[nt][3] = -INFINITY;
+      if (!alive) continue;
+      const uint8_t* sK = ring + st * kStageBytes;
+      const uint8_t* sV = sK + T::kTileBytes;
+      const int tile_t0 = t_begin + i * T::kTile;
+      const int rows = min(T::kTile, t_end - tile_t0);
+      // int8: K and V row scales of this lane's tokens (R+gq, R+gq+8 of each slab)
+      float sk[kSlabs][2], sv[kSlabs][2];
+      if constexpr (KVF == kKvI8) {
+        const uint16_t* tsk = scl + st * (kScaleStageBytes / 2);
+  #pragma unroll
+        for (int sl = 0; sl < kSlabs; ++sl)
+  #pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int r = (warp * kSlabs + sl) * 16 + gq + 8 * u;
+            sk[sl][u] = r < rows ? __uint_as_float((uint32_t)tsk[r] << 16) : 0.f;
+            sv[sl][u] = r < rows ? __uint_as_float((uint32_t)tsk[T::kTile + r] << 16) : 0.f;
+          }
       }
 
-      // ---- online softmax per column (max over the slab's 16 tokens)
-      float nm[kNT][2];
-      bool grow = false;
-#pragma unroll
-      for (int nt = 0; nt < kNT; ++nt) {
-        float h0 = fmaxf(x[nt][0], x[nt][2]), h1 = fmaxf(x[nt][1], x[nt][3]);
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-          h0 = fmaxf(h0, __shfl_xor_sync(0xffffffffu, h0, off));
-          h1 = fmaxf(h1, __shfl_xor_sync(0xffffffffu, h1, off));
+  #pragma unroll
+      for (int sl = 0; sl < kSlabs; ++sl) {
+        const int R = (warp * kSlabs + sl) * 16;  // first tile row of this slab
+        if (R >= rows) break;                     // warp-uniform
+        const bool partial = R + 16 > rows;
+
+        // ---- scores: S^T[16 tokens x 8] = K . Q^T for each n-tile
+        float sc[kNT][4];
+  #pragma unroll
+        for (int nt = 0; nt < kNT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+        {
+          const uint8_t* k0 = sK + (R + gq) * T::kRowBytes;
+          const uint8_t* k1 = k0 + 8 * T::kRowBytes;
+          if constexpr (is_8bit(KVF)) {
+  #pragma unroll
+            for (int ci = 0; ci < 2; ++ci) {
+              const uint4 x = *reinterpret_cast<const uint4*>(k0 + 16 * (cq + 4 * ci));
+              const uint4 y = *reinterpret_cast<const uint4*>(k1 + 16 * (cq + 4 * ci));
+              const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+  #pragma unroll
+              for (int s4 = 0; s4 < 4; ++s4) {
+                const int ks = 4 * ci + s4;
+                uint32_t a0, a1, a2, a3;
+                widen4<KVF>(xs[s4], a0, a2);  // row gq: dims (4s,4s+1), (4s+2,4s+3)
+                widen4<KVF>(ys[s4], a1, a3);  // row gq+8
+  #pragma unroll
+                for (int nt = 0; nt < kNT; ++nt) mma16816<false>(sc[nt], a0, a1, a2, a3, qb[nt][ks][0], qb[nt][ks][1]);
+              }
+            }
+          } else {
+  #pragma unroll
+            for (int ci = 0; ci < 4; ++ci) {
+              const uint4 x = *reinterpret_cast<const uint4*>(k0 + 16 * (cq + 4 * ci));
+              const uint4 y = *reinterpret_cast<const uint4*>(k1 + 16 * (cq + 4 * ci));
+  #pragma unroll
+              for (int nt = 0; nt < kNT; ++nt) {
+                mma16816<kBF16>(sc[nt], x.x, y.x, x.y, y.y, qb[nt][2 * ci][0], qb[nt][2 * ci][1]);
+                mma16816<kBF16>(sc[nt], x.z, y.z, x.w, y.w, qb[nt][2 * ci + 1][0], qb[nt][2 * ci + 1][1]);
+              }
+            }
+          }
         }
-        nm[nt][0] = fmaxf(m[nt][0], h0);
-        nm[nt][1] = fmaxf(m[nt][1], h1);
-        grow |= nm[nt][0] > m[nt][0] || nm[nt][1] > m[nt][1];
-      }
-      if (__any_sync(0xffffffffu, grow)) {
-#pragma unroll
+        // sc[nt]: [0] token R+gq column 2cq, [1] token R+gq column 2cq+1, [2]/[3] token R+gq+8
+        const int ta = tile_t0 + R + gq, tb = ta + 8;
+        float x[kNT][4];
+  #pragma unroll
         for (int nt = 0; nt < kNT; ++nt) {
-          // 0 when the old max was -inf; 1 when unchanged (also covers -inf == -inf)
-          const float a0 = nm[nt][0] == m[nt][0] ? 1.f : ex2(m[nt][0] - nm[nt][0]);
-          const float a1 = nm[nt][1] == m[nt][1] ? 1.f : ex2(m[nt][1] - nm[nt][1]);
-          l[nt][0] *= a0;
-          l[nt][1] *= a1;
-#pragma unroll
-          for (int mt = 0; mt < 8; ++mt) {
-            o[nt][mt][0] *= a0;
-            o[nt][mt][2] *= a0;
-            o[nt][mt][1] *= a1;
-            o[nt][mt][3] *= a1;
+  #pragma unroll
+          for (int e = 0; e < 4; ++e) x[nt][e] = sc[nt][e] * sl2;
+          if constexpr (KVF == kKvI8) {  // per-row K scale multiplies that token's scores
+            x[nt][0] *= sk[sl][0];
+            x[nt][1] *= sk[sl][0];
+            x[nt][2] *= sk[sl][1];
+            x[nt][3] *= sk[sl][1];
           }
-          m[nt][0] = nm[nt][0];
-          m[nt][1] = nm[nt][1];
+          if (ta >= lim[nt]) x[nt][0] = x[nt][1] = -INFINITY;  // select, never multiply
+          if (tb >= lim[nt]) x[nt][2] = x[nt][3] = -INFINITY;
         }
-      }
 
-      // ---- P^T B-fragments per n-tile: lane (gq, cq) needs column gq of tokens
-      // 2cq, 2cq+1 (b0) and 2cq+8, 2cq+9 (b1), held by lanes src0/src1 as
-      // (column pair) packs.
-      uint32_t bh[kNT][2], bl[kNT][2];
-#pragma unroll
-      for (int nt = 0; nt < kNT; ++nt) {
-        const float p0 = x[nt][0] == -INFINITY ? 0.f : ex2(x[nt][0] - m[nt][0]);
-        const float p1 = x[nt][1] == -INFINITY ? 0.f : ex2(x[nt][1] - m[nt][1]);
-        const float p2 = x[nt][2] == -INFINITY ? 0.f : ex2(x[nt][2] - m[nt][0]);
-        const float p3 = x[nt][3] == -INFINITY ? 0.f : ex2(x[nt][3] - m[nt][1]);
-        bl[nt][0] = bl[nt][1] = 0u;
-        if constexpr (kBF16) {
-          const uint32_t ph_a = pack_bf16(p0, p1), ph_b = pack_bf16(p2, p3);
-          const uint32_t pl_a = pack_bf16(p0 - bf16_lo_to_f32(ph_a), p1 - bf16_hi_to_f32(ph_a));
-          const uint32_t pl_b = pack_bf16(p2 - bf16_lo_to_f32(ph_b), p3 - bf16_hi_to_f32(ph_b));
-          l[nt][0] += bf16_lo_to_f32(ph_a) + bf16_lo_to_f32(pl_a) + bf16_lo_to_f32(ph_b) + bf16_lo_to_f32(pl_b);
-          l[nt][1] += bf16_hi_to_f32(ph_a) + bf16_hi_to_f32(pl_a) + bf16_hi_to_f32(ph_b) + bf16_hi_to_f32(pl_b);
-          bh[nt][0] = prmt(__shfl_sync(0xffffffffu, ph_a, src0), __shfl_sync(0xffffffffu, ph_a, src1), half_sel);
-          bh[nt][1] = prmt(__shfl_sync(0xffffffffu, ph_b, src0), __shfl_sync(0xffffffffu, ph_b, src1), half_sel);
-          bl[nt][0] = prmt(__shfl_sync(0xffffffffu, pl_a, src0), __shfl_sync(0xffffffffu, pl_a, src1), half_sel);
-          bl[nt][1] = prmt(__shfl_sync(0xffffffffu, pl_b, src0), __shfl_sync(0xffffffffu, pl_b, src1), half_sel);
-        } else if constexpr (KVF == kKvI8) {
-          // the per-row V scale joins the weight of its token; the denominator
-          // keeps the unscaled weights
-          const uint32_t pa = pack_f16(p0 * sv[sl][0], p1 * sv[sl][0]);
-          const uint32_t pb = pack_f16(p2 * sv[sl][1], p3 * sv[sl][1]);
-          l[nt][0] += p0 + p2;
-          l[nt][1] += p1 + p3;
-          bh[nt][0] = prmt(__shfl_sync(0xffffffffu, pa, src0), __shfl_sync(0xffffffffu, pa, src1), half_sel);
-          bh[nt][1] = prmt(__shfl_sync(0xffffffffu, pb, src0), __shfl_sync(0xffffffffu, pb, src1), half_sel);
-        } else {
-          const uint32_t pa = pack_f16(p0, p1), pb = pack_f16(p2, p3);
-          // the denominator sums the same rounded weights the tensor core multiplies
-          const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&pa));
-          const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&pb));
-          l[nt][0] += fa.x + fb.x;
-          l[nt][1] += fa.y + fb.y;
-          bh[nt][0] = prmt(__shfl_sync(0xffffffffu, pa, src0), __shfl_sync(0xffffffffu, pa, src1), half_sel);
-          bh[nt][1] = prmt(__shfl_sync(0xffffffffu, pb, src0), __shfl_sync(0xffffffffu, pb, src1), half_sel);
+        // ---- online softmax per column (max over the slab's 16 tokens)
+        float nm[kNT][2];
+        bool grow = false;
+  #pragma unroll
+        for (int nt = 0; nt < kNT; ++nt) {
+          float h0 = fmaxf(x[nt][0], x[nt][2]), h1 = fmaxf(x[nt][1], x[nt][3]);
+  #pragma unroll
+          for (int off = 4; off < 32; off <<= 1) {
+            h0 = fmaxf(h0, __shfl_xor_sync(0xffffffffu, h0, off));
+            h1 = fmaxf(h1, __shfl_xor_sync(0xffffffffu, h1, off));
+          }
+          nm[nt][0] = fmaxf(m[nt][0], h0);
+          nm[nt][1] = fmaxf(m[nt][1], h1);
+          grow |= nm[nt][0] > m[nt][0] || nm[nt][1] > m[nt][1];
         }
-      }
+        if (__any_sync(0xffffffffu, grow)) {
+  #pragma unroll
+          for (int nt = 0; nt < kNT; ++nt) {
+            // 0 when the old max was -inf; 1 when unchanged (also covers -inf == -inf)
+            const float a0 = nm[nt][0] == m[nt][0] ? 1.f : ex2(m[nt][0] - nm[nt][0]);
+            const float a1 = nm[nt][1] == m[nt][1] ? 1.f : ex2(m[nt][1] - nm[nt][1]);
+            l[nt][0] *= a0;
+            l[nt][1] *= a1;
+  #pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+              o[nt][mt][0] *= a0;
+              o[nt][mt][2] *= a0;
+              o[nt][mt][1] *= a1;
+              o[nt][mt][3] *= a1;
+            }
+            m[nt][0] = nm[nt][0];
+            m[nt][1] = nm[nt][1];
+          }
+        }
 
-      // ---- O^T[128 dims x 8] += V^T . P^T per n-tile: lane (gq, cq) reads dims
-      // 16gq..16gq+15 of tokens R+2cq, R+2cq+1, R+2cq+8, R+2cq+9.
-      const int r0 = R + 2 * cq;
-      const uint8_t* v0 = sV + r0 * T::kRowBytes;
-      const bool ok0 = !partial || r0 < rows, ok1 = !partial || r0 + 1 < rows;
-      const bool ok2 = !partial || r0 + 8 < rows, ok3 = !partial || r0 + 9 < rows;
-      if constexpr (is_8bit(KVF)) {
-        uint4 w0 = *reinterpret_cast<const uint4*>(v0 + 16 * gq);
-        uint4 w1 = *reinterpret_cast<const uint4*>(v0 + T::kRowBytes + 16 * gq);
-        uint4 w2 = *reinterpret_cast<const uint4*>(v0 + 8 * T::kRowBytes + 16 * gq);
-        uint4 w3 = *reinterpret_cast<const uint4*>(v0 + 9 * T::kRowBytes + 16 * gq);
-        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-        if (!ok0) w0 = z;
-        if (!ok1) w1 = z;
-        if (!ok2) w2 = z;
-        if (!ok3) w3 = z;
-        const uint32_t a[4] = {w0.x, w0.y, w0.z, w0.w}, bq[4] = {w1.x, w1.y, w1.z, w1.w};
-        const uint32_t c[4] = {w2.x, w2.y, w2.z, w2.w}, d[4] = {w3.x, w3.y, w3.z, w3.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {  // word j: dims 16gq+4j .. +3 -> m-tiles 2j, 2j+1
-          // pair the two tokens of each k-step: bytes [r0.d, r1.d, r0.d', r1.d']
-          uint32_t A0, A1, A2, A3;
-          widen4<KVF>(prmt(a[j], bq[j], 0x5140u), A0, A1);  // dims 4j, 4j+1 of tokens r0, r0+1
-          widen4<KVF>(prmt(c[j], d[j], 0x5140u), A2, A3);   // tokens r0+8, r0+9
-#pragma unroll
-          for (int nt = 0; nt < kNT; ++nt) mma16816<false>(o[nt][2 * j], A0, A1, A2, A3, bh[nt][0], bh[nt][1]);
-          widen4<KVF>(prmt(a[j], bq[j], 0x7362u), A0, A1);  // dims 4j+2, 4j+3
-          widen4<KVF>(prmt(c[j], d[j], 0x7362u), A2, A3);
-#pragma unroll
-          for (int nt = 0; nt < kNT; ++nt)
-            mma16816<false>(o[nt][2 * j + 1], A0, A1, A2, A3, bh[nt][0], bh[nt][1]);
+        // ---- P^T B-fragments per n-tile: lane (gq, cq) needs column gq of tokens
+        // 2cq, 2cq+1 (b0) and 2cq+8, 2cq+9 (b1), held by lanes src0/src1 as
+        // (column pair) packs.
+        uint32_t bh[kNT][2], bl[kNT][2];
+  #pragma unroll
+        for (int nt = 0; nt < kNT; ++nt) {
+          const float p0 = x[nt][0] == -INFINITY ? 0.f : ex2(x[nt][0] - m[nt][0]);
+          const float p1 = x[nt][1] == -INFINITY ? 0.f : ex2(x[nt][1] - m[nt][1]);
+          const float p2 = x[nt][2] == -INFINITY ? 0.f : ex2(x[nt][2] - m[nt][0]);
+          const float p3 = x[nt][3] == -INFINITY ? 0.f : ex2(x[nt][3] - m[nt][1]);
+          bl[nt][0] = bl[nt][1] = 0u;
+          if constexpr (kBF16) {
+            const uint32_t ph_a = pack_bf16(p0, p1), ph_b = pack_bf16(p2, p3);
+            const uint32_t pl_a = pack_bf16(p0 - bf16_lo_to_f32(ph_a), p1 - bf16_hi_to_f32(ph_a));
+            const uint32_t pl_b = pack_bf16(p2 - bf16_lo_to_f32(ph_b), p3 - bf16_hi_to_f32(ph_b));
+            l[nt][0] += bf16_lo_to_f32(ph_a) + bf16_lo_to_f32(pl_a) + bf16_lo_to_f32(ph_b) + bf16_lo_to_f32(pl_b);
+            l[nt][1] += bf16_hi_to_f32(ph_a) + bf16_hi_to_f32(pl_a) + bf16_hi_to_f32(ph_b) + bf16_hi_to_f32(pl_b);
+            bh[nt][0] = prmt(__shfl_sync(0xffffffffu, ph_a, src0), __shfl_sync(0xffffffffu, ph_a, src1), half_sel);
+            bh[nt][1] = prmt(__shfl_sync(0xffffffffu, ph_b, src0), __shfl_sync(0xffffffffu, ph_b, src1), half_sel);
+            bl[nt][0] = prmt(__shfl_sync(0xffffffffu, pl_a, src0), __shfl_sync(0xffffffffu, pl_a, src1), half_sel);
+            bl[nt][1] = prmt(__shfl_sync(0xffffffffu, pl_b, src0), __shfl_sync(0xffffffffu, pl_b, src1), half_sel);
+          } else if constexpr (KVF == kKvI8) {
+            // the per-row V scale joins the weight of its token; the denominator
+            // keeps the unscaled weights
+            const uint32_t pa = pack_f16(p0 * sv[sl][0], p1 * sv[sl][0]);
+            const uint32_t pb = pack_f16(p2 * sv[sl][1], p3 * sv[sl][1]);
+            l[nt][0] += p0 + p2;
+            l[nt][1] += p1 + p3;
+            bh[nt][0] = prmt(__shfl_sync(0xffffffffu, pa, src0), __shfl_sync(0xffffffffu, pa, src1), half_sel);
+            bh[nt][1] = prmt(__shfl_sync(0xffffffffu, pb, src0), __shfl_sync(0xffffffffu, pb, src1), half_sel);
+          } else {
+            const uint32_t pa = pack_f16(p0, p1), pb = pack_f16(p2, p3);
+            // the denominator sums the same rounded weights the tensor core multiplies
+            const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&pa));
+            const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&pb));
+            l[nt][0] += fa.x + fb.x;
+            l[nt][1] += fa.y + fb.y;
+            bh[nt][0] = prmt(__shfl_sync(0xffffffffu, pa, src0), __shfl_sync(0xffffffffu, pa, src1), half_sel);
+            bh[nt][1] = prmt(__shfl_sync(0xffffffffu, pb, src0), __shfl_sync(0xffffffffu, pb, src1), half_sel);
+          }
         }
-      } else {
-        const uint8_t* v1 = v0 + T::kRowBytes;
-        const uint8_t* v2 = v0 + 8 * T::kRowBytes;
-        const uint8_t* v3 = v0 + 9 * T::kRowBytes;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {  // dims 16gq + 8half .. +7 -> m-tiles 4half..4half+3
-          uint4 w0 = *reinterpret_cast<const uint4*>(v0 + 32 * gq + 16 * half);
-          uint4 w1 = *reinterpret_cast<const uint4*>(v1 + 32 * gq + 16 * half);
-          uint4 w2 = *reinterpret_cast<const uint4*>(v2 + 32 * gq + 16 * half);
-          uint4 w3 = *reinterpret_cast<const uint4*>(v3 + 32 * gq + 16 * half);
+
+        // ---- O^T[128 dims x 8] += V^T . P^T per n-tile: lane (gq, cq) reads dims
+        // 16gq..16gq+15 of tokens R+2cq, R+2cq+1, R+2cq+8, R+2cq+9.
+        const int r0 = R + 2 * cq;
+        const uint8_t* v0 = sV + r0 * T::kRowBytes;
+        const bool ok0 = !partial || r0 < rows, ok1 = !partial || r0 + 1 < rows;
+        const bool ok2 = !partial || r0 + 8 < rows, ok3 = !partial || r0 + 9 < rows;
+        if constexpr (is_8bit(KVF)) {
+          uint4 w0 = *reinterpret_cast<const uint4*>(v0 + 16 * gq);
+          uint4 w1 = *reinterpret_cast<const uint4*>(v0 + T::kRowBytes + 16 * gq);
+          uint4 w2 = *reinterpret_cast<const uint4*>(v0 + 8 * T::kRowBytes + 16 * gq);
+          uint4 w3 = *reinterpret_cast<const uint4*>(v0 + 9 * T::kRowBytes + 16 * gq);
           const uint4 z = make_uint4(0u, 0u, 0u, 0u);
           if (!ok0) w0 = z;
           if (!ok1) w1 = z;
@@ -584,89 +739,123 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
           if (!ok3) w3 = z;
           const uint32_t a[4] = {w0.x, w0.y, w0.z, w0.w}, bq[4] = {w1.x, w1.y, w1.z, w1.w};
           const uint32_t c[4] = {w2.x, w2.y, w2.z, w2.w}, d[4] = {w3.x, w3.y, w3.z, w3.w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {  // word j: dims 16gq + 8half + 2j, +1 -> m-tile 4half + j
-            const uint32_t A0 = prmt(a[j], bq[j], 0x5410u), A1 = prmt(a[j], bq[j], 0x7632u);
-            const uint32_t A2 = prmt(c[j], d[j], 0x5410u), A3 = prmt(c[j], d[j], 0x7632u);
-#pragma unroll
-            for (int nt = 0; nt < kNT; ++nt) {
-              mma16816<kBF16>(o[nt][4 * half + j], A0, A1, A2, A3, bh[nt][0], bh[nt][1]);
-              if constexpr (kBF16) mma16816<kBF16>(o[nt][4 * half + j], A0, A1, A2, A3, bl[nt][0], bl[nt][1]);
+  #pragma unroll
+          for (int j = 0; j < 4; ++j) {  // word j: dims 16gq+4j .. +3 -> m-tiles 2j, 2j+1
+            // pair the two tokens of each k-step: bytes [r0.d, r1.d, r0.d', r1.d']
+            uint32_t A0, A1, A2, A3;
+            widen4<KVF>(prmt(a[j], bq[j], 0x5140u), A0, A1);  // dims 4j, 4j+1 of tokens r0, r0+1
+            widen4<KVF>(prmt(c[j], d[j], 0x5140u), A2, A3);   // tokens r0+8, r0+9
+  #pragma unroll
+            for (int nt = 0; nt < kNT; ++nt) mma16816<false>(o[nt][2 * j], A0, A1, A2, A3, bh[nt][0], bh[nt][1]);
+            widen4<KVF>(prmt(a[j], bq[j], 0x7362u), A0, A1);  // dims 4j+2, 4j+3
+            widen4<KVF>(prmt(c[j], d[j], 0x7362u), A2, A3);
+  #pragma unroll
+            for (int nt = 0; nt < kNT; ++nt)
+              mma16816<false>(o[nt][2 * j + 1], A0, A1, A2, A3, bh[nt][0], bh[nt][1]);
+          }
+        } else {
+          const uint8_t* v1 = v0 + T::kRowBytes;
+          const uint8_t* v2 = v0 + 8 * T::kRowBytes;
+          const uint8_t* v3 = v0 + 9 * T::kRowBytes;
+  #pragma unroll
+          for (int half = 0; half < 2; ++half) {  // dims 16gq + 8half .. +7 -> m-tiles 4half..4half+3
+            uint4 w0 = *reinterpret_cast<const uint4*>(v0 + 32 * gq + 16 * half);
+            uint4 w1 = *reinterpret_cast<const uint4*>(v1 + 32 * gq + 16 * half);
+            uint4 w2 = *reinterpret_cast<const uint4*>(v2 + 32 * gq + 16 * half);
+            uint4 w3 = *reinterpret_cast<const uint4*>(v3 + 32 * gq + 16 * half);
+            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+            if (!ok0) w0 = z;
+            if (!ok1) w1 = z;
+            if (!ok2) w2 = z;
+            if (!ok3) w3 = z;
+            const uint32_t a[4] = {w0.x, w0.y, w0.z, w0.w}, bq[4] = {w1.x, w1.y, w1.z, w1.w};
+            const uint32_t c[4] = {w2.x, w2.y, w2.z, w2.w}, d[4] = {w3.x, w3.y, w3.z, w3.w};
+  #pragma unroll
+            for (int j = 0; j < 4; ++j) {  // word j: dims 16gq + 8half + 2j, +1 -> m-tile 4half + j
+              const uint32_t A0 = prmt(a[j], bq[j], 0x5410u), A1 = prmt(a[j], bq[j], 0x7632u);
+              const uint32_t A2 = prmt(c[j], d[j], 0x5410u), A3 = prmt(c[j], d[j], 0x7632u);
+  #pragma unroll
+              for (int nt = 0; nt < kNT; ++nt) {
+                mma16816<kBF16>(o[nt][4 * half + j], A0, A1, A2, A3, bh[nt][0], bh[nt][1]);
+                if constexpr (kBF16) mma16816<kBF16>(o[nt][4 * half + j], A0, A1, A2, A3, bl[nt][0], bl[nt][1]);
+              }
             }
           }
         }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[st]);
-  }
 
-  // ---- per-warp denominators: sum over the 8 lanes holding each column
-#pragma unroll
-  for (int nt = 0; nt < kNT; ++nt)
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      l[nt][0] += __shfl_xor_sync(0xffffffffu, l[nt][0], off);
-      l[nt][1] += __shfl_xor_sync(0xffffffffu, l[nt][1], off);
-    }
-  // every consumer warp is done with the ring: reuse it for the merge
-  named_barrier_sync(1, kMmaConsumerWarps * 32);
-  // O^T fragment: o[nt][mt][0] = O[dim 16gq+2mt][column 2cq], [1] = [..][2cq+1],
-  //               o[nt][mt][2] = O[dim 16gq+2mt+1][2cq],  [3] = [..+1][2cq+1]
-#pragma unroll
-  for (int nt = 0; nt < kNT; ++nt) {
-    const int col = 8 * nt + 2 * cq;  // this lane's first column in the n-tile
-    if (col < kCols) {
-      float* ha = mrg_acc + (warp * kCols + col) * kD + 16 * gq;
-      float* hb = ha + kD;
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        *reinterpret_cast<float2*>(ha + 2 * mt) = make_float2(o[nt][mt][0], o[nt][mt][2]);
-        *reinterpret_cast<float2*>(hb + 2 * mt) = make_float2(o[nt][mt][1], o[nt][mt][3]);
+    // ---- per-warp denominators: sum over the 8 lanes holding each column
+  #pragma unroll
+    for (int nt = 0; nt < kNT; ++nt)
+  #pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        l[nt][0] += __shfl_xor_sync(0xffffffffu, l[nt][0], off);
+        l[nt][1] += __shfl_xor_sync(0xffffffffu, l[nt][1], off);
       }
-      if (gq == 0) {
-        mrg_m[warp * kCols + col] = m[nt][0];
-        mrg_m[warp * kCols + col + 1] = m[nt][1];
-        mrg_l[warp * kCols + col] = l[nt][0];
-        mrg_l[warp * kCols + col + 1] = l[nt][1];
+    // every consumer warp is done with the piece (and, with one piece per CTA,
+    // with the ring, which then holds the merge area); with several pieces this
+    // also keeps the previous piece's merge reads ahead of these writes
+    named_barrier_sync(1, kMmaConsumerWarps * 32);
+    // O^T fragment: o[nt][mt][0] = O[dim 16gq+2mt][column 2cq], [1] = [..][2cq+1],
+    //               o[nt][mt][2] = O[dim 16gq+2mt+1][2cq],  [3] = [..+1][2cq+1]
+  #pragma unroll
+    for (int nt = 0; nt < kNT; ++nt) {
+      const int col = 8 * nt + 2 * cq;  // this lane's first column in the n-tile
+      if (col < kCols) {
+        float* ha = mrg_acc + (warp * kCols + col) * kD + 16 * gq;
+        float* hb = ha + kD;
+  #pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          *reinterpret_cast<float2*>(ha + 2 * mt) = make_float2(o[nt][mt][0], o[nt][mt][2]);
+          *reinterpret_cast<float2*>(hb + 2 * mt) = make_float2(o[nt][mt][1], o[nt][mt][3]);
+        }
+        if (gq == 0) {
+          mrg_m[warp * kCols + col] = m[nt][0];
+          mrg_m[warp * kCols + col + 1] = m[nt][1];
+          mrg_l[warp * kCols + col] = l[nt][0];
+          mrg_l[warp * kCols + col + 1] = l[nt][1];
+        }
       }
     }
-  }
-  named_barrier_sync(1, kMmaConsumerWarps * 32);
+    named_barrier_sync(1, kMmaConsumerWarps * 32);
 
-  // ---- merge the 4 warps: thread -> (column, dims d0..d0+3)
-  const int ctid = threadIdx.x;
-  const int d0 = 4 * (ctid & 31);
-#pragma unroll
-  for (int it = 0; it < NQ; ++it) {
-    const int col = (ctid >> 5) + kGroup * it;  // query token it, head ctid/32
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kMmaConsumerWarps; ++w) M = fmaxf(M, mrg_m[w * kCols + col]);
-    float Ls = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int w = 0; w < kMmaConsumerWarps; ++w) {
-      const float mw = mrg_m[w * kCols + col];
-      const float a = mw == -INFINITY ? 0.f : ex2(mw - M);
-      Ls = fmaf(mrg_l[w * kCols + col], a, Ls);
-      const float4 v = *reinterpret_cast<const float4*>(&mrg_acc[(w * kCols + col) * kD + d0]);
-      acc.x = fmaf(v.x, a, acc.x);
-      acc.y = fmaf(v.y, a, acc.y);
-      acc.z = fmaf(v.z, a, acc.z);
-      acc.w = fmaf(v.w, a, acc.w);
-    }
-    const int row = (b * NQ + it) * kHq + g * kGroup + (ctid >> 5);  // (b, query token, head)
-    if (p.splits_eff == 1) {
-      const float inv = Ls > 0.f ? p.v_scale / Ls : 0.f;  // a query with no slot gets zeros
-      *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) + ((size_t)row * kD + d0) * 2) =
-          make_uint2(pack_out<QF>(acc.x * inv, acc.y * inv), pack_out<QF>(acc.z * inv, acc.w * inv));
-    } else {
-      const size_t idx = (size_t)row * p.num_splits + s;
-      *reinterpret_cast<float4*>(p.part_o + idx * kD + d0) = acc;
-      if (d0 == 0) {
-        p.part_m[idx] = M;
-        p.part_l[idx] = Ls;
+    // ---- merge the 4 warps: thread -> (column, dims d0..d0+3)
+    const int ctid = threadIdx.x;
+    const int d0 = 4 * (ctid & 31);
+  #pragma unroll
+    for (int it = 0; it < NQ; ++it) {
+      const int col = (ctid >> 5) + kGroup * it;  // query token it, head ctid/32
+      float M = -INFINITY;
+  #pragma unroll
+      for (int w = 0; w < kMmaConsumerWarps; ++w) M = fmaxf(M, mrg_m[w * kCols + col]);
+      float Ls = 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  #pragma unroll
+      for (int w = 0; w < kMmaConsumerWarps; ++w) {
+        const float mw = mrg_m[w * kCols + col];
+        const float a = mw == -INFINITY ? 0.f : ex2(mw - M);
+        Ls = fmaf(mrg_l[w * kCols + col], a, Ls);
+        const float4 v = *reinterpret_cast<const float4*>(&mrg_acc[(w * kCols + col) * kD + d0]);
+        acc.x = fmaf(v.x, a, acc.x);
+        acc.y = fmaf(v.y, a, acc.y);
+        acc.z = fmaf(v.z, a, acc.z);
+        acc.w = fmaf(v.w, a, acc.w);
+      }
+      const int row = (b * NQ + it) * kHq + g * kGroup + (ctid >> 5);  // (b, query token, head)
+      if (pc.direct) {
+        const float inv = Ls > 0.f ? p.v_scale / Ls : 0.f;  // a query with no slot gets zeros
+        *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) + ((size_t)row * kD + d0) * 2) =
+            make_uint2(pack_out<QF>(acc.x * inv, acc.y * inv), pack_out<QF>(acc.z * inv, acc.w * inv));
+      } else {
+        const size_t idx = (size_t)row * p.num_splits + pc.slot;
+        *reinterpret_cast<float4*>(p.part_o + idx * kD + d0) = acc;
+        if (d0 == 0) {
+          p.part_m[idx] = M;
+          p.part_l[idx] = Ls;
+        }
       }
     }
   }

@@ -447,14 +447,25 @@ def test_paged_out_of_range_page_ids_are_clamped_and_flagged():
     assert gq.get_status(ws) & api.FLAG_PAGE_CLAMPED
 
 
-def test_paged_full_size_bitwise_equals_contiguous():
-    t = _make(inputs.WORKLOADS[4])
+def test_paged_full_size_matches_oracle_and_contiguous():
+    # the paged cache runs its own balanced schedule (4 waves of pieces), so
+    # its FP32 rounding order differs from the contiguous launch: compare
+    # both against the oracle on sampled units and with each other at the bar
+    w = inputs.WORKLOADS[4]
+    t = _make(w)
     contiguous = _run(t).out.clone()
+    rng = np.random.default_rng(44)
+    units = sorted({(int(b), int(g)) for b, g in zip(rng.integers(0, w.batch, 4), rng.integers(0, 8, 4))}
+                   | {(0, 0), (w.batch - 1, 7)})
+    ref = _oracle_units(t, units)
     pt = inputs.paginate(t, 256, extra_pages=7)
     del t["kv"]
     out = _paged(pt)
     torch.cuda.synchronize()
-    assert torch.equal(out.view(torch.int16), contiguous.view(torch.int16))
+    got = _gpu_rows(out)
+    rows = sorted(ref)
+    _assert_parity(got[rows], np.stack([ref[r] for r in rows]), "paged full size, sampled")
+    _assert_parity(got, _gpu_rows(contiguous).astype(np.float64), "paged vs contiguous")
 
 
 
