@@ -240,6 +240,79 @@ def test_max_capacity_sampled():
                        f"C=2^20 splits={p.num_splits}")
 
 
+# ------------------------------------------- balanced schedule (many waves)
+#
+# Grids of more than one wave of (split, KV head, batch row) work items run
+# the balanced schedule: one CTA per resident slot, each taking an equal run
+# of the tiles of all rows (lengths read on the device), rows cut into pieces
+# wherever the runs end.  These cases are all well past one wave.
+
+
+@pytest.mark.parametrize("kv_dtype", ["f16", "bf16", "e4m3", "i8"])
+@pytest.mark.parametrize("S", [None, 2, 16])
+def test_balanced_ragged_every_element(kv_dtype, S):
+    rng = np.random.default_rng(7)
+    C = 2048
+    lens = rng.integers(1, C + 1, 96)
+    lens[:6] = [1, 64, 128, 129, C, C - 1]  # tile edges of both tile sizes, full rows
+    w = inputs.custom(96, C, 1, kv_dtype=kv_dtype, kv_std=2.0 if kv_dtype == "e4m3" else 1.0, nan_tail=True)
+    t = _make(w, lens=lens.tolist())
+    p = _run(t, num_splits=S)
+    _assert_parity(_gpu_rows(p.out), _oracle_full(t), f"balanced {kv_dtype} splits={p.num_splits}")
+
+
+def test_balanced_zero_length_rows_and_all_zero():
+    C, B = 2048, 64
+    lens = [0 if b % 3 == 0 else (b * 97) % C + 1 for b in range(B)]
+    t = _make(inputs.custom(B, C, 1), lens=lens)
+    p = _run(t, num_splits=8)
+    assert gq.get_status(p) & api.FLAG_LENGTH_CLAMPED
+    out = p.out.view(B, 32, 128)
+    zero = [b for b in range(B) if lens[b] == 0]
+    keep = [b for b in range(B) if lens[b] > 0]
+    assert not out[zero].any()
+    sub = dict(t, q=t["q"][keep], kv=t["kv"][keep], lens=t["lens"][keep])
+    _assert_parity(_gpu_rows(out[keep]), _oracle_full(sub), "balanced, zero-length rows")
+    t["lens"].zero_()
+    p.out.fill_(1.0)
+    gq.launch(p)
+    torch.cuda.synchronize()
+    assert not p.out.any()
+
+
+def test_balanced_one_long_row_among_short_ones():
+    # one row holds almost all the tiles: runs are cut by the split-slot bound
+    C, B = 65536, 64
+    lens = [C] + [1 + 5 * b for b in range(1, B)]
+    t = _make(inputs.custom(B, C, 1, kv_dtype="bf16"), lens=lens)
+    for S in (None, 4):
+        p = _run(t, num_splits=S)
+        _assert_parity(_gpu_rows(p.out), _oracle_full(t), f"one long row, splits={p.num_splits}")
+
+
+@pytest.mark.parametrize("B", [1024, 1025])
+def test_balanced_batch_limit(B):
+    # 1024 rows is the largest batch the balanced prologue scans; 1025 runs the
+    # one-piece-per-CTA grid
+    rng = np.random.default_rng(B)
+    t = _make(inputs.custom(B, 256, 1), lens=rng.integers(1, 257, B).tolist())
+    p = _run(t, num_splits=4)
+    _assert_parity(_gpu_rows(p.out), _oracle_full(t), f"B={B}")
+
+
+@pytest.mark.parametrize("kv_dtype", ["f16", "e4m3"])
+def test_balanced_paged_ragged(kv_dtype):
+    rng = np.random.default_rng(11)
+    C = 4096
+    w = inputs.custom(48, C, 1, kv_dtype=kv_dtype, kv_std=2.0 if kv_dtype == "e4m3" else 1.0, nan_tail=True)
+    t = _make(w, lens=rng.integers(1, C + 1, 48).tolist())
+    ref = _oracle_full(t)
+    pt = inputs.paginate(t, 256, extra_pages=5)
+    out = _paged(pt, num_splits=8)
+    torch.cuda.synchronize()
+    _assert_parity(_gpu_rows(out), ref, f"balanced paged {kv_dtype}")
+
+
 # ------------------------------------------------------ unused slots, safety
 
 
