@@ -261,6 +261,39 @@ def time_calls(fn, n, flush=None, stream=None):
     return res[len(res) // 2]
 
 
+def sdpa_context(t, w, n, flush):
+    """Context only: torch SDPA (enable_gqa=True, default backend) on the same
+    GPU inputs, K and V copied out contiguously beforehand (untimed); ragged
+    lengths become a boolean mask over the capacity."""
+    import math
+    import torch
+    F = torch.nn.functional
+    q = t["q"].unsqueeze(2)  # [B, 32, 1, 128]
+    k = t["kv"][:, 0].contiguous()  # [B, 8, C, 128]
+    v = t["kv"][:, 1].contiguous()
+    mask = None
+    if not (w.len_lo == w.len_hi == w.capacity):
+        pos = torch.arange(w.capacity, device=q.device)
+        mask = (pos[None, :] < t["lens"][:, None].long())[:, None, None, :]
+    scale = t["q_scale"] / math.sqrt(128.0)
+
+    def fn():
+        F.scaled_dot_product_attention(q, k, v, attn_mask=mask, scale=scale, enable_gqa=True)
+
+    try:
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        us = time_calls(fn, n, flush=flush)
+    except Exception as e:  # an SDPA backend without this shape or dtype
+        return {"unavailable": f"{type(e).__name__}: {str(e)[:120]}"}
+    row = {"us_per_call": round(us, 2),
+           "note": "torch SDPA, enable_gqa=True, default backend, contiguous K/V copies; context only"}
+    if mask is not None:
+        row["note"] += "; boolean mask over the capacity (slots past a length may hold NaN: timing only)"
+    return row
+
+
 def per_config_table(dev, peak, gq, inputs, quick=False):
     import torch
     flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
@@ -297,6 +330,8 @@ def per_config_table(dev, peak, gq, inputs, quick=False):
                "splits": p.num_splits, "l2": "cold (512 MB written, then 256 MB read, before each call)"}
         if w.kv_dtype == "i8":
             row["note"] = "int8 codes + bf16 row scales, workload 5 shape (not one of the five workloads)"
+        if w.kv_dtype in ("f16", "bf16"):
+            row["torch_sdpa"] = sdpa_context(t, w, n, flush)
         if w.batch * w.capacity <= 1 << 12:
             # warm L2, device time: 20 calls back to back inside one CUDA graph
             reps = 20
