@@ -298,6 +298,13 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
   pdl_launch_dependents();
   const int C = p.capacity;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {  // ring barriers first: the prologue below hides their initialisation
+    for (int i = 0; i < kMmaStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kMmaConsumerWarps);
+    }
+    fence_barrier_init();
+  }
 
   // ---- this CTA's pieces
   PieceCursor<T::kTile, BAL> cur;
@@ -308,7 +315,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
     // Prefix sums of tiles per row over the batch (all threads; the merge
     // area is the scratch, idle until the first epilogue: per-thread sums,
     // the total, the first row and its prefix, then the clamped lengths).
-    int* scan = reinterpret_cast<int*>(mrg_acc);
+    int* scan = reinterpret_cast<int*>(mrg_acc);  // [0, 5): warp sums; then first row, its prefix
     int* lsh = scan + kMmaThreads + 3;
     const int B = p.batch;
     const int per_t = (B + kMmaThreads - 1) / kMmaThreads;
@@ -322,48 +329,36 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
       mine += (lsh[bb] + T::kTile - 1) / T::kTile;
     }
     if (clamped && blockIdx.x == 0) atomicOr(p.flags, GQA_FLAG_LENGTH_CLAMPED);
-    scan[threadIdx.x] = mine;
-    __syncthreads();
-    if (warp == 0) {  // exclusive scan of the 160 per-thread sums
-      constexpr int kPer = (kMmaThreads + 31) / 32;
-      int v[kPer], sum = 0;
+    // exclusive prefix of the per-thread sums: a scan within each warp, then
+    // the sums of the warps before
+    int incl = mine;
 #pragma unroll
-      for (int k = 0; k < kPer; ++k) {
-        const int idx = lane * kPer + k;
-        v[k] = idx < kMmaThreads ? scan[idx] : 0;
-        sum += v[k];
-      }
-      int incl = sum;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int t = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += t;
-      }
-      int run = incl - sum;
-#pragma unroll
-      for (int k = 0; k < kPer; ++k) {
-        const int idx = lane * kPer + k;
-        if (idx < kMmaThreads) scan[idx] = run;
-        run += v[k];
-      }
-      if (lane == 31) scan[kMmaThreads] = incl;
+    for (int off = 1; off < 32; off <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += t;
     }
+    if (lane == 31) scan[warp] = incl;
     __syncthreads();
-    const int total = kHkv * scan[kMmaThreads];
+    int pre = incl - mine, per_head = 0;
+#pragma unroll
+    for (int w = 0; w < kMmaThreads / 32; ++w) {
+      const int ws = scan[w];
+      if (w < warp) pre += ws;
+      per_head += ws;
+    }
+    const int total = kHkv * per_head;
     const int q = max((total + (int)gridDim.x - 1) / (int)gridDim.x, p.bal_q_min);
     const int x0 = (int)blockIdx.x * q;
-    if (x0 < total) {  // the thread whose rows hold tile x0 records the first row
-      int pre = scan[threadIdx.x];
-      if (kHkv * pre <= x0 && x0 < kHkv * (pre + mine)) {
-        for (int bb = rb0; bb < rb1; ++bb) {
-          const int nb = (lsh[bb] + T::kTile - 1) / T::kTile;
-          if (x0 < kHkv * (pre + nb)) {
-            scan[kMmaThreads + 1] = bb;
-            scan[kMmaThreads + 2] = pre;
-            break;
-          }
-          pre += nb;
+    // the thread whose rows hold tile x0 records the first row and its prefix
+    if (x0 < total && kHkv * pre <= x0 && x0 < kHkv * (pre + mine)) {
+      for (int bb = rb0; bb < rb1; ++bb) {
+        const int nb = (lsh[bb] + T::kTile - 1) / T::kTile;
+        if (x0 < kHkv * (pre + nb)) {
+          scan[kMmaThreads + 1] = bb;
+          scan[kMmaThreads + 2] = pre;
+          break;
         }
+        pre += nb;
       }
     }
     __syncthreads();
@@ -395,14 +390,9 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
     cur.start_single(b, g, L, t_begin, t_end, s, p.splits_eff == 1);
   }
 
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < kMmaStages; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kMmaConsumerWarps);
-    }
-    fence_barrier_init();
-  }
-  __syncthreads();
+  // the barriers' initialisation is visible to every thread (the balanced
+  // prologue has synchronised the CTA already)
+  if constexpr (!BAL) __syncthreads();
   const uint64_t deadline = global_timer_ns() + p.wait_budget_ns;
 
   if (warp == kMmaConsumerWarps) {
