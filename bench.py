@@ -294,7 +294,28 @@ def sdpa_context(t, w, n, flush):
     return row
 
 
-def per_config_table(dev, peak, gq, inputs, quick=False):
+def oracle_config(t, w, nbytes, reps):
+    """The oracle (all host cores) on a sample of the workload: every batch row
+    for small batches, else the first few (all 32 query heads each); CPU GB/s
+    and the µs a whole call would take at that rate."""
+    import oracle
+    threads = oracle.default_threads()
+    rows_b = w.batch if w.batch * w.capacity <= 32 * 8192 else (1 if w.index == 4 else 4)
+    hosts = [host_batch_row(t, b) for b in range(rows_b)]
+    best = None
+    for _ in range(reps):
+        secs = sb = 0
+        for host in hosts:
+            s_, b_ = oracle_rows(t, host, list(range(32)), threads)
+            secs, sb = secs + s_, sb + b_
+        best = secs if best is None else min(best, secs)
+    gbs = sb / best / 1e9
+    return {"GBps": round(gbs, 3), "us_per_call": round(nbytes / gbs / 1e3, 1), "cores": threads,
+            "sample": f"{rows_b} of {w.batch} batch rows, best of {reps}" + ("" if rows_b == w.batch else
+                                                                             "; us_per_call scaled by bytes")}
+
+
+def per_config_table(dev, peak, gq, inputs, quick=False, cpu=True):
     import torch
     flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     clean_buf = torch.ones(64 << 20, dtype=torch.float32, device=dev)  # 256 MB
@@ -332,6 +353,8 @@ def per_config_table(dev, peak, gq, inputs, quick=False):
             row["note"] = "int8 codes + bf16 row scales, workload 5 shape (not one of the five workloads)"
         if w.kv_dtype in ("f16", "bf16"):
             row["torch_sdpa"] = sdpa_context(t, w, n, flush)
+        if cpu and w.kv_dtype != "i8":
+            row["oracle_cpu"] = oracle_config(t, w, nbytes, 3 if idx in (1, 2, 3) else 1)
         if w.batch * w.capacity <= 1 << 12:
             # warm L2, device time: 20 calls back to back inside one CUDA graph
             reps = 20
@@ -536,7 +559,8 @@ def run_gpu(args):
                                 "sample": f"{nrows} query-head rows ({nrows // 32} batch rows) of "
                                           f"'{w.name}', FP64, {threads} threads; {sb} KV bytes"}
     if rank == 0 and not args.no_per_config:
-        line["per_config"] = per_config_table(dev, peak, gq, inputs, quick=args.quick)
+        line["per_config"] = per_config_table(dev, peak, gq, inputs, quick=args.quick,
+                                              cpu=not args.no_cpu_baseline)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
