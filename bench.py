@@ -437,12 +437,18 @@ def run_gpu(args):
     w = inputs.WORKLOADS[args.workload]
     if args.batch:
         w = inputs.with_(w, batch=args.batch)
+    if args.kv_dtype:
+        eight = args.kv_dtype in ("e4m3", "i8")
+        w = inputs.with_(w, kv_dtype=args.kv_dtype, q_dtype="bf16" if eight else args.kv_dtype,
+                         name=f"{w.name} with {args.kv_dtype} KV")
     t = inputs.make(w, dev, seed=w.seed + 7919 * rank)
     lens_list = t["lens"].cpu().tolist()
     fp8 = w.kv_dtype == "e4m3"
     out = torch.empty_like(t["q"])
-    p = gq.prepare({"Q": t["q"], "KV": t["kv"], "O": out, "sequence_lengths": t["lens"]},
-                   q_scale=t["q_scale"], k_scale=t["k_scale"] if fp8 else None,
+    tensors = {"Q": t["q"], "KV": t["kv"], "O": out, "sequence_lengths": t["lens"]}
+    if t["kv_scales"] is not None:
+        tensors["KV_SCALES"] = t["kv_scales"]
+    p = gq.prepare(tensors, q_scale=t["q_scale"], k_scale=t["k_scale"] if fp8 else None,
                    v_scale=t["v_scale"] if fp8 else None)
     splits_eff = p.splits_effective
     launches_per_step = 2 if splits_eff > 1 else 1
@@ -469,11 +475,14 @@ def run_gpu(args):
     end.record(stream)
     torch.cuda.synchronize(dev)
     # the dominant kernel's own duration: the split kernel alone, each launch
-    # bracketed by events
+    # bracketed by events (stage 1 alone takes no int8 cache: there, the step)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     for i in range(K):
         ev[i][0].record(stream)
-        gq.split_stage(p)
+        if w.kv_dtype == "i8":
+            gq.launch(p)
+        else:
+            gq.split_stage(p)
         ev[i][1].record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
@@ -522,7 +531,8 @@ def run_gpu(args):
         del hq, hkv, hlens, hout
 
     achieved = nbytes / (split_ms * 1e-3) / 1e9
-    traffic = traffic_per_launch(args.workload)
+    # the committed capture is of the workload as defined (no batch or KV override)
+    traffic = traffic_per_launch(args.workload) if not (args.batch or args.kv_dtype) else None
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": max(3, args.warmup), "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
@@ -578,6 +588,8 @@ def main(argv=None):
     ap.add_argument("--workload", type=int, default=4, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch (smaller cases for profiling)")
+    ap.add_argument("--kv-dtype", choices=["f16", "bf16", "e4m3", "i8"], default=None,
+                    help="override the workload's KV format (8-bit formats take a bf16 query)")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-batch-rows", type=int, default=4,
                     help="batch rows (all 32 query heads each) in the oracle CPU-baseline sample")
