@@ -8,8 +8,10 @@ sampled (b, KV head) units (all 4 query heads each).  Also covered: ragged
 lengths and tile edges, capacity 1, every split count, q_scale 0, distinct
 fp8 scales, NaN tails (bit-exact output whatever the unused slots hold; the
 cache is never written), guard bands around the output and the workspace,
-run-to-run determinism, CUDA-graph capture and replay, length clamping flags,
-the convenience and staged entry points, and errors reported before launch.
+run-to-run determinism, CUDA-graph capture and replay (the prepared call, the
+append + decode serving step, the paged, int8 and verify entry points), length
+clamping flags, the convenience and staged entry points, errors reported
+before launch, and the balanced schedule's edge cases.
 """
 import numpy as np
 import pytest
@@ -721,3 +723,107 @@ def test_append_then_decode_matches_the_oracle_chain():
         kv_bits0[b, 1, :, s_] = bits_of(vp[b])
     ref, _ = oracle.gqa_decode(q_bits, oracle.BF16, kv_bits0, oracle.BF16, lens.cpu().numpy())
     _assert_parity(_gpu_rows(out), ref, "append -> decode chain")
+
+
+# ------------------------------------------------ CUDA graphs beyond prepare
+
+
+def _replay_equals_eager(step, outs):
+    """Capture `step` (no allocation, no host sync inside), replay it, and
+    compare with an eager run on the same inputs, bit for bit."""
+    step()
+    torch.cuda.synchronize()
+    eager = [o.clone() for o in outs]
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()  # warm-up on a side stream before capture
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for o in outs:
+        o.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    for o, e in zip(outs, eager):
+        assert torch.equal(o.view(torch.int16) if o.element_size() == 2 else o, e.view(torch.int16)
+                           if e.element_size() == 2 else e)
+    return g
+
+
+def test_graph_append_then_decode_serving_step():
+    # one decode step of a server as one graph: append the new token (norm,
+    # RoPE, cache write at `slots`), then decode over len = slot + 1; the
+    # next step only rewrites inputs in place and replays
+    B, C = 8, 4096
+    qp, kp, vp, wq, wk, pos, _ = _append_inputs(B, C, "bf16", seed=9)
+    t = _make(inputs.custom(B, C, 1000, 3000, kv_dtype="bf16"))
+    slots = t["lens"].clone()
+    lens = slots + 1
+    q_out = torch.empty_like(qp)
+    out = torch.empty_like(qp)
+    hdr = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    S = 8
+    p = gq.prepare({"Q": q_out, "KV": t["kv"], "O": out, "sequence_lengths": lens}, num_splits=S)
+
+    def step():
+        gq.append_kv(qp, kp, vp, wq, wk, pos, slots, t["kv"], q_out=q_out, workspace=hdr)
+        gq.launch(p)
+
+    g = _replay_equals_eager(step, [q_out, out])
+    # next token: new projections, positions, slots and lengths written in place
+    qp2, kp2, vp2, _, _, _, _ = _append_inputs(B, C, "bf16", seed=10)
+    kv_before = t["kv"].clone()
+    for dst, src in ((qp, qp2), (kp, kp2), (vp, vp2)):
+        dst.copy_(src)
+    pos.add_(1)
+    slots.add_(1)
+    lens.add_(1)
+    g.replay()
+    torch.cuda.synchronize()
+    replayed = out.clone()
+    t["kv"].copy_(kv_before)
+    step()
+    torch.cuda.synchronize()
+    assert torch.equal(replayed.view(torch.int16), out.view(torch.int16))
+    assert gq.get_status(hdr) == 0
+
+
+@pytest.mark.parametrize("kind", ["paged", "int8", "verify2"])
+def test_graph_capture_other_entry_points(kind):
+    B, C, S = 16, 2048, 8
+    rng = np.random.default_rng(21)
+    lens = rng.integers(1, C + 1, B).tolist()
+    if kind == "int8":
+        t = _make(inputs.custom(B, C, 1, kv_dtype="i8"), lens=lens)
+    elif kind == "verify2":
+        t = _make(inputs.custom(B, C, 2, q_len=2), lens=[max(2, x) for x in lens])
+    else:
+        t = _make(inputs.custom(B, C, 1), lens=lens)
+    out = torch.empty_like(t["q"])
+    rows = B * (2 if kind == "verify2" else 1)
+    ws = torch.zeros(gq.workspace_size(rows, C, S), dtype=torch.uint8, device=DEV)
+    if kind == "paged":
+        pt = inputs.paginate(t, 64, extra_pages=3)
+
+        def step():
+            gq.gqa_decode_paged(pt["q"], pt["kv_pages"], pt["block_table"], pt["lens"], out=out,
+                                num_splits=S, workspace=ws)
+    elif kind == "int8":
+        def step():
+            gq.gqa_decode_int8kv(t["q"], t["kv"], t["kv_scales"], t["lens"], out=out, num_splits=S,
+                                 workspace=ws)
+    else:
+        def step():
+            gq.gqa_decode_verify(t["q"], t["kv"], t["lens"], out=out, num_splits=S, workspace=ws)
+    g = _replay_equals_eager(step, [out])
+    _assert_parity(_gpu_rows(out), _oracle_full(t), f"graph {kind}")
+    # shorter lengths, written in place, then replay
+    lens_t = pt["lens"] if kind == "paged" else t["lens"]
+    lens_t.copy_(torch.clamp(lens_t // 2, min=2))
+    g.replay()
+    torch.cuda.synchronize()
+    if kind == "paged":
+        t["lens"] = pt["lens"]
+    _assert_parity(_gpu_rows(out), _oracle_full(t), f"graph {kind}, lengths halved")
