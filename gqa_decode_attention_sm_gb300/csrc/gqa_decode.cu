@@ -283,6 +283,14 @@ cudaError_t launch_split_t(const SplitParams& sp, int q_len, int bal_ctas, cudaS
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kMmaThreads, 1, 1);
   cfg.stream = stream;
+  // programmatic dependent launch: CTAs may become resident while the
+  // previous grid in the stream drains; they wait (griddepcontrol.wait)
+  // before reading any input
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (bal_ctas > 0) {
     cfg.gridDim = dim3(bal_ctas, 1, 1);
     cfg.dynamicSmemBytes = mma_smem_bytes(KVF, 1) + kBalMergeBytes;
@@ -670,6 +678,13 @@ gqa_status_t gqa_append_kv(const void* q_proj, const void* k_proj, const void* v
   cfg.gridDim = dim3(batch, 1, 1);
   cfg.blockDim = dim3(kAppendThreads, 1, 1);
   cfg.stream = static_cast<cudaStream_t>(stream);
+  // programmatic dependent launch, as the split kernel: the kernel waits for
+  // the previous grid before its first read
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   cudaError_t e;
   const bool bf = dtype == GQA_BF16;
   if (fmt == kKvF16) e = cudaLaunchKernelEx(&cfg, append_kv_kernel<kKvF16, kQF16>, ap);

@@ -65,6 +65,10 @@ __device__ __forceinline__ uint8_t to_e4m3(float x) {
 template <int KVF, int QF>
 __global__ void __launch_bounds__(kAppendThreads) append_kv_kernel(const __grid_constant__ AppendParams p) {
   __shared__ float cs[kD / 2], sn[kD / 2];
+  // the decode that follows may be scheduled now (it waits for this grid);
+  // this grid waits for the previous one before its first read
+  pdl_launch_dependents();
+  pdl_wait_prior_grid();
   const int b = blockIdx.x;
   const int pos = __ldg(p.positions + b);
   if (threadIdx.x < kD / 2) {

@@ -92,7 +92,8 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
   const int g = blockIdx.x, bq = blockIdx.y;  // bq = b * q_len + query token
   const int b = bq / p.q_len, jq = bq % p.q_len;
   const size_t row = (size_t)bq * kHq + g * kGroup + (threadIdx.x >> 5);
-  int n;
+  int n;      // splits or pieces to merge
+  bool zero = false;  // a row without tokens
   if (p.bal_ctas > 0) {
     // The tile counts stage 1 used (integers, so both kernels agree exactly),
     // read while stage 1 still runs.
@@ -120,21 +121,24 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
       all += red[1][w];
     }
     const int nb = (min(max(__ldg(p.lens + b), 0), p.capacity) + p.tile - 1) / p.tile;
-    if (nb == 0) {  // no tokens: a zero row (stage 1 holds no piece of it)
-      merge_splits<QF>(p, row, 0);
-      return;
-    }
     const int total = kHkv * all;
     const int q = max((total + p.bal_ctas - 1) / p.bal_ctas, p.bal_q_min);
     const int tf = kHkv * before + g * nb;
-    n = (tf + nb - 1) / q - tf / q + 1;
-    if (n == 1) return;  // one piece: stage 1 wrote the row itself
+    n = nb > 0 ? (tf + nb - 1) / q - tf / q + 1 : 0;
+    zero = nb == 0;  // no tokens: a zero row (stage 1 holds no piece of it)
   } else {
     const int L = min(max(__ldg(p.lens + b), 0), p.capacity) - p.q_len + 1 + jq;
     n = L > 0 ? (L + p.chunk - 1) / p.chunk : 0;
   }
-  // launched as a programmatic dependent of stage 1: wait for its partials
+  // Launched as a programmatic dependent of stage 1: wait for its partials.
+  // Every CTA waits, also those with nothing to merge, so that this grid
+  // completes after stage 1 and work later in the stream sees all of `out`.
   pdl_wait_prior_grid();
+  // Stage 1 is complete: the next grid in the stream may be scheduled now (it
+  // waits for this one before it reads or writes anything).  Triggering
+  // earlier let the next split kernel take SM slots during this split's tail.
+  pdl_launch_dependents();
+  if (p.bal_ctas > 0 && n == 1 && !zero) return;  // one piece: stage 1 wrote the row itself
   merge_splits<QF>(p, row, n);
 }
 

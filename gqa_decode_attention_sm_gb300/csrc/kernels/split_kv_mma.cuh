@@ -305,6 +305,10 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
     }
     fence_barrier_init();
   }
+  // Launched as a programmatic dependent of the previous grid in the stream:
+  // wait for it (its writes, e.g. an appended token, must be visible) before
+  // the first read of any input.  A no-op otherwise.
+  pdl_wait_prior_grid();
 
   // ---- this CTA's pieces
   PieceCursor<T::kTile, BAL> cur;
