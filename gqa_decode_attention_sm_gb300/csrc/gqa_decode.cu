@@ -257,14 +257,31 @@ gqa_status_t static_workspace(int dev, void** ptr) {
 // --------------------------------------------------------------- planning
 
 int plan_splits(int batch, int capacity, int kv_format, int sm_count) {
-  // Aim for about 8 waves of work items (as many resident per SM as the
-  // single-token split kernel of this format allows) over the worst case
-  // (every length = capacity), with whole tiles per split.
   const long long tile = tile_tokens(kv_format);
   const long long units = (long long)batch * kHkv;
   const long long ctas_per_sm = mma_ctas_per_sm(kv_format, 1);
-  const long long target_ctas = 8LL * ctas_per_sm * (sm_count > 0 ? sm_count : 148);
-  long long per = (units * capacity + target_ctas - 1) / target_ctas;
+  const long long slots = ctas_per_sm * (sm_count > 0 ? sm_count : 148);
+  const long long nmax = (capacity + tile - 1) / tile;
+  long long per;
+  if (units * nmax <= 16 * slots) {
+    // Latency-bound sizes (at most 16 tiles per resident slot over the worst
+    // case): one wave of work items at most, about sqrt(6 nmax) splits per
+    // row — fewer leave each CTA more tiles to stream, more leave the merge
+    // more partials.  Measured in CUDA graphs on GB300 (us per call, the
+    // 8-wave rule -> this): bf16 1 x 4096 10.7 -> 9.0, 1 x 16384 20.6 -> 17.1,
+    // 4 x 4096 16.4 -> 14.6, e4m3 1 x 8192 11.5 -> 10.3, fp16 1 x 1024 6.3.
+    long long s = (long long)std::llround(std::sqrt(6.0 * (double)nmax));
+    const long long wave = slots / units;
+    if (s > wave) s = wave;
+    if (s < 1) s = 1;
+    per = (capacity + s - 1) / s;
+  } else {
+    // Otherwise about 8 waves of work items over the worst case (every
+    // length = capacity); such grids run the balanced schedule, where the
+    // split count only bounds the pieces of a row.
+    const long long target_ctas = 8LL * slots;
+    per = (units * capacity + target_ctas - 1) / target_ctas;
+  }
   per = (per + tile - 1) / tile * tile;
   // at least two tiles per split: a one-tile split costs more in fixed
   // prologue/epilogue than it streams (measured on the 1 x 1024 fp16 case)

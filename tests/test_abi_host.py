@@ -86,8 +86,9 @@ def _chunk(C, S, fmt):
 
 
 # (batch, capacity, format, SM count) -> splits: about 8 waves of work items
-# (2 resident per SM for 16-bit KV, 3 for 8-bit KV) over the worst case, whole
-# tiles per split (at least two), 1..256 splits.
+# (2 resident per SM for 16-bit KV, 3 for 8-bit KV) over the worst case, or,
+# when all rows hold at most 16 tiles per resident slot, about sqrt(6 * tiles
+# per row) capped at one wave; whole tiles per split (at least two), 1..256.
 PLAN_TABLE = [
     ((1, 64, KV_F16, 152), 1),
     ((1, 1024, KV_F16, 152), 8),
@@ -99,6 +100,11 @@ PLAN_TABLE = [
     ((1, 1, KV_F16, 152), 1),
     ((65535, 64, KV_F16, 152), 1),
     ((2, 65536, KV_BF16, 100), 94),
+    # latency-bound sizes: about sqrt(6 * tiles per row) splits, one wave at most
+    ((1, 4096, KV_BF16, 152), 16),
+    ((1, 16384, KV_BF16, 152), 37),
+    ((4, 4096, KV_BF16, 152), 8),
+    ((1, 8192, KV_E4M3, 152), 16),
 ]
 
 
