@@ -6,9 +6,11 @@ closed forms (length 1 gives V[0]; q_scale = 0 or equal keys give the mean of
 V; a very large q_scale gives the value row of the largest score), invariants
 of softmax attention (slot permutation, a common shift of every key, the
 convex hull of the value rows, power-of-two scaling of V, k_scale and q_scale
-acting only through their product), the grouped head map, and torch's float64
-scaled_dot_product_attention on the dequantised inputs.
+acting only through their product), the grouped head map, torch's float64
+scaled_dot_product_attention on the dequantised inputs, and a brute-force
+restatement in 40-digit decimal arithmetic on tiny caches.
 """
+import decimal
 import json
 import math
 import os
@@ -52,6 +54,60 @@ def _run(lib, t, qb, kvb, lens, **kw):
         args["kv_scales"] = bits_of(t["kv_scales"])
     args.update(kw)
     return oracle.gqa_decode(qb, FMT[w.q_dtype], kvb, FMT[w.kv_dtype], lens, lib=lib, **args)
+
+
+# ------------------------------------------------- brute force, 40 digits
+
+
+def _brute_force_decimal(q_vals, k_vals, v_vals, lens, q_scale, k_scale, v_scale):
+    """Softmax attention written out in decimal arithmetic at 40 digits from
+    the decoded values (exact binary fractions, so Decimal(x) is exact)."""
+    ctx = decimal.Context(prec=40)
+    Dd = decimal.Decimal
+    B = q_vals.shape[0]
+    scale = ctx.divide(ctx.multiply(Dd(q_scale), Dd(k_scale)), ctx.sqrt(Dd(D)))
+    out = np.zeros((B * HQ, D))
+    for b in range(B):
+        L = int(lens[b])
+        for h in range(HQ):
+            g = h // (HQ // HKV)
+            s = []
+            for t in range(L):
+                acc = Dd(0)
+                for d in range(D):
+                    acc = ctx.add(acc, ctx.multiply(Dd(float(q_vals[b, h, d])), Dd(float(k_vals[b, g, t, d]))))
+                s.append(ctx.multiply(scale, acc))
+            m = max(s)
+            w = [ctx.exp(ctx.subtract(x, m)) for x in s]
+            den = sum(w, Dd(0))
+            for d in range(D):
+                num = sum((ctx.multiply(w[t], Dd(float(v_vals[b, g, t, d]))) for t in range(L)), Dd(0))
+                out[b * HQ + h, d] = float(ctx.multiply(Dd(v_scale), ctx.divide(num, den)))
+    return out
+
+
+@pytest.mark.parametrize("fmt", ["f16", "bf16", "e4m3"])
+def test_matches_40_digit_brute_force_on_tiny_caches(orc, fmt):
+    rng = np.random.default_rng({"f16": 1, "bf16": 2, "e4m3": 3}[fmt])
+    B, C = 2, 8
+    q_fmt = "bf16" if fmt == "e4m3" else fmt
+    qv = rng.standard_normal((B, HQ, D)) * 1.5
+    qb = f16_bits(qv) if q_fmt == "f16" else bf16_bits(qv)
+    kv = rng.standard_normal((B, 2, HKV, C, D)) * 2.0
+    if fmt == "e4m3":
+        kvb = torch.from_numpy(kv.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        k_scale, v_scale = 0.75, 1.25  # distinct, both applied
+    else:
+        kvb = _to_bits(kv, fmt)
+        k_scale = v_scale = 1.0
+    lens = np.array([int(rng.integers(1, C + 1)), C], dtype=np.int32)
+    q_scale = 0.8
+    got, _ = oracle.gqa_decode(qb, FMT[q_fmt], kvb, FMT[fmt], lens, q_scale=q_scale, k_scale=k_scale,
+                               v_scale=v_scale, lib=orc)
+    q_vals = values_of_bits(qb, q_fmt)
+    kv_vals = values_of_bits(kvb, fmt)
+    want = _brute_force_decimal(q_vals, kv_vals[:, 0], kv_vals[:, 1], lens, q_scale, k_scale, v_scale)
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-14)
 
 
 # ------------------------------------------------------------------ golden
