@@ -1,11 +1,19 @@
 // Stage 1 of GQA decode with the QK^T and P.V contractions on the tensor cores.
 //
-// One CTA
-// per (split s, KV head g, batch row b) serving the 4 query heads of its KV
-// head, so every K/V byte of the chunk [s*chunk, min((s+1)*chunk, len[b])) is
-// read from HBM exactly once; a producer warp streams 16 KB K and V tiles with
-// 1-D bulk copies (TMA unit) into an mbarrier ring, copying only rows below
-// the length.  The contractions run on the tensor cores because ncu showed an
+// Work comes in pieces: tokens [t_begin, t_end) of one (batch row b, KV head g)
+// row, served for the 4 query heads of that KV head, so every K/V byte below
+// the length is read from HBM exactly once.  Two schedules:
+//   one piece per CTA — grid (8, B, splits), CTA (g, b, s) takes chunk s of
+//     row (b, g); verify windows, batches above kBalMaxBatch, and grids of
+//     at most one wave;
+//   balanced — one CTA per resident slot; the tiles of all rows form one
+//     stream and each CTA takes an equal run of it (lengths read on the
+//     device), cut into pieces at row ends.
+// A piece that is its row's only one writes the normalised output; the
+// others write FP32 partials that stage 2 merges.  A producer warp streams
+// 16 KB K and V tiles with 1-D bulk copies (TMA unit) into an mbarrier ring,
+// copying only rows below the length, straight from one piece into the next.
+// The contractions run on the tensor cores because ncu showed an
 // FP32 CUDA-core version of the same kernel to be instruction-bound (about 75
 // warp instructions per token and KV head; on e4m3 KV, short-scoreboard stalls
 // held DRAM throughput near a quarter of peak); this version executes about
@@ -54,7 +62,7 @@ struct SplitParams {
   const void* kv;         // [B,2,8,C,128] fp16/bf16/e4m3/int8
   const uint16_t* kv_scales;  // int8 cache: bf16 [B,2,8,C], one scale per (plane, KV head, slot)
   const int32_t* lens;    // [B]
-  void* out;              // [B,32,128], written when the effective split count is 1
+  void* out;              // [B,32,128], written by pieces that are their row's only one
   float* part_o;          // [B,32,S,128] unnormalised accumulator
   float* part_m;          // [B,32,S]  running max, log2 domain
   float* part_l;          // [B,32,S]  softmax denominator
@@ -100,14 +108,15 @@ constexpr int kScaleStageBytes = 2 * 128 * 2;  // int8 cache: K and V row scales
 __host__ __device__ constexpr int mma_smem_bytes(int kvf, int nq) {
   return mma_stages(kvf, nq) * (kStageBytes + kScaleStageBytes + 2 * 8);
 }
-// Balanced schedule (one CTA per resident slot, each taking an equal run of
-// the tiles of all rows): batches up to this size (the prologue scans the
-// lengths), single-token decode only.  Its merge area sits outside the ring.
+// Balanced schedule: batches up to this size (every CTA's prologue scans the
+// lengths), single-token decode only.  Its merge area sits outside the ring,
+// which keeps streaming the next piece while the consumers merge the last.
 constexpr int kBalMaxBatch = 1024;
 constexpr int kBalMergeBytes = kMmaConsumerWarps * kGroup * (kD + 2) * 4;
 static_assert((kMmaThreads + 3 + kBalMaxBatch) * 4 <= kBalMergeBytes, "the length scan uses the merge area");
-// The epilogue merges the 4 warps' states in the ring (idle by then):
-// [warp][column][128] accumulators + [warp][column] max and denominator.
+// With one piece per CTA the epilogue merges the 4 warps' states in the ring
+// (idle by then): [warp][column][128] accumulators + [warp][column] max and
+// denominator.
 static_assert(kMmaConsumerWarps * kGroup * 1 * (kD + 2) * 4 <= mma_stages(kKvE4M3, 1) * kStageBytes &&
                   kMmaConsumerWarps * kGroup * kMaxQLen * (kD + 2) * 4 <= mma_stages(kKvF16, kMaxQLen) * kStageBytes,
               "merge area must fit in the ring");
@@ -316,10 +325,11 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
     // Balanced schedule: the tiles of every (b, KV head) row, rows in order,
     // form one stream of 8 * sum_b ceil(len_b / tile) tiles; CTA c takes
     // tiles [c * Q, (c + 1) * Q) with Q = max(ceil(total / grid), q_min).
-    // Prefix sums of tiles per row over the batch (all threads; the merge
-    // area is the scratch, idle until the first epilogue: per-thread sums,
-    // the total, the first row and its prefix, then the clamped lengths).
-    int* scan = reinterpret_cast<int*>(mrg_acc);  // [0, 5): warp sums; then first row, its prefix
+    // Prefix sums of tiles per row over the batch, by all threads, each over
+    // a contiguous block of rows.  Scratch: the merge area, idle until the
+    // first epilogue — warp sums at [0, 5), the first row and its prefix at
+    // [161, 163), the clamped lengths from 163 on.
+    int* scan = reinterpret_cast<int*>(mrg_acc);
     int* lsh = scan + kMmaThreads + 3;
     const int B = p.batch;
     const int per_t = (B + kMmaThreads - 1) / kMmaThreads;
