@@ -50,7 +50,7 @@ def _declare(lib):
         "gqa_decode_get_status": (i, [p, sz, p, ctypes.POINTER(ctypes.c_uint32)]),
         "gqa_decode_noalloc": (i, [p, p, p, p, i, i, i, f, i, p]),
         "gqa_decode_int8kv": (i, [p, p, p, p, p, i, i, i, f, i, p, sz, p]),
-        "gqa_decode_paged": (i, [p, i, p, i, p, i, i, i, p, p, i, f, f, f, i, p, sz, p]),
+        "gqa_decode_paged": (i, [p, i, p, i, p, p, i, i, i, p, p, i, i, f, f, f, i, p, sz, p]),
         "gqa_decode_verify": (i, [p, i, p, i, p, p, p, i, i, i, f, f, f, i, p, sz, p]),
         "gqa_append_kv": (i, [p, p, p, p, p, i, p, p, i, p, p, i, p, i, f, f, f, f, p, sz, p]),
         "gqa_decode_debug_skip_tile": (i, [p, i, p, i, p, p, i, i, f, f, f, i, p, sz, i,

@@ -274,13 +274,19 @@ def gqa_decode_int8kv(q, kv, kv_scales, sequence_lengths, q_scale: float = 1.0, 
 
 def gqa_decode_paged(q, kv_pages, block_table, sequence_lengths, q_scale: float = 1.0,
                      k_scale: float = 1.0, v_scale: float = 1.0, out=None, num_splits=None,
-                     workspace=None):
-    """Paged cache: kv_pages [num_pages, 2, 8, page_size, 128] (fp16/bf16, or e4m3 as
-    uint8/float8_e4m3fn), block_table int32 [batch, max_pages]; returns out."""
+                     workspace=None, kv_scales=None):
+    """Paged cache: kv_pages [num_pages, 2, 8, page_size, 128] (fp16/bf16, e4m3 as
+    uint8/float8_e4m3fn, or int8 with kv_scales bf16 [num_pages, 2, 8, page_size]),
+    block_table int32 [batch, max_pages]; q [batch, 32, 128], or [batch, T, 32, 128]
+    for a verify window of T = 1..4 tokens; returns out (q's shape)."""
     _require(q, "q", None, (torch.float16, torch.bfloat16))
     B = q.shape[0]
-    if q.dim() != 3 or q.shape[1:] != (HQ, D):
-        raise ValueError(f"q must be [batch, {HQ}, {D}]")
+    if q.dim() == 3 and q.shape[1:] == (HQ, D):
+        T = 1
+    elif q.dim() == 4 and q.shape[2:] == (HQ, D) and 1 <= q.shape[1] <= 4:
+        T = q.shape[1]
+    else:
+        raise ValueError(f"q must be [batch, {HQ}, {D}] or [batch, T (1..4), {HQ}, {D}]")
     if kv_pages.dim() != 5 or kv_pages.shape[1:3] != (2, HKV) or kv_pages.shape[4] != D:
         raise ValueError("kv_pages must be [num_pages, 2, 8, page_size, 128]")
     _require(kv_pages, "kv_pages", None, tuple(_KVF), q.device)
@@ -290,19 +296,22 @@ def gqa_decode_paged(q, kv_pages, block_table, sequence_lengths, q_scale: float 
     _require(sequence_lengths, "sequence_lengths", (B,), (torch.int32,), q.device)
     kvf = _KVF[kv_pages.dtype]
     num_pages, page_size, max_pages = kv_pages.shape[0], kv_pages.shape[3], block_table.shape[1]
+    if kvf == KV_I8:
+        _require(kv_scales, "kv_scales", (num_pages, 2, HKV, page_size), (torch.bfloat16,), q.device)
     C = max_pages * page_size
     if out is None:
         out = torch.empty_like(q)
     _require(out, "out", q.shape, (q.dtype,), q.device)
     S = plan(B, C, kvf, q.device) if not num_splits else int(num_splits)
-    nbytes = workspace_size(B, C, S)
+    nbytes = workspace_size(B * T, C, S)
     if workspace is None:
         workspace = torch.zeros(nbytes, dtype=torch.uint8, device=q.device)
     with torch.cuda.device(q.device):
         _lib.check(_lib.load().gqa_decode_paged(
-            _ptr(q), _QDT[q.dtype], _ptr(kv_pages), kvf, _ptr(block_table), max_pages, num_pages,
-            page_size, _ptr(sequence_lengths), _ptr(out), B, float(q_scale), float(k_scale),
-            float(v_scale), S, _ptr(workspace), workspace.numel(), _stream(q.device)))
+            _ptr(q), _QDT[q.dtype], _ptr(kv_pages), kvf, _ptr(kv_scales) if kvf == KV_I8 else None,
+            _ptr(block_table), max_pages, num_pages, page_size, _ptr(sequence_lengths), _ptr(out), B, T,
+            float(q_scale), float(k_scale), float(v_scale), S, _ptr(workspace), workspace.numel(),
+            _stream(q.device)))
     return out
 
 

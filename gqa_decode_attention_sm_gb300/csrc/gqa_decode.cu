@@ -222,7 +222,8 @@ gqa_status_t validate(const Call& c, bool q_scale_positive, bool need_q) {
       return fail(GQA_ERR_ALIASING, "out or the workspace overlaps the block table");
   }
   if (c.kv_format == kKvI8) {
-    const size_t sc_bytes = (size_t)c.batch * 2 * kHkv * (size_t)c.capacity * 2;
+    const size_t sc_bytes = c.block_table ? (size_t)c.num_pages * 2 * kHkv * ((size_t)1 << c.page_log2) * 2
+                                          : (size_t)c.batch * 2 * kHkv * (size_t)c.capacity * 2;
     if (overlap(c.out, qo_bytes, c.kv_scales, sc_bytes) || overlap(c.workspace, need, c.kv_scales, sc_bytes))
       return fail(GQA_ERR_ALIASING, "out or the workspace overlaps the int8 scales");
   }
@@ -588,24 +589,32 @@ gqa_status_t gqa_decode_int8kv(const void* q, const int8_t* kv_i8, const uint16_
 }
 
 gqa_status_t gqa_decode_paged(const void* q, gqa_dtype_t q_dtype, const void* kv_pages, gqa_kv_format_t kv_format,
-                              const int32_t* block_table, int max_pages_per_seq, int num_pages, int page_size,
-                              const int32_t* lens, void* out, int batch, float q_scale, float k_scale,
-                              float v_scale, int num_splits, void* workspace, size_t workspace_bytes,
-                              void* stream) {
+                              const uint16_t* kv_scales_pages, const int32_t* block_table, int max_pages_per_seq,
+                              int num_pages, int page_size, const int32_t* lens, void* out, int batch, int q_len,
+                              float q_scale, float k_scale, float v_scale, int num_splits, void* workspace,
+                              size_t workspace_bytes, void* stream) {
   if (!block_table) return fail(GQA_ERR_INVALID_ARGUMENT, "block_table is null");
-  if (kv_format == GQA_KV_I8) return fail(GQA_ERR_INVALID_ARGUMENT, "a paged int8 cache is not supported");
   if (page_size < 16 || page_size > 65536 || (page_size & (page_size - 1)) != 0)
     return fail(GQA_ERR_INVALID_ARGUMENT, "page_size %d is not a power of two in [16, 65536]", page_size);
   if (num_pages < 1 || max_pages_per_seq < 1)
     return fail(GQA_ERR_INVALID_ARGUMENT, "num_pages and max_pages_per_seq must be >= 1");
+  if (q_len < 1 || q_len > kMaxQLen)
+    return fail(GQA_ERR_INVALID_ARGUMENT, "q_len %d outside [1, %d]", q_len, kMaxQLen);
   const long long cap = (long long)max_pages_per_seq * page_size;
   if (cap > (1LL << 30)) return fail(GQA_ERR_INVALID_ARGUMENT, "max_pages_per_seq * page_size exceeds 2^30");
   if (!aligned(block_table, 4)) return fail(GQA_ERR_INVALID_ARGUMENT, "block_table must be 4-byte aligned");
+  if (kv_format == GQA_KV_I8) {
+    if (!kv_scales_pages) return fail(GQA_ERR_INVALID_ARGUMENT, "an int8 cache needs its row scales");
+    if (!aligned(kv_scales_pages, 16))
+      return fail(GQA_ERR_INVALID_ARGUMENT, "the int8 scale pool must be 16-byte aligned");
+  }
   Call c{q, (int)q_dtype, kv_pages, (int)kv_format, lens, out, batch, (int)cap, q_scale, k_scale, v_scale,
          num_splits, workspace, workspace_bytes, static_cast<cudaStream_t>(stream)};
   c.block_table = block_table;
   c.max_pages = max_pages_per_seq;
   c.num_pages = num_pages;
+  c.q_len = q_len;
+  if (kv_format == GQA_KV_I8) c.kv_scales = kv_scales_pages;
   int lg = 0;
   while ((1 << lg) < page_size) ++lg;
   c.page_log2 = lg;

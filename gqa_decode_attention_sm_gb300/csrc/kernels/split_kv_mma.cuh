@@ -60,7 +60,7 @@ constexpr int kStageBytes = 2 * 16384;  // one K tile + one V tile (16 KB each)
 struct SplitParams {
   const void* q;          // [B,32,128] fp16/bf16
   const void* kv;         // [B,2,8,C,128] fp16/bf16/e4m3/int8
-  const uint16_t* kv_scales;  // int8 cache: bf16 [B,2,8,C], one scale per (plane, KV head, slot)
+  const uint16_t* kv_scales;  // int8 cache: bf16 [B or num_pages, 2, 8, C or page size], one scale per row
   const int32_t* lens;    // [B]
   void* out;              // [B,32,128], written by pieces that are their row's only one
   float* part_o;          // [B,32,S,128] unnormalised accumulator
@@ -445,29 +445,20 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
         const int rows = min(T::kTile, t_end - t0);
         uint8_t* dK = ring + st * kStageBytes;
         uint8_t* dV = dK + T::kTileBytes;
-        uint32_t scale_bytes = 0;
-        const uint16_t* gsk = nullptr;
         uint16_t* dsk = scl + st * (kScaleStageBytes / 2);
-        if constexpr (KVF == kKvI8) {
-          // row scales of the tile (contiguous cache): whole 16-byte groups by
-          // bulk copy, the ragged tail (< 8 rows) with plain loads before the arrive
-          gsk = p.kv_scales + ((size_t)b * 2 * kHkv + g) * (size_t)C + t0;
-          const int n8 = rows & ~7;
-          if (lane == 0)
-            for (int r = n8; r < rows; ++r) {
-              dsk[r] = gsk[r];
-              dsk[T::kTile + r] = gsk[(size_t)kHkv * C + r];
-            }
-          scale_bytes = 2u * (uint32_t)n8 * 2u;
-        }
-        if (lane == 0) mbar_arrive_expect_tx(&full[st], 2u * (uint32_t)rows * T::kRowBytes + scale_bytes);
-        // rows [t0, t0 + rows) in page segments; a contiguous cache is one page per batch row
-        for (int t = t0; t < t0 + rows;) {
-          size_t page = (size_t)b;
-          int in_page = t, seg_end = t0 + rows;
+        // The page of slot t (all lanes take part: they fetch block-table
+        // entries 32 at a time): its id, the row in it, and the end of the
+        // segment [t, seg_end) that stays in it.  A contiguous cache is one
+        // page per batch row.
+        const auto seg_of = [&](int t, size_t& page, int& in_page, int& seg_end) {
+          page = (size_t)b;
+          in_page = t;
+          seg_end = t0 + rows;
           if (paged) {
             const int pg = t >> p.page_log2;
-            if (bt_first < 0 || pg >= bt_first + 32) {
+            // (the int8 scale tail looks up a tile's last page before its
+            // first, so the window may have to move back as well as forward)
+            if (bt_first < 0 || pg < bt_first || pg >= bt_first + 32) {
               bt_first = pg;
               const int e = pg + lane;
               bt_val = e < p.max_pages ? __ldg(p.block_table + (size_t)b * p.max_pages + e) : 0;
@@ -481,19 +472,47 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
             in_page = t - (pg << p.page_log2);
             seg_end = min(t0 + rows, (pg + 1) << p.page_log2);
           }
+        };
+        // int8 row scales ([page or b][2][8][rows] bf16): whole 16-byte groups
+        // of 8 rows by bulk copy with their page segment, the ragged tail
+        // (< 8 rows, all in the last page) by plain loads before the arrive
+        const int n8 = rows & ~7;
+        if constexpr (KVF == kKvI8) {
+          if (n8 < rows) {
+            size_t page;
+            int in_page, seg_end;
+            seg_of(t0 + n8, page, in_page, seg_end);
+            if (lane == 0) {
+              const uint16_t* gs = p.kv_scales + (page * 2 * kHkv + g) * page_rows + in_page;
+              for (int r = 0; r < rows - n8; ++r) {
+                dsk[n8 + r] = gs[r];
+                dsk[T::kTile + n8 + r] = gs[(size_t)kHkv * page_rows + r];
+              }
+            }
+          }
+        }
+        const uint32_t scale_bytes = KVF == kKvI8 ? 4u * (uint32_t)n8 : 0u;
+        if (lane == 0) mbar_arrive_expect_tx(&full[st], 2u * (uint32_t)rows * T::kRowBytes + scale_bytes);
+        for (int t = t0; t < t0 + rows;) {
+          size_t page;
+          int in_page, seg_end;
+          seg_of(t, page, in_page, seg_end);
           if (lane == 0) {
             const uint32_t seg_bytes = (uint32_t)(seg_end - t) * T::kRowBytes;
             const uint8_t* src = base + (page * 2 * kHkv + g) * head_bytes + (size_t)in_page * T::kRowBytes;
             bulk_load(dK + (t - t0) * T::kRowBytes, src, seg_bytes, &full[st], pol);
             bulk_load(dV + (t - t0) * T::kRowBytes, src + kHkv * head_bytes, seg_bytes, &full[st], pol);
+            if constexpr (KVF == kKvI8) {
+              const int s_end = min(seg_end, t0 + n8);
+              if (s_end > t) {
+                const uint16_t* gs = p.kv_scales + (page * 2 * kHkv + g) * page_rows + in_page;
+                const uint32_t sb = (uint32_t)(s_end - t) * 2u;
+                bulk_load(dsk + (t - t0), gs, sb, &full[st], pol);
+                bulk_load(dsk + T::kTile + (t - t0), gs + (size_t)kHkv * page_rows, sb, &full[st], pol);
+              }
+            }
           }
           t = seg_end;
-        }
-        if constexpr (KVF == kKvI8) {
-          if (lane == 0 && scale_bytes > 0) {
-            bulk_load(dsk, gsk, scale_bytes / 2, &full[st], pol);
-            bulk_load(dsk + T::kTile, gsk + (size_t)kHkv * C, scale_bytes / 2, &full[st], pol);
-          }
         }
   #pragma unroll
         for (int k = 0; k < kMmaStages; ++k)

@@ -200,10 +200,12 @@ def paginate(t: dict, page_size: int, extra_pages: int = 3, seed: int = 0) -> di
     """Scatter a contiguous cache into a shuffled page pool (a paged cache).
 
     Returns a copy of ``t`` with kv_pages [num_pages, 2, 8, page_size, 128]
-    (same dtype), block_table int32 [B, C/page_size] and num_pages.  Page ids
-    are a seeded permutation; ``extra_pages`` spare pages, and the block-table
-    entries of pages past each length, point at pages filled with NaN (0x7F
-    for e4m3 bytes), which a correct kernel never reads.
+    (same dtype), block_table int32 [B, C/page_size] and num_pages; an int8
+    cache also gets kv_scale_pages bf16 [num_pages, 2, 8, page_size].  Page
+    ids are a seeded permutation; ``extra_pages`` spare pages, and the
+    block-table entries of pages past each length, point at pages filled with
+    NaN (0x7F for e4m3 bytes, -128 codes with NaN scales for int8), which a
+    correct kernel never reads.
     """
     kv = t["kv"]
     B, _, H, C, Dd = kv.shape
@@ -222,12 +224,19 @@ def paginate(t: dict, page_size: int, extra_pages: int = 3, seed: int = 0) -> di
         pages.fill_(-128)
     else:
         pages.fill_(float("nan"))
+    scales = t.get("kv_scales")
+    spages = None
+    if scales is not None:
+        spages = torch.full((num_pages, 2, H, page_size), float("nan"), dtype=scales.dtype, device=kv.device)
     spare = [int(x) for x in ids[len(used):]] or [int(ids[0])]
     table = torch.full((B, per), spare[0], dtype=torch.int32)
     for n, (b, j) in enumerate(used):
         pid = int(ids[n])
         table[b, j] = pid
         pages[pid].copy_(kv[b, :, :, j * page_size:(j + 1) * page_size, :])
+        if spages is not None:
+            spages[pid].copy_(scales[b, :, :, j * page_size:(j + 1) * page_size])
     out = dict(t)
-    out.update(kv_pages=pages, block_table=table.to(kv.device), num_pages=num_pages, page_size=page_size)
+    out.update(kv_pages=pages, block_table=table.to(kv.device), num_pages=num_pages, page_size=page_size,
+               kv_scale_pages=spages)
     return out

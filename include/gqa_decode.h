@@ -169,26 +169,32 @@ gqa_status_t gqa_decode_int8kv(const void* q, const int8_t* kv_i8, const uint16_
 /* Paged KV cache.  The pages only say that a paged cache is gathered into
  * one contiguous prefix matrix before attention; this entry reads the pages
  * in place instead, with the same result.  Layout (this library's reading):
- *   kv_pages    [num_pages, 2, 8, page_size, 128] in `kv_format` (fp16, bf16
- *               or e4m3; not int8), each (page, plane, KV head) block contiguous
- *   block_table int32 [batch, max_pages_per_seq], device memory, read only by
- *               the kernels: slot t of batch row b is row t % page_size of page
- *               block_table[b][t / page_size]
+ *   kv_pages        [num_pages, 2, 8, page_size, 128] in `kv_format` (fp16,
+ *                   bf16, e4m3 or int8), each (page, plane, KV head) block
+ *                   contiguous
+ *   kv_scales_pages int8 only (NULL otherwise): bf16 [num_pages, 2, 8,
+ *                   page_size], the row scales of the same page rows,
+ *                   16-byte aligned
+ *   block_table     int32 [batch, max_pages_per_seq], device memory, read only
+ *                   by the kernels: slot t of batch row b is row t % page_size
+ *                   of page block_table[b][t / page_size]
  * page_size is a power of two in [16, 65536]; the capacity is
  * max_pages_per_seq * page_size (<= 2^30), and lengths follow the usual
  * contract against it.  Only the entries of pages holding slots < len[b] are
  * used; an entry outside [0, num_pages) is clamped and flagged with
- * GQA_FLAG_PAGE_CLAMPED, never dereferenced out of bounds.  q/out dtype
- * `q_dtype` (must equal fp16/bf16 KV; either for e4m3).  k_scale, v_scale as
- * gqa_decode_fp8kv (1 for fp16/bf16).  Both stages, no allocation, no host
- * sync; the workspace as gqa_decode_prepared for capacity
- * max_pages_per_seq * page_size. */
+ * GQA_FLAG_PAGE_CLAMPED, never dereferenced out of bounds.  q_len 1..4: q
+ * and out are [batch, q_len, 32, 128] and query j attends slots
+ * [0, len - q_len + j] (gqa_decode_verify); 1 is plain decode.  q/out dtype
+ * `q_dtype` (must equal fp16/bf16 KV; either for 8-bit KV).  k_scale,
+ * v_scale as gqa_decode_fp8kv (1 for the other formats).  Both stages, no
+ * allocation, no host sync; the workspace as gqa_decode_prepared for batch
+ * * q_len rows and capacity max_pages_per_seq * page_size. */
 gqa_status_t gqa_decode_paged(const void* q, gqa_dtype_t q_dtype, const void* kv_pages,
-                              gqa_kv_format_t kv_format, const int32_t* block_table,
-                              int max_pages_per_seq, int num_pages, int page_size,
-                              const int32_t* lens, void* out, int batch, float q_scale,
-                              float k_scale, float v_scale, int num_splits, void* workspace,
-                              size_t workspace_bytes, void* stream);
+                              gqa_kv_format_t kv_format, const uint16_t* kv_scales_pages,
+                              const int32_t* block_table, int max_pages_per_seq, int num_pages,
+                              int page_size, const int32_t* lens, void* out, int batch, int q_len,
+                              float q_scale, float k_scale, float v_scale, int num_splits,
+                              void* workspace, size_t workspace_bytes, void* stream);
 
 /* Verify window: q_len query tokens per request (1..4), the draft tokens of
  * speculative / multi-token-prediction decoding (the "FP8 KV cache port on

@@ -175,16 +175,17 @@ def gqa_decode(q_bits: np.ndarray, q_fmt: int, kv_bits: np.ndarray, kv_fmt: int,
 def gather_pages(pages: np.ndarray, block_table: np.ndarray, lens: np.ndarray) -> np.ndarray:
     """A paged cache gathered into one contiguous prefix matrix per batch row.
 
-    pages [num_pages, 2, 8, page_size, 128] (bits), block_table int [B, max_pages]:
-    slot t of row b is row t % page_size of page block_table[b, t // page_size].
-    Only the pages that hold slots below each length are gathered; the rest of
-    the returned [B, 2, 8, max_pages * page_size, 128] array is zero.
+    pages [num_pages, 2, 8, page_size, 128] (bits), or an int8 cache's row-scale
+    pool [num_pages, 2, 8, page_size]; block_table int [B, max_pages]: slot t of
+    row b is row t % page_size of page block_table[b, t // page_size].  Only the
+    pages that hold slots below each length are gathered; the rest of the
+    returned [B, 2, 8, max_pages * page_size(, 128)] array is zero.
     (The "FreeToken-Kai on Turing" notes, change 7: gather the prefix out of the
     paged cache so the keys are one contiguous matrix.)
     """
     B, max_pages = block_table.shape
     ps = pages.shape[3]
-    out = np.zeros((B, 2, HKV, max_pages * ps, D), dtype=pages.dtype)
+    out = np.zeros((B, 2, HKV, max_pages * ps) + tuple(pages.shape[4:]), dtype=pages.dtype)
     for b in range(B):
         for j in range(-(-int(lens[b]) // ps)):
             out[b, :, :, j * ps:(j + 1) * ps] = pages[int(block_table[b, j])]

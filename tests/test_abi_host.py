@@ -217,20 +217,23 @@ def test_paged_validation(lib):
     BT = 0x70000000
 
     def call(**kw):
-        a = dict(q=Q, qd=F16, kv=KV, kvf=KV_F16, bt=BT, maxp=4, nump=16, ps=64, lens=LENS, out=OUT, B=2,
-                 S=1, ws=WS, wsb=256)
+        a = dict(q=Q, qd=F16, kv=KV, kvf=KV_F16, sc=None, bt=BT, maxp=4, nump=16, ps=64, lens=LENS, out=OUT,
+                 B=2, T=1, S=1, ws=WS, wsb=256)
         a.update(kw)
-        return f(a["q"], a["qd"], a["kv"], a["kvf"], a["bt"], a["maxp"], a["nump"], a["ps"], a["lens"],
-                 a["out"], a["B"], 1.0, 1.0, 1.0, a["S"], a["ws"], a["wsb"], None)
+        return f(a["q"], a["qd"], a["kv"], a["kvf"], a["sc"], a["bt"], a["maxp"], a["nump"], a["ps"],
+                 a["lens"], a["out"], a["B"], a["T"], 1.0, 1.0, 1.0, a["S"], a["ws"], a["wsb"], None)
 
     assert call(bt=None) == EINVAL
-    assert call(kvf=KV_I8) == EINVAL                 # no paged int8
+    assert call(kvf=KV_I8) == EINVAL                 # int8 without its scale pool
+    assert call(kvf=KV_I8, sc=0x60000008) == EINVAL  # scale pool not 16-byte aligned
+    assert call(T=0) == EINVAL and call(T=5) == EINVAL
     assert call(ps=48) == EINVAL and call(ps=8) == EINVAL and call(ps=1 << 17) == EINVAL
     assert call(nump=0) == EINVAL and call(maxp=0) == EINVAL
     assert call(maxp=1 << 20, ps=2048) == EINVAL     # capacity above 2^30
     assert call(bt=BT + 2) == EINVAL
     assert call(out=BT) == EALIAS                    # out on the block table
     assert call(S=4) == EWS
+    assert call(S=4, T=2, wsb=lib.gqa_decode_workspace_size(2, 256, 4)) == EWS  # the window needs 2 x rows
 
 
 def test_verify_validation(lib):

@@ -485,7 +485,53 @@ def _paged(pt, out=None, num_splits=None):
     fp8 = w.kv_dtype == "e4m3"
     return gq.gqa_decode_paged(pt["q"], pt["kv_pages"], pt["block_table"], pt["lens"],
                                q_scale=pt["q_scale"], k_scale=pt["k_scale"] if fp8 else 1.0,
-                               v_scale=pt["v_scale"] if fp8 else 1.0, out=out, num_splits=num_splits)
+                               v_scale=pt["v_scale"] if fp8 else 1.0, out=out, num_splits=num_splits,
+                               kv_scales=pt.get("kv_scale_pages"))
+
+
+@pytest.mark.parametrize("q_dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("page_size", [16, 64, 256])
+def test_paged_int8_matches_oracle_and_contiguous_path(q_dtype, page_size):
+    # lengths with ragged scale tails (1, 17, 300: not multiples of 8) and
+    # tiles spanning several 16-row pages
+    w = inputs.custom(5, 1024, 1, 1024, kv_dtype="i8", q_dtype=q_dtype, nan_tail=True)
+    t = _make(w, lens=[1, 17, 300, 1000, 1024])
+    pt = inputs.paginate(t, page_size, extra_pages=5, seed=page_size)
+    ref = _oracle_full(t)
+    for S in (None, 3):
+        out = _paged(pt, num_splits=S)
+        torch.cuda.synchronize()
+        _assert_parity(_gpu_rows(out), ref, f"paged int8 page {page_size} splits {S}")
+        contiguous = _run(t, num_splits=S).out
+        assert torch.equal(out.view(torch.int16), contiguous.view(torch.int16))
+
+
+def test_paged_int8_balanced_schedule():
+    rng = np.random.default_rng(12)
+    C = 4096
+    w = inputs.custom(48, C, 1, kv_dtype="i8", nan_tail=True)
+    t = _make(w, lens=rng.integers(1, C + 1, 48).tolist())
+    ref = _oracle_full(t)
+    pt = inputs.paginate(t, 64, extra_pages=5)
+    out = _paged(pt, num_splits=8)
+    torch.cuda.synchronize()
+    _assert_parity(_gpu_rows(out), ref, "paged int8, balanced")
+
+
+@pytest.mark.parametrize("kv_dtype", ["f16", "e4m3", "i8"])
+@pytest.mark.parametrize("T", [2, 4])
+def test_paged_verify_window(kv_dtype, T):
+    w = inputs.custom(4, 1024, T, 1024, kv_dtype=kv_dtype, kv_std=2.0 if kv_dtype == "e4m3" else 1.0,
+                      nan_tail=True, q_len=T)
+    t = _make(w, lens=[T, 100, 777, 1024])
+    pt = inputs.paginate(t, 64, extra_pages=3, seed=T)
+    ref = _oracle_full(t)
+    for S in (None, 5):
+        out = _paged(pt, num_splits=S)
+        torch.cuda.synchronize()
+        _assert_parity(_gpu_rows(out), ref, f"paged window {T} {kv_dtype} splits {S}")
+        contiguous = _verify(t, num_splits=S)
+        assert torch.equal(out.view(torch.int16), contiguous.view(torch.int16))
 
 
 @pytest.mark.parametrize("kv_dtype", ["f16", "bf16", "e4m3"])

@@ -375,6 +375,22 @@ def test_paged_gather_reproduces_the_contiguous_cache(orc, page_size):
     assert np.array_equal(a, c)
 
 
+@pytest.mark.parametrize("page_size", [16, 64])
+def test_paged_gather_of_an_int8_cache_and_its_scale_pool(orc, page_size):
+    w = inputs.custom(3, 256, 1, 256, kv_dtype="i8", nan_tail=True)
+    t, qb, kvb, lens = _random(w, seed=6)
+    pt = inputs.paginate(t, page_size, extra_pages=4, seed=10)
+    g = oracle.gather_pages(bits_of(pt["kv_pages"]), pt["block_table"].numpy(), lens)
+    gs = oracle.gather_pages(bits_of(pt["kv_scale_pages"]), pt["block_table"].numpy(), lens)
+    sc = bits_of(t["kv_scales"])
+    for b in range(3):
+        assert np.array_equal(g[b, :, :, :lens[b]], kvb[b, :, :, :lens[b]])
+        assert np.array_equal(gs[b, :, :, :lens[b]], sc[b, :, :, :lens[b]])
+    a, _ = _run(orc, t, qb, kvb, lens)
+    c, _ = _run(orc, t, qb, g, lens, kv_scales=gs)
+    assert np.array_equal(a, c)
+
+
 # ----------------------------------------------------------- verify window
 
 
