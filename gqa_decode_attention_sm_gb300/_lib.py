@@ -20,7 +20,7 @@ EXPORTS = (
     "gqa_decode", "gqa_decode_prepared", "gqa_decode_fp8kv", "gqa_decode_split_stage",
     "gqa_decode_combine_stage", "gqa_decode_workspace_init", "gqa_decode_get_status",
     "gqa_decode_noalloc", "gqa_decode_debug_skip_tile", "gqa_decode_int8kv", "gqa_decode_paged",
-    "gqa_decode_verify", "gqa_append_kv",
+    "gqa_decode_verify", "gqa_append_kv", "gqa_append_kv_paged",
 )
 
 
@@ -53,6 +53,7 @@ def _declare(lib):
         "gqa_decode_paged": (i, [p, i, p, i, p, p, i, i, i, p, p, i, i, f, f, f, i, p, sz, p]),
         "gqa_decode_verify": (i, [p, i, p, i, p, p, p, i, i, i, f, f, f, i, p, sz, p]),
         "gqa_append_kv": (i, [p, p, p, p, p, i, p, p, i, p, p, i, p, i, f, f, f, f, p, sz, p]),
+        "gqa_append_kv_paged": (i, [p, p, p, p, p, i, p, p, i, p, p, i, p, p, i, i, i, f, f, f, f, p, sz, p]),
         "gqa_decode_debug_skip_tile": (i, [p, i, p, i, p, p, i, i, f, f, f, i, p, sz, i,
                                            ctypes.c_uint64, p]),
     }

@@ -33,7 +33,7 @@ _QDT = {torch.float16: F16, torch.bfloat16: BF16}
 _KVF = {torch.float16: KV_F16, torch.bfloat16: KV_BF16, torch.uint8: KV_E4M3,
         torch.float8_e4m3fn: KV_E4M3, torch.int8: KV_I8}
 
-__all__ = ["GqaError", "gqa_decode", "gqa_decode_fp8kv", "gqa_decode_int8kv", "gqa_decode_paged",
+__all__ = ["GqaError", "append_kv_paged", "gqa_decode", "gqa_decode_fp8kv", "gqa_decode_int8kv", "gqa_decode_paged",
            "gqa_decode_verify", "append_kv",
            "prepare", "launch",
            "Prepared",
@@ -375,6 +375,47 @@ def append_kv(q_proj, k_proj, v_proj, q_norm_w, k_norm_w, positions, slots, kv, 
             _ptr(positions), _ptr(slots), B, _ptr(q_out), _ptr(kv), kvf,
             _ptr(kv_scales) if kv_scales is not None else None, kv.shape[3], float(eps), float(rope_theta),
             float(k_scale), float(v_scale), _ptr(workspace) if workspace is not None else None,
+            workspace.numel() if workspace is not None else 0, _stream(q_proj.device)))
+    return q_out
+
+
+def append_kv_paged(q_proj, k_proj, v_proj, q_norm_w, k_norm_w, positions, slots, kv_pages, block_table,
+                    q_out=None, eps: float = 1e-6, rope_theta: float = 1e6, k_scale: float = 1.0,
+                    v_scale: float = 1.0, kv_scales=None, workspace=None):
+    """append_kv on a paged cache: kv_pages [num_pages, 2, 8, page_size, 128] (and,
+    for int8, kv_scales [num_pages, 2, 8, page_size] bf16), block_table int32
+    [batch, max_pages]; slot s of row b lands in row s % page_size of page
+    block_table[b, s // page_size]."""
+    _require(q_proj, "q_proj", None, (torch.float16, torch.bfloat16))
+    B = q_proj.shape[0]
+    dt = q_proj.dtype
+    _require(q_proj, "q_proj", (B, HQ, D), (dt,))
+    _require(k_proj, "k_proj", (B, HKV, D), (dt,), q_proj.device)
+    _require(v_proj, "v_proj", (B, HKV, D), (dt,), q_proj.device)
+    _require(q_norm_w, "q_norm_w", (D,), (dt,), q_proj.device)
+    _require(k_norm_w, "k_norm_w", (D,), (dt,), q_proj.device)
+    _require(positions, "positions", (B,), (torch.int32,), q_proj.device)
+    _require(slots, "slots", (B,), (torch.int32,), q_proj.device)
+    if kv_pages.dim() != 5 or kv_pages.shape[1:3] != (2, HKV) or kv_pages.shape[4] != D:
+        raise ValueError("kv_pages must be [num_pages, 2, 8, page_size, 128]")
+    _require(kv_pages, "kv_pages", None, tuple(_KVF), q_proj.device)
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("block_table must be [batch, max_pages]")
+    _require(block_table, "block_table", None, (torch.int32,), q_proj.device)
+    kvf = _KVF[kv_pages.dtype]
+    num_pages, page_size = kv_pages.shape[0], kv_pages.shape[3]
+    if kvf == KV_I8:
+        _require(kv_scales, "kv_scales", (num_pages, 2, HKV, page_size), (torch.bfloat16,), q_proj.device)
+    if q_out is None:
+        q_out = torch.empty_like(q_proj)
+    _require(q_out, "q_out", q_proj.shape, (dt,), q_proj.device)
+    with torch.cuda.device(q_proj.device):
+        _lib.check(_lib.load().gqa_append_kv_paged(
+            _ptr(q_proj), _ptr(k_proj), _ptr(v_proj), _ptr(q_norm_w), _ptr(k_norm_w), _QDT[dt],
+            _ptr(positions), _ptr(slots), B, _ptr(q_out), _ptr(kv_pages), kvf,
+            _ptr(kv_scales) if kv_scales is not None else None, _ptr(block_table), block_table.shape[1],
+            num_pages, page_size, float(eps), float(rope_theta), float(k_scale), float(v_scale),
+            _ptr(workspace) if workspace is not None else None,
             workspace.numel() if workspace is not None else 0, _stream(q_proj.device)))
     return q_out
 

@@ -484,6 +484,97 @@ gqa_status_t prepare_call(Call& c, bool q_scale_positive, bool need_q) {
   return st;
 }
 
+// The append step on a contiguous cache (block_table = nullptr; `units` =
+// batch, `unit_rows` = capacity) or a paged one (units = num_pages, unit_rows
+// = page size, capacity = max_pages * page size).
+gqa_status_t append_kv(const void* q_proj, const void* k_proj, const void* v_proj, const void* q_norm_w,
+                       const void* k_norm_w, gqa_dtype_t dtype, const int32_t* positions, const int32_t* slots,
+                       int batch, void* q_out, void* kv, gqa_kv_format_t kv_format, uint16_t* kv_scales_bf16,
+                       int capacity, const int32_t* block_table, int max_pages, int num_pages, int page_log2,
+                       size_t units, size_t unit_rows, float eps, float rope_theta, float k_scale, float v_scale,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q_proj || !k_proj || !v_proj || !q_norm_w || !k_norm_w || !positions || !slots || !q_out || !kv)
+    return fail(GQA_ERR_INVALID_ARGUMENT, "null pointer argument");
+  gqa_status_t st = validate_shape(batch, capacity);
+  if (st != GQA_OK) return st;
+  if (dtype != GQA_F16 && dtype != GQA_BF16) return fail(GQA_ERR_INVALID_ARGUMENT, "unknown dtype %d", (int)dtype);
+  const int fmt = (int)kv_format;
+  if (fmt != kKvF16 && fmt != kKvBF16 && fmt != kKvE4M3 && fmt != kKvI8)
+    return fail(GQA_ERR_INVALID_ARGUMENT, "unknown KV format %d", fmt);
+  if (!is_8bit(fmt) && fmt != (int)dtype)
+    return fail(GQA_ERR_INVALID_ARGUMENT, "fp16/bf16 KV must have the dtype of the projections");
+  if (fmt == kKvI8 && !kv_scales_bf16) return fail(GQA_ERR_INVALID_ARGUMENT, "an int8 cache needs kv_scales_bf16");
+  if (!std::isfinite(eps) || eps < 0.f) return fail(GQA_ERR_INVALID_ARGUMENT, "eps must be finite and >= 0");
+  if (!std::isfinite(rope_theta) || rope_theta <= 0.f)
+    return fail(GQA_ERR_INVALID_ARGUMENT, "rope_theta must be finite and > 0");
+  if (!std::isfinite(k_scale) || k_scale <= 0.f || !std::isfinite(v_scale) || v_scale <= 0.f)
+    return fail(GQA_ERR_INVALID_ARGUMENT, "k_scale and v_scale must be finite and > 0");
+  if (workspace && workspace_bytes < GQA_WORKSPACE_HEADER_BYTES)
+    return fail(GQA_ERR_WORKSPACE_TOO_SMALL, "workspace smaller than its %d-byte header", GQA_WORKSPACE_HEADER_BYTES);
+  const void* h16[] = {q_proj, k_proj, v_proj, q_norm_w, k_norm_w, q_out};
+  for (const void* ptr : h16)
+    if (!aligned(ptr, 2)) return fail(GQA_ERR_INVALID_ARGUMENT, "16-bit arrays must be 2-byte aligned");
+  if (!aligned(positions, 4) || !aligned(slots, 4) || (workspace && !aligned(workspace, 4)) ||
+      (!is_8bit(fmt) && !aligned(kv, 2)) || (kv_scales_bf16 && !aligned(kv_scales_bf16, 2)))
+    return fail(GQA_ERR_INVALID_ARGUMENT, "misaligned argument");
+  const size_t qb = (size_t)batch * kHq * kD * 2, kvb_in = (size_t)batch * kHkv * kD * 2;
+  const size_t cache = units * 2 * kHkv * unit_rows * kD * kv_elem_bytes(fmt);
+  const void* ins[] = {q_proj, k_proj, v_proj};
+  const size_t in_bytes[] = {qb, kvb_in, kvb_in};
+  for (int i = 0; i < 3; ++i)
+    if (overlap(q_out, qb, ins[i], in_bytes[i]) || overlap(kv, cache, ins[i], in_bytes[i]))
+      return fail(GQA_ERR_ALIASING, "q_out or kv overlaps an input projection");
+  if (overlap(q_out, qb, kv, cache)) return fail(GQA_ERR_ALIASING, "q_out overlaps kv");
+  int dev_sms = 0;
+  st = current_device_ready(&dev_sms);
+  if (st != GQA_OK) return st;
+  AppendParams ap;
+  ap.q_proj = q_proj;
+  ap.k_proj = k_proj;
+  ap.v_proj = v_proj;
+  ap.q_norm_w = q_norm_w;
+  ap.k_norm_w = k_norm_w;
+  ap.positions = positions;
+  ap.slots = slots;
+  ap.q_out = q_out;
+  ap.kv = kv;
+  ap.kv_scales = kv_scales_bf16;
+  ap.flags = static_cast<uint32_t*>(workspace);
+  ap.batch = batch;
+  ap.capacity = capacity;
+  ap.block_table = block_table;
+  ap.max_pages = max_pages;
+  ap.num_pages = num_pages;
+  ap.page_log2 = page_log2;
+  ap.eps = eps;
+  ap.k_inv_scale = 1.f / k_scale;
+  ap.v_inv_scale = 1.f / v_scale;
+  ap.theta = (double)rope_theta;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(batch, 1, 1);
+  cfg.blockDim = dim3(kAppendThreads, 1, 1);
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  // programmatic dependent launch, as the split kernel: the kernel waits for
+  // the previous grid before its first read
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e;
+  const bool bf = dtype == GQA_BF16;
+  if (fmt == kKvF16) e = cudaLaunchKernelEx(&cfg, append_kv_kernel<kKvF16, kQF16>, ap);
+  else if (fmt == kKvBF16) e = cudaLaunchKernelEx(&cfg, append_kv_kernel<kKvBF16, kQBF16>, ap);
+  else if (fmt == kKvE4M3)
+    e = bf ? cudaLaunchKernelEx(&cfg, append_kv_kernel<kKvE4M3, kQBF16>, ap)
+           : cudaLaunchKernelEx(&cfg, append_kv_kernel<kKvE4M3, kQF16>, ap);
+  else
+    e = bf ? cudaLaunchKernelEx(&cfg, append_kv_kernel<kKvI8, kQBF16>, ap)
+           : cudaLaunchKernelEx(&cfg, append_kv_kernel<kKvI8, kQF16>, ap);
+  if (e != cudaSuccess) return cuda_fail(e, "append kernel launch");
+  return GQA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -642,87 +733,39 @@ gqa_status_t gqa_decode_verify(const void* q, gqa_dtype_t q_dtype, const void* k
   return run_combine(c);
 }
 
+
 gqa_status_t gqa_append_kv(const void* q_proj, const void* k_proj, const void* v_proj, const void* q_norm_w,
                            const void* k_norm_w, gqa_dtype_t dtype, const int32_t* positions, const int32_t* slots,
                            int batch, void* q_out, void* kv, gqa_kv_format_t kv_format, uint16_t* kv_scales_bf16,
                            int capacity, float eps, float rope_theta, float k_scale, float v_scale, void* workspace,
                            size_t workspace_bytes, void* stream) {
-  if (!q_proj || !k_proj || !v_proj || !q_norm_w || !k_norm_w || !positions || !slots || !q_out || !kv)
-    return fail(GQA_ERR_INVALID_ARGUMENT, "null pointer argument");
-  gqa_status_t st = validate_shape(batch, capacity);
-  if (st != GQA_OK) return st;
-  if (dtype != GQA_F16 && dtype != GQA_BF16) return fail(GQA_ERR_INVALID_ARGUMENT, "unknown dtype %d", (int)dtype);
-  const int fmt = (int)kv_format;
-  if (fmt != kKvF16 && fmt != kKvBF16 && fmt != kKvE4M3 && fmt != kKvI8)
-    return fail(GQA_ERR_INVALID_ARGUMENT, "unknown KV format %d", fmt);
-  if (!is_8bit(fmt) && fmt != (int)dtype)
-    return fail(GQA_ERR_INVALID_ARGUMENT, "fp16/bf16 KV must have the dtype of the projections");
-  if (fmt == kKvI8 && !kv_scales_bf16) return fail(GQA_ERR_INVALID_ARGUMENT, "an int8 cache needs kv_scales_bf16");
-  if (!std::isfinite(eps) || eps < 0.f) return fail(GQA_ERR_INVALID_ARGUMENT, "eps must be finite and >= 0");
-  if (!std::isfinite(rope_theta) || rope_theta <= 0.f)
-    return fail(GQA_ERR_INVALID_ARGUMENT, "rope_theta must be finite and > 0");
-  if (!std::isfinite(k_scale) || k_scale <= 0.f || !std::isfinite(v_scale) || v_scale <= 0.f)
-    return fail(GQA_ERR_INVALID_ARGUMENT, "k_scale and v_scale must be finite and > 0");
-  if (workspace && workspace_bytes < GQA_WORKSPACE_HEADER_BYTES)
-    return fail(GQA_ERR_WORKSPACE_TOO_SMALL, "workspace smaller than its %d-byte header", GQA_WORKSPACE_HEADER_BYTES);
-  const void* h16[] = {q_proj, k_proj, v_proj, q_norm_w, k_norm_w, q_out};
-  for (const void* ptr : h16)
-    if (!aligned(ptr, 2)) return fail(GQA_ERR_INVALID_ARGUMENT, "16-bit arrays must be 2-byte aligned");
-  if (!aligned(positions, 4) || !aligned(slots, 4) || (workspace && !aligned(workspace, 4)) ||
-      (!is_8bit(fmt) && !aligned(kv, 2)) || (kv_scales_bf16 && !aligned(kv_scales_bf16, 2)))
-    return fail(GQA_ERR_INVALID_ARGUMENT, "misaligned argument");
-  const size_t qb = (size_t)batch * kHq * kD * 2, kvb_in = (size_t)batch * kHkv * kD * 2;
-  const size_t cache = (size_t)batch * 2 * kHkv * (size_t)capacity * kD * kv_elem_bytes(fmt);
-  const void* ins[] = {q_proj, k_proj, v_proj};
-  const size_t in_bytes[] = {qb, kvb_in, kvb_in};
-  for (int i = 0; i < 3; ++i)
-    if (overlap(q_out, qb, ins[i], in_bytes[i]) || overlap(kv, cache, ins[i], in_bytes[i]))
-      return fail(GQA_ERR_ALIASING, "q_out or kv overlaps an input projection");
-  if (overlap(q_out, qb, kv, cache)) return fail(GQA_ERR_ALIASING, "q_out overlaps kv");
-  int dev_sms = 0;
-  st = current_device_ready(&dev_sms);
-  if (st != GQA_OK) return st;
-  AppendParams ap;
-  ap.q_proj = q_proj;
-  ap.k_proj = k_proj;
-  ap.v_proj = v_proj;
-  ap.q_norm_w = q_norm_w;
-  ap.k_norm_w = k_norm_w;
-  ap.positions = positions;
-  ap.slots = slots;
-  ap.q_out = q_out;
-  ap.kv = kv;
-  ap.kv_scales = kv_scales_bf16;
-  ap.flags = static_cast<uint32_t*>(workspace);
-  ap.batch = batch;
-  ap.capacity = capacity;
-  ap.eps = eps;
-  ap.k_inv_scale = 1.f / k_scale;
-  ap.v_inv_scale = 1.f / v_scale;
-  ap.theta = (double)rope_theta;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(batch, 1, 1);
-  cfg.blockDim = dim3(kAppendThreads, 1, 1);
-  cfg.stream = static_cast<cudaStream_t>(stream);
-  // programmatic dependent launch, as the split kernel: the kernel waits for
-  // the previous grid before its first read
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaError_t e;
-  const bool bf = dtype == GQA_BF16;
-  if (fmt == kKvF16) e = cudaLaunchKernelEx(&cfg, append_kv_kernel<kKvF16, kQF16>, ap);
-  else if (fmt == kKvBF16) e = cudaLaunchKernelEx(&cfg, append_kv_kernel<kKvBF16, kQBF16>, ap);
-  else if (fmt == kKvE4M3)
-    e = bf ? cudaLaunchKernelEx(&cfg, append_kv_kernel<kKvE4M3, kQBF16>, ap)
-           : cudaLaunchKernelEx(&cfg, append_kv_kernel<kKvE4M3, kQF16>, ap);
-  else
-    e = bf ? cudaLaunchKernelEx(&cfg, append_kv_kernel<kKvI8, kQBF16>, ap)
-           : cudaLaunchKernelEx(&cfg, append_kv_kernel<kKvI8, kQF16>, ap);
-  if (e != cudaSuccess) return cuda_fail(e, "append kernel launch");
-  return GQA_OK;
+  if (capacity < 1) return fail(GQA_ERR_INVALID_ARGUMENT, "capacity %d < 1", capacity);
+  return append_kv(q_proj, k_proj, v_proj, q_norm_w, k_norm_w, dtype, positions, slots, batch, q_out, kv, kv_format,
+                   kv_scales_bf16, capacity, nullptr, 0, 0, 0, batch > 0 ? (size_t)batch : 0, (size_t)capacity,
+                   eps, rope_theta, k_scale, v_scale, workspace, workspace_bytes, stream);
+}
+
+gqa_status_t gqa_append_kv_paged(const void* q_proj, const void* k_proj, const void* v_proj,
+                                 const void* q_norm_w, const void* k_norm_w, gqa_dtype_t dtype,
+                                 const int32_t* positions, const int32_t* slots, int batch, void* q_out,
+                                 void* kv_pages, gqa_kv_format_t kv_format, uint16_t* kv_scales_pages,
+                                 const int32_t* block_table, int max_pages_per_seq, int num_pages, int page_size,
+                                 float eps, float rope_theta, float k_scale, float v_scale, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  if (!block_table) return fail(GQA_ERR_INVALID_ARGUMENT, "block_table is null");
+  if (page_size < 16 || page_size > 65536 || (page_size & (page_size - 1)) != 0)
+    return fail(GQA_ERR_INVALID_ARGUMENT, "page_size %d is not a power of two in [16, 65536]", page_size);
+  if (num_pages < 1 || max_pages_per_seq < 1)
+    return fail(GQA_ERR_INVALID_ARGUMENT, "num_pages and max_pages_per_seq must be >= 1");
+  const long long cap = (long long)max_pages_per_seq * page_size;
+  if (cap > (1LL << 30)) return fail(GQA_ERR_INVALID_ARGUMENT, "max_pages_per_seq * page_size exceeds 2^30");
+  if (!aligned(block_table, 4)) return fail(GQA_ERR_INVALID_ARGUMENT, "block_table must be 4-byte aligned");
+  int lg = 0;
+  while ((1 << lg) < page_size) ++lg;
+  return append_kv(q_proj, k_proj, v_proj, q_norm_w, k_norm_w, dtype, positions, slots, batch, q_out, kv_pages,
+                   kv_format, kv_scales_pages, (int)cap, block_table, max_pages_per_seq, num_pages, lg,
+                   (size_t)num_pages, (size_t)page_size, eps, rope_theta, k_scale, v_scale, workspace,
+                   workspace_bytes, stream);
 }
 
 gqa_status_t gqa_decode_split_stage(const void* q, gqa_dtype_t q_dtype, const void* kv,

@@ -35,10 +35,14 @@ struct AppendParams {
   const int32_t* positions;  // [B] rotary positions
   const int32_t* slots;      // [B] cache slots to write
   void* q_out;             // [B,32,128]
-  void* kv;                // [B,2,8,C,128] in the cache format
-  uint16_t* kv_scales;     // int8 cache: [B,2,8,C] bf16
+  void* kv;                // [B,2,8,C,128] in the cache format (paged: [num_pages,2,8,page,128])
+  uint16_t* kv_scales;     // int8 cache: [B,2,8,C] bf16 (paged: [num_pages,2,8,page])
   uint32_t* flags;         // optional status word
-  int batch, capacity;
+  int batch, capacity;     // capacity: C, or max_pages * page size for a paged cache
+  // paged cache (block_table != nullptr): slot s of row b is row s % page of
+  // page block_table[b * max_pages + s / page]
+  const int32_t* block_table;
+  int max_pages, num_pages, page_log2;
   float eps, k_inv_scale, v_inv_scale;  // e4m3: 1/k_scale, 1/v_scale
   double theta;
 };
@@ -81,8 +85,21 @@ __global__ void __launch_bounds__(kAppendThreads) append_kv_kernel(const __grid_
   __syncthreads();
   const int C = p.capacity;
   const int slot = __ldg(p.slots + b);
-  const bool slot_ok = slot >= 0 && slot < C;
+  bool slot_ok = slot >= 0 && slot < C;
   if (!slot_ok && threadIdx.x == 0 && p.flags) atomicOr(p.flags, GQA_FLAG_SLOT_CLAMPED);
+  // where the slot's row lives: (unit, row) in [units][2][8][unit_rows][128],
+  // unit = the batch row of a contiguous cache or a page of a paged one
+  size_t unit = (size_t)b, row_in = (size_t)max(slot, 0), unit_rows = (size_t)C;
+  if (p.block_table != nullptr && slot_ok) {
+    const int id = __ldg(p.block_table + (size_t)b * p.max_pages + (slot >> p.page_log2));
+    if (id < 0 || id >= p.num_pages) {  // never write through an out-of-range entry
+      slot_ok = false;
+      if (threadIdx.x == 0 && p.flags) atomicOr(p.flags, GQA_FLAG_PAGE_CLAMPED);
+    }
+    unit = (size_t)max(id, 0);
+    unit_rows = (size_t)1 << p.page_log2;
+    row_in = (size_t)(slot & ((1 << p.page_log2) - 1));
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int dims[4] = {lane, lane + 32, lane + 64, lane + 96};
 
@@ -120,7 +137,8 @@ __global__ void __launch_bounds__(kAppendThreads) append_kv_kernel(const __grid_
     }
     if (!slot_ok) continue;  // never write outside the cache
     const int plane = is_k ? 0 : 1;
-    const size_t crow = ((((size_t)b * 2 + plane) * kHkv + g) * (size_t)C + slot) * kD;
+    const size_t srow = ((unit * 2 + plane) * kHkv + g) * unit_rows + row_in;  // the scale's index
+    const size_t crow = srow * kD;
     if constexpr (KVF == kKvE4M3) {
       const float inv = is_k ? p.k_inv_scale : p.v_inv_scale;
       uint8_t* dst = static_cast<uint8_t*>(p.kv) + crow;
@@ -139,7 +157,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_kv_kernel(const __grid_
         const int code = max(-127, min(127, __float2int_rn(z[k] / scale)));
         dst[dims[k]] = (int8_t)code;
       }
-      if (lane == 0) p.kv_scales[(((size_t)b * 2 + plane) * kHkv + g) * (size_t)C + slot] = sb;
+      if (lane == 0) p.kv_scales[srow] = sb;
     } else {
       uint16_t* dst = static_cast<uint16_t*>(p.kv) + crow;
 #pragma unroll

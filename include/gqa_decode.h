@@ -87,7 +87,7 @@ typedef enum { GQA_KV_F16 = 0, GQA_KV_BF16 = 1, GQA_KV_E4M3 = 2, GQA_KV_I8 = 3 }
 /* Bits of the status word in the workspace header. */
 #define GQA_FLAG_LENGTH_CLAMPED 0x1u  /* some lens[b] was outside [1, capacity] */
 #define GQA_FLAG_WAIT_TIMEOUT 0x2u    /* a pipeline wait gave up; outputs are invalid */
-#define GQA_FLAG_PAGE_CLAMPED 0x4u    /* a block-table entry was outside [0, num_pages) */
+#define GQA_FLAG_PAGE_CLAMPED 0x4u    /* a block-table entry was outside [0, num_pages) (decode: clamped; append: not written) */
 #define GQA_FLAG_SLOT_CLAMPED 0x8u    /* gqa_append_kv: a slot outside [0, capacity), not written */
 
 /* Name of a status code (static string). */
@@ -306,6 +306,23 @@ gqa_status_t gqa_append_kv(const void* q_proj, const void* k_proj, const void* v
                            void* kv, gqa_kv_format_t kv_format, uint16_t* kv_scales_bf16, int capacity,
                            float eps, float rope_theta, float k_scale, float v_scale, void* workspace,
                            size_t workspace_bytes, void* stream);
+
+/* The same step on a paged cache (the layout of gqa_decode_paged): slot
+ * slots[b] of row b is row slots[b] % page_size of page
+ * block_table[b][slots[b] / page_size]; an int8 cache writes its fresh row
+ * scale into kv_scales_pages [num_pages, 2, 8, page_size].  A slot outside
+ * [0, max_pages_per_seq * page_size) sets GQA_FLAG_SLOT_CLAMPED and a
+ * block-table entry outside [0, num_pages) sets GQA_FLAG_PAGE_CLAMPED; in both
+ * cases nothing of that row is written to the cache (q_out still is).  Other
+ * arguments and rules as gqa_append_kv. */
+gqa_status_t gqa_append_kv_paged(const void* q_proj, const void* k_proj, const void* v_proj,
+                                 const void* q_norm_w, const void* k_norm_w, gqa_dtype_t dtype,
+                                 const int32_t* positions, const int32_t* slots, int batch,
+                                 void* q_out, void* kv_pages, gqa_kv_format_t kv_format,
+                                 uint16_t* kv_scales_pages, const int32_t* block_table,
+                                 int max_pages_per_seq, int num_pages, int page_size, float eps,
+                                 float rope_theta, float k_scale, float v_scale, void* workspace,
+                                 size_t workspace_bytes, void* stream);
 
 /* Zero the workspace header (status flags) on `stream`.  Asynchronous. */
 gqa_status_t gqa_decode_workspace_init(void* workspace, size_t workspace_bytes, void* stream);

@@ -236,6 +236,26 @@ def test_paged_validation(lib):
     assert call(S=4, T=2, wsb=lib.gqa_decode_workspace_size(2, 256, 4)) == EWS  # the window needs 2 x rows
 
 
+def test_append_paged_validation(lib):
+    f = lib.gqa_append_kv_paged
+    P = 0x11000000  # stand-in device addresses (validation fails before any launch)
+
+    def call(**kw):
+        a = dict(bt=0x70000000, kvf=KV_F16, sc=None, maxp=4, nump=16, ps=64, ws=None, wsb=0)
+        a.update(kw)
+        return f(P, P + 0x100000, P + 0x200000, P + 0x300000, P + 0x400000, F16, 0x12000000, 0x12100000, 2,
+                 0x13000000, KV, a["kvf"], a["sc"], a["bt"], a["maxp"], a["nump"], a["ps"], 1e-6, 1e6, 1.0,
+                 1.0, a["ws"], a["wsb"], None)
+
+    assert call(bt=None) == EINVAL
+    assert call(ps=48) == EINVAL and call(ps=8) == EINVAL
+    assert call(nump=0) == EINVAL and call(maxp=0) == EINVAL
+    assert call(maxp=1 << 20, ps=2048) == EINVAL
+    assert call(bt=0x70000002) == EINVAL
+    assert call(kvf=KV_I8) == EINVAL  # int8 without its scale pool
+    assert call(ws=WS, wsb=8) == EWS
+
+
 def test_verify_validation(lib):
     f = lib.gqa_decode_verify
     assert f(Q, F16, KV, KV_F16, None, LENS, OUT, 2, 64, 0, 1.0, 1.0, 1.0, 1, WS, 256, None) == EINVAL

@@ -748,6 +748,71 @@ def test_append_out_of_range_slot_is_skipped_and_flagged():
     assert torch.equal(kv.view(torch.int16), before.view(torch.int16))
 
 
+def _append_fmt_inputs(fmt, B, C, seed):
+    dtype = "bf16" if fmt in ("bf16", "e4m3", "i8") else "f16"
+    qp, kp, vp, wq, wk, pos, _ = _append_inputs(B, C, dtype, seed=seed)
+    return dtype, qp, kp, vp, wq, wk, pos
+
+
+@pytest.mark.parametrize("fmt", ["f16", "bf16", "e4m3", "i8"])
+@pytest.mark.parametrize("page_size", [16, 64])
+def test_append_paged_equals_contiguous(fmt, page_size):
+    # the same token appended into a paged cache and into the contiguous cache
+    # it was paged from: the pool gathered back equals the contiguous cache bit
+    # for bit, and the decodes that follow agree bit for bit
+    B, C = 4, 1024
+    lens = [page_size * k + 5 for k in (1, 3, 7, 11)]  # the next slot stays in a used page
+    w = inputs.custom(B, C, 1, kv_dtype=fmt, q_dtype="bf16" if fmt in ("e4m3", "i8") else fmt,
+                      kv_std=2.0 if fmt == "e4m3" else 1.0)
+    t = _make(w, lens=lens)
+    pt = inputs.paginate(t, page_size, extra_pages=3, seed=page_size)
+    _, qp, kp, vp, wq, wk, pos = _append_fmt_inputs(fmt, B, C, seed=13)
+    slots = t["lens"].clone()
+    ks = t["k_scale"] if fmt == "e4m3" else 1.0
+    vs = t["v_scale"] if fmt == "e4m3" else 1.0
+    q1 = gq.append_kv(qp, kp, vp, wq, wk, pos, slots, t["kv"], k_scale=ks, v_scale=vs,
+                      kv_scales=t["kv_scales"])
+    q2 = gq.append_kv_paged(qp, kp, vp, wq, wk, pos, slots, pt["kv_pages"], pt["block_table"], k_scale=ks,
+                            v_scale=vs, kv_scales=pt.get("kv_scale_pages"))
+    torch.cuda.synchronize()
+    assert torch.equal(q1.view(torch.int16), q2.view(torch.int16))
+    lens1 = (slots + 1).cpu().numpy()
+    g = oracle.gather_pages(bits_of(pt["kv_pages"]), pt["block_table"].cpu().numpy(), lens1)
+    kvb = bits_of(t["kv"])
+    for b in range(B):
+        assert np.array_equal(g[b, :, :, :lens1[b]], kvb[b, :, :, :lens1[b]])
+    if fmt == "i8":
+        gs = oracle.gather_pages(bits_of(pt["kv_scale_pages"]), pt["block_table"].cpu().numpy(), lens1)
+        sb = bits_of(t["kv_scales"])
+        for b in range(B):
+            assert np.array_equal(gs[b, :, :, :lens1[b]], sb[b, :, :, :lens1[b]])
+    t["lens"].copy_(slots + 1)
+    t["q"] = q1
+    pt["q"] = q2
+    out_c = _run(t, num_splits=4).out
+    out_p = _paged(pt, num_splits=4)
+    torch.cuda.synchronize()
+    assert torch.equal(out_c.view(torch.int16), out_p.view(torch.int16))
+
+
+def test_append_paged_out_of_range_entry_is_not_written():
+    B, C, ps = 2, 512, 64
+    t = _make(inputs.custom(B, C, 100, 100))
+    pt = inputs.paginate(t, ps, extra_pages=1)
+    _, qp, kp, vp, wq, wk, pos = _append_fmt_inputs("f16", B, C, seed=14)
+    slots = torch.tensor([100, 101], dtype=torch.int32, device=DEV)
+    pt["block_table"][0, 100 // ps] = pt["num_pages"] + 3  # row 0's page for its slot is out of range
+    before = pt["kv_pages"].clone()
+    hdr = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    q_out = gq.append_kv_paged(qp, kp, vp, wq, wk, pos, slots, pt["kv_pages"], pt["block_table"], workspace=hdr)
+    torch.cuda.synchronize()
+    assert gq.get_status(hdr) & api.FLAG_PAGE_CLAMPED
+    page1 = int(pt["block_table"][1, 101 // ps])
+    changed = (pt["kv_pages"].view(torch.int16) != before.view(torch.int16)).flatten(1).any(1)  # per page, bits
+    assert changed.nonzero().flatten().tolist() == [page1]  # only row 1's page was written
+    assert torch.isfinite(q_out.float()).all()
+
+
 def test_append_then_decode_matches_the_oracle_chain():
     # GPU: append the new token, then decode over len = slot + 1.  Oracle: the
     # same two steps computed from the same inputs, rounding the appended rows
