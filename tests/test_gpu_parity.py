@@ -131,6 +131,47 @@ def test_full_size_workload_sampled(index):
     assert np.isfinite(got).all()
 
 
+def _oracle_units_window(t, units):
+    """Oracle rows of sampled (b, g) units for every query token of a window."""
+    w = t["workload"]
+    T, C = w.q_len, w.capacity
+    lens = t["lens"].cpu().numpy()
+    res = {}
+    for b, g in units:
+        kvb = np.zeros((1, 2, 8, C, 128), dtype=np.uint8 if w.kv_dtype in ("e4m3", "i8") else np.uint16)
+        kvb[0, :, g] = bits_of(t["kv"][b, :, g])
+        rows = [jt * HQ + 4 * g + j for jt in range(T) for j in range(4)]
+        out, _ = oracle.gqa_decode(bits_of(t["q"][b:b + 1]), FMT[w.q_dtype], kvb, FMT[w.kv_dtype], lens[b:b + 1],
+                                   q_scale=t["q_scale"], k_scale=t["k_scale"], v_scale=t["v_scale"], rows=rows)
+        for k, r in enumerate(rows):
+            res[b * T * HQ + r] = out[k]
+    return res
+
+
+def test_full_size_verify_window_sampled():
+    # workload 4 with a 2-token window, in the launch configuration the benchmark times
+    w = inputs.with_(inputs.WORKLOADS[4], q_len=2)
+    t = _make(w)
+    out = _verify(t)
+    ref = _oracle_units_window(t, [(0, 0), (3, 5), (7, 7)])
+    rows = sorted(ref)
+    _assert_parity(_gpu_rows(out)[rows], np.stack([ref[r] for r in rows]), "workload 4, window 2, sampled")
+
+
+def test_full_size_paged_int8_sampled():
+    # the int8 cache of workload 5's shape in shuffled 256-token pages, as benchmarked
+    w = inputs.custom(64, 32768, 16384, 32768, kv_dtype="i8", index=5)
+    t = _make(w)
+    units = [(0, 0), (17, 3), (63, 7)]
+    ref = _oracle_units(t, units)
+    pt = inputs.paginate(t, 256, extra_pages=8)
+    del t["kv"]
+    out = _paged(pt)
+    torch.cuda.synchronize()
+    rows = sorted(ref)
+    _assert_parity(_gpu_rows(out)[rows], np.stack([ref[r] for r in rows]), "paged int8 full size, sampled")
+
+
 # ---------------------------------------------------------------- edge cases
 
 
