@@ -272,6 +272,15 @@ def test_large_batch_small_capacity():
     _assert_parity(_gpu_rows(p.out), _oracle_full(t), "B=4096 C=64")
 
 
+def test_max_batch():
+    # 65535 rows, the largest batch the ABI takes (the one-piece grid's y limit)
+    B = 65535
+    rng = np.random.default_rng(65535)
+    t = _make(inputs.custom(B, 16, 1, 16), lens=rng.integers(1, 17, B).tolist())
+    p = _run(t)
+    _assert_parity(_gpu_rows(p.out), _oracle_full(t), "B=65535 C=16")
+
+
 def test_max_capacity_sampled():
     w = inputs.custom(1, 1 << 20, 1 << 20, kv_dtype="bf16")
     t = _make(w)
