@@ -18,8 +18,10 @@
  *
  * Layouts (all dense, row-major, contiguous; element offsets):
  *   q    [batch, 32, 128]              fp16 or bf16 (gqa_dtype_t)
- *   kv   [batch, 2, 8, capacity, 128]  plane 0 = K, plane 1 = V;
- *                                      same dtype as q, or e4m3 bytes (fp8 entry)
+ *   kv   [batch, 2, 8, capacity, 128]  plane 0 = K, plane 1 = V; same dtype
+ *                                      as q, e4m3 bytes (fp8 entry) or int8
+ *                                      codes with bf16 row scales (int8 entry);
+ *                                      a paged pool on the paged entries
  *   lens int32 [batch], device memory, read only by the kernels; the contract
  *        is 1 <= lens[b] <= capacity (see "Lengths" below)
  *   out  [batch, 32, 128]              same dtype as q (bf16 on the fp8 entry)
@@ -50,10 +52,14 @@
  * gqa_decode_workspace_size(batch, capacity, num_splits) bytes.  It holds a
  * 256-byte header (status flags) and FP32 partial results (unnormalised
  * output, running max in the log2 domain, softmax denominator) per
- * (b, query head, split).  Zero the header once before first use
- * (gqa_decode_workspace_init).  Launches that may run concurrently (different
- * streams or graphs) need distinct workspaces; launches ordered on one stream
- * may share one.
+ * (b, query head, split slot).  How a row is cut is decided per call from the
+ * sizes: into num_splits chunks of capacity (one CTA each), or, for grids of
+ * more than one wave, into pieces of equal runs of all rows' tiles taken by
+ * the resident CTAs (lengths read on the device); either way a row has at
+ * most num_splits pieces, and the results are deterministic.  Zero the header
+ * once before first use (gqa_decode_workspace_init).  Launches that may run
+ * concurrently (different streams or graphs) need distinct workspaces;
+ * launches ordered on one stream may share one.
  */
 #ifndef GQA_DECODE_H_
 #define GQA_DECODE_H_
@@ -103,9 +109,11 @@ size_t gqa_decode_workspace_size(int batch, int capacity, int num_splits);
 
 /* Host-only split planner (no CUDA call besides a cached SM-count query; safe
  * during stream capture once the device has been seen).  Picks the number of
- * KV splits from batch x capacity, the KV format and the SM count of `device`,
- * so that the (batch, KV head, split) work items fill the GPU several times
- * over.  Writes the chosen count (1..GQA_MAX_SPLITS) to *num_splits_out. */
+ * KV splits from batch x capacity, the KV format and the SM count of `device`:
+ * about 8 waves of (batch, KV head, split) work items over the worst case, or,
+ * for latency-bound sizes (at most 16 tiles per resident CTA in all), about
+ * sqrt(6 x tiles per row) capped at one wave.  Writes the chosen count
+ * (1..GQA_MAX_SPLITS) to *num_splits_out. */
 gqa_status_t gqa_decode_plan(int batch, int capacity, gqa_kv_format_t kv_format, int device,
                              int* num_splits_out);
 
@@ -115,10 +123,11 @@ gqa_status_t gqa_decode_plan_for(int batch, int capacity, gqa_kv_format_t kv_for
                                  int* num_splits_out);
 
 /* Split geometry (pure host arithmetic): tokens per split, rounded up to
- * whole 64-token (fp16/bf16) or 128-token (e4m3) tiles, and the number of
- * splits that hold slots, ceil(capacity / chunk) <= num_splits.  Split s covers
- * slots [s * chunk, min((s + 1) * chunk, len)); stage 2 runs only when the
- * effective count is above 1. */
+ * whole 64-token (fp16/bf16) or 128-token (8-bit) tiles, and the number of
+ * splits that hold slots, ceil(capacity / chunk) <= num_splits.  With one
+ * piece per CTA, split s covers slots [s * chunk, min((s + 1) * chunk, len));
+ * the balanced schedule cuts rows elsewhere but never into more pieces.
+ * Stage 2 runs only when the effective count is above 1. */
 gqa_status_t gqa_decode_split_geometry(int capacity, int num_splits, gqa_kv_format_t kv_format,
                                        int* chunk_tokens_out, int* splits_effective_out);
 
