@@ -95,14 +95,15 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
   int n;      // splits or pieces to merge
   bool zero = false;  // a row without tokens
   if (p.bal_ctas > 0) {
-    // The tile counts stage 1 used (integers, so both kernels agree exactly),
-    // read while stage 1 still runs.
+    // The stream positions stage 1 used (integers, so both kernels agree
+    // exactly), read while stage 1 still runs.
     __shared__ int red[2][kCombineThreads / 32];
     int before = 0, all = 0;
     for (int bb = threadIdx.x; bb < p.batch; bb += kCombineThreads) {
       const int nb = (min(max(__ldg(p.lens + bb), 0), p.capacity) + p.tile - 1) / p.tile;
-      all += nb;
-      if (bb < b) before += nb;
+      const int wb = nb > 0 ? nb + 1 : 0;  // stream positions of the row (a piece cost + its tiles)
+      all += wb;
+      if (bb < b) before += wb;
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
@@ -123,7 +124,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
     const int nb = (min(max(__ldg(p.lens + b), 0), p.capacity) + p.tile - 1) / p.tile;
     const int total = kHkv * all;
     const int q = max((total + p.bal_ctas - 1) / p.bal_ctas, p.bal_q_min);
-    const int tf = kHkv * before + g * nb;
+    const int tf = kHkv * before + g * (nb + 1) + 1;  // the row's first tile in the stream
     n = nb > 0 ? (tf + nb - 1) / q - tf / q + 1 : 0;
     zero = nb == 0;  // no tokens: a zero row (stage 1 holds no piece of it)
   } else {

@@ -227,15 +227,25 @@ struct PieceCursor<kTile, false> {
   }
 };
 
-// Balanced schedule: the CTA's tiles [x, x1) of the global stream (rows
-// r = 8b + g in order, ceil(L_b / tile) tiles each), cut at row ends.  Row r
-// starts at global tile tf = 8 pb + g nb (pb: tiles per KV head of the rows
-// before b); CTA c holds its piece number c - floor(tf / q), and the row has
-// floor((tf + nb - 1) / q) - floor(tf / q) + 1 pieces.
+// Balanced schedule: the CTA's positions [x, x1) of the global stream.  Rows
+// r = 8b + g come in order; a row of n tiles occupies w = n + 1 positions, one
+// for the fixed cost of a piece (reloading q, the epilogue: about one tile's
+// streaming time) and one per tile, so a CTA whose run crosses many row starts
+// takes fewer tiles.  Row r's first tile sits at stream position
+// tf = 8 pb + g w + 1 (pb: positions per KV head of the rows before b); CTA c
+// holds its piece number c - floor(tf / q), and the row has
+// floor((tf + n - 1) / q) - floor(tf / q) + 1 pieces.
+__host__ __device__ inline int bal_row_positions(int n_tiles) { return n_tiles > 0 ? n_tiles + 1 : 0; }
+
 template <int kTile>
 struct PieceCursor<kTile, true> {
   const int32_t* lens;
-  int batch, capacity, b, g, j, nb, L, L_next, pb, x, x1, q;
+  int batch, capacity, b, g, j, nb, wb, L, L_next, pb, x, x1, q;
+  __device__ void set_row(int len) {
+    L = len;
+    nb = (L + kTile - 1) / kTile;
+    wb = bal_row_positions(nb);
+  }
   // L0, L1: clamped lengths of rows b0 and b0 + 1 (0 past the batch)
   __device__ void start(const int32_t* lens_, int B, int C, int b0, int pb0, int L0, int L1, int x0, int x1_,
                         int q_) {
@@ -247,36 +257,40 @@ struct PieceCursor<kTile, true> {
     x = x0;
     x1 = x1_;
     q = q_;
-    L = L0;
+    set_row(L0);
     L_next = L1;
-    nb = (L + kTile - 1) / kTile;
     const int within = x0 - kHkv * pb;
-    g = within / nb;
-    j = within - g * nb;
+    g = within / wb;
+    j = within - g * wb;  // position in the row; 0 is the piece-cost position
   }
   __device__ bool next(Piece& pc, int cta) {
-    if (x >= x1) return false;
-    const int cnt = min(nb - j, x1 - x);
-    const int tf = kHkv * pb + g * nb;
-    const int fq = tf / q;
-    pc = Piece{b, g, L, j * kTile, min(L, (j + cnt) * kTile), cta - fq, (tf + nb - 1) / q == fq};
-    x += cnt;
-    j += cnt;
-    if (j == nb) {
-      j = 0;
-      if (++g == kHkv) {
-        g = 0;
-        pb += nb;
-        while (x < x1) {  // the next row that holds tokens; its successor's
-          ++b;              // length is loaded a whole piece ahead of its use
-          L = L_next;
-          L_next = b + 1 < batch ? min(max(__ldg(lens + b + 1), 0), capacity) : 0;
-          nb = (L + kTile - 1) / kTile;
-          if (nb > 0) break;
+    while (x < x1) {
+      const int cnt = min(wb - j, x1 - x);
+      const int r0 = max(j, 1), r1 = j + cnt;  // tile positions [r0, r1) of this run
+      const bool has_tiles = r1 > r0;
+      if (has_tiles) {
+        const int tf = kHkv * pb + g * wb + 1;
+        const int fq = tf / q;
+        pc = Piece{b, g, L, (r0 - 1) * kTile, min(L, (r1 - 1) * kTile), cta - fq, (tf + nb - 1) / q == fq};
+      }
+      x += cnt;
+      j += cnt;
+      if (j == wb) {
+        j = 0;
+        if (++g == kHkv) {
+          g = 0;
+          pb += wb;
+          while (x < x1) {  // the next row that holds tokens; its successor's
+            ++b;              // length is loaded a whole piece ahead of its use
+            set_row(L_next);
+            L_next = b + 1 < batch ? min(max(__ldg(lens + b + 1), 0), capacity) : 0;
+            if (wb > 0) break;
+          }
         }
       }
+      if (has_tiles) return true;
     }
-    return true;
+    return false;
   }
 };
 
@@ -322,10 +336,11 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
   // ---- this CTA's pieces
   PieceCursor<T::kTile, BAL> cur;
   if constexpr (BAL) {
-    // Balanced schedule: the tiles of every (b, KV head) row, rows in order,
-    // form one stream of 8 * sum_b ceil(len_b / tile) tiles; CTA c takes
-    // tiles [c * Q, (c + 1) * Q) with Q = max(ceil(total / grid), q_min).
-    // Prefix sums of tiles per row over the batch, by all threads, each over
+    // Balanced schedule: the positions of every (b, KV head) row, rows in
+    // order, form one stream of 8 * sum_b w_b positions (w = tiles + 1 for a
+    // row that holds tokens); CTA c takes positions [c * Q, (c + 1) * Q) with
+    // Q = max(ceil(total / grid), q_min).
+    // Prefix sums of positions per row over the batch, by all threads, each over
     // a contiguous block of rows.  Scratch: the merge area, idle until the
     // first epilogue — warp sums at [0, 5), the first row and its prefix at
     // [161, 163), the clamped lengths from 163 on.
@@ -340,7 +355,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
       const int lr = __ldg(p.lens + bb);
       clamped |= lr < 1 || lr > C;
       lsh[bb] = min(max(lr, 0), C);
-      mine += (lsh[bb] + T::kTile - 1) / T::kTile;
+      mine += bal_row_positions((lsh[bb] + T::kTile - 1) / T::kTile);
     }
     if (clamped && blockIdx.x == 0) atomicOr(p.flags, GQA_FLAG_LENGTH_CLAMPED);
     // exclusive prefix of the per-thread sums: a scan within each warp, then
@@ -363,16 +378,16 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
     const int total = kHkv * per_head;
     const int q = max((total + (int)gridDim.x - 1) / (int)gridDim.x, p.bal_q_min);
     const int x0 = (int)blockIdx.x * q;
-    // the thread whose rows hold tile x0 records the first row and its prefix
+    // the thread whose rows hold position x0 records the first row and its prefix
     if (x0 < total && kHkv * pre <= x0 && x0 < kHkv * (pre + mine)) {
       for (int bb = rb0; bb < rb1; ++bb) {
-        const int nb = (lsh[bb] + T::kTile - 1) / T::kTile;
-        if (x0 < kHkv * (pre + nb)) {
+        const int wb = bal_row_positions((lsh[bb] + T::kTile - 1) / T::kTile);
+        if (x0 < kHkv * (pre + wb)) {
           scan[kMmaThreads + 1] = bb;
           scan[kMmaThreads + 2] = pre;
           break;
         }
-        pre += nb;
+        pre += wb;
       }
     }
     __syncthreads();
