@@ -364,8 +364,8 @@ Layout layout_of(void* ws, int batch, int splits) {
 // The balanced schedule serves single-token decode of batches up to
 // kBalMaxBatch whose rows can be split (two or more tiles of capacity) and
 // whose one-piece-per-CTA grid would take more than one wave, as long as the
-// global stream (n + 1 positions for a row of n tiles: one stands for the
-// piece's fixed cost) fits an int.  q_min keeps every row within the
+// global stream (n + kBalRowCost positions for a row of n tiles, the first
+// ones standing for the piece's fixed cost) fits an int.  q_min keeps every row within the
 // workspace's split slots: a row of n <= nmax tiles meets at most
 // ceil(n / q) + 1 <= num_splits CTAs.  Measured on GB300 (us per call, back
 // to back): fp16 32 x U[1,8192] 96.4 -> 89.9, e4m3 64 x U[16k,32k] 459.4 ->
@@ -382,7 +382,7 @@ BalPlan bal_plan(const Call& c) {
   if (c.q_len != 1 || c.batch > kBalMaxBatch || c.num_splits < 2 || c.sms < 1) return bp;
   const int splits_eff = split_count(c.capacity, c.num_splits, c.kv_format);
   if (splits_eff < 2) return bp;
-  if ((long long)kHkv * c.batch * (nmax + 1) > 0x7fffffffLL) return bp;
+  if ((long long)kHkv * c.batch * (nmax + kBalRowCost) > 0x7fffffffLL) return bp;
   const long long slots = (long long)mma_ctas_per_sm(c.kv_format, 1) * c.sms;
   // one wave of pieces or less: nothing to balance, the plain grid starts sooner
   if ((long long)kHkv * c.batch * splits_eff <= slots) return bp;

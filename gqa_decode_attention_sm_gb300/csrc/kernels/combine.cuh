@@ -96,35 +96,45 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
   bool zero = false;  // a row without tokens
   if (p.bal_ctas > 0) {
     // The stream positions stage 1 used (integers, so both kernels agree
-    // exactly), read while stage 1 still runs.
-    __shared__ int red[2][kCombineThreads / 32];
-    int before = 0, all = 0;
+    // exactly), read while stage 1 still runs: tiles and rows with tokens
+    // before row b and in all, and the shortest row.
+    constexpr int kW = kCombineThreads / 32;
+    __shared__ int red[5][kW];
+    int v[5] = {0, 0, 0, 0, INT_MAX};  // tiles before b, rows before b, all tiles, all rows, min
     for (int bb = threadIdx.x; bb < p.batch; bb += kCombineThreads) {
       const int nb = (min(max(__ldg(p.lens + bb), 0), p.capacity) + p.tile - 1) / p.tile;
-      const int wb = nb > 0 ? nb + 1 : 0;  // stream positions of the row (a piece cost + its tiles)
-      all += wb;
-      if (bb < b) before += wb;
+      if (bb < b) {
+        v[0] += nb;
+        v[1] += nb > 0;
+      }
+      v[2] += nb;
+      v[3] += nb > 0;
+      if (nb > 0) v[4] = min(v[4], nb);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
-      before += __shfl_xor_sync(0xffffffffu, before, off);
-      all += __shfl_xor_sync(0xffffffffu, all, off);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) v[k] += __shfl_xor_sync(0xffffffffu, v[k], off);
+      v[4] = min(v[4], __shfl_xor_sync(0xffffffffu, v[4], off));
     }
     if ((threadIdx.x & 31) == 0) {
-      red[0][threadIdx.x >> 5] = before;
-      red[1][threadIdx.x >> 5] = all;
+#pragma unroll
+      for (int k = 0; k < 5; ++k) red[k][threadIdx.x >> 5] = v[k];
     }
     __syncthreads();
-    before = all = 0;
+    v[0] = v[1] = v[2] = v[3] = 0;
+    v[4] = INT_MAX;
 #pragma unroll
-    for (int w = 0; w < kCombineThreads / 32; ++w) {
-      before += red[0][w];
-      all += red[1][w];
+    for (int w = 0; w < kW; ++w) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) v[k] += red[k][w];
+      v[4] = min(v[4], red[4][w]);
     }
     const int nb = (min(max(__ldg(p.lens + b), 0), p.capacity) + p.tile - 1) / p.tile;
-    const int total = kHkv * all;
+    const int rc = bal_row_cost(v[2], v[4], p.bal_ctas, p.bal_q_min);
+    const int total = kHkv * (v[2] + rc * v[3]);
     const int q = max((total + p.bal_ctas - 1) / p.bal_ctas, p.bal_q_min);
-    const int tf = kHkv * before + g * (nb + 1) + 1;  // the row's first tile in the stream
+    const int tf = kHkv * (v[0] + rc * v[1]) + g * bal_row_positions(nb, rc) + rc;  // the row's first tile
     n = nb > 0 ? (tf + nb - 1) / q - tf / q + 1 : 0;
     zero = nb == 0;  // no tokens: a zero row (stage 1 holds no piece of it)
   } else {

@@ -29,6 +29,25 @@ __host__ __device__ constexpr int tile_tokens(int kv_format) {
   return is_8bit(kv_format) ? 128 : 64;
 }
 
+// Balanced schedule of the split kernel: the stream positions a row of n tiles
+// occupies, rc for the fixed cost of a piece (loading q, the epilogue: about
+// one tile's streaming time) and then one per tile; none for a row without
+// tokens.  The split and combine kernels both count with these functions.
+constexpr int kBalRowCost = 1;
+__host__ __device__ constexpr int bal_row_positions(int n_tiles, int rc) {
+  return n_tiles > 0 ? n_tiles + rc : 0;
+}
+// The row cost in use: kBalRowCost when some row holding tokens is shorter
+// than a CTA's run without it (CTAs then differ in how many pieces they hold),
+// else 0 (every CTA holds one or two pieces; counting the cost would only move
+// the cuts off the run length's multiples, which measured slower on GB300 for
+// bf16 8 x 131072).  sum_tiles: tiles over all rows of one KV head; min_tiles:
+// the fewest tiles of a row that holds tokens.
+__host__ __device__ inline int bal_row_cost(int sum_tiles, int min_tiles, int ctas, int q_min) {
+  const int q0 = (kHkv * sum_tiles + ctas - 1) / ctas;
+  return min_tiles < (q0 > q_min ? q0 : q_min) ? kBalRowCost : 0;
+}
+
 template <int KVF>
 struct KvTraits {
   static constexpr int kElemBytes = is_8bit(KVF) ? 1 : 2;
@@ -164,14 +183,21 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t two) {
   return h2;
 }
 
-// Two int8 codes (low byte = first element) -> exact f16x2.  With b = code +
-// 128 (flip the sign bit), the f16 pattern 0x6400 | b is 1024 + b; subtracting
-// 1152 leaves the code.  Four codes of a word give two pairs.
-__device__ __forceinline__ void i8x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+// Two int8 codes (low byte = first element) -> exact f16x2 of code + 1152.
+// With b = code + 128 (flip the sign bit), the f16 pattern 0x6400 | b is
+// 1024 + b, an integer in [1024, 1279], exact in f16.  Four codes of a word
+// give two pairs.  A dot product with these exceeds the codes' by
+// kI8Bias times the sum of the other operand.
+constexpr float kI8Bias = 1152.f;
+__device__ __forceinline__ void i8x4_to_f16x2x2_biased(uint32_t w, uint32_t& lo, uint32_t& hi) {
   const uint32_t x = w ^ 0x80808080u;
+  asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(lo) : "r"(x), "r"(0x64646464u));
+  asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(hi) : "r"(x), "r"(0x64646464u));
+}
+// The codes themselves: subtracting 1152 is exact.
+__device__ __forceinline__ void i8x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
   uint32_t a, b;
-  asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(a) : "r"(x), "r"(0x64646464u));
-  asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(b) : "r"(x), "r"(0x64646464u));
+  i8x4_to_f16x2x2_biased(w, a, b);
   const uint32_t bias = 0x64806480u;  // (1152, 1152)
   asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(bias));
   asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(bias));

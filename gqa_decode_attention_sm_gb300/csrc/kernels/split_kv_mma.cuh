@@ -176,6 +176,15 @@ __device__ __forceinline__ void widen4(uint32_t w, uint32_t& lo, uint32_t& hi) {
   }
 }
 
+// K operand: int8 codes enter the scores as code + 1152 (one f16 subtraction
+// per pair saved); the consumer takes 1152 * sum_d q_d off each score column
+// in the scale step.  e4m3 as widen4.
+template <int KVF>
+__device__ __forceinline__ void widen4_k(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  if constexpr (KVF == kKvI8) i8x4_to_f16x2x2_biased(w, lo, hi);
+  else widen4<KVF>(w, lo, hi);
+}
+
 // Tensor-core element type: bf16 for bf16 KV, f16 otherwise (8-bit KV widens to f16).
 template <int KVF>
 constexpr bool kMmaBF16 = KVF == kKvBF16;
@@ -219,7 +228,7 @@ struct PieceCursor<kTile, false> {
     one = Piece{b, g, L, t_begin, t_end, slot, direct};
     pending = true;
   }
-  __device__ bool next(Piece& pc, int) {
+  __device__ bool next(Piece& pc, const SplitParams&) {
     if (!pending) return false;
     pc = one;
     pending = false;
@@ -228,50 +237,48 @@ struct PieceCursor<kTile, false> {
 };
 
 // Balanced schedule: the CTA's positions [x, x1) of the global stream.  Rows
-// r = 8b + g come in order; a row of n tiles occupies w = n + 1 positions, one
-// for the fixed cost of a piece (reloading q, the epilogue: about one tile's
-// streaming time) and one per tile, so a CTA whose run crosses many row starts
-// takes fewer tiles.  Row r's first tile sits at stream position
-// tf = 8 pb + g w + 1 (pb: positions per KV head of the rows before b); CTA c
-// holds its piece number c - floor(tf / q), and the row has
-// floor((tf + n - 1) / q) - floor(tf / q) + 1 pieces.
-__host__ __device__ inline int bal_row_positions(int n_tiles) { return n_tiles > 0 ? n_tiles + 1 : 0; }
+// r = 8b + g come in order; a row of n tiles occupies w = n + rc positions
+// (none without tokens), the first rc (the row cost) for the fixed cost of a
+// piece, so a CTA whose run crosses many row starts takes fewer tiles.  Row
+// r's first tile sits at stream position tf = 8 pb + g w + rc (pb: positions
+// per KV head of the rows before b); CTA c holds its piece number
+// c - floor(tf / q), and the row has floor((tf + n - 1) / q) - floor(tf / q) + 1
+// pieces.
 
 template <int kTile>
 struct PieceCursor<kTile, true> {
-  const int32_t* lens;
-  int batch, capacity, b, g, j, nb, wb, L, L_next, pb, x, x1, q;
-  __device__ void set_row(int len) {
+  // The cursor rests on rows that hold tokens, so the row cost is wb - nb.
+  // The lengths, batch and capacity are read from the kernel parameters.
+  int b, g, j, nb, wb, L, L_next, pb, x, x1, q;
+  __device__ void set_row(int len, int rc) {
     L = len;
     nb = (L + kTile - 1) / kTile;
-    wb = bal_row_positions(nb);
+    wb = bal_row_positions(nb, rc);
   }
   // L0, L1: clamped lengths of rows b0 and b0 + 1 (0 past the batch)
-  __device__ void start(const int32_t* lens_, int B, int C, int b0, int pb0, int L0, int L1, int x0, int x1_,
-                        int q_) {
-    lens = lens_;
-    batch = B;
-    capacity = C;
+  __device__ void start(int b0, int pb0, int L0, int L1, int x0, int x1_, int q_, int rc) {
     b = b0;
     pb = pb0;
     x = x0;
     x1 = x1_;
     q = q_;
-    set_row(L0);
+    set_row(L0, rc);
     L_next = L1;
     const int within = x0 - kHkv * pb;
     g = within / wb;
-    j = within - g * wb;  // position in the row; 0 is the piece-cost position
+    j = within - g * wb;  // position in the row; [0, rc) stand for the piece cost
   }
-  __device__ bool next(Piece& pc, int cta) {
+  __device__ bool next(Piece& pc, const SplitParams& p) {
+    const int cta = blockIdx.x;
     while (x < x1) {
+      const int rc = wb - nb;
       const int cnt = min(wb - j, x1 - x);
-      const int r0 = max(j, 1), r1 = j + cnt;  // tile positions [r0, r1) of this run
+      const int r0 = max(j, rc), r1 = j + cnt;  // tile positions [r0, r1) of this run
       const bool has_tiles = r1 > r0;
       if (has_tiles) {
-        const int tf = kHkv * pb + g * wb + 1;
+        const int tf = kHkv * pb + g * wb + rc;
         const int fq = tf / q;
-        pc = Piece{b, g, L, (r0 - 1) * kTile, min(L, (r1 - 1) * kTile), cta - fq, (tf + nb - 1) / q == fq};
+        pc = Piece{b, g, L, (r0 - rc) * kTile, min(L, (r1 - rc) * kTile), cta - fq, (tf + nb - 1) / q == fq};
       }
       x += cnt;
       j += cnt;
@@ -282,8 +289,8 @@ struct PieceCursor<kTile, true> {
           pb += wb;
           while (x < x1) {  // the next row that holds tokens; its successor's
             ++b;              // length is loaded a whole piece ahead of its use
-            set_row(L_next);
-            L_next = b + 1 < batch ? min(max(__ldg(lens + b + 1), 0), capacity) : 0;
+            set_row(L_next, rc);
+            L_next = b + 1 < p.batch ? min(max(__ldg(p.lens + b + 1), 0), p.capacity) : 0;
             if (wb > 0) break;
           }
         }
@@ -337,51 +344,72 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
   PieceCursor<T::kTile, BAL> cur;
   if constexpr (BAL) {
     // Balanced schedule: the positions of every (b, KV head) row, rows in
-    // order, form one stream of 8 * sum_b w_b positions (w = tiles + 1 for a
+    // order, form one stream of 8 * sum_b w_b positions (w = tiles + rc for a
     // row that holds tokens); CTA c takes positions [c * Q, (c + 1) * Q) with
     // Q = max(ceil(total / grid), q_min).
-    // Prefix sums of positions per row over the batch, by all threads, each over
-    // a contiguous block of rows.  Scratch: the merge area, idle until the
-    // first epilogue — warp sums at [0, 5), the first row and its prefix at
-    // [161, 163), the clamped lengths from 163 on.
+    // Prefix sums of tiles and of rows with tokens over the batch, by all
+    // threads, each over a contiguous block of rows, and the shortest row.
+    // Scratch: the merge area, idle until the first epilogue — warp sums at
+    // [0, 15), the first row and its prefix at [161, 163), the clamped lengths
+    // from 163 on.
     int* scan = reinterpret_cast<int*>(mrg_acc);
     int* lsh = scan + kMmaThreads + 3;
     const int B = p.batch;
     const int per_t = (B + kMmaThreads - 1) / kMmaThreads;
     const int rb0 = min(B, (int)threadIdx.x * per_t), rb1 = min(B, rb0 + per_t);
-    int mine = 0;
+    int mine_n = 0, mine_r = 0, mn = INT_MAX;
     bool clamped = false;
     for (int bb = rb0; bb < rb1; ++bb) {
       const int lr = __ldg(p.lens + bb);
       clamped |= lr < 1 || lr > C;
       lsh[bb] = min(max(lr, 0), C);
-      mine += bal_row_positions((lsh[bb] + T::kTile - 1) / T::kTile);
+      const int nb = (lsh[bb] + T::kTile - 1) / T::kTile;
+      mine_n += nb;
+      mine_r += nb > 0;
+      if (nb > 0) mn = min(mn, nb);
     }
     if (clamped && blockIdx.x == 0) atomicOr(p.flags, GQA_FLAG_LENGTH_CLAMPED);
-    // exclusive prefix of the per-thread sums: a scan within each warp, then
+    // exclusive prefixes of the per-thread sums: scans within each warp, then
     // the sums of the warps before
-    int incl = mine;
+    int incl_n = mine_n, incl_r = mine_r;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += t;
+      const int tn = __shfl_up_sync(0xffffffffu, incl_n, off);
+      const int tr = __shfl_up_sync(0xffffffffu, incl_r, off);
+      if (lane >= off) {
+        incl_n += tn;
+        incl_r += tr;
+      }
     }
-    if (lane == 31) scan[warp] = incl;
-    __syncthreads();
-    int pre = incl - mine, per_head = 0;
 #pragma unroll
-    for (int w = 0; w < kMmaThreads / 32; ++w) {
-      const int ws = scan[w];
-      if (w < warp) pre += ws;
-      per_head += ws;
+    for (int off = 16; off > 0; off >>= 1) mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+    constexpr int kW = kMmaThreads / 32;
+    if (lane == 31) {
+      scan[warp] = incl_n;
+      scan[kW + warp] = incl_r;
+      scan[2 * kW + warp] = mn;
     }
-    const int total = kHkv * per_head;
+    __syncthreads();
+    int pre_n = incl_n - mine_n, pre_r = incl_r - mine_r, sum_n = 0, sum_r = 0, min_n = INT_MAX;
+#pragma unroll
+    for (int w = 0; w < kW; ++w) {
+      if (w < warp) {
+        pre_n += scan[w];
+        pre_r += scan[kW + w];
+      }
+      sum_n += scan[w];
+      sum_r += scan[kW + w];
+      min_n = min(min_n, scan[2 * kW + w]);
+    }
+    const int rc = bal_row_cost(sum_n, min_n, (int)gridDim.x, p.bal_q_min);
+    const int total = kHkv * (sum_n + rc * sum_r);
     const int q = max((total + (int)gridDim.x - 1) / (int)gridDim.x, p.bal_q_min);
     const int x0 = (int)blockIdx.x * q;
+    int pre = pre_n + rc * pre_r;
     // the thread whose rows hold position x0 records the first row and its prefix
-    if (x0 < total && kHkv * pre <= x0 && x0 < kHkv * (pre + mine)) {
+    if (x0 < total && kHkv * pre <= x0 && x0 < kHkv * (pre + mine_n + rc * mine_r)) {
       for (int bb = rb0; bb < rb1; ++bb) {
-        const int wb = bal_row_positions((lsh[bb] + T::kTile - 1) / T::kTile);
+        const int wb = bal_row_positions((lsh[bb] + T::kTile - 1) / T::kTile, rc);
         if (x0 < kHkv * (pre + wb)) {
           scan[kMmaThreads + 1] = bb;
           scan[kMmaThreads + 2] = pre;
@@ -393,8 +421,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
     __syncthreads();
     if (x0 >= total) return;  // more CTAs than work
     const int b0 = scan[kMmaThreads + 1];
-    cur.start(p.lens, B, C, b0, scan[kMmaThreads + 2], lsh[b0], b0 + 1 < B ? lsh[b0 + 1] : 0, x0,
-              min(x0 + q, total), q);
+    cur.start(b0, scan[kMmaThreads + 2], lsh[b0], b0 + 1 < B ? lsh[b0 + 1] : 0, x0, min(x0 + q, total), q, rc);
   } else {
     // one piece per CTA: split s of row (b, g)
     const int g = blockIdx.x, b = blockIdx.y, s = blockIdx.z;
@@ -441,7 +468,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
     bool ok = true;
     int it = 0;
     Piece pc;
-    while (ok && cur.next(pc, blockIdx.x)) {
+    while (ok && cur.next(pc, p)) {
       const int b = pc.b, g = pc.g, t_begin = pc.t_begin, t_end = pc.t_end;
       const int n_tiles = (t_end - t_begin + T::kTile - 1) / T::kTile;
       int bt_first = -1, bt_val = 0;  // paged: entry bt_first + lane of this row's block table
@@ -554,7 +581,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
   bool alive = true;  // false once a wait has run out: the remaining tiles are skipped
   int it = 0;         // this CTA's tiles over all its pieces (ring stage and phase)
   Piece pc;
-  while (cur.next(pc, blockIdx.x)) {
+  while (cur.next(pc, p)) {
     const int b = pc.b, g = pc.g, L = pc.L, t_begin = pc.t_begin, t_end = pc.t_end;
     const int n_tiles = (t_end - t_begin + T::kTile - 1) / T::kTile;
     // Column n of n-tile nt is (query token 2nt + n/4, head n%4).  This lane's
@@ -584,6 +611,28 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
           if constexpr (is_8bit(KVF) && QF == kQBF16) v = pack_f16_satfinite(bf16_lo_to_f32(w), bf16_hi_to_f32(w));
           qb[nt][ks][pr] = real ? v : 0u;
         }
+    }
+    // int8 K: score offset of each of this lane's columns (2cq, 2cq+1),
+    // -1152 * sum_d q_d * scale_log2, added in the scale step (the K operand
+    // is code + 1152, see widen4_k).
+    float kb[kNT][2];
+  #pragma unroll
+    for (int nt = 0; nt < kNT; ++nt) {
+      kb[nt][0] = kb[nt][1] = 0.f;
+      if constexpr (KVF == kKvI8) {
+        float qs = 0.f;  // this lane's part of column gq's sum
+  #pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+  #pragma unroll
+          for (int pr = 0; pr < 2; ++pr) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&qb[nt][ks][pr]));
+            qs += f.x + f.y;
+          }
+        qs += __shfl_xor_sync(0xffffffffu, qs, 1);  // lanes 4n..4n+3 hold column n
+        qs += __shfl_xor_sync(0xffffffffu, qs, 2);
+        kb[nt][0] = -kI8Bias * sl2 * __shfl_sync(0xffffffffu, qs, 8 * cq);
+        kb[nt][1] = -kI8Bias * sl2 * __shfl_sync(0xffffffffu, qs, 8 * cq + 4);
+      }
     }
 
     float o[kNT][8][4];
@@ -646,8 +695,8 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
               for (int s4 = 0; s4 < 4; ++s4) {
                 const int ks = 4 * ci + s4;
                 uint32_t a0, a1, a2, a3;
-                widen4<KVF>(xs[s4], a0, a2);  // row gq: dims (4s,4s+1), (4s+2,4s+3)
-                widen4<KVF>(ys[s4], a1, a3);  // row gq+8
+                widen4_k<KVF>(xs[s4], a0, a2);  // row gq: dims (4s,4s+1), (4s+2,4s+3)
+                widen4_k<KVF>(ys[s4], a1, a3);  // row gq+8
   #pragma unroll
                 for (int nt = 0; nt < kNT; ++nt) mma16816<false>(sc[nt], a0, a1, a2, a3, qb[nt][ks][0], qb[nt][ks][1]);
               }
@@ -671,7 +720,10 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
   #pragma unroll
         for (int nt = 0; nt < kNT; ++nt) {
   #pragma unroll
-          for (int e = 0; e < 4; ++e) x[nt][e] = sc[nt][e] * sl2;
+          for (int e = 0; e < 4; ++e) {
+            if constexpr (KVF == kKvI8) x[nt][e] = fmaf(sc[nt][e], sl2, kb[nt][e & 1]);
+            else x[nt][e] = sc[nt][e] * sl2;
+          }
           if constexpr (KVF == kKvI8) {  // per-row K scale multiplies that token's scores
             x[nt][0] *= sk[sl][0];
             x[nt][1] *= sk[sl][0];

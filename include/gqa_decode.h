@@ -55,12 +55,12 @@
  * (b, query head, split slot).  How a row is cut is decided per call from the
  * sizes: into num_splits chunks of capacity (one CTA each), or, for grids of
  * more than one wave, into pieces of equal runs of one stream of all rows'
- * tiles (each row start weighs one more tile) taken by the resident CTAs
- * (lengths read on the device); either way a row has at
- * most num_splits pieces, and the results are deterministic.  Zero the header
- * once before first use (gqa_decode_workspace_init).  Launches that may run
- * concurrently (different streams or graphs) need distinct workspaces;
- * launches ordered on one stream may share one.
+ * tiles (each row start weighs one more tile when some row is shorter than
+ * a run) taken by the resident CTAs (lengths read on the device); either way
+ * a row has at most num_splits pieces, and the results are deterministic.
+ * Zero the header once before first use (gqa_decode_workspace_init).
+ * Launches that may run concurrently (different streams or graphs) need
+ * distinct workspaces; launches ordered on one stream may share one.
  */
 #ifndef GQA_DECODE_H_
 #define GQA_DECODE_H_

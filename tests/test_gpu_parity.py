@@ -214,6 +214,19 @@ def test_int8_every_element(q_dtype):
         _assert_parity(_gpu_rows(p.out), _oracle_full(t), f"int8 KV, {q_dtype} q, splits={p.num_splits}")
 
 
+@pytest.mark.parametrize("q_dtype,shift,q_scale", [("bf16", 8.0, 2.0), ("f16", 3.0, 4.0)])
+def test_int8_large_q_sum_sharp_softmax(q_dtype, shift, q_scale):
+    # int8 K enters the tensor core as code + 1152 and the scores take
+    # 1152 * sum_d q_d back off: q with a large mean (a large sum) and a sharp
+    # softmax make that difference as large as it gets relative to the scores
+    w = inputs.custom(4, 4096, 1, 4096, kv_dtype="i8", q_dtype=q_dtype, index=90, q_scale=q_scale)
+    t = _make(w)
+    t["q"] = (t["q"].float() + shift).to(t["q"].dtype)
+    for S in (None, 1):
+        p = _run(t, num_splits=S)
+        _assert_parity(_gpu_rows(p.out), _oracle_full(t), f"int8, q + {shift}, q_scale {q_scale}, splits={S}")
+
+
 def test_int8_full_size_sampled():
     # the e4m3 workload's shape and length mix with an int8 cache (4.3 GB of codes)
     w = inputs.custom(64, 32768, 16384, 32768, kv_dtype="i8", index=5)
@@ -340,6 +353,17 @@ def test_balanced_one_long_row_among_short_ones():
     for S in (None, 4):
         p = _run(t, num_splits=S)
         _assert_parity(_gpu_rows(p.out), _oracle_full(t), f"one long row, splits={p.num_splits}")
+
+
+@pytest.mark.parametrize("B,L,kv_dtype", [(16, 8192, "bf16"), (256, 1000, "f16"), (96, 3000, "e4m3")])
+def test_balanced_uniform_rows(B, L, kv_dtype):
+    # equal lengths: rows at least one CTA's run long are cut without the
+    # per-row piece cost (16 x 8192), shorter ones with it (256 x 1000,
+    # 96 x 3000); both kernels take the same choice from the lengths
+    w = inputs.custom(B, L, L, kv_dtype=kv_dtype, kv_std=2.0 if kv_dtype == "e4m3" else 1.0)
+    t = _make(w)
+    p = _run(t, num_splits=8)
+    _assert_parity(_gpu_rows(p.out), _oracle_full(t), f"uniform {B} x {L} {kv_dtype}")
 
 
 @pytest.mark.parametrize("B", [1024, 1025])
