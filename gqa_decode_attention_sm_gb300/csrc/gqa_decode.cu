@@ -60,11 +60,15 @@ cudaError_t set_split_attributes() {
   const auto set = [&](auto kernel, int bytes) {
     if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   };
-  set(split_kv_mma_kernel<KVF, QF, 1, false>, mma_smem_bytes(KVF, 1));
-  set(split_kv_mma_kernel<KVF, QF, 2, false>, mma_smem_bytes(KVF, 2));
-  set(split_kv_mma_kernel<KVF, QF, 3, false>, mma_smem_bytes(KVF, 3));
-  set(split_kv_mma_kernel<KVF, QF, 4, false>, mma_smem_bytes(KVF, 4));
-  set(split_kv_mma_kernel<KVF, QF, 1, true>, mma_smem_bytes(KVF, 1) + kBalMergeBytes);
+  set(split_kv_mma_kernel<KVF, QF, 1, false, false>, mma_smem_bytes(KVF, 1));
+  set(split_kv_mma_kernel<KVF, QF, 2, false, false>, mma_smem_bytes(KVF, 2));
+  set(split_kv_mma_kernel<KVF, QF, 3, false, false>, mma_smem_bytes(KVF, 3));
+  set(split_kv_mma_kernel<KVF, QF, 4, false, false>, mma_smem_bytes(KVF, 4));
+  set(split_kv_mma_kernel<KVF, QF, 1, true, false>, mma_smem_bytes(KVF, 1) + kBalMergeBytes);
+  set(split_kv_mma_kernel<KVF, QF, 1, false, true>, mma_smem_bytes(KVF, 1));
+  set(split_kv_mma_kernel<KVF, QF, 2, false, true>, mma_smem_bytes(KVF, 2));
+  set(split_kv_mma_kernel<KVF, QF, 3, false, true>, mma_smem_bytes(KVF, 3));
+  set(split_kv_mma_kernel<KVF, QF, 4, false, true>, mma_smem_bytes(KVF, 4));
   return e;
 }
 
@@ -296,15 +300,27 @@ int plan_splits(int batch, int capacity, int kv_format, int sm_count) {
 // ---------------------------------------------------------------- launches
 
 // `bal_ctas` > 0: the balanced schedule on that many CTAs (single token).
+// `cluster`: the one-piece grid as clusters of its `cluster` splits, merged
+// on chip (no combine kernel).
+template <int KVF, int QF, bool CL>
+cudaError_t launch_one_piece(cudaLaunchConfig_t& cfg, const SplitParams& sp, int q_len) {
+  switch (q_len) {
+    case 1: return cudaLaunchKernelEx(&cfg, split_kv_mma_kernel<KVF, QF, 1, false, CL>, sp);
+    case 2: return cudaLaunchKernelEx(&cfg, split_kv_mma_kernel<KVF, QF, 2, false, CL>, sp);
+    case 3: return cudaLaunchKernelEx(&cfg, split_kv_mma_kernel<KVF, QF, 3, false, CL>, sp);
+    default: return cudaLaunchKernelEx(&cfg, split_kv_mma_kernel<KVF, QF, 4, false, CL>, sp);
+  }
+}
+
 template <int KVF, int QF>
-cudaError_t launch_split_t(const SplitParams& sp, int q_len, int bal_ctas, cudaStream_t stream) {
+cudaError_t launch_split_t(const SplitParams& sp, int q_len, int bal_ctas, int cluster, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kMmaThreads, 1, 1);
   cfg.stream = stream;
   // programmatic dependent launch: CTAs may become resident while the
   // previous grid in the stream drains; they wait (griddepcontrol.wait)
   // before reading any input
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
@@ -312,16 +328,19 @@ cudaError_t launch_split_t(const SplitParams& sp, int q_len, int bal_ctas, cudaS
   if (bal_ctas > 0) {
     cfg.gridDim = dim3(bal_ctas, 1, 1);
     cfg.dynamicSmemBytes = mma_smem_bytes(KVF, 1) + kBalMergeBytes;
-    return cudaLaunchKernelEx(&cfg, split_kv_mma_kernel<KVF, QF, 1, true>, sp);
+    return cudaLaunchKernelEx(&cfg, split_kv_mma_kernel<KVF, QF, 1, true, false>, sp);
   }
   cfg.gridDim = dim3(kHkv, sp.batch, sp.splits_eff);
   cfg.dynamicSmemBytes = mma_smem_bytes(KVF, q_len);
-  switch (q_len) {
-    case 1: return cudaLaunchKernelEx(&cfg, split_kv_mma_kernel<KVF, QF, 1, false>, sp);
-    case 2: return cudaLaunchKernelEx(&cfg, split_kv_mma_kernel<KVF, QF, 2, false>, sp);
-    case 3: return cudaLaunchKernelEx(&cfg, split_kv_mma_kernel<KVF, QF, 3, false>, sp);
-    default: return cudaLaunchKernelEx(&cfg, split_kv_mma_kernel<KVF, QF, 4, false>, sp);
+  if (cluster > 0) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = (unsigned)cluster;
+    cfg.numAttrs = 2;
+    return launch_one_piece<KVF, QF, true>(cfg, sp, q_len);
   }
+  return launch_one_piece<KVF, QF, false>(cfg, sp, q_len);
 }
 
 template <int QF>
@@ -396,6 +415,19 @@ BalPlan bal_plan(const Call& c) {
   return bp;
 }
 
+// The one-piece grid merges on chip when its 2..8 splits that hold slots fit
+// one portable thread-block cluster (distributed shared memory), which saves
+// the combine launch and the partials' round trip through HBM.  (Clusters of
+// 9..16, a non-portable size, measured slower on GB300 when warm: e4m3
+// 1 x 8192 in a graph 10.3 -> 12.2 us, a 4-token window at 1 x 4096 9.6 ->
+// 13.7.)  Returns the cluster size, or 0 for the combine kernel.
+constexpr int kClusterMaxSplits = 8;
+int cluster_splits(const Call& c) {
+  if (bal_plan(c).ctas > 0) return 0;
+  const int s = split_count(c.capacity, c.num_splits, c.kv_format);
+  return s >= 2 && s <= kClusterMaxSplits ? s : 0;
+}
+
 gqa_status_t run_split(const Call& c) {
   const Layout lay = layout_of(c.workspace, c.batch * c.q_len, c.num_splits);
   SplitParams sp;
@@ -425,22 +457,22 @@ gqa_status_t run_split(const Call& c) {
   const BalPlan bp = bal_plan(c);
   sp.bal_q_min = bp.q_min;
   cudaError_t e;
-  const int ql = c.q_len, nb = bp.ctas;
-  if (c.kv_format == kKvF16) e = launch_split_t<kKvF16, kQF16>(sp, ql, nb, c.stream);
-  else if (c.kv_format == kKvBF16) e = launch_split_t<kKvBF16, kQBF16>(sp, ql, nb, c.stream);
+  const int ql = c.q_len, nb = bp.ctas, cl = cluster_splits(c);
+  if (c.kv_format == kKvF16) e = launch_split_t<kKvF16, kQF16>(sp, ql, nb, cl, c.stream);
+  else if (c.kv_format == kKvBF16) e = launch_split_t<kKvBF16, kQBF16>(sp, ql, nb, cl, c.stream);
   else if (c.kv_format == kKvE4M3)
-    e = c.q_dtype == GQA_BF16 ? launch_split_t<kKvE4M3, kQBF16>(sp, ql, nb, c.stream)
-                              : launch_split_t<kKvE4M3, kQF16>(sp, ql, nb, c.stream);
+    e = c.q_dtype == GQA_BF16 ? launch_split_t<kKvE4M3, kQBF16>(sp, ql, nb, cl, c.stream)
+                              : launch_split_t<kKvE4M3, kQF16>(sp, ql, nb, cl, c.stream);
   else
-    e = c.q_dtype == GQA_BF16 ? launch_split_t<kKvI8, kQBF16>(sp, ql, nb, c.stream)
-                              : launch_split_t<kKvI8, kQF16>(sp, ql, nb, c.stream);
+    e = c.q_dtype == GQA_BF16 ? launch_split_t<kKvI8, kQBF16>(sp, ql, nb, cl, c.stream)
+                              : launch_split_t<kKvI8, kQF16>(sp, ql, nb, cl, c.stream);
   if (e != cudaSuccess) return cuda_fail(e, "split kernel launch");
   return GQA_OK;
 }
 
 gqa_status_t run_combine(const Call& c) {
   const int splits_eff = split_count(c.capacity, c.num_splits, c.kv_format);
-  if (splits_eff == 1) return GQA_OK;
+  if (splits_eff == 1 || cluster_splits(c) > 0) return GQA_OK;  // merged by stage 1
   const Layout lay = layout_of(c.workspace, c.batch * c.q_len, c.num_splits);
   CombineParams cp;
   cp.lens = c.lens;

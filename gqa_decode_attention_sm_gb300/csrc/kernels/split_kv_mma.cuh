@@ -121,6 +121,13 @@ static_assert(kMmaConsumerWarps * kGroup * 1 * (kD + 2) * 4 <= mma_stages(kKvE4M
                   kMmaConsumerWarps * kGroup * kMaxQLen * (kD + 2) * 4 <= mma_stages(kKvF16, kMaxQLen) * kStageBytes,
               "merge area must fit in the ring");
 
+// ... and the cluster merge's state [column][128] + max + denominator after it.
+static_assert(kMmaConsumerWarps * kGroup * kMaxQLen * (kD + 2) * 4 + kGroup * kMaxQLen * (kD + 2) * 4 <=
+                      mma_stages(kKvF16, kMaxQLen) * kStageBytes &&
+                  kMmaConsumerWarps * kGroup * (kD + 2) * 4 + kGroup * (kD + 2) * 4 <=
+                      mma_stages(kKvE4M3, 1) * kStageBytes,
+              "cluster merge state must fit in the ring");
+
 // ---------------------------------------------------------------- mma.sync
 
 template <bool BF16>
@@ -301,7 +308,56 @@ struct PieceCursor<kTile, true> {
   }
 };
 
-template <int KVF, int QF, int NQ, bool BAL>
+// Cluster merge (one-piece grid whose splits form one thread-block cluster
+// per (b, KV head)): each CTA has left its merged state — unnormalised output
+// st[col][128], running max st_m[col], denominator st_l[col], column
+// col = 4 * query token + head — in its own shared memory.  After a cluster
+// barrier, CTA r of the S in the cluster merges the (column, 4-dim) units
+// u = r, r + S, ... by reading every CTA's state through distributed shared
+// memory, in rank order (deterministic), and writes the output; a second
+// barrier keeps every state alive until all reads are done.  All threads of
+// every CTA call this exactly once.
+template <int QF, int NQ>
+__device__ __forceinline__ void cluster_merge_tail(const SplitParams& p, const float* st) {
+  constexpr int kCols = kGroup * NQ;
+  __syncwarp();  // the barrier's .aligned form wants each warp converged
+  cluster_sync_all();
+  if (threadIdx.x < kMmaConsumerWarps * 32) {
+    const int S = (int)cluster_size(), r = (int)cluster_rank();
+    const int b = blockIdx.y, g = blockIdx.x;
+    const uint32_t base = smem_addr(st);
+    for (int u = r + S * (int)threadIdx.x; u < kCols * 32; u += S * kMmaConsumerWarps * 32) {
+      const int col = u >> 5, d0 = 4 * (u & 31);
+      const uint32_t a_o = base + (uint32_t)(col * kD + d0) * 4u;
+      const uint32_t a_m = base + (uint32_t)(kCols * kD + col) * 4u;
+      const uint32_t a_l = a_m + (uint32_t)kCols * 4u;
+      float M = -INFINITY;
+      for (int k = 0; k < S; ++k) M = fmaxf(M, cluster_ld(cluster_map(a_m, k)));
+      float Ls = 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int k = 0; k < S; ++k) {
+        const float mk = cluster_ld(cluster_map(a_m, k));
+        const float a = mk == -INFINITY ? 0.f : ex2(mk - M);  // a split without slots adds nothing
+        Ls = fmaf(cluster_ld(cluster_map(a_l, k)), a, Ls);
+        const float4 v = cluster_ld4(cluster_map(a_o, k));
+        acc.x = fmaf(v.x, a, acc.x);
+        acc.y = fmaf(v.y, a, acc.y);
+        acc.z = fmaf(v.z, a, acc.z);
+        acc.w = fmaf(v.w, a, acc.w);
+      }
+      const float inv = Ls > 0.f ? p.v_scale / Ls : 0.f;  // a query with no slot gets zeros
+      const int row = (b * NQ + col / kGroup) * kHq + g * kGroup + col % kGroup;
+      *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) + ((size_t)row * kD + d0) * 2) =
+          make_uint2(pack_out<QF>(acc.x * inv, acc.y * inv), pack_out<QF>(acc.z * inv, acc.w * inv));
+    }
+  }
+  __syncwarp();
+  cluster_sync_all();
+}
+
+// CL: the one-piece grid launched as clusters of its splits, merged on chip
+// (cluster_merge_tail) instead of through partials and the combine kernel.
+template <int KVF, int QF, int NQ, bool BAL, bool CL>
 __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
     split_kv_mma_kernel(const __grid_constant__ SplitParams p) {
   constexpr int kMmaStages = mma_stages(KVF, NQ);
@@ -316,12 +372,16 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
   uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(scl) + kMmaStages * kScaleStageBytes);
   uint64_t* empty = full + kMmaStages;
   static_assert(!BAL || NQ == 1, "the balanced schedule serves single-token decode");
+  static_assert(!(BAL && CL), "the cluster merge serves the one-piece grid");
   // epilogue merge area [4 warps][kCols][128] + max + denominator: in the idle
   // ring with one piece per CTA, after the barriers with several (the ring is
   // then still streaming the next piece)
   float* mrg_acc = BAL ? reinterpret_cast<float*>(empty + kMmaStages) : reinterpret_cast<float*>(ring);
   float* mrg_m = mrg_acc + kMmaConsumerWarps * kCols * kD;           // [4][kCols]
   float* mrg_l = mrg_m + kMmaConsumerWarps * kCols;                  // [4][kCols]
+  // cluster merge: this CTA's merged state [kCols][128] + max + denominator,
+  // after the merge area in the idle ring
+  float* cl_state = mrg_l + kMmaConsumerWarps * kCols;
 
   // Every CTA of this grid is resident or done: let stage 2 be scheduled
   // (it waits for this grid's completion before reading the partials).
@@ -431,7 +491,8 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
       atomicOr(p.flags, GQA_FLAG_LENGTH_CLAMPED);
     const int t_begin = s * p.chunk;
     const int t_end = min(L, t_begin + p.chunk);
-    if (t_begin >= t_end) {
+    // (a cluster member keeps going with no tiles: it must reach the merge)
+    if (!CL && t_begin >= t_end) {
       if (p.splits_eff == 1 && threadIdx.x < kMmaConsumerWarps * 32) {
         // one-split launch with length 0: the output rows are zero
         const int hh = threadIdx.x / 32, d0 = 4 * (threadIdx.x % 32);
@@ -443,7 +504,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
       }
       return;
     }
-    cur.start_single(b, g, L, t_begin, t_end, s, p.splits_eff == 1);
+    cur.start_single(b, g, L, t_begin, max(t_begin, t_end), s, !CL && p.splits_eff == 1);
   }
 
   // the barriers' initialisation is visible to every thread (the balanced
@@ -569,6 +630,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
       for (int k = 0; k < kMmaStages; ++k)
         if (last[k] >= 0) mbar_wait(&full[k], (last[k] / kMmaStages) & 1, deadline + p.wait_budget_ns);
     }
+    if constexpr (CL) cluster_merge_tail<QF, NQ>(p, cl_state);
     return;
   }
 
@@ -935,7 +997,13 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
         acc.w = fmaf(v.w, a, acc.w);
       }
       const int row = (b * NQ + it) * kHq + g * kGroup + (ctid >> 5);  // (b, query token, head)
-      if (pc.direct) {
+      if constexpr (CL) {
+        *reinterpret_cast<float4*>(cl_state + col * kD + d0) = acc;
+        if (d0 == 0) {
+          cl_state[kCols * kD + col] = M;
+          cl_state[kCols * kD + kCols + col] = Ls;
+        }
+      } else if (pc.direct) {
         const float inv = Ls > 0.f ? p.v_scale / Ls : 0.f;  // a query with no slot gets zeros
         *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) + ((size_t)row * kD + d0) * 2) =
             make_uint2(pack_out<QF>(acc.x * inv, acc.y * inv), pack_out<QF>(acc.z * inv, acc.w * inv));
@@ -949,6 +1017,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
       }
     }
   }
+  if constexpr (CL) cluster_merge_tail<QF, NQ>(p, cl_state);
 }
 
 }  // namespace gqa

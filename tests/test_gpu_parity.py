@@ -702,6 +702,23 @@ def test_verify_window_every_element(kv_dtype, T):
         _assert_parity(_gpu_rows(out), _oracle_full(t), f"verify T={T} {kv_dtype} splits={S}")
 
 
+@pytest.mark.parametrize("kv_dtype,T", [("f16", 1), ("bf16", 1), ("e4m3", 1), ("i8", 1), ("bf16", 3)])
+def test_cluster_merge_every_split_count(kv_dtype, T):
+    # one-piece grids of 2..8 splits run as one thread-block cluster per
+    # (row, KV head) and merge on chip; row 0 holds slots in its first split
+    # only, so the other members of its clusters merge empty states.  16
+    # splits (16-bit KV; 2048 slots give 8-bit KV at most 8) merge through
+    # the combine kernel instead: the control.
+    C = 2048
+    w = inputs.custom(3, C, T, kv_dtype=kv_dtype, kv_std=2.0 if kv_dtype == "e4m3" else 1.0, nan_tail=True,
+                      q_len=T)
+    t = _make(w, lens=[T, 700, C])
+    ref = _oracle_full(t)
+    for S in list(range(2, 9)) + [16]:
+        out = _verify(t, num_splits=S) if T > 1 else _run(t, num_splits=S).out
+        _assert_parity(_gpu_rows(out), ref, f"{kv_dtype} T={T} splits={S}")
+
+
 def test_verify_window_of_one_is_the_plain_decode():
     t = _make(inputs.WORKLOADS[3])
     plain = _run(t).out
