@@ -672,12 +672,36 @@ def run_gpu(args):
     if rank == 0 and not args.no_per_config:
         line["per_config"] = per_config_table(dev, peak, gq, inputs, quick=args.quick,
                                               cpu=not args.no_cpu_baseline)
+    if rank == 0 and world == 1 and args.read_ceiling:
+        line["read_ceiling"] = read_ceiling(achieved)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def read_ceiling(achieved):
+    """Context for the roofline: the read rate this GPU reaches with the split
+    kernel's data movement alone (bench_read_ceiling.cu: contiguous runs of a
+    4.3 GB buffer streamed through a shared-memory ring by 1-D bulk copies, no
+    arithmetic), built with nvcc for sm_103a and run in a child process after
+    the timed region.  Adds the split kernel's GB/s as a fraction of the best."""
+    import subprocess
+    from gqa_decode_attention_sm_gb300 import build as gbuild
+    out_dir = os.path.join(ROOT, "_build")
+    os.makedirs(out_dir, exist_ok=True)
+    exe = os.path.join(out_dir, "read_ceiling")
+    subprocess.run([gbuild.nvcc(), "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17", "-o", exe,
+                    os.path.join(ROOT, "bench_read_ceiling.cu")], check=True)
+    run = subprocess.run([exe], capture_output=True, text=True, timeout=300)
+    d = json.loads(run.stdout.strip().splitlines()[-1])
+    if run.returncode != 0 or "best_GBps" not in d:
+        raise RuntimeError(f"read-ceiling probe failed: {run.stdout[-300:]} {run.stderr[-300:]}")
+    d["split_kernel_GBps"] = round(achieved, 1)
+    d["split_kernel_frac_of_best"] = round(achieved / d["best_GBps"], 4)
+    return d
 
 
 def main(argv=None):
@@ -698,6 +722,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true")
     ap.add_argument("--quick", action="store_true")
+    ap.add_argument("--read-ceiling", action="store_true",
+                    help="also build and run bench_read_ceiling.cu (the read rate of the split kernel's data "
+                         "movement without arithmetic) and report the split kernel as a fraction of it")
     args = ap.parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
