@@ -405,12 +405,16 @@ BalPlan bal_plan(const Call& c) {
   const long long slots = (long long)mma_ctas_per_sm(c.kv_format, 1) * c.sms;
   // one wave of pieces or less: nothing to balance, the plain grid starts sooner
   if ((long long)kHkv * c.batch * splits_eff <= slots) return bp;
-  // One CTA per resident slot for a contiguous cache.  A paged cache runs 4
-  // waves of smaller runs: its per-CTA rates vary more (pages scattered over
-  // HBM), and the later waves let the hardware even them out (bf16 8 x 131072
-  // in shuffled 256-token pages, GB300: 608 us with one wave, 590 with four,
-  // 592 with the one-piece-per-CTA grid).
-  bp.ctas = (int)((c.block_table != nullptr ? 4 : 1) * slots);
+  // One CTA per resident slot for a contiguous cache.  A paged 16-bit cache
+  // runs 4 waves of smaller runs: its per-CTA rates vary more (pages
+  // scattered over HBM), and the later waves let the hardware even them out
+  // (bf16 8 x 131072 in shuffled 256-token pages, GB300: 586 us back to back
+  // with one wave, 580 with four).  A paged 8-bit cache keeps one wave: at 3
+  // CTAs per SM its issue-heavier CTAs pay more for the extra prologues and
+  // pieces (64 x U[16k, 32k] in 256-token pages: int8 461 us with one wave,
+  // 469 with four; e4m3 444 against 451).
+  const bool waves4 = c.block_table != nullptr && !is_8bit(c.kv_format);
+  bp.ctas = (int)((waves4 ? 4 : 1) * slots);
   bp.q_min = (int)((nmax + c.num_splits - 2) / (c.num_splits - 1));
   return bp;
 }

@@ -35,7 +35,9 @@
 //           B-fragment layout through 4 shuffles.  bf16 P is split into a
 //           high and a low bf16 part (two mma) so the weights keep ~16 bits.
 // e4m3 K/V are widened with the hardware cvt (e4m3x2 -> f16x2, exact), int8
-// codes with a byte permute and one f16 subtraction (exact); the tensor-core
+// V codes with a byte permute and one f16 subtraction (exact), int8 K codes
+// to code + 1152 without it (exact; the scale step takes 1152 * sum_d q_d off
+// each score column); the tensor-core
 // type is then f16 and a bf16 q is converted to f16 once per CTA (exact for
 // 2^-17 <= |q| <= 65504; smaller magnitudes round to the f16 subnormal grid,
 // larger ones saturate).  fp16 and bf16 KV use their own type.  For the int8
