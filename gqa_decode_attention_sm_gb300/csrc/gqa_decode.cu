@@ -420,16 +420,21 @@ BalPlan bal_plan(const Call& c) {
 }
 
 // The one-piece grid merges on chip when its 2..8 splits that hold slots fit
-// one portable thread-block cluster (distributed shared memory), which saves
-// the combine launch and the partials' round trip through HBM.  (Clusters of
-// 9..16, a non-portable size, measured slower on GB300 when warm: e4m3
-// 1 x 8192 in a graph 10.3 -> 12.2 us, a 4-token window at 1 x 4096 9.6 ->
-// 13.7.)  Returns the cluster size, or 0 for the combine kernel.
+// one portable thread-block cluster (distributed shared memory) and the grid
+// is one wave at most: latency-bound launches, where the combine launch and
+// the partials' round trip through HBM are a large share of the time.
+// Measured on GB300: clusters of 9..16 (a non-portable size) were slower when
+// warm (e4m3 1 x 8192 in a graph 10.3 -> 12.2 us, a 4-token window at
+// 1 x 4096 9.6 -> 13.7), and so were multi-wave grids of clusters (int8
+// 64 x U[16k, 32k] with a 2-token window, 8 splits, 4096 CTAs: 530 -> 760 us).
+// Returns the cluster size, or 0 for the combine kernel.
 constexpr int kClusterMaxSplits = 8;
 int cluster_splits(const Call& c) {
-  if (bal_plan(c).ctas > 0) return 0;
+  if (bal_plan(c).ctas > 0 || c.sms < 1) return 0;
   const int s = split_count(c.capacity, c.num_splits, c.kv_format);
-  return s >= 2 && s <= kClusterMaxSplits ? s : 0;
+  if (s < 2 || s > kClusterMaxSplits) return 0;
+  const long long slots = (long long)mma_ctas_per_sm(c.kv_format, c.q_len) * c.sms;
+  return (long long)kHkv * c.batch * s <= slots ? s : 0;
 }
 
 gqa_status_t run_split(const Call& c) {

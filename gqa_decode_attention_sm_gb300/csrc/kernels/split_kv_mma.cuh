@@ -185,13 +185,42 @@ __device__ __forceinline__ void widen4(uint32_t w, uint32_t& lo, uint32_t& hi) {
   }
 }
 
-// K operand: int8 codes enter the scores as code + 1152 (one f16 subtraction
-// per pair saved); the consumer takes 1152 * sum_d q_d off each score column
-// in the scale step.  e4m3 as widen4.
+// Tensor-core operands from 8-bit K and V: int8 codes enter as code + 1152
+// (one f16 subtraction per pair saved); the consumer takes the offset off
+// the scores (1152 * sum_d q_d per column, in the scale step) and off the
+// output accumulator (1152 * the column's summed weights, take_v_bias).  e4m3
+// as widen4.
 template <int KVF>
-__device__ __forceinline__ void widen4_k(uint32_t w, uint32_t& lo, uint32_t& hi) {
+__device__ __forceinline__ void widen4_biased(uint32_t w, uint32_t& lo, uint32_t& hi) {
   if constexpr (KVF == kKvI8) i8x4_to_f16x2x2_biased(w, lo, hi);
   else widen4<KVF>(w, lo, hi);
+}
+
+// int8 V: o holds O + 1152 * (summed weights) per column; vw[nt][c] is this
+// lane's share of the weights of column 2cq + c (its tokens gq, gq + 8 of
+// every slab since the last call).  Sum the shares over the 8 lanes holding
+// each column, take 1152 times that off every accumulator of the column and
+// start again.
+template <int kNT>
+__device__ __forceinline__ void take_v_bias(float (&o)[kNT][8][4], float (&vw)[kNT][2]) {
+#pragma unroll
+  for (int nt = 0; nt < kNT; ++nt) {
+    float s0 = vw[nt][0], s1 = vw[nt][1];
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      s0 += __shfl_xor_sync(0xffffffffu, s0, off);
+      s1 += __shfl_xor_sync(0xffffffffu, s1, off);
+    }
+    const float c0 = -kI8Bias * s0, c1 = -kI8Bias * s1;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      o[nt][mt][0] += c0;
+      o[nt][mt][2] += c0;
+      o[nt][mt][1] += c1;
+      o[nt][mt][3] += c1;
+    }
+    vw[nt][0] = vw[nt][1] = 0.f;
+  }
 }
 
 // Tensor-core element type: bf16 for bf16 KV, f16 otherwise (8-bit KV widens to f16).
@@ -678,7 +707,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
     }
     // int8 K: score offset of each of this lane's columns (2cq, 2cq+1),
     // -1152 * sum_d q_d * scale_log2, added in the scale step (the K operand
-    // is code + 1152, see widen4_k).
+    // is code + 1152, see widen4_biased).
     float kb[kNT][2];
   #pragma unroll
     for (int nt = 0; nt < kNT; ++nt) {
@@ -701,10 +730,12 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
 
     float o[kNT][8][4];
     float m[kNT][2], l[kNT][2];  // per column: running max (log2 domain), this lane's denominator share
+    float vw[kNT][2];            // int8: this lane's share of the V weights since take_v_bias
 #pragma unroll
     for (int nt = 0; nt < kNT; ++nt) {
       m[nt][0] = m[nt][1] = -INFINITY;
       l[nt][0] = l[nt][1] = 0.f;
+      vw[nt][0] = vw[nt][1] = 0.f;
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
@@ -759,8 +790,8 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
               for (int s4 = 0; s4 < 4; ++s4) {
                 const int ks = 4 * ci + s4;
                 uint32_t a0, a1, a2, a3;
-                widen4_k<KVF>(xs[s4], a0, a2);  // row gq: dims (4s,4s+1), (4s+2,4s+3)
-                widen4_k<KVF>(ys[s4], a1, a3);  // row gq+8
+                widen4_biased<KVF>(xs[s4], a0, a2);  // row gq: dims (4s,4s+1), (4s+2,4s+3)
+                widen4_biased<KVF>(ys[s4], a1, a3);  // row gq+8
   #pragma unroll
                 for (int nt = 0; nt < kNT; ++nt) mma16816<false>(sc[nt], a0, a1, a2, a3, qb[nt][ks][0], qb[nt][ks][1]);
               }
@@ -821,6 +852,8 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
             const float a1 = nm[nt][1] == m[nt][1] ? 1.f : ex2(m[nt][1] - nm[nt][1]);
             l[nt][0] *= a0;
             l[nt][1] *= a1;
+            vw[nt][0] *= a0;
+            vw[nt][1] *= a1;
   #pragma unroll
             for (int mt = 0; mt < 8; ++mt) {
               o[nt][mt][0] *= a0;
@@ -861,6 +894,10 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
             const uint32_t pb = pack_f16(p2 * sv[sl][1], p3 * sv[sl][1]);
             l[nt][0] += p0 + p2;
             l[nt][1] += p1 + p3;
+            // the weights exactly as the tensor core multiplies them (V offset)
+            const float2 fa = f16x2_to_f32x2(pa), fb = f16x2_to_f32x2(pb);
+            vw[nt][0] += fa.x + fb.x;
+            vw[nt][1] += fa.y + fb.y;
             bh[nt][0] = prmt(__shfl_sync(0xffffffffu, pa, src0), __shfl_sync(0xffffffffu, pa, src1), half_sel);
             bh[nt][1] = prmt(__shfl_sync(0xffffffffu, pb, src0), __shfl_sync(0xffffffffu, pb, src1), half_sel);
           } else {
@@ -897,12 +934,12 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
           for (int j = 0; j < 4; ++j) {  // word j: dims 16gq+4j .. +3 -> m-tiles 2j, 2j+1
             // pair the two tokens of each k-step: bytes [r0.d, r1.d, r0.d', r1.d']
             uint32_t A0, A1, A2, A3;
-            widen4<KVF>(prmt(a[j], bq[j], 0x5140u), A0, A1);  // dims 4j, 4j+1 of tokens r0, r0+1
-            widen4<KVF>(prmt(c[j], d[j], 0x5140u), A2, A3);   // tokens r0+8, r0+9
+            widen4_biased<KVF>(prmt(a[j], bq[j], 0x5140u), A0, A1);  // dims 4j, 4j+1 of tokens r0, r0+1
+            widen4_biased<KVF>(prmt(c[j], d[j], 0x5140u), A2, A3);   // tokens r0+8, r0+9
   #pragma unroll
             for (int nt = 0; nt < kNT; ++nt) mma16816<false>(o[nt][2 * j], A0, A1, A2, A3, bh[nt][0], bh[nt][1]);
-            widen4<KVF>(prmt(a[j], bq[j], 0x7362u), A0, A1);  // dims 4j+2, 4j+3
-            widen4<KVF>(prmt(c[j], d[j], 0x7362u), A2, A3);
+            widen4_biased<KVF>(prmt(a[j], bq[j], 0x7362u), A0, A1);  // dims 4j+2, 4j+3
+            widen4_biased<KVF>(prmt(c[j], d[j], 0x7362u), A2, A3);
   #pragma unroll
             for (int nt = 0; nt < kNT; ++nt)
               mma16816<false>(o[nt][2 * j + 1], A0, A1, A2, A3, bh[nt][0], bh[nt][1]);
@@ -937,9 +974,15 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
           }
         }
       }
+      // int8 V offset: taken off every 16 tiles, so the accumulator never
+      // carries more than 16 tiles' worth of it
+      if constexpr (KVF == kKvI8) {
+        if ((i & 15) == 15) take_v_bias(o, vw);
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
     }
+    if constexpr (KVF == kKvI8) take_v_bias(o, vw);
 
     // ---- per-warp denominators: sum over the 8 lanes holding each column
   #pragma unroll

@@ -58,10 +58,10 @@
  * tiles (each row start weighs one more tile when some row is shorter than
  * a run) taken by the resident CTAs (lengths read on the device); either way
  * a row has at most num_splits pieces, and the results are deterministic.
- * With one piece per CTA and 2..8 splits that hold slots, the splits of each
- * (b, KV head) run as one thread-block cluster and merge on chip through
- * distributed shared memory: no partial is written and stage 2 launches
- * nothing.  Zero the header once before first use (gqa_decode_workspace_init).
+ * With one piece per CTA, 2..8 splits that hold slots and a grid of one wave
+ * at most, the splits of each (b, KV head) run as one thread-block cluster
+ * and merge on chip through distributed shared memory: no partial is
+ * written and stage 2 launches nothing.  Zero the header once before first use (gqa_decode_workspace_init).
  * Launches that may run concurrently (different streams or graphs) need
  * distinct workspaces; launches ordered on one stream may share one.
  */
@@ -132,8 +132,8 @@ gqa_status_t gqa_decode_plan_for(int batch, int capacity, gqa_kv_format_t kv_for
  * piece per CTA, split s covers slots [s * chunk, min((s + 1) * chunk, len));
  * the balanced schedule cuts rows elsewhere but never into more pieces.
  * Stage 2 runs only when the effective count is above 1 and the splits do
- * not merge on chip (2..8 of them with one piece per CTA do, in a
- * thread-block cluster). */
+ * not merge on chip (2..8 of them with one piece per CTA in a grid of one
+ * wave do, in a thread-block cluster). */
 gqa_status_t gqa_decode_split_geometry(int capacity, int num_splits, gqa_kv_format_t kv_format,
                                        int* chunk_tokens_out, int* splits_effective_out);
 
@@ -233,7 +233,7 @@ gqa_status_t gqa_decode_verify(const void* q, gqa_dtype_t q_dtype, const void* k
  * them separately.  Stage 1 streams K/V once per (b, KV head, split) and
  * writes FP32 partials to the workspace, or the final output when
  * num_splits == 1 or when its 2..8 effective splits merge on chip (one
- * thread-block cluster per (b, KV head), one piece per CTA).  Stage 2 merges
+ * thread-block cluster per (b, KV head), one piece per CTA, one wave).  Stage 2 merges
  * the partials of each (b, query head) with a log-sum-exp combine and writes
  * `out`; when stage 1 wrote the output it launches nothing.  Both must be given the same geometry, scales and workspace, in
  * this order, on one stream.  Validation as gqa_decode_prepared, except that

@@ -719,6 +719,28 @@ def test_cluster_merge_every_split_count(kv_dtype, T):
         _assert_parity(_gpu_rows(out), ref, f"{kv_dtype} T={T} splits={S}")
 
 
+@pytest.mark.parametrize("B,T,merged_on_chip", [(2, 1, True), (2, 2, True), (64, 2, False)])
+def test_cluster_merge_only_for_single_wave_grids(B, T, merged_on_chip):
+    # the cluster merge writes no partials: a workspace whose partial area
+    # holds a sentinel keeps it when the 4 splits merge on chip (a one-wave
+    # grid: 8 x 2 x 4 CTAs) and loses it when the combine kernel merges
+    # (8 x 64 x 4 = 2048 CTAs, several waves).  Both match the oracle.
+    C, S = 1024, 4
+    t = _make(inputs.custom(B, C, C, q_len=T))
+    ws = torch.full((gq.workspace_size(B * T, C, S),), 0xA5, dtype=torch.uint8, device=DEV)
+    gq.workspace_init(ws)
+    if T == 1:
+        p = _prepare(t, num_splits=S, workspace=ws)
+        gq.launch(p)
+        out = p.out
+    else:
+        out = gq.gqa_decode_verify(t["q"], t["kv"], t["lens"], num_splits=S, workspace=ws)
+    torch.cuda.synchronize()
+    untouched = bool(torch.all(ws[256:] == 0xA5))
+    assert untouched == merged_on_chip
+    _assert_parity(_gpu_rows(out), _oracle_full(t), f"B={B} T={T} splits={S}")
+
+
 def test_verify_window_of_one_is_the_plain_decode():
     t = _make(inputs.WORKLOADS[3])
     plain = _run(t).out
