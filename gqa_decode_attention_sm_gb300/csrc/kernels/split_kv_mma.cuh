@@ -6,11 +6,14 @@
 //   one piece per CTA — grid (8, B, splits), CTA (g, b, s) takes chunk s of
 //     row (b, g); verify windows, batches above kBalMaxBatch, and grids of
 //     at most one wave;
-//   balanced — one CTA per resident slot; the tiles of all rows form one
-//     stream and each CTA takes an equal run of it (lengths read on the
-//     device), cut into pieces at row ends.
+//   balanced — one CTA per resident slot; the tiles of all rows (each row
+//     start weighing one more tile when some row is shorter than a run)
+//     form one stream and each CTA takes an equal run of it (lengths read on
+//     the device), cut into pieces at row ends.
 // A piece that is its row's only one writes the normalised output; the
-// others write FP32 partials that stage 2 merges.  A producer warp streams
+// others write FP32 partials that stage 2 merges, or, in a one-wave grid of
+// 2..8 splits launched as thread-block clusters, merge on chip through
+// distributed shared memory (cluster_merge_tail).  A producer warp streams
 // 16 KB K and V tiles with 1-D bulk copies (TMA unit) into an mbarrier ring,
 // copying only rows below the length, straight from one piece into the next.
 // The contractions run on the tensor cores because ncu showed an
@@ -35,9 +38,10 @@
 //           B-fragment layout through 4 shuffles.  bf16 P is split into a
 //           high and a low bf16 part (two mma) so the weights keep ~16 bits.
 // e4m3 K/V are widened with the hardware cvt (e4m3x2 -> f16x2, exact), int8
-// V codes with a byte permute and one f16 subtraction (exact), int8 K codes
-// to code + 1152 without it (exact; the scale step takes 1152 * sum_d q_d off
-// each score column); the tensor-core
+// codes with byte permutes to the f16 integer code + 1152 (exact); the
+// offset comes off the scores (1152 * sum_d q_d per column, in the scale
+// step) and off the output accumulator (1152 * the column's summed f16
+// weights, every 16 tiles and at the piece's end); the tensor-core
 // type is then f16 and a bf16 q is converted to f16 once per CTA (exact for
 // 2^-17 <= |q| <= 65504; smaller magnitudes round to the f16 subnormal grid,
 // larger ones saturate).  fp16 and bf16 KV use their own type.  For the int8
@@ -414,8 +418,9 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
   // after the merge area in the idle ring
   float* cl_state = mrg_l + kMmaConsumerWarps * kCols;
 
-  // Every CTA of this grid is resident or done: let stage 2 be scheduled
-  // (it waits for this grid's completion before reading the partials).
+  // Every CTA of this grid is resident or done: let the next grid in the
+  // stream (stage 2, or the next launch after an on-chip merge) be scheduled;
+  // it waits for this grid's completion before reading what this grid writes.
   pdl_launch_dependents();
   const int C = p.capacity;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
