@@ -46,11 +46,38 @@ KERNEL_SOURCES = ["gqa_decode_attention_sm_gb300/csrc/kernels/common.cuh",
 # ------------------------------------------------------------------ helpers
 
 
+def code_tokens(text: str) -> str:
+    """C++ source with comments removed and whitespace collapsed (string and
+    character literals kept): what the compiler sees, so that a comment edit
+    leaves the hash below, and the traffic capture keyed to it, in place."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        elif c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash() -> str:
+    """Hash of the split kernel's code (comments and layout ignored)."""
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(code_tokens(f.read()).encode())
     return h.hexdigest()[:16]
 
 

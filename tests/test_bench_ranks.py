@@ -73,3 +73,18 @@ def test_reference_arm_prints_once_under_two_ranks(tmp_path):
     d = json.loads(lines0[0])
     assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_kernel_hash_ignores_comments_but_not_code():
+    # the committed traffic capture is keyed to the split kernel's code:
+    # comment and layout edits keep the key, any code edit changes it
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_mod", os.path.join(ROOT, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    src = 'int a = 1;  // note\n/* block\n comment */ const char* s = "// kept";\nchar q = \'"\';\n'
+    assert bench.code_tokens(src) == 'int a = 1; const char* s = "// kept"; char q = \'"\';'
+    assert bench.code_tokens(src.replace("// note", "// other note")) == bench.code_tokens(src)
+    assert bench.code_tokens(src.replace("a = 1", "a = 2")) != bench.code_tokens(src)
+    with open(os.path.join(ROOT, "profiles", "split_kv_traffic.json")) as f:
+        assert len(json.load(f)["source_hash"]) == len(bench.kernel_source_hash()) == 16
