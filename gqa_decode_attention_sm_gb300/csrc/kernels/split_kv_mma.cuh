@@ -758,19 +758,12 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
       const uint8_t* sV = sK + T::kTileBytes;
       const int tile_t0 = t_begin + i * T::kTile;
       const int rows = min(T::kTile, t_end - tile_t0);
-      // int8: K and V row scales of this lane's tokens (R+gq, R+gq+8 of each slab)
-      float sk[kSlabs][2], sv[kSlabs][2];
-      if constexpr (KVF == kKvI8) {
-        const uint16_t* tsk = scl + st * (kScaleStageBytes / 2);
-  #pragma unroll
-        for (int sl = 0; sl < kSlabs; ++sl)
-  #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int r = (warp * kSlabs + sl) * 16 + gq + 8 * u;
-            sk[sl][u] = r < rows ? __uint_as_float((uint32_t)tsk[r] << 16) : 0.f;
-            sv[sl][u] = r < rows ? __uint_as_float((uint32_t)tsk[T::kTile + r] << 16) : 0.f;
-          }
-      }
+      // int8: the bf16 row scale of tile row r (plane 0: K, 1: V), read where
+      // it is used (fewer live registers); 0 past the tile's rows
+      const uint16_t* tsk = scl + st * (kScaleStageBytes / 2);
+      const auto row_scale = [&](int r, int plane) {
+        return r < rows ? __uint_as_float((uint32_t)tsk[plane * T::kTile + r] << 16) : 0.f;
+      };
 
   #pragma unroll
       for (int sl = 0; sl < kSlabs; ++sl) {
@@ -825,10 +818,11 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
             else x[nt][e] = sc[nt][e] * sl2;
           }
           if constexpr (KVF == kKvI8) {  // per-row K scale multiplies that token's scores
-            x[nt][0] *= sk[sl][0];
-            x[nt][1] *= sk[sl][0];
-            x[nt][2] *= sk[sl][1];
-            x[nt][3] *= sk[sl][1];
+            const float ks_a = row_scale(R + gq, 0), ks_b = row_scale(R + gq + 8, 0);
+            x[nt][0] *= ks_a;
+            x[nt][1] *= ks_a;
+            x[nt][2] *= ks_b;
+            x[nt][3] *= ks_b;
           }
           if (ta >= lim[nt]) x[nt][0] = x[nt][1] = -INFINITY;  // select, never multiply
           if (tb >= lim[nt]) x[nt][2] = x[nt][3] = -INFINITY;
@@ -895,8 +889,9 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
           } else if constexpr (KVF == kKvI8) {
             // the per-row V scale joins the weight of its token; the denominator
             // keeps the unscaled weights
-            const uint32_t pa = pack_f16(p0 * sv[sl][0], p1 * sv[sl][0]);
-            const uint32_t pb = pack_f16(p2 * sv[sl][1], p3 * sv[sl][1]);
+            const float vs_a = row_scale(R + gq, 1), vs_b = row_scale(R + gq + 8, 1);
+            const uint32_t pa = pack_f16(p0 * vs_a, p1 * vs_a);
+            const uint32_t pb = pack_f16(p2 * vs_b, p3 * vs_b);
             l[nt][0] += p0 + p2;
             l[nt][1] += p1 + p3;
             // the weights exactly as the tensor core multiplies them (V offset)
