@@ -64,7 +64,10 @@ cudaError_t set_split_attributes() {
   set(split_kv_mma_kernel<KVF, QF, 2, false, false>, mma_smem_bytes(KVF, 2));
   set(split_kv_mma_kernel<KVF, QF, 3, false, false>, mma_smem_bytes(KVF, 3));
   set(split_kv_mma_kernel<KVF, QF, 4, false, false>, mma_smem_bytes(KVF, 4));
-  set(split_kv_mma_kernel<KVF, QF, 1, true, false>, mma_smem_bytes(KVF, 1) + kBalMergeBytes);
+  set(split_kv_mma_kernel<KVF, QF, 1, true, false>, mma_smem_bytes(KVF, 1, true));
+  set(split_kv_mma_kernel<KVF, QF, 2, true, false>, mma_smem_bytes(KVF, 2, true));
+  set(split_kv_mma_kernel<KVF, QF, 3, true, false>, mma_smem_bytes(KVF, 3, true));
+  set(split_kv_mma_kernel<KVF, QF, 4, true, false>, mma_smem_bytes(KVF, 4, true));
   set(split_kv_mma_kernel<KVF, QF, 1, false, true>, mma_smem_bytes(KVF, 1));
   set(split_kv_mma_kernel<KVF, QF, 2, false, true>, mma_smem_bytes(KVF, 2));
   set(split_kv_mma_kernel<KVF, QF, 3, false, true>, mma_smem_bytes(KVF, 3));
@@ -302,13 +305,13 @@ int plan_splits(int batch, int capacity, int kv_format, int sm_count) {
 // `bal_ctas` > 0: the balanced schedule on that many CTAs (single token).
 // `cluster`: the one-piece grid as clusters of its `cluster` splits, merged
 // on chip (no combine kernel).
-template <int KVF, int QF, bool CL>
-cudaError_t launch_one_piece(cudaLaunchConfig_t& cfg, const SplitParams& sp, int q_len) {
+template <int KVF, int QF, bool BAL, bool CL>
+cudaError_t launch_nq(cudaLaunchConfig_t& cfg, const SplitParams& sp, int q_len) {
   switch (q_len) {
-    case 1: return cudaLaunchKernelEx(&cfg, split_kv_mma_kernel<KVF, QF, 1, false, CL>, sp);
-    case 2: return cudaLaunchKernelEx(&cfg, split_kv_mma_kernel<KVF, QF, 2, false, CL>, sp);
-    case 3: return cudaLaunchKernelEx(&cfg, split_kv_mma_kernel<KVF, QF, 3, false, CL>, sp);
-    default: return cudaLaunchKernelEx(&cfg, split_kv_mma_kernel<KVF, QF, 4, false, CL>, sp);
+    case 1: return cudaLaunchKernelEx(&cfg, split_kv_mma_kernel<KVF, QF, 1, BAL, CL>, sp);
+    case 2: return cudaLaunchKernelEx(&cfg, split_kv_mma_kernel<KVF, QF, 2, BAL, CL>, sp);
+    case 3: return cudaLaunchKernelEx(&cfg, split_kv_mma_kernel<KVF, QF, 3, BAL, CL>, sp);
+    default: return cudaLaunchKernelEx(&cfg, split_kv_mma_kernel<KVF, QF, 4, BAL, CL>, sp);
   }
 }
 
@@ -327,8 +330,8 @@ cudaError_t launch_split_t(const SplitParams& sp, int q_len, int bal_ctas, int c
   cfg.numAttrs = 1;
   if (bal_ctas > 0) {
     cfg.gridDim = dim3(bal_ctas, 1, 1);
-    cfg.dynamicSmemBytes = mma_smem_bytes(KVF, 1) + kBalMergeBytes;
-    return cudaLaunchKernelEx(&cfg, split_kv_mma_kernel<KVF, QF, 1, true, false>, sp);
+    cfg.dynamicSmemBytes = mma_smem_bytes(KVF, q_len, true);
+    return launch_nq<KVF, QF, true, false>(cfg, sp, q_len);
   }
   cfg.gridDim = dim3(kHkv, sp.batch, sp.splits_eff);
   cfg.dynamicSmemBytes = mma_smem_bytes(KVF, q_len);
@@ -338,9 +341,9 @@ cudaError_t launch_split_t(const SplitParams& sp, int q_len, int bal_ctas, int c
     attr[1].val.clusterDim.y = 1;
     attr[1].val.clusterDim.z = (unsigned)cluster;
     cfg.numAttrs = 2;
-    return launch_one_piece<KVF, QF, true>(cfg, sp, q_len);
+    return launch_nq<KVF, QF, false, true>(cfg, sp, q_len);
   }
-  return launch_one_piece<KVF, QF, false>(cfg, sp, q_len);
+  return launch_nq<KVF, QF, false, false>(cfg, sp, q_len);
 }
 
 template <int QF>
@@ -380,15 +383,15 @@ Layout layout_of(void* ws, int batch, int splits) {
   return l;
 }
 
-// The balanced schedule serves single-token decode of batches up to
+// The balanced schedule serves decode and verify windows of batches up to
 // kBalMaxBatch whose rows can be split (two or more tiles of capacity) and
 // whose one-piece-per-CTA grid would take more than one wave, as long as the
 // global stream (n + kBalRowCost positions for a row of n tiles, the first
-// ones standing for the piece's fixed cost) fits an int.  q_min keeps every row within the
-// workspace's split slots: a row of n <= nmax tiles meets at most
-// ceil(n / q) + 1 <= num_splits CTAs.  Measured on GB300 (us per call, back
-// to back): fp16 32 x U[1,8192] 96.4 -> 89.9, e4m3 64 x U[16k,32k] 459.4 ->
-// 443.7, bf16 8 x 131072 589.4 -> 584.3.
+// ones standing for the piece's fixed cost) fits an int.  q_min keeps every
+// row within the workspace's split slots: a row of n <= nmax tiles meets at
+// most ceil(n / q) + 1 <= num_splits CTAs.  Measured on GB300 (us per call,
+// back to back): fp16 32 x U[1,8192] 96.4 -> 89.9, e4m3 64 x U[16k,32k]
+// 459.4 -> 443.7, bf16 8 x 131072 589.4 -> 584.3.
 struct BalPlan {
   int ctas = 0;  // 0: the one-piece-per-CTA grid
   int q_min = 0;
@@ -398,11 +401,11 @@ BalPlan bal_plan(const Call& c) {
   BalPlan bp;
   const int tile = tile_tokens(c.kv_format);
   const long long nmax = ((long long)c.capacity + tile - 1) / tile;
-  if (c.q_len != 1 || c.batch > kBalMaxBatch || c.num_splits < 2 || c.sms < 1) return bp;
+  if (c.batch > kBalMaxBatch || c.num_splits < 2 || c.sms < 1) return bp;
   const int splits_eff = split_count(c.capacity, c.num_splits, c.kv_format);
   if (splits_eff < 2) return bp;
   if ((long long)kHkv * c.batch * (nmax + kBalRowCost) > 0x7fffffffLL) return bp;
-  const long long slots = (long long)mma_ctas_per_sm(c.kv_format, 1) * c.sms;
+  const long long slots = (long long)mma_ctas_per_sm(c.kv_format, c.q_len) * c.sms;
   // one wave of pieces or less: nothing to balance, the plain grid starts sooner
   if ((long long)kHkv * c.batch * splits_eff <= slots) return bp;
   // One CTA per resident slot for a contiguous cache.  A paged 16-bit cache

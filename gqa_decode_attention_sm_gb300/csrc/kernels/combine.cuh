@@ -57,7 +57,9 @@ __device__ __forceinline__ void merge_splits(const CombineParams& p, size_t row,
     const int cnt = min(32, n - s0);
     float w = 0.f, lw = 0.f;
     if (lane < cnt) {
-      w = ex2(p.part_m[base + s0 + lane] - M);
+      // a piece without slots for this query (a window's causal limit) adds nothing
+      const float ms = p.part_m[base + s0 + lane];
+      w = ms == -INFINITY ? 0.f : ex2(ms - M);
       lw = w * p.part_l[base + s0 + lane];
     }
 #pragma unroll
@@ -73,7 +75,7 @@ __device__ __forceinline__ void merge_splits(const CombineParams& p, size_t row,
       o.w = fmaf(wk, v.w, o.w);
     }
   }
-  const float inv = n > 0 ? p.v_scale / Ls : 0.f;
+  const float inv = Ls > 0.f ? p.v_scale / Ls : 0.f;  // a query with no slot gets zeros
   uint2 packed;
   if constexpr (QF == kQF16) {
     const __half2 a = __floats2half2_rn(o.x * inv, o.y * inv);

@@ -4,8 +4,7 @@
 // row, served for the 4 query heads of that KV head, so every K/V byte below
 // the length is read from HBM exactly once.  Two schedules:
 //   one piece per CTA — grid (8, B, splits), CTA (g, b, s) takes chunk s of
-//     row (b, g); verify windows, batches above kBalMaxBatch, and grids of
-//     at most one wave;
+//     row (b, g); batches above kBalMaxBatch and grids of at most one wave;
 //   balanced — one CTA per resident slot; the tiles of all rows (each row
 //     start weighing one more tile when some row is shorter than a run)
 //     form one stream and each CTA takes an equal run of it (lengths read on
@@ -111,15 +110,21 @@ __host__ __device__ constexpr int mma_stages(int kvf, int nq) { return is_8bit(k
 __host__ __device__ constexpr int mma_ctas_per_sm(int kvf, int nq) { return is_8bit(kvf) && nq == 1 ? 3 : 2; }
 constexpr int kMaxQLen = 4;  // query tokens per request (a verify window when > 1)
 constexpr int kScaleStageBytes = 2 * 128 * 2;  // int8 cache: K and V row scales of one 128-token tile
-__host__ __device__ constexpr int mma_smem_bytes(int kvf, int nq) {
-  return mma_stages(kvf, nq) * (kStageBytes + kScaleStageBytes + 2 * 8);
-}
 // Balanced schedule: batches up to this size (every CTA's prologue scans the
-// lengths), single-token decode only.  Its merge area sits outside the ring,
-// which keeps streaming the next piece while the consumers merge the last.
+// lengths).  Its merge area sits outside the ring, which keeps streaming the
+// next piece while the consumers merge the last: [4 warps][4 heads][128 + 2],
+// one query token of a window at a time.
 constexpr int kBalMaxBatch = 1024;
 constexpr int kBalMergeBytes = kMmaConsumerWarps * kGroup * (kD + 2) * 4;
 static_assert((kMmaThreads + 3 + kBalMaxBatch) * 4 <= kBalMergeBytes, "the length scan uses the merge area");
+__host__ __device__ constexpr int mma_smem_bytes(int kvf, int nq, bool bal = false) {
+  return mma_stages(kvf, nq) * (kStageBytes + kScaleStageBytes + 2 * 8) + (bal ? kBalMergeBytes : 0);
+}
+// 228 KB of shared memory per SM, 1 KB of it reserved per resident CTA
+static_assert(2 * (mma_smem_bytes(kKvF16, kMaxQLen, true) + 1024) <= 228 * 1024 &&
+                  2 * (mma_smem_bytes(kKvF16, 1, true) + 1024) <= 228 * 1024 &&
+                  3 * (mma_smem_bytes(kKvE4M3, 1, true) + 1024) <= 228 * 1024,
+              "the balanced schedule keeps its residency");
 // With one piece per CTA the epilogue merges the 4 warps' states in the ring
 // (idle by then): [warp][column][128] accumulators + [warp][column] max and
 // denominator.
@@ -406,17 +411,19 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
   uint16_t* scl = reinterpret_cast<uint16_t*>(smem + kMmaStages * kStageBytes);  // [stage][K|V][128]
   uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(scl) + kMmaStages * kScaleStageBytes);
   uint64_t* empty = full + kMmaStages;
-  static_assert(!BAL || NQ == 1, "the balanced schedule serves single-token decode");
   static_assert(!(BAL && CL), "the cluster merge serves the one-piece grid");
-  // epilogue merge area [4 warps][kCols][128] + max + denominator: in the idle
-  // ring with one piece per CTA, after the barriers with several (the ring is
-  // then still streaming the next piece)
+  // epilogue merge area [4 warps][kRC][128] + max + denominator: in the idle
+  // ring with one piece per CTA (all kCols columns in one round), after the
+  // barriers with several (the ring is then still streaming the next piece;
+  // one query token's 4 columns per round)
+  constexpr int kRounds = BAL ? NQ : 1;
+  constexpr int kRC = kCols / kRounds;  // columns merged per round
   float* mrg_acc = BAL ? reinterpret_cast<float*>(empty + kMmaStages) : reinterpret_cast<float*>(ring);
-  float* mrg_m = mrg_acc + kMmaConsumerWarps * kCols * kD;           // [4][kCols]
-  float* mrg_l = mrg_m + kMmaConsumerWarps * kCols;                  // [4][kCols]
+  float* mrg_m = mrg_acc + kMmaConsumerWarps * kRC * kD;             // [4][kRC]
+  float* mrg_l = mrg_m + kMmaConsumerWarps * kRC;                    // [4][kRC]
   // cluster merge: this CTA's merged state [kCols][128] + max + denominator,
   // after the merge area in the idle ring
-  float* cl_state = mrg_l + kMmaConsumerWarps * kCols;
+  float* cl_state = mrg_l + kMmaConsumerWarps * kRC;
 
   // Every CTA of this grid is resident or done: let the next grid in the
   // stream (stage 2, or the next launch after an on-chip merge) be scheduled;
@@ -457,7 +464,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
     bool clamped = false;
     for (int bb = rb0; bb < rb1; ++bb) {
       const int lr = __ldg(p.lens + bb);
-      clamped |= lr < 1 || lr > C;
+      clamped |= lr < NQ || lr > C;  // a window of NQ queries needs NQ slots
       lsh[bb] = min(max(lr, 0), C);
       const int nb = (lsh[bb] + T::kTile - 1) / T::kTile;
       mine_n += nb;
@@ -996,68 +1003,78 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
     // with the ring, which then holds the merge area); with several pieces this
     // also keeps the previous piece's merge reads ahead of these writes
     named_barrier_sync(1, kMmaConsumerWarps * 32);
+    // The 4 warps' states merge through shared memory in rounds of kRC
+    // columns: all of them at once in the idle ring with one piece per CTA,
+    // one query token (4 heads) per round in the balanced schedule's smaller
+    // merge area outside the ring.
     // O^T fragment: o[nt][mt][0] = O[dim 16gq+2mt][column 2cq], [1] = [..][2cq+1],
     //               o[nt][mt][2] = O[dim 16gq+2mt+1][2cq],  [3] = [..+1][2cq+1]
-  #pragma unroll
-    for (int nt = 0; nt < kNT; ++nt) {
-      const int col = 8 * nt + 2 * cq;  // this lane's first column in the n-tile
-      if (col < kCols) {
-        float* ha = mrg_acc + (warp * kCols + col) * kD + 16 * gq;
-        float* hb = ha + kD;
-  #pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          *reinterpret_cast<float2*>(ha + 2 * mt) = make_float2(o[nt][mt][0], o[nt][mt][2]);
-          *reinterpret_cast<float2*>(hb + 2 * mt) = make_float2(o[nt][mt][1], o[nt][mt][3]);
-        }
-        if (gq == 0) {
-          mrg_m[warp * kCols + col] = m[nt][0];
-          mrg_m[warp * kCols + col + 1] = m[nt][1];
-          mrg_l[warp * kCols + col] = l[nt][0];
-          mrg_l[warp * kCols + col + 1] = l[nt][1];
-        }
-      }
-    }
-    named_barrier_sync(1, kMmaConsumerWarps * 32);
-
-    // ---- merge the 4 warps: thread -> (column, dims d0..d0+3)
     const int ctid = threadIdx.x;
     const int d0 = 4 * (ctid & 31);
   #pragma unroll
-    for (int it = 0; it < NQ; ++it) {
-      const int col = (ctid >> 5) + kGroup * it;  // query token it, head ctid/32
-      float M = -INFINITY;
+    for (int rd = 0; rd < kRounds; ++rd) {
+      if (rd > 0) named_barrier_sync(1, kMmaConsumerWarps * 32);  // the last round's reads are done
   #pragma unroll
-      for (int w = 0; w < kMmaConsumerWarps; ++w) M = fmaxf(M, mrg_m[w * kCols + col]);
-      float Ls = 0.f;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int nt = 0; nt < kNT; ++nt) {
+        const int col = 8 * nt + 2 * cq;  // this lane's first column in the n-tile
+        if (col < kCols && col / kRC == rd) {
+          const int lc = col - rd * kRC;
+          float* ha = mrg_acc + (warp * kRC + lc) * kD + 16 * gq;
+          float* hb = ha + kD;
   #pragma unroll
-      for (int w = 0; w < kMmaConsumerWarps; ++w) {
-        const float mw = mrg_m[w * kCols + col];
-        const float a = mw == -INFINITY ? 0.f : ex2(mw - M);
-        Ls = fmaf(mrg_l[w * kCols + col], a, Ls);
-        const float4 v = *reinterpret_cast<const float4*>(&mrg_acc[(w * kCols + col) * kD + d0]);
-        acc.x = fmaf(v.x, a, acc.x);
-        acc.y = fmaf(v.y, a, acc.y);
-        acc.z = fmaf(v.z, a, acc.z);
-        acc.w = fmaf(v.w, a, acc.w);
-      }
-      const int row = (b * NQ + it) * kHq + g * kGroup + (ctid >> 5);  // (b, query token, head)
-      if constexpr (CL) {
-        *reinterpret_cast<float4*>(cl_state + col * kD + d0) = acc;
-        if (d0 == 0) {
-          cl_state[kCols * kD + col] = M;
-          cl_state[kCols * kD + kCols + col] = Ls;
+          for (int mt = 0; mt < 8; ++mt) {
+            *reinterpret_cast<float2*>(ha + 2 * mt) = make_float2(o[nt][mt][0], o[nt][mt][2]);
+            *reinterpret_cast<float2*>(hb + 2 * mt) = make_float2(o[nt][mt][1], o[nt][mt][3]);
+          }
+          if (gq == 0) {
+            mrg_m[warp * kRC + lc] = m[nt][0];
+            mrg_m[warp * kRC + lc + 1] = m[nt][1];
+            mrg_l[warp * kRC + lc] = l[nt][0];
+            mrg_l[warp * kRC + lc + 1] = l[nt][1];
+          }
         }
-      } else if (pc.direct) {
-        const float inv = Ls > 0.f ? p.v_scale / Ls : 0.f;  // a query with no slot gets zeros
-        *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) + ((size_t)row * kD + d0) * 2) =
-            make_uint2(pack_out<QF>(acc.x * inv, acc.y * inv), pack_out<QF>(acc.z * inv, acc.w * inv));
-      } else {
-        const size_t idx = (size_t)row * p.num_splits + pc.slot;
-        *reinterpret_cast<float4*>(p.part_o + idx * kD + d0) = acc;
-        if (d0 == 0) {
-          p.part_m[idx] = M;
-          p.part_l[idx] = Ls;
+      }
+      named_barrier_sync(1, kMmaConsumerWarps * 32);
+
+      // ---- merge the 4 warps: thread -> (column, dims d0..d0+3)
+  #pragma unroll
+      for (int il = 0; il < kRC / kGroup; ++il) {
+        const int lc = (ctid >> 5) + kGroup * il;  // column in this round
+        const int col = rd * kRC + lc;             // query token col / 4, head ctid / 32
+        float M = -INFINITY;
+  #pragma unroll
+        for (int w = 0; w < kMmaConsumerWarps; ++w) M = fmaxf(M, mrg_m[w * kRC + lc]);
+        float Ls = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  #pragma unroll
+        for (int w = 0; w < kMmaConsumerWarps; ++w) {
+          const float mw = mrg_m[w * kRC + lc];
+          const float a = mw == -INFINITY ? 0.f : ex2(mw - M);
+          Ls = fmaf(mrg_l[w * kRC + lc], a, Ls);
+          const float4 v = *reinterpret_cast<const float4*>(&mrg_acc[(w * kRC + lc) * kD + d0]);
+          acc.x = fmaf(v.x, a, acc.x);
+          acc.y = fmaf(v.y, a, acc.y);
+          acc.z = fmaf(v.z, a, acc.z);
+          acc.w = fmaf(v.w, a, acc.w);
+        }
+        const int row = (b * NQ + col / kGroup) * kHq + g * kGroup + (ctid >> 5);  // (b, query token, head)
+        if constexpr (CL) {
+          *reinterpret_cast<float4*>(cl_state + col * kD + d0) = acc;
+          if (d0 == 0) {
+            cl_state[kCols * kD + col] = M;
+            cl_state[kCols * kD + kCols + col] = Ls;
+          }
+        } else if (pc.direct) {
+          const float inv = Ls > 0.f ? p.v_scale / Ls : 0.f;  // a query with no slot gets zeros
+          *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) + ((size_t)row * kD + d0) * 2) =
+              make_uint2(pack_out<QF>(acc.x * inv, acc.y * inv), pack_out<QF>(acc.z * inv, acc.w * inv));
+        } else {
+          const size_t idx = (size_t)row * p.num_splits + pc.slot;
+          *reinterpret_cast<float4*>(p.part_o + idx * kD + d0) = acc;
+          if (d0 == 0) {
+            p.part_m[idx] = M;
+            p.part_l[idx] = Ls;
+          }
         }
       }
     }

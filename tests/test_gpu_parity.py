@@ -741,6 +741,34 @@ def test_cluster_merge_only_for_single_wave_grids(B, T, merged_on_chip):
     _assert_parity(_gpu_rows(out), _oracle_full(t), f"B={B} T={T} splits={S}")
 
 
+@pytest.mark.parametrize("kv_dtype", ["f16", "bf16", "e4m3", "i8"])
+@pytest.mark.parametrize("T", [2, 4])
+def test_balanced_verify_window(kv_dtype, T):
+    # a ragged batch well past one wave runs the balanced schedule with a
+    # window too: rows are cut at run ends, and a piece may hold no slot for
+    # an early query of the window (its causal limit); lengths below T give
+    # zero rows for the queries without slots and the clamp flag
+    B, C = 96, 2048
+    rng = np.random.default_rng(T)
+    lens = rng.integers(T, C + 1, B)
+    lens[:6] = [T - 1, T, T + 1, 64, C, C - 1]
+    w = inputs.custom(B, C, 1, kv_dtype=kv_dtype, kv_std=2.0 if kv_dtype == "e4m3" else 1.0, nan_tail=True,
+                      q_len=T)
+    t = _make(w, lens=lens.tolist())
+    fp8 = kv_dtype == "e4m3"
+    ws = torch.zeros(gq.workspace_size(B * T, C, 4), dtype=torch.uint8, device=DEV)
+    out = gq.gqa_decode_verify(t["q"], t["kv"], t["lens"], q_scale=t["q_scale"],
+                               k_scale=t["k_scale"] if fp8 else 1.0, v_scale=t["v_scale"] if fp8 else 1.0,
+                               kv_scales=t["kv_scales"], num_splits=4, workspace=ws)
+    assert gq.get_status(ws) & api.FLAG_LENGTH_CLAMPED
+    got = out.view(B, T, 32, 128)
+    assert not got[0, 0].any()  # length T - 1: the first query has no slot
+    keep = list(range(1, B))
+    sub = dict(t, q=t["q"][keep], kv=t["kv"][keep], lens=t["lens"][keep],
+               kv_scales=t["kv_scales"][keep] if t["kv_scales"] is not None else None)
+    _assert_parity(_gpu_rows(got[keep]), _oracle_full(sub), f"balanced window T={T} {kv_dtype}")
+
+
 def test_verify_window_of_one_is_the_plain_decode():
     t = _make(inputs.WORKLOADS[3])
     plain = _run(t).out
