@@ -432,27 +432,30 @@ def per_config_table(dev, peak, gq, inputs, quick=False, cpu=True):
         table[str(idx)] = row
         del t, out, p
         torch.cuda.empty_cache()
-    # a 2-token verify window over workload 4 (two queries per request read the cache once)
-    w = inputs.with_(inputs.WORKLOADS[4], q_len=2)
-    t = inputs.make(w, dev)
-    out = torch.empty_like(t["q"])
-    S = gq.plan(w.batch, w.capacity, 1, dev)
-    ws = torch.zeros(gq.workspace_size(w.batch * 2, w.capacity, S), dtype=torch.uint8, device=dev)
+    # a 2-token verify window (two queries per request read the cache once):
+    # over workload 4, and over the ragged workload 3 (the balanced schedule)
+    for idx, note in ((4, "workload 4 with a 2-token verify window (q_len 2, causal within the window)"),
+                      (3, "workload 3 (ragged, NaN tail) with a 2-token verify window")):
+        w = inputs.with_(inputs.WORKLOADS[idx], q_len=2)
+        t = inputs.make(w, dev)
+        out = torch.empty_like(t["q"])
+        S = gq.plan(w.batch, w.capacity, 1, dev)
+        ws = torch.zeros(gq.workspace_size(w.batch * 2, w.capacity, S), dtype=torch.uint8, device=dev)
 
-    def window():
-        gq.gqa_decode_verify(t["q"], t["kv"], t["lens"], out=out, num_splits=S, workspace=ws)
+        def window():
+            gq.gqa_decode_verify(t["q"], t["kv"], t["lens"], out=out, num_splits=S, workspace=ws)
 
-    for _ in range(3):
-        window()
-    torch.cuda.synchronize()
-    nbytes = algorithmic_bytes(w, t["lens"].cpu().tolist()) + w.batch * 32 * 128 * 2 * 2  # 2x q and out
-    us = time_calls(window, 5 if quick else 20, flush=flush)
-    table["4-window2"] = {"us_per_call": round(us, 2), "GBps": round(nbytes / us / 1e3, 1),
-                          "frac_of_peak": round(nbytes / us / 1e3 / peak, 4), "alg_bytes": nbytes, "splits": S,
-                          "l2": "cold (512 MB written, then 256 MB read, before each call)",
-                          "note": "workload 4 with a 2-token verify window (q_len 2, causal within the window)"}
-    del t, out, ws
-    torch.cuda.empty_cache()
+        for _ in range(3):
+            window()
+        torch.cuda.synchronize()
+        nbytes = algorithmic_bytes(w, t["lens"].cpu().tolist()) + w.batch * 32 * 128 * 2 * 2  # 2x q and out
+        us = time_calls(window, 5 if quick else 20, flush=flush)
+        table[f"{idx}-window2"] = {"us_per_call": round(us, 2), "GBps": round(nbytes / us / 1e3, 1),
+                                   "frac_of_peak": round(nbytes / us / 1e3 / peak, 4), "alg_bytes": nbytes,
+                                   "splits": S, "l2": "cold (512 MB written, then 256 MB read, before each call)",
+                                   "note": note}
+        del t, out, ws
+        torch.cuda.empty_cache()
 
     # a paged cache: workload 4 scattered over a shuffled pool of 256-token pages
     w = inputs.WORKLOADS[4]

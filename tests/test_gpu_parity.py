@@ -608,6 +608,22 @@ def test_paged_verify_window(kv_dtype, T):
         assert torch.equal(out.view(torch.int16), contiguous.view(torch.int16))
 
 
+@pytest.mark.parametrize("kv_dtype,T", [("bf16", 2), ("i8", 2), ("e4m3", 3)])
+def test_paged_verify_window_balanced(kv_dtype, T):
+    # a ragged paged batch well past one wave: the balanced schedule (4 waves
+    # for a 16-bit cache, 1 for 8-bit) with a window, pages shuffled
+    B, C = 64, 2048
+    rng = np.random.default_rng(31 + T)
+    w = inputs.custom(B, C, 1, kv_dtype=kv_dtype, kv_std=2.0 if kv_dtype == "e4m3" else 1.0, nan_tail=True,
+                      q_len=T)
+    t = _make(w, lens=rng.integers(T, C + 1, B).tolist())
+    ref = _oracle_full(t)
+    pt = inputs.paginate(t, 128, extra_pages=9, seed=T)
+    out = _paged(pt, num_splits=4)
+    torch.cuda.synchronize()
+    _assert_parity(_gpu_rows(out), ref, f"paged window {T} {kv_dtype}, balanced")
+
+
 @pytest.mark.parametrize("kv_dtype", ["f16", "bf16", "e4m3"])
 @pytest.mark.parametrize("page_size", [16, 64, 256])
 def test_paged_matches_oracle_and_contiguous_path(kv_dtype, page_size):
