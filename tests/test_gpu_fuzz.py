@@ -1,0 +1,125 @@
+"""Seeded random cases through the C ABI against the FP64 oracle, every element.
+
+The fixed-shape parity tests pin chosen edge cases; these draw the rest at
+random so that the launch paths meet in combinations nobody picked: the KV
+format (fp16, bf16, e4m3, int8 with row scales), the window (1-4 query
+tokens), batch and capacity, uniform or ragged lengths (some rows empty),
+the split count (planner or explicit), and a contiguous or paged cache
+(shuffled pages of 16-256 slots).  Together they reach every schedule: one
+piece per CTA merged by the combine kernel, one-wave grids merged on chip in
+thread-block clusters, and the balanced schedule with and without the
+per-row cost, single tokens and windows, 1 or 4 waves.  Sizes stay small
+enough for the oracle to check every output element in a few seconds.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import gqa_decode_attention_sm_gb300 as gq
+from gqa_decode_attention_sm_gb300 import inputs
+from helpers import bits_of, tolerance_ok
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda", 0)
+FMT = {"f16": oracle.F16, "bf16": oracle.BF16, "e4m3": oracle.E4M3, "i8": oracle.I8}
+N_CASES = 48
+
+
+def _cases():
+    rng = np.random.default_rng(2026)
+    out = []
+    while len(out) < N_CASES:
+        kv_dtype = str(rng.choice(["f16", "bf16", "e4m3", "i8"]))
+        T = int(rng.choice([1, 1, 1, 2, 3, 4]))
+        paged = bool(rng.random() < 0.4)
+        page = int(rng.choice([16, 64, 256]))
+        B = int(rng.choice([1, 2, 3, 5, 8, 17, 40, 96, 160]))
+        C = int(rng.choice([64, 128, 256, 512, 768, 1024, 2048]))
+        if paged:
+            C = max(page, C // page * page)
+        if B * C * T > 400_000:
+            continue
+        kind = str(rng.choice(["uniform", "ragged", "ragged", "ragged_empty"]))
+        if kind == "uniform":
+            lens = [C] * B
+        else:
+            lens = rng.integers(T, C + 1, B).tolist()
+            if kind == "ragged_empty" and B > 1:
+                for b in rng.choice(B, size=max(1, B // 8), replace=False):
+                    lens[int(b)] = 0
+        S = rng.choice([None, None, None, 1, 2, 3, 4, 8, 16, 38])
+        S = None if S is None else int(S)
+        q_scale = float(rng.choice([1.0, 0.5, 2.0]))
+        out.append((len(out), kv_dtype, T, paged, page, B, C, [int(x) for x in lens], S, q_scale))
+    return out
+
+
+def _balanced_cases():
+    """Cases built to need the balanced schedule: batches of 48-128 rows,
+    capacity >= 1024 and 4-16 splits put the one-piece grid past one wave."""
+    rng = np.random.default_rng(7)
+    out = []
+    while len(out) < 16:
+        kv_dtype = str(rng.choice(["f16", "bf16", "e4m3", "i8"]))
+        T = int(rng.choice([1, 1, 2, 3, 4]))
+        paged = bool(rng.random() < 0.4)
+        page = int(rng.choice([64, 256]))
+        B = int(rng.choice([48, 64, 96, 128]))
+        C = int(rng.choice([1024, 2048]))
+        if B * C * T > 400_000:
+            continue
+        lens = rng.integers(T, C + 1, B).tolist()
+        if rng.random() < 0.3:
+            for b in rng.choice(B, size=B // 10, replace=False):
+                lens[int(b)] = 0
+        if rng.random() < 0.2:
+            lens = [C] * B
+        S = int(rng.choice([4, 8, 16]))
+        q_scale = float(rng.choice([1.0, 0.5, 2.0]))
+        out.append((100 + len(out), kv_dtype, T, paged, page, B, C, [int(x) for x in lens], S, q_scale))
+    return out
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from gqa_decode_attention_sm_gb300 import build as gbuild
+    gbuild.build()
+    oracle.build()
+    torch.cuda.init()
+
+
+@pytest.mark.parametrize("case", _cases() + _balanced_cases(), ids=lambda c: f"case{c[0]}-{c[1]}-T{c[2]}-{'paged' if c[3] else 'contig'}"
+                         f"-B{c[5]}-C{c[6]}-S{c[8]}")
+def test_random_case_matches_oracle(case):
+    idx, kv_dtype, T, paged, page, B, C, lens, S, q_scale = case
+    fp8 = kv_dtype == "e4m3"
+    w = inputs.custom(B, C, 1, kv_dtype=kv_dtype, kv_std=2.0 if fp8 else 1.0, nan_tail=True, q_scale=q_scale,
+                      index=500 + idx, q_len=T)
+    t = inputs.make(w, DEV, lens=lens)
+    ks, vs = (t["k_scale"], t["v_scale"]) if fp8 else (1.0, 1.0)
+    q4 = t["q"] if T > 1 else t["q"][:, None].contiguous()
+    if paged:
+        pt = inputs.paginate(t, page, extra_pages=3, seed=idx)
+        out = gq.gqa_decode_paged(q4 if T > 1 else t["q"], pt["kv_pages"], pt["block_table"], pt["lens"],
+                                  q_scale=q_scale, k_scale=ks, v_scale=vs, num_splits=S,
+                                  kv_scales=pt.get("kv_scale_pages"))
+    else:
+        out = gq.gqa_decode_verify(q4, t["kv"], t["lens"], q_scale=q_scale, k_scale=ks, v_scale=vs,
+                                   kv_scales=t["kv_scales"], num_splits=S)
+    torch.cuda.synchronize()
+    got = out.float().view(B, T, 32, 128).cpu().numpy()
+    keep = [b for b in range(B) if lens[b] > 0]
+    empty = [b for b in range(B) if lens[b] == 0]
+    assert not np.any(got[empty]), "rows without slots must be zero"
+    if not keep:
+        return
+    args = dict(q_scale=q_scale, k_scale=t["k_scale"], v_scale=t["v_scale"])
+    if t["kv_scales"] is not None:
+        args["kv_scales"] = bits_of(t["kv_scales"][keep])
+    qk = t["q"][keep]
+    ref, _ = oracle.gqa_decode(bits_of(qk), FMT[w.q_dtype], bits_of(t["kv"][keep]), FMT[kv_dtype],
+                               np.array([lens[b] for b in keep], np.int32), **args)
+    ok, err, excess = tolerance_ok(got[keep].reshape(-1, 128), ref)
+    assert ok, f"case {idx}: max |gpu - oracle| {err:.3e} exceeds the bar by {excess:.3e}"
