@@ -22,6 +22,8 @@
 #include "kernels/common.cuh"
 #include "kernels/split_kv_mma.cuh"
 
+static_assert(GQA_MAX_SPLITS <= 32 * gqa::kCombineChunks, "the combine's chunks cover every split slot");
+
 namespace {
 
 using namespace gqa;
@@ -350,7 +352,7 @@ template <int QF>
 cudaError_t launch_combine_t(const CombineParams& cp, int batch_rows, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(kHkv, batch_rows, 1);
-  cfg.blockDim = dim3(kCombineThreads, 1, 1);
+  cfg.blockDim = dim3(kGroup * 32 * cp.warps_per_head, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   // programmatic dependent launch: may be scheduled while stage 1 drains; the
@@ -360,7 +362,11 @@ cudaError_t launch_combine_t(const CombineParams& cp, int batch_rows, cudaStream
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, combine_kernel<QF>, cp);
+  switch (cp.warps_per_head) {
+    case 1: return cudaLaunchKernelEx(&cfg, combine_kernel<QF, 1>, cp);
+    case 2: return cudaLaunchKernelEx(&cfg, combine_kernel<QF, 2>, cp);
+    default: return cudaLaunchKernelEx(&cfg, combine_kernel<QF, 4>, cp);
+  }
 }
 
 struct Layout {
@@ -502,6 +508,15 @@ gqa_status_t run_combine(const Call& c) {
   cp.bal_q_min = bp.q_min;
   cp.tile = tile_tokens(c.kv_format);
   cp.batch = c.batch;
+  // Warps per query head: enough that each merges at most about 8 pieces of
+  // its row in one round of loads (up to 4).  Pieces per row: the splits
+  // that hold slots, or under the balanced schedule about CTAs / rows + 2 (a
+  // row meets that many runs, plus the partial ones at its ends).
+  const long long expected =
+      bp.ctas > 0 ? std::min<long long>(c.num_splits, bp.ctas / (kHkv * (long long)c.batch) + 2) : splits_eff;
+  int W = 1;
+  while (W < kCombineMaxWarpsPerHead && expected > 8LL * W) W *= 2;
+  cp.warps_per_head = W;
   cudaError_t e = c.q_dtype == GQA_F16 ? launch_combine_t<kQF16>(cp, c.batch * c.q_len, c.stream)
                                        : launch_combine_t<kQBF16>(cp, c.batch * c.q_len, c.stream);
   if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
