@@ -504,6 +504,34 @@ def per_config_table(dev, peak, gq, inputs, quick=False, cpu=True):
                              "frac_of_peak": round(nbytes / us / 1e3 / peak, 4), "alg_bytes": nbytes, "splits": S,
                              "l2": "cold (512 MB written, then 256 MB read, before each call)",
                              "note": "int8 codes + bf16 row scales (workload 5 shape) in shuffled 256-token pages"}
+    del t, pt, out, ws
+    torch.cuda.empty_cache()
+
+    # one long request: bf16, batch 1, 131072 tokens (all parallelism from splitting the row)
+    w = inputs.custom(1, 131072, 131072, kv_dtype="bf16", index=4)
+    t = inputs.make(w, dev)
+    out = torch.empty_like(t["q"])
+    p = gq.prepare({"Q": t["q"], "KV": t["kv"], "O": out, "sequence_lengths": t["lens"]}, q_scale=1.0)
+
+    def long_one():
+        gq.launch(p)
+
+    for _ in range(3):
+        long_one()
+    torch.cuda.synchronize()
+    nbytes = algorithmic_bytes(w, t["lens"].cpu().tolist())
+    us = time_calls(long_one, 5 if quick else 20, flush=flush)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(20):
+        long_one()
+    b.record()
+    torch.cuda.synchronize()
+    table["bf16-1x131072"] = {"us_per_call": round(us, 2), "GBps": round(nbytes / us / 1e3, 1),
+                              "frac_of_peak": round(nbytes / us / 1e3 / peak, 4), "alg_bytes": nbytes,
+                              "splits": p.num_splits, "l2": "cold (512 MB written, then 256 MB read, before each call)",
+                              "us_per_call_back_to_back": round(a.elapsed_time(b) / 20 * 1e3, 2),
+                              "note": "one long request: batch 1, 131072 bf16 tokens"}
     return table
 
 
