@@ -117,8 +117,9 @@ constexpr int kScaleStageBytes = 2 * 128 * 2;  // int8 cache: K and V row scales
 constexpr int kBalMaxBatch = 1024;
 constexpr int kBalMergeBytes = kMmaConsumerWarps * kGroup * (kD + 2) * 4;
 static_assert((kMmaThreads + 3 + kBalMaxBatch) * 4 <= kBalMergeBytes, "the length scan uses the merge area");
+constexpr int kBalRunBytes = 16;  // the run length Q, after the merge area
 __host__ __device__ constexpr int mma_smem_bytes(int kvf, int nq, bool bal = false) {
-  return mma_stages(kvf, nq) * (kStageBytes + kScaleStageBytes + 2 * 8) + (bal ? kBalMergeBytes : 0);
+  return mma_stages(kvf, nq) * (kStageBytes + kScaleStageBytes + 2 * 8) + (bal ? kBalMergeBytes + kBalRunBytes : 0);
 }
 // 228 KB of shared memory per SM, 1 KB of it reserved per resident CTA
 static_assert(2 * (mma_smem_bytes(kKvF16, kMaxQLen, true) + 1024) <= 228 * 1024 &&
@@ -296,19 +297,20 @@ template <int kTile>
 struct PieceCursor<kTile, true> {
   // The cursor rests on rows that hold tokens, so the row cost is wb - nb.
   // The lengths, batch and capacity are read from the kernel parameters.
-  int b, g, j, nb, wb, L, L_next, pb, x, x1, q;
+  int b, g, j, nb, wb, L, L_next, pb, x, x1;
+  const int* q_sm;  // the run length Q, in shared memory (one register fewer)
   __device__ void set_row(int len, int rc) {
     L = len;
     nb = (L + kTile - 1) / kTile;
     wb = bal_row_positions(nb, rc);
   }
   // L0, L1: clamped lengths of rows b0 and b0 + 1 (0 past the batch)
-  __device__ void start(int b0, int pb0, int L0, int L1, int x0, int x1_, int q_, int rc) {
+  __device__ void start(int b0, int pb0, int L0, int L1, int x0, int x1_, const int* q_, int rc) {
     b = b0;
     pb = pb0;
     x = x0;
     x1 = x1_;
-    q = q_;
+    q_sm = q_;
     set_row(L0, rc);
     L_next = L1;
     const int within = x0 - kHkv * pb;
@@ -324,6 +326,7 @@ struct PieceCursor<kTile, true> {
       const bool has_tiles = r1 > r0;
       if (has_tiles) {
         const int tf = kHkv * pb + g * wb + rc;
+        const int q = *q_sm;
         const int fq = tf / q;
         pc = Piece{b, g, L, (r0 - rc) * kTile, min(L, (r1 - rc) * kTile), cta - fq, (tf + nb - 1) / q == fq};
       }
@@ -424,6 +427,8 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
   // cluster merge: this CTA's merged state [kCols][128] + max + denominator,
   // after the merge area in the idle ring
   float* cl_state = mrg_l + kMmaConsumerWarps * kRC;
+  // balanced schedule: the run length Q, read by the cursor at each piece
+  int* q_sm = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(mrg_acc) + kBalMergeBytes);
 
   // Every CTA of this grid is resident or done: let the next grid in the
   // stream (stage 2, or the next launch after an on-chip merge) be scheduled;
@@ -508,6 +513,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
     const int total = kHkv * (sum_n + rc * sum_r);
     const int q = max((total + (int)gridDim.x - 1) / (int)gridDim.x, p.bal_q_min);
     const int x0 = (int)blockIdx.x * q;
+    if (threadIdx.x == 0) *q_sm = q;  // visible to the cursor after the barrier below
     int pre = pre_n + rc * pre_r;
     // the thread whose rows hold position x0 records the first row and its prefix
     if (x0 < total && kHkv * pre <= x0 && x0 < kHkv * (pre + mine_n + rc * mine_r)) {
@@ -524,7 +530,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
     __syncthreads();
     if (x0 >= total) return;  // more CTAs than work
     const int b0 = scan[kMmaThreads + 1];
-    cur.start(b0, scan[kMmaThreads + 2], lsh[b0], b0 + 1 < B ? lsh[b0 + 1] : 0, x0, min(x0 + q, total), q, rc);
+    cur.start(b0, scan[kMmaThreads + 2], lsh[b0], b0 + 1 < B ? lsh[b0 + 1] : 0, x0, min(x0 + q, total), q_sm, rc);
   } else {
     // one piece per CTA: split s of row (b, g)
     const int g = blockIdx.x, b = blockIdx.y, s = blockIdx.z;
