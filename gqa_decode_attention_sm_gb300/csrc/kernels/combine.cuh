@@ -48,7 +48,8 @@ struct CombineParams {
 // of pieces (the merge runs after stage 1 and before the next launch, so its
 // latency is the step's): every piece's max and denominator (lane k holds
 // the share's pieces k, k + 32, ...), then, per 32 pieces, all partial-output
-// vectors before any is accumulated.  Weights 2^(m_s - M) are formed once
+// vectors before any is accumulated; a share of up to 8 (or 16) pieces
+// issues both in one round.  Weights 2^(m_s - M) are formed once
 // per piece and broadcast with shuffles; pieces are accumulated in order
 // (deterministic).
 constexpr int kCombineChunks = 8;  // 32-piece chunks: 256 split slots, the most a workspace holds
@@ -75,12 +76,57 @@ __device__ __forceinline__ void accumulate_pieces(float4& o, const float4* pc, s
 
 // kMaxN: the most vectors one round may hold in registers (the kernel's
 // thread count sets the budget).
+// A share of at most kN pieces in a single round of loads: the partial
+// vectors go out with the maxima and denominators, before the weights exist.
+// The same arithmetic in the same order as the general path below, so the
+// result is the same bit for bit.
+template <int kN>
+__device__ __forceinline__ void merge_pieces_one_round(const CombineParams& p, size_t base, int cnt, int j, int W,
+                                                       float& M, float& Ls, float4& o) {
+  const int lane = threadIdx.x & 31;
+  const size_t stride = (size_t)W * (kD / 4);
+  const float4* po = reinterpret_cast<const float4*>(p.part_o) + (base + j) * (kD / 4) + lane;
+  float4 v[kN];
+#pragma unroll
+  for (int k = 0; k < kN; ++k) v[k] = po[(size_t)min(k, cnt - 1) * stride];
+  float m = -INFINITY, l = 0.f;
+  if (lane < cnt) {
+    m = p.part_m[base + j + (size_t)W * lane];
+    l = p.part_l[base + j + (size_t)W * lane];
+  }
+  M = m;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  const float w = m == -INFINITY ? 0.f : ex2(m - M);
+  Ls = fmaf(w, l, 0.f);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, off);
+  o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int k = 0; k < kN; ++k) {
+    const float wk = __shfl_sync(0xffffffffu, w, k);  // past the share's last piece the weight is 0
+    o.x = fmaf(wk, v[k].x, o.x);
+    o.y = fmaf(wk, v[k].y, o.y);
+    o.z = fmaf(wk, v[k].z, o.z);
+    o.w = fmaf(wk, v[k].w, o.w);
+  }
+}
+
 template <int kMaxN>
 __device__ __forceinline__ void merge_pieces(const CombineParams& p, size_t row, int n, int j, int W, float& M,
                                              float& Ls, float4& o) {
   const int lane = threadIdx.x & 31;
   const size_t base = row * p.num_splits;
   const int cnt = n > j ? (n - j + W - 1) / W : 0;  // this warp's pieces
+  // few pieces (warp-uniform): one round of loads instead of two
+  if (cnt >= 1 && cnt <= 8) {
+    merge_pieces_one_round<8>(p, base, cnt, j, W, M, Ls, o);
+    return;
+  }
+  if (kMaxN >= 16 && cnt > 8 && cnt <= 16) {
+    merge_pieces_one_round<(kMaxN >= 16 ? 16 : 8)>(p, base, cnt, j, W, M, Ls, o);
+    return;
+  }
   float wc[kCombineChunks];  // share piece 32c + lane: its max, then its weight
   float lc[kCombineChunks];  // its denominator
   M = -INFINITY;
