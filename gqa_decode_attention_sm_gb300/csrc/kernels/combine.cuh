@@ -74,8 +74,6 @@ __device__ __forceinline__ void accumulate_pieces(float4& o, const float4* pc, s
   }
 }
 
-// kMaxN: the most vectors one round may hold in registers (the kernel's
-// thread count sets the budget).
 // A share of at most kN pieces in a single round of loads: the partial
 // vectors go out with the maxima and denominators, before the weights exist.
 // The same arithmetic in the same order as the general path below, so the
@@ -112,6 +110,8 @@ __device__ __forceinline__ void merge_pieces_one_round(const CombineParams& p, s
   }
 }
 
+// kMaxN: the most vectors one round may hold in registers (the kernel's
+// thread count sets the budget).
 template <int kMaxN>
 __device__ __forceinline__ void merge_pieces(const CombineParams& p, size_t row, int n, int j, int W, float& M,
                                              float& Ls, float4& o) {
