@@ -114,7 +114,8 @@ def bytes_per_token(kv_dtype: str) -> int:
 
 
 def algorithmic_bytes(w, lens_list) -> int:
-    return sum(lens_list) * bytes_per_token(w.kv_dtype) + 2 * w.batch * 32 * 128 * 2 + 4 * w.batch
+    """KV bytes below the lengths, plus q and out (q_len query tokens each) and the lengths."""
+    return sum(lens_list) * bytes_per_token(w.kv_dtype) + 2 * w.batch * w.q_len * 32 * 128 * 2 + 4 * w.batch
 
 
 class ClockSampler:
@@ -448,7 +449,7 @@ def per_config_table(dev, peak, gq, inputs, quick=False, cpu=True):
         for _ in range(3):
             window()
         torch.cuda.synchronize()
-        nbytes = algorithmic_bytes(w, t["lens"].cpu().tolist()) + w.batch * 32 * 128 * 2 * 2  # 2x q and out
+        nbytes = algorithmic_bytes(w, t["lens"].cpu().tolist())  # q and out of both query tokens
         us = time_calls(window, 5 if quick else 20, flush=flush)
         table[f"{idx}-window2"] = {"us_per_call": round(us, 2), "GBps": round(nbytes / us / 1e3, 1),
                                    "frac_of_peak": round(nbytes / us / 1e3 / peak, 4), "alg_bytes": nbytes,
@@ -541,6 +542,7 @@ def run_gpu(args):
 
     from gqa_decode_attention_sm_gb300 import build as gbuild
     import gqa_decode_attention_sm_gb300 as gq
+    from gqa_decode_attention_sm_gb300 import api as gapi
     from gqa_decode_attention_sm_gb300 import inputs
 
     rank, world, local = dist_env()
@@ -561,22 +563,42 @@ def run_gpu(args):
         eight = args.kv_dtype in ("e4m3", "i8")
         w = inputs.with_(w, kv_dtype=args.kv_dtype, q_dtype="bf16" if eight else args.kv_dtype,
                          name=f"{w.name} with {args.kv_dtype} KV")
+    T = args.q_len
+    if T > 1:
+        w = inputs.with_(w, q_len=T, name=f"{w.name} with a {T}-token verify window")
     t = inputs.make(w, dev, seed=w.seed + 7919 * rank)
     lens_list = t["lens"].cpu().tolist()
     fp8 = w.kv_dtype == "e4m3"
     out = torch.empty_like(t["q"])
-    tensors = {"Q": t["q"], "KV": t["kv"], "O": out, "sequence_lengths": t["lens"]}
-    if t["kv_scales"] is not None:
-        tensors["KV_SCALES"] = t["kv_scales"]
-    p = gq.prepare(tensors, q_scale=t["q_scale"], k_scale=t["k_scale"] if fp8 else None,
-                   v_scale=t["v_scale"] if fp8 else None)
-    splits_eff = p.splits_effective
+    kvf = {"f16": gapi.KV_F16, "bf16": gapi.KV_BF16, "e4m3": gapi.KV_E4M3, "i8": gapi.KV_I8}[w.kv_dtype]
+    if T == 1:
+        tensors = {"Q": t["q"], "KV": t["kv"], "O": out, "sequence_lengths": t["lens"]}
+        if t["kv_scales"] is not None:
+            tensors["KV_SCALES"] = t["kv_scales"]
+        p = gq.prepare(tensors, q_scale=t["q_scale"], k_scale=t["k_scale"] if fp8 else None,
+                       v_scale=t["v_scale"] if fp8 else None)
+        num_splits, splits_eff = p.num_splits, p.splits_effective
+
+        def step():
+            gq.launch(p)
+    else:
+        # a verify window: both stages through gqa_decode_verify, one workspace
+        num_splits = gq.plan(w.batch, w.capacity, kvf, dev)
+        splits_eff = gapi.split_geometry(w.capacity, num_splits, kvf)[1]
+        ws = torch.zeros(gq.workspace_size(w.batch * T, w.capacity, num_splits), dtype=torch.uint8, device=dev)
+        kw = {"k_scale": t["k_scale"], "v_scale": t["v_scale"]} if fp8 else {}
+        if t["kv_scales"] is not None:
+            kw["kv_scales"] = t["kv_scales"]
+
+        def step():
+            gq.gqa_decode_verify(t["q"], t["kv"], t["lens"], q_scale=t["q_scale"], out=out,
+                                 num_splits=num_splits, workspace=ws, **kw)
     launches_per_step = 2 if splits_eff > 1 else 1
     nbytes = algorithmic_bytes(w, lens_list)
     stream = torch.cuda.current_stream(dev)
 
     for _ in range(max(3, args.warmup)):
-        gq.launch(p)
+        step()
     torch.cuda.synchronize(dev)
 
     clocks = ClockSampler(local).start()
@@ -591,16 +613,17 @@ def run_gpu(args):
     # during the split kernel's tail (programmatic dependent launch)
     start.record(stream)
     for _ in range(K):
-        gq.launch(p)
+        step()
     end.record(stream)
     torch.cuda.synchronize(dev)
     # the dominant kernel's own duration: the split kernel alone, each launch
-    # bracketed by events (stage 1 alone takes no int8 cache: there, the step)
+    # bracketed by events (stage 1 alone takes no int8 cache and no window:
+    # there, the step)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     for i in range(K):
         ev[i][0].record(stream)
-        if w.kv_dtype == "i8":
-            gq.launch(p)
+        if w.kv_dtype == "i8" or T > 1:
+            step()
         else:
             gq.split_stage(p)
         ev[i][1].record(stream)
@@ -667,7 +690,7 @@ def run_gpu(args):
             t["q"].copy_(hq, non_blocking=True)
             t["kv"].copy_(hkv, non_blocking=True)
             t["lens"].copy_(hlens, non_blocking=True)
-            gq.launch(p)
+            step()
             hout.copy_(out, non_blocking=True)
 
         e2e_step()
@@ -684,21 +707,22 @@ def run_gpu(args):
         e2e = {"value": round(all_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                "ms_per_step": round(e2e_ms, 3), "steps": ke, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": hout.numel() * hout.element_size(),
-               "path": "pinned host q/kv/lens -> H2D -> gqa_decode_prepared/fp8kv -> D2H out",
+               "path": "pinned host q/kv/lens -> H2D -> " +
+                       ("gqa_decode_prepared/fp8kv/int8kv" if T == 1 else "gqa_decode_verify") + " -> D2H out",
                "host_cpus": f"{min(cpus)}-{max(cpus)}", "h2d_probe_GBps": h2d_probe,
                "h2d_full_size_GBps": full_rates}
         del hq, hkv, hlens, hout
 
     achieved = nbytes / (split_ms * 1e-3) / 1e9
     # the committed capture is of the workload as defined (no batch or KV override)
-    traffic = traffic_per_launch(args.workload) if not (args.batch or args.kv_dtype) else None
+    traffic = traffic_per_launch(args.workload) if not (args.batch or args.kv_dtype or T > 1) else None
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": max(3, args.warmup), "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": w.name, "batch": w.batch, "capacity": w.capacity, "kv_dtype": w.kv_dtype,
-                   "q_dtype": w.q_dtype, "lengths": f"U[{w.len_lo},{w.len_hi}]" if w.len_lo != w.len_hi
-                   else w.len_lo, "num_splits": p.num_splits, "splits_effective": splits_eff,
+                   "q_dtype": w.q_dtype, "q_len": T, "lengths": f"U[{w.len_lo},{w.len_hi}]" if w.len_lo != w.len_hi
+                   else w.len_lo, "num_splits": num_splits, "splits_effective": splits_eff,
                    "alg_bytes_per_step_per_gpu": nbytes,
                    "l2": f"inputs ({nbytes / 1e9:.2f} GB) larger than L2 (129 MB); no flush between steps"
                    if nbytes > 2 * 129e6 else "inputs smaller than 2x L2: steps run warm",
@@ -714,7 +738,7 @@ def run_gpu(args):
         "clocks": clocks.summary(wall0, wall1),
         "e2e": e2e,
     }
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and T == 1:
         import oracle
         oracle.build()
         threads = oracle.default_threads()
@@ -773,6 +797,8 @@ def main(argv=None):
                     help="override the workload's batch (smaller cases for profiling)")
     ap.add_argument("--kv-dtype", choices=["f16", "bf16", "e4m3", "i8"], default=None,
                     help="override the workload's KV format (8-bit formats take a bf16 query)")
+    ap.add_argument("--q-len", type=int, default=1, choices=[1, 2, 3, 4],
+                    help="query tokens per request: above 1 the step is a verify window (gqa_decode_verify)")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-batch-rows", type=int, default=4,
                     help="batch rows (all 32 query heads each) in the oracle CPU-baseline sample")
