@@ -593,7 +593,9 @@ def run_gpu(args):
         def step():
             gq.gqa_decode_verify(t["q"], t["kv"], t["lens"], q_scale=t["q_scale"], out=out,
                                  num_splits=num_splits, workspace=ws, **kw)
-    launches_per_step = 2 if splits_eff > 1 else 1
+    # kernels per step, by the library's own rule (one when the splits merge on chip)
+    launches_per_step = gapi.launch_count(w.batch, w.capacity, kvf, T, num_splits,
+                                          torch.cuda.get_device_properties(dev).multi_processor_count)
     nbytes = algorithmic_bytes(w, lens_list)
     stream = torch.cuda.current_stream(dev)
 

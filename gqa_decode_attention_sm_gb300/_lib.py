@@ -16,7 +16,7 @@ _lock = threading.Lock()
 # Every extern "C" function declared in include/gqa_decode.h.
 EXPORTS = (
     "gqa_status_string", "gqa_last_error", "gqa_decode_workspace_size", "gqa_decode_plan",
-    "gqa_decode_plan_for", "gqa_decode_split_geometry",
+    "gqa_decode_plan_for", "gqa_decode_split_geometry", "gqa_decode_launch_count_for",
     "gqa_decode", "gqa_decode_prepared", "gqa_decode_fp8kv", "gqa_decode_split_stage",
     "gqa_decode_combine_stage", "gqa_decode_workspace_init", "gqa_decode_get_status",
     "gqa_decode_noalloc", "gqa_decode_debug_skip_tile", "gqa_decode_int8kv", "gqa_decode_paged",
@@ -41,6 +41,7 @@ def _declare(lib):
         "gqa_decode_plan_for": (i, [i, i, i, i, ctypes.POINTER(ctypes.c_int)]),
         "gqa_decode_split_geometry": (i, [i, i, i, ctypes.POINTER(ctypes.c_int),
                                           ctypes.POINTER(ctypes.c_int)]),
+        "gqa_decode_launch_count_for": (i, [i, i, i, i, i, i, ctypes.POINTER(ctypes.c_int)]),
         "gqa_decode": (i, [p, p, p, p, i, i, i, f, p]),
         "gqa_decode_prepared": (i, [p, p, p, p, i, i, i, f, i, p, sz, p]),
         "gqa_decode_fp8kv": (i, [p, p, p, p, i, i, f, f, f, i, p, sz, p]),

@@ -99,6 +99,15 @@ def split_geometry(capacity: int, num_splits: int, kv_format: int):
     return chunk.value, eff.value
 
 
+def launch_count(batch: int, capacity: int, kv_format: int, q_len: int, num_splits: int, sm_count: int) -> int:
+    """Kernels one decode call of these sizes enqueues: 1 (one split, or the
+    splits merged on chip in a thread-block cluster) or 2 (split + combine)."""
+    out = ctypes.c_int(0)
+    _lib.check(_lib.load().gqa_decode_launch_count_for(batch, capacity, kv_format, q_len, num_splits, sm_count,
+                                                       ctypes.byref(out)))
+    return out.value
+
+
 def gqa_decode(q, kv, sequence_lengths, q_scale: float = 1.0, out=None):
     """Convenience call: plans, takes a stream-ordered workspace, launches."""
     B, C = _geometry(q, kv, sequence_lengths)

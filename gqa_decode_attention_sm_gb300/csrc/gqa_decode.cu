@@ -701,6 +701,31 @@ gqa_status_t gqa_decode_split_geometry(int capacity, int num_splits, gqa_kv_form
   return GQA_OK;
 }
 
+gqa_status_t gqa_decode_launch_count_for(int batch, int capacity, gqa_kv_format_t kv_format, int q_len,
+                                        int num_splits, int sm_count, int* launches_out) {
+  if (!launches_out) return fail(GQA_ERR_INVALID_ARGUMENT, "launches_out is null");
+  gqa_status_t st = validate_shape(batch, capacity);
+  if (st != GQA_OK) return st;
+  if (kv_format != GQA_KV_F16 && kv_format != GQA_KV_BF16 && kv_format != GQA_KV_E4M3 &&
+      kv_format != GQA_KV_I8)
+    return fail(GQA_ERR_INVALID_ARGUMENT, "unknown KV format %d", (int)kv_format);
+  if (q_len < 1 || q_len > kMaxQLen) return fail(GQA_ERR_INVALID_ARGUMENT, "q_len %d outside [1, %d]", q_len, kMaxQLen);
+  if (num_splits < 1 || num_splits > GQA_MAX_SPLITS)
+    return fail(GQA_ERR_INVALID_ARGUMENT, "num_splits %d outside [1, %d]", num_splits, GQA_MAX_SPLITS);
+  if (sm_count < 1) return fail(GQA_ERR_INVALID_ARGUMENT, "sm_count %d < 1", sm_count);
+  // the same rules run_split / run_combine apply to a launch of these sizes
+  Call c{};
+  c.kv_format = (int)kv_format;
+  c.batch = batch;
+  c.capacity = capacity;
+  c.num_splits = num_splits;
+  c.q_len = q_len;
+  c.sms = sm_count;
+  const bool merged = split_count(capacity, num_splits, (int)kv_format) == 1 || cluster_splits(c) > 0;
+  *launches_out = merged ? 1 : 2;
+  return GQA_OK;
+}
+
 gqa_status_t gqa_decode_prepared(const void* q, const void* kv, const int32_t* lens, void* out, int batch,
                                  int capacity, gqa_dtype_t dtype, float q_scale, int num_splits,
                                  void* workspace, size_t workspace_bytes, void* stream) {

@@ -137,6 +137,15 @@ gqa_status_t gqa_decode_plan_for(int batch, int capacity, gqa_kv_format_t kv_for
 gqa_status_t gqa_decode_split_geometry(int capacity, int num_splits, gqa_kv_format_t kv_format,
                                        int* chunk_tokens_out, int* splits_effective_out);
 
+/* Kernels one decode call of these sizes enqueues on its stream (pure host
+ * arithmetic, no CUDA call): 1 when a single split holds every slot or the
+ * splits merge on chip in a thread-block cluster, else 2 (the split kernel
+ * and the combine).  The same for the contiguous and paged entries; q_len
+ * 1..4 as gqa_decode_verify; num_splits 1..GQA_MAX_SPLITS after resolving 0;
+ * sm_count < 1 is invalid.  Writes the count to *launches_out. */
+gqa_status_t gqa_decode_launch_count_for(int batch, int capacity, gqa_kv_format_t kv_format, int q_len,
+                                         int num_splits, int sm_count, int* launches_out);
+
 /* Convenience call (the article's sm110_gqa_decode): plans the split count,
  * takes a stream-ordered workspace with cudaMallocAsync/cudaFreeAsync on
  * `stream`, and launches.  q_scale must be finite and >= 0 (0 gives the mean

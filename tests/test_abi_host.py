@@ -135,6 +135,32 @@ def test_split_geometry(lib, C, S, fmt, chunk, eff):
     assert (a.value, b.value) == (chunk, eff) == (_chunk(C, S, fmt), -(-C // _chunk(C, S, fmt)))
 
 
+@pytest.mark.parametrize("B,C,fmt,T,S,launches", [
+    (1, 64, KV_F16, 1, 1, 1),            # one split: the split kernel writes the output
+    (1, 1024, KV_F16, 1, 8, 1),          # 8 splits, one wave: merged on chip in a cluster
+    (1, 1024, KV_F16, 4, 8, 1),          # the same with a 4-token window
+    (1, 1024, KV_F16, 1, 16, 2),         # 16 splits: more than a portable cluster holds
+    (8, 131072, KV_BF16, 1, 38, 2),      # balanced grid + combine
+    (32, 8192, KV_F16, 1, 10, 2),        # ragged workload shape: balanced + combine
+    (64, 32768, KV_E4M3, 1, 8, 2),       # 8-bit, balanced at 3 CTAs per SM
+    (1, 100, KV_F16, 1, 256, 1),         # 256 splits asked, 2 hold slots: cluster of 2
+])
+def test_launch_count(lib, B, C, fmt, T, S, launches):
+    n = ctypes.c_int(0)
+    assert lib.gqa_decode_launch_count_for(B, C, fmt, T, S, 152, ctypes.byref(n)) == OK
+    assert n.value == launches
+
+
+def test_launch_count_rejects_bad_arguments(lib):
+    n = ctypes.c_int(0)
+    assert lib.gqa_decode_launch_count_for(1, 64, KV_F16, 0, 1, 152, ctypes.byref(n)) == EINVAL
+    assert lib.gqa_decode_launch_count_for(1, 64, KV_F16, 5, 1, 152, ctypes.byref(n)) == EINVAL
+    assert lib.gqa_decode_launch_count_for(1, 64, KV_F16, 1, 0, 152, ctypes.byref(n)) == EINVAL
+    assert lib.gqa_decode_launch_count_for(1, 64, KV_F16, 1, 1, 0, ctypes.byref(n)) == EINVAL
+    assert lib.gqa_decode_launch_count_for(1, 64, 9, 1, 1, 152, ctypes.byref(n)) == EINVAL
+    assert lib.gqa_decode_launch_count_for(1, 64, KV_F16, 1, 1, 152, None) == EINVAL
+
+
 def test_plan_rejects_bad_arguments(lib):
     assert _plan(lib, 0, 64, KV_F16, 152)[0] == EINVAL
     assert _plan(lib, 1, 64, 7, 152)[0] == EINVAL
