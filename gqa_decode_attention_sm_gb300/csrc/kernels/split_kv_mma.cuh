@@ -102,12 +102,12 @@ __device__ __forceinline__ uint32_t pack_out(float a, float b) {
 constexpr int kMmaConsumerWarps = 4;
 constexpr int kMmaThreads = (kMmaConsumerWarps + 1) * 32;
 // Ring depth and residency: 8-bit KV does twice the arithmetic per byte, and
-// with one query token it fits in <= 136 registers, so 3 CTAs of 2 stages
-// share an SM (more warps to hide latency); 16-bit KV and verify windows use
-// 3 stages at 2 CTAs per SM (measured: bf16 streams fastest so, e4m3 is 2-3 %
-// faster at 3 CTAs).
-__host__ __device__ constexpr int mma_stages(int kvf, int nq) { return is_8bit(kvf) && nq == 1 ? 2 : 3; }
-__host__ __device__ constexpr int mma_ctas_per_sm(int kvf, int nq) { return is_8bit(kvf) && nq == 1 ? 3 : 2; }
+// with one or two query tokens (8 mma columns) it fits in <= 136 registers
+// without spills, so 3 CTAs of 2 stages share an SM (more warps to hide
+// latency); 16-bit KV and longer verify windows use 3 stages at 2 CTAs per
+// SM (measured: bf16 streams fastest so, e4m3 is 2-3 % faster at 3 CTAs).
+__host__ __device__ constexpr int mma_stages(int kvf, int nq) { return is_8bit(kvf) && nq <= 2 ? 2 : 3; }
+__host__ __device__ constexpr int mma_ctas_per_sm(int kvf, int nq) { return is_8bit(kvf) && nq <= 2 ? 3 : 2; }
 constexpr int kMaxQLen = 4;  // query tokens per request (a verify window when > 1)
 constexpr int kScaleStageBytes = 2 * 128 * 2;  // int8 cache: K and V row scales of one 128-token tile
 // Balanced schedule: batches up to this size (every CTA's prologue scans the
@@ -124,20 +124,22 @@ __host__ __device__ constexpr int mma_smem_bytes(int kvf, int nq, bool bal = fal
 // 228 KB of shared memory per SM, 1 KB of it reserved per resident CTA
 static_assert(2 * (mma_smem_bytes(kKvF16, kMaxQLen, true) + 1024) <= 228 * 1024 &&
                   2 * (mma_smem_bytes(kKvF16, 1, true) + 1024) <= 228 * 1024 &&
-                  3 * (mma_smem_bytes(kKvE4M3, 1, true) + 1024) <= 228 * 1024,
+                  3 * (mma_smem_bytes(kKvE4M3, 1, true) + 1024) <= 228 * 1024 &&
+                  3 * (mma_smem_bytes(kKvE4M3, 2, true) + 1024) <= 228 * 1024 &&
+                  2 * (mma_smem_bytes(kKvE4M3, kMaxQLen, true) + 1024) <= 228 * 1024,
               "the balanced schedule keeps its residency");
 // With one piece per CTA the epilogue merges the 4 warps' states in the ring
 // (idle by then): [warp][column][128] accumulators + [warp][column] max and
 // denominator.
-static_assert(kMmaConsumerWarps * kGroup * 1 * (kD + 2) * 4 <= mma_stages(kKvE4M3, 1) * kStageBytes &&
+static_assert(kMmaConsumerWarps * kGroup * 2 * (kD + 2) * 4 <= mma_stages(kKvE4M3, 2) * kStageBytes &&
                   kMmaConsumerWarps * kGroup * kMaxQLen * (kD + 2) * 4 <= mma_stages(kKvF16, kMaxQLen) * kStageBytes,
               "merge area must fit in the ring");
 
 // ... and the cluster merge's state [column][128] + max + denominator after it.
 static_assert(kMmaConsumerWarps * kGroup * kMaxQLen * (kD + 2) * 4 + kGroup * kMaxQLen * (kD + 2) * 4 <=
                       mma_stages(kKvF16, kMaxQLen) * kStageBytes &&
-                  kMmaConsumerWarps * kGroup * (kD + 2) * 4 + kGroup * (kD + 2) * 4 <=
-                      mma_stages(kKvE4M3, 1) * kStageBytes,
+                  kMmaConsumerWarps * kGroup * 2 * (kD + 2) * 4 + kGroup * 2 * (kD + 2) * 4 <=
+                      mma_stages(kKvE4M3, 2) * kStageBytes,
               "cluster merge state must fit in the ring");
 
 // ---------------------------------------------------------------- mma.sync
