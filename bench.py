@@ -436,15 +436,18 @@ def per_config_table(dev, peak, gq, inputs, quick=False, cpu=True):
     # a 2-token verify window (two queries per request read the cache once):
     # over workload 4, and over the ragged workload 3 (the balanced schedule)
     for idx, note in ((4, "workload 4 with a 2-token verify window (q_len 2, causal within the window)"),
-                      (3, "workload 3 (ragged, NaN tail) with a 2-token verify window")):
+                      (3, "workload 3 (ragged, NaN tail) with a 2-token verify window"),
+                      (5, "workload 5 (e4m3 KV) with a 2-token verify window")):
         w = inputs.with_(inputs.WORKLOADS[idx], q_len=2)
         t = inputs.make(w, dev)
         out = torch.empty_like(t["q"])
-        S = gq.plan(w.batch, w.capacity, 1, dev)
+        fp8 = w.kv_dtype == "e4m3"
+        S = gq.plan(w.batch, w.capacity, 2 if fp8 else 1, dev)
         ws = torch.zeros(gq.workspace_size(w.batch * 2, w.capacity, S), dtype=torch.uint8, device=dev)
+        scales = {"k_scale": t["k_scale"], "v_scale": t["v_scale"]} if fp8 else {}
 
         def window():
-            gq.gqa_decode_verify(t["q"], t["kv"], t["lens"], out=out, num_splits=S, workspace=ws)
+            gq.gqa_decode_verify(t["q"], t["kv"], t["lens"], out=out, num_splits=S, workspace=ws, **scales)
 
         for _ in range(3):
             window()
