@@ -158,6 +158,18 @@ def test_full_size_verify_window_sampled():
     _assert_parity(_gpu_rows(out)[rows], np.stack([ref[r] for r in rows]), "workload 4, window 2, sampled")
 
 
+def test_full_size_fp8_verify_window_sampled():
+    # workload 5 (e4m3 KV) with a 2-token window, as the per-workload table times
+    # it: 8-bit 2-token windows run 3 CTAs of 2 stages per SM
+    w = inputs.with_(inputs.WORKLOADS[5], q_len=2)
+    t = _make(w)
+    S = gq.plan(w.batch, w.capacity, 2, DEV)
+    out = _verify(t, num_splits=S)
+    ref = _oracle_units_window(t, [(0, 0), (29, 4), (63, 7)])
+    rows = sorted(ref)
+    _assert_parity(_gpu_rows(out)[rows], np.stack([ref[r] for r in rows]), "workload 5, window 2, sampled")
+
+
 def test_full_size_paged_int8_sampled():
     # the int8 cache of workload 5's shape in shuffled 256-token pages, as benchmarked
     w = inputs.custom(64, 32768, 16384, 32768, kv_dtype="i8", index=5)
