@@ -157,6 +157,33 @@ def make(w: Workload, device="cpu", seed: int | None = None, lens=None) -> dict:
                 v_scale=v_scale, kv_scales=kv_scales, workload=w)
 
 
+def make_row(w: Workload, b: int, device="cpu", seed: int | None = None) -> dict:
+    """Batch row ``b`` of ``make(w)``, drawn from the same generators without
+    building the other rows: q [1,32,128], kv [1,2,8,C,128], lens [1].
+
+    Only the 16-bit formats (f16, bf16): the e4m3 recipe needs one amax over
+    the whole cache.  Lets a CPU test use one row of a multi-GB workload."""
+    if w.kv_dtype not in _TORCH:
+        raise ValueError("make_row draws 16-bit caches only")
+    seed = w.seed if seed is None else int(seed)
+    device = torch.device(device)
+    B = w.batch
+    if w.len_lo == w.len_hi:
+        lens_t = torch.full((B,), w.len_lo, dtype=torch.int32)
+    else:
+        lens_t = torch.randint(w.len_lo, w.len_hi + 1, (B,), generator=_gen("cpu", seed),
+                               dtype=torch.int64).to(torch.int32)
+    q_shape = (B, HQ, D) if w.q_len == 1 else (B, w.q_len, HQ, D)
+    q = torch.randn(q_shape, generator=_gen(device, seed + 1), device=device,
+                    dtype=torch.float32).to(_TORCH[w.q_dtype])
+    kv = _kv_row_fp32(w, b, device, seed).to(_TORCH[w.kv_dtype]).unsqueeze(0)
+    lens_b = lens_t[b:b + 1].clone()
+    if w.nan_tail:
+        fill_tail(kv, lens_b, w.kv_dtype)
+    return dict(q=q[b:b + 1].clone(), kv=kv, lens=lens_b.to(device), q_scale=w.q_scale, k_scale=1.0,
+                v_scale=1.0, kv_scales=None, workload=w)
+
+
 def fill_tail(kv: torch.Tensor, lens, kv_dtype: str, value: float = float("nan")) -> None:
     """Overwrite every K and V slot t >= lens[b] with ``value`` (NaN by default).
 

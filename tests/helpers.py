@@ -84,3 +84,20 @@ def tolerance_ok(got: np.ndarray, ref: np.ndarray):
     allowed = np.where(np.abs(ref) > REL_FLOOR, np.maximum(ABS_TOL, REL_TOL * np.abs(ref)), ABS_TOL)
     excess = err - allowed
     return bool(np.all(excess <= 0) and np.all(np.isfinite(got))), float(err.max()), float(excess.max())
+
+
+# Second gate for long contexts.  There the outputs are averages of many V
+# rows and shrink like 1/sqrt(length) (about 4.6e-3 RMS at 131072 tokens), so
+# the absolute 3e-3 bar is most of the signal and would pass an output that
+# lost a whole split of the sequence (such a loss moves it by roughly
+# RMS / sqrt(splits)).  The kernels' own errors are about 1-2 % of the RMS,
+# set by the final fp16/bf16 rounding and the 16-bit softmax weights.
+RMS_GATE = 0.05
+
+
+def rms_gate_ok(got: np.ndarray, ref: np.ndarray, frac: float = RMS_GATE):
+    """max |got - ref| <= frac * RMS(ref); returns (ok, max error / RMS(ref))."""
+    rms = float(np.sqrt(np.mean(np.square(ref))))
+    err = float(np.max(np.abs(got - ref)))
+    ratio = err / rms if rms > 0 else (0.0 if err == 0 else float("inf"))
+    return bool(ratio <= frac and np.all(np.isfinite(got))), ratio

@@ -20,7 +20,7 @@ import torch
 import oracle
 import gqa_decode_attention_sm_gb300 as gq
 from gqa_decode_attention_sm_gb300 import api, inputs
-from helpers import HQ, bits_of, tolerance_ok
+from helpers import HQ, RMS_GATE, bits_of, rms_gate_ok, tolerance_ok
 
 pytestmark = pytest.mark.gpu
 
@@ -99,11 +99,15 @@ def _gpu_rows(out):
     return out.float().cpu().numpy().reshape(-1, 128)
 
 
-def _assert_parity(got, ref, what=""):
+def _assert_parity(got, ref, what="", rms_gate=False):
+    """The element-wise bar; with ``rms_gate`` also max |err| <= 0.05 RMS(ref)
+    (long contexts, where the absolute bar is most of the signal)."""
     ok, err, excess = tolerance_ok(got, ref)
-    rms = float(np.sqrt(np.mean(ref ** 2))) or 1.0
-    print(f"{what}: max|err| {err:.3e}, max err / rms(ref) {err / rms:.3e}")
+    gate_ok, ratio = rms_gate_ok(got, ref)
+    print(f"PARITY {what}: max|err| {err:.3e}, max err / rms(ref) {ratio:.3e}")
     assert ok, f"{what}: max |gpu - oracle| {err:.3e} exceeds the bar by {excess:.3e}"
+    if rms_gate:
+        assert gate_ok, f"{what}: max |gpu - oracle| is {ratio:.3e} of RMS(oracle), above {RMS_GATE}"
 
 
 # ---------------------------------------------------------------- workloads
@@ -113,7 +117,8 @@ def _assert_parity(got, ref, what=""):
 def test_workload_every_element(index):
     t = _make(inputs.WORKLOADS[index])
     p = _run(t)
-    _assert_parity(_gpu_rows(p.out), _oracle_full(t), f"workload {index} (splits {p.num_splits})")
+    _assert_parity(_gpu_rows(p.out), _oracle_full(t), f"workload {index} (splits {p.num_splits})",
+                   rms_gate=True)
 
 
 @pytest.mark.parametrize("index", [4, 5])
@@ -127,7 +132,7 @@ def test_full_size_workload_sampled(index):
     ref = _oracle_units(t, units)
     got = _gpu_rows(p.out)
     rows = sorted(ref)
-    _assert_parity(got[rows], np.stack([ref[r] for r in rows]), f"workload {index} sampled")
+    _assert_parity(got[rows], np.stack([ref[r] for r in rows]), f"workload {index} sampled", rms_gate=True)
     assert np.isfinite(got).all()
 
 
@@ -155,7 +160,8 @@ def test_full_size_verify_window_sampled():
     out = _verify(t)
     ref = _oracle_units_window(t, [(0, 0), (3, 5), (7, 7)])
     rows = sorted(ref)
-    _assert_parity(_gpu_rows(out)[rows], np.stack([ref[r] for r in rows]), "workload 4, window 2, sampled")
+    _assert_parity(_gpu_rows(out)[rows], np.stack([ref[r] for r in rows]), "workload 4, window 2, sampled",
+                   rms_gate=True)
 
 
 def test_full_size_fp8_verify_window_sampled():
@@ -167,7 +173,8 @@ def test_full_size_fp8_verify_window_sampled():
     out = _verify(t, num_splits=S)
     ref = _oracle_units_window(t, [(0, 0), (29, 4), (63, 7)])
     rows = sorted(ref)
-    _assert_parity(_gpu_rows(out)[rows], np.stack([ref[r] for r in rows]), "workload 5, window 2, sampled")
+    _assert_parity(_gpu_rows(out)[rows], np.stack([ref[r] for r in rows]), "workload 5, window 2, sampled",
+                   rms_gate=True)
 
 
 def test_full_size_paged_int8_sampled():
@@ -181,7 +188,8 @@ def test_full_size_paged_int8_sampled():
     out = _paged(pt)
     torch.cuda.synchronize()
     rows = sorted(ref)
-    _assert_parity(_gpu_rows(out)[rows], np.stack([ref[r] for r in rows]), "paged int8 full size, sampled")
+    _assert_parity(_gpu_rows(out)[rows], np.stack([ref[r] for r in rows]), "paged int8 full size, sampled",
+                   rms_gate=True)
 
 
 # ---------------------------------------------------------------- edge cases
@@ -239,6 +247,40 @@ def test_int8_large_q_sum_sharp_softmax(q_dtype, shift, q_scale):
         _assert_parity(_gpu_rows(p.out), _oracle_full(t), f"int8, q + {shift}, q_scale {q_scale}, splits={S}")
 
 
+@pytest.mark.parametrize("kv_dtype", ["e4m3", "i8"])
+@pytest.mark.parametrize("T", [1, 3])
+@pytest.mark.parametrize("case", ["huge", "tiny", "mixed"])
+def test_8bit_cache_takes_a_bf16_q_of_any_magnitude(kv_dtype, T, case):
+    # 8-bit caches run on f16 tensor cores, whose range (6e-8 .. 65504) a bf16
+    # q can leave; each query column is scaled by a power of two before its
+    # conversion, so q is taken exactly.  huge: |q| ~ 1e6 (a near one-hot
+    # softmax; saturating at 65504 would change which token wins).  tiny:
+    # |q| ~ 1e-7 with q_scale 2e7 (an ordinary softmax of q values below the
+    # f16 normal range).  mixed: head h at 10^(-7 + 13h/31), and element 0 of
+    # every vector 1e3 times its neighbours.  T = 3 runs two mma n-tiles.
+    B, C = 4, 704  # an int8 cache takes capacities that are multiples of 8
+    w = inputs.custom(B, C, 1, kv_dtype=kv_dtype, kv_std=2.0 if kv_dtype == "e4m3" else 1.0, nan_tail=True,
+                      q_len=T)
+    t = _make(w, lens=[T, 129, 500, 700])
+    g = torch.Generator(device=DEV)
+    g.manual_seed(7)
+    q = torch.randn(t["q"].shape, generator=g, device=DEV, dtype=torch.float32)
+    q_scale = 1.0
+    if case == "huge":
+        q *= 1e6
+    elif case == "tiny":
+        q *= 1e-7
+        q_scale = 2e7
+    else:
+        q *= (10.0 ** torch.linspace(-7, 6, HQ, device=DEV)).view(HQ, 1)
+        q[..., 0] *= 1e3
+    t["q"] = q.to(torch.bfloat16)
+    t["q_scale"] = q_scale
+    for S in (None, 1):
+        out = _verify(t, num_splits=S)
+        _assert_parity(_gpu_rows(out), _oracle_full(t), f"{kv_dtype} T={T} bf16 q {case} splits={S}")
+
+
 def test_int8_full_size_sampled():
     # the e4m3 workload's shape and length mix with an int8 cache (4.3 GB of codes)
     w = inputs.custom(64, 32768, 16384, 32768, kv_dtype="i8", index=5)
@@ -247,7 +289,8 @@ def test_int8_full_size_sampled():
     units = [(0, 0), (17, 3), (40, 6), (63, 7)]
     ref = _oracle_units(t, units)
     rows = sorted(ref)
-    _assert_parity(_gpu_rows(p.out)[rows], np.stack([ref[r] for r in rows]), "int8 64 x U[16k,32k] sampled")
+    _assert_parity(_gpu_rows(p.out)[rows], np.stack([ref[r] for r in rows]), "int8 64 x U[16k,32k] sampled",
+                   rms_gate=True)
 
 
 def test_bf16_every_element_multi_split():
@@ -314,7 +357,20 @@ def test_max_capacity_sampled():
         ref = _oracle_units(t, [(0, 0), (0, 5)])
         rows = sorted(ref)
         _assert_parity(_gpu_rows(p.out)[rows], np.stack([ref[r] for r in rows]),
-                       f"C=2^20 splits={p.num_splits}")
+                       f"C=2^20 splits={p.num_splits}", rms_gate=True)
+
+
+def test_long_request_sampled():
+    # one long request (bf16, batch 1, 131072 tokens), in the launch
+    # configuration the benchmark times: every KV head's row is cut into ~38
+    # pieces by the balanced schedule and merged by the combine kernel
+    w = inputs.custom(1, 131072, 131072, kv_dtype="bf16", index=4)
+    t = _make(w)
+    p = _run(t)
+    ref = _oracle_units(t, [(0, 0), (0, 2), (0, 5), (0, 7)])
+    rows = sorted(ref)
+    _assert_parity(_gpu_rows(p.out)[rows], np.stack([ref[r] for r in rows]),
+                   f"bf16 1 x 131072 splits={p.num_splits}", rms_gate=True)
 
 
 # ------------------------------------------- balanced schedule (many waves)
@@ -687,8 +743,8 @@ def test_paged_full_size_matches_oracle_and_contiguous():
     torch.cuda.synchronize()
     got = _gpu_rows(out)
     rows = sorted(ref)
-    _assert_parity(got[rows], np.stack([ref[r] for r in rows]), "paged full size, sampled")
-    _assert_parity(got, _gpu_rows(contiguous).astype(np.float64), "paged vs contiguous")
+    _assert_parity(got[rows], np.stack([ref[r] for r in rows]), "paged full size, sampled", rms_gate=True)
+    _assert_parity(got, _gpu_rows(contiguous).astype(np.float64), "paged vs contiguous", rms_gate=True)
 
 
 
@@ -843,8 +899,21 @@ def _vals(t):
     return t.float().cpu().numpy().astype(np.float64)
 
 
+def _ulps_apart(got_bits, ref_bits):
+    """Distance in units in the last place between 16-bit float patterns of
+    the same format (ordered by value; +0 and -0 coincide)."""
+    def ordered(b):
+        b = np.asarray(b, dtype=np.int64)
+        mag = b & 0x7FFF
+        return np.where(b & 0x8000, -mag, mag)
+    return np.abs(ordered(got_bits) - ordered(ref_bits))
+
+
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 def test_append_matches_oracle_and_touches_only_its_slot(dtype):
+    # An element-wise step rounded once: every q_out and K element must be the
+    # oracle's correctly rounded value or one of its two neighbours (the kernel
+    # rounds an FP32 value within ~2^-21 of exact; the oracle an FP64 one).
     B, C = 6, 300
     qp, kp, vp, wq, wk, pos, slots = _append_inputs(B, C, dtype, seed=1)
     kv = _make(inputs.custom(B, C, C, kv_dtype=dtype))["kv"]
@@ -853,10 +922,14 @@ def test_append_matches_oracle_and_touches_only_its_slot(dtype):
     torch.cuda.synchronize()
     qo, ko, vo = oracle.append_kv(_vals(qp), _vals(kp), _vals(vp), _vals(wq), _vals(wk),
                                   pos.cpu().numpy(), 1e-6, 1e6)
-    _assert_parity(_gpu_rows(q_out), qo.reshape(-1, 128), f"append q_out {dtype}")
+    fmt = FMT[dtype]
+    d_q = _ulps_apart(bits_of(q_out), oracle.round_to(qo, fmt))
+    assert d_q.max() <= 1, f"append q_out {dtype}: {int(d_q.max())} ulps from the oracle"
     sl = slots.cpu().tolist()
     k_new = torch.stack([kv[b, 0, :, sl[b]] for b in range(B)])
-    _assert_parity(_gpu_rows(k_new), ko.reshape(-1, 128), f"append k {dtype}")
+    d_k = _ulps_apart(bits_of(k_new), oracle.round_to(ko, fmt))
+    assert d_k.max() <= 1, f"append k {dtype}: {int(d_k.max())} ulps from the oracle"
+    print(f"PARITY append {dtype}: q_out {np.mean(d_q > 0):.2%}, k {np.mean(d_k > 0):.2%} of elements one ulp off")
     v_new = torch.stack([kv[b, 1, :, sl[b]] for b in range(B)])
     assert torch.equal(v_new.view(torch.int16), vp.view(torch.int16))
     for b in range(B):  # nothing else in the cache changed
