@@ -18,6 +18,15 @@
 // l holds dims l, l+32, l+64, l+96, so every RoPE pair (i, i+64) stays in one
 // lane.  The 64 angles are formed in FP64 (pos * theta^(-i/64) reaches 1e5
 // radians at long contexts, beyond FP32's reach) once per CTA.
+//
+// Precision: the result before its one rounding is within about 2^-21 of the
+// exact value relative to itself, so the stored fp16/bf16 value is the
+// correctly rounded one or its neighbour.  The rotation is linear, so it runs
+// on a = x * w (exact in FP32: two 16-bit significands) and the norm factor
+// r = 1/sqrt(mean(x^2) + eps) multiplies last.  The rotation would lose that
+// bound wherever a_i cos and a_{i+64} sin nearly cancel; it keeps it with cos
+// and sin held as FP32 hi + lo pairs and the rounding error of one product
+// recovered exactly by an FMA (rotate_pair).
 #pragma once
 
 #include "common.cuh"
@@ -66,9 +75,20 @@ __device__ __forceinline__ uint8_t to_e4m3(float x) {
   return (uint8_t)(two & 0xffu);
 }
 
+// a * c + b * s with c = ch + cl and s = sh + sl (FP32 hi/lo pairs of FP64
+// values): b * sh = pb + eb exactly (FMA), h = a * ch + pb rounded once, and
+// the small terms a * cl + b * sl + eb added last.  Error about 2^-23 of the
+// result, even when the two products nearly cancel.
+__device__ __forceinline__ float rotate_pair(float a, float ch, float cl, float b, float sh, float sl) {
+  const float pb = b * sh;
+  const float eb = fmaf(b, sh, -pb);
+  const float h = fmaf(a, ch, pb);
+  return h + fmaf(a, cl, fmaf(b, sl, eb));
+}
+
 template <int KVF, int QF>
 __global__ void __launch_bounds__(kAppendThreads) append_kv_kernel(const __grid_constant__ AppendParams p) {
-  __shared__ float cs[kD / 2], sn[kD / 2];
+  __shared__ float cs[kD / 2], cs_lo[kD / 2], sn[kD / 2], sn_lo[kD / 2];
   // the decode that follows may be scheduled now (it waits for this grid);
   // this grid waits for the previous one before its first read
   pdl_launch_dependents();
@@ -79,8 +99,11 @@ __global__ void __launch_bounds__(kAppendThreads) append_kv_kernel(const __grid_
     const double a = (double)pos * pow(p.theta, -(double)threadIdx.x / (kD / 2));
     double sv, cv;
     sincos(a, &sv, &cv);
-    cs[threadIdx.x] = (float)cv;
-    sn[threadIdx.x] = (float)sv;
+    const float ch = (float)cv, sh = (float)sv;
+    cs[threadIdx.x] = ch;
+    cs_lo[threadIdx.x] = (float)(cv - (double)ch);
+    sn[threadIdx.x] = sh;
+    sn_lo[threadIdx.x] = (float)(sv - (double)sh);
   }
   __syncthreads();
   const int C = p.capacity;
@@ -119,15 +142,17 @@ __global__ void __launch_bounds__(kAppendThreads) append_kv_kernel(const __grid_
       for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
       const float r = 1.f / sqrtf(ss / kD + p.eps);
       const void* w = is_q ? p.q_norm_w : p.k_norm_w;
-      float y[4];
+      float a[4];  // x * w, exact
 #pragma unroll
-      for (int k = 0; k < 4; ++k) y[k] = z[k] * r * load_elem<QF>(w, dims[k]);
+      for (int k = 0; k < 4; ++k) a[k] = z[k] * load_elem<QF>(w, dims[k]);
       // pairs (lane, lane+64) with angle lane, (lane+32, lane+96) with angle lane+32
-      const float c0 = cs[lane], s0 = sn[lane], c1 = cs[lane + 32], s1 = sn[lane + 32];
-      z[0] = y[0] * c0 - y[2] * s0;
-      z[2] = y[2] * c0 + y[0] * s0;
-      z[1] = y[1] * c1 - y[3] * s1;
-      z[3] = y[3] * c1 + y[1] * s1;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int i = lane + 32 * k;
+        const float ch = cs[i], cl = cs_lo[i], sh = sn[i], sl = sn_lo[i];
+        z[k] = r * rotate_pair(a[k], ch, cl, a[k + 2], -sh, -sl);
+        z[k + 2] = r * rotate_pair(a[k + 2], ch, cl, a[k], sh, sl);
+      }
     }
     if (is_q) {
       uint16_t* out = static_cast<uint16_t*>(p.q_out) + row;

@@ -41,9 +41,11 @@
 // offset comes off the scores (1152 * sum_d q_d per column, in the scale
 // step) and off the output accumulator (1152 * the column's summed f16
 // weights, every 16 tiles and at the piece's end); the tensor-core
-// type is then f16 and a bf16 q is converted to f16 once per CTA (exact for
-// 2^-17 <= |q| <= 65504; smaller magnitudes round to the f16 subnormal grid,
-// larger ones saturate).  fp16 and bf16 KV use their own type.  For the int8
+// type is then f16 and a bf16 q is converted to f16 once per piece after a
+// power-of-two scaling per query column (its largest magnitude brought to
+// [2^14, 2^15), the inverse folded into that column's score scale), so any
+// finite bf16 q is taken exactly down to 2^-31 of its column's maximum and
+// nothing saturates.  fp16 and bf16 KV use their own type.  For the int8
 // cache ("Qwen3-VL official BF16 on Jetson Orin (SM87)" docs, "INT8 KV cache
 // (kv_mode)": one bf16 scale per (position, KV head) row) the K row scale
 // multiplies that token's scores and the V row scale joins that token's
@@ -707,8 +709,17 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
       lim[nt] = jq < NQ ? min(t_end, L - NQ + 1 + jq) : 0;
     }
 
-    // Q^T B-fragments: column gq of each n-tile, unscaled (zero for padding).
+    // Q^T B-fragments: column gq of each n-tile (zero for padding).  A bf16 q
+    // meeting f16 tensor cores (8-bit KV) is first scaled by a power of two
+    // 2^e per column, chosen so that the column's largest |q| lands in
+    // [2^14, 2^15): every element of magnitude >= 2^-31 of that maximum is
+    // then exact in f16, the rest round on the f16 subnormal grid (2^-39 of
+    // the maximum at most), and nothing saturates.  The column's score scale
+    // takes 2^-e (sl2c below); power-of-two scaling commutes with FP32
+    // rounding, so a q already in f16 range scores bit for bit as unscaled.
+    constexpr bool kQPow2 = is_8bit(KVF) && QF == kQBF16;
     uint32_t qb[kNT][8][2];
+    float sl2c[kNT][2];  // score scale of this lane's columns 2cq, 2cq+1 (scale_log2 * 2^-e)
   #pragma unroll
     for (int nt = 0; nt < kNT; ++nt) {
       const int jq = 2 * nt + (gq >> 2);
@@ -718,12 +729,41 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
   #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
   #pragma unroll
-        for (int pr = 0; pr < 2; ++pr) {
-          const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(qrow + qk_dim<KVF>(cq, ks, pr)));
-          uint32_t v = w;
-          if constexpr (is_8bit(KVF) && QF == kQBF16) v = pack_f16_satfinite(bf16_lo_to_f32(w), bf16_hi_to_f32(w));
-          qb[nt][ks][pr] = real ? v : 0u;
-        }
+        for (int pr = 0; pr < 2; ++pr)
+          qb[nt][ks][pr] = __ldg(reinterpret_cast<const uint32_t*>(qrow + qk_dim<KVF>(cq, ks, pr)));
+      sl2c[nt][0] = sl2c[nt][1] = sl2;
+      if constexpr (kQPow2) {
+        // the column's largest magnitude, as bf16 bits (monotone in the value)
+        uint32_t amax = 0;
+  #pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+  #pragma unroll
+          for (int pr = 0; pr < 2; ++pr)
+            amax = max(amax, max(qb[nt][ks][pr] & 0x7fffu, (qb[nt][ks][pr] >> 16) & 0x7fffu));
+        amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));  // lanes 4gq..4gq+3 hold column gq
+        amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        // e = 14 - floor(log2 amax) from the biased exponent; amax below
+        // 2^-126 (bf16 subnormal) takes the largest e, 126; all zero takes 0
+        const int ebits = (int)(amax >> 7);
+        const int e = ebits > 0 ? min(141 - ebits, 126) : (amax ? 126 : 0);
+        const float up = __uint_as_float((uint32_t)(127 + e) << 23);    // 2^e
+        const float down = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e
+  #pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+  #pragma unroll
+          for (int pr = 0; pr < 2; ++pr) {
+            const uint32_t w = qb[nt][ks][pr];
+            qb[nt][ks][pr] = pack_f16_satfinite(bf16_lo_to_f32(w) * up, bf16_hi_to_f32(w) * up);
+          }
+        const float mine = sl2 * down;  // column gq's score scale
+        sl2c[nt][0] = __shfl_sync(0xffffffffu, mine, 8 * cq);      // column 2cq
+        sl2c[nt][1] = __shfl_sync(0xffffffffu, mine, 8 * cq + 4);  // column 2cq + 1
+      }
+  #pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+  #pragma unroll
+        for (int pr = 0; pr < 2; ++pr)
+          if (!real) qb[nt][ks][pr] = 0u;
     }
     // int8 K: score offset of each of this lane's columns (2cq, 2cq+1),
     // -1152 * sum_d q_d * scale_log2, added in the scale step (the K operand
@@ -743,8 +783,8 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
           }
         qs += __shfl_xor_sync(0xffffffffu, qs, 1);  // lanes 4n..4n+3 hold column n
         qs += __shfl_xor_sync(0xffffffffu, qs, 2);
-        kb[nt][0] = -kI8Bias * sl2 * __shfl_sync(0xffffffffu, qs, 8 * cq);
-        kb[nt][1] = -kI8Bias * sl2 * __shfl_sync(0xffffffffu, qs, 8 * cq + 4);
+        kb[nt][0] = -kI8Bias * sl2c[nt][0] * __shfl_sync(0xffffffffu, qs, 8 * cq);
+        kb[nt][1] = -kI8Bias * sl2c[nt][1] * __shfl_sync(0xffffffffu, qs, 8 * cq + 4);
       }
     }
 
@@ -829,8 +869,8 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
         for (int nt = 0; nt < kNT; ++nt) {
   #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            if constexpr (KVF == kKvI8) x[nt][e] = fmaf(sc[nt][e], sl2, kb[nt][e & 1]);
-            else x[nt][e] = sc[nt][e] * sl2;
+            if constexpr (KVF == kKvI8) x[nt][e] = fmaf(sc[nt][e], sl2c[nt][e & 1], kb[nt][e & 1]);
+            else x[nt][e] = sc[nt][e] * sl2c[nt][e & 1];
           }
           if constexpr (KVF == kKvI8) {  // per-row K scale multiplies that token's scores
             const float ks_a = row_scale(R + gq, 0), ks_b = row_scale(R + gq + 8, 0);
