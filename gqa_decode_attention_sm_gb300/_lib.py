@@ -19,7 +19,7 @@ EXPORTS = (
     "gqa_decode_plan_for", "gqa_decode_split_geometry", "gqa_decode_launch_count_for",
     "gqa_decode", "gqa_decode_prepared", "gqa_decode_fp8kv", "gqa_decode_split_stage",
     "gqa_decode_combine_stage", "gqa_decode_workspace_init", "gqa_decode_get_status",
-    "gqa_decode_noalloc", "gqa_decode_debug_skip_tile", "gqa_decode_int8kv", "gqa_decode_paged",
+    "gqa_decode_noalloc", "gqa_decode_noalloc_get_status", "gqa_decode_debug_skip_tile", "gqa_decode_int8kv", "gqa_decode_paged",
     "gqa_decode_verify", "gqa_append_kv", "gqa_append_kv_paged",
 )
 
@@ -50,6 +50,7 @@ def _declare(lib):
         "gqa_decode_workspace_init": (i, [p, sz, p]),
         "gqa_decode_get_status": (i, [p, sz, p, ctypes.POINTER(ctypes.c_uint32)]),
         "gqa_decode_noalloc": (i, [p, p, p, p, i, i, i, f, i, p]),
+        "gqa_decode_noalloc_get_status": (i, [p, ctypes.POINTER(ctypes.c_uint32)]),
         "gqa_decode_int8kv": (i, [p, p, p, p, p, i, i, i, f, i, p, sz, p]),
         "gqa_decode_paged": (i, [p, i, p, i, p, p, i, i, i, p, p, i, i, f, f, f, i, p, sz, p]),
         "gqa_decode_verify": (i, [p, i, p, i, p, p, p, i, i, i, f, f, f, i, p, sz, p]),

@@ -10,6 +10,7 @@
 // workspace owned by the caller.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -48,8 +49,12 @@ gqa_status_t cuda_fail(cudaError_t e, const char* what) {
 
 constexpr int kMaxDevices = 64;
 
+// Per-device result of the one-time check.  Kept once known for good: the
+// device is ready (sm_count set) or is not a compute capability 10.3 part.  A
+// CUDA error during the check is not kept, so a later call retries it.
 struct DeviceState {
-  std::once_flag once;
+  std::mutex mu;
+  std::atomic<int> state{0};  // 0 unknown, 1 ready, 2 unsupported
   gqa_status_t status = GQA_ERR_UNSUPPORTED_DEVICE;
   int sm_count = 0;
   std::string message;
@@ -119,8 +124,19 @@ void init_device(int dev, DeviceState& st) {
 gqa_status_t device_ready(int dev, int* sm_count) {
   if (dev < 0 || dev >= kMaxDevices) return fail(GQA_ERR_UNSUPPORTED_DEVICE, "device %d out of range", dev);
   DeviceState& st = g_devices[dev];
-  std::call_once(st.once, [&] { init_device(dev, st); });
-  if (st.status != GQA_OK) return fail(st.status, "%s", st.message.c_str());
+  int known = st.state.load(std::memory_order_acquire);
+  if (known == 0) {
+    std::lock_guard<std::mutex> lock(st.mu);
+    known = st.state.load(std::memory_order_relaxed);
+    if (known == 0) {
+      init_device(dev, st);
+      if (st.status == GQA_OK) known = 1;
+      else if (st.status == GQA_ERR_UNSUPPORTED_DEVICE) known = 2;
+      else return fail(st.status, "%s", st.message.c_str());  // not kept: retried next call
+      st.state.store(known, std::memory_order_release);
+    }
+  }
+  if (known == 2) return fail(GQA_ERR_UNSUPPORTED_DEVICE, "%s", st.message.c_str());
   if (sm_count) *sm_count = st.sm_count;
   return GQA_OK;
 }
@@ -248,19 +264,33 @@ constexpr size_t kStaticWorkspaceBytes = GQA_STATIC_WORKSPACE_BYTES;
 static __device__ __align__(256) unsigned char g_static_workspace[kStaticWorkspaceBytes];
 
 struct StaticWorkspace {
-  std::once_flag once;
-  cudaError_t err = cudaSuccess;
-  void* ptr = nullptr;
+  std::mutex mu;
+  std::atomic<void*> ptr{nullptr};  // set once set-up has succeeded on the device
 };
 StaticWorkspace g_static_ws[kMaxDevices];
 
-// Device address of the static scratch on the current device `dev`.
-gqa_status_t static_workspace(int dev, void** ptr) {
+// Device address of the static scratch on the current device `dev`.  Set-up
+// (the first successful call per device): look the address up and zero the
+// header (the status word) on `stream`.  Only a successful set-up is kept: a
+// failed lookup (no context yet, a transient error) is retried by the next
+// call.  The address stays valid for the life of the device's primary
+// context; it goes stale after cudaDeviceReset.
+gqa_status_t static_workspace(int dev, cudaStream_t stream, void** ptr) {
   if (dev < 0 || dev >= kMaxDevices) return fail(GQA_ERR_UNSUPPORTED_DEVICE, "device %d out of range", dev);
   StaticWorkspace& s = g_static_ws[dev];
-  std::call_once(s.once, [&] { s.err = cudaGetSymbolAddress(&s.ptr, g_static_workspace); });
-  if (s.err != cudaSuccess) return cuda_fail(s.err, "cudaGetSymbolAddress(static workspace)");
-  *ptr = s.ptr;
+  void* p = s.ptr.load(std::memory_order_acquire);
+  if (!p) {
+    std::lock_guard<std::mutex> lock(s.mu);
+    p = s.ptr.load(std::memory_order_relaxed);
+    if (!p) {
+      cudaError_t e = cudaGetSymbolAddress(&p, g_static_workspace);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static workspace)");
+      e = cudaMemsetAsync(p, 0, GQA_WORKSPACE_HEADER_BYTES, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(static workspace header)");
+      s.ptr.store(p, std::memory_order_release);
+    }
+  }
+  *ptr = p;
   return GQA_OK;
 }
 
@@ -974,7 +1004,7 @@ gqa_status_t gqa_decode_noalloc(const void* q, const void* kv, const int32_t* le
   st = device_ready(dev, &sms);
   if (st != GQA_OK) return st;
   void* ws = nullptr;
-  st = static_workspace(dev, &ws);
+  st = static_workspace(dev, c.stream, &ws);
   if (st != GQA_OK) return st;
   int S = num_splits;
   if (S == 0) {
@@ -987,9 +1017,8 @@ gqa_status_t gqa_decode_noalloc(const void* q, const void* kv, const int32_t* le
   c.workspace_bytes = kStaticWorkspaceBytes;
   st = validate(c, false, true);
   if (st != GQA_OK) return st;
-  // the status word accumulates with atomicOr: start every call from zero
-  e = cudaMemsetAsync(ws, 0, GQA_WORKSPACE_HEADER_BYTES, c.stream);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(static workspace header)");
+  // the status word (zeroed at set-up) accumulates over calls until
+  // gqa_decode_noalloc_get_status reads and clears it
   st = run_split(c);
   if (st != GQA_OK) return st;
   return run_combine(c);
@@ -1015,6 +1044,19 @@ gqa_status_t gqa_decode_get_status(void* workspace, size_t workspace_bytes, void
   if (e != cudaSuccess) return cuda_fail(e, "reading the workspace status word");
   *flags = host;
   return GQA_OK;
+}
+
+gqa_status_t gqa_decode_noalloc_get_status(void* stream, uint32_t* flags) {
+  if (!flags) return fail(GQA_ERR_INVALID_ARGUMENT, "flags must be non-null");
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  gqa_status_t st = device_ready(dev, nullptr);
+  if (st != GQA_OK) return st;
+  void* ws = nullptr;
+  st = static_workspace(dev, static_cast<cudaStream_t>(stream), &ws);
+  if (st != GQA_OK) return st;
+  return gqa_decode_get_status(ws, GQA_WORKSPACE_HEADER_BYTES, stream, flags);
 }
 
 }  // extern "C"

@@ -30,12 +30,13 @@
  * Pointers are device pointers unless stated.  `stream` is a cudaStream_t
  * (NULL = the legacy default stream).  Every launching call is asynchronous,
  * enqueues on `stream`, reads nothing back to the host and performs no host
- * synchronisation, except gqa_decode_get_status (documented there).
+ * synchronisation, except gqa_decode_get_status and
+ * gqa_decode_noalloc_get_status (documented there).
  *
  * Ownership: the caller owns every buffer (q, kv, lens, out, workspace).  The
  * library never frees caller memory and keeps no pointer past the call.  The
  * only library-owned state is a per-device cache of the device check and of
- * kernel attributes.
+ * kernel attributes, and the static scratch of gqa_decode_noalloc.
  *
  * Errors: every function validates its arguments before any CUDA call and
  * returns a gqa_status_t; no exception or abort crosses this ABI.  A
@@ -269,16 +270,22 @@ gqa_status_t gqa_decode_combine_stage(const int32_t* lens, void* out, gqa_dtype_
  * The split-KV scratch lives in a file-scope static __device__ array of
  * GQA_STATIC_WORKSPACE_BYTES (16 MiB) that every GPU which loads this library
  * holds until the process exits.  The caller still passes q, kv, lens and out.
- * This call performs no cudaMalloc, cudaFree or other allocation; it clears
- * the scratch header with cudaMemsetAsync and launches the two stages on
- * `stream`.
+ * This call performs no cudaMalloc, cudaFree or other allocation; it launches
+ * the two stages on `stream`.
  *
  * Set-up: the first call on a device (with that device current) looks up the
- * array's device address with cudaGetSymbolAddress and caches it; make that
- * first call before any stream capture.  Every call on a device shares the
- * one array, which keeps the last call's contents: calls that may overlap on
- * the GPU (different streams or graphs without ordering) race and corrupt
- * each other's results; order them on one stream.
+ * array's device address with cudaGetSymbolAddress, zeroes its 256-byte
+ * header (the status word) with cudaMemsetAsync on `stream`, and caches the
+ * address; make that first call before any stream capture.  A failed lookup
+ * is reported (GQA_ERR_CUDA) and retried by the next call.  The cached
+ * address belongs to the device's primary context: do not use this call (or
+ * gqa_decode_noalloc_get_status) on a device after cudaDeviceReset.  Every
+ * call on a device shares the one array, which keeps the last call's
+ * contents: calls that may overlap on the GPU (different streams or graphs
+ * without ordering) race and corrupt each other's results; order them on one
+ * stream.  The partials need no clearing (each call writes before it reads);
+ * the status flags (GQA_FLAG_LENGTH_CLAMPED, GQA_FLAG_WAIT_TIMEOUT) accumulate
+ * over calls until gqa_decode_noalloc_get_status reads and clears them.
  *
  * num_splits = 0 takes gqa_decode_plan's choice, lowered if needed to the
  * largest split count whose scratch fits the array.  An explicit num_splits
@@ -289,6 +296,14 @@ gqa_status_t gqa_decode_combine_stage(const int32_t* lens, void* out, gqa_dtype_
 gqa_status_t gqa_decode_noalloc(const void* q, const void* kv, const int32_t* lens, void* out,
                                 int batch, int capacity, gqa_dtype_t dtype, float q_scale,
                                 int num_splits, void* stream);
+
+/* The status word of the static scratch of gqa_decode_noalloc on the current
+ * device (GQA_FLAG_* bits, accumulated since set-up or the last read): copies
+ * it to *flags and clears it.  Like gqa_decode_get_status it synchronises
+ * `stream`, so it is for checks outside the hot path, never inside a
+ * capture.  Performs the static scratch's set-up if no call has yet (flags
+ * are then 0).  The pages have no counterpart to this call. */
+gqa_status_t gqa_decode_noalloc_get_status(void* stream, uint32_t* flags);
 
 /* Test hook for the failure path (not for production use).  Launches stage 1
  * exactly as gqa_decode_split_stage does, except that the producer never

@@ -126,6 +126,26 @@ def test_plan_invariants(lib, B, C, fmt):
     assert 1 <= splits_eff <= S
 
 
+def test_noalloc_auto_plan_fits_the_static_scratch(lib):
+    # gqa_decode_noalloc lowers an automatic split count whose scratch would
+    # not fit its 16 MiB static array.  On GB300's SM count (152; 160 for the
+    # full die) that lowering never triggers: the planner keeps
+    # batch x splits near the resident CTA count, and the largest automatic
+    # scratch over batches 1..65535 and capacities 1..2^30 is about 10 MB.  So
+    # the lowering loop is only a guard, and this pins why.
+    batches = sorted(set(range(1, 400)) | {456, 512, 1000, 1024, 1025, 4096, 65535})
+    caps = [1, 16, 64, 65, 129, 300, 1000, 1024, 4096, 8192, 32768, 131072, 1 << 20, 1 << 30]
+    for sms in (152, 160):
+        worst = 0
+        for fmt in (KV_F16, KV_BF16):
+            for B in batches:
+                for C in caps:
+                    st, S = _plan(lib, B, C, fmt, sms)
+                    assert st == OK
+                    worst = max(worst, lib.gqa_decode_workspace_size(B, C, S))
+        assert worst <= (16 << 20) * 0.7, (sms, worst)
+
+
 @pytest.mark.parametrize("C,S,fmt,chunk,eff", [(64, 1, KV_F16, 64, 1), (1024, 16, KV_F16, 64, 16),
                                                 (1000, 7, KV_F16, 192, 6), (1000, 256, KV_E4M3, 128, 8),
                                                 (131072, 19, KV_BF16, 6912, 19), (1, 3, KV_F16, 64, 1)])
@@ -332,3 +352,4 @@ def test_status_calls_validate(lib):
     assert lib.gqa_decode_get_status(WS, 16, None, ctypes.byref(flags)) == EINVAL
     assert lib.gqa_decode_workspace_init(None, 256, None) == EINVAL
     assert lib.gqa_decode_workspace_init(WS, 8, None) == EINVAL
+    assert lib.gqa_decode_noalloc_get_status(None, None) == EINVAL
