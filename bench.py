@@ -309,8 +309,8 @@ def near_host_cpus(dev):
     return groups[best], rates
 
 
-def time_calls(fn, n, flush=None, stream=None):
-    """Median us of `fn` over n calls, each bracketed by CUDA events (flush outside)."""
+def call_samples(fn, n, flush=None, stream=None):
+    """us of `fn` on each of n calls, each bracketed by CUDA events (flush outside)."""
     import torch
     res = []
     for _ in range(n):
@@ -322,8 +322,52 @@ def time_calls(fn, n, flush=None, stream=None):
         b.record(stream)
         b.synchronize()
         res.append(a.elapsed_time(b) * 1e3)
-    res.sort()
+    return sorted(res)
+
+
+def time_calls(fn, n, flush=None, stream=None):
+    """Median us of `fn` over n calls, each bracketed by CUDA events (flush outside)."""
+    res = call_samples(fn, n, flush, stream)
     return res[len(res) // 2]
+
+
+def timer_resolution_us(samples):
+    """The event timer's step as seen in the samples: the smallest gap between
+    two distinct values (event times on this GPU come in steps of ~2.05 us)."""
+    vals = sorted(set(round(x, 4) for x in samples))
+    gaps = [b - a for a, b in zip(vals, vals[1:]) if b - a > 1e-3]
+    return round(min(gaps), 3) if gaps else None
+
+
+def cold_graph_us(fn, flush, calls=40, reps=7):
+    """us per cold call below the event timer's step: one CUDA graph of
+    `calls` x (flush, fn) and one of `calls` x flush, each replayed `reps`
+    times between two events; the median difference over `calls`.  The
+    calls run as a graph does (no launch from the host between them)."""
+    import torch
+    graphs = []
+    for with_call in (True, False):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(calls):
+                flush()
+                if with_call:
+                    fn()
+        graphs.append(g)
+    for g in graphs:
+        g.replay()
+    torch.cuda.synchronize()
+    times = {True: [], False: []}
+    for _ in range(reps):
+        for g, key in zip(graphs, (True, False)):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            g.replay()
+            b.record()
+            b.synchronize()
+            times[key].append(a.elapsed_time(b) * 1e3)
+    med = lambda v: sorted(v)[len(v) // 2]  # noqa: E731
+    return (med(times[True]) - med(times[False])) / calls
 
 
 def sdpa_context(t, w, n, flush):
@@ -410,10 +454,20 @@ def per_config_table(dev, peak, gq, inputs, quick=False, cpu=True):
             gq.launch(p)
         torch.cuda.synchronize()
         n = 5 if quick else (20 if w.capacity * w.batch > 1 << 20 else 50)
-        us = time_calls(lambda: gq.launch(p), n, flush=flush)
+        samples = call_samples(lambda: gq.launch(p), n, flush=flush)
+        us = samples[len(samples) // 2]
         row = {"us_per_call": round(us, 2), "GBps": round(nbytes / us / 1e3, 1),
                "frac_of_peak": round(nbytes / us / 1e3 / peak, 4), "alg_bytes": nbytes,
-               "splits": p.num_splits, "l2": "cold (512 MB written, then 256 MB read, before each call)"}
+               "splits": p.num_splits, "l2": "cold (512 MB written, then 256 MB read, before each call)",
+               "us_per_call_mean": round(sum(samples) / len(samples), 3),
+               "timer_resolution_us": timer_resolution_us(samples)}
+        if w.batch * w.capacity <= 1 << 12:
+            # the latency-bound sizes take a few event steps: also time them
+            # below the step, as the difference of two CUDA graphs
+            cg = cold_graph_us(lambda: gq.launch(p), flush, calls=10 if quick else 40, reps=3 if quick else 7)
+            row["us_per_call_cold_graph"] = round(cg, 3)
+            row["cold_graph_note"] = ("(graph of 40 x [flush, call] - graph of 40 x flush) / 40, median of 7 "
+                                      "replays each: cold L2, launched from a graph; resolution ~0.1 us")
         if w.kv_dtype == "i8":
             row["note"] = "int8 codes + bf16 row scales, workload 5 shape (not one of the five workloads)"
         if w.kv_dtype in ("f16", "bf16"):
@@ -435,31 +489,54 @@ def per_config_table(dev, peak, gq, inputs, quick=False, cpu=True):
         torch.cuda.empty_cache()
     # a 2-token verify window (two queries per request read the cache once):
     # over workload 4, and over the ragged workload 3 (the balanced schedule)
-    for idx, note in ((4, "workload 4 with a 2-token verify window (q_len 2, causal within the window)"),
-                      (3, "workload 3 (ragged, NaN tail) with a 2-token verify window"),
-                      (5, "workload 5 (e4m3 KV) with a 2-token verify window")):
-        w = inputs.with_(inputs.WORKLOADS[idx], q_len=2)
-        t = inputs.make(w, dev)
+    # verify windows (T query tokens per request read the cache once): 2
+    # tokens over workloads 3-5, and 3 and 4 tokens over the 8-bit caches of
+    # workload 5's shape (e4m3, and int8 with bf16 row scales)
+    i8_w5 = inputs.custom(64, 32768, 16384, 32768, kv_dtype="i8", index=5)
+    window_rows = [(f"{i}-window2", inputs.with_(inputs.WORKLOADS[i], q_len=2), n) for i, n in (
+        (4, "workload 4 with a 2-token verify window (q_len 2, causal within the window)"),
+        (3, "workload 3 (ragged, NaN tail) with a 2-token verify window"),
+        (5, "workload 5 (e4m3 KV) with a 2-token verify window"))]
+    window_rows += [(f"5-window{T}", inputs.with_(inputs.WORKLOADS[5], q_len=T),
+                     f"workload 5 (e4m3 KV) with a {T}-token verify window") for T in (3, 4)]
+    window_rows += [(f"5-int8-window{T}", inputs.with_(i8_w5, q_len=T),
+                     f"int8 cache + bf16 row scales (workload 5 shape) with a {T}-token verify window")
+                    for T in (3, 4)]
+    made = {}
+    for key, w, note in window_rows:
+        base = (w.index, w.kv_dtype)
+        if base not in made:  # one cache per shape and format; the windows differ in q only
+            made.clear()
+            torch.cuda.empty_cache()
+            made[base] = inputs.make(inputs.with_(w, q_len=1), dev)
+        t = dict(made[base])
+        g = torch.Generator(device=dev)
+        g.manual_seed(w.seed + 1)
+        t["q"] = torch.randn((w.batch, w.q_len, 32, 128), generator=g, device=dev,
+                             dtype=torch.float32).to(torch.float16 if w.q_dtype == "f16" else torch.bfloat16)
         out = torch.empty_like(t["q"])
         fp8 = w.kv_dtype == "e4m3"
-        S = gq.plan(w.batch, w.capacity, 2 if fp8 else 1, dev)
-        ws = torch.zeros(gq.workspace_size(w.batch * 2, w.capacity, S), dtype=torch.uint8, device=dev)
+        fmt = {"f16": 0, "bf16": 1, "e4m3": 2, "i8": 3}[w.kv_dtype]
+        S = gq.plan(w.batch, w.capacity, fmt, dev)
+        ws = torch.zeros(gq.workspace_size(w.batch * w.q_len, w.capacity, S), dtype=torch.uint8, device=dev)
         scales = {"k_scale": t["k_scale"], "v_scale": t["v_scale"]} if fp8 else {}
 
         def window():
-            gq.gqa_decode_verify(t["q"], t["kv"], t["lens"], out=out, num_splits=S, workspace=ws, **scales)
+            gq.gqa_decode_verify(t["q"], t["kv"], t["lens"], out=out, num_splits=S, workspace=ws,
+                                 kv_scales=t["kv_scales"], **scales)
 
         for _ in range(3):
             window()
         torch.cuda.synchronize()
-        nbytes = algorithmic_bytes(w, t["lens"].cpu().tolist())  # q and out of both query tokens
+        nbytes = algorithmic_bytes(w, t["lens"].cpu().tolist())  # q and out of every query token
         us = time_calls(window, 5 if quick else 20, flush=flush)
-        table[f"{idx}-window2"] = {"us_per_call": round(us, 2), "GBps": round(nbytes / us / 1e3, 1),
-                                   "frac_of_peak": round(nbytes / us / 1e3 / peak, 4), "alg_bytes": nbytes,
-                                   "splits": S, "l2": "cold (512 MB written, then 256 MB read, before each call)",
-                                   "note": note}
+        table[key] = {"us_per_call": round(us, 2), "GBps": round(nbytes / us / 1e3, 1),
+                      "frac_of_peak": round(nbytes / us / 1e3 / peak, 4), "alg_bytes": nbytes,
+                      "splits": S, "l2": "cold (512 MB written, then 256 MB read, before each call)",
+                      "note": note}
         del t, out, ws
-        torch.cuda.empty_cache()
+    made.clear()
+    torch.cuda.empty_cache()
 
     # a paged cache: workload 4 scattered over a shuffled pool of 256-token pages
     w = inputs.WORKLOADS[4]
