@@ -8,7 +8,7 @@ loop of K launches of stage 1 alone, each bracketed by events.  The headline wor
 (batch 8, 32 q / 8 KV heads, head_dim 128, capacity = length = 131072: 4.3 GB
 of KV per step, far larger than the 129 MB L2, so no flush is needed between
 steps).  Every workload's us/call and GB/s are reported in ``per_config``
-(cold L2: a 512 MB buffer is written and a 256 MB one read before each timed
+(cold L2: a 512 MB buffer is written and a 1 GB one read before each timed
 call, so the L2 holds none of the inputs and no dirty lines).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 4]
@@ -92,16 +92,19 @@ def measured_peak():
 
 
 def traffic_per_launch(workload_index: int):
-    """DRAM bytes per split-kernel launch from the committed ncu summary, if it
-    was taken on the current kernel source and this workload; else None."""
+    """DRAM bytes per split-kernel launch of this workload from the committed
+    ncu summary, and how they were obtained, if the summary was taken on the
+    current kernel source; else (None, None).  The capture may be of a
+    smaller case of the same kernel (one batch row), scaled to the full
+    workload by the units processed; the summary states the factor."""
     try:
         with open(TRAFFIC_FILE) as f:
             d = json.load(f)
     except (OSError, ValueError):
-        return None
+        return None, None
     if d.get("source_hash") != kernel_source_hash() or d.get("workload") != workload_index:
-        return None
-    return d.get("dram_bytes_per_launch")
+        return None, None
+    return d.get("dram_bytes_per_launch"), d.get("note")
 
 
 def bytes_per_token(kv_dtype: str) -> int:
@@ -424,15 +427,22 @@ def oracle_config(t, w, nbytes, reps):
                                                                              "; us_per_call scaled by bytes")}
 
 
+L2_COLD = "cold (512 MB written, then 1 GB read, before each call)"
+
+
 def per_config_table(dev, peak, gq, inputs, quick=False, cpu=True):
     import torch
     flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
-    clean_buf = torch.ones(64 << 20, dtype=torch.float32, device=dev)  # 256 MB
+    clean_buf = torch.ones(256 << 20, dtype=torch.float32, device=dev)  # 1 GB
 
     def flush():
         # Write a buffer larger than L2 (cold for the inputs), then read another
         # one so the L2 holds clean lines: the timed call should not pay for
-        # writing back the flush's dirty lines.
+        # writing back the flush's dirty lines.  The read is 1 GB (8x L2): after
+        # a 256 MB read some dirty lines were still resident, and the timed
+        # call paid for writing them back (per-CTA timelines on GB300: a wider
+        # tail, +6 us on workload 3, +13 us on workload 4; 512 MB or more, or no
+        # write at all, removed it).
         flush_buf.fill_(1)
         clean_buf.max()
 
@@ -458,7 +468,7 @@ def per_config_table(dev, peak, gq, inputs, quick=False, cpu=True):
         us = samples[len(samples) // 2]
         row = {"us_per_call": round(us, 2), "GBps": round(nbytes / us / 1e3, 1),
                "frac_of_peak": round(nbytes / us / 1e3 / peak, 4), "alg_bytes": nbytes,
-               "splits": p.num_splits, "l2": "cold (512 MB written, then 256 MB read, before each call)",
+               "splits": p.num_splits, "l2": L2_COLD,
                "us_per_call_mean": round(sum(samples) / len(samples), 3),
                "timer_resolution_us": timer_resolution_us(samples)}
         if w.batch * w.capacity <= 1 << 12:
@@ -532,7 +542,7 @@ def per_config_table(dev, peak, gq, inputs, quick=False, cpu=True):
         us = time_calls(window, 5 if quick else 20, flush=flush)
         table[key] = {"us_per_call": round(us, 2), "GBps": round(nbytes / us / 1e3, 1),
                       "frac_of_peak": round(nbytes / us / 1e3 / peak, 4), "alg_bytes": nbytes,
-                      "splits": S, "l2": "cold (512 MB written, then 256 MB read, before each call)",
+                      "splits": S, "l2": L2_COLD,
                       "note": note}
         del t, out, ws
     made.clear()
@@ -558,7 +568,7 @@ def per_config_table(dev, peak, gq, inputs, quick=False, cpu=True):
     us = time_calls(paged, 5 if quick else 20, flush=flush)
     table["4-paged"] = {"us_per_call": round(us, 2), "GBps": round(nbytes / us / 1e3, 1),
                         "frac_of_peak": round(nbytes / us / 1e3 / peak, 4), "alg_bytes": nbytes, "splits": S,
-                        "l2": "cold (512 MB written, then 256 MB read, before each call)",
+                        "l2": L2_COLD,
                         "note": "workload 4 in a shuffled pool of 256-token pages (block table)"}
     del t, pt, out, ws
     torch.cuda.empty_cache()
@@ -583,7 +593,7 @@ def per_config_table(dev, peak, gq, inputs, quick=False, cpu=True):
     us = time_calls(paged_i8, 5 if quick else 20, flush=flush)
     table["5-int8-paged"] = {"us_per_call": round(us, 2), "GBps": round(nbytes / us / 1e3, 1),
                              "frac_of_peak": round(nbytes / us / 1e3 / peak, 4), "alg_bytes": nbytes, "splits": S,
-                             "l2": "cold (512 MB written, then 256 MB read, before each call)",
+                             "l2": L2_COLD,
                              "note": "int8 codes + bf16 row scales (workload 5 shape) in shuffled 256-token pages"}
     del t, pt, out, ws
     torch.cuda.empty_cache()
@@ -610,7 +620,7 @@ def per_config_table(dev, peak, gq, inputs, quick=False, cpu=True):
     torch.cuda.synchronize()
     table["bf16-1x131072"] = {"us_per_call": round(us, 2), "GBps": round(nbytes / us / 1e3, 1),
                               "frac_of_peak": round(nbytes / us / 1e3 / peak, 4), "alg_bytes": nbytes,
-                              "splits": p.num_splits, "l2": "cold (512 MB written, then 256 MB read, before each call)",
+                              "splits": p.num_splits, "l2": L2_COLD,
                               "us_per_call_back_to_back": round(a.elapsed_time(b) / 20 * 1e3, 2),
                               "note": "one long request: batch 1, 131072 bf16 tokens"}
     return table
@@ -797,7 +807,8 @@ def run_gpu(args):
 
     achieved = nbytes / (split_ms * 1e-3) / 1e9
     # the committed capture is of the workload as defined (no batch or KV override)
-    traffic = traffic_per_launch(args.workload) if not (args.batch or args.kv_dtype or T > 1) else None
+    traffic, traffic_note = (traffic_per_launch(args.workload) if not (args.batch or args.kv_dtype or T > 1)
+                             else (None, None))
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": max(3, args.warmup), "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
@@ -814,7 +825,7 @@ def run_gpu(args):
         "roofline": {"bound": "hbm", "kernel": "split_kv_mma_kernel", "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs (copy, burst)", "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "frac_of_nominal_7900": round(achieved / NOMINAL_HBM_GBS, 4),
-                     "traffic": traffic, "kernel_ms": round(split_ms, 4),
+                     "traffic": traffic, "traffic_note": traffic_note, "kernel_ms": round(split_ms, 4),
                      "alg_bytes_per_launch": nbytes},
         "gpu_launches": K * launches_per_step,
         "clocks": clocks.summary(wall0, wall1),

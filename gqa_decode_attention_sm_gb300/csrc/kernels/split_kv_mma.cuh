@@ -34,7 +34,7 @@
 //   output  O^T[128 dims x 8] += V^T[128 x 16 tokens] . P^T[16 x 8] as 8 mma
 //           (one per 16-dim m-tile).  Each lane reads 16 contiguous dims of 4
 //           token rows and pairs tokens with byte permutes; P^T reaches the
-//           B-fragment layout through 4 shuffles.  bf16 P is split into a
+//           B-fragment layout by two 8x8 transposes (movmatrix).  bf16 P is split into a
 //           high and a low bf16 part (two mma) so the weights keep ~16 bits.
 // e4m3 K/V are widened with the hardware cvt (e4m3x2 -> f16x2, exact), int8
 // codes with byte permutes to the f16 integer code + 1152 (exact); the
@@ -162,6 +162,16 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
   }
+}
+
+// Transpose of an 8x8 matrix of 16-bit elements spread over the warp, lane i
+// holding row i/4, columns 2(i%4) and 2(i%4)+1 (low half first): lane i gets
+// row i/4 of the transpose.  The score accumulator's packed weights (rows =
+// tokens, columns = query columns) become the P^T B-fragment this way.
+__device__ __forceinline__ uint32_t transpose8x8_b16(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
 }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
@@ -691,8 +701,6 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
   const int gq = lane >> 2, cq = lane & 3;
   const float sl2 = p.scale_log2;
   // P^T shuffle sources: tokens 2cq and 2cq+1 of the slab, column pair gq/2
-  const int src0 = 4 * (2 * cq) + (gq >> 1), src1 = 4 * (2 * cq + 1) + (gq >> 1);
-  const uint32_t half_sel = (gq & 1) ? 0x7632u : 0x5410u;
   bool alive = true;  // false once a wait has run out: the remaining tiles are skipped
   int it = 0;         // this CTA's tiles over all its pieces (ring stage and phase)
   Piece pc;
@@ -921,8 +929,9 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
         }
 
         // ---- P^T B-fragments per n-tile: lane (gq, cq) needs column gq of tokens
-        // 2cq, 2cq+1 (b0) and 2cq+8, 2cq+9 (b1), held by lanes src0/src1 as
-        // (column pair) packs.
+        // 2cq, 2cq+1 (b0) and 2cq+8, 2cq+9 (b1); the packed weights hold
+        // (token gq, columns 2cq, 2cq+1) and (token gq+8, ...): one 8x8
+        // transpose each.
         uint32_t bh[kNT][2], bl[kNT][2];
   #pragma unroll
         for (int nt = 0; nt < kNT; ++nt) {
@@ -937,10 +946,10 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
             const uint32_t pl_b = pack_bf16(p2 - bf16_lo_to_f32(ph_b), p3 - bf16_hi_to_f32(ph_b));
             l[nt][0] += bf16_lo_to_f32(ph_a) + bf16_lo_to_f32(pl_a) + bf16_lo_to_f32(ph_b) + bf16_lo_to_f32(pl_b);
             l[nt][1] += bf16_hi_to_f32(ph_a) + bf16_hi_to_f32(pl_a) + bf16_hi_to_f32(ph_b) + bf16_hi_to_f32(pl_b);
-            bh[nt][0] = prmt(__shfl_sync(0xffffffffu, ph_a, src0), __shfl_sync(0xffffffffu, ph_a, src1), half_sel);
-            bh[nt][1] = prmt(__shfl_sync(0xffffffffu, ph_b, src0), __shfl_sync(0xffffffffu, ph_b, src1), half_sel);
-            bl[nt][0] = prmt(__shfl_sync(0xffffffffu, pl_a, src0), __shfl_sync(0xffffffffu, pl_a, src1), half_sel);
-            bl[nt][1] = prmt(__shfl_sync(0xffffffffu, pl_b, src0), __shfl_sync(0xffffffffu, pl_b, src1), half_sel);
+            bh[nt][0] = transpose8x8_b16(ph_a);
+            bh[nt][1] = transpose8x8_b16(ph_b);
+            bl[nt][0] = transpose8x8_b16(pl_a);
+            bl[nt][1] = transpose8x8_b16(pl_b);
           } else if constexpr (KVF == kKvI8) {
             // the per-row V scale joins the weight of its token; the denominator
             // keeps the unscaled weights
@@ -953,8 +962,8 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
             const float2 fa = f16x2_to_f32x2(pa), fb = f16x2_to_f32x2(pb);
             vw[nt][0] += fa.x + fb.x;
             vw[nt][1] += fa.y + fb.y;
-            bh[nt][0] = prmt(__shfl_sync(0xffffffffu, pa, src0), __shfl_sync(0xffffffffu, pa, src1), half_sel);
-            bh[nt][1] = prmt(__shfl_sync(0xffffffffu, pb, src0), __shfl_sync(0xffffffffu, pb, src1), half_sel);
+            bh[nt][0] = transpose8x8_b16(pa);
+            bh[nt][1] = transpose8x8_b16(pb);
           } else {
             const uint32_t pa = pack_f16(p0, p1), pb = pack_f16(p2, p3);
             // the denominator sums the same rounded weights the tensor core multiplies
@@ -962,8 +971,8 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
             const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&pb));
             l[nt][0] += fa.x + fb.x;
             l[nt][1] += fa.y + fb.y;
-            bh[nt][0] = prmt(__shfl_sync(0xffffffffu, pa, src0), __shfl_sync(0xffffffffu, pa, src1), half_sel);
-            bh[nt][1] = prmt(__shfl_sync(0xffffffffu, pb, src0), __shfl_sync(0xffffffffu, pb, src1), half_sel);
+            bh[nt][0] = transpose8x8_b16(pa);
+            bh[nt][1] = transpose8x8_b16(pb);
           }
         }
 
