@@ -335,11 +335,17 @@ def time_calls(fn, n, flush=None, stream=None):
 
 
 def timer_resolution_us(samples):
-    """The event timer's step as seen in the samples: the smallest gap between
-    two distinct values (event times on this GPU come in steps of ~2.05 us)."""
+    """(The event timer's resolution as seen in the samples: the smallest gap
+    between two distinct values; the share of samples equal to the median).
+    The timer resolves 32 ns, but a cold call's event interval on this GPU
+    mostly lands on whole multiples of 2.048 us (most samples of the small
+    workloads are exactly 8.192 or 10.24 us), so their medians cannot show
+    changes below that step: cold_graph_us measures those calls instead."""
     vals = sorted(set(round(x, 4) for x in samples))
-    gaps = [b - a for a, b in zip(vals, vals[1:]) if b - a > 1e-3]
-    return round(min(gaps), 3) if gaps else None
+    gaps = [round(b - a, 3) for a, b in zip(vals, vals[1:]) if b - a > 1e-3]
+    med = sorted(samples)[len(samples) // 2]
+    at_median = sum(1 for x in samples if abs(x - med) < 1e-4) / len(samples)
+    return (min(gaps) if gaps else None), round(at_median, 3)
 
 
 def cold_graph_us(fn, flush, calls=40, reps=7):
@@ -469,13 +475,14 @@ def per_config_table(dev, peak, gq, inputs, quick=False, cpu=True):
         row = {"us_per_call": round(us, 2), "GBps": round(nbytes / us / 1e3, 1),
                "frac_of_peak": round(nbytes / us / 1e3 / peak, 4), "alg_bytes": nbytes,
                "splits": p.num_splits, "l2": L2_COLD,
-               "us_per_call_mean": round(sum(samples) / len(samples), 3),
-               "timer_resolution_us": timer_resolution_us(samples)}
+               "us_per_call_mean": round(sum(samples) / len(samples), 3)}
+        row["timer_resolution_us"], row["samples_at_median"] = timer_resolution_us(samples)
         if w.batch * w.capacity <= 1 << 12:
             # the latency-bound sizes take a few event steps: also time them
             # below the step, as the difference of two CUDA graphs
             cg = cold_graph_us(lambda: gq.launch(p), flush, calls=10 if quick else 40, reps=3 if quick else 7)
             row["us_per_call_cold_graph"] = round(cg, 3)
+            row["event_samples_us"] = [round(x, 3) for x in samples]
             row["cold_graph_note"] = ("(graph of 40 x [flush, call] - graph of 40 x flush) / 40, median of 7 "
                                       "replays each: cold L2, launched from a graph; resolution ~0.1 us")
         if w.kv_dtype == "i8":
