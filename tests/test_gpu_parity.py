@@ -177,6 +177,39 @@ def test_full_size_fp8_verify_window_sampled():
                    rms_gate=True)
 
 
+@pytest.mark.parametrize("kv_dtype,T", [("e4m3", 3), ("i8", 4)])
+def test_full_size_8bit_long_window_sampled(kv_dtype, T):
+    # 3- and 4-token windows over an 8-bit cache of workload 5's shape, as the
+    # per-workload table times them: the balanced schedule, two mma n-tiles,
+    # 2 CTAs of 3 stages per SM
+    base = inputs.WORKLOADS[5] if kv_dtype == "e4m3" else inputs.custom(64, 32768, 16384, 32768, kv_dtype="i8",
+                                                                          index=5)
+    w = inputs.with_(base, q_len=T)
+    t = _make(w)
+    fmt = {"e4m3": 2, "i8": 3}[kv_dtype]
+    out = _verify(t, num_splits=gq.plan(w.batch, w.capacity, fmt, DEV))
+    units = [(0, 0), (21, 6), (63, 7)]
+    ref = {}
+    for b, g in units:
+        kvb = np.zeros((1, 2, 8, w.capacity, 128), dtype=np.uint8)
+        kvb[0, :, g] = bits_of(t["kv"][b, :, g])
+        extra = {}
+        if t.get("kv_scales") is not None:
+            scb = np.zeros((1, 2, 8, w.capacity), dtype=np.uint16)
+            scb[0, :, g] = bits_of(t["kv_scales"][b, :, g])
+            extra["kv_scales"] = scb
+        rows = [jt * HQ + 4 * g + j for jt in range(T) for j in range(4)]
+        o, _ = oracle.gqa_decode(bits_of(t["q"][b:b + 1]), FMT[w.q_dtype], kvb, FMT[kv_dtype],
+                                 t["lens"].cpu().numpy()[b:b + 1], q_scale=t["q_scale"], k_scale=t["k_scale"],
+                                 v_scale=t["v_scale"], rows=rows, **extra)
+        for k, r in enumerate(rows):
+            ref[b * T * HQ + r] = o[k]
+    rows = sorted(ref)
+    _assert_parity(_gpu_rows(out)[rows], np.stack([ref[r] for r in rows]),
+                   f"{kv_dtype} 64 x U[16k,32k], window {T}, sampled", rms_gate=True)
+    assert np.isfinite(_gpu_rows(out)).all()
+
+
 def test_full_size_paged_int8_sampled():
     # the int8 cache of workload 5's shape in shuffled 256-token pages, as benchmarked
     w = inputs.custom(64, 32768, 16384, 32768, kv_dtype="i8", index=5)
