@@ -104,10 +104,13 @@ __device__ __forceinline__ uint32_t pack_out(float a, float b) {
 constexpr int kMmaConsumerWarps = 4;
 constexpr int kMmaThreads = (kMmaConsumerWarps + 1) * 32;
 // Ring depth and residency: 8-bit KV does twice the arithmetic per byte, and
-// with one or two query tokens (8 mma columns) it fits in <= 136 registers
+// with one or two query tokens (8 mma columns) it fits in <= 128 registers
 // without spills, so 3 CTAs of 2 stages share an SM (more warps to hide
 // latency); 16-bit KV and longer verify windows use 3 stages at 2 CTAs per
 // SM (measured: bf16 streams fastest so, e4m3 is 2-3 % faster at 3 CTAs).
+// (A warp's registers come from one quarter of the SM's register file: 3
+// CTAs of 5 warps put 4 warps on some quarter, 128 registers each at most;
+// 2 CTAs put 3, 168 at most.)
 __host__ __device__ constexpr int mma_stages(int kvf, int nq) { return is_8bit(kvf) && nq <= 2 ? 2 : 3; }
 __host__ __device__ constexpr int mma_ctas_per_sm(int kvf, int nq) { return is_8bit(kvf) && nq <= 2 ? 3 : 2; }
 constexpr int kMaxQLen = 4;  // query tokens per request (a verify window when > 1)
