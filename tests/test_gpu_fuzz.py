@@ -5,7 +5,8 @@ random so that the launch paths meet in combinations nobody picked: the KV
 format (fp16, bf16, e4m3, int8 with row scales), the window (1-4 query
 tokens), batch and capacity, uniform or ragged lengths (some rows empty),
 the split count (planner or explicit), and a contiguous or paged cache
-(shuffled pages of 16-256 slots).  Together they reach every schedule: one
+(shuffled pages of 16-256 slots).  With an 8-bit cache, q's magnitude is
+drawn from 1e-7 to 1e6 as well (q_scale compensates).  Together they reach every schedule: one
 piece per CTA merged by the combine kernel, one-wave grids merged on chip in
 thread-block clusters, and the balanced schedule with and without the
 per-row cost, single tokens and windows, 1 or 4 waves.  Sizes stay small
@@ -98,6 +99,14 @@ def test_random_case_matches_oracle(case):
     w = inputs.custom(B, C, 1, kv_dtype=kv_dtype, kv_std=2.0 if fp8 else 1.0, nan_tail=True, q_scale=q_scale,
                       index=500 + idx, q_len=T)
     t = inputs.make(w, DEV, lens=lens)
+    if kv_dtype in ("e4m3", "i8"):
+        # 8-bit caches run f16 tensor cores on a bf16 q: draw q's magnitude
+        # from 1e-7 to 1e6 (q_scale divided by the same factor keeps the
+        # softmax ordinary), so every case also crosses the f16 range that
+        # the per-column power-of-two scaling bridges
+        f = float(10.0 ** np.random.default_rng(9000 + idx).uniform(-7.0, 6.0))
+        t["q"] = (t["q"].float() * f).to(t["q"].dtype)
+        q_scale = q_scale / f
     ks, vs = (t["k_scale"], t["v_scale"]) if fp8 else (1.0, 1.0)
     q4 = t["q"] if T > 1 else t["q"][:, None].contiguous()
     if paged:
