@@ -2,8 +2,9 @@
 // heads and write its key and value into the cache.
 //
 // "Qwen3-VL official BF16 on Jetson Thor (SM110)" docs, "Runtime
-// architecture": fused Q/K norm + RoPE + KV-write kernels (q staged for
-// attention, k and v written at the cache position); decode graphs are keyed
+// architecture": fused kernels that normalise Q and K, rotate them and
+// write the cache (q staged for attention, k and v written at the cache
+// position); decode graphs are keyed
 // by (cache_pos, rope_pos), so the rotary position and the cache slot are
 // separate inputs.  For each head vector x of 128 (32 query heads, 8 KV heads):
 //   y_d = x_d / sqrt(mean(x^2) + eps) * w_d      (w = q_norm_w or k_norm_w)

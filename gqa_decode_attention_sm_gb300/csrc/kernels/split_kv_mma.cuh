@@ -47,7 +47,7 @@
 // finite bf16 q is taken exactly down to 2^-31 of its column's maximum and
 // nothing saturates.  fp16 and bf16 KV use their own type.  For the int8
 // cache ("Qwen3-VL official BF16 on Jetson Orin (SM87)" docs, "INT8 KV cache
-// (kv_mode)": one bf16 scale per (position, KV head) row) the K row scale
+// (kv_mode)": a bf16 scale for each (position, KV head) row) the K row scale
 // multiplies that token's scores and the V row scale joins that token's
 // weight in P; the scales of slots past the length are never read.
 //

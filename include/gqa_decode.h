@@ -9,7 +9,7 @@
  *
  *   Fixed geometry: 32 query heads, 8 KV heads, head_dim 128, one query token
  *   per request.  Query head h reads KV head g = h / 4 (the grouped view
- *   q.view(batch, 8, 4, 128)).  For every batch row b and query head h:
+ *   that splits the 32 heads into 8 groups of 4 consecutive heads).  For every batch row b and query head h:
  *     s_t   = q_scale * k_scale / sqrt(128) * dot(q[b,h,:], K[b,g,t,:]),  0 <= t < len[b]
  *     out[b,h,:] = v_scale * sum_t softmax(s)_t * V[b,g,t,:]
  *   k_scale = v_scale = 1 except on the e4m3 entry point.  Slots t >= len[b]
@@ -177,8 +177,8 @@ gqa_status_t gqa_decode_fp8kv(const void* q_bf16, const uint8_t* kv_e4m3, const 
                               size_t workspace_bytes, void* stream);
 
 /* INT8 KV cache (the "Qwen3-VL official BF16 on Jetson Orin (SM87)" docs,
- * section "INT8 KV cache (kv_mode)": INT8 mirrors of the cache with one BF16
- * scale per (position, KV head) row).  kv_i8 holds int8 codes [batch, 2, 8,
+ * section "INT8 KV cache (kv_mode)": the cache kept as int8 codes, each
+ * (position, KV head) row with its own bf16 scale).  kv_i8 holds int8 codes [batch, 2, 8,
  * capacity, 128]; kv_scales_bf16 holds bf16 scales [batch, 2, 8, capacity]
  * (plane 0 K rows, plane 1 V rows), 16-byte aligned, and capacity must be a
  * multiple of 8 (the scales are staged by 16-byte bulk copies); element (b, p, g, t, d)
@@ -323,7 +323,8 @@ gqa_status_t gqa_decode_debug_skip_tile(const void* q, gqa_dtype_t q_dtype, cons
 
 /* The step before decode: one new token per batch row (the "Qwen3-VL
  * official BF16 on Jetson Thor (SM110)" docs, "Runtime architecture": fused
- * Q/K norm + RoPE + KV-write kernels; decode graphs keyed by (cache_pos,
+ * kernels that normalise Q and K, rotate them and write the cache; decode
+ * graphs keyed by (cache_pos,
  * rope_pos)).  For each query head and each KV head vector x of 128:
  *   y_d = x_d / sqrt(mean(x^2) + eps) * w_d     (w = q_norm_w or k_norm_w, [128])
  *   z_i = y_i cos a_i - y_{i+64} sin a_i,  z_{i+64} = y_{i+64} cos a_i + y_i sin a_i,

@@ -12,14 +12,14 @@ computes, and the pages it restates:
 * "FlashInfer sm110_gqa_decode" article, sections "Input contract" and
   "Convenience API": q [batch,32,128], kv [batch,2,8,capacity,128] (K plane 0,
   V plane 1), int32 lengths in [1, capacity]; softmax scale q_scale/sqrt(128);
-  query heads 4g..4g+3 read KV head g (the grouped view q.view(batch,8,4,128)).
+  query heads 4g..4g+3 read KV head g (the grouped view: 8 groups of 4 consecutive heads).
 * "FP8 KV cache port on Jetson AGX Thor" blog, section 1 (patches 1 and 2):
   e4m3 cache bytes are reinterpreted, not converted; scores are multiplied by
   k_scale and the normalised output by v_scale.
 * "Qwen3-VL official BF16 on Jetson Orin (SM87)" docs, "INT8 KV cache
-  (kv_mode)": int8 codes with one bf16 scale per (position, KV head) row.
-* "FreeToken-Kai on Turing" notes, change 7: score the whole key range, then a
-  plain softmax with no running maximum.
+  (kv_mode)": int8 codes, a bf16 scale for each (position, KV head) row.
+* "FreeToken-Kai on Turing" notes, change 7: every key of the range scored
+  first, then one ordinary softmax over all of them.
 
 Every function here is pinned by ``tests/test_oracle_*.py`` against closed
 forms, invariants, exhaustive format tables and torch's float64
@@ -180,8 +180,8 @@ def gather_pages(pages: np.ndarray, block_table: np.ndarray, lens: np.ndarray) -
     row b is row t % page_size of page block_table[b, t // page_size].  Only the
     pages that hold slots below each length are gathered; the rest of the
     returned [B, 2, 8, max_pages * page_size(, 128)] array is zero.
-    (The "FreeToken-Kai on Turing" notes, change 7: gather the prefix out of the
-    paged cache so the keys are one contiguous matrix.)
+    (The "FreeToken-Kai on Turing" notes, change 7: a paged cache's prefix is
+    first copied into one contiguous key matrix.)
     """
     B, max_pages = block_table.shape
     ps = pages.shape[3]

@@ -12,20 +12,21 @@
  *         "Input contract" (q [batch,32,128], kv [batch,2,8,capacity,128],
  *         K plane 0 / V plane 1, lengths in [1,capacity] read only on the
  *         device), "Convenience API" (q_scale and the softmax scale
- *         q_scale/sqrt(128); grouped view q.view(batch,8,4,128): query heads
- *         4g..4g+3 share KV head g).
+ *         q_scale/sqrt(128); the grouped view of q in 8 groups of 4
+ *         consecutive heads: query heads 4g..4g+3 share KV head g).
  *   [FP8] "FP8 KV cache port on Jetson AGX Thor" blog (kipfel.ltd),
  *         section 1, patch 2: the e4m3 tile is promoted before the dot
  *         product, scores are multiplied by k_scale, the normalised output
  *         by v_scale; patch 1 item 5: the cache bytes are reinterpreted as
  *         float8_e4m3fn, not converted.
  *   [ORIN] "Qwen3-VL official BF16 on Jetson Orin (SM87)" docs, section
- *         "INT8 KV cache (kv_mode)": INT8 mirrors of the cache with one BF16
- *         scale per (position, KV head) row; section "Decode weight
- *         quantization": INT8 symmetric, scale = amax/127.
- *   [TU]  "FreeToken-Kai on Turing" notes, change 7: the whole key range is
- *         scored at once and the softmax is the plain one (no running
- *         maximum, nothing to rescale).  This oracle takes that form.
+ *         "INT8 KV cache (kv_mode)": the cache kept as int8 codes, each
+ *         (position, KV head) row with its own bf16 scale; section "Decode
+ *         weight quantization": symmetric int8, the scale amax/127.
+ *   [TU]  "FreeToken-Kai on Turing" notes, change 7: below Ampere every key
+ *         of the range is scored first and one ordinary softmax runs over
+ *         all of them, with no running maximum.  This oracle takes that
+ *         two-pass form.
  *
  * Definition computed for every requested (b, h):
  *   g   = h / 4                                  (grouped view, [FI])
@@ -308,7 +309,8 @@ int orc_gqa_decode(const void* q, int q_type, const void* kv, int kv_type,
 /* ------------------------------------------------------------ K/V append */
 
 /* The step before decode ("Qwen3-VL official BF16 on Jetson Thor (SM110)"
- * docs, "Runtime architecture": fused Q/K norm + RoPE + KV-write kernels;
+ * docs, "Runtime architecture": fused kernels that normalise Q and K,
+ * rotate them and write the cache;
  * decode graphs keyed by (cache_pos, rope_pos)).  For one new token per batch
  * row b, each query head and each KV head vector x of 128:
  *   y_d  = x_d / sqrt(mean_e(x_e^2) + eps) * w_d            (RMS norm, weight w)
