@@ -545,6 +545,39 @@ def test_deterministic_across_runs():
         assert torch.equal(gq.launch(p).view(torch.int16), first.view(torch.int16))
 
 
+def test_concurrent_streams_with_their_own_workspaces():
+    # Launches on different streams with distinct workspaces may overlap on
+    # the GPU: nothing in the library is shared between them.  Two problems
+    # on two streams, launched alternately with no synchronisation between
+    # them, each give the output of their sequential run bit for bit.
+    ta = _make(inputs.WORKLOADS[3])                                   # fp16, balanced grid + combine
+    tb = _make(inputs.custom(6, 2048, 900, 2048, kv_dtype="e4m3", kv_std=2.0, q_len=3))  # e4m3 window
+    pa = _prepare(ta)
+    ref_a = gq.launch(pa).clone()
+    fp8 = dict(k_scale=tb["k_scale"], v_scale=tb["v_scale"])
+    wsb = torch.zeros(gq.workspace_size(6 * 3, 2048, 4), dtype=torch.uint8, device=DEV)
+    out_b = torch.empty_like(tb["q"])
+
+    def run_b():
+        gq.gqa_decode_verify(tb["q"], tb["kv"], tb["lens"], out=out_b, num_splits=4, workspace=wsb, **fp8)
+
+    run_b()
+    torch.cuda.synchronize()
+    ref_b = out_b.clone()
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    sa.wait_stream(torch.cuda.current_stream())
+    sb.wait_stream(torch.cuda.current_stream())
+    for _ in range(8):
+        with torch.cuda.stream(sa):
+            gq.launch(pa)
+        with torch.cuda.stream(sb):
+            run_b()
+    torch.cuda.synchronize()
+    assert torch.equal(pa.out.view(torch.int16), ref_a.view(torch.int16))
+    assert torch.equal(out_b.view(torch.int16), ref_b.view(torch.int16))
+    _assert_parity(_gpu_rows(out_b), _oracle_full(tb), "e4m3 3-token window after concurrent launches")
+
+
 def test_graph_capture_replay_matches_eager():
     w = inputs.custom(4, 4096, 1000, 4096)
     t = _make(w)
