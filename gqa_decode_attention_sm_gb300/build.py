@@ -39,3 +39,23 @@ def build(force: bool = False, verbose: bool = False) -> str:
     subprocess.run(cmd, check=True)
     os.replace(tmp, LIB_PATH)
     return LIB_PATH
+
+
+CHECKED_LIB_PATH = os.path.join(PKG, "libgqa_decode_checked.so")
+
+
+def build_checked(force: bool = False, verbose: bool = False) -> str:
+    """The same library with every kernel access range-checked (-DGQA_CHECKED):
+    an access outside its buffer sets GQA_FLAG_BOUNDS and is redirected inside
+    it.  For tests only; the product library is built without the checks."""
+    if not force and os.path.exists(CHECKED_LIB_PATH):
+        newest = max(os.path.getmtime(s) for s in _sources())
+        if os.path.getmtime(CHECKED_LIB_PATH) >= newest:
+            return CHECKED_LIB_PATH
+    tmp = CHECKED_LIB_PATH + f".tmp{os.getpid()}"
+    cmd = [nvcc(), *NVCC_FLAGS, "-DGQA_CHECKED", "-I" + INCLUDE, "-o", tmp, MAIN_SRC]
+    if verbose:
+        print(" ".join(cmd))
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, CHECKED_LIB_PATH)
+    return CHECKED_LIB_PATH

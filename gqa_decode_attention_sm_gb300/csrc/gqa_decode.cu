@@ -504,6 +504,10 @@ gqa_status_t run_split(const Call& c) {
   sp.num_pages = c.num_pages;
   const BalPlan bp = bal_plan(c);
   sp.bal_q_min = bp.q_min;
+  const size_t page_rows = c.block_table ? ((size_t)1 << c.page_log2) : (size_t)c.capacity;
+  const size_t units = c.block_table ? (size_t)c.num_pages : (size_t)c.batch;
+  sp.kv_bytes = units * 2 * kHkv * page_rows * kD * kv_elem_bytes(c.kv_format);
+  sp.scales_bytes = c.kv_format == kKvI8 ? units * 2 * kHkv * page_rows * 2 : 0;
   cudaError_t e;
   const int ql = c.q_len, nb = bp.ctas, cl = cluster_splits(c);
   if (c.kv_format == kKvF16) e = launch_split_t<kKvF16, kQF16>(sp, ql, nb, cl, c.stream);
@@ -538,6 +542,7 @@ gqa_status_t run_combine(const Call& c) {
   cp.bal_q_min = bp.q_min;
   cp.tile = tile_tokens(c.kv_format);
   cp.batch = c.batch;
+  cp.flags = lay.flags;
   // Warps per query head: enough that each merges at most about 8 pieces of
   // its row in one round of loads (up to 4).  Pieces per row: the splits
   // that hold slots, or under the balanced schedule about CTAs / rows + 2 (a
@@ -640,6 +645,7 @@ gqa_status_t append_kv(const void* q_proj, const void* k_proj, const void* v_pro
   ap.k_inv_scale = 1.f / k_scale;
   ap.v_inv_scale = 1.f / v_scale;
   ap.theta = (double)rope_theta;
+  ap.kv_rows = units * 2 * kHkv * unit_rows;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(batch, 1, 1);
   cfg.blockDim = dim3(kAppendThreads, 1, 1);

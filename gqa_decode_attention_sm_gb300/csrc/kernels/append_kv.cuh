@@ -55,6 +55,7 @@ struct AppendParams {
   int max_pages, num_pages, page_log2;
   float eps, k_inv_scale, v_inv_scale;  // e4m3: 1/k_scale, 1/v_scale
   double theta;
+  size_t kv_rows;  // rows of 128 in the cache (units x 2 x 8 x rows per unit), for checked builds
 };
 
 template <int QF>
@@ -164,6 +165,12 @@ __global__ void __launch_bounds__(kAppendThreads) append_kv_kernel(const __grid_
     if (!slot_ok) continue;  // never write outside the cache
     const int plane = is_k ? 0 : 1;
     const size_t srow = ((unit * 2 + plane) * kHkv + g) * unit_rows + row_in;  // the scale's index
+    if constexpr (kChecked) {  // the row inside the cache (and its scale inside the scale array)
+      if (srow >= p.kv_rows) {
+        if (lane == 0 && p.flags) atomicOr(p.flags, GQA_FLAG_BOUNDS);
+        continue;
+      }
+    }
     const size_t crow = srow * kD;
     if constexpr (KVF == kKvE4M3) {
       const float inv = is_k ? p.k_inv_scale : p.v_inv_scale;

@@ -39,6 +39,7 @@ struct CombineParams {
   // follow from the lengths, the CTA count, q_min and the tile size
   int bal_ctas, bal_q_min, tile, batch;
   int warps_per_head;  // W (1, 2 or 4): blockDim.x = 4 * 32 * W
+  uint32_t* flags;     // workspace status word (range checks of checked builds)
 };
 
 // One warp's share of the merge of one (b, query head) row: pieces j, j + W,
@@ -202,7 +203,7 @@ __global__ void __launch_bounds__(kGroup * 32 * W) combine_kernel(const __grid_c
   const int g = blockIdx.x, bq = blockIdx.y;  // bq = b * q_len + query token
   const int b = bq / p.q_len, jq = bq % p.q_len;
   const int warp = threadIdx.x >> 5, h = warp % kGroup, share = warp / kGroup;  // head, its warp's share
-  const size_t row = (size_t)bq * kHq + g * kGroup + h;
+  size_t row = (size_t)bq * kHq + g * kGroup + h;
   int n;      // splits or pieces to merge
   bool zero = false;  // a row without tokens
   if (p.bal_ctas > 0) {
@@ -260,6 +261,13 @@ __global__ void __launch_bounds__(kGroup * 32 * W) combine_kernel(const __grid_c
   // earlier let the next split kernel take SM slots during this split's tail.
   pdl_launch_dependents();
   if (p.bal_ctas > 0 && n == 1 && !zero) return;  // one piece: stage 1 wrote the row itself
+  if constexpr (kChecked) {  // the row in the batch, its pieces in the workspace's split slots
+    if (row >= (size_t)p.batch * p.q_len * kHq || n < 0 || n > p.num_splits) {
+      atomicOr(p.flags, GQA_FLAG_BOUNDS);
+      row = 0;
+      n = min(max(n, 0), p.num_splits);
+    }
+  }
   float M, Ls;
   float4 o;
   merge_pieces<kMaxN>(p, row, n, share, W, M, Ls, o);

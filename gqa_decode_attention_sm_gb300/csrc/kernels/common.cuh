@@ -68,6 +68,23 @@ __host__ __device__ inline int split_count(int capacity, int num_splits, int kv_
   return (capacity + chunk - 1) / chunk;
 }
 
+// Checked builds (compiled with -DGQA_CHECKED; the product library is not):
+// every global-memory access of the kernels is tested against the extent of
+// its buffer first.  One outside it sets GQA_FLAG_BOUNDS in the status word
+// and is redirected to an address inside the buffer, so a bad index is
+// reported and nothing faults.  The tests run their cases through such a
+// build and require the flag never to be set.
+#ifdef GQA_CHECKED
+constexpr bool kChecked = true;
+#else
+constexpr bool kChecked = false;
+#endif
+// [p, p + bytes) lies inside [base, base + extent)
+__device__ __forceinline__ bool in_extent(const void* base, size_t extent, const void* p, size_t bytes) {
+  const uintptr_t b = reinterpret_cast<uintptr_t>(base), a = reinterpret_cast<uintptr_t>(p);
+  return a >= b && bytes <= extent && a - b <= extent - bytes;
+}
+
 // Default bound of a pipeline wait (a healthy wait lasts microseconds).
 constexpr uint64_t kWaitBudgetNs = 4000000000ull;
 

@@ -88,7 +88,22 @@ struct SplitParams {
   // balanced schedule: the least number of tiles a CTA takes (so that no row
   // is cut into more pieces than the workspace has split slots)
   int bal_q_min;
+  // byte extents of the cache (or page pool) and of its int8 row scales, for
+  // the range checks of checked builds
+  size_t kv_bytes, scales_bytes;
 };
+
+// Row r of q, out or the partials ((b * q_len + j) * 32 + head): checked
+// builds report a row outside the batch and redirect it to row 0.
+__device__ __forceinline__ size_t checked_row(const SplitParams& p, int nq, size_t row) {
+  if constexpr (kChecked) {
+    if (row >= (size_t)p.batch * nq * kHq) {
+      atomicOr(p.flags, GQA_FLAG_BOUNDS);
+      return 0;
+    }
+  }
+  return row;
+}
 
 template <int QF>
 __device__ __forceinline__ uint32_t pack_out(float a, float b) {
@@ -406,8 +421,8 @@ __device__ __forceinline__ void cluster_merge_tail(const SplitParams& p, const f
         acc.w = fmaf(v.w, a, acc.w);
       }
       const float inv = Ls > 0.f ? p.v_scale / Ls : 0.f;  // a query with no slot gets zeros
-      const int row = (b * NQ + col / kGroup) * kHq + g * kGroup + col % kGroup;
-      *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) + ((size_t)row * kD + d0) * 2) =
+      const size_t row = checked_row(p, NQ, (size_t)(b * NQ + col / kGroup) * kHq + g * kGroup + col % kGroup);
+      *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) + (row * kD + d0) * 2) =
           make_uint2(pack_out<QF>(acc.x * inv, acc.y * inv), pack_out<QF>(acc.z * inv, acc.w * inv));
     }
   }
@@ -563,10 +578,10 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
         // one-split launch with length 0: the output rows are zero
         const int hh = threadIdx.x / 32, d0 = 4 * (threadIdx.x % 32);
 #pragma unroll
-        for (int jq = 0; jq < NQ; ++jq)
-          *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) +
-                                    ((size_t)((b * NQ + jq) * kHq + g * kGroup + hh) * kD + d0) * 2) =
-              make_uint2(0u, 0u);
+        for (int jq = 0; jq < NQ; ++jq) {
+          const size_t row = checked_row(p, NQ, (size_t)(b * NQ + jq) * kHq + g * kGroup + hh);
+          *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) + (row * kD + d0) * 2) = make_uint2(0u, 0u);
+        }
       }
       return;
     }
@@ -654,8 +669,16 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
             if (lane == 0) {
               const uint16_t* gs = p.kv_scales + (page * 2 * kHkv + g) * page_rows + in_page;
               for (int r = 0; r < rows - n8; ++r) {
-                dsk[n8 + r] = gs[r];
-                dsk[T::kTile + n8 + r] = gs[(size_t)kHkv * page_rows + r];
+                const uint16_t* sk = gs + r;
+                const uint16_t* sv = gs + (size_t)kHkv * page_rows + r;
+                if constexpr (kChecked) {
+                  if (!in_extent(p.kv_scales, p.scales_bytes, sk, 2) || !in_extent(p.kv_scales, p.scales_bytes, sv, 2)) {
+                    atomicOr(p.flags, GQA_FLAG_BOUNDS);
+                    sk = sv = p.kv_scales;
+                  }
+                }
+                dsk[n8 + r] = *sk;
+                dsk[T::kTile + n8 + r] = *sv;
               }
             }
           }
@@ -669,15 +692,32 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
           if (lane == 0) {
             const uint32_t seg_bytes = (uint32_t)(seg_end - t) * T::kRowBytes;
             const uint8_t* src = base + (page * 2 * kHkv + g) * head_bytes + (size_t)in_page * T::kRowBytes;
+            const uint8_t* srcV = src + kHkv * head_bytes;
+            if constexpr (kChecked) {  // both source ranges in the cache, the destination in the stage
+              if (!in_extent(p.kv, p.kv_bytes, src, seg_bytes) || !in_extent(p.kv, p.kv_bytes, srcV, seg_bytes) ||
+                  (uint32_t)(t - t0) * T::kRowBytes + seg_bytes > (uint32_t)T::kTileBytes) {
+                atomicOr(p.flags, GQA_FLAG_BOUNDS);
+                src = base;
+                srcV = base + kHkv * head_bytes;
+              }
+            }
             bulk_load(dK + (t - t0) * T::kRowBytes, src, seg_bytes, &full[st], pol);
-            bulk_load(dV + (t - t0) * T::kRowBytes, src + kHkv * head_bytes, seg_bytes, &full[st], pol);
+            bulk_load(dV + (t - t0) * T::kRowBytes, srcV, seg_bytes, &full[st], pol);
             if constexpr (KVF == kKvI8) {
               const int s_end = min(seg_end, t0 + n8);
               if (s_end > t) {
                 const uint16_t* gs = p.kv_scales + (page * 2 * kHkv + g) * page_rows + in_page;
+                const uint16_t* gsv = gs + (size_t)kHkv * page_rows;
                 const uint32_t sb = (uint32_t)(s_end - t) * 2u;
+                if constexpr (kChecked) {
+                  if (!in_extent(p.kv_scales, p.scales_bytes, gs, sb) || !in_extent(p.kv_scales, p.scales_bytes, gsv, sb)) {
+                    atomicOr(p.flags, GQA_FLAG_BOUNDS);
+                    gs = p.kv_scales;
+                    gsv = p.kv_scales + (size_t)kHkv * page_rows;
+                  }
+                }
                 bulk_load(dsk + (t - t0), gs, sb, &full[st], pol);
-                bulk_load(dsk + T::kTile + (t - t0), gs + (size_t)kHkv * page_rows, sb, &full[st], pol);
+                bulk_load(dsk + T::kTile + (t - t0), gsv, sb, &full[st], pol);
               }
             }
           }
@@ -736,7 +776,8 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
       const int jq = 2 * nt + (gq >> 2);
       const bool real = jq < NQ;
       const uint16_t* qrow = static_cast<const uint16_t*>(p.q) +
-                             ((size_t)((b * NQ + (real ? jq : 0)) * kHq) + g * kGroup + (gq & 3)) * kD;
+                             checked_row(p, NQ, (size_t)((b * NQ + (real ? jq : 0)) * kHq) + g * kGroup + (gq & 3)) *
+                                 kD;
   #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
   #pragma unroll
@@ -1135,10 +1176,17 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
           }
         } else if (pc.direct) {
           const float inv = Ls > 0.f ? p.v_scale / Ls : 0.f;  // a query with no slot gets zeros
-          *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) + ((size_t)row * kD + d0) * 2) =
+          *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.out) + (checked_row(p, NQ, row) * kD + d0) * 2) =
               make_uint2(pack_out<QF>(acc.x * inv, acc.y * inv), pack_out<QF>(acc.z * inv, acc.w * inv));
         } else {
-          const size_t idx = (size_t)row * p.num_splits + pc.slot;
+          int slot = pc.slot;
+          if constexpr (kChecked) {
+            if (slot < 0 || slot >= p.num_splits) {
+              atomicOr(p.flags, GQA_FLAG_BOUNDS);
+              slot = 0;
+            }
+          }
+          const size_t idx = checked_row(p, NQ, row) * p.num_splits + slot;
           *reinterpret_cast<float4*>(p.part_o + idx * kD + d0) = acc;
           if (d0 == 0) {
             p.part_m[idx] = M;

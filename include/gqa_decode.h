@@ -100,6 +100,8 @@ typedef enum { GQA_KV_F16 = 0, GQA_KV_BF16 = 1, GQA_KV_E4M3 = 2, GQA_KV_I8 = 3 }
 #define GQA_FLAG_WAIT_TIMEOUT 0x2u    /* a pipeline wait gave up; outputs are invalid */
 #define GQA_FLAG_PAGE_CLAMPED 0x4u    /* a block-table entry was outside [0, num_pages) (decode: clamped; append: not written) */
 #define GQA_FLAG_SLOT_CLAMPED 0x8u    /* gqa_append_kv: a slot outside [0, capacity), not written */
+#define GQA_FLAG_BOUNDS 0x10u         /* checked builds only (GQA_CHECKED): an access fell outside its
+                                         buffer and was redirected inside it; the library has a bug */
 
 /* Name of a status code (static string). */
 const char* gqa_status_string(gqa_status_t status);
