@@ -150,6 +150,17 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
 
+    def wait_first(self, timeout: float = 10.0):
+        """Block until nvidia-smi has printed its first sample (or timeout):
+        its start-up (NVML initialisation, over a second on a fresh machine)
+        must not overlap a timed region."""
+        t_end = time.time() + timeout
+        while self.proc is not None and not self.samples and time.time() < t_end:
+            if self.proc.poll() is not None:
+                break
+            time.sleep(0.02)
+        return self
+
     def stop(self):
         if self.proc is not None:
             self.proc.terminate()
@@ -700,7 +711,7 @@ def run_gpu(args):
         step()
     torch.cuda.synchronize(dev)
 
-    clocks = ClockSampler(local).start()
+    clocks = ClockSampler(local).start().wait_first()
     time.sleep(0.3)
     K = args.steps
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
