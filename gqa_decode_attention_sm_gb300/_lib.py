@@ -19,7 +19,8 @@ EXPORTS = (
     "gqa_decode_plan_for", "gqa_decode_split_geometry", "gqa_decode_launch_count_for",
     "gqa_decode", "gqa_decode_prepared", "gqa_decode_fp8kv", "gqa_decode_split_stage",
     "gqa_decode_combine_stage", "gqa_decode_workspace_init", "gqa_decode_get_status",
-    "gqa_decode_noalloc", "gqa_decode_noalloc_get_status", "gqa_decode_debug_skip_tile", "gqa_decode_int8kv", "gqa_decode_paged",
+    "gqa_decode_noalloc", "gqa_decode_noalloc_get_status", "gqa_decode_debug_skip_tile",
+    "gqa_decode_debug_cut_extents", "gqa_decode_int8kv", "gqa_decode_paged",
     "gqa_decode_verify", "gqa_append_kv", "gqa_append_kv_paged",
 )
 
@@ -58,6 +59,7 @@ def _declare(lib):
         "gqa_append_kv_paged": (i, [p, p, p, p, p, i, p, p, i, p, p, i, p, p, i, i, i, f, f, f, f, p, sz, p]),
         "gqa_decode_debug_skip_tile": (i, [p, i, p, i, p, p, i, i, f, f, f, i, p, sz, i,
                                            ctypes.c_uint64, p]),
+        "gqa_decode_debug_cut_extents": (i, [ctypes.c_uint64, ctypes.c_uint64]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

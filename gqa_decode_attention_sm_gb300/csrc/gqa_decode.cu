@@ -419,6 +419,11 @@ Layout layout_of(void* ws, int batch, int splits) {
   return l;
 }
 
+// Checked builds: how far the extents given to the split kernel's range
+// checks are cut short (gqa_decode_debug_cut_extents), so a test can make
+// the checks fire while every redirected access stays in the real buffers.
+std::atomic<uint64_t> g_cut_kv_bytes{0}, g_cut_scales_bytes{0};
+
 // The balanced schedule serves decode and verify windows of batches up to
 // kBalMaxBatch whose rows can be split (two or more tiles of capacity) and
 // whose one-piece-per-CTA grid would take more than one wave, as long as the
@@ -508,6 +513,10 @@ gqa_status_t run_split(const Call& c) {
   const size_t units = c.block_table ? (size_t)c.num_pages : (size_t)c.batch;
   sp.kv_bytes = units * 2 * kHkv * page_rows * kD * kv_elem_bytes(c.kv_format);
   sp.scales_bytes = c.kv_format == kKvI8 ? units * 2 * kHkv * page_rows * 2 : 0;
+  if (kChecked) {
+    sp.kv_bytes -= std::min<size_t>(sp.kv_bytes, g_cut_kv_bytes.load());
+    sp.scales_bytes -= std::min<size_t>(sp.scales_bytes, g_cut_scales_bytes.load());
+  }
   cudaError_t e;
   const int ql = c.q_len, nb = bp.ctas, cl = cluster_splits(c);
   if (c.kv_format == kKvF16) e = launch_split_t<kKvF16, kQF16>(sp, ql, nb, cl, c.stream);
@@ -1049,6 +1058,14 @@ gqa_status_t gqa_decode_get_status(void* workspace, size_t workspace_bytes, void
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return cuda_fail(e, "reading the workspace status word");
   *flags = host;
+  return GQA_OK;
+}
+
+gqa_status_t gqa_decode_debug_cut_extents(uint64_t kv_cut_bytes, uint64_t scales_cut_bytes) {
+  if (!kChecked && (kv_cut_bytes || scales_cut_bytes))
+    return fail(GQA_ERR_INVALID_ARGUMENT, "extent cuts exist only in the range-checked build (GQA_CHECKED)");
+  g_cut_kv_bytes = kv_cut_bytes;
+  g_cut_scales_bytes = scales_cut_bytes;
   return GQA_OK;
 }
 

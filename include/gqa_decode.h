@@ -323,6 +323,19 @@ gqa_status_t gqa_decode_debug_skip_tile(const void* q, gqa_dtype_t q_dtype, cons
                                         size_t workspace_bytes, int skip_tile,
                                         uint64_t wait_budget_ns, void* stream);
 
+/* Test hook of the range-checked build (compiled with GQA_CHECKED; not for
+ * production use).  From the next launch of this process on, the extents
+ * that the split kernel's range checks compare against are cut short: the
+ * KV cache (or page pool) by `kv_cut_bytes` and the int8 row scales by
+ * `scales_cut_bytes` (each to 0 at most).  A cache access past the cut extent
+ * then sets GQA_FLAG_BOUNDS and is redirected to an address inside the
+ * buffer, as a real out-of-range access would be, so a test can see the
+ * checks fire without any access leaving the real buffers; outputs of such
+ * launches are invalid.  0, 0 restores the true extents.  The product build
+ * has no range checks: there it accepts 0, 0 and rejects anything else with
+ * GQA_ERR_INVALID_ARGUMENT.  The pages have no counterpart to this call. */
+gqa_status_t gqa_decode_debug_cut_extents(uint64_t kv_cut_bytes, uint64_t scales_cut_bytes);
+
 /* The step before decode: one new token per batch row (the "Qwen3-VL
  * official BF16 on Jetson Thor (SM110)" docs, "Runtime architecture": fused
  * kernels that normalise Q and K, rotate them and write the cache; decode

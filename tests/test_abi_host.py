@@ -353,3 +353,11 @@ def test_status_calls_validate(lib):
     assert lib.gqa_decode_workspace_init(None, 256, None) == EINVAL
     assert lib.gqa_decode_workspace_init(WS, 8, None) == EINVAL
     assert lib.gqa_decode_noalloc_get_status(None, None) == EINVAL
+
+
+def test_extent_cuts_are_refused_by_the_product_build(lib):
+    # the product library carries no range checks: only "no cut" is accepted
+    assert lib.gqa_decode_debug_cut_extents(0, 0) == 0
+    assert lib.gqa_decode_debug_cut_extents(1, 0) == EINVAL
+    assert lib.gqa_decode_debug_cut_extents(0, 4096) == EINVAL
+    assert "checked build" in lib.gqa_last_error().decode()

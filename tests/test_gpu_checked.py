@@ -185,3 +185,46 @@ def test_no_allocation_entry():
     _check(flags.value, "no-allocation entry")
     ok, err, _ = tolerance_ok(_rows(out), _oracle(t))
     assert ok, f"noalloc: max err {err:.3e}"
+
+
+@pytest.mark.parametrize("case", ["bf16", "bf16 paged", "i8 scales"])
+def test_cut_extents_make_the_checks_fire(case):
+    """With the extents the checks compare against cut short, accesses past
+    the cut must be reported (and redirected inside the real buffers, so
+    nothing faults); with the true extents restored the same call is clean
+    and matches the oracle."""
+    lib = _lib.load()
+    kv_dtype = "i8" if case.startswith("i8") else "bf16"
+    B, C, S = 4, 1024, 4
+    lens = [C, 700, C, 8 * (C // 16) + 5]  # the last: a tail of int8 scales loaded one by one
+    w = inputs.custom(B, C, 1, kv_dtype=kv_dtype)
+    t = inputs.make(w, DEV, lens=lens)
+    kv_bytes = t["kv"].numel() * t["kv"].element_size()
+    sc_bytes = t["kv_scales"].numel() * 2 if t["kv_scales"] is not None else 0
+
+    def run():
+        ws = torch.zeros(gq.workspace_size(B, C, S), dtype=torch.uint8, device=DEV)
+        if case.endswith("paged"):
+            pt = inputs.paginate(t, 64, extra_pages=2)
+            out = gq.gqa_decode_paged(t["q"], pt["kv_pages"], pt["block_table"], pt["lens"], num_splits=S,
+                                      workspace=ws)
+        else:
+            out = gq.gqa_decode_verify(t["q"][:, None].contiguous(), t["kv"], t["lens"], num_splits=S, workspace=ws,
+                                       kv_scales=t["kv_scales"])
+        torch.cuda.synchronize(DEV)
+        return out, gq.get_status(ws)
+
+    try:
+        if case.startswith("i8"):
+            assert lib.gqa_decode_debug_cut_extents(0, sc_bytes // 2) == 0
+        else:
+            assert lib.gqa_decode_debug_cut_extents(kv_bytes // 2, 0) == 0
+        _, flags = run()
+        assert flags & FLAG_BOUNDS, f"{case}: the cut extent was not reported (flags {flags:#x})"
+        assert not flags & api.FLAG_WAIT_TIMEOUT
+    finally:
+        assert lib.gqa_decode_debug_cut_extents(0, 0) == 0
+    out, flags = run()
+    _check(flags, f"{case}, true extents")
+    ok, err, _ = tolerance_ok(_rows(out), _oracle(t))
+    assert ok, f"{case}: max err {err:.3e}"
