@@ -101,3 +101,13 @@ def rms_gate_ok(got: np.ndarray, ref: np.ndarray, frac: float = RMS_GATE):
     err = float(np.max(np.abs(got - ref)))
     ratio = err / rms if rms > 0 else (0.0 if err == 0 else float("inf"))
     return bool(ratio <= frac and np.all(np.isfinite(got))), ratio
+
+
+def ulps_apart(got_bits, ref_bits) -> np.ndarray:
+    """Distance in units in the last place between 16-bit float patterns of
+    the same format (ordered by value; +0 and -0 coincide)."""
+    def ordered(b):
+        b = np.asarray(b, dtype=np.int64)
+        mag = b & 0x7FFF
+        return np.where(b & 0x8000, -mag, mag)
+    return np.abs(ordered(got_bits) - ordered(ref_bits))

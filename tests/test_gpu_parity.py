@@ -20,7 +20,7 @@ import torch
 import oracle
 import gqa_decode_attention_sm_gb300 as gq
 from gqa_decode_attention_sm_gb300 import api, inputs
-from helpers import HQ, RMS_GATE, bits_of, rms_gate_ok, tolerance_ok
+from helpers import HQ, RMS_GATE, bits_of, rms_gate_ok, tolerance_ok, ulps_apart
 
 pytestmark = pytest.mark.gpu
 
@@ -965,16 +965,6 @@ def _vals(t):
     return t.float().cpu().numpy().astype(np.float64)
 
 
-def _ulps_apart(got_bits, ref_bits):
-    """Distance in units in the last place between 16-bit float patterns of
-    the same format (ordered by value; +0 and -0 coincide)."""
-    def ordered(b):
-        b = np.asarray(b, dtype=np.int64)
-        mag = b & 0x7FFF
-        return np.where(b & 0x8000, -mag, mag)
-    return np.abs(ordered(got_bits) - ordered(ref_bits))
-
-
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 def test_append_matches_oracle_and_touches_only_its_slot(dtype):
     # An element-wise step rounded once: every q_out and K element must be the
@@ -989,11 +979,11 @@ def test_append_matches_oracle_and_touches_only_its_slot(dtype):
     qo, ko, vo = oracle.append_kv(_vals(qp), _vals(kp), _vals(vp), _vals(wq), _vals(wk),
                                   pos.cpu().numpy(), 1e-6, 1e6)
     fmt = FMT[dtype]
-    d_q = _ulps_apart(bits_of(q_out), oracle.round_to(qo, fmt))
+    d_q = ulps_apart(bits_of(q_out), oracle.round_to(qo, fmt))
     assert d_q.max() <= 1, f"append q_out {dtype}: {int(d_q.max())} ulps from the oracle"
     sl = slots.cpu().tolist()
     k_new = torch.stack([kv[b, 0, :, sl[b]] for b in range(B)])
-    d_k = _ulps_apart(bits_of(k_new), oracle.round_to(ko, fmt))
+    d_k = ulps_apart(bits_of(k_new), oracle.round_to(ko, fmt))
     assert d_k.max() <= 1, f"append k {dtype}: {int(d_k.max())} ulps from the oracle"
     print(f"PARITY append {dtype}: q_out {np.mean(d_q > 0):.2%}, k {np.mean(d_k > 0):.2%} of elements one ulp off")
     v_new = torch.stack([kv[b, 1, :, sl[b]] for b in range(B)])
