@@ -439,6 +439,14 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
   using T = KvTraits<KVF>;
   constexpr bool kBF16 = kMmaBF16<KVF>;
   constexpr int kSlabs = T::kTile / (16 * kMmaConsumerWarps);  // 16-token slabs per warp per tile
+  // Slabs taken together: two for 4-token windows over an e4m3 cache, whose
+  // 16 columns are all real and which is latency-bound (more independent
+  // work between the max reductions, half as many of them).  Measured cold
+  // at 64 x U[16k, 32k] on GB300: e4m3 4 tokens 540.7 -> 514.1 us; the
+  // 3-token e4m3 and the int8 windows were slower (507.9 -> 526.3, int8
+  // 618.5 / 620.5 -> 639.0 / 669.7: more spills at 168 registers).
+  constexpr int kSG = KVF == kKvE4M3 && NQ == 4 ? 2 : 1;
+  static_assert(kSlabs % kSG == 0, "whole slab groups");
   constexpr int kCols = kGroup * NQ;                            // (query token, head) columns
   constexpr int kNT = (kCols + 7) / 8;                          // 8-column mma n-tiles
   extern __shared__ __align__(128) uint8_t smem[];
@@ -873,10 +881,21 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
       };
 
   #pragma unroll
-      for (int sl = 0; sl < kSlabs; ++sl) {
-        const int R = (warp * kSlabs + sl) * 16;  // first tile row of this slab
-        if (R >= rows) break;                     // warp-uniform
-        const bool partial = R + 16 > rows;
+      for (int sg = 0; sg < kSlabs; sg += kSG) {
+        // this warp's slabs sg .. sg + kSG - 1 of the tile (kSG = 2: both QK
+        // products, one max reduction over their 32 tokens, both P.V products)
+        if ((warp * kSlabs + sg) * 16 >= rows) break;  // warp-uniform
+        float x[kSG][kNT][4];      // scaled, masked scores
+        float vsa[kSG], vsb[kSG];  // int8: V row scales of this lane's tokens
+  #pragma unroll
+        for (int sj = 0; sj < kSG; ++sj) {
+        const int R = (warp * kSlabs + sg + sj) * 16;  // first tile row of this slab
+        vsa[sj] = vsb[sj] = 0.f;
+        if (sj > 0 && R >= rows) {  // warp-uniform: past the tile's rows, no token
+  #pragma unroll
+          for (int nt = 0; nt < kNT; ++nt) x[sj][nt][0] = x[sj][nt][1] = x[sj][nt][2] = x[sj][nt][3] = -INFINITY;
+          continue;
+        }
 
         // ---- scores: S^T[16 tokens x 8] = K . Q^T for each n-tile
         float sc[kNT][4];
@@ -918,31 +937,31 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
         // n-tile loops below they were read again for each n-tile (3-4-token
         // windows of the int8 cache of 64 x U[16k, 32k] on GB300, us per call
         // back to back: 638.7 -> 612.2, 640.4 -> 613.3; the same output)
-        float ks_a = 0.f, ks_b = 0.f, vs_a = 0.f, vs_b = 0.f;
+        float ks_a = 0.f, ks_b = 0.f;
         if constexpr (KVF == kKvI8) {
           ks_a = row_scale(R + gq, 0);
           ks_b = row_scale(R + gq + 8, 0);
-          vs_a = row_scale(R + gq, 1);
-          vs_b = row_scale(R + gq + 8, 1);
+          vsa[sj] = row_scale(R + gq, 1);
+          vsb[sj] = row_scale(R + gq + 8, 1);
         }
         // sc[nt]: [0] token R+gq column 2cq, [1] token R+gq column 2cq+1, [2]/[3] token R+gq+8
         const int ta = tile_t0 + R + gq, tb = ta + 8;
-        float x[kNT][4];
   #pragma unroll
         for (int nt = 0; nt < kNT; ++nt) {
   #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            if constexpr (KVF == kKvI8) x[nt][e] = fmaf(sc[nt][e], sl2c[nt][e & 1], kb[nt][e & 1]);
-            else x[nt][e] = sc[nt][e] * sl2c[nt][e & 1];
+            if constexpr (KVF == kKvI8) x[sj][nt][e] = fmaf(sc[nt][e], sl2c[nt][e & 1], kb[nt][e & 1]);
+            else x[sj][nt][e] = sc[nt][e] * sl2c[nt][e & 1];
           }
           if constexpr (KVF == kKvI8) {  // per-row K scale multiplies that token's scores
-            x[nt][0] *= ks_a;
-            x[nt][1] *= ks_a;
-            x[nt][2] *= ks_b;
-            x[nt][3] *= ks_b;
+            x[sj][nt][0] *= ks_a;
+            x[sj][nt][1] *= ks_a;
+            x[sj][nt][2] *= ks_b;
+            x[sj][nt][3] *= ks_b;
           }
-          if (ta >= lim[nt]) x[nt][0] = x[nt][1] = -INFINITY;  // select, never multiply
-          if (tb >= lim[nt]) x[nt][2] = x[nt][3] = -INFINITY;
+          if (ta >= lim[nt]) x[sj][nt][0] = x[sj][nt][1] = -INFINITY;  // select, never multiply
+          if (tb >= lim[nt]) x[sj][nt][2] = x[sj][nt][3] = -INFINITY;
+        }
         }
 
         // ---- online softmax per column (max over the slab's 16 tokens)
@@ -950,7 +969,12 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
         bool grow = false;
   #pragma unroll
         for (int nt = 0; nt < kNT; ++nt) {
-          float h0 = fmaxf(x[nt][0], x[nt][2]), h1 = fmaxf(x[nt][1], x[nt][3]);
+          float h0 = fmaxf(x[0][nt][0], x[0][nt][2]), h1 = fmaxf(x[0][nt][1], x[0][nt][3]);
+  #pragma unroll
+          for (int sj = 1; sj < kSG; ++sj) {
+            h0 = fmaxf(h0, fmaxf(x[sj][nt][0], x[sj][nt][2]));
+            h1 = fmaxf(h1, fmaxf(x[sj][nt][1], x[sj][nt][3]));
+          }
   #pragma unroll
           for (int off = 4; off < 32; off <<= 1) {
             h0 = fmaxf(h0, __shfl_xor_sync(0xffffffffu, h0, off));
@@ -986,37 +1010,39 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
         // 2cq, 2cq+1 (b0) and 2cq+8, 2cq+9 (b1); the packed weights hold
         // (token gq, columns 2cq, 2cq+1) and (token gq+8, ...): one 8x8
         // transpose each.
-        uint32_t bh[kNT][2], bl[kNT][2];
+        uint32_t bh[kSG][kNT][2], bl[kSG][kNT][2];
+  #pragma unroll
+        for (int sj = 0; sj < kSG; ++sj) {
   #pragma unroll
         for (int nt = 0; nt < kNT; ++nt) {
-          const float p0 = x[nt][0] == -INFINITY ? 0.f : ex2(x[nt][0] - m[nt][0]);
-          const float p1 = x[nt][1] == -INFINITY ? 0.f : ex2(x[nt][1] - m[nt][1]);
-          const float p2 = x[nt][2] == -INFINITY ? 0.f : ex2(x[nt][2] - m[nt][0]);
-          const float p3 = x[nt][3] == -INFINITY ? 0.f : ex2(x[nt][3] - m[nt][1]);
-          bl[nt][0] = bl[nt][1] = 0u;
+          const float p0 = x[sj][nt][0] == -INFINITY ? 0.f : ex2(x[sj][nt][0] - m[nt][0]);
+          const float p1 = x[sj][nt][1] == -INFINITY ? 0.f : ex2(x[sj][nt][1] - m[nt][1]);
+          const float p2 = x[sj][nt][2] == -INFINITY ? 0.f : ex2(x[sj][nt][2] - m[nt][0]);
+          const float p3 = x[sj][nt][3] == -INFINITY ? 0.f : ex2(x[sj][nt][3] - m[nt][1]);
+          bl[sj][nt][0] = bl[sj][nt][1] = 0u;
           if constexpr (kBF16) {
             const uint32_t ph_a = pack_bf16(p0, p1), ph_b = pack_bf16(p2, p3);
             const uint32_t pl_a = pack_bf16(p0 - bf16_lo_to_f32(ph_a), p1 - bf16_hi_to_f32(ph_a));
             const uint32_t pl_b = pack_bf16(p2 - bf16_lo_to_f32(ph_b), p3 - bf16_hi_to_f32(ph_b));
             l[nt][0] += bf16_lo_to_f32(ph_a) + bf16_lo_to_f32(pl_a) + bf16_lo_to_f32(ph_b) + bf16_lo_to_f32(pl_b);
             l[nt][1] += bf16_hi_to_f32(ph_a) + bf16_hi_to_f32(pl_a) + bf16_hi_to_f32(ph_b) + bf16_hi_to_f32(pl_b);
-            bh[nt][0] = transpose8x8_b16(ph_a);
-            bh[nt][1] = transpose8x8_b16(ph_b);
-            bl[nt][0] = transpose8x8_b16(pl_a);
-            bl[nt][1] = transpose8x8_b16(pl_b);
+            bh[sj][nt][0] = transpose8x8_b16(ph_a);
+            bh[sj][nt][1] = transpose8x8_b16(ph_b);
+            bl[sj][nt][0] = transpose8x8_b16(pl_a);
+            bl[sj][nt][1] = transpose8x8_b16(pl_b);
           } else if constexpr (KVF == kKvI8) {
             // the per-row V scale joins the weight of its token; the denominator
             // keeps the unscaled weights
-            const uint32_t pa = pack_f16(p0 * vs_a, p1 * vs_a);
-            const uint32_t pb = pack_f16(p2 * vs_b, p3 * vs_b);
+            const uint32_t pa = pack_f16(p0 * vsa[sj], p1 * vsa[sj]);
+            const uint32_t pb = pack_f16(p2 * vsb[sj], p3 * vsb[sj]);
             l[nt][0] += p0 + p2;
             l[nt][1] += p1 + p3;
             // the weights exactly as the tensor core multiplies them (V offset)
             const float2 fa = f16x2_to_f32x2(pa), fb = f16x2_to_f32x2(pb);
             vw[nt][0] += fa.x + fb.x;
             vw[nt][1] += fa.y + fb.y;
-            bh[nt][0] = transpose8x8_b16(pa);
-            bh[nt][1] = transpose8x8_b16(pb);
+            bh[sj][nt][0] = transpose8x8_b16(pa);
+            bh[sj][nt][1] = transpose8x8_b16(pb);
           } else {
             const uint32_t pa = pack_f16(p0, p1), pb = pack_f16(p2, p3);
             // the denominator sums the same rounded weights the tensor core multiplies
@@ -1024,13 +1050,19 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
             const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&pb));
             l[nt][0] += fa.x + fb.x;
             l[nt][1] += fa.y + fb.y;
-            bh[nt][0] = transpose8x8_b16(pa);
-            bh[nt][1] = transpose8x8_b16(pb);
+            bh[sj][nt][0] = transpose8x8_b16(pa);
+            bh[sj][nt][1] = transpose8x8_b16(pb);
           }
+        }
         }
 
         // ---- O^T[128 dims x 8] += V^T . P^T per n-tile: lane (gq, cq) reads dims
         // 16gq..16gq+15 of tokens R+2cq, R+2cq+1, R+2cq+8, R+2cq+9.
+  #pragma unroll
+        for (int sj = 0; sj < kSG; ++sj) {
+        const int R = (warp * kSlabs + sg + sj) * 16;
+        if (sj > 0 && R >= rows) break;  // warp-uniform
+        const bool partial = R + 16 > rows;
         const int r0 = R + 2 * cq;
         const uint8_t* v0 = sV + r0 * T::kRowBytes;
         const bool ok0 = !partial || r0 < rows, ok1 = !partial || r0 + 1 < rows;
@@ -1054,12 +1086,12 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
             widen4_biased<KVF>(prmt(a[j], bq[j], 0x5140u), A0, A1);  // dims 4j, 4j+1 of tokens r0, r0+1
             widen4_biased<KVF>(prmt(c[j], d[j], 0x5140u), A2, A3);   // tokens r0+8, r0+9
   #pragma unroll
-            for (int nt = 0; nt < kNT; ++nt) mma16816<false>(o[nt][2 * j], A0, A1, A2, A3, bh[nt][0], bh[nt][1]);
+            for (int nt = 0; nt < kNT; ++nt) mma16816<false>(o[nt][2 * j], A0, A1, A2, A3, bh[sj][nt][0], bh[sj][nt][1]);
             widen4_biased<KVF>(prmt(a[j], bq[j], 0x7362u), A0, A1);  // dims 4j+2, 4j+3
             widen4_biased<KVF>(prmt(c[j], d[j], 0x7362u), A2, A3);
   #pragma unroll
             for (int nt = 0; nt < kNT; ++nt)
-              mma16816<false>(o[nt][2 * j + 1], A0, A1, A2, A3, bh[nt][0], bh[nt][1]);
+              mma16816<false>(o[nt][2 * j + 1], A0, A1, A2, A3, bh[sj][nt][0], bh[sj][nt][1]);
           }
         } else {
           const uint8_t* v1 = v0 + T::kRowBytes;
@@ -1084,11 +1116,12 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
               const uint32_t A2 = prmt(c[j], d[j], 0x5410u), A3 = prmt(c[j], d[j], 0x7632u);
   #pragma unroll
               for (int nt = 0; nt < kNT; ++nt) {
-                mma16816<kBF16>(o[nt][4 * half + j], A0, A1, A2, A3, bh[nt][0], bh[nt][1]);
-                if constexpr (kBF16) mma16816<kBF16>(o[nt][4 * half + j], A0, A1, A2, A3, bl[nt][0], bl[nt][1]);
+                mma16816<kBF16>(o[nt][4 * half + j], A0, A1, A2, A3, bh[sj][nt][0], bh[sj][nt][1]);
+                if constexpr (kBF16) mma16816<kBF16>(o[nt][4 * half + j], A0, A1, A2, A3, bl[sj][nt][0], bl[sj][nt][1]);
               }
             }
           }
+        }
         }
       }
       // int8 V offset: taken off every 16 tiles, so the accumulator never
