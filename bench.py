@@ -447,7 +447,8 @@ def oracle_config(t, w, nbytes, reps):
 L2_COLD = "cold (512 MB written, then 1 GB read, before each call)"
 
 
-def per_config_table(dev, peak, gq, inputs, quick=False, cpu=True):
+def make_cold_flush(dev):
+    """The flush run before every cold call."""
     import torch
     flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     clean_buf = torch.ones(256 << 20, dtype=torch.float32, device=dev)  # 1 GB
@@ -463,6 +464,63 @@ def per_config_table(dev, peak, gq, inputs, quick=False, cpu=True):
         flush_buf.fill_(1)
         clean_buf.max()
 
+    return flush
+
+
+# Shapes away from the five workloads, for the automatic plan (split count,
+# balanced schedule or one piece per CTA, cluster merge): (KV format, batch,
+# capacity).  Each runs with every length = capacity and, from batch 8 on,
+# with lengths U[capacity / 4, capacity].
+SWEEP_SHAPES = (
+    ("bf16", 1, 4096), ("bf16", 1, 32768), ("bf16", 4, 16384), ("bf16", 8, 4096), ("bf16", 8, 32768),
+    ("bf16", 64, 4096), ("bf16", 64, 32768), ("bf16", 256, 4096), ("bf16", 16, 131072), ("bf16", 1024, 1024),
+    ("bf16", 4, 8192), ("e4m3", 1, 32768), ("e4m3", 8, 4096), ("e4m3", 8, 8192), ("e4m3", 16, 32768),
+    ("e4m3", 128, 8192), ("e4m3", 256, 16384), ("e4m3", 4, 262144), ("i8", 1, 32768), ("i8", 8, 4096),
+    ("i8", 16, 32768), ("i8", 128, 8192),
+)
+
+
+def planner_sweep(dev, peak, gq, inputs, quick=False):
+    """Cold us per call and the fraction of the peak over SWEEP_SHAPES, each
+    through prepare/launch with the automatic split count."""
+    import torch
+    from gqa_decode_attention_sm_gb300 import api as gapi
+    flush = make_cold_flush(dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    rows = []
+    for n, (kv, B, C) in enumerate(SWEEP_SHAPES):
+        for ragged in ((False, True) if B >= 8 else (False,)):
+            w = inputs.custom(B, C, C // 4 if ragged else C, C, kv_dtype=kv, kv_std=2.0 if kv == "e4m3" else 1.0,
+                              index=700 + n)
+            t = inputs.make(w, dev)
+            out = torch.empty_like(t["q"])
+            fp8 = kv == "e4m3"
+            tensors = {"Q": t["q"], "KV": t["kv"], "O": out, "sequence_lengths": t["lens"]}
+            if t["kv_scales"] is not None:
+                tensors["KV_SCALES"] = t["kv_scales"]
+            p = gq.prepare(tensors, q_scale=t["q_scale"], k_scale=t["k_scale"] if fp8 else None,
+                           v_scale=t["v_scale"] if fp8 else None)
+            nbytes = algorithmic_bytes(w, t["lens"].cpu().tolist())
+            for _ in range(3):
+                gq.launch(p)
+            torch.cuda.synchronize()
+            us = time_calls(lambda: gq.launch(p), 5 if quick else 20, flush=flush)
+            timing = "events"
+            if us < 100.0:  # a few event steps (2.048 us each): the difference of two CUDA graphs instead
+                us = cold_graph_us(lambda: gq.launch(p), flush, calls=10 if quick else 40, reps=3 if quick else 7)
+                timing = "graph difference"
+            rows.append({"timing": timing, "kv": kv, "batch": B, "capacity": C, "lengths": f"U[{C // 4},{C}]" if ragged else "capacity",
+                         "splits": p.num_splits, "kernels": gapi.launch_count(B, C, p.kv_format, 1, p.num_splits, sms),
+                         "us_per_call": round(us, 2), "GBps": round(nbytes / us / 1e3, 1),
+                         "frac_of_peak": round(nbytes / us / 1e3 / peak, 4), "alg_bytes": nbytes})
+            del t, out, p, tensors
+            torch.cuda.empty_cache()
+    return rows
+
+
+def per_config_table(dev, peak, gq, inputs, quick=False, cpu=True):
+    import torch
+    flush = make_cold_flush(dev)
     table = {}
     cases = dict(inputs.WORKLOADS)
     # beyond the five workloads: an int8 cache (one bf16 scale per row) with workload 5's shape
@@ -867,6 +925,8 @@ def run_gpu(args):
                                               cpu=not args.no_cpu_baseline)
     if rank == 0 and world == 1 and args.read_ceiling:
         line["read_ceiling"] = read_ceiling(achieved)
+    if rank == 0 and args.sweep:
+        line["sweep"] = {"l2": L2_COLD, "rows": planner_sweep(dev, peak, gq, inputs, quick=args.quick)}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -917,6 +977,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true")
     ap.add_argument("--quick", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="also time SWEEP_SHAPES (batch x capacity x KV format, uniform and ragged lengths) "
+                         "with the automatic plan, cold, and report them under 'sweep'")
     ap.add_argument("--read-ceiling", action="store_true",
                     help="also build and run bench_read_ceiling.cu (the read rate of the split kernel's data "
                          "movement without arithmetic) and report the split kernel as a fraction of it")

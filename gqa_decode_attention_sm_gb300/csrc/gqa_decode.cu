@@ -48,6 +48,7 @@ gqa_status_t cuda_fail(cudaError_t e, const char* what) {
 // ---------------------------------------------------------------- devices
 
 constexpr int kMaxDevices = 64;
+constexpr int kClusterMaxSplits = 8;  // the on-chip merge: clusters of 2..8 splits (portable sizes)
 
 // Per-device result of the one-time check.  Kept once known for good: the
 // device is ready (sm_count set) or is not a compute capability 10.3 part.  A
@@ -58,6 +59,11 @@ struct DeviceState {
   gqa_status_t status = GQA_ERR_UNSUPPORTED_DEVICE;
   int sm_count = 0;
   std::string message;
+  // The most clusters of s CTAs of the cluster-merge split kernel that can be
+  // resident at once, by [KV format][q format][q_len - 1][s]
+  // (cudaOccupancyMaxActiveClusters).  A cluster's CTAs share one GPC, so a
+  // grid that nearly fills the SMs can hold fewer clusters than slots / s.
+  int cluster_fit[4][2][kMaxQLen][kClusterMaxSplits + 1] = {};
 };
 DeviceState g_devices[kMaxDevices];
 
@@ -82,8 +88,40 @@ cudaError_t set_split_attributes() {
   return e;
 }
 
-// One-time per-device check (compute capability 10.3) and opt-in to the
-// split kernel's dynamic shared memory.  Runs with `dev` current.
+template <int KVF, int QF, int NQ>
+cudaError_t query_cluster_fit(DeviceState& st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kMmaThreads, 1, 1);
+  cfg.dynamicSmemBytes = mma_smem_bytes(KVF, NQ);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  for (int s = 2; s <= kClusterMaxSplits; ++s) {
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = (unsigned)s;
+    cfg.gridDim = dim3(kHkv, 1, (unsigned)s);
+    int n = 0;
+    const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, split_kv_mma_kernel<KVF, QF, NQ, false, true>, &cfg);
+    if (e != cudaSuccess) return e;
+    st.cluster_fit[KVF][QF][NQ - 1][s] = n;
+  }
+  return cudaSuccess;
+}
+
+template <int KVF, int QF>
+cudaError_t query_cluster_fits(DeviceState& st) {
+  cudaError_t e = query_cluster_fit<KVF, QF, 1>(st);
+  if (e == cudaSuccess) e = query_cluster_fit<KVF, QF, 2>(st);
+  if (e == cudaSuccess) e = query_cluster_fit<KVF, QF, 3>(st);
+  if (e == cudaSuccess) e = query_cluster_fit<KVF, QF, 4>(st);
+  return e;
+}
+
+// One-time per-device check (compute capability 10.3), opt-in to the split
+// kernel's dynamic shared memory, and the cluster occupancy table.  Runs
+// with `dev` current.
 void init_device(int dev, DeviceState& st) {
   int major = 0, minor = 0, sms = 0;
   cudaError_t e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
@@ -111,10 +149,20 @@ void init_device(int dev, DeviceState& st) {
   if (a == cudaSuccess) a = set_split_attributes<kKvE4M3, kQF16>();
   if (a == cudaSuccess) a = set_split_attributes<kKvI8, kQBF16>();
   if (a == cudaSuccess) a = set_split_attributes<kKvI8, kQF16>();
+  const char* what = "cudaFuncSetAttribute";
+  if (a == cudaSuccess) {
+    what = "cudaOccupancyMaxActiveClusters";
+    a = query_cluster_fits<kKvF16, kQF16>(st);
+    if (a == cudaSuccess) a = query_cluster_fits<kKvBF16, kQBF16>(st);
+    if (a == cudaSuccess) a = query_cluster_fits<kKvE4M3, kQBF16>(st);
+    if (a == cudaSuccess) a = query_cluster_fits<kKvE4M3, kQF16>(st);
+    if (a == cudaSuccess) a = query_cluster_fits<kKvI8, kQBF16>(st);
+    if (a == cudaSuccess) a = query_cluster_fits<kKvI8, kQF16>(st);
+  }
   if (prev >= 0 && prev != dev) cudaSetDevice(prev);
   if (a != cudaSuccess) {
     st.status = GQA_ERR_CUDA;
-    st.message = std::string("cudaFuncSetAttribute failed: ") + cudaGetErrorString(a);
+    st.message = std::string(what) + " failed: " + cudaGetErrorString(a);
     return;
   }
   st.sm_count = sms;
@@ -471,14 +519,39 @@ BalPlan bal_plan(const Call& c) {
 // warm (e4m3 1 x 8192 in a graph 10.3 -> 12.2 us, a 4-token window at
 // 1 x 4096 9.6 -> 13.7), and so were multi-wave grids of clusters (int8
 // 64 x U[16k, 32k] with a 2-token window, 8 splits, 4096 CTAs: 530 -> 760 us).
+// The clusters must also all be resident at once (the device's occupancy
+// table): a cluster's CTAs share one GPC, and near full occupancy clusters
+// of some sizes pack into fewer than the slots allow, leaving the rest for a
+// second wave.  Measured on GB300: e4m3 8 x 4096 (7 splits, 448 CTAs in
+// clusters of 7, 456 slots) took 24.8 us per cold call, against 18.4 with 6
+// splits.  Such a grid runs as the plain grid with the combine kernel.
 // Returns the cluster size, or 0 for the combine kernel.
-constexpr int kClusterMaxSplits = 8;
+int cluster_fit(const Call& c, int s) {
+  // the current device's table, once it has been set up with this SM count
+  // (0: unknown, e.g. host-only planning without a device)
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();  // (no device here: clear the error)
+    return 0;
+  }
+  const DeviceState& st = g_devices[dev];
+  if (st.state.load(std::memory_order_acquire) != 1 || st.sm_count != c.sms) return 0;
+  const auto& row = st.cluster_fit[c.kv_format];
+  const int nq = c.q_len - 1;
+  if (!is_8bit(c.kv_format)) return row[c.kv_format == kKvF16 ? kQF16 : kQBF16][nq][s];
+  // an 8-bit cache with either q format when the call does not say which
+  if (c.q_dtype == GQA_F16 || c.q_dtype == GQA_BF16) return row[c.q_dtype][nq][s];
+  return std::min(row[kQF16][nq][s], row[kQBF16][nq][s]);
+}
+
 int cluster_splits(const Call& c) {
   if (bal_plan(c).ctas > 0 || c.sms < 1) return 0;
   const int s = split_count(c.capacity, c.num_splits, c.kv_format);
   if (s < 2 || s > kClusterMaxSplits) return 0;
   const long long slots = (long long)mma_ctas_per_sm(c.kv_format, c.q_len) * c.sms;
-  return (long long)kHkv * c.batch * s <= slots ? s : 0;
+  if ((long long)kHkv * c.batch * s > slots) return 0;
+  const int fit = cluster_fit(c, s);
+  return fit > 0 && (long long)kHkv * c.batch > fit ? 0 : s;
 }
 
 gqa_status_t run_split(const Call& c) {
@@ -761,6 +834,7 @@ gqa_status_t gqa_decode_launch_count_for(int batch, int capacity, gqa_kv_format_
   // the same rules run_split / run_combine apply to a launch of these sizes
   Call c{};
   c.kv_format = (int)kv_format;
+  c.q_dtype = -1;  // (either q format)
   c.batch = batch;
   c.capacity = capacity;
   c.num_splits = num_splits;

@@ -136,15 +136,20 @@ gqa_status_t gqa_decode_plan_for(int batch, int capacity, gqa_kv_format_t kv_for
  * the balanced schedule cuts rows elsewhere but never into more pieces.
  * Stage 2 runs only when the effective count is above 1 and the splits do
  * not merge on chip (2..8 of them with one piece per CTA in a grid of one
- * wave do, in a thread-block cluster). */
+ * wave whose clusters can all be resident at once do, in a thread-block
+ * cluster). */
 gqa_status_t gqa_decode_split_geometry(int capacity, int num_splits, gqa_kv_format_t kv_format,
                                        int* chunk_tokens_out, int* splits_effective_out);
 
-/* Kernels one decode call of these sizes enqueues on its stream (pure host
- * arithmetic, no CUDA call): 1 when a single split holds every slot or the
- * splits merge on chip in a thread-block cluster, else 2 (the split kernel
- * and the combine).  The same for the contiguous and paged entries; q_len
- * 1..4 as gqa_decode_verify; num_splits 1..GQA_MAX_SPLITS after resolving 0;
+/* Kernels one decode call of these sizes enqueues on its stream (host
+ * arithmetic; no work is enqueued): 1 when a single split holds every slot
+ * or the splits merge on chip in a thread-block cluster, else 2 (the split
+ * kernel and the combine).  The on-chip merge also needs all its clusters
+ * resident at once; once the current device has been set up by a call that
+ * launches, and sm_count is its SM count, its cluster occupancy (queried at
+ * set-up) decides that as the launches do, else only the SM count does.
+ * The same for the contiguous and paged entries; q_len 1..4 as
+ * gqa_decode_verify; num_splits 1..GQA_MAX_SPLITS after resolving 0;
  * sm_count < 1 is invalid.  Writes the count to *launches_out. */
 gqa_status_t gqa_decode_launch_count_for(int batch, int capacity, gqa_kv_format_t kv_format, int q_len,
                                          int num_splits, int sm_count, int* launches_out);

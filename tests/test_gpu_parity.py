@@ -891,6 +891,30 @@ def test_cluster_merge_only_for_single_wave_grids(B, T, merged_on_chip):
     _assert_parity(_gpu_rows(out), _oracle_full(t), f"B={B} T={T} splits={S}")
 
 
+@pytest.mark.parametrize("kv_dtype,B,S", [("e4m3", 8, 7), ("e4m3", 8, 6), ("i8", 8, 7), ("bf16", 4, 8),
+                                           ("bf16", 8, 4), ("f16", 19, 2)])
+def test_cluster_merge_matches_the_launch_count(kv_dtype, B, S):
+    # one-wave grids near full occupancy: the merge stays on chip only when
+    # every cluster can be resident at once (the device's cluster occupancy),
+    # else the combine kernel merges; the host-side launch count says which,
+    # the partial area shows which ran, and both match the oracle
+    C = 4096
+    w = inputs.custom(B, C, C // 2, C, kv_dtype=kv_dtype, kv_std=2.0 if kv_dtype == "e4m3" else 1.0)
+    t = _make(w)
+    fp8 = kv_dtype == "e4m3"
+    ws = torch.full((gq.workspace_size(B, C, S),), 0xA5, dtype=torch.uint8, device=DEV)
+    gq.workspace_init(ws)
+    p = _prepare(t, num_splits=S, workspace=ws)
+    gq.launch(p)
+    torch.cuda.synchronize()
+    kvf = {"f16": api.KV_F16, "bf16": api.KV_BF16, "e4m3": api.KV_E4M3, "i8": api.KV_I8}[kv_dtype]
+    n = api.launch_count(B, C, kvf, 1, S, torch.cuda.get_device_properties(DEV).multi_processor_count)
+    on_chip = bool(torch.all(ws[256:] == 0xA5))
+    print(f"PARITY cluster {kv_dtype} B={B} S={S}: {'on chip' if on_chip else 'combine kernel'}")
+    assert on_chip == (n == 1)
+    _assert_parity(_gpu_rows(p.out), _oracle_full(t), f"{kv_dtype} B={B} splits={S}")
+
+
 @pytest.mark.parametrize("kv_dtype", ["f16", "bf16", "e4m3", "i8"])
 @pytest.mark.parametrize("T", [2, 4])
 def test_balanced_verify_window(kv_dtype, T):
