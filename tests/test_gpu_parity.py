@@ -13,6 +13,8 @@ append + decode serving step, the paged, int8 and verify entry points), length
 clamping flags, the convenience and staged entry points, errors reported
 before launch, and the balanced schedule's edge cases.
 """
+import zlib
+
 import numpy as np
 import pytest
 import torch
@@ -543,6 +545,40 @@ def test_deterministic_across_runs():
     first = gq.launch(p).clone()
     for _ in range(3):
         assert torch.equal(gq.launch(p).view(torch.int16), first.view(torch.int16))
+
+
+@pytest.mark.parametrize("kv_dtype", ["f16", "bf16", "e4m3", "i8"])
+@pytest.mark.parametrize("T", [1, 2, 4])
+@pytest.mark.parametrize("grid", ["balanced", "cluster", "combine", "paged"])
+def test_determinism_soak(kv_dtype, T, grid):
+    # 16 launches back to back, no synchronisation between them, each output
+    # copied off on the stream: every one bitwise equal to the first.  A race
+    # in a merge area shared between a CTA's pieces, between the ring and the
+    # epilogue, or between cluster members would show as a differing bit.
+    B, C, S = {"balanced": (96, 2048, 4), "cluster": (2, 1024, 4), "combine": (2, 2048, 16),
+               "paged": (64, 2048, 4)}[grid]
+    rng = np.random.default_rng(zlib.crc32(f"{kv_dtype}/{T}/{grid}".encode()))
+    lens = rng.integers(T, C + 1, B).tolist()
+    w = inputs.custom(B, C, 1, kv_dtype=kv_dtype, kv_std=2.0 if kv_dtype == "e4m3" else 1.0, nan_tail=True,
+                      q_len=T)
+    t = _make(w, lens=lens)
+    fp8 = dict(k_scale=t["k_scale"], v_scale=t["v_scale"]) if kv_dtype == "e4m3" else {}
+    q4 = t["q"] if T > 1 else t["q"][:, None].contiguous()
+    ws = torch.zeros(gq.workspace_size(B * T, C, S), dtype=torch.uint8, device=DEV)
+    if grid == "paged":
+        pt = inputs.paginate(t, 64, extra_pages=2)
+        run = lambda: gq.gqa_decode_paged(q4 if T > 1 else t["q"], pt["kv_pages"], pt["block_table"],  # noqa: E731
+                                          pt["lens"], num_splits=S, workspace=ws,
+                                          kv_scales=pt.get("kv_scale_pages"), **fp8)
+    else:
+        run = lambda: gq.gqa_decode_verify(q4, t["kv"], t["lens"], num_splits=S, workspace=ws,  # noqa: E731
+                                           kv_scales=t["kv_scales"], **fp8)
+    outs = [run().clone() for _ in range(16)]
+    torch.cuda.synchronize()
+    first = outs[0].view(torch.int16)
+    for i, o in enumerate(outs[1:], 1):
+        assert torch.equal(o.view(torch.int16), first), f"{kv_dtype} T={T} {grid}: launch {i} differs"
+    assert not gq.get_status(ws) & (api.FLAG_WAIT_TIMEOUT | api.FLAG_LENGTH_CLAMPED)
 
 
 def test_concurrent_streams_with_their_own_workspaces():
