@@ -358,9 +358,23 @@ int plan_splits(int batch, int capacity, int kv_format, int sm_count) {
     // more partials.  Measured in CUDA graphs on GB300 (us per call, the
     // 8-wave rule -> this): bf16 1 x 4096 10.7 -> 9.0, 1 x 16384 20.6 -> 17.1,
     // 4 x 4096 16.4 -> 14.6, e4m3 1 x 8192 11.5 -> 10.3, fp16 1 x 1024 6.3.
+    //
+    // Batches of 8 or more rows of 4096 slots or more are not capped at one
+    // wave, so they run the balanced schedule: a decode batch's lengths are
+    // ragged, and only the balanced schedule spreads the actual tokens over
+    // all the resident CTAs (a one-wave grid waits for the CTAs of its
+    // longest rows).  Warm, in a CUDA graph, us per call, one wave ->
+    // balanced, lengths U[C/4, C] and all = C: bf16 8 x 4096 22.7 -> 18.9 and
+    // 24.2 -> 25.7, e4m3 16 x 4096 24.8 -> 21.2 and 26.4 -> 27.1, e4m3 8 x
+    // 4096 15.6 -> 14.7 and 17.2 -> 17.6, int8 8 x 8192 26.8 -> 22.6 and 28.3
+    // -> 28.3.  Shorter rows or smaller batches keep the one-wave grid: there
+    // the balanced grid's extra pieces and combine cost more than it
+    // balances (bf16 32 x 512 12.8 -> 14.9 and 13.7 -> 18.3, e4m3 16 x 1024
+    // 10.4 -> 12.6 and 11.1 -> 14.3; bf16 4 x 8192 22.2 -> 20.2 but 24.1 ->
+    // 26.1).
     long long s = (long long)std::llround(std::sqrt(6.0 * (double)nmax));
     const long long wave = slots / units;
-    if (s > wave) s = wave;
+    if (s > wave && !(batch >= 8 && capacity >= 4096)) s = wave;
     if (s < 1) s = 1;
     per = (capacity + s - 1) / s;
   } else {

@@ -88,7 +88,9 @@ def _chunk(C, S, fmt):
 # (batch, capacity, format, SM count) -> splits: about 8 waves of work items
 # (2 resident per SM for 16-bit KV, 3 for 8-bit KV) over the worst case, or,
 # when all rows hold at most 16 tiles per resident slot, about sqrt(6 * tiles
-# per row) capped at one wave; whole tiles per split (at least two), 1..256.
+# per row), capped at one wave unless the batch has 8 or more rows of 4096
+# slots or more (then the balanced schedule takes the grid); whole tiles per
+# split (at least two), 1..256.
 PLAN_TABLE = [
     ((1, 64, KV_F16, 152), 1),
     ((1, 1024, KV_F16, 152), 8),
@@ -105,6 +107,11 @@ PLAN_TABLE = [
     ((1, 16384, KV_BF16, 152), 37),
     ((4, 4096, KV_BF16, 152), 8),
     ((1, 8192, KV_E4M3, 152), 16),
+    ((8, 2048, KV_BF16, 152), 4),
+    ((32, 512, KV_BF16, 152), 1),
+    # batches of 8+ rows of 4096+ slots: not capped at one wave
+    ((8, 4096, KV_BF16, 152), 16),
+    ((16, 4096, KV_E4M3, 152), 11),
 ]
 
 
