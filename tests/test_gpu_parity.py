@@ -21,7 +21,7 @@ import torch
 
 import oracle
 import gqa_decode_attention_sm_gb300 as gq
-from gqa_decode_attention_sm_gb300 import api, inputs
+from gqa_decode_attention_sm_gb300 import _lib, api, inputs
 from helpers import HQ, RMS_GATE, bits_of, rms_gate_ok, tolerance_ok, ulps_apart
 
 pytestmark = pytest.mark.gpu
@@ -579,6 +579,60 @@ def test_determinism_soak(kv_dtype, T, grid):
     for i, o in enumerate(outs[1:], 1):
         assert torch.equal(o.view(torch.int16), first), f"{kv_dtype} T={T} {grid}: launch {i} differs"
     assert not gq.get_status(ws) & (api.FLAG_WAIT_TIMEOUT | api.FLAG_LENGTH_CLAMPED)
+
+
+def test_host_threads_launch_concurrently():
+    # Four host threads, each with its own stream and prepared problem
+    # (different formats and schedules), launch 10 times each while a fifth
+    # thread makes calls that fail validation.  The library's shared state
+    # (device set-up, the per-device tables) is guarded and its last-error
+    # string is per thread: every output equals its sequential run bit for
+    # bit, and each failing call reads its own message.
+    import threading
+    problems = [
+        _make(inputs.custom(48, 2048, 1, 2048)),                                   # fp16, balanced
+        _make(inputs.custom(2, 1024, 1024, kv_dtype="bf16")),                        # bf16, cluster merge
+        _make(inputs.custom(64, 4096, 1024, 4096, kv_dtype="e4m3", kv_std=2.0)),    # e4m3, balanced
+        _make(inputs.custom(8, 4096, 1024, 4096, kv_dtype="i8")),                   # int8, balanced
+    ]
+    preps = [_prepare(t) for t in problems]
+    refs = [gq.launch(p).clone() for p in preps]
+    torch.cuda.synchronize()
+    for p in preps:
+        p.out.zero_()
+    errors, failures = [], []
+    start = threading.Barrier(5)
+
+    def worker(i):
+        try:
+            s = torch.cuda.Stream()
+            start.wait()
+            with torch.cuda.stream(s):
+                for _ in range(10):
+                    gq.launch(preps[i])
+            s.synchronize()
+        except Exception as e:  # noqa: BLE001 - reported below
+            errors.append(f"thread {i}: {e!r}")
+
+    def failing():
+        lib = _lib.load()
+        start.wait()
+        for k in range(200):
+            st = lib.gqa_decode_prepared(None, None, None, None, 1, 64 + k, 0, 1.0, 1, None, 0, None)
+            msg = lib.gqa_last_error().decode()
+            if st == 0 or "null" not in msg:
+                failures.append((st, msg))
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(4)] + [threading.Thread(target=failing)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join(timeout=120)
+    assert not errors, errors
+    assert not failures, failures[:3]
+    torch.cuda.synchronize()
+    for i, (p, ref) in enumerate(zip(preps, refs)):
+        assert torch.equal(p.out.view(torch.int16), ref.view(torch.int16)), f"problem {i} differs"
 
 
 def test_concurrent_streams_with_their_own_workspaces():
