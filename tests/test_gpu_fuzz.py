@@ -83,6 +83,25 @@ def _balanced_cases():
     return out
 
 
+def _long_row_cases():
+    """Automatic plans for batches of 8-16 rows of 4096-8192 slots, where
+    the one-wave grid gives way to the balanced schedule; uniform and ragged
+    lengths, 1-2 query tokens, contiguous or paged."""
+    rng = np.random.default_rng(11)
+    out = []
+    while len(out) < 8:
+        kv_dtype = str(rng.choice(["f16", "bf16", "e4m3", "i8"]))
+        T = int(rng.choice([1, 1, 2]))
+        B = int(rng.choice([8, 12, 16]))
+        C = int(rng.choice([4096, 6144, 8192]))
+        if B * C * T > 140_000:
+            continue
+        paged = bool(rng.random() < 0.3)
+        lens = [C] * B if rng.random() < 0.3 else rng.integers(max(T, C // 4), C + 1, B).tolist()
+        out.append((200 + len(out), kv_dtype, T, paged, 256, B, C, [int(x) for x in lens], None, 1.0))
+    return out
+
+
 @pytest.fixture(scope="module", autouse=True)
 def _built():
     from gqa_decode_attention_sm_gb300 import build as gbuild
@@ -91,7 +110,7 @@ def _built():
     torch.cuda.init()
 
 
-@pytest.mark.parametrize("case", _cases() + _balanced_cases(), ids=lambda c: f"case{c[0]}-{c[1]}-T{c[2]}-{'paged' if c[3] else 'contig'}"
+@pytest.mark.parametrize("case", _cases() + _balanced_cases() + _long_row_cases(), ids=lambda c: f"case{c[0]}-{c[1]}-T{c[2]}-{'paged' if c[3] else 'contig'}"
                          f"-B{c[5]}-C{c[6]}-S{c[8]}")
 def test_random_case_matches_oracle(case):
     idx, kv_dtype, T, paged, page, B, C, lens, S, q_scale = case
