@@ -28,6 +28,7 @@ FLAG_LENGTH_CLAMPED = 0x1
 FLAG_WAIT_TIMEOUT = 0x2
 FLAG_PAGE_CLAMPED = 0x4
 FLAG_SLOT_CLAMPED = 0x8
+FLAG_BOUNDS = 0x10  # range-checked build only: an access fell outside its buffer
 
 _QDT = {torch.float16: F16, torch.bfloat16: BF16}
 _KVF = {torch.float16: KV_F16, torch.bfloat16: KV_BF16, torch.uint8: KV_E4M3,
@@ -37,7 +38,8 @@ __all__ = ["GqaError", "append_kv_paged", "gqa_decode", "gqa_decode_fp8kv", "gqa
            "gqa_decode_verify", "append_kv",
            "prepare", "launch",
            "Prepared",
-           "workspace_size", "plan", "get_status", "split_stage", "combine_stage", "split_geometry"]
+           "workspace_size", "plan", "get_status", "split_stage", "combine_stage", "split_geometry",
+           "launch_count"]
 
 
 def _ptr(t: torch.Tensor) -> int:

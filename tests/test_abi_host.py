@@ -368,3 +368,13 @@ def test_extent_cuts_are_refused_by_the_product_build(lib):
     assert lib.gqa_decode_debug_cut_extents(1, 0) == EINVAL
     assert lib.gqa_decode_debug_cut_extents(0, 4096) == EINVAL
     assert "checked build" in lib.gqa_last_error().decode()
+
+
+def test_status_flags_agree_with_the_header():
+    # every GQA_FLAG_* of the header has the binding's value
+    text = open(HEADER).read()
+    flags = dict(re.findall(r"#define GQA_FLAG_([A-Z_]+)\s+(0x[0-9a-fA-F]+)u", text))
+    from gqa_decode_attention_sm_gb300 import api
+    assert flags, "no GQA_FLAG_* in the header"
+    for name, value in flags.items():
+        assert getattr(api, "FLAG_" + name) == int(value, 16), name

@@ -28,7 +28,7 @@ pytestmark = pytest.mark.gpu
 
 DEV = torch.device("cuda", 0)
 FMT = {"f16": oracle.F16, "bf16": oracle.BF16, "e4m3": oracle.E4M3, "i8": oracle.I8}
-FLAG_BOUNDS = 0x10
+FLAG_BOUNDS = api.FLAG_BOUNDS
 
 
 @pytest.fixture(scope="module", autouse=True)
