@@ -138,9 +138,18 @@ constexpr int kBalMaxBatch = 1024;
 constexpr int kBalMergeBytes = kMmaConsumerWarps * kGroup * (kD + 2) * 4;
 static_assert((kMmaThreads + 3 + kBalMaxBatch) * 4 <= kBalMergeBytes, "the length scan uses the merge area");
 constexpr int kBalRunBytes = 16;  // the run length Q, after the merge area
+// 3- and 4-token windows over 8-bit caches keep their Q^T fragments in
+// shared memory, one copy per CTA ([k-step][lane][n-tile][2 words]; in the
+// balanced schedule's merge area, idle while a piece streams, else after the
+// ring's barriers): 32 registers fewer, so each warp can take two slabs of a
+// tile together without spills.
+__host__ __device__ constexpr bool mma_q_in_smem(int kvf, int nq) { return is_8bit(kvf) && nq > 2; }
+constexpr int kQSmemBytes = 8 * 32 * 2 * 2 * 4;
 __host__ __device__ constexpr int mma_smem_bytes(int kvf, int nq, bool bal = false) {
-  return mma_stages(kvf, nq) * (kStageBytes + kScaleStageBytes + 2 * 8) + (bal ? kBalMergeBytes + kBalRunBytes : 0);
+  return mma_stages(kvf, nq) * (kStageBytes + kScaleStageBytes + 2 * 8) + (bal ? kBalMergeBytes + kBalRunBytes : 0) +
+         (!bal && mma_q_in_smem(kvf, nq) ? kQSmemBytes : 0);
 }
+static_assert(kQSmemBytes <= kBalMergeBytes, "the Q^T fragments fit the merge area");
 // 228 KB of shared memory per SM, 1 KB of it reserved per resident CTA
 static_assert(2 * (mma_smem_bytes(kKvF16, kMaxQLen, true) + 1024) <= 228 * 1024 &&
                   2 * (mma_smem_bytes(kKvF16, 1, true) + 1024) <= 228 * 1024 &&
@@ -190,6 +199,16 @@ __device__ __forceinline__ uint32_t transpose8x8_b16(uint32_t x) {
   uint32_t y;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
   return y;
+}
+
+// 16 bytes of this CTA's shared memory, loaded where the code reads them
+// (volatile: never hoisted into registers held across the loop)
+__device__ __forceinline__ uint4 ld_shared_u4(const void* p) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"((uint32_t)__cvta_generic_to_shared(p)));
+  return v;
 }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
@@ -439,13 +458,16 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
   using T = KvTraits<KVF>;
   constexpr bool kBF16 = kMmaBF16<KVF>;
   constexpr int kSlabs = T::kTile / (16 * kMmaConsumerWarps);  // 16-token slabs per warp per tile
-  // Slabs taken together: two for 4-token windows over an e4m3 cache, whose
-  // 16 columns are all real and which is latency-bound (more independent
-  // work between the max reductions, half as many of them).  Measured cold
-  // at 64 x U[16k, 32k] on GB300: e4m3 4 tokens 540.7 -> 514.1 us; the
-  // 3-token e4m3 and the int8 windows were slower (507.9 -> 526.3, int8
-  // 618.5 / 620.5 -> 639.0 / 669.7: more spills at 168 registers).
-  constexpr int kSG = KVF == kKvE4M3 && NQ == 4 ? 2 : 1;
+  // Slabs taken together: two for 3- and 4-token windows over 8-bit caches,
+  // which are latency-bound (more independent work between the max
+  // reductions, half as many of them).  With the Q^T fragments in shared
+  // memory (kQS) they fit the 168 registers with small spills; measured cold
+  // at 64 x U[16k, 32k] on GB300, one slab -> pairs, us per call: e4m3 3 / 4
+  // tokens 507.9 / 540.7 -> 503.8 / 507.9, int8 618.5 / 620.5 -> 602.1 /
+  // 616.4 (pairs with Q in registers spilled more and made all but the e4m3
+  // 4-token window slower).
+  constexpr int kSG = is_8bit(KVF) && NQ > 2 ? 2 : 1;
+  constexpr bool kQS = mma_q_in_smem(KVF, NQ);
   static_assert(kSlabs % kSG == 0, "whole slab groups");
   constexpr int kCols = kGroup * NQ;                            // (query token, head) columns
   constexpr int kNT = (kCols + 7) / 8;                          // 8-column mma n-tiles
@@ -469,6 +491,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
   float* cl_state = mrg_l + kMmaConsumerWarps * kRC;
   // balanced schedule: the run length Q, read by the cursor at each piece
   int* q_sm = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(mrg_acc) + kBalMergeBytes);
+  uint32_t* qfr = reinterpret_cast<uint32_t*>(empty + kMmaStages);  // Q^T fragments (kQS)
 
   // Every CTA of this grid is resident or done: let the next grid in the
   // stream (stage 2, or the next launch after an on-chip merge) be scheduled;
@@ -571,6 +594,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
     if (x0 >= total) return;  // more CTAs than work
     const int b0 = scan[kMmaThreads + 1];
     cur.start(b0, scan[kMmaThreads + 2], lsh[b0], b0 + 1 < B ? lsh[b0 + 1] : 0, x0, min(x0 + q, total), q_sm, rc);
+    if constexpr (kQS) __syncthreads();  // every thread has read the scratch the Q^T fragments overwrite
   } else {
     // one piece per CTA: split s of row (b, g)
     const int g = blockIdx.x, b = blockIdx.y, s = blockIdx.z;
@@ -761,6 +785,8 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
     // Column n of n-tile nt is (query token 2nt + n/4, head n%4).  This lane's
     // score/output columns are n = 2cq, 2cq+1: query token 2nt + cq/2, heads
     // 2(cq%2) and 2(cq%2)+1.  A column past the window is zero padding.
+    // (Q^T in shared memory: the previous piece's merge has read its area)
+    if constexpr (kQS && BAL) named_barrier_sync(1, kMmaConsumerWarps * 32);
     int lim[kNT];  // slots below lim[nt] are attended by this lane's columns
 #pragma unroll
     for (int nt = 0; nt < kNT; ++nt) {
@@ -847,6 +873,16 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
         kb[nt][1] = -kI8Bias * sl2c[nt][1] * __shfl_sync(0xffffffffu, qs, 8 * cq + 4);
       }
     }
+    if constexpr (kQS) {
+      static_assert(kNT == 2, "the shared Q^T layout holds two n-tiles");
+      if (warp == 0) {  // every consumer warp holds the same fragments
+  #pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          *reinterpret_cast<uint4*>(qfr + (ks * 32 + lane) * 4) =
+              make_uint4(qb[0][ks][0], qb[0][ks][1], qb[1][ks][0], qb[1][ks][1]);
+      }
+      named_barrier_sync(1, kMmaConsumerWarps * 32);
+    }
 
     float o[kNT][8][4];
     float m[kNT][2], l[kNT][2];  // per column: running max (log2 domain), this lane's denominator share
@@ -916,8 +952,15 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
                 uint32_t a0, a1, a2, a3;
                 widen4_biased<KVF>(xs[s4], a0, a2);  // row gq: dims (4s,4s+1), (4s+2,4s+3)
                 widen4_biased<KVF>(ys[s4], a1, a3);  // row gq+8
+                if constexpr (kQS) {
+                  const uint4 qv = ld_shared_u4(qfr + (ks * 32 + lane) * 4);
+                  mma16816<false>(sc[0], a0, a1, a2, a3, qv.x, qv.y);
+                  mma16816<false>(sc[kNT - 1], a0, a1, a2, a3, qv.z, qv.w);
+                } else {
   #pragma unroll
-                for (int nt = 0; nt < kNT; ++nt) mma16816<false>(sc[nt], a0, a1, a2, a3, qb[nt][ks][0], qb[nt][ks][1]);
+                  for (int nt = 0; nt < kNT; ++nt)
+                    mma16816<false>(sc[nt], a0, a1, a2, a3, qb[nt][ks][0], qb[nt][ks][1]);
+                }
               }
             }
           } else {
