@@ -712,11 +712,11 @@ def run_gpu(args):
     from gqa_decode_attention_sm_gb300 import inputs
 
     rank, world, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)  # before the process group, so NCCL binds this rank's GPU
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
     if rank == 0:
         gbuild.build()
     barrier(world)
