@@ -751,19 +751,27 @@ def test_errors_are_reported_before_launch():
     assert e.value.name == "GQA_ERR_ALIASING"
 
 
-def test_stalled_pipeline_times_out_is_flagged_and_context_survives():
-    # The test hook never issues tile 3 of each split: the consumers' bounded
-    # wait runs out after 100 ms, the CTAs flag GQA_FLAG_WAIT_TIMEOUT, drain
-    # their own copies and return.  No fault, no hang; the next launch is fine.
+@pytest.mark.parametrize("grid", ["cluster", "combine", "balanced"])
+def test_stalled_pipeline_times_out_is_flagged_and_context_survives(grid):
+    # The test hook never issues tile 3 of each split (of each CTA's stream
+    # under the balanced schedule): the consumers' bounded wait runs out
+    # after 100 ms, and so does the producer's wait for the stage they never
+    # release; the CTAs flag GQA_FLAG_WAIT_TIMEOUT, skip their remaining
+    # tiles, still pass every barrier of their epilogues (and, in a cluster,
+    # the cluster barriers), drain their own copies and return.  No fault, no
+    # hang; the next launch is fine.
     import time
-    t = _make(inputs.custom(1, 1024, 1024))
-    p = _prepare(t, num_splits=2)  # 16 CTAs of 8 tiles
+    B, C, S = {"cluster": (1, 1024, 2),       # 16 CTAs of 8 tiles, clusters of 2
+               "combine": (2, 4096, 16),      # one-wave grid of 256 CTAs of 4 tiles, 16 splits
+               "balanced": (48, 2048, 8)}[grid]  # 3072 pieces > one wave: the balanced grid
+    t = _make(inputs.custom(B, C, C))
+    p = _prepare(t, num_splits=S)
     lib = api._lib.load()
     stream = torch.cuda.current_stream(DEV).cuda_stream
     t0 = time.time()
     st = lib.gqa_decode_debug_skip_tile(
-        t["q"].data_ptr(), 0, t["kv"].data_ptr(), 0, t["lens"].data_ptr(), p.out.data_ptr(), 1, 1024,
-        1.0, 1.0, 1.0, 2, p.workspace.data_ptr(), p.workspace_bytes, 3, 100_000_000, stream)
+        t["q"].data_ptr(), 0, t["kv"].data_ptr(), 0, t["lens"].data_ptr(), p.out.data_ptr(), B, C,
+        1.0, 1.0, 1.0, S, p.workspace.data_ptr(), p.workspace_bytes, 3, 100_000_000, stream)
     assert st == 0, lib.gqa_last_error().decode()
     flags = gq.get_status(p)  # synchronises
     assert flags & api.FLAG_WAIT_TIMEOUT
