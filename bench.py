@@ -13,6 +13,8 @@ call, so the L2 holds none of the inputs and no dirty lines).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 4]
   python bench.py --impl reference ...   # the FP64 CPU oracle, same metric
+  python bench.py --sweep                # + the automatic plan over SWEEP_SHAPES, cold
+  python bench.py --read-ceiling         # + the read rate of the same data movement without arithmetic
 
 GB/s counts algorithmic bytes: sum_b len_b x (4096 B fp16/bf16 | 2048 B e4m3)
 of K+V, plus q, out and the lengths; workspace traffic is not counted.
