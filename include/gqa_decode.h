@@ -250,10 +250,12 @@ gqa_status_t gqa_decode_verify(const void* q, gqa_dtype_t q_dtype, const void* k
  * them separately.  Stage 1 streams K/V once per (b, KV head, split) and
  * writes FP32 partials to the workspace, or the final output when
  * num_splits == 1 or when its 2..8 effective splits merge on chip (one
- * thread-block cluster per (b, KV head), one piece per CTA, one wave).  Stage 2 merges
- * the partials of each (b, query head) with a log-sum-exp combine and writes
- * `out`; when stage 1 wrote the output it launches nothing.  Both must be given the same geometry, scales and workspace, in
- * this order, on one stream.  Validation as gqa_decode_prepared, except that
+ * thread-block cluster per (b, KV head), one piece per CTA, one wave, every
+ * cluster resident at once).  Stage 2 merges the partials of each (b, query
+ * head) with a log-sum-exp combine and writes `out`; when stage 1 wrote the
+ * output it launches nothing.  Both must be given the same geometry, scales
+ * and workspace, in this order, on one stream, with the same device
+ * current.  Validation as gqa_decode_prepared, except that
  * q_scale may be 0.  Stage 1 does not take an int8 cache (it has no scale
  * argument: use gqa_decode_int8kv); stage 2 accepts every format. */
 gqa_status_t gqa_decode_split_stage(const void* q, gqa_dtype_t q_dtype, const void* kv,
