@@ -520,6 +520,75 @@ def planner_sweep(dev, peak, gq, inputs, quick=False):
     return rows
 
 
+def warm_graph_us(fn, calls=20, reps=10):
+    """us per call of `fn` with warm L2, launched from one CUDA graph of
+    `calls` back-to-back calls (median over `reps` replays)."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(calls):
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    return time_calls(g.replay, reps) / calls
+
+
+def append_rows(dev, gq, inputs, flush, quick=False):
+    """The step before decode (RMS norm + RoPE of each request's new token,
+    its K and V written into the cache at a device-side slot), alone and as
+    a serving step with the decode that follows, both launched from one CUDA
+    graph; over workloads 4 and 5.  Each call rewrites the last slot below
+    the length, so every call writes the same bytes."""
+    import torch
+    rows = {}
+    for key, w in (("4-append-decode", inputs.WORKLOADS[4]), ("5-append-decode", inputs.WORKLOADS[5])):
+        t = inputs.make(w, dev)
+        B = w.batch
+        g = torch.Generator(device=dev)
+        g.manual_seed(4242)
+
+        def rnd(*shape, scale=1.0, base=0.0):
+            return (base + scale * torch.randn(shape, generator=g, device=dev)).to(torch.bfloat16)
+
+        qp, kp, vp = rnd(B, 32, 128), rnd(B, 8, 128), rnd(B, 8, 128)
+        wq, wk = rnd(128, scale=0.1, base=1.0), rnd(128, scale=0.1, base=1.0)
+        slots = (t["lens"] - 1).contiguous()
+        pos = slots.clone()
+        fp8 = w.kv_dtype == "e4m3"
+        ks, vs = (t["k_scale"], t["v_scale"]) if fp8 else (1.0, 1.0)
+        q_out = torch.empty(B, 32, 128, dtype=torch.bfloat16, device=dev)
+        out = torch.empty_like(q_out)
+        hdr = torch.zeros(256, dtype=torch.uint8, device=dev)
+        tensors = {"Q": q_out, "KV": t["kv"], "O": out, "sequence_lengths": t["lens"]}
+        p = gq.prepare(tensors, q_scale=t["q_scale"], k_scale=ks if fp8 else None, v_scale=vs if fp8 else None)
+
+        def append():
+            gq.append_kv(qp, kp, vp, wq, wk, pos, slots, t["kv"], q_out=q_out, k_scale=ks, v_scale=vs,
+                         kv_scales=t["kv_scales"], workspace=hdr)
+
+        def step():
+            append()
+            gq.launch(p)
+
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        n = 5 if quick else 20
+        rows[key] = {
+            "append_us_cold": round(cold_graph_us(append, flush, calls=10 if quick else 40, reps=3 if quick else 7), 3),
+            "append_us_warm_graph": round(warm_graph_us(append, calls=n), 3),
+            "step_us_warm_graph": round(warm_graph_us(step, calls=n), 2),
+            "decode_us_warm_graph": round(warm_graph_us(lambda: gq.launch(p), calls=n), 2),
+            "batch": B, "kv": w.kv_dtype,
+            "note": (f"append (norm + RoPE + K/V write, {B} requests) alone, cold (graph difference) and warm "
+                     "(in a CUDA graph); a serving step = append then decode over the full cache, in a CUDA "
+                     "graph, next to the decode alone"),
+        }
+        del t, out, p, tensors
+        torch.cuda.empty_cache()
+    return rows
+
+
 def per_config_table(dev, peak, gq, inputs, quick=False, cpu=True):
     import torch
     flush = make_cold_flush(dev)
@@ -675,6 +744,9 @@ def per_config_table(dev, peak, gq, inputs, quick=False, cpu=True):
                              "note": "int8 codes + bf16 row scales (workload 5 shape) in shuffled 256-token pages"}
     del t, pt, out, ws
     torch.cuda.empty_cache()
+
+    # the append step, alone and followed by the decode (a serving step)
+    table.update(append_rows(dev, gq, inputs, flush, quick=quick))
 
     # one long request: bf16, batch 1, 131072 tokens (all parallelism from splitting the row)
     w = inputs.custom(1, 131072, 131072, kv_dtype="bf16", index=4)

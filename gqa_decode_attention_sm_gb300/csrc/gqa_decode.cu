@@ -740,7 +740,7 @@ gqa_status_t append_kv(const void* q_proj, const void* k_proj, const void* v_pro
   ap.eps = eps;
   ap.k_inv_scale = 1.f / k_scale;
   ap.v_inv_scale = 1.f / v_scale;
-  ap.theta = (double)rope_theta;
+  for (int i = 0; i < kD / 2; ++i) ap.inv_freq[i] = std::pow((double)rope_theta, -(double)i / (kD / 2));
   ap.kv_rows = units * 2 * kHkv * unit_rows;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(batch, 1, 1);

@@ -18,7 +18,11 @@
 // One CTA per batch row, 8 warps; each warp takes whole head vectors and lane
 // l holds dims l, l+32, l+64, l+96, so every RoPE pair (i, i+64) stays in one
 // lane.  The 64 angles are formed in FP64 (pos * theta^(-i/64) reaches 1e5
-// radians at long contexts, beyond FP32's reach) once per CTA.
+// radians at long contexts, beyond FP32's reach) once per CTA: the inverse
+// frequencies theta^(-i/64) come from the host (FP64, once per call), and
+// each angle is reduced modulo 2 pi before its sine and cosine (FP64 is
+// slow on this GPU: forming the frequencies and reducing large angles on
+// the device took half of the kernel's time).
 //
 // Precision: the result before its one rounding is within about 2^-21 of the
 // exact value relative to itself, so the stored fp16/bf16 value is the
@@ -54,7 +58,7 @@ struct AppendParams {
   const int32_t* block_table;
   int max_pages, num_pages, page_log2;
   float eps, k_inv_scale, v_inv_scale;  // e4m3: 1/k_scale, 1/v_scale
-  double theta;
+  double inv_freq[kD / 2];  // theta^(-i/64), i = 0..63, formed on the host in FP64
   size_t kv_rows;  // rows of 128 in the cache (units x 2 x 8 x rows per unit), for checked builds
 };
 
@@ -70,6 +74,12 @@ __device__ __forceinline__ uint16_t round_elem(float x) {
   if constexpr (QF == kQF16) return __half_as_ushort(__float2half_rn(x));
   else return __bfloat16_as_ushort(__float2bfloat16_rn(x));
 }
+
+// 2 pi as the double nearest to it plus the double nearest to the rest (the
+// two parts agree with 2 pi to about 2^-107 relative), and 1 / (2 pi).
+constexpr double kTwoPiHi = 0x1.921fb54442d18p+2;
+constexpr double kTwoPiLo = 0x1.1a62633145c07p-52;
+constexpr double kInvTwoPi = 0x1.45f306dc9c883p-3;
 
 __device__ __forceinline__ uint8_t to_e4m3(float x) {
   uint16_t two;
@@ -98,9 +108,16 @@ __global__ void __launch_bounds__(kAppendThreads) append_kv_kernel(const __grid_
   const int b = blockIdx.x;
   const int pos = __ldg(p.positions + b);
   if (threadIdx.x < kD / 2) {
-    const double a = (double)pos * pow(p.theta, -(double)threadIdx.x / (kD / 2));
+    // a = pos * theta^(-i/64), less k whole turns: the FMA forms a - k * hi
+    // with the product exact and one rounding of a result below about 4, and
+    // the second FMA takes off k * lo, so r equals the reduced angle to about
+    // 2^-51 absolute for any k below 2^31
+    const double a = (double)pos * p.inv_freq[threadIdx.x];
+    const double k = rint(a * kInvTwoPi);
+    double r = fma(-k, kTwoPiHi, a);
+    r = fma(-k, kTwoPiLo, r);
     double sv, cv;
-    sincos(a, &sv, &cv);
+    sincos(r, &sv, &cv);
     const float ch = (float)cv, sh = (float)sv;
     cs[threadIdx.x] = ch;
     cs_lo[threadIdx.x] = (float)(cv - (double)ch);
