@@ -15,9 +15,9 @@
 // e4m3 (value / scale, RNE, saturating), int8 (one bf16 scale amax/127 per
 // row, codes round-to-nearest-even, clipped to +-127).
 //
-// One CTA per batch row, 8 warps; each warp takes whole head vectors and lane
-// l holds dims l, l+32, l+64, l+96, so every RoPE pair (i, i+64) stays in one
-// lane.  The 64 angles are formed in FP64 (pos * theta^(-i/64) reaches 1e5
+// One CTA per batch row, 8 warps; each warp takes six whole head vectors (all
+// their loads issued together) and lane l holds dims l, l+32, l+64, l+96, so
+// every RoPE pair (i, i+64) stays in one lane.  The 64 angles are formed in FP64 (pos * theta^(-i/64) reaches 1e5
 // radians at long contexts, beyond FP32's reach) once per CTA: the inverse
 // frequencies theta^(-i/64) come from the host (FP64, once per call), and
 // each angle is reduced modulo 2 pi before its sine and cosine (FP64 is
@@ -107,6 +107,30 @@ __global__ void __launch_bounds__(kAppendThreads) append_kv_kernel(const __grid_
   pdl_wait_prior_grid();
   const int b = blockIdx.x;
   const int pos = __ldg(p.positions + b);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int dims[4] = {lane, lane + 32, lane + 64, lane + 96};
+  // Every load of this warp's head vectors (vectors 0..31: query heads;
+  // 32..39: key heads; 40..47: value heads; warp w takes w, w + 8, ...) and
+  // of both norm weights is issued here, before the angles: they overlap one
+  // another and the FP64 work, instead of one round of latency per vector.
+  constexpr int kVecs = kHq + 2 * kHkv, kWarps = kAppendThreads / 32, kPerWarp = kVecs / kWarps;
+  static_assert(kVecs % kWarps == 0, "whole vectors per warp");
+  float zz[kPerWarp][4], wq[4], wk[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    wq[k] = load_elem<QF>(p.q_norm_w, dims[k]);
+    wk[k] = load_elem<QF>(p.k_norm_w, dims[k]);
+  }
+#pragma unroll
+  for (int j = 0; j < kPerWarp; ++j) {
+    const int v = warp + kWarps * j;
+    const bool is_q = v < kHq, is_k = v >= kHq && v < kHq + kHkv;
+    const int g = is_q ? 0 : (v - kHq) % kHkv;
+    const void* src = is_q ? p.q_proj : (is_k ? p.k_proj : p.v_proj);
+    const size_t row = is_q ? ((size_t)b * kHq + v) * kD : ((size_t)b * kHkv + g) * kD;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) zz[j][k] = load_elem<QF>(src, row + dims[k]);
+  }
   if (threadIdx.x < kD / 2) {
     // a = pos * theta^(-i/64), less k whole turns: the FMA forms a - k * hi
     // with the product exact and one rounding of a result below about 4, and
@@ -142,28 +166,24 @@ __global__ void __launch_bounds__(kAppendThreads) append_kv_kernel(const __grid_
     unit_rows = (size_t)1 << p.page_log2;
     row_in = (size_t)(slot & ((1 << p.page_log2) - 1));
   }
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int dims[4] = {lane, lane + 32, lane + 64, lane + 96};
-
-  // vectors 0..31: query heads; 32..39: key heads; 40..47: value heads
-  for (int v = warp; v < kHq + 2 * kHkv; v += kAppendThreads / 32) {
+#pragma unroll
+  for (int j = 0; j < kPerWarp; ++j) {
+    const int v = warp + kWarps * j;
     const bool is_q = v < kHq, is_k = v >= kHq && v < kHq + kHkv;
     const int g = is_q ? 0 : (v - kHq) % kHkv;
-    const void* src = is_q ? p.q_proj : (is_k ? p.k_proj : p.v_proj);
     const size_t row = is_q ? ((size_t)b * kHq + v) * kD : ((size_t)b * kHkv + g) * kD;
     float z[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) z[k] = load_elem<QF>(src, row + dims[k]);
+    for (int k = 0; k < 4; ++k) z[k] = zz[j][k];
     if (!is_q && !is_k && !slot_ok) continue;
     if (is_q || is_k) {
       float ss = z[0] * z[0] + z[1] * z[1] + z[2] * z[2] + z[3] * z[3];
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
       const float r = 1.f / sqrtf(ss / kD + p.eps);
-      const void* w = is_q ? p.q_norm_w : p.k_norm_w;
       float a[4];  // x * w, exact
 #pragma unroll
-      for (int k = 0; k < 4; ++k) a[k] = z[k] * load_elem<QF>(w, dims[k]);
+      for (int k = 0; k < 4; ++k) a[k] = z[k] * (is_q ? wq[k] : wk[k]);
       // pairs (lane, lane+64) with angle lane, (lane+32, lane+96) with angle lane+32
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
