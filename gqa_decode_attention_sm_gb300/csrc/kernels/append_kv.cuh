@@ -20,9 +20,9 @@
 // every RoPE pair (i, i+64) stays in one lane.  The 64 angles are formed in FP64 (pos * theta^(-i/64) reaches 1e5
 // radians at long contexts, beyond FP32's reach) once per CTA: the inverse
 // frequencies theta^(-i/64) come from the host (FP64, once per call), and
-// each angle is reduced modulo 2 pi before its sine and cosine (FP64 is
-// slow on this GPU: forming the frequencies and reducing large angles on
-// the device took half of the kernel's time).
+// the sine and cosine are evaluated by sincos_series below (FP64 is slow on
+// this GPU: forming the frequencies with pow and the library's sincos of
+// angles up to 1e6 rad took about two thirds of the kernel's time).
 //
 // Precision: the result before its one rounding is within about 2^-21 of the
 // exact value relative to itself, so the stored fp16/bf16 value is the
@@ -75,11 +75,49 @@ __device__ __forceinline__ uint16_t round_elem(float x) {
   else return __bfloat16_as_ushort(__float2bfloat16_rn(x));
 }
 
-// 2 pi as the double nearest to it plus the double nearest to the rest (the
-// two parts agree with 2 pi to about 2^-107 relative), and 1 / (2 pi).
-constexpr double kTwoPiHi = 0x1.921fb54442d18p+2;
-constexpr double kTwoPiLo = 0x1.1a62633145c07p-52;
-constexpr double kInvTwoPi = 0x1.45f306dc9c883p-3;
+// pi / 2 as the double nearest to it plus the double nearest to the rest
+// (together within about 2^-107 of pi / 2, relative), and 2 / pi.
+constexpr double kHalfPiHi = 0x1.921fb54442d18p+0;
+constexpr double kHalfPiLo = 0x1.1a62633145c07p-54;
+constexpr double kTwoOverPi = 0x1.45f306dc9c883p-1;
+
+// sin a and cos a in FP64 for an angle below 2^31 radians, from the
+// mathematics rather than the library routine (whose general path is slow
+// where FP64 is): a = q pi/2 + x with q the integer nearest 2a/pi, q pi/2
+// taken off by two FMAs (the first with the product exact and one rounding
+// of a result below 1, the second taking off q times the rest of pi/2), so
+// |x| <= pi/4 within about 2^-52; then the Taylor series of sin x and cos x
+// about 0 to the x^17 and x^16 terms by Horner's rule in x^2 (Estrin's
+// scheme, fewer dependent steps, measured no faster), with the
+// coefficients (-1)^k/(2k+1)! and (-1)^k/(2k)! rounded to doubles (the first
+// terms left out are below 2^-60 for |x| <= pi/4); q mod 4 picks the
+// quadrant: the swap of sin and cos and their signs.  Within a few units of
+// 2^-53 of the exact values at the given a.
+__device__ __forceinline__ void sincos_series(double a, double& s, double& c) {
+  constexpr double kSin[9] = {0x1p+0, -0x1.5555555555555p-3, 0x1.1111111111111p-7, -0x1.a01a01a01a01ap-13,
+                              0x1.71de3a556c734p-19, -0x1.ae64567f544e4p-26, 0x1.6124613a86d09p-33,
+                              -0x1.ae7f3e733b81fp-41, 0x1.952c77030ad4ap-49};
+  constexpr double kCos[9] = {0x1p+0, -0x1p-1, 0x1.5555555555555p-5, -0x1.6c16c16c16c17p-10,
+                              0x1.a01a01a01a01ap-16, -0x1.27e4fb7789f5cp-22, 0x1.1eed8eff8d898p-29,
+                              -0x1.93974a8c07c9dp-37, 0x1.ae7f3e733b81fp-45};
+  const double q = rint(a * kTwoOverPi);
+  double x = fma(-q, kHalfPiHi, a);
+  x = fma(-q, kHalfPiLo, x);
+  const double x2 = x * x;
+  double ps = kSin[8], pc = kCos[8];
+#pragma unroll
+  for (int k = 7; k >= 0; --k) {
+    ps = fma(ps, x2, kSin[k]);
+    pc = fma(pc, x2, kCos[k]);
+  }
+  const double sx = x * ps, cx = pc;
+  switch ((int)((long long)q & 3)) {
+    case 0: s = sx; c = cx; break;
+    case 1: s = cx; c = -sx; break;
+    case 2: s = -sx; c = -cx; break;
+    default: s = -cx; c = sx; break;
+  }
+}
 
 __device__ __forceinline__ uint8_t to_e4m3(float x) {
   uint16_t two;
@@ -132,16 +170,10 @@ __global__ void __launch_bounds__(kAppendThreads) append_kv_kernel(const __grid_
     for (int k = 0; k < 4; ++k) zz[j][k] = load_elem<QF>(src, row + dims[k]);
   }
   if (threadIdx.x < kD / 2) {
-    // a = pos * theta^(-i/64), less k whole turns: the FMA forms a - k * hi
-    // with the product exact and one rounding of a result below about 4, and
-    // the second FMA takes off k * lo, so r equals the reduced angle to about
-    // 2^-51 absolute for any k below 2^31
+    // a = pos * theta^(-i/64)
     const double a = (double)pos * p.inv_freq[threadIdx.x];
-    const double k = rint(a * kInvTwoPi);
-    double r = fma(-k, kTwoPiHi, a);
-    r = fma(-k, kTwoPiLo, r);
     double sv, cv;
-    sincos(r, &sv, &cv);
+    sincos_series(a, sv, cv);
     const float ch = (float)cv, sh = (float)sv;
     cs[threadIdx.x] = ch;
     cs_lo[threadIdx.x] = (float)(cv - (double)ch);
