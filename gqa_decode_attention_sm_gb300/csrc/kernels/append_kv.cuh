@@ -84,8 +84,9 @@ constexpr double kTwoOverPi = 0x1.45f306dc9c883p-1;
 // sin a and cos a in FP64 for an angle below 2^31 radians, from the
 // mathematics rather than the library routine (whose general path is slow
 // where FP64 is): a = q pi/2 + x with q the integer nearest 2a/pi, q pi/2
-// taken off by two FMAs (the first with the product exact and one rounding
-// of a result below 1, the second taking off q times the rest of pi/2), so
+// taken off by two FMAs, after Cody and Waite's reduction with pi/2 split in
+// two constants (the first FMA with the product exact and one rounding of a
+// result below 1, the second taking off q times the rest of pi/2), so
 // |x| <= pi/4 within about 2^-52; then the Taylor series of sin x and cos x
 // about 0 to the x^17 and x^16 terms by Horner's rule in x^2 (Estrin's
 // scheme, fewer dependent steps, measured no faster), with the
