@@ -1115,6 +1115,28 @@ def test_append_matches_oracle_and_touches_only_its_slot(dtype):
     assert torch.equal(kv.view(torch.int16), before.view(torch.int16))
 
 
+@pytest.mark.parametrize("theta", [1e4, 1e6])
+def test_append_rotary_angles_up_to_2_31(theta):
+    # The kernel takes the rotary sine and cosine by its own reduction modulo
+    # pi/2 and Taylor series: positions up to 2^31 - 1 (angles up to 2^31
+    # radians for the first frequency), each still within one ulp of the
+    # oracle's RNE value for every q_out and K element.
+    positions = [0, 1, 2 ** 20, 2 ** 24 + 1, 2 ** 30, 2 ** 31 - 1]
+    B, C = len(positions), 64
+    qp, kp, vp, wq, wk, _, slots = _append_inputs(B, C, "bf16", seed=21)
+    pos = torch.tensor(positions, dtype=torch.int32, device=DEV)
+    kv = _make(inputs.custom(B, C, C, kv_dtype="bf16"))["kv"]
+    q_out = gq.append_kv(qp, kp, vp, wq, wk, pos, slots, kv, eps=1e-6, rope_theta=theta)
+    torch.cuda.synchronize()
+    qo, ko, _ = oracle.append_kv(_vals(qp), _vals(kp), _vals(vp), _vals(wq), _vals(wk), pos.cpu().numpy(), 1e-6,
+                                 theta)
+    d_q = ulps_apart(bits_of(q_out), oracle.round_to(qo, FMT["bf16"]))
+    sl = slots.cpu().tolist()
+    k_new = torch.stack([kv[b, 0, :, sl[b]] for b in range(B)])
+    d_k = ulps_apart(bits_of(k_new), oracle.round_to(ko, FMT["bf16"]))
+    assert d_q.max() <= 1 and d_k.max() <= 1, f"theta {theta}: q {int(d_q.max())}, k {int(d_k.max())} ulps"
+
+
 def _nearest_codes(ref, table_vals):
     """Indices of the two representable values bracketing ref (sorted table)."""
     i = np.searchsorted(table_vals, ref)
