@@ -17,12 +17,14 @@
 //
 // One CTA per batch row, 8 warps; each warp takes six whole head vectors (all
 // their loads issued together) and lane l holds dims l, l+32, l+64, l+96, so
-// every RoPE pair (i, i+64) stays in one lane.  The 64 angles are formed in FP64 (pos * theta^(-i/64) reaches 1e5
-// radians at long contexts, beyond FP32's reach) once per CTA: the inverse
-// frequencies theta^(-i/64) come from the host (FP64, once per call), and
-// the sine and cosine are evaluated by sincos_series below (FP64 is slow on
-// this GPU: forming the frequencies with pow and the library's sincos of
-// angles up to 1e6 rad took about two thirds of the kernel's time).
+// every RoPE pair (i, i+64) stays in one lane.  The 64 angles are formed
+// and reduced in FP64 (pos * theta^(-i/64) reaches 1e5 radians at long
+// contexts, beyond FP32's reach) once per CTA: the inverse frequencies
+// theta^(-i/64) come from the host (FP64, once per call), and the sine and
+// cosine are evaluated by sincos_series below in double-float arithmetic
+// (FP64 is slow on sm_103a: forming the frequencies with pow and the
+// library's sincos of angles up to 1e6 rad took about two thirds of the
+// kernel's time).
 //
 // Precision: the result before its one rounding is within about 2^-21 of the
 // exact value relative to itself, so the stored fp16/bf16 value is the
@@ -81,42 +83,80 @@ constexpr double kHalfPiHi = 0x1.921fb54442d18p+0;
 constexpr double kHalfPiLo = 0x1.1a62633145c07p-54;
 constexpr double kTwoOverPi = 0x1.45f306dc9c883p-1;
 
-// sin a and cos a in FP64 for an angle below 2^31 radians, from the
-// mathematics rather than the library routine (whose general path is slow
-// where FP64 is): a = q pi/2 + x with q the integer nearest 2a/pi, q pi/2
-// taken off by two FMAs, after Cody and Waite's reduction with pi/2 split in
-// two constants (the first FMA with the product exact and one rounding of a
+// Double-float arithmetic: a value as an unevaluated sum hi + lo of two
+// floats with |lo| <= ulp(hi) / 2 (Dekker; Knuth's two-sum), about 48 bits.
+// The sums and products below are the error-free transformations, so they
+// use the _rn intrinsics, which the compiler never fuses into FMAs.
+struct Float2 {
+  float hi, lo;
+};
+__device__ __forceinline__ Float2 fast_two_sum(float a, float b) {  // |a| >= |b|
+  const float s = __fadd_rn(a, b);
+  return {s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+__device__ __forceinline__ Float2 df_mul(Float2 a, Float2 b) {
+  const float p = __fmul_rn(a.hi, b.hi);
+  float e = fmaf(a.hi, b.hi, -p);  // the product's rounding error, exactly
+  e = fmaf(a.hi, b.lo, e);
+  e = fmaf(a.lo, b.hi, e);
+  return fast_two_sum(p, e);
+}
+__device__ __forceinline__ Float2 df_add(Float2 a, Float2 c) {
+  const float s = __fadd_rn(a.hi, c.hi);
+  const float bb = __fsub_rn(s, a.hi);
+  float err = __fadd_rn(__fsub_rn(a.hi, __fsub_rn(s, bb)), __fsub_rn(c.hi, bb));  // two-sum error
+  err = __fadd_rn(err, __fadd_rn(a.lo, c.lo));
+  return fast_two_sum(s, err);
+}
+__device__ __forceinline__ constexpr Float2 df_const(double d) { return {(float)d, (float)(d - (double)(float)d)}; }
+
+// sin a and cos a for an angle below 2^31 radians as double-float pairs,
+// from the mathematics rather than the library routine.  FP64 issues at a
+// small fraction of the FP32 rate on sm_103a, and the same series in FP64
+// cost about 1 us of this kernel, so only the reduction stays in FP64:
+// a = q pi/2 + x with q the integer nearest 2a/pi, q pi/2 taken off in FP64
+// by two FMAs, after Cody and Waite's reduction with pi/2 split in two
+// constants (the first FMA with the product exact and one rounding of a
 // result below 1, the second taking off q times the rest of pi/2), so
 // |x| <= pi/4 within about 2^-52; then the Taylor series of sin x and cos x
-// about 0 to the x^17 and x^16 terms by Horner's rule in x^2 (Estrin's
-// scheme, fewer dependent steps, measured no faster), with the
-// coefficients (-1)^k/(2k+1)! and (-1)^k/(2k)! rounded to doubles (the first
-// terms left out are below 2^-60 for |x| <= pi/4); q mod 4 picks the
-// quadrant: the swap of sin and cos and their signs.  Within a few units of
-// 2^-53 of the exact values at the given a.
-__device__ __forceinline__ void sincos_series(double a, double& s, double& c) {
-  constexpr double kSin[9] = {0x1p+0, -0x1.5555555555555p-3, 0x1.1111111111111p-7, -0x1.a01a01a01a01ap-13,
-                              0x1.71de3a556c734p-19, -0x1.ae64567f544e4p-26, 0x1.6124613a86d09p-33,
-                              -0x1.ae7f3e733b81fp-41, 0x1.952c77030ad4ap-49};
-  constexpr double kCos[9] = {0x1p+0, -0x1p-1, 0x1.5555555555555p-5, -0x1.6c16c16c16c17p-10,
-                              0x1.a01a01a01a01ap-16, -0x1.27e4fb7789f5cp-22, 0x1.1eed8eff8d898p-29,
-                              -0x1.93974a8c07c9dp-37, 0x1.ae7f3e733b81fp-45};
+// about 0 to the x^17 and x^16 terms by Horner's rule in x^2, in
+// double-float arithmetic, with the coefficients (-1)^k/(2k+1)! and
+// (-1)^k/(2k)! rounded to doubles and split into pairs (the first terms left
+// out are below 2^-60 for |x| <= pi/4); q mod 4 picks the quadrant: the swap
+// of sin and cos and their signs.  Within about 2^-47 of the exact values at
+// the given a (checked against libm on the CPU by an emulation of the same
+// float operations over |x| <= pi/4).
+__device__ __forceinline__ void sincos_series(double a, Float2& s, Float2& c) {
+  constexpr Float2 kSin[9] = {df_const(0x1p+0), df_const(-0x1.5555555555555p-3), df_const(0x1.1111111111111p-7),
+                              df_const(-0x1.a01a01a01a01ap-13), df_const(0x1.71de3a556c734p-19),
+                              df_const(-0x1.ae64567f544e4p-26), df_const(0x1.6124613a86d09p-33),
+                              df_const(-0x1.ae7f3e733b81fp-41), df_const(0x1.952c77030ad4ap-49)};
+  constexpr Float2 kCos[9] = {df_const(0x1p+0), df_const(-0x1p-1), df_const(0x1.5555555555555p-5),
+                              df_const(-0x1.6c16c16c16c17p-10), df_const(0x1.a01a01a01a01ap-16),
+                              df_const(-0x1.27e4fb7789f5cp-22), df_const(0x1.1eed8eff8d898p-29),
+                              df_const(-0x1.93974a8c07c9dp-37), df_const(0x1.ae7f3e733b81fp-45)};
   const double q = rint(a * kTwoOverPi);
-  double x = fma(-q, kHalfPiHi, a);
-  x = fma(-q, kHalfPiLo, x);
-  const double x2 = x * x;
-  double ps = kSin[8], pc = kCos[8];
+  double xd = fma(-q, kHalfPiHi, a);
+  xd = fma(-q, kHalfPiLo, xd);
+  const float xh = (float)xd;
+  const Float2 x = {xh, (float)(xd - (double)xh)};
+  const float p = __fmul_rn(xh, xh);
+  float e = fmaf(xh, xh, -p);
+  e = fmaf(__fadd_rn(xh, xh), x.lo, e);  // + 2 xh xl (xl^2 is below 2^-48 x^2)
+  const Float2 x2 = fast_two_sum(p, e);
+  Float2 ps = kSin[8], pc = kCos[8];
 #pragma unroll
   for (int k = 7; k >= 0; --k) {
-    ps = fma(ps, x2, kSin[k]);
-    pc = fma(pc, x2, kCos[k]);
+    ps = df_add(df_mul(ps, x2), kSin[k]);
+    pc = df_add(df_mul(pc, x2), kCos[k]);
   }
-  const double sx = x * ps, cx = pc;
+  const Float2 sx = df_mul(ps, x), cx = pc;
+  const Float2 nsx = {-sx.hi, -sx.lo}, ncx = {-cx.hi, -cx.lo};
   switch ((int)((long long)q & 3)) {
     case 0: s = sx; c = cx; break;
-    case 1: s = cx; c = -sx; break;
-    case 2: s = -sx; c = -cx; break;
-    default: s = -cx; c = sx; break;
+    case 1: s = cx; c = nsx; break;
+    case 2: s = nsx; c = ncx; break;
+    default: s = ncx; c = sx; break;
   }
 }
 
@@ -173,13 +213,12 @@ __global__ void __launch_bounds__(kAppendThreads) append_kv_kernel(const __grid_
   if (threadIdx.x < kD / 2) {
     // a = pos * theta^(-i/64)
     const double a = (double)pos * p.inv_freq[threadIdx.x];
-    double sv, cv;
+    Float2 sv, cv;
     sincos_series(a, sv, cv);
-    const float ch = (float)cv, sh = (float)sv;
-    cs[threadIdx.x] = ch;
-    cs_lo[threadIdx.x] = (float)(cv - (double)ch);
-    sn[threadIdx.x] = sh;
-    sn_lo[threadIdx.x] = (float)(sv - (double)sh);
+    cs[threadIdx.x] = cv.hi;
+    cs_lo[threadIdx.x] = cv.lo;
+    sn[threadIdx.x] = sv.hi;
+    sn_lo[threadIdx.x] = sv.lo;
   }
   __syncthreads();
   const int C = p.capacity;
