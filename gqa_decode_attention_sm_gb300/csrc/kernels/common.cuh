@@ -150,6 +150,12 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
 
 // 1-D bulk copy global -> shared through the TMA unit; completion is counted
 // in bytes on `bar`.  dst, src 16-byte aligned; bytes a multiple of 16.
+// Bulk prefetch of global memory into L2: a hint with no completion to
+// track.  `src` 16-byte aligned, `bytes` a multiple of 16, the range inside
+// the allocation.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
                                           uint64_t* bar, uint64_t policy) {
   asm volatile(
