@@ -137,7 +137,9 @@ constexpr int kScaleStageBytes = 2 * 128 * 2;  // int8 cache: K and V row scales
 constexpr int kBalMaxBatch = 1024;
 constexpr int kBalMergeBytes = kMmaConsumerWarps * kGroup * (kD + 2) * 4;
 static_assert((kMmaThreads + 3 + kBalMaxBatch) * 4 <= kBalMergeBytes, "the length scan uses the merge area");
-constexpr int kBalRunBytes = 16;  // the run length Q, after the merge area
+// the balanced cursor's slot of 12 ints per warp (its state, or only the
+// run length Q), after the merge area
+constexpr int kBalRunBytes = (kMmaConsumerWarps + 1) * 12 * 4;
 // 3- and 4-token windows over 8-bit caches keep their Q^T fragments in
 // shared memory, one copy per CTA ([k-step][lane][n-tile][2 words]; in the
 // balanced schedule's merge area, idle while a piece streams, else after the
@@ -145,6 +147,15 @@ constexpr int kBalRunBytes = 16;  // the run length Q, after the merge area
 // tile together without spills.
 __host__ __device__ constexpr bool mma_q_in_smem(int kvf, int nq) { return is_8bit(kvf) && nq > 2; }
 constexpr int kQSmemBytes = 8 * 32 * 2 * 2 * 4;
+// The balanced cursor's state in shared memory rather than in registers held
+// through the streaming loop.  With 3-4-token windows at the 168-register
+// cap it cuts the spills (int8 44-68 -> 8-12 bytes, e4m3 0-44 -> 0-28, fp16
+// 4 -> 0; bf16 0-4 -> 8-12).  Cold on GB300, us per call, registers ->
+// shared memory: e4m3 64 x U[16k, 32k] with 3 / 4 tokens 503.8 / 505.9 ->
+// 501.7 / 487.4, int8 of that shape 602.1 / 616.5 -> 614.4 / 602.1, bf16
+// 256 x U[1, 4096] 346.1 / 358.4 -> 340.0 / 346.1; single-token batches
+// within noise.  So every kernel takes it but the int8 3-token window.
+__host__ __device__ constexpr bool mma_cursor_in_smem(int kvf, int nq) { return !(kvf == kKvI8 && nq == 3); }
 __host__ __device__ constexpr int mma_smem_bytes(int kvf, int nq, bool bal = false) {
   return mma_stages(kvf, nq) * (kStageBytes + kScaleStageBytes + 2 * 8) + (bal ? kBalMergeBytes + kBalRunBytes : 0) +
          (!bal && mma_q_in_smem(kvf, nq) ? kQSmemBytes : 0);
@@ -315,12 +326,12 @@ struct Piece {
   bool direct;
 };
 
-template <int kTile, bool BAL>
+template <int kTile, bool BAL, bool kStateInSmem>
 struct PieceCursor;
 
 // One piece per CTA (grid = KV heads x batch x splits).
-template <int kTile>
-struct PieceCursor<kTile, false> {
+template <int kTile, bool kStateInSmem>
+struct PieceCursor<kTile, false, kStateInSmem> {
   Piece one;
   bool pending = false;
   __device__ void start_single(int b, int g, int L, int t_begin, int t_end, int slot, bool direct) {
@@ -344,24 +355,34 @@ struct PieceCursor<kTile, false> {
 // c - floor(tf / q), and the row has floor((tf + n - 1) / q) - floor(tf / q) + 1
 // pieces.
 
+// The cursor rests on rows that hold tokens, so the row cost is wb - nb.
+// The lengths, batch and capacity are read from the kernel parameters.  Each
+// warp walks its own copy; every lane of the warp calls start and next with
+// the same values.  The state lives either in the warp's slot of shared
+// memory, read and written only when the warp moves to its next piece, or in
+// registers held through the streaming loop, with only the run length Q in
+// the slot; mma_cursor_in_smem picks one per kernel.
+enum { kCurB, kCurG, kCurJ, kCurNb, kCurWb, kCurL, kCurLNext, kCurPb, kCurX, kCurX1, kCurQ, kCurSlotInts = 12 };
+static_assert(kBalRunBytes == (kMmaConsumerWarps + 1) * kCurSlotInts * 4, "one cursor slot per warp");
+
+// State in registers.
 template <int kTile>
-struct PieceCursor<kTile, true> {
-  // The cursor rests on rows that hold tokens, so the row cost is wb - nb.
-  // The lengths, batch and capacity are read from the kernel parameters.
+struct PieceCursor<kTile, true, false> {
   int b, g, j, nb, wb, L, L_next, pb, x, x1;
-  const int* q_sm;  // the run length Q, in shared memory (one register fewer)
+  const int* q_sm;  // the run length Q, in the slot (one register fewer)
   __device__ void set_row(int len, int rc) {
     L = len;
     nb = (L + kTile - 1) / kTile;
     wb = bal_row_positions(nb, rc);
   }
   // L0, L1: clamped lengths of rows b0 and b0 + 1 (0 past the batch)
-  __device__ void start(int b0, int pb0, int L0, int L1, int x0, int x1_, const int* q_, int rc) {
+  __device__ void start(int b0, int pb0, int L0, int L1, int x0, int x1_, int q, int rc, int* slot) {
+    slot[kCurQ] = q;
+    q_sm = slot + kCurQ;
     b = b0;
     pb = pb0;
     x = x0;
     x1 = x1_;
-    q_sm = q_;
     set_row(L0, rc);
     L_next = L1;
     const int within = x0 - kHkv * pb;
@@ -399,6 +420,81 @@ struct PieceCursor<kTile, true> {
       if (has_tiles) return true;
     }
     return false;
+  }
+};
+
+// State in shared memory (the same walk as above).
+template <int kTile>
+struct PieceCursor<kTile, true, true> {
+  enum { kB = kCurB, kG = kCurG, kJ = kCurJ, kNb = kCurNb, kWb = kCurWb, kL = kCurL, kLNext = kCurLNext,
+         kPb = kCurPb, kX = kCurX, kX1 = kCurX1, kQ = kCurQ };
+  volatile int* st;  // this warp's slot
+  __device__ void start(int b0, int pb0, int L0, int L1, int x0, int x1, int q, int rc, int* slot) {
+    st = slot;
+    const int nb = (L0 + kTile - 1) / kTile, wb = bal_row_positions(nb, rc);
+    const int within = x0 - kHkv * pb0;
+    const int g = within / wb;
+    st[kB] = b0;
+    st[kG] = g;
+    st[kJ] = within - g * wb;  // position in the row; [0, rc) stand for the piece cost
+    st[kNb] = nb;
+    st[kWb] = wb;
+    st[kL] = L0;
+    st[kLNext] = L1;  // clamped length of row b0 + 1 (0 past the batch)
+    st[kPb] = pb0;
+    st[kX] = x0;
+    st[kX1] = x1;
+    st[kQ] = q;
+  }
+  __device__ bool next(Piece& pc, const SplitParams& p) {
+    const int cta = blockIdx.x;
+    int b = st[kB], g = st[kG], j = st[kJ], nb = st[kNb], wb = st[kWb], L = st[kL], L_next = st[kLNext],
+        pb = st[kPb], x = st[kX];
+    const int x1 = st[kX1], q = st[kQ];
+    __syncwarp();  // every lane has read the slot before any lane writes it
+    bool found = false;
+    while (x < x1) {
+      const int rc = wb - nb;
+      const int cnt = min(wb - j, x1 - x);
+      const int r0 = max(j, rc), r1 = j + cnt;  // tile positions [r0, r1) of this run
+      const bool has_tiles = r1 > r0;
+      if (has_tiles) {
+        const int tf = kHkv * pb + g * wb + rc;
+        const int fq = tf / q;
+        pc = Piece{b, g, L, (r0 - rc) * kTile, min(L, (r1 - rc) * kTile), cta - fq, (tf + nb - 1) / q == fq};
+      }
+      x += cnt;
+      j += cnt;
+      if (j == wb) {
+        j = 0;
+        if (++g == kHkv) {
+          g = 0;
+          pb += wb;
+          while (x < x1) {  // the next row that holds tokens; its successor's
+            ++b;              // length is loaded a whole piece ahead of its use
+            L = L_next;
+            nb = (L + kTile - 1) / kTile;
+            wb = bal_row_positions(nb, rc);
+            L_next = b + 1 < p.batch ? min(max(__ldg(p.lens + b + 1), 0), p.capacity) : 0;
+            if (wb > 0) break;
+          }
+        }
+      }
+      if (has_tiles) {
+        found = true;
+        break;
+      }
+    }
+    st[kB] = b;
+    st[kG] = g;
+    st[kJ] = j;
+    st[kNb] = nb;
+    st[kWb] = wb;
+    st[kL] = L;
+    st[kLNext] = L_next;
+    st[kPb] = pb;
+    st[kX] = x;
+    return found;
   }
 };
 
@@ -489,8 +585,8 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
   // cluster merge: this CTA's merged state [kCols][128] + max + denominator,
   // after the merge area in the idle ring
   float* cl_state = mrg_l + kMmaConsumerWarps * kRC;
-  // balanced schedule: the run length Q, read by the cursor at each piece
-  int* q_sm = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(mrg_acc) + kBalMergeBytes);
+  // balanced schedule: the cursor's slot of each warp
+  int* cur_sm = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(mrg_acc) + kBalMergeBytes);
   uint32_t* qfr = reinterpret_cast<uint32_t*>(empty + kMmaStages);  // Q^T fragments (kQS)
 
   // Every CTA of this grid is resident or done: let the next grid in the
@@ -512,7 +608,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
   pdl_wait_prior_grid();
 
   // ---- this CTA's pieces
-  PieceCursor<T::kTile, BAL> cur;
+  PieceCursor<T::kTile, BAL, mma_cursor_in_smem(KVF, NQ)> cur;
   if constexpr (BAL) {
     // Balanced schedule: the positions of every (b, KV head) row, rows in
     // order, form one stream of 8 * sum_b w_b positions (w = tiles + rc for a
@@ -576,7 +672,6 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
     const int total = kHkv * (sum_n + rc * sum_r);
     const int q = max((total + (int)gridDim.x - 1) / (int)gridDim.x, p.bal_q_min);
     const int x0 = (int)blockIdx.x * q;
-    if (threadIdx.x == 0) *q_sm = q;  // visible to the cursor after the barrier below
     int pre = pre_n + rc * pre_r;
     // the thread whose rows hold position x0 records the first row and its prefix
     if (x0 < total && kHkv * pre <= x0 && x0 < kHkv * (pre + mine_n + rc * mine_r)) {
@@ -593,7 +688,8 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
     __syncthreads();
     if (x0 >= total) return;  // more CTAs than work
     const int b0 = scan[kMmaThreads + 1];
-    cur.start(b0, scan[kMmaThreads + 2], lsh[b0], b0 + 1 < B ? lsh[b0 + 1] : 0, x0, min(x0 + q, total), q_sm, rc);
+    cur.start(b0, scan[kMmaThreads + 2], lsh[b0], b0 + 1 < B ? lsh[b0 + 1] : 0, x0, min(x0 + q, total), q, rc,
+              cur_sm + warp * kCurSlotInts);
     if constexpr (kQS) __syncthreads();  // every thread has read the scratch the Q^T fragments overwrite
   } else {
     // one piece per CTA: split s of row (b, g)
