@@ -153,8 +153,9 @@ constexpr int kQSmemBytes = 8 * 32 * 2 * 2 * 4;
 // 4 -> 0; bf16 0-4 -> 8-12).  Cold on GB300, us per call, registers ->
 // shared memory: e4m3 64 x U[16k, 32k] with 3 / 4 tokens 503.8 / 505.9 ->
 // 501.7 / 487.4, int8 of that shape 602.1 / 616.5 -> 614.4 / 602.1, bf16
-// 256 x U[1, 4096] 346.1 / 358.4 -> 340.0 / 346.1; single-token batches
-// within noise.  So every kernel takes it but the int8 3-token window.
+// 256 x U[1, 4096] 346.1 / 358.4 -> 340.0 / 346.1; 1- and 2-token kernels
+// (no spills either way) within 1 %.  So every kernel takes it but the int8
+// 3-token window.
 __host__ __device__ constexpr bool mma_cursor_in_smem(int kvf, int nq) { return !(kvf == kKvI8 && nq == 3); }
 __host__ __device__ constexpr int mma_smem_bytes(int kvf, int nq, bool bal = false) {
   return mma_stages(kvf, nq) * (kStageBytes + kScaleStageBytes + 2 * 8) + (bal ? kBalMergeBytes + kBalRunBytes : 0) +
