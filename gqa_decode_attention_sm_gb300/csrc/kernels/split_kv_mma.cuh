@@ -137,9 +137,9 @@ constexpr int kScaleStageBytes = 2 * 128 * 2;  // int8 cache: K and V row scales
 constexpr int kBalMaxBatch = 1024;
 constexpr int kBalMergeBytes = kMmaConsumerWarps * kGroup * (kD + 2) * 4;
 static_assert((kMmaThreads + 3 + kBalMaxBatch) * 4 <= kBalMergeBytes, "the length scan uses the merge area");
-// the balanced cursor's slot of 12 ints per warp (its state, or only the
-// run length Q), after the merge area
-constexpr int kBalRunBytes = (kMmaConsumerWarps + 1) * 12 * 4;
+// the balanced cursor's slot of 16 ints per warp (its state and the current
+// piece's output coordinates), after the merge area
+constexpr int kBalRunBytes = (kMmaConsumerWarps + 1) * 16 * 4;
 // 3- and 4-token windows over 8-bit caches keep their Q^T fragments in
 // shared memory, one copy per CTA ([k-step][lane][n-tile][2 words]; in the
 // balanced schedule's merge area, idle while a piece streams, else after the
@@ -147,16 +147,6 @@ constexpr int kBalRunBytes = (kMmaConsumerWarps + 1) * 12 * 4;
 // tile together without spills.
 __host__ __device__ constexpr bool mma_q_in_smem(int kvf, int nq) { return is_8bit(kvf) && nq > 2; }
 constexpr int kQSmemBytes = 8 * 32 * 2 * 2 * 4;
-// The balanced cursor's state in shared memory rather than in registers held
-// through the streaming loop.  With 3-4-token windows at the 168-register
-// cap it cuts the spills (int8 44-68 -> 8-12 bytes, e4m3 0-44 -> 0-28, fp16
-// 4 -> 0; bf16 0-4 -> 8-12).  Cold on GB300, us per call, registers ->
-// shared memory: e4m3 64 x U[16k, 32k] with 3 / 4 tokens 503.8 / 505.9 ->
-// 501.7 / 487.4, int8 of that shape 602.1 / 616.5 -> 614.4 / 602.1, bf16
-// 256 x U[1, 4096] 346.1 / 358.4 -> 340.0 / 346.1; 1- and 2-token kernels
-// (no spills either way) within 1 %.  So every kernel takes it but the int8
-// 3-token window.
-__host__ __device__ constexpr bool mma_cursor_in_smem(int kvf, int nq) { return !(kvf == kKvI8 && nq == 3); }
 __host__ __device__ constexpr int mma_smem_bytes(int kvf, int nq, bool bal = false) {
   return mma_stages(kvf, nq) * (kStageBytes + kScaleStageBytes + 2 * 8) + (bal ? kBalMergeBytes + kBalRunBytes : 0) +
          (!bal && mma_q_in_smem(kvf, nq) ? kQSmemBytes : 0);
@@ -327,12 +317,12 @@ struct Piece {
   bool direct;
 };
 
-template <int kTile, bool BAL, bool kStateInSmem>
+template <int kTile, bool BAL>
 struct PieceCursor;
 
 // One piece per CTA (grid = KV heads x batch x splits).
-template <int kTile, bool kStateInSmem>
-struct PieceCursor<kTile, false, kStateInSmem> {
+template <int kTile>
+struct PieceCursor<kTile, false> {
   Piece one;
   bool pending = false;
   __device__ void start_single(int b, int g, int L, int t_begin, int t_end, int slot, bool direct) {
@@ -345,6 +335,7 @@ struct PieceCursor<kTile, false, kStateInSmem> {
     pending = false;
     return true;
   }
+  __device__ void reload(Piece&) const {}
 };
 
 // Balanced schedule: the CTA's positions [x, x1) of the global stream.  Rows
@@ -358,75 +349,30 @@ struct PieceCursor<kTile, false, kStateInSmem> {
 
 // The cursor rests on rows that hold tokens, so the row cost is wb - nb.
 // The lengths, batch and capacity are read from the kernel parameters.  Each
-// warp walks its own copy; every lane of the warp calls start and next with
-// the same values.  The state lives either in the warp's slot of shared
-// memory, read and written only when the warp moves to its next piece, or in
-// registers held through the streaming loop, with only the run length Q in
-// the slot; mma_cursor_in_smem picks one per kernel.
-enum { kCurB, kCurG, kCurJ, kCurNb, kCurWb, kCurL, kCurLNext, kCurPb, kCurX, kCurX1, kCurQ, kCurSlotInts = 12 };
+// warp walks its own copy, kept in the warp's slot of shared memory and read
+// and written only when the warp moves to its next piece, not in registers
+// held through the streaming loop; every lane of the warp calls start and
+// next with the same values and writes the same words.  The slot also holds
+// the current piece's output coordinates, so a consumer warp drops them
+// from its registers while it streams the piece and reads them back for the
+// epilogue (reload).
+//
+// At the 168-register cap of the 3-4-token window kernels this took their
+// spills from 4-68 bytes to 0-8.  Cold on GB300, us per call, before ->
+// after: e4m3 64 x U[16k, 32k] with 3 / 4 tokens 503.8 / 505.9 -> 483.3 /
+// 491.5, int8 of that shape 602.1 / 616.5 -> 577.5 / 598.0, bf16 256 x
+// U[1, 4096] 346.1 / 358.4 -> 333.8 / 344.1; 1- and 2-token kernels (no
+// spills either way) within 1 %.  With the state alone in shared memory and
+// the coordinates in registers, the int8 3-token window was slower (614.4).
+enum {
+  kCurB, kCurG, kCurJ, kCurNb, kCurWb, kCurL, kCurLNext, kCurPb, kCurX, kCurX1, kCurQ,
+  kCurPcB, kCurPcG, kCurPcSlot, kCurPcDirect,  // the current piece's fields the epilogue needs
+  kCurSlotInts = 16
+};
 static_assert(kBalRunBytes == (kMmaConsumerWarps + 1) * kCurSlotInts * 4, "one cursor slot per warp");
 
-// State in registers.
 template <int kTile>
-struct PieceCursor<kTile, true, false> {
-  int b, g, j, nb, wb, L, L_next, pb, x, x1;
-  const int* q_sm;  // the run length Q, in the slot (one register fewer)
-  __device__ void set_row(int len, int rc) {
-    L = len;
-    nb = (L + kTile - 1) / kTile;
-    wb = bal_row_positions(nb, rc);
-  }
-  // L0, L1: clamped lengths of rows b0 and b0 + 1 (0 past the batch)
-  __device__ void start(int b0, int pb0, int L0, int L1, int x0, int x1_, int q, int rc, int* slot) {
-    slot[kCurQ] = q;
-    q_sm = slot + kCurQ;
-    b = b0;
-    pb = pb0;
-    x = x0;
-    x1 = x1_;
-    set_row(L0, rc);
-    L_next = L1;
-    const int within = x0 - kHkv * pb;
-    g = within / wb;
-    j = within - g * wb;  // position in the row; [0, rc) stand for the piece cost
-  }
-  __device__ bool next(Piece& pc, const SplitParams& p) {
-    const int cta = blockIdx.x;
-    while (x < x1) {
-      const int rc = wb - nb;
-      const int cnt = min(wb - j, x1 - x);
-      const int r0 = max(j, rc), r1 = j + cnt;  // tile positions [r0, r1) of this run
-      const bool has_tiles = r1 > r0;
-      if (has_tiles) {
-        const int tf = kHkv * pb + g * wb + rc;
-        const int q = *q_sm;
-        const int fq = tf / q;
-        pc = Piece{b, g, L, (r0 - rc) * kTile, min(L, (r1 - rc) * kTile), cta - fq, (tf + nb - 1) / q == fq};
-      }
-      x += cnt;
-      j += cnt;
-      if (j == wb) {
-        j = 0;
-        if (++g == kHkv) {
-          g = 0;
-          pb += wb;
-          while (x < x1) {  // the next row that holds tokens; its successor's
-            ++b;              // length is loaded a whole piece ahead of its use
-            set_row(L_next, rc);
-            L_next = b + 1 < p.batch ? min(max(__ldg(p.lens + b + 1), 0), p.capacity) : 0;
-            if (wb > 0) break;
-          }
-        }
-      }
-      if (has_tiles) return true;
-    }
-    return false;
-  }
-};
-
-// State in shared memory (the same walk as above).
-template <int kTile>
-struct PieceCursor<kTile, true, true> {
+struct PieceCursor<kTile, true> {
   enum { kB = kCurB, kG = kCurG, kJ = kCurJ, kNb = kCurNb, kWb = kCurWb, kL = kCurL, kLNext = kCurLNext,
          kPb = kCurPb, kX = kCurX, kX1 = kCurX1, kQ = kCurQ };
   volatile int* st;  // this warp's slot
@@ -463,6 +409,10 @@ struct PieceCursor<kTile, true, true> {
         const int tf = kHkv * pb + g * wb + rc;
         const int fq = tf / q;
         pc = Piece{b, g, L, (r0 - rc) * kTile, min(L, (r1 - rc) * kTile), cta - fq, (tf + nb - 1) / q == fq};
+        st[kCurPcB] = pc.b;
+        st[kCurPcG] = pc.g;
+        st[kCurPcSlot] = pc.slot;
+        st[kCurPcDirect] = pc.direct;
       }
       x += cnt;
       j += cnt;
@@ -496,6 +446,12 @@ struct PieceCursor<kTile, true, true> {
     st[kPb] = pb;
     st[kX] = x;
     return found;
+  }
+  __device__ void reload(Piece& pc) const {
+    pc.b = st[kCurPcB];
+    pc.g = st[kCurPcG];
+    pc.slot = st[kCurPcSlot];
+    pc.direct = st[kCurPcDirect] != 0;
   }
 };
 
@@ -609,7 +565,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
   pdl_wait_prior_grid();
 
   // ---- this CTA's pieces
-  PieceCursor<T::kTile, BAL, mma_cursor_in_smem(KVF, NQ)> cur;
+  PieceCursor<T::kTile, BAL> cur;
   if constexpr (BAL) {
     // Balanced schedule: the positions of every (b, KV head) row, rows in
     // order, form one stream of 8 * sum_b w_b positions (w = tiles + rc for a
@@ -1293,6 +1249,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
       if (lane == 0) mbar_arrive(&empty[st]);
     }
     if constexpr (KVF == kKvI8) take_v_bias(o, vw);
+    cur.reload(pc);  // the piece's output coordinates (from shared memory, with the cursor there)
 
     // ---- per-warp denominators: sum over the 8 lanes holding each column
   #pragma unroll
@@ -1360,7 +1317,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
           acc.z = fmaf(v.z, a, acc.z);
           acc.w = fmaf(v.w, a, acc.w);
         }
-        const int row = (b * NQ + col / kGroup) * kHq + g * kGroup + (ctid >> 5);  // (b, query token, head)
+        const int row = (pc.b * NQ + col / kGroup) * kHq + pc.g * kGroup + (ctid >> 5);  // (b, query token, head)
         if constexpr (CL) {
           *reinterpret_cast<float4*>(cl_state + col * kD + d0) = acc;
           if (d0 == 0) {
