@@ -1249,7 +1249,7 @@ __global__ void __launch_bounds__(kMmaThreads, mma_ctas_per_sm(KVF, NQ))
       if (lane == 0) mbar_arrive(&empty[st]);
     }
     if constexpr (KVF == kKvI8) take_v_bias(o, vw);
-    cur.reload(pc);  // the piece's output coordinates (from shared memory, with the cursor there)
+    cur.reload(pc);  // the piece's output coordinates (the balanced cursor keeps them in shared memory)
 
     // ---- per-warp denominators: sum over the 8 lanes holding each column
   #pragma unroll
