@@ -116,6 +116,19 @@ def test_every_path(kv_dtype, T, grid):
     assert ok, f"{kv_dtype} T={T} {grid}: max err {err:.3e}"
 
 
+@pytest.mark.parametrize("kv_dtype", ["f16", "e4m3", "i8"])
+@pytest.mark.parametrize("T", [1, 3])
+def test_capacity_off_the_tile_grid(kv_dtype, T):
+    # one-piece grids (clusters, and with 9 splits the combine kernel) whose
+    # last chunk, and the L2 prefetch of its first tile, end inside a tile
+    for C, S in ((1000, 6), (1032, 5), (1032, 16)):
+        lens = [C, C - 1, C // 2 + 3, T]
+        t, out, ws = _window(kv_dtype, 4, C, T, lens, S)
+        _check(gq.get_status(ws), f"{kv_dtype} T={T} C={C} S={S}")
+        ok, err, _ = tolerance_ok(_rows(out), _oracle(t))
+        assert ok, f"{kv_dtype} T={T} C={C} S={S}: max err {err:.3e}"
+
+
 def test_out_of_contract_lengths_and_pages_are_clamped_not_out_of_range():
     B, C, T = 4, 512, 2
     t, _, ws = _window("bf16", B, C, T, [0, C + 9, 1, 300], 4)

@@ -727,6 +727,23 @@ def test_out_of_range_lengths_are_clamped_and_flagged(S):
     assert gq.get_status(p) == 0
 
 
+@pytest.mark.parametrize("kv_dtype", ["f16", "bf16", "e4m3", "i8"])
+@pytest.mark.parametrize("C,S", [(1000, 6), (1032, 5), (1032, 16), (200, 3)])
+def test_capacity_off_the_tile_grid(kv_dtype, C, S):
+    # The last chunk of each row ends inside a tile (64 slots for 16-bit
+    # caches, 128 for 8-bit ones), and so does the L2 prefetch of its first
+    # tile (8, 40 or 72 slots here).  (1032, 16) plans 9 splits, past the
+    # cluster merge, so the combine kernel runs; the others merge in
+    # clusters.  Rows end at the capacity, one slot short of it, mid-row and
+    # at slot 1, so some chunks start past their row's length.
+    lens = [C, C - 1, C // 2 + 3, 1]
+    w = inputs.custom(4, C, 1, kv_dtype=kv_dtype, kv_std=2.0 if kv_dtype == "e4m3" else 1.0, nan_tail=True)
+    t = _make(w, lens=lens)
+    p = _run(t, num_splits=S)
+    assert gq.get_status(p) == 0
+    _assert_parity(_gpu_rows(p.out), _oracle_full(t), f"{kv_dtype} C={C} S={S}")
+
+
 def test_in_contract_lengths_raise_no_flags():
     t = _make(inputs.WORKLOADS[3])
     p = _run(t)
