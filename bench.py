@@ -890,14 +890,16 @@ def run_gpu(args):
         all_cpus = os.sched_getaffinity(0)
         cpus, h2d_probe = near_host_cpus(dev)
 
+        # the step's inputs: q, the cache (with its int8 row scales) and the lengths
+        in_keys = ("q", "kv", "lens") + (("kv_scales",) if t["kv_scales"] is not None else ())
+
         def pin_inputs(grp):
-            """Pinned host copies of the step's inputs, first touched (and so
-            placed) from the CPUs grp; returns them and the GB/s of one
-            full-size host-to-device copy of the cache."""
+            """Pinned host copies of the step's inputs (in_keys, then out),
+            first touched (and so placed) from the CPUs grp; returns them and
+            the GB/s of one full-size host-to-device copy of the cache."""
             os.sched_setaffinity(0, grp)
             try:
-                bufs = [torch.empty(t[k].shape, dtype=t[k].dtype, pin_memory=True).copy_(t[k])
-                        for k in ("q", "kv", "lens")]
+                bufs = [torch.empty(t[k].shape, dtype=t[k].dtype, pin_memory=True).copy_(t[k]) for k in in_keys]
                 bufs.append(torch.empty(out.shape, dtype=out.dtype, pin_memory=True).zero_())
             finally:
                 os.sched_setaffinity(0, all_cpus)  # the oracle below uses every core
@@ -910,28 +912,28 @@ def run_gpu(args):
 
         # The 1 GiB probe can miss how a multi-GB buffer is placed: check the
         # real buffers and, well short of the probe, try the other CPU group.
-        (hq, hkv, hlens, hout), full_rate = pin_inputs(cpus)
+        hbufs, full_rate = pin_inputs(cpus)
         full_rates = {f"{min(cpus)}-{max(cpus)}": full_rate}
         others = [set(c) for c in ([sorted(all_cpus)[:len(all_cpus) // 2], sorted(all_cpus)[len(all_cpus) // 2:]]
                                    if len(all_cpus) > 1 else []) if set(c) != set(cpus)]
         if h2d_probe and others and full_rate < 0.85 * max(h2d_probe.values()):
             first = cpus
-            del hq, hkv, hlens, hout
-            (hq, hkv, hlens, hout), alt_rate = pin_inputs(others[0])
+            del hbufs
+            hbufs, alt_rate = pin_inputs(others[0])
             full_rates[f"{min(others[0])}-{max(others[0])}"] = alt_rate
             cpus = others[0]
             if alt_rate < full_rate:
-                del hq, hkv, hlens, hout
-                (hq, hkv, hlens, hout), _ = pin_inputs(first)
+                del hbufs
+                hbufs, _ = pin_inputs(first)
                 cpus = first
-        t["kv"].copy_(hkv, non_blocking=True)  # the device cache holds what the host copy holds
+        hin, hout = dict(zip(in_keys, hbufs[:-1])), hbufs[-1]
+        t["kv"].copy_(hin["kv"], non_blocking=True)  # the device cache holds what the host copy holds
         torch.cuda.synchronize(dev)
         ke = max(2, min(K, args.e2e_steps))
 
         def e2e_step():
-            t["q"].copy_(hq, non_blocking=True)
-            t["kv"].copy_(hkv, non_blocking=True)
-            t["lens"].copy_(hlens, non_blocking=True)
+            for k in in_keys:
+                t[k].copy_(hin[k], non_blocking=True)
             step()
             hout.copy_(out, non_blocking=True)
 
@@ -945,15 +947,15 @@ def run_gpu(args):
         b.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms = max_over_ranks(a.elapsed_time(b) / ke, world, dev)
-        h2d = hq.numel() * hq.element_size() + hkv.numel() * hkv.element_size() + hlens.numel() * 4
+        h2d = sum(b.numel() * b.element_size() for b in hin.values())
         e2e = {"value": round(all_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                "ms_per_step": round(e2e_ms, 3), "steps": ke, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": hout.numel() * hout.element_size(),
-               "path": "pinned host q/kv/lens -> H2D -> " +
+               "path": "pinned host " + "/".join(in_keys) + " -> H2D -> " +
                        ("gqa_decode_prepared/fp8kv/int8kv" if T == 1 else "gqa_decode_verify") + " -> D2H out",
                "host_cpus": f"{min(cpus)}-{max(cpus)}", "h2d_probe_GBps": h2d_probe,
                "h2d_full_size_GBps": full_rates}
-        del hq, hkv, hlens, hout
+        del hbufs, hin, hout
 
     achieved = nbytes / (split_ms * 1e-3) / 1e9
     # the committed capture is of the workload as defined (no batch or KV override)
